@@ -1,0 +1,304 @@
+/*
+ * moe_oracle.c -- the CPU oracle of the routed-MoE layer (test infrastructure).
+ *
+ * Straight loops, no blocking or fusion: a full scan per top-k slot, a
+ * counting sort for the permutation, scalar int32 block dots and fp64 sums
+ * in block order.  Floating point that decides an integer (the routing score,
+ * the int8 codes of x and of h) is computed in fp32, the precision the CUDA
+ * library uses for those decisions; every other quantity is fp64.
+ * Build: cc -std=c99 -O2 -ffp-contract=off -fPIC -shared (no fused
+ * multiply-adds other than the explicit fmaf calls in ora_spec_exp).
+ * Definitions and page citations: oracle.h.
+ */
+#include "oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------ spec-exp
+ * e(x) for the router's sigmoid, defined so that any IEEE-754 fp32 machine
+ * gets the same bits: clamp x to [-86, 88]; n = rint(x * log2(e)); Cody-Waite
+ * reduction r = (x - n*C1) - n*C2 with C1 = 355/512 (exact products) and
+ * C2 = fp32(ln2 - C1) (the split of Cody & Waite as used in Cephes);
+ * p = degree-7 Taylor polynomial of e^r, coefficients fp32(1/k!), Horner with
+ * fmaf; result p * 2^n with 2^n built exactly (n stays in [-124, 127]). */
+float ora_spec_exp(float x) {
+  const float log2e = 0x1.715476p+0f;
+  const float c1 = 0x1.63p-1f;       /* 0.693359375 */
+  const float c2 = -0x1.bd0106p-13f; /* ln2 - c1 */
+  const float t7 = 0x1.a01a02p-13f;  /* 1/5040 */
+  const float t6 = 0x1.6c16c2p-10f;  /* 1/720  */
+  const float t5 = 0x1.111112p-7f;   /* 1/120  */
+  const float t4 = 0x1.555556p-5f;   /* 1/24   */
+  const float t3 = 0x1.555556p-3f;   /* 1/6    */
+  const float t2 = 0.5f, t1 = 1.0f, t0 = 1.0f;
+  if (x < -86.0f) x = -86.0f;
+  if (x > 88.0f) x = 88.0f;
+  float n = rintf(x * log2e);
+  float r = fmaf(-n, c1, x);
+  r = fmaf(-n, c2, r);
+  float p = t7;
+  p = fmaf(p, r, t6);
+  p = fmaf(p, r, t5);
+  p = fmaf(p, r, t4);
+  p = fmaf(p, r, t3);
+  p = fmaf(p, r, t2);
+  p = fmaf(p, r, t1);
+  p = fmaf(p, r, t0);
+  int ni = (int)n;
+  uint32_t bits = (uint32_t)(ni + 127) << 23;
+  float two_n;
+  memcpy(&two_n, &bits, sizeof two_n);
+  return p * two_n;
+}
+
+void ora_spec_exp_n(uint32_t n, const float *x, float *out) {
+  for (uint32_t i = 0; i < n; ++i) out[i] = ora_spec_exp(x[i]);
+}
+
+/* fp16 bit pattern -> exact double */
+double ora_f16_to_f64(uint16_t h) {
+  int neg = (h >> 15) & 1;
+  int e = (h >> 10) & 31;
+  int m = h & 1023;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24);
+  } else if (e == 31) {
+    v = m ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(m + 1024), e - 25);
+  }
+  return neg ? -v : v;
+}
+
+/* ------------------------------------------------------------------ A1 score */
+void ora_score(uint32_t E, const float *logit, const float *bias, float *sigma, float *c) {
+  for (uint32_t i = 0; i < E; ++i) {
+    float e = ora_spec_exp(-logit[i]);
+    float sg = 1.0f / (1.0f + e);
+    if (sigma) sigma[i] = sg;
+    c[i] = sg + bias[i];
+  }
+}
+
+/* ------------------------------------------------------------------ A2 top-k
+ * Slot j takes the largest c among experts not yet taken; scanning upward
+ * with a strict '>' keeps the lower index on ties. */
+void ora_topk(uint32_t E, uint32_t k, const float *c, int32_t *idx) {
+  unsigned char *taken = (unsigned char *)calloc(E, 1);
+  for (uint32_t j = 0; j < k; ++j) {
+    int32_t best = -1;
+    for (uint32_t i = 0; i < E; ++i) {
+      if (taken[i]) continue;
+      if (best < 0 || c[i] > c[best]) best = (int32_t)i;
+    }
+    idx[j] = best;
+    taken[best] = 1;
+  }
+  free(taken);
+}
+
+/* router for T tokens; weights w_j = s * sigma_j / sum_j sigma_j in fp64 */
+void ora_route(uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
+               const float *bias, int32_t *idx, float *w) {
+  float *c = (float *)malloc(sizeof(float) * E);
+  for (uint32_t t = 0; t < T; ++t) {
+    const float *l = logits + (size_t)t * E;
+    ora_score(E, l, bias, NULL, c);
+    ora_topk(E, k, c, idx + (size_t)t * k);
+    if (w) {
+      double sum = 0.0;
+      for (uint32_t j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
+      for (uint32_t j = 0; j < k; ++j) {
+        double sg = 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
+        w[t * k + j] = (float)((double)s * sg / sum);
+      }
+    }
+  }
+  free(c);
+}
+
+/* ------------------------------------------------------------------ A3 permute
+ * Counting sort, stable in (token, slot) order. */
+void ora_permute(uint32_t T, uint32_t E, uint32_t k, const int32_t *idx, int32_t *off,
+                 int32_t *perm, int32_t *pos) {
+  uint32_t R = T * k;
+  int32_t *cursor = (int32_t *)calloc(E + 1, sizeof(int32_t));
+  for (uint32_t e = 0; e <= E; ++e) off[e] = 0;
+  for (uint32_t r = 0; r < R; ++r) off[idx[r] + 1] += 1;
+  for (uint32_t e = 0; e < E; ++e) off[e + 1] += off[e];
+  for (uint32_t e = 0; e < E; ++e) cursor[e] = off[e];
+  for (uint32_t r = 0; r < R; ++r) {
+    int32_t p = cursor[idx[r]]++;
+    if (perm) perm[p] = (int32_t)r;
+    if (pos) pos[r] = p;
+  }
+  free(cursor);
+}
+
+/* ------------------------------------------------------------------ A4 quantise */
+void ora_quantize(uint32_t n, const float *x, int8_t *q, float *scale) {
+  for (uint32_t b = 0; b < n / 32; ++b) {
+    const float *xb = x + 32 * b;
+    float a = 0.0f;
+    for (int i = 0; i < 32; ++i) {
+      float v = fabsf(xb[i]);
+      if (v > a) a = v;
+    }
+    float sx = a / 127.0f;
+    scale[b] = sx;
+    for (int i = 0; i < 32; ++i) {
+      if (sx == 0.0f) {
+        q[32 * b + i] = 0;
+        continue;
+      }
+      float v = roundf(xb[i] / sx); /* C99 roundf: halfway cases away from zero */
+      if (v > 127.0f) v = 127.0f;
+      if (v < -127.0f) v = -127.0f;
+      q[32 * b + i] = (int8_t)v;
+    }
+  }
+}
+
+/* ------------------------------------------------------------------ A10 2-bit */
+void ora_decode_q2(uint32_t K, const uint8_t *codes, int8_t *out) {
+  for (uint32_t i = 0; i < K; ++i) {
+    int c = (codes[i / 4] >> (2 * (i % 4))) & 3;
+    out[i] = (int8_t)(2 * c - 3);
+  }
+}
+
+/* ------------------------------------------------------------------ A5/A7 dots */
+void ora_block_dots(int32_t fmt, uint32_t K, const void *wq_row, const int8_t *xq,
+                    int32_t *isum) {
+  int8_t *w = (int8_t *)malloc(K);
+  if (fmt == ORA_FMT_Q2S)
+    ora_decode_q2(K, (const uint8_t *)wq_row, w);
+  else
+    memcpy(w, wq_row, K);
+  for (uint32_t b = 0; b < K / 32; ++b) {
+    int32_t acc = 0;
+    for (int i = 0; i < 32; ++i) acc += (int32_t)w[32 * b + i] * (int32_t)xq[32 * b + i];
+    isum[b] = acc;
+  }
+  free(w);
+}
+
+static size_t row_bytes(int32_t fmt, uint32_t K) { return fmt == ORA_FMT_Q2S ? K / 4 : K; }
+
+void ora_matvec(int32_t fmt, uint32_t rows, uint32_t K, const void *wq, const uint16_t *ws,
+                const int8_t *xq, const float *xs, double *out) {
+  uint32_t nb = K / 32;
+  int32_t *isum = (int32_t *)malloc(sizeof(int32_t) * nb);
+  for (uint32_t n = 0; n < rows; ++n) {
+    const char *row = (const char *)wq + (size_t)n * row_bytes(fmt, K);
+    ora_block_dots(fmt, K, row, xq, isum);
+    double acc = 0.0;
+    for (uint32_t b = 0; b < nb; ++b)
+      acc += (double)isum[b] * (ora_f16_to_f64(ws[(size_t)n * nb + b]) * (double)xs[b]);
+    out[n] = acc;
+  }
+  free(isum);
+}
+
+/* one expert on one quantised activation row: hq/hs (may be NULL) and o[d] */
+int ora_expert_row(int32_t fmt, uint32_t d, uint32_t width, const ora_expert *ex,
+                   const int8_t *xq, const float *xs, int8_t *hq, float *hs, double *o) {
+  if (!ex || !ex->gate_q || !ex->gate_s || !ex->up_q || !ex->up_s || !ex->down_q ||
+      !ex->down_s)
+    return ORA_MISSING_EXPERT;
+  double *g = (double *)malloc(sizeof(double) * width);
+  double *u = (double *)malloc(sizeof(double) * width);
+  float *h = (float *)malloc(sizeof(float) * width);
+  int8_t *hq_l = (int8_t *)malloc(width);
+  float *hs_l = (float *)malloc(sizeof(float) * (width / 32));
+  ora_matvec(fmt, width, d, ex->gate_q, ex->gate_s, xq, xs, g);
+  ora_matvec(fmt, width, d, ex->up_q, ex->up_s, xq, xs, u);
+  for (uint32_t n = 0; n < width; ++n) h[n] = (float)(g[n] / (1.0 + exp(-g[n])) * u[n]);
+  ora_quantize(width, h, hq_l, hs_l);
+  ora_matvec(fmt, d, width, ex->down_q, ex->down_s, hq_l, hs_l, o);
+  if (hq) memcpy(hq, hq_l, width);
+  if (hs) memcpy(hs, hs_l, sizeof(float) * (width / 32));
+  free(g);
+  free(u);
+  free(h);
+  free(hq_l);
+  free(hs_l);
+  return ORA_OK;
+}
+
+/* ------------------------------------------------------------------ the layer */
+int ora_layer(const ora_desc *desc, const ora_expert *experts, const ora_expert *shared,
+              uint32_t T, const float *x, const float *logits, const float *bias,
+              const uint8_t *want, ora_out *out) {
+  uint32_t E = desc->n_expert, k = desc->top_k, d = desc->d, f = desc->f, fs = desc->f_shared;
+  if (E == 0 || k == 0 || k > E || d == 0 || f == 0 || d % 32 || f % 32 || fs % 32)
+    return ORA_BAD_ARG;
+  if (desc->routed_fmt != ORA_FMT_Q8_0 && desc->routed_fmt != ORA_FMT_Q2S) return ORA_BAD_ARG;
+  uint32_t R = T * k;
+  int rc = ORA_OK;
+  int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (R + 1));
+  float *w32 = (float *)malloc(sizeof(float) * (R + 1));
+  int32_t *off = (int32_t *)malloc(sizeof(int32_t) * (E + 1));
+  int32_t *perm = (int32_t *)malloc(sizeof(int32_t) * (R + 1));
+  int32_t *pos = (int32_t *)malloc(sizeof(int32_t) * (R + 1));
+  int8_t *xq = (int8_t *)malloc((size_t)T * d + 1);
+  float *xs = (float *)malloc(sizeof(float) * ((size_t)T * d / 32 + 1));
+  double *o = (double *)malloc(sizeof(double) * d);
+  double *acc = (double *)malloc(sizeof(double) * d);
+  double *wd = (double *)malloc(sizeof(double) * k);
+  for (uint32_t t = 0; t < T; ++t)
+    ora_quantize(d, x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * d / 32);
+  ora_route(T, E, k, desc->s, logits, bias, idx, w32);
+  ora_permute(T, E, k, idx, off, perm, pos);
+  for (uint32_t t = 0; t < T && rc == ORA_OK; ++t) {
+    if (want && !want[t]) continue;
+    const int8_t *xqt = xq + (size_t)t * d;
+    const float *xst = xs + (size_t)t * d / 32;
+    const float *l = logits + (size_t)t * E;
+    /* routing weights in fp64 (the fp32 copy in w32 is only an output) */
+    double sum = 0.0;
+    for (uint32_t j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
+    for (uint32_t j = 0; j < k; ++j)
+      wd[j] = (double)desc->s * (1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]))) / sum;
+    for (uint32_t m = 0; m < d; ++m) acc[m] = 0.0;
+    if (fs > 0) {
+      rc = ora_expert_row(ORA_FMT_Q8_0, d, fs, shared, xqt, xst,
+                          out->hq_s ? out->hq_s + (size_t)t * fs : NULL,
+                          out->hs_s ? out->hs_s + (size_t)t * fs / 32 : NULL, o);
+      if (rc != ORA_OK) break;
+      for (uint32_t m = 0; m < d; ++m) acc[m] = o[m];
+    }
+    for (uint32_t j = 0; j < k; ++j) {
+      int32_t e = idx[t * k + j];
+      size_t p = (size_t)pos[t * k + j];
+      rc = ora_expert_row(desc->routed_fmt, d, f, &experts[e], xqt, xst,
+                          out->hq_r ? out->hq_r + p * f : NULL,
+                          out->hs_r ? out->hs_r + p * f / 32 : NULL, o);
+      if (rc != ORA_OK) break;
+      for (uint32_t m = 0; m < d; ++m) acc[m] += wd[j] * o[m];
+    }
+    if (out->y)
+      for (uint32_t m = 0; m < d; ++m) out->y[(size_t)t * d + m] = (float)acc[m];
+  }
+  if (out->idx) memcpy(out->idx, idx, sizeof(int32_t) * R);
+  if (out->w) memcpy(out->w, w32, sizeof(float) * R);
+  if (out->off) memcpy(out->off, off, sizeof(int32_t) * (E + 1));
+  if (out->perm) memcpy(out->perm, perm, sizeof(int32_t) * R);
+  if (out->pos) memcpy(out->pos, pos, sizeof(int32_t) * R);
+  if (out->xq) memcpy(out->xq, xq, (size_t)T * d);
+  if (out->xs) memcpy(out->xs, xs, sizeof(float) * ((size_t)T * d / 32));
+  free(idx);
+  free(w32);
+  free(off);
+  free(perm);
+  free(pos);
+  free(xq);
+  free(xs);
+  free(o);
+  free(acc);
+  free(wd);
+  return rc;
+}
