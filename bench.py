@@ -1,0 +1,539 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 routed-MoE layer: prints ONE JSON line on rank 0.
+
+Default workload: single-token decode of a GLM-5.2-shaped layer (E=256
+experts, top-8, d=6144, f=2048, shared expert 2048, Q8_0 weights, s=2.5,
+Zipf-skewed router logits), one token per step, token seeds 0..99.  A step is
+one moe_layer call (route -> permute -> quantise -> expert FFN -> shared
+expert -> combine), captured as a CUDA graph per step.  Inputs and weights are
+resident in HBM; L2 (129 MB) is flushed by writing a 2x-L2 buffer between
+steps, outside the per-step CUDA-event timing.
+
+--gpus N (under torchrun) runs N replicas: each rank decodes its own tokens on
+its own copy of the weights with no data-path collective (token-parallel
+decode, weak scaling).  ``value`` = all ranks' tokens / max over ranks of the
+device time.
+
+--impl reference times the CPU oracle (plain C, one host core) on bounded
+samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import platform
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s and achieved HBM GB/s (% of GB300 roofline) at T=1/16/512"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="decode_t1")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the oracle CPU-baseline sample")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the T=2/16/512 and 2-bit side measurements")
+    ap.add_argument("--no-graph", action="store_true", help="time eager calls, no CUDA graphs")
+    ap.add_argument("--flags", type=int, default=0, help="moe_desc.flags for the timed calls")
+    return ap.parse_args(argv)
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def rank_seeds(seeds, rank: int):
+    """Token seeds of one replica: rank 0 keeps the workload's seeds, rank r
+    shifts them by 1000*r so that replicas decode different tokens."""
+    return tuple(s + 1000 * rank for s in seeds)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ bytes model
+def row_bytes(fmt: int, K: int) -> int:
+    """Bytes of one quantised weight row of K weights: codes + fp16 block scales."""
+    return (K if fmt == 0 else K // 4) + (K // 32) * 2
+
+
+def stage_bytes(spec, U_routed: int):
+    """Algorithmic HBM bytes of the selected experts' and the shared expert's weights."""
+    gu = U_routed * 2 * spec.f * row_bytes(spec.fmt, spec.d)
+    dn = U_routed * spec.d * row_bytes(spec.fmt, spec.f)
+    if spec.f_shared:
+        gu += 2 * spec.f_shared * row_bytes(0, spec.d)
+        dn += spec.d * row_bytes(0, spec.f_shared)
+    return {"gateup": gu, "down": dn, "total": gu + dn}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+def source_hash(paths):
+    h = hashlib.sha256()
+    for p in paths:
+        with open(os.path.join(ROOT, p), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel_stage: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh)
+    for r in rec.get("records", []):
+        if r.get("stage") == kernel_stage and r.get("workload") == workload:
+            if r.get("source_hash") != source_hash(r.get("sources", [])):
+                return None
+            return float(r["dram_bytes_per_launch"])
+    return None
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import synth
+    import __graft_entry__ as ge
+    from routed_expert_decode_gb300 import moe
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    ge.build()
+    spec, T, seeds = synth.WORKLOADS[args.workload]
+    seeds = rank_seeds(seeds, rank)
+    K, W = args.steps, args.warmup
+
+    weights = synth.fill_layer_device(spec, dev)
+    layer = moe.Layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, weights,
+                      dev)
+    desc = layer.desc(args.flags)
+    ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=dev)
+    bias = torch.from_numpy(synth.bias(spec)).to(dev)
+    host_in = {s: synth.token_inputs(spec, s, T) for s in seeds}
+    dev_in = {s: (torch.from_numpy(host_in[s][1]).to(dev), torch.from_numpy(host_in[s][0]).to(dev))
+              for s in seeds}
+    y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    # unique routed experts per seed (setup pass through the library's router)
+    U_of = {}
+    off = torch.empty(spec.E + 1, dtype=torch.int32, device=dev)
+    idx = torch.empty((T, spec.k), dtype=torch.int32, device=dev)
+    wts = torch.empty((T, spec.k), dtype=torch.float32, device=dev)
+    perm = torch.empty(T * spec.k, dtype=torch.int32, device=dev)
+    pos = torch.empty(T * spec.k, dtype=torch.int32, device=dev)
+    for s in seeds:
+        moe.route(desc, dev_in[s][1], bias, idx, wts, off, perm, pos)
+        U_of[s] = int((off[1:] - off[:-1] > 0).sum().item())
+
+    names = moe.stage_names()
+    nst = len(names)
+    step_seed = [seeds[i % len(seeds)] for i in range(K)]
+    stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    stream = torch.cuda.current_stream(dev)
+
+    def eager(i, s):
+        x_d, l_d = dev_in[s]
+        moe.layer_timed(desc, layer.weights, x_d, l_d, bias, y, ws, stage_ev[i])
+
+    for evs in stage_ev:  # create every CUDA event before any capture
+        for ev in evs:
+            ev.record()
+    for i in range(W):  # warm-up
+        eager(i % K, step_seed[i % K])
+    torch.cuda.synchronize()
+
+    graphs = None
+    if not args.no_graph:
+        graphs = []
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for i in range(K):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    eager(i, step_seed[i])
+                graphs.append(g)
+        stream.wait_stream(cap)
+        for i in range(min(W, K)):
+            graphs[i].replay()
+        torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(K):
+        flush_buf.zero_()  # evict the previous step's weights from L2 (not timed)
+        ev0[i].record()
+        if graphs is not None:
+            graphs[i].replay()
+        else:
+            eager(i, step_seed[i])
+        ev1[i].record()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+
+    step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+    stage_ms = {n: [stage_ev[i][j].elapsed_time(stage_ev[i][j + 1]) for i in range(K)]
+                for j, n in enumerate(names)}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / K
+    tokens = T * K * world
+    value = tokens / (total_ms / 1e3)
+
+    # roofline of the dominant kernel
+    peak, peak_src = load_peaks()
+    bytes_steps = [stage_bytes(spec, U_of[s]) for s in step_seed]
+    mean_stage = {n: statistics.mean(v) for n, v in stage_ms.items()}
+    dom = max(mean_stage, key=mean_stage.get)
+    dom_bytes = sum(b.get(dom, 0) for b in bytes_steps) / K
+    achieved = dom_bytes / (mean_stage[dom] / 1e3) / 1e9 if dom in ("gateup", "down") else None
+    layer_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
+
+    # end-to-end through the C ABI with host buffers: H2D inputs, layer, D2H output
+    if True:
+        pin_in = {s: (torch.from_numpy(host_in[s][1]).pin_memory(),
+                      torch.from_numpy(host_in[s][0]).pin_memory()) for s in seeds}
+        x_d = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
+        l_d = torch.empty((T, spec.E), dtype=torch.float32, device=dev)
+        y_h = torch.empty((T, spec.d), dtype=torch.float32).pin_memory()
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+        for i in range(-W, K):
+            s = step_seed[i % K]
+            flush_buf.zero_()
+            if i >= 0:
+                e0[i].record()
+            x_d.copy_(pin_in[s][0], non_blocking=True)
+            l_d.copy_(pin_in[s][1], non_blocking=True)
+            moe.layer(desc, layer.weights, x_d, l_d, bias, y, ws)
+            y_h.copy_(y, non_blocking=True)
+            if i >= 0:
+                e1[i].record()
+        torch.cuda.synchronize()
+        e2e_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K))
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": round(tokens / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * spec.d * 4 + T * spec.E * 4,
+               "d2h_bytes_per_step": T * spec.d * 4}
+    assert moe.check_device_error(ws) == 0
+
+    sweep = None
+    if not args.no_sweep and world == 1 and args.workload == "decode_t1":
+        del graphs
+        sweep = run_sweep(torch, moe, synth, dev, layer, flush_buf, peak)
+
+    cpu = None
+    if rank == 0 and world == 1:
+        cpu = cpu_baseline(args.workload, args.cpu_seconds)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return None
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 x int8 -> int32 block dots, fp32 scales/accumulation",
+        "data": "synthetic (seeded counter-based generator; random Q8_0 weights of the layer's shape)",
+        "config": {
+            "workload": f"{args.workload}: T={T}, E={spec.E}, top_k={spec.k}, d={spec.d}, f={spec.f}, "
+                        f"f_shared={spec.f_shared}, fmt={'Q8_0' if spec.fmt == 0 else 'Q2S'}, "
+                        f"s={spec.s}, zipf_beta={spec.zipf_beta}",
+            "token_seeds": f"{seeds[0]}..{seeds[-1]}",
+            "tokens_per_step": T,
+            "l2": "flushed between steps (2x L2 write), outside the per-step CUDA-event time",
+            "timing": ("eager calls" if args.no_graph else "one CUDA graph per step")
+                      + "; CUDA events around each step and between stages",
+            "parallelism": f"replicas x{world} (token-parallel decode, no collective)",
+            "host": f"{platform.machine()}, {os.cpu_count()} cores",
+        },
+        "hbm": {"algorithmic_bytes_per_step": round(statistics.mean(b["total"] for b in bytes_steps)),
+                "achieved_gbs": round(layer_gbs, 1), "peak_gbs": peak,
+                "frac_of_measured": round(layer_gbs / peak, 4),
+                "frac_of_8tbs_nominal": round(layer_gbs / 8000.0, 4)},
+        "stage_us": {n: round(v * 1e3, 2) for n, v in mean_stage.items()},
+        "roofline": {"bound": "hbm", "kernel": dom,
+                     "achieved": round(achieved, 1) if achieved else None,
+                     "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4) if achieved else None,
+                     "peak_source": peak_src,
+                     "algorithmic_bytes_per_launch": round(dom_bytes),
+                     "traffic": traffic_for(dom, args.workload)},
+        "gpu_launches": K * nst,
+        "clocks": clk,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if sweep:
+        line["sweep"] = sweep
+    return line
+
+
+def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
+    """Side measurements at T=2/16/512 on the same layer and T=64 on the 2-bit
+    layer (eager calls, 10 steps each after 3 warm-ups, L2 flushed between)."""
+    out = {}
+    cases = [("batch_t2", layer), ("batch_t16", layer), ("prefill_t512", layer), ("q2_t64", None)]
+    for name, lay in cases:
+        spec, T, seeds = synth.WORKLOADS[name]
+        if lay is None:
+            w = synth.fill_layer_device(spec, dev)
+            lay = moe.Layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, w, dev)
+        desc = lay.desc()
+        ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=dev)
+        bias = torch.from_numpy(synth.bias(spec)).to(dev)
+        logits, x = synth.token_inputs(spec, seeds[0], T)
+        x_d, l_d = torch.from_numpy(x).to(dev), torch.from_numpy(logits).to(dev)
+        y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
+        names = moe.stage_names()
+        n = 10
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
+               for _ in range(n)]
+        for i in range(3):
+            moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[0])
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush_buf.zero_()
+            moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[i])
+        torch.cuda.synchronize()
+        step = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(n)]
+        stage = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
+                 for j, nm in enumerate(names)}
+        lay_off = lay.views(ws, T)["off"].cpu()
+        U = int((lay_off[1:] - lay_off[:-1] > 0).sum().item())
+        b = stage_bytes(spec, U)
+        ms = statistics.mean(step)
+        out[name] = {"T": T, "unique_experts": U, "ms_per_step": round(ms, 4),
+                     "tokens_per_s": round(T / (ms / 1e3), 1),
+                     "algorithmic_bytes": b["total"],
+                     "hbm_gbs": round(b["total"] / (ms / 1e3) / 1e9, 1),
+                     "frac_of_measured": round(b["total"] / (ms / 1e3) / 1e9 / peak, 4),
+                     "stage_us": {k: round(v * 1e3, 1) for k, v in stage.items()}}
+        assert moe.check_device_error(ws) == 0
+    return out
+
+
+# ------------------------------------------------------------------ CPU oracle
+_HOST_EXPERTS = {}
+
+
+def _host_expert(spec, e):
+    key = (spec.name, e)
+    if key not in _HOST_EXPERTS:
+        if len(_HOST_EXPERTS) > 64:
+            _HOST_EXPERTS.clear()
+        import synth
+
+        _HOST_EXPERTS[key] = synth.expert_host(spec, e)
+    return _HOST_EXPERTS[key]
+
+
+def oracle_tokens(workload: str, seconds: float, max_tokens=None, start=0):
+    """Time the oracle on successive tokens of the workload (from sample number
+    `start`) until `seconds` of oracle time have been spent or `max_tokens` are
+    done.  Returns (tokens, oracle_seconds, description)."""
+    import oracle
+    import synth
+
+    spec, T, seeds = synth.WORKLOADS[workload]
+    bias = synth.bias(spec)
+    shared = _host_expert(spec, spec.E) if spec.f_shared else None
+    done = 0
+    spent = 0.0
+    while True:
+        sample = start + done
+        s = seeds[sample % len(seeds)]
+        logits, x = synth.token_inputs(spec, s, T)
+        # one token of the batch per sample (tokens are independent given the routing)
+        t_pick = (sample * 37) % T
+        idx, _ = oracle.route(logits, bias, spec.k, spec.s)
+        cache = {int(e): _host_expert(spec, int(e)) for e in idx[t_pick]}
+        t0 = time.perf_counter()
+        oracle.layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, cache,
+                     shared, x, logits, bias, want=[t_pick])
+        spent += time.perf_counter() - t0
+        done += 1
+        if spent >= seconds or (max_tokens and done >= max_tokens):
+            break
+    desc = (f"{done} token(s) of {workload} (T={T} batch routed, one token's experts + shared "
+            f"expert run through the oracle per sample)")
+    return done, spent, desc
+
+
+def cpu_baseline(workload: str, seconds: float):
+    n, spent, desc = oracle_tokens(workload, seconds)
+    return {"value": round(n / spent, 4), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": desc, "oracle_seconds": round(spent, 2)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import synth
+
+    spec, T, seeds = synth.WORKLOADS[args.workload]
+    K, W = args.steps, args.warmup
+    for i in range(W):
+        oracle_tokens(args.workload, 0.0, max_tokens=1, start=i)
+    per = []
+    total_tokens = 0
+    t0 = time.perf_counter()
+    for i in range(K):
+        n, spent, desc = oracle_tokens(args.workload, 0.0, max_tokens=1, start=i)
+        per.append(spent)
+        total_tokens += n
+    wall = time.perf_counter() - t0
+    value = total_tokens / sum(per)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": W,
+        "ms_per_step": round(1e3 * sum(per) / K, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "int8 x int8 -> int32 block dots, fp64 sums (CPU oracle)",
+        "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": args.workload, "tokens_per_step": 1,
+                   "host": f"{platform.machine()}, {os.cpu_count()} cores"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
+                         "kind": "oracle", "sample": f"{K} steps x 1 token of {args.workload}"},
+        "e2e": {"value": round(value, 4), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "wall_s": round(wall, 2),
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        line = run_reference(args)
+    else:
+        line = run_ours(args)
+    if line is not None:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

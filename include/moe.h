@@ -1,0 +1,174 @@
+/*
+ * moe.h -- C ABI of the GB300 routed Mixture-of-Experts layer (libmoe.so).
+ *
+ * The layer (as run by the ds4 / NeutronStar engines for GLM-5.2 and Hy3):
+ *   1. score every expert with sigmoid(logit) + selection bias and keep the
+ *      top_k ("sigmoid routing with top-8": "256 experts, 512 lines", section
+ *      "Why GLM-5.2 in an engine built for DeepSeek"; "192-expert top-8 sigmoid
+ *      router with expert bias": NeutronStar main README, Hy3 paragraph), with
+ *      n_expert / top_k / scale as parameters, never constants ("256 experts,
+ *      512 lines", section "The constant that always said 256");
+ *   2. group the token->expert rows by expert (per-expert batches: NeutronStar
+ *      README, sections "MTP speculative decoding" and "Long-prompt prefill");
+ *   3. quantise activations to int8 per 32-block and run each selected expert's
+ *      SwiGLU FFN with int8 x int8 block dot products over block-quantised
+ *      weights (the dp4a expert kernels: NeutronStar README, "What this branch
+ *      adds over upstream"; Q8_0: "The model");
+ *   4. add the always-on shared expert ("MoE with shared expert") and combine
+ *      the routed outputs with their routing weights.
+ *
+ * Arithmetic contract (bit-exact parts are identical to the CPU oracle):
+ *   score     c_i = fp32(sigma_i + b_i), sigma_i = fp32(1 / (1 + spec_exp(-l_i)));
+ *             spec_exp: clamp to [-86, 88], n = rint(x*log2e), Cody-Waite
+ *             reduction with C1 = 355/512 and C2 = fp32(ln2 - C1), degree-7
+ *             Taylor polynomial (fp32 coefficients 1/k!, Horner with fma), times
+ *             2^n -- all fp32 round-to-nearest.
+ *   top-k     largest c first, equal c -> lower expert index first.
+ *   weights   w_j = s * sigma_j / sum_j sigma_j (fp32; not bit-exact).
+ *   permute   off[e] = rows before expert e; rows of one expert in (token, slot)
+ *             order: perm[off[e] + r] = t*top_k + j; pos is perm's inverse.
+ *   quantise  per 32-block: scale = max|x| / 127 (fp32), q = clamp(
+ *             round_half_away(x / scale), -127, 127); a zero scale gives q = 0.
+ *   expert    g = sum_b isum_b * ws_b * xs_b (isum_b exact int32), likewise u;
+ *             h = g * sigmoid(g) * u requantised as above; o likewise with the
+ *             down matrix.  Only isum_b and the int8 x codes are bit-exact; h codes
+ *             may differ by one step where fp32 order matters.
+ *   combine   y[t] = o_shared[t] + sum_j w[t,j] * o[t,j], shared first, then
+ *             slots in order (no atomics: run-to-run deterministic).
+ *
+ * Memory: every pointer is caller-owned DEVICE memory except the desc/weights
+ * structs (host).  The library allocates nothing.  Scratch comes from the
+ * caller's workspace (moe_workspace_size).  Calls are asynchronous on `stream`
+ * (a cudaStream_t; NULL = legacy default stream), stateless and re-entrant as
+ * long as concurrent calls use different workspaces.  Arguments are checked on
+ * the host before anything is enqueued; nothing aborts or exits.  Device-side
+ * argument faults (an expert index out of range in moe_ffn's inputs) set an
+ * error word in the workspace, read by moe_check_device_error.
+ * NaN or infinite inputs are unsupported.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* bad shape, null or misaligned pointer */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  MOE_ERR_WORKSPACE = 3,    /* ws_bytes < moe_workspace_size() */
+  MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
+  MOE_ERR_TIMEOUT = 5,      /* a bounded device wait gave up */
+  MOE_ERR_DEVICE_CHECK = 6  /* the kernels flagged a bad input on the device */
+} moe_status;
+
+/* Weight formats, both planar: a code plane and an fp16 scale plane, one scale
+ * per 32 consecutive weights along the reduction dimension.
+ *   MOE_FMT_Q8_0: int8 codes, row of K weights = K bytes + K/32 fp16.
+ *   MOE_FMT_Q2S : 2-bit codes c in {0,1,2,3} meaning {-3,-1,+1,+3}; weight i of
+ *                 a row sits at bits 2(i%4) of byte i/4 (LSB first); a row of K
+ *                 weights = K/4 bytes + K/32 fp16. */
+typedef enum { MOE_FMT_Q8_0 = 0, MOE_FMT_Q2S = 1 } moe_fmt;
+
+/* One quantised matrix of all experts: q = code plane, scale = fp16 bits.
+ * q must be 32-byte aligned, scale 16-byte aligned. */
+typedef struct {
+  const void *q;
+  const uint16_t *scale;
+} moe_mat;
+
+/* flags */
+#define MOE_FLAG_DEBUG_TAPS 0x1u /* write sampled int32 block dots into the workspace */
+#define MOE_FLAG_FORCE_GEMV 0x2u /* every expert on the dp4a path (no tensor-core path) */
+#define MOE_FLAG_FORCE_TC 0x4u   /* every routed expert with >= 1 row on the tensor path */
+
+typedef struct {
+  uint32_t n_expert; /* E, 1..1024 */
+  uint32_t top_k;    /* k, 1..E (and <= 32) */
+  uint32_t d;        /* hidden size, multiple of 32 */
+  uint32_t f;        /* routed expert width, multiple of 32 */
+  uint32_t f_shared; /* shared expert width, multiple of 32; 0 = no shared expert */
+  int32_t routed_fmt;/* moe_fmt of the routed experts (the shared expert is Q8_0) */
+  float s;           /* routing scale */
+  uint32_t flags;    /* MOE_FLAG_* */
+} moe_desc;
+
+/* Routed experts, expert-major: gate, up [E][f][d]; down [E][d][f] (codes; for
+ * Q2S the last dimension is in bytes = K/4), scales [E][rows][K/32].
+ * Shared expert (Q8_0): s_gate, s_up [f_shared][d]; s_down [d][f_shared]. */
+typedef struct {
+  moe_mat gate, up, down;
+  moe_mat s_gate, s_up, s_down;
+} moe_weights;
+
+/* Regions of the workspace (byte offsets), for debug taps and tests.
+ * Rows of the expert FFN are "slots": routed rows at p = pos[t*k+j] in [0, R),
+ * shared rows at R + t, R = T*k.  Widths use fmax = max(f, f_shared). */
+typedef struct {
+  size_t idx, w, off, perm, pos; /* moe_layer's routing results */
+  size_t xq, xs;                 /* int8 [T][d], fp32 [T][d/32] */
+  size_t hq, hs;                 /* int8 [R+T][fmax], fp32 [R+T][fmax/32] */
+  size_t h, o;                   /* fp32 [R+T][fmax], fp32 [R+T][d] */
+  size_t plan;                   /* internal work list */
+  size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
+  size_t err;                    /* uint32 device error word: always offset 0 */
+  size_t total;
+  uint32_t n_tap;                /* tapped features per row (gate/up and down) */
+} moe_ws_layout;
+
+/* Tap layout: gate/up: tap_gu[slot][2][n_tap][d/32] int32 (0 = gate, 1 = up) for
+ * the features n_j = (j * width / n_tap + j) % width, j < n_tap;
+ * down: tap_dn[slot][n_tap][fmax/32] int32 for outputs m_j = (j * d / n_tap + j) % d. */
+
+/* Workspace bytes moe_ffn / moe_layer need for T tokens (0 on invalid desc). */
+size_t moe_workspace_size(const moe_desc *desc, uint32_t T);
+moe_status moe_workspace_layout(const moe_desc *desc, uint32_t T, moe_ws_layout *out);
+
+/* Router + permutation.  logits [T][E], bias [E] (fp32) -> idx [T][k] int32,
+ * w [T][k] fp32, off [E+1] int32, perm [T*k] int32, pos [T*k] int32.
+ * Needs no workspace (ws may be NULL). T = 0 writes off = 0 and returns MOE_OK. */
+moe_status moe_route(const moe_desc *desc, const float *logits, const float *bias, uint32_t T,
+                     int32_t *idx, float *w, int32_t *off, int32_t *perm, int32_t *pos,
+                     void *ws, size_t ws_bytes, void *stream);
+
+/* Expert FFN + shared expert + combine for routing results produced by
+ * moe_route (or any equivalent producer): x [T][d] fp32 -> y [T][d] fp32. */
+moe_status moe_ffn(const moe_desc *desc, const moe_weights *wts, const float *x, uint32_t T,
+                   const int32_t *idx, const float *w, const int32_t *off,
+                   const int32_t *perm, const int32_t *pos, float *y, void *ws,
+                   size_t ws_bytes, void *stream);
+
+/* The whole layer: moe_route into the workspace, then moe_ffn. */
+moe_status moe_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
+                     const float *logits, const float *bias, uint32_t T, float *y, void *ws,
+                     size_t ws_bytes, void *stream);
+
+/* moe_layer with timing markers for profiling.  `events` holds n_events
+ * cudaEvent_t handles (created by the caller); events[0] is recorded on
+ * `stream` before the first stage and events[i] after stage i-1, for
+ * i < n_events (as external records, so they also work inside CUDA graph
+ * capture).  Stage names come from moe_stage_name.  events == NULL or
+ * n_events == 0 makes this identical to moe_layer. */
+moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const float *x,
+                           const float *logits, const float *bias, uint32_t T, float *y,
+                           void *ws, size_t ws_bytes, void *stream, void *const *events,
+                           uint32_t n_events);
+
+/* Name of stage i of moe_layer ("route", "permute", ...), NULL past the last. */
+const char *moe_stage_name(uint32_t i);
+
+/* Synchronise `stream` and read (then clear) the workspace's device error word
+ * (the first 4 bytes of any workspace).
+ * MOE_OK if no kernel flagged a fault; MOE_ERR_DEVICE_CHECK otherwise. */
+moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream);
+
+const char *moe_status_string(moe_status st);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H */

@@ -1,0 +1,256 @@
+// moe_api.cu -- the C ABI (moe.h): argument checks, workspace layout and the
+// launch sequence.  The host only validates and enqueues; every step of the
+// layer runs in this library's kernels on the caller's stream.
+#include <string.h>
+
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+bool desc_ok(const moe_desc *d) {
+  if (!d) return false;
+  if (d->n_expert < 1 || d->n_expert > 1024) return false;
+  if (d->top_k < 1 || d->top_k > d->n_expert || d->top_k > 32) return false;
+  if (d->d == 0 || d->d % 32 || d->f == 0 || d->f % 32 || d->f_shared % 32) return false;
+  if (d->routed_fmt != MOE_FMT_Q8_0 && d->routed_fmt != MOE_FMT_Q2S) return false;
+  if (!(d->s == d->s)) return false;  // NaN scale
+  // int32 indexing of rows and work items
+  if ((uint64_t)d->n_expert * d->f > (1u << 30) || (uint64_t)d->n_expert * d->d > (1u << 30))
+    return false;
+  return true;
+}
+
+bool mat_ok(const moe_mat &m, int fmt) {
+  if (!m.q || !m.scale) return false;
+  if (!aligned(m.q, fmt == MOE_FMT_Q2S ? 8 : 32)) return false;
+  if (!aligned(m.scale, 2)) return false;
+  return true;
+}
+
+bool weights_ok(const moe_desc *d, const moe_weights *w) {
+  if (!w) return false;
+  const int f = d->routed_fmt;
+  if (!mat_ok(w->gate, f) || !mat_ok(w->up, f) || !mat_ok(w->down, f)) return false;
+  if (d->f_shared) {
+    if (!mat_ok(w->s_gate, MOE_FMT_Q8_0) || !mat_ok(w->s_up, MOE_FMT_Q8_0) ||
+        !mat_ok(w->s_down, MOE_FMT_Q8_0))
+      return false;
+  }
+  return true;
+}
+
+moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
+  moe_ws_layout L;
+  memset(&L, 0, sizeof L);
+  const size_t R = (size_t)T * d->top_k;
+  const size_t slots = R + (d->f_shared ? T : 0);
+  const size_t fmax = d->f > d->f_shared ? d->f : d->f_shared;
+  size_t p = 0;
+  L.err = p;
+  p = align_up(p + sizeof(uint32_t));
+  L.idx = p; p = align_up(p + R * 4);
+  L.w = p; p = align_up(p + R * 4);
+  L.off = p; p = align_up(p + (size_t)(d->n_expert + 1) * 4);
+  L.perm = p; p = align_up(p + R * 4);
+  L.pos = p; p = align_up(p + R * 4);
+  L.plan = p; p = align_up(p + PlanView::ints(d->n_expert) * 4);
+  L.xq = p; p = align_up(p + (size_t)T * d->d);
+  L.xs = p; p = align_up(p + (size_t)T * (d->d / 32) * 4);
+  L.h = p; p = align_up(p + slots * fmax * 4);
+  L.hq = p; p = align_up(p + slots * fmax);
+  L.hs = p; p = align_up(p + slots * (fmax / 32) * 4);
+  L.o = p; p = align_up(p + slots * d->d * 4);
+  L.n_tap = kNTap;
+  if (d->flags & MOE_FLAG_DEBUG_TAPS) {
+    L.tap_gu = p; p = align_up(p + slots * 2 * kNTap * (d->d / 32) * 4);
+    L.tap_dn = p; p = align_up(p + slots * kNTap * (fmax / 32) * 4);
+  } else {
+    L.tap_gu = L.tap_dn = 0;
+  }
+  L.total = p;
+  return L;
+}
+
+int sm_count_of_current_device() {
+  int dev = 0, n = kSmCount;
+  if (cudaGetDevice(&dev) == cudaSuccess)
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n > 0 ? n : kSmCount;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void *stream) {
+  Ctx c;
+  memset(&c, 0, sizeof c);
+  c.desc = *d;
+  if (w) c.wts = *w;
+  c.T = T;
+  c.R = T * d->top_k;
+  c.fmax = d->f > d->f_shared ? d->f : d->f_shared;
+  c.ws = (uint8_t *)ws;
+  c.L = make_layout(d, T);
+  c.stream = (cudaStream_t)stream;
+  c.sm_count = sm_count_of_current_device();
+  return c;
+}
+
+const char *const kStageNames[] = {"route", "permute", "plan",  "quant_x",
+                                   "gateup", "requant", "down", "combine"};
+constexpr uint32_t kNumStages = sizeof(kStageNames) / sizeof(kStageNames[0]);
+
+// optional timing markers: events[i] after stage i-1
+struct Marks {
+  void *const *ev;
+  uint32_t n;
+  cudaStream_t s;
+  cudaError_t mark(uint32_t i) const {
+    // external records also become event nodes when the stream is being captured
+    if (ev && i < n) return cudaEventRecordWithFlags((cudaEvent_t)ev[i], s, cudaEventRecordExternal);
+    return cudaSuccess;
+  }
+};
+
+// FFN stages shared by moe_ffn and moe_layer (stage numbers 2..7)
+moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float *w,
+                   const int32_t *off, const int32_t *perm, const int32_t *pos, float *y,
+                   const Marks &mk) {
+  uint32_t *err = (uint32_t *)(c.ws + c.L.err);
+  cudaError_t e;
+  if ((e = launch_plan(c, off, idx, perm, pos, err)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(3)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_quant_x(c, x)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(4)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_gateup(c, perm)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(5)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_requant_h(c)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(6)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_down(c)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(7)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_combine(c, w, pos, y)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(8)) != cudaSuccess) return from_cuda(e);
+  return MOE_OK;
+}
+
+moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
+                     const float *logits, const float *bias, uint32_t T, float *y, void *ws,
+                     size_t ws_bytes, void *stream, void *const *events, uint32_t n_events) {
+  if (!desc_ok(desc) || !weights_ok(desc, wts)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !bias || !y)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
+  Ctx c = make_ctx(desc, wts, T, ws, stream);
+  Marks mk{events, n_events, c.stream};
+  int32_t *idx = (int32_t *)(c.ws + c.L.idx);
+  float *w = (float *)(c.ws + c.L.w);
+  int32_t *off = (int32_t *)(c.ws + c.L.off);
+  int32_t *perm = (int32_t *)(c.ws + c.L.perm);
+  int32_t *pos = (int32_t *)(c.ws + c.L.pos);
+  uint32_t *err = (uint32_t *)(c.ws + c.L.err);
+  cudaError_t e;
+  if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_route(c, logits, bias, idx, w)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_permute(c, idx, off, perm, pos, err)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(2)) != cudaSuccess) return from_cuda(e);
+  return run_ffn(c, x, idx, w, off, perm, pos, y, mk);
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_desc *desc, uint32_t T) {
+  if (!desc_ok(desc)) return 0;
+  return make_layout(desc, T).total;
+}
+
+moe_status moe_workspace_layout(const moe_desc *desc, uint32_t T, moe_ws_layout *out) {
+  if (!desc_ok(desc) || !out) return MOE_ERR_INVALID_ARG;
+  *out = make_layout(desc, T);
+  return MOE_OK;
+}
+
+moe_status moe_route(const moe_desc *desc, const float *logits, const float *bias, uint32_t T,
+                     int32_t *idx, float *w, int32_t *off, int32_t *perm, int32_t *pos,
+                     void *ws, size_t ws_bytes, void *stream) {
+  (void)ws;
+  (void)ws_bytes;
+  if (!desc_ok(desc)) return MOE_ERR_INVALID_ARG;
+  if (!off) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !bias || !idx || !w || !perm || !pos)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
+  Ctx c = make_ctx(desc, nullptr, T, nullptr, stream);
+  cudaError_t e;
+  if ((e = launch_route(c, logits, bias, idx, w)) != cudaSuccess) return from_cuda(e);
+  // moe_route's own idx is always in range, so the device error word is not needed
+  if ((e = launch_permute(c, idx, off, perm, pos, nullptr)) != cudaSuccess) return from_cuda(e);
+  return MOE_OK;
+}
+
+moe_status moe_ffn(const moe_desc *desc, const moe_weights *wts, const float *x, uint32_t T,
+                   const int32_t *idx, const float *w, const int32_t *off,
+                   const int32_t *perm, const int32_t *pos, float *y, void *ws,
+                   size_t ws_bytes, void *stream) {
+  if (!desc_ok(desc) || !weights_ok(desc, wts)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || !off) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !idx || !w || !perm || !pos || !y)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
+  Ctx c = make_ctx(desc, wts, T, ws, stream);
+  return run_ffn(c, x, idx, w, off, perm, pos, y, Marks{nullptr, 0, c.stream});
+}
+
+moe_status moe_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
+                     const float *logits, const float *bias, uint32_t T, float *y, void *ws,
+                     size_t ws_bytes, void *stream) {
+  return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0);
+}
+
+moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const float *x,
+                           const float *logits, const float *bias, uint32_t T, float *y,
+                           void *ws, size_t ws_bytes, void *stream, void *const *events,
+                           uint32_t n_events) {
+  return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, events, n_events);
+}
+
+const char *moe_stage_name(uint32_t i) { return i < kNumStages ? kStageNames[i] : nullptr; }
+
+moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream) {
+  if (!ws || ws_bytes < sizeof(uint32_t)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint32_t word = 0;
+  if (cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (word == 0) return MOE_OK;
+  if (cudaMemsetAsync(ws, 0, sizeof word, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  return (word & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_CHECK;
+}
+
+const char *moe_status_string(moe_status st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_DEVICE_CHECK: return "device-side input check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,186 @@
+// moe_internal.cuh -- device helpers and kernel launchers shared by the
+// library's translation units.  Nothing here is shared with the CPU oracle.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kWarp = 32;
+constexpr int kBlock = 32;   // quantisation block (weights and activations)
+constexpr int kNTap = 8;     // tapped features per slot when MOE_FLAG_DEBUG_TAPS
+constexpr int kSmCount = 152;
+
+// device error word bits
+constexpr uint32_t kErrBadIndex = 1u;   // expert index outside [0, E)
+constexpr uint32_t kErrBadOffsets = 2u; // off[] not a valid prefix of R rows
+constexpr uint32_t kErrTimeout = 4u;    // a bounded wait gave up
+
+// ---------------------------------------------------------------- plan layout
+// int32 array in the workspace describing the active experts of one call.
+//   [0] U (active experts incl. the shared one)   [1] gate/up work items
+//   [2] down work items   [3] largest routed row count   [4..7] reserved
+//   act_e[E+1]   expert id per active slot u (E = the shared expert)
+//   act_row0[E+1] first FFN slot of expert u; act_rows[E+1] its row count
+//   item_gu[E+2]  exclusive prefix of gate/up items (features) per u
+struct PlanView {
+  int *hdr, *act_e, *act_row0, *act_rows, *item_gu;
+  __host__ __device__ PlanView(int *base, uint32_t E) {
+    hdr = base;
+    act_e = base + 8;
+    act_row0 = act_e + (E + 1);
+    act_rows = act_row0 + (E + 1);
+    item_gu = act_rows + (E + 1);
+  }
+  __host__ __device__ static size_t ints(uint32_t E) { return 8 + 4 * (size_t)(E + 2); }
+};
+
+// ---------------------------------------------------------------- spec-exp
+// e^x, bit-reproducible on any IEEE fp32 machine: clamp to [-86, 88];
+// n = rint(x * log2e); Cody-Waite reduction r = (x - n*C1) - n*C2 with
+// C1 = 355/512 and C2 = fp32(ln2 - C1); degree-7 Taylor polynomial of e^r with
+// fp32(1/k!) coefficients by Horner (fma); scaled by an exactly built 2^n.
+__device__ __forceinline__ float spec_exp(float x) {
+  x = fminf(fmaxf(x, -86.0f), 88.0f);
+  const float n = rintf(__fmul_rn(x, 0x1.715476p+0f));
+  float r = __fmaf_rn(-n, 0x1.63p-1f, x);
+  r = __fmaf_rn(-n, -0x1.bd0106p-13f, r);
+  float p = 0x1.a01a02p-13f;            // 1/7!
+  p = __fmaf_rn(p, r, 0x1.6c16c2p-10f); // 1/6!
+  p = __fmaf_rn(p, r, 0x1.111112p-7f);  // 1/5!
+  p = __fmaf_rn(p, r, 0x1.555556p-5f);  // 1/4!
+  p = __fmaf_rn(p, r, 0x1.555556p-3f);  // 1/3!
+  p = __fmaf_rn(p, r, 0.5f);
+  p = __fmaf_rn(p, r, 1.0f);
+  p = __fmaf_rn(p, r, 1.0f);
+  const int ni = __float2int_rn(n);
+  return __fmul_rn(p, __int_as_float((ni + 127) << 23));
+}
+
+__device__ __forceinline__ float sigmoid_rn(float x) {
+  return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
+}
+
+// one 32-element block: scale = amax/127, q = clamp(round_half_away(x/scale))
+__device__ __forceinline__ int quant_one(float x, float scale) {
+  if (scale == 0.0f) return 0;
+  float v = roundf(__fdiv_rn(x, scale));
+  v = fminf(fmaxf(v, -127.0f), 127.0f);
+  return (int)v;
+}
+
+__device__ __forceinline__ float half_bits_to_float(uint16_t b) {
+  return __half2float(__ushort_as_half(b));
+}
+
+// ---------------------------------------------------------------- loads
+struct W8 {
+  uint32_t v[8];
+};
+
+// 32 bytes, read-only, streamed (no L1 allocation)
+__device__ __forceinline__ W8 ld_stream32(const void *p) {
+  W8 w;
+  asm("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w.v[0]), "=r"(w.v[1]), "=r"(w.v[2]), "=r"(w.v[3]), "=r"(w.v[4]), "=r"(w.v[5]),
+        "=r"(w.v[6]), "=r"(w.v[7])
+      : "l"(p));
+  return w;
+}
+
+// 32 bytes, read-only, cached (activations reused by many warps)
+__device__ __forceinline__ W8 ld_cached32(const void *p) {
+  W8 w;
+  asm("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(w.v[0]), "=r"(w.v[1]), "=r"(w.v[2]), "=r"(w.v[3]), "=r"(w.v[4]), "=r"(w.v[5]),
+        "=r"(w.v[6]), "=r"(w.v[7])
+      : "l"(p));
+  return w;
+}
+
+__device__ __forceinline__ uint2 ld_stream8(const void *p) {
+  uint2 w;
+  asm("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(w.x), "=r"(w.y) : "l"(p));
+  return w;
+}
+
+// ---------------------------------------------------------------- block dots
+// Weight block in registers, per format.  Q8_0: 8 words of int8.  Q2S: the
+// 8 code bytes spread to 8 words of one code (0..3) per byte lane.
+template <int FMT>
+struct WBlock;
+
+template <>
+struct WBlock<MOE_FMT_Q8_0> {
+  W8 w;
+  static constexpr int kRowBytesPer32 = 32;
+  __device__ __forceinline__ void load(const int8_t *row, int b) { w = ld_stream32(row + 32 * b); }
+  __device__ __forceinline__ int dot(const W8 &x) const {
+    int s = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s = __dp4a((int)w.v[q], (int)x.v[q], s);
+    return s;
+  }
+};
+
+__device__ __forceinline__ uint32_t spread_codes(uint32_t byte) {
+  return (byte | (byte << 6) | (byte << 12) | (byte << 18)) & 0x03030303u;
+}
+
+template <>
+struct WBlock<MOE_FMT_Q2S> {
+  uint2 c;
+  static constexpr int kRowBytesPer32 = 8;
+  __device__ __forceinline__ void load(const int8_t *row, int b) { c = ld_stream8(row + 8 * b); }
+  // sum_i (2c_i - 3) x_i = 2 sum c_i x_i - 3 sum x_i, exact in int32
+  __device__ __forceinline__ int dot(const W8 &x) const {
+    int sc = 0, sx = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const uint32_t word = q < 4 ? c.x : c.y;
+      const uint32_t cw = spread_codes((word >> (8 * (q & 3))) & 0xFFu);
+      sc = __dp4a((int)cw, (int)x.v[q], sc);
+      sx = __dp4a(0x01010101, (int)x.v[q], sx);
+    }
+    return 2 * sc - 3 * sx;
+  }
+};
+
+__host__ __device__ inline size_t row_bytes(int fmt, uint32_t K) {
+  return fmt == MOE_FMT_Q2S ? K / 4 : K;
+}
+
+// tapped feature j of a row of `width` outputs
+__host__ __device__ inline uint32_t tap_feature(uint32_t j, uint32_t width) {
+  return (uint32_t)(((uint64_t)j * width / kNTap + j) % width);
+}
+
+// ---------------------------------------------------------------- launchers
+struct Ctx {
+  moe_desc desc;
+  moe_weights wts;
+  uint32_t T, R;
+  uint32_t fmax;
+  uint8_t *ws;
+  moe_ws_layout L;
+  cudaStream_t stream;
+  int sm_count;
+};
+
+cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, int32_t *idx,
+                         float *w);
+cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32_t *perm,
+                           int32_t *pos, uint32_t *err);
+cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
+                        const int32_t *perm, const int32_t *pos, uint32_t *err);
+cudaError_t launch_quant_x(const Ctx &c, const float *x);
+cudaError_t launch_gateup(const Ctx &c, const int32_t *perm);
+cudaError_t launch_requant_h(const Ctx &c);
+cudaError_t launch_down(const Ctx &c);
+cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, float *y);
+
+}  // namespace moe

@@ -1,0 +1,320 @@
+// route.cu -- router, permutation, work plan and activation quantiser.
+//
+// Router: sigmoid scoring plus a selection bias, top_k per token ("sigmoid
+// routing with top-8": "256 experts, 512 lines", section "Why GLM-5.2 in an
+// engine built for DeepSeek"; Hy3's "192-expert top-8 sigmoid router with expert
+// bias": NeutronStar main README).  One generic warp-per-token kernel for every
+// n_expert / top_k / scale: no constant is baked in (the lesson of "The constant
+// that always said 256").
+#include "moe_internal.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kRouteWarps = 8;
+
+// One warp per token.  Lane l owns experts l, l+32, ...; each of the top_k
+// rounds takes every lane's best unpicked expert and reduces them with a
+// butterfly argmax whose order is (score descending, index ascending), so all
+// lanes agree on a unique winner and ties go to the lower index.
+__global__ void __launch_bounds__(kRouteWarps * 32)
+    k_route(const float *__restrict__ logits, const float *__restrict__ bias, uint32_t T,
+            uint32_t E, uint32_t k, float s, int32_t *__restrict__ idx, float *__restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t t = blockIdx.x * kRouteWarps + threadIdx.x / 32;
+  if (t >= T) return;
+  const float *l = logits + (size_t)t * E;
+  const int nper = (int)((E + 31) / 32);
+  float c[32], sg[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint32_t e = (uint32_t)lane + 32u * i;
+    c[i] = -INFINITY;
+    sg[i] = 0.0f;
+    if (i < nper && e < E) {
+      const float sgm = sigmoid_rn(l[e]);
+      sg[i] = sgm;
+      c[i] = __fadd_rn(sgm, bias[e]);
+    }
+  }
+  uint32_t taken = 0;
+  float my_sigma = 0.0f;  // lane j keeps the sigma of slot j
+  for (uint32_t j = 0; j < k; ++j) {
+    float bc = -INFINITY, bs = 0.0f;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      if (i < nper && !((taken >> i) & 1u) && c[i] > bc) {
+        bc = c[i];
+        be = lane + 32 * i;
+        bs = sg[i];
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      if (oc > bc || (oc == bc && oe < be)) {
+        bc = oc;
+        be = oe;
+        bs = os;
+      }
+    }
+    if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    if ((uint32_t)lane == j) my_sigma = bs;
+    if (lane == 0) idx[(size_t)t * k + j] = be;
+  }
+  // w_j = s * sigma_j / sum_j sigma_j, the sum taken in slot order
+  float sum = 0.0f;
+  for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
+  if ((uint32_t)lane < k) w[(size_t)t * k + lane] = __fmul_rn(s, __fdiv_rn(my_sigma, sum));
+}
+
+// Stable permutation without position atomics (1 CTA, 32 warps).
+// Rows r = t*k + j.  Warp w owns a contiguous range of tokens; (A) each warp
+// counts its rows per expert, (B) a per-expert scan over warps gives each warp's
+// starting rank, (C) a scan over experts gives off[], (D) each warp walks its
+// rows in order, ranking equal experts inside a 32-row group with match_any.
+constexpr int kPermThreads = 1024;
+constexpr int kPermWarps = kPermThreads / 32;
+
+__global__ void __launch_bounds__(kPermThreads)
+    k_permute(const int32_t *__restrict__ idx, uint32_t T, uint32_t E, uint32_t k,
+              int32_t *__restrict__ off, int32_t *__restrict__ perm, int32_t *__restrict__ pos,
+              uint32_t *err) {
+  extern __shared__ int smem[];
+  int *hist = smem;                       // [kPermWarps][E]
+  int *cnt = hist + (size_t)kPermWarps * E;  // [E]
+  int *scan = cnt + E;                    // [kPermThreads]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t R = T * k;
+  for (uint32_t i = tid; i < (uint32_t)kPermWarps * E; i += kPermThreads) hist[i] = 0;
+  __syncthreads();
+  const uint32_t tok_per_warp = (T + kPermWarps - 1) / kPermWarps;
+  const uint32_t r_begin = min(T, warp * tok_per_warp) * k;
+  const uint32_t r_end = min(T, (warp + 1) * tok_per_warp) * k;
+  // (A)
+  for (uint32_t r = r_begin + lane; r < r_end; r += 32) {
+    const int e = idx[r];
+    if (e < 0 || (uint32_t)e >= E) {
+      if (err) atomicOr(err, kErrBadIndex);
+      continue;
+    }
+    atomicAdd(&hist[(size_t)warp * E + e], 1);
+  }
+  __syncthreads();
+  // (B) hist[w][e] := rows of e in warps < w
+  for (uint32_t e = tid; e < E; e += kPermThreads) {
+    int run = 0;
+    for (int w2 = 0; w2 < kPermWarps; ++w2) {
+      const int v = hist[(size_t)w2 * E + e];
+      hist[(size_t)w2 * E + e] = run;
+      run += v;
+    }
+    cnt[e] = run;
+  }
+  __syncthreads();
+  // (C) exclusive scan of cnt over experts, in chunks of kPermThreads
+  int carry = 0;
+  for (uint32_t base = 0; base < E; base += kPermThreads) {
+    const uint32_t e = base + tid;
+    const int v = e < E ? cnt[e] : 0;
+    scan[tid] = v;
+    __syncthreads();
+    for (int o = 1; o < kPermThreads; o <<= 1) {
+      const int add = tid >= o ? scan[tid - o] : 0;
+      __syncthreads();
+      scan[tid] += add;
+      __syncthreads();
+    }
+    if (e < E) {
+      const int excl = carry + scan[tid] - v;
+      off[e] = excl;
+      cnt[e] = excl;  // cnt now holds off[e]
+    }
+    carry += scan[kPermThreads - 1];
+    __syncthreads();
+  }
+  if (tid == 0) off[E] = carry;
+  __syncthreads();
+  // (D)
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (uint32_t g = r_begin; g < r_end; g += 32) {
+    const uint32_t r = g + lane;
+    const bool live = r < r_end;
+    int e = live ? idx[r] : -1;
+    if (e >= (int)E) e = -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    if (live && e >= 0) {
+      const int rank = __popc(peers & lt_mask);
+      int *run = &hist[(size_t)warp * E + e];
+      const int p = cnt[e] + *run + rank;
+      perm[p] = (int32_t)r;
+      pos[r] = p;
+    }
+    __syncwarp();
+    // the highest lane of each peer group advances that expert's running rank
+    if (live && e >= 0 && (peers >> lane) == 1u) hist[(size_t)warp * E + e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+// Work plan from off[] (1 CTA).  Validates off, perm, pos and idx against one
+// another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
+// no work (so no kernel indexes with untrusted values).  Otherwise it lists the
+// active experts in ascending order, the shared expert last.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads)
+    k_plan(const int32_t *__restrict__ off, const int32_t *__restrict__ idx,
+           const int32_t *__restrict__ perm, const int32_t *__restrict__ pos, uint32_t T,
+           uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int *plan, uint32_t *err) {
+  __shared__ int scan[kPlanThreads];
+  __shared__ int bad;
+  const int tid = threadIdx.x;
+  const uint32_t R = T * k;
+  PlanView P(plan, E);
+  if (tid == 0) {
+    *err = 0u;
+    bad = (off[0] != 0 || off[E] != (int)R) ? 1 : 0;
+  }
+  __syncthreads();
+  for (uint32_t e = tid; e < E; e += kPlanThreads)
+    if (off[e + 1] < off[e]) bad = 1;
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      atomicOr(err, kErrBadOffsets);
+      for (int i = 0; i < 8; ++i) P.hdr[i] = 0;  // hdr[4] = 0: nothing validated
+      P.item_gu[0] = 0;
+    }
+    return;
+  }
+  // cross-check the routing arrays: slot p of expert e's segment holds a row
+  // r of e with pos[r] == p, and every pos[r] points back at r
+  for (uint32_t p = tid; p < R; p += kPlanThreads) {
+    const int r = perm[p];
+    int lo = 0, hi = (int)E;  // largest e with off[e] <= p
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (off[mid] <= (int)p) lo = mid; else hi = mid;
+    }
+    if (r < 0 || (uint32_t)r >= R || idx[r] != lo || pos[r] != (int)p) bad = 2;
+  }
+  for (uint32_t r = tid; r < R; r += kPlanThreads) {
+    const int p = pos[r];
+    if (p < 0 || (uint32_t)p >= R || perm[p] != (int)r) bad = 2;
+  }
+  __syncthreads();
+  if (bad) {
+    if (tid == 0) {
+      atomicOr(err, kErrBadIndex);
+      for (int i = 0; i < 8; ++i) P.hdr[i] = 0;
+      P.item_gu[0] = 0;
+    }
+    return;
+  }
+  // active routed experts, ascending
+  int carry = 0, maxrows = 0;
+  for (uint32_t base = 0; base < E; base += kPlanThreads) {
+    const uint32_t e = base + tid;
+    const int rows = e < E ? off[e + 1] - off[e] : 0;
+    const int flag = rows > 0 ? 1 : 0;
+    scan[tid] = flag;
+    __syncthreads();
+    for (int o = 1; o < kPlanThreads; o <<= 1) {
+      const int add = tid >= o ? scan[tid - o] : 0;
+      __syncthreads();
+      scan[tid] += add;
+      __syncthreads();
+    }
+    if (flag) {
+      const int u = carry + scan[tid] - 1;
+      P.act_e[u] = (int)e;
+      P.act_row0[u] = off[e];
+      P.act_rows[u] = rows;
+      P.item_gu[u] = u * (int)f;
+    }
+    carry += scan[kPlanThreads - 1];
+    __syncthreads();
+  }
+  if (tid == 0) {
+    for (uint32_t e = 0; e < E; ++e) maxrows = max(maxrows, off[e + 1] - off[e]);
+    int U = carry;
+    int items = U * (int)f;
+    if (fs > 0 && T > 0) {
+      P.act_e[U] = (int)E;
+      P.act_row0[U] = (int)R;
+      P.act_rows[U] = (int)T;
+      P.item_gu[U] = items;
+      items += (int)fs;
+      U += 1;
+    }
+    P.item_gu[U] = items;
+    P.hdr[0] = U;
+    P.hdr[1] = items;
+    P.hdr[2] = U * (int)d;
+    P.hdr[3] = maxrows;
+    P.hdr[4] = 1;  // routing arrays validated: the combine may read pos[]
+  }
+}
+
+// Activation quantiser: one warp per 32-block.
+__global__ void __launch_bounds__(256)
+    k_quant(const float *__restrict__ x, uint32_t nblocks, int8_t *__restrict__ xq,
+            float *__restrict__ xs) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t b = blockIdx.x * 8 + threadIdx.x / 32;
+  if (b >= nblocks) return;
+  const float v = x[(size_t)b * 32 + lane];
+  float a = fabsf(v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const float sc = __fdiv_rn(a, 127.0f);
+  xq[(size_t)b * 32 + lane] = (int8_t)quant_one(v, sc);
+  if (lane == 0) xs[b] = sc;
+}
+
+}  // namespace
+
+cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, int32_t *idx,
+                         float *w) {
+  if (c.T == 0) return cudaSuccess;
+  const unsigned grid = (c.T + kRouteWarps - 1) / kRouteWarps;
+  k_route<<<grid, kRouteWarps * 32, 0, c.stream>>>(logits, bias, c.T, c.desc.n_expert,
+                                                   c.desc.top_k, c.desc.s, idx, w);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32_t *perm,
+                           int32_t *pos, uint32_t *err) {
+  const uint32_t E = c.desc.n_expert;
+  const size_t smem = sizeof(int) * ((size_t)kPermWarps * E + E + kPermThreads);
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  k_permute<<<1, kPermThreads, smem, c.stream>>>(idx, c.T, E, c.desc.top_k, off, perm, pos, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
+                             const int32_t *perm, const int32_t *pos, uint32_t *err) {
+  int *plan = (int *)(c.ws + c.L.plan);
+  k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, c.desc.n_expert,
+                                           c.desc.top_k, c.desc.f, c.desc.f_shared, c.desc.d,
+                                           plan, err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quant_x(const Ctx &c, const float *x) {
+  const uint32_t nblocks = c.T * (c.desc.d / 32);
+  if (nblocks == 0) return cudaSuccess;
+  k_quant<<<(nblocks + 7) / 8, 256, 0, c.stream>>>(x, nblocks, (int8_t *)(c.ws + c.L.xq),
+                                                    (float *)(c.ws + c.L.xs));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,318 @@
+"""Python binding of ``libmoe.so`` (C ABI in ``include/moe.h``).
+
+Argument marshalling only: every step of the layer runs in the library's CUDA
+kernels.  PyTorch provides device memory and the current stream.  There is no
+CPU fallback: if the library is missing or the tensors are not on a CUDA
+device, the call raises.
+
+Entry points mirror the C names: ``workspace_size``, ``workspace_layout``,
+``route``, ``ffn``, ``layer``, ``check_device_error``, ``status_string``.
+``Layer`` bundles one layer's weights, descriptor and workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_OK = 0
+STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
+                3: "MOE_ERR_WORKSPACE", 4: "MOE_ERR_CUDA", 5: "MOE_ERR_TIMEOUT",
+                6: "MOE_ERR_DEVICE_CHECK"}
+FMT_Q8_0 = 0
+FMT_Q2S = 1
+FLAG_DEBUG_TAPS = 0x1
+FLAG_FORCE_GEMV = 0x2
+FLAG_FORCE_TC = 0x4
+
+_vp = ctypes.c_void_p
+_sz = ctypes.c_size_t
+_u32 = ctypes.c_uint32
+
+
+class MoeMat(ctypes.Structure):
+    _fields_ = [("q", _vp), ("scale", _vp)]
+
+
+class MoeDesc(ctypes.Structure):
+    _fields_ = [("n_expert", _u32), ("top_k", _u32), ("d", _u32), ("f", _u32),
+                ("f_shared", _u32), ("routed_fmt", ctypes.c_int32), ("s", ctypes.c_float),
+                ("flags", _u32)]
+
+
+class MoeWeights(ctypes.Structure):
+    _fields_ = [(n, MoeMat) for n in ("gate", "up", "down", "s_gate", "s_up", "s_down")]
+
+
+LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
+                 "tap_gu", "tap_dn", "err", "total")
+
+
+class MoeWsLayout(ctypes.Structure):
+    _fields_ = [(n, _sz) for n in LAYOUT_FIELDS] + [("n_tap", _u32)]
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} "
+                         f"({status_string(status) if _lib else ''})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so; raise (never fall back) if it is absent."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        L.moe_workspace_size.restype = _sz
+        L.moe_workspace_size.argtypes = [ctypes.POINTER(MoeDesc), _u32]
+        L.moe_workspace_layout.restype = ctypes.c_int
+        L.moe_workspace_layout.argtypes = [ctypes.POINTER(MoeDesc), _u32,
+                                           ctypes.POINTER(MoeWsLayout)]
+        L.moe_route.restype = ctypes.c_int
+        L.moe_route.argtypes = [ctypes.POINTER(MoeDesc), _vp, _vp, _u32, _vp, _vp, _vp, _vp, _vp,
+                                _vp, _sz, _vp]
+        L.moe_ffn.restype = ctypes.c_int
+        L.moe_ffn.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp, _u32,
+                              _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]
+        L.moe_layer.restype = ctypes.c_int
+        L.moe_layer.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp, _vp,
+                                _vp, _u32, _vp, _vp, _sz, _vp]
+        L.moe_layer_timed.restype = ctypes.c_int
+        L.moe_layer_timed.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
+                                      _vp, _vp, _u32, _vp, _vp, _sz, _vp,
+                                      ctypes.POINTER(_vp), _u32]
+        L.moe_stage_name.restype = ctypes.c_char_p
+        L.moe_stage_name.argtypes = [_u32]
+        L.moe_check_device_error.restype = ctypes.c_int
+        L.moe_check_device_error.argtypes = [_vp, _sz, _vp]
+        L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_status_string.argtypes = [ctypes.c_int]
+        _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().moe_status_string(int(status)).decode()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dev_ptr(t: Optional[torch.Tensor], dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def make_desc(n_expert, top_k, d, f, f_shared, routed_fmt, s, flags=0) -> MoeDesc:
+    return MoeDesc(n_expert, top_k, d, f, f_shared, routed_fmt, float(s), flags)
+
+
+def workspace_size(desc: MoeDesc, T: int) -> int:
+    return int(lib().moe_workspace_size(ctypes.byref(desc), T))
+
+
+def workspace_layout(desc: MoeDesc, T: int) -> MoeWsLayout:
+    out = MoeWsLayout()
+    _check("moe_workspace_layout", lib().moe_workspace_layout(ctypes.byref(desc), T,
+                                                              ctypes.byref(out)))
+    return out
+
+
+def route(desc: MoeDesc, logits, bias, idx, w, off, perm, pos, stream=None):
+    T = logits.shape[0] if logits is not None else 0
+    st = lib().moe_route(ctypes.byref(desc), _dev_ptr(logits, torch.float32, "logits"),
+                         _dev_ptr(bias, torch.float32, "bias"), T,
+                         _dev_ptr(idx, torch.int32, "idx"), _dev_ptr(w, torch.float32, "w"),
+                         _dev_ptr(off, torch.int32, "off"), _dev_ptr(perm, torch.int32, "perm"),
+                         _dev_ptr(pos, torch.int32, "pos"), None, 0, _stream(stream))
+    _check("moe_route", st)
+
+
+def ffn(desc: MoeDesc, weights: MoeWeights, x, idx, w, off, perm, pos, y, ws, stream=None):
+    st = lib().moe_ffn(ctypes.byref(desc), ctypes.byref(weights),
+                       _dev_ptr(x, torch.float32, "x"), x.shape[0],
+                       _dev_ptr(idx, torch.int32, "idx"), _dev_ptr(w, torch.float32, "w"),
+                       _dev_ptr(off, torch.int32, "off"), _dev_ptr(perm, torch.int32, "perm"),
+                       _dev_ptr(pos, torch.int32, "pos"), _dev_ptr(y, torch.float32, "y"),
+                       _dev_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check("moe_ffn", st)
+
+
+def layer(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, stream=None):
+    st = lib().moe_layer(ctypes.byref(desc), ctypes.byref(weights),
+                         _dev_ptr(x, torch.float32, "x"), _dev_ptr(logits, torch.float32, "logits"),
+                         _dev_ptr(bias, torch.float32, "bias"), x.shape[0],
+                         _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
+                         ws.numel(), _stream(stream))
+    _check("moe_layer", st)
+
+
+def layer_timed(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, events,
+                stream=None):
+    """moe_layer with ``events`` (torch.cuda.Event list) recorded between stages:
+    events[0] before the first stage, events[i] after stage i-1."""
+    for ev in events:  # torch creates the CUDA event lazily, on its first record
+        if not ev.cuda_event:
+            ev.record()
+    handles = (_vp * len(events))(*[ev.cuda_event for ev in events])
+    st = lib().moe_layer_timed(ctypes.byref(desc), ctypes.byref(weights),
+                               _dev_ptr(x, torch.float32, "x"),
+                               _dev_ptr(logits, torch.float32, "logits"),
+                               _dev_ptr(bias, torch.float32, "bias"), x.shape[0],
+                               _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
+                               ws.numel(), _stream(stream), handles, len(events))
+    _check("moe_layer_timed", st)
+
+
+def stage_names() -> list:
+    names = []
+    while True:
+        n = lib().moe_stage_name(len(names))
+        if n is None:
+            return names
+        names.append(n.decode())
+
+
+def check_device_error(ws, stream=None) -> int:
+    """Returns the moe_status of the workspace's device error word (and clears it)."""
+    return int(lib().moe_check_device_error(_dev_ptr(ws, torch.uint8, "ws"), ws.numel(),
+                                            _stream(stream)))
+
+
+# ------------------------------------------------------------------ convenience
+@dataclass
+class LayerOutput:
+    y: torch.Tensor
+    idx: torch.Tensor
+    w: torch.Tensor
+    off: torch.Tensor
+    perm: torch.Tensor
+    pos: torch.Tensor
+    xq: torch.Tensor
+    xs: torch.Tensor
+    hq: torch.Tensor
+    hs: torch.Tensor
+    tap_gu: Optional[torch.Tensor]
+    tap_dn: Optional[torch.Tensor]
+
+
+class Layer:
+    """One routed-MoE layer resident on a device: weights, descriptor, workspace.
+
+    ``tensors`` holds the planar weights: ``gate_q`` [E,f,d] (int8, or uint8 2-bit
+    codes [E,f,d/4]), ``gate_s`` [E,f,d/32] fp16, likewise ``up_*``, ``down_q``
+    [E,d,f(/4)], ``down_s`` [E,d,f/32], and the shared expert as ``s_gate_q`` ...
+    """
+
+    def __init__(self, n_expert, top_k, d, f, f_shared, routed_fmt, s, tensors: dict,
+                 device=None):
+        self.n_expert, self.top_k, self.d, self.f = n_expert, top_k, d, f
+        self.f_shared, self.routed_fmt, self.s = f_shared, routed_fmt, float(s)
+        self.tensors = tensors
+        self.device = device or tensors["gate_q"].device
+        self.weights = MoeWeights()
+        names = ["gate", "up", "down"] + (["s_gate", "s_up", "s_down"] if f_shared else [])
+        for n in names:
+            q, sc = tensors[n + "_q"], tensors[n + "_s"]
+            setattr(self.weights, n, MoeMat(_dev_ptr(q, None, n + "_q"),
+                                           _dev_ptr(sc, torch.float16, n + "_s")))
+        self._ws = {}
+
+    @classmethod
+    def from_host(cls, spec, experts: dict, shared: Optional[dict], device):
+        """Stack per-expert host arrays (numpy, planar) into device tensors."""
+        import numpy as np
+
+        t = {}
+        for name in ("gate", "up", "down"):
+            q = np.stack([experts[e][name + "_q"] for e in range(spec.E)])
+            sc = np.stack([np.asarray(experts[e][name + "_s"]).view(np.float16)
+                           for e in range(spec.E)])
+            t[name + "_q"] = torch.from_numpy(q).to(device)
+            t[name + "_s"] = torch.from_numpy(sc).to(device)
+            if spec.f_shared:
+                t["s_" + name + "_q"] = torch.from_numpy(np.ascontiguousarray(
+                    shared[name + "_q"])).to(device)
+                t["s_" + name + "_s"] = torch.from_numpy(np.ascontiguousarray(
+                    np.asarray(shared[name + "_s"]).view(np.float16))).to(device)
+        return cls(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, t, device)
+
+    def desc(self, flags=0) -> MoeDesc:
+        return make_desc(self.n_expert, self.top_k, self.d, self.f, self.f_shared,
+                         self.routed_fmt, self.s, flags)
+
+    def workspace(self, T: int, flags=0) -> torch.Tensor:
+        key = (T, flags & FLAG_DEBUG_TAPS)
+        if key not in self._ws:
+            n = workspace_size(self.desc(flags), T)
+            self._ws[key] = torch.zeros(max(n, 256), dtype=torch.uint8, device=self.device)
+        return self._ws[key]
+
+    def views(self, ws: torch.Tensor, T: int, flags=0) -> dict:
+        """Typed views of the workspace regions (for taps and tests)."""
+        L = workspace_layout(self.desc(flags), T)
+        R = T * self.top_k
+        slots = R + (T if self.f_shared else 0)
+        fmax = max(self.f, self.f_shared)
+
+        def v(off, n, dtype, shape):
+            nbytes = n * torch.tensor([], dtype=dtype).element_size()
+            return ws[off:off + nbytes].view(dtype).view(shape)
+
+        out = dict(
+            idx=v(L.idx, R, torch.int32, (T, self.top_k)), w=v(L.w, R, torch.float32, (T, self.top_k)),
+            off=v(L.off, self.n_expert + 1, torch.int32, (self.n_expert + 1,)),
+            perm=v(L.perm, R, torch.int32, (R,)), pos=v(L.pos, R, torch.int32, (R,)),
+            xq=v(L.xq, T * self.d, torch.int8, (T, self.d)),
+            xs=v(L.xs, T * self.d // 32, torch.float32, (T, self.d // 32)),
+            hq=v(L.hq, slots * fmax, torch.int8, (slots, fmax)),
+            hs=v(L.hs, slots * fmax // 32, torch.float32, (slots, fmax // 32)),
+            tap_gu=None, tap_dn=None)
+        if flags & FLAG_DEBUG_TAPS:
+            nt = L.n_tap
+            out["tap_gu"] = v(L.tap_gu, slots * 2 * nt * (self.d // 32), torch.int32,
+                              (slots, 2, nt, self.d // 32))
+            out["tap_dn"] = v(L.tap_dn, slots * nt * (fmax // 32), torch.int32,
+                              (slots, nt, fmax // 32))
+        return out
+
+    def forward(self, x: torch.Tensor, logits: torch.Tensor, bias: torch.Tensor,
+                taps: bool = False, flags: int = 0, y: Optional[torch.Tensor] = None,
+                stream=None) -> LayerOutput:
+        flags = flags | (FLAG_DEBUG_TAPS if taps else 0)
+        T = x.shape[0]
+        ws = self.workspace(T, flags)
+        if y is None:
+            y = torch.empty((T, self.d), dtype=torch.float32, device=self.device)
+        layer(self.desc(flags), self.weights, x, logits, bias, y, ws, stream)
+        v = self.views(ws, T, flags)
+        return LayerOutput(y=y, **v)

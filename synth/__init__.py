@@ -146,6 +146,11 @@ GLM_LAYER = LayerSpec("e256_k8_d6144_f2048_q8", E=256, k=8, d=6144, f=2048, f_sh
 Q2_LAYER = LayerSpec("e192_k8_d4096_f1536_q2", E=192, k=8, d=4096, f=1536, f_shared=1536,
                      fmt=FMT_Q2S, s=1.0, zipf_beta=0.4)
 
+# Same per-token shapes as GLM_LAYER with 32 experts (1.3 GB of weights, 361 MB
+# read per token): the small case that profiler captures run on.
+GLM_LAYER_E32 = LayerSpec("e32_k8_d6144_f2048_q8", E=32, k=8, d=6144, f=2048, f_shared=2048,
+                          fmt=FMT_Q8_0, s=2.5, zipf_beta=0.4)
+
 # workloads: (layer, tokens per step, token seeds)
 WORKLOADS = {
     "tiny_t4": (TINY, 4, (0,)),
@@ -154,6 +159,8 @@ WORKLOADS = {
     "batch_t2": (GLM_LAYER, 2, (0,)),
     "prefill_t512": (GLM_LAYER, 512, (0,)),
     "q2_t64": (Q2_LAYER, 64, (0,)),
+    "profile_decode_t1": (GLM_LAYER_E32, 1, tuple(range(8))),
+    "profile_prefill_t512": (GLM_LAYER_E32, 512, (0,)),
 }
 
 

@@ -1,0 +1,188 @@
+"""CUDA path vs the CPU oracle, through the C ABI, on a GB300 (sm_103a)."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from parity import run_case, device_layer
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec(**kw):
+    base = dict(name="t", E=16, k=4, d=256, f=128, f_shared=0, fmt=0, s=1.0, zipf_beta=0.0)
+    base.update(kw)
+    return synth.LayerSpec(**base)
+
+
+# ---------------------------------------------------------------- small layers, all tokens
+SMALL = [
+    ("tiny_t4", synth.TINY, 4),
+    ("tiny_ragged_t37", synth.TINY, 37),
+    ("shared_e64", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 9),
+    ("e192_q2", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=1, zipf_beta=0.4), 13),
+    ("e384_k6", _spec(E=384, k=6, d=256, f=96, f_shared=64, s=1.5), 7),
+    ("e256_d6144", _spec(E=256, k=8, d=6144, f=64, f_shared=96, s=2.5, zipf_beta=0.4), 3),
+    ("k1_s1", _spec(E=16, k=1, d=256, f=128), 6),
+    ("k_eq_E", _spec(E=8, k=8, d=128, f=64, f_shared=32), 5),
+    ("e1024_k32", _spec(E=1024, k=32, d=128, f=32, f_shared=0), 3),
+    ("many_rows_per_expert", _spec(E=4, k=2, d=256, f=128, f_shared=64), 40),
+]
+
+
+@pytest.mark.parametrize("name,spec,T", SMALL, ids=[s[0] for s in SMALL])
+def test_small_layers(gpu, name, spec, T):
+    rep = run_case(spec, T, seed=11, device=gpu)
+    print(name, rep)
+
+
+def test_tie_logits_pick_lower_index(gpu):
+    """Equal logits and bias: every token must take experts 0..k-1 in order."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=32, k=4)
+    layer = device_layer(spec, gpu)
+    T = 3
+    logits = torch.zeros((T, 32), dtype=torch.float32, device=gpu)
+    bias = torch.zeros(32, dtype=torch.float32, device=gpu)
+    x = torch.ones((T, spec.d), dtype=torch.float32, device=gpu)
+    out = layer.forward(x, logits, bias)
+    torch.cuda.synchronize()
+    assert out.idx.cpu().tolist() == [[0, 1, 2, 3]] * T
+    assert np.allclose(out.w.cpu().numpy(), 0.25)
+
+
+def test_zero_tokens(gpu):
+    spec = synth.TINY
+    layer = device_layer(spec, gpu)
+    x = torch.empty((0, spec.d), dtype=torch.float32, device=gpu)
+    lg = torch.empty((0, spec.E), dtype=torch.float32, device=gpu)
+    out = layer.forward(x, lg, torch.zeros(spec.E, device=gpu))
+    torch.cuda.synchronize()
+    assert out.y.shape == (0, spec.d)
+    assert out.off.cpu().tolist() == [0] * (spec.E + 1)
+
+
+def test_zero_activation_block(gpu):
+    """An all-zero 32-block quantises to scale 0 and codes 0 (no division by zero)."""
+    spec = synth.TINY
+    layer = device_layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 3, 2)
+    x[:, 32:96] = 0.0
+    out = layer.forward(torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
+                        torch.from_numpy(synth.bias(spec)).to(gpu))
+    torch.cuda.synchronize()
+    assert (out.xs.cpu().numpy()[:, 1:3] == 0).all()
+    assert (out.xq.cpu().numpy()[:, 32:96] == 0).all()
+    assert np.isfinite(out.y.cpu().numpy()).all()
+
+
+def test_deterministic_across_runs(gpu):
+    spec = _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 5, 21)
+    args = [torch.from_numpy(a).to(gpu) for a in (x, logits, synth.bias(spec))]
+    y1 = layer.forward(*args).y.clone()
+    y2 = layer.forward(*args).y.clone()
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_ffn_entry_matches_layer(gpu):
+    """moe_route + moe_ffn on caller buffers equals moe_layer."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    T = 10
+    logits, x = synth.token_inputs(spec, 8, T)
+    x_d, l_d = torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu)
+    b_d = torch.from_numpy(synth.bias(spec)).to(gpu)
+    ref = layer.forward(x_d, l_d, b_d).y.clone()
+    idx = torch.empty((T, spec.k), dtype=torch.int32, device=gpu)
+    w = torch.empty((T, spec.k), dtype=torch.float32, device=gpu)
+    off = torch.empty(spec.E + 1, dtype=torch.int32, device=gpu)
+    perm = torch.empty(T * spec.k, dtype=torch.int32, device=gpu)
+    pos = torch.empty(T * spec.k, dtype=torch.int32, device=gpu)
+    desc = layer.desc()
+    moe.route(desc, l_d, b_d, idx, w, off, perm, pos)
+    y = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
+    ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
+    moe.ffn(desc, layer.weights, x_d, idx, w, off, perm, pos, y, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y, ref)
+    assert moe.check_device_error(ws) == 0
+
+
+def test_ffn_rejects_inconsistent_routing_on_device(gpu):
+    """Corrupted off/perm/idx are caught by the device-side check: the call
+    reports MOE_ERR_DEVICE_CHECK, runs no expert and leaves y at zero."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=16, k=4, d=256, f=128)
+    layer = device_layer(spec, gpu)
+    T = 4
+    logits, x = synth.token_inputs(spec, 9, T)
+    x_d, l_d = torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu)
+    b_d = torch.from_numpy(synth.bias(spec)).to(gpu)
+    idx = torch.empty((T, spec.k), dtype=torch.int32, device=gpu)
+    w = torch.empty((T, spec.k), dtype=torch.float32, device=gpu)
+    off = torch.empty(spec.E + 1, dtype=torch.int32, device=gpu)
+    perm = torch.empty(T * spec.k, dtype=torch.int32, device=gpu)
+    pos = torch.empty(T * spec.k, dtype=torch.int32, device=gpu)
+    desc = layer.desc()
+    moe.route(desc, l_d, b_d, idx, w, off, perm, pos)
+    ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
+    y = torch.full((T, spec.d), 7.0, dtype=torch.float32, device=gpu)
+    for corrupt in ("off", "perm", "idx"):
+        o2, p2, i2 = off.clone(), perm.clone(), idx.clone()
+        if corrupt == "off":
+            o2[3] += 100
+        elif corrupt == "perm":
+            p2[0] = 10 ** 6
+        else:
+            i2[0, 0] = spec.E + 5
+        moe.ffn(desc, layer.weights, x_d, i2, w, o2, p2, pos, y, ws)
+        assert moe.check_device_error(ws) == 6, corrupt
+        assert (y == 0).all()
+    moe.ffn(desc, layer.weights, x_d, idx, w, off, perm, pos, y, ws)
+    assert moe.check_device_error(ws) == 0
+
+
+def test_device_fill_matches_host_generator(gpu):
+    spec = synth.GLM_LAYER
+    small = synth.LayerSpec("fillcheck", E=3, k=1, d=spec.d, f=256, f_shared=128, fmt=0, s=1.0,
+                            zipf_beta=0.0)
+    for sp in (small, synth.LayerSpec("fill2", E=2, k=1, d=512, f=96, f_shared=64, fmt=1, s=1.0,
+                                      zipf_beta=0.0)):
+        t = synth.fill_layer_device(sp, gpu)
+        for e in range(sp.E):
+            h = synth.expert_host(sp, e)
+            for name in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+                dev = t[name][e].cpu().numpy()
+                assert np.array_equal(dev.view(np.uint8), np.asarray(h[name]).view(np.uint8)), name
+        hs = synth.expert_host(sp, sp.E)
+        for name in ("gate_q", "gate_s", "down_q", "down_s"):
+            dev = t["s_" + name].cpu().numpy()
+            assert np.array_equal(dev.view(np.uint8), np.asarray(hs[name]).view(np.uint8))
+
+
+# ---------------------------------------------------------------- full-size layers, sampled
+def test_decode_t1_full_size(gpu):
+    for seed in (0, 1, 2):
+        rep = run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu)
+        print("decode_t1", seed, rep)
+
+
+def test_small_batch_t2_t16_full_size(gpu):
+    print("batch_t2", run_case(synth.GLM_LAYER, 2, seed=0, device=gpu))
+    print("batch_t16", run_case(synth.GLM_LAYER, 16, seed=0, device=gpu, sample=[0, 7, 15]))
+
+
+def test_prefill_t512_full_size(gpu):
+    print("prefill_t512", run_case(synth.GLM_LAYER, 512, seed=0, device=gpu,
+                                   sample=[0, 255, 511]))
+
+
+def test_q2_t64_full_size(gpu):
+    print("q2_t64", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 33, 63]))
