@@ -168,6 +168,10 @@ moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream);
 
 const char *moe_status_string(moe_status st);
 
+/* Name of the CUDA error behind the calling thread's last MOE_ERR_CUDA
+ * ("no error" if there was none).  Static storage; do not free. */
+const char *moe_last_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -85,7 +85,13 @@ int sm_count_of_current_device() {
   return n > 0 ? n : kSmCount;
 }
 
-moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+thread_local const char *t_last_error = "no error";
+
+moe_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  t_last_error = cudaGetErrorName(e);
+  return MOE_ERR_CUDA;
+}
 
 Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void *stream) {
   Ctx c;
@@ -111,10 +117,17 @@ struct Marks {
   void *const *ev;
   uint32_t n;
   cudaStream_t s;
+  bool capturing;
+  Marks(void *const *e, uint32_t k, cudaStream_t st) : ev(e), n(k), s(st), capturing(false) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (ev && n && cudaStreamIsCapturing(s, &cs) == cudaSuccess)
+      capturing = cs == cudaStreamCaptureStatusActive;
+  }
   cudaError_t mark(uint32_t i) const {
-    // external records also become event nodes when the stream is being captured
-    if (ev && i < n) return cudaEventRecordWithFlags((cudaEvent_t)ev[i], s, cudaEventRecordExternal);
-    return cudaSuccess;
+    if (!ev || i >= n) return cudaSuccess;
+    // inside stream capture an external record becomes an event-record node
+    return capturing ? cudaEventRecordWithFlags((cudaEvent_t)ev[i], s, cudaEventRecordExternal)
+                     : cudaEventRecord((cudaEvent_t)ev[i], s);
   }
 };
 
@@ -148,7 +161,7 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
   Ctx c = make_ctx(desc, wts, T, ws, stream);
-  Marks mk{events, n_events, c.stream};
+  Marks mk(events, n_events, c.stream);
   int32_t *idx = (int32_t *)(c.ws + c.L.idx);
   float *w = (float *)(c.ws + c.L.w);
   int32_t *off = (int32_t *)(c.ws + c.L.off);
@@ -209,7 +222,7 @@ moe_status moe_ffn(const moe_desc *desc, const moe_weights *wts, const float *x,
   if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
   Ctx c = make_ctx(desc, wts, T, ws, stream);
-  return run_ffn(c, x, idx, w, off, perm, pos, y, Marks{nullptr, 0, c.stream});
+  return run_ffn(c, x, idx, w, off, perm, pos, y, Marks(nullptr, 0, c.stream));
 }
 
 moe_status moe_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
@@ -226,6 +239,8 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
 }
 
 const char *moe_stage_name(uint32_t i) { return i < kNumStages ? kStageNames[i] : nullptr; }
+
+const char *moe_last_error(void) { return t_last_error; }
 
 moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream) {
   if (!ws || ws_bytes < sizeof(uint32_t)) return MOE_ERR_INVALID_ARG;

@@ -60,8 +60,10 @@ class MoeWsLayout(ctypes.Structure):
 
 class MoeError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} "
-                         f"({status_string(status) if _lib else ''})")
+        detail = status_string(status) if _lib else ""
+        if status == 4 and _lib:
+            detail += ": " + _lib.moe_last_error().decode()
+        super().__init__(f"{fn}: {STATUS_NAMES.get(status, status)} ({detail})")
         self.status = status
 
 
@@ -97,6 +99,8 @@ def lib():
         L.moe_stage_name.argtypes = [_u32]
         L.moe_check_device_error.restype = ctypes.c_int
         L.moe_check_device_error.argtypes = [_vp, _sz, _vp]
+        L.moe_last_error.restype = ctypes.c_char_p
+        L.moe_last_error.argtypes = []
         L.moe_status_string.restype = ctypes.c_char_p
         L.moe_status_string.argtypes = [ctypes.c_int]
         _lib = L
