@@ -161,6 +161,28 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
 /* Name of stage i of moe_layer ("route", "permute", ...), NULL past the last. */
 const char *moe_stage_name(uint32_t i);
 
+/* ---- Allocation-free variant (the pages have no counterpart of this) ----
+ * moe_layer without a workspace argument, for callers that cannot allocate
+ * device memory: code running inside an engine whose device-memory arena was
+ * reserved up front, plugins and plain-C hosts without an allocator, and
+ * latency-critical paths that must not touch the allocator.  The scratch the
+ * layer needs lives in one static device array of MOE_NOALLOC_SCRATCH_BYTES,
+ * held by every GPU that loads the library until the process exits.
+ * - Calls whose moe_workspace_size(desc, T) exceeds it return
+ *   MOE_ERR_WORKSPACE (moe_last_error says why) and launch nothing.  For the
+ *   E=256 / d=6144 / f=2048 layer with a shared expert that is T <= 48.
+ * - All calls on a device share the array, which keeps the last call's
+ *   contents; each call resets what must start at zero (the error word).
+ *   Calls that overlap on the GPU race on the array: serialise them.
+ * - The first call on each device looks up the array's device address and
+ *   caches it; make that first call before any stream capture begins.
+ * - Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
+ * Inputs and outputs are the caller's device buffers, as for moe_layer. */
+#define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+moe_status moe_layer_noalloc(const moe_desc *desc, const moe_weights *wts, const float *x,
+                             const float *logits, const float *bias, uint32_t T, float *y,
+                             void *stream);
+
 /* Synchronise `stream` and read (then clear) the workspace's device error word
  * (the first 4 bytes of any workspace).
  * MOE_OK if no kernel flagged a fault; MOE_ERR_DEVICE_CHECK otherwise. */

@@ -178,6 +178,16 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
 }
 
 }  // namespace
+
+// Entry points for other translation units of the library.
+moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, const float *x,
+                              const float *logits, const float *bias, uint32_t T, float *y,
+                              void *ws, size_t ws_bytes, void *stream) {
+  return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0);
+}
+
+void set_last_error(const char *msg) { t_last_error = msg; }
+
 }  // namespace moe
 
 using namespace moe;

@@ -183,4 +183,9 @@ cudaError_t launch_requant_h(const Ctx &c);
 cudaError_t launch_down(const Ctx &c);
 cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, float *y);
 
+moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, const float *x,
+                              const float *logits, const float *bias, uint32_t T, float *y,
+                              void *ws, size_t ws_bytes, void *stream);
+void set_last_error(const char *msg);
+
 }  // namespace moe

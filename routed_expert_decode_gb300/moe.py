@@ -97,6 +97,9 @@ def lib():
                                       ctypes.POINTER(_vp), _u32]
         L.moe_stage_name.restype = ctypes.c_char_p
         L.moe_stage_name.argtypes = [_u32]
+        L.moe_layer_noalloc.restype = ctypes.c_int
+        L.moe_layer_noalloc.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
+                                        _vp, _vp, _u32, _vp, _vp]
         L.moe_check_device_error.restype = ctypes.c_int
         L.moe_check_device_error.argtypes = [_vp, _sz, _vp]
         L.moe_last_error.restype = ctypes.c_char_p
@@ -195,6 +198,21 @@ def layer_timed(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, even
                                _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
                                ws.numel(), _stream(stream), handles, len(events))
     _check("moe_layer_timed", st)
+
+
+def layer_noalloc(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, stream=None):
+    """moe_layer_noalloc: the layer without a workspace, for callers that cannot
+    allocate device memory; scratch comes from the library's fixed 16 MiB device
+    array (calls on one device must not overlap)."""
+    st = lib().moe_layer_noalloc(ctypes.byref(desc), ctypes.byref(weights),
+                                 _dev_ptr(x, torch.float32, "x"),
+                                 _dev_ptr(logits, torch.float32, "logits"),
+                                 _dev_ptr(bias, torch.float32, "bias"), x.shape[0],
+                                 _dev_ptr(y, torch.float32, "y"), _stream(stream))
+    _check("moe_layer_noalloc", st)
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 def stage_names() -> list:
