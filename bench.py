@@ -86,7 +86,7 @@ def stage_bytes(spec, U_routed: int):
     if spec.f_shared:
         gu += 2 * spec.f_shared * row_bytes(0, spec.d)
         dn += spec.d * row_bytes(0, spec.f_shared)
-    return {"gateup": gu, "down": dn, "total": gu + dn}
+    return {"gateup": gu, "down": dn, "total": gu + dn, "decode_fused": gu + dn}
 
 
 # ------------------------------------------------------------------ clocks
@@ -217,7 +217,8 @@ def run_ours(args):
         moe.route(desc, dev_in[s][1], bias, idx, wts, off, perm, pos)
         U_of[s] = int((off[1:] - off[:-1] > 0).sum().item())
 
-    names = moe.stage_names()
+    names = moe.stage_names(desc, T)
+    path = moe.layer_path(desc, T)
     nst = len(names)
     step_seed = [seeds[i % len(seeds)] for i in range(K)]
     stage_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nst + 1)] for _ in range(K)]
@@ -290,7 +291,8 @@ def run_ours(args):
     mean_stage = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(mean_stage, key=mean_stage.get)
     dom_bytes = sum(b.get(dom, 0) for b in bytes_steps) / K
-    achieved = dom_bytes / (mean_stage[dom] / 1e3) / 1e9 if dom in ("gateup", "down") else None
+    achieved = (dom_bytes / (mean_stage[dom] / 1e3) / 1e9
+                if dom in ("gateup", "down", "decode_fused") else None)
     layer_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
 
     # end-to-end through the C ABI with host buffers: H2D inputs, layer, D2H output
@@ -374,7 +376,8 @@ def run_ours(args):
                      "peak_source": peak_src,
                      "algorithmic_bytes_per_launch": round(dom_bytes),
                      "traffic": traffic_for(dom, args.workload)},
-        "gpu_launches": K * nst,
+        "gpu_launches": K * (1 if path == "fused_decode" else nst),
+        "path": path,
         "clocks": clk,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -401,7 +404,7 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
         logits, x = synth.token_inputs(spec, seeds[0], T)
         x_d, l_d = torch.from_numpy(x).to(dev), torch.from_numpy(logits).to(dev)
         y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
-        names = moe.stage_names()
+        names = moe.stage_names(desc, T)
         n = 10
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
                for _ in range(n)]

@@ -85,6 +85,10 @@ typedef struct {
 #define MOE_FLAG_DEBUG_TAPS 0x1u /* write sampled int32 block dots into the workspace */
 #define MOE_FLAG_FORCE_GEMV 0x2u /* every expert on the dp4a path (no tensor-core path) */
 #define MOE_FLAG_FORCE_TC 0x4u   /* every routed expert with >= 1 row on the tensor path */
+/* Failure-detection test only: the fused decode kernel never publishes its
+ * routing result, so its bounded waits run out (~10 ms) and the call's error
+ * word reports MOE_ERR_TIMEOUT; nothing faults and the context stays usable. */
+#define MOE_FLAG_TEST_STALL 0x8u
 
 typedef struct {
   uint32_t n_expert; /* E, 1..1024 */
@@ -114,6 +118,7 @@ typedef struct {
   size_t hq, hs;                 /* int8 [R+T][fmax], fp32 [R+T][fmax/32] */
   size_t h, o;                   /* fp32 [R+T][fmax], fp32 [R+T][d] */
   size_t plan;                   /* internal work list */
+  size_t sync;                   /* counters of the fused decode kernel */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
@@ -158,8 +163,13 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
                            void *ws, size_t ws_bytes, void *stream, void *const *events,
                            uint32_t n_events);
 
-/* Name of stage i of moe_layer ("route", "permute", ...), NULL past the last. */
-const char *moe_stage_name(uint32_t i);
+/* Which implementation moe_layer uses for (desc, T) on the current device:
+ * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */
+const char *moe_layer_path(const moe_desc *desc, uint32_t T);
+
+/* Name of stage i of that path (what moe_layer_timed's events bracket),
+ * NULL past the last stage. */
+const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i);
 
 /* ---- Allocation-free variant (the pages have no counterpart of this) ----
  * moe_layer without a workspace argument, for callers that cannot allocate

@@ -61,6 +61,7 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
   L.perm = p; p = align_up(p + R * 4);
   L.pos = p; p = align_up(p + R * 4);
   L.plan = p; p = align_up(p + PlanView::ints(d->n_expert) * 4);
+  L.sync = p; p = align_up(p + fused_sync_ints(d) * 4);
   L.xq = p; p = align_up(p + (size_t)T * d->d);
   L.xs = p; p = align_up(p + (size_t)T * (d->d / 32) * 4);
   L.h = p; p = align_up(p + slots * fmax * 4);
@@ -111,6 +112,8 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
 const char *const kStageNames[] = {"route", "permute", "plan",  "quant_x",
                                    "gateup", "requant", "down", "combine"};
 constexpr uint32_t kNumStages = sizeof(kStageNames) / sizeof(kStageNames[0]);
+const char *const kFusedStageNames[] = {"zero_sync", "decode_fused"};
+constexpr uint32_t kNumFusedStages = 2;
 
 // optional timing markers: events[i] after stage i-1
 struct Marks {
@@ -169,6 +172,14 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   int32_t *pos = (int32_t *)(c.ws + c.L.pos);
   uint32_t *err = (uint32_t *)(c.ws + c.L.err);
   cudaError_t e;
+  if (T > 0 && fused_eligible(c)) {
+    if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
+    if ((e = zero_decode_fused(c)) != cudaSuccess) return from_cuda(e);
+    if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_decode_fused(c, x, logits, bias, y)) != cudaSuccess) return from_cuda(e);
+    if ((e = mk.mark(2)) != cudaSuccess) return from_cuda(e);
+    return MOE_OK;
+  }
   if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_route(c, logits, bias, idx, w)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
@@ -248,7 +259,18 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
   return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, events, n_events);
 }
 
-const char *moe_stage_name(uint32_t i) { return i < kNumStages ? kStageNames[i] : nullptr; }
+const char *moe_layer_path(const moe_desc *desc, uint32_t T) {
+  if (!desc_ok(desc)) return nullptr;
+  Ctx c = make_ctx(desc, nullptr, T, nullptr, nullptr);
+  return (T > 0 && fused_eligible(c)) ? "fused_decode" : "multi_kernel";
+}
+
+const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i) {
+  const char *path = moe_layer_path(desc, T);
+  if (!path) return nullptr;
+  if (path[0] == 'f') return i < kNumFusedStages ? kFusedStageNames[i] : nullptr;
+  return i < kNumStages ? kStageNames[i] : nullptr;
+}
 
 const char *moe_last_error(void) { return t_last_error; }
 

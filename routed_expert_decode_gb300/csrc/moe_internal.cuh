@@ -183,6 +183,13 @@ cudaError_t launch_requant_h(const Ctx &c);
 cudaError_t launch_down(const Ctx &c);
 cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, float *y);
 
+// fused single-kernel decode (T <= 2): decode_fused.cu
+size_t fused_sync_ints(const moe_desc *d);
+bool fused_eligible(const Ctx &c);
+cudaError_t zero_decode_fused(const Ctx &c);
+cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logits,
+                                const float *bias, float *y);
+
 moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, const float *x,
                               const float *logits, const float *bias, uint32_t T, float *y,
                               void *ws, size_t ws_bytes, void *stream);

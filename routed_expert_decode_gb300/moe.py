@@ -30,6 +30,7 @@ FMT_Q2S = 1
 FLAG_DEBUG_TAPS = 0x1
 FLAG_FORCE_GEMV = 0x2
 FLAG_FORCE_TC = 0x4
+FLAG_TEST_STALL = 0x8
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -51,7 +52,7 @@ class MoeWeights(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "tap_gu", "tap_dn", "err", "total")
+                 "sync", "tap_gu", "tap_dn", "err", "total")
 
 
 class MoeWsLayout(ctypes.Structure):
@@ -95,8 +96,10 @@ def lib():
         L.moe_layer_timed.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
                                       _vp, _vp, _u32, _vp, _vp, _sz, _vp,
                                       ctypes.POINTER(_vp), _u32]
-        L.moe_stage_name.restype = ctypes.c_char_p
-        L.moe_stage_name.argtypes = [_u32]
+        L.moe_layer_path.restype = ctypes.c_char_p
+        L.moe_layer_path.argtypes = [ctypes.POINTER(MoeDesc), _u32]
+        L.moe_layer_stage_name.restype = ctypes.c_char_p
+        L.moe_layer_stage_name.argtypes = [ctypes.POINTER(MoeDesc), _u32, _u32]
         L.moe_layer_noalloc.restype = ctypes.c_int
         L.moe_layer_noalloc.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
                                         _vp, _vp, _u32, _vp, _vp]
@@ -215,10 +218,14 @@ def layer_noalloc(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, stream
 NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
-def stage_names() -> list:
+def layer_path(desc: MoeDesc, T: int) -> str:
+    return lib().moe_layer_path(ctypes.byref(desc), T).decode()
+
+
+def stage_names(desc: MoeDesc, T: int) -> list:
     names = []
     while True:
-        n = lib().moe_stage_name(len(names))
+        n = lib().moe_layer_stage_name(ctypes.byref(desc), T, len(names))
         if n is None:
             return names
         names.append(n.decode())

@@ -186,3 +186,87 @@ def test_prefill_t512_full_size(gpu):
 
 def test_q2_t64_full_size(gpu):
     print("q2_t64", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 33, 63]))
+
+
+# ---------------------------------------------------------------- fused decode kernel (T <= 2)
+FUSED = [
+    ("fused_e64_t1", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 1),
+    ("fused_e64_t2", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 2),
+    ("fused_noshared_t2", _spec(E=32, k=8, d=768, f=512, f_shared=0), 2),
+    ("fused_wide_shared_t1", _spec(E=384, k=6, d=1024, f=256, f_shared=512, s=1.5), 1),
+    ("fused_k32_t2", _spec(E=1024, k=32, d=256, f=256, f_shared=256), 2),
+]
+
+
+@pytest.mark.parametrize("name,spec,T", FUSED, ids=[s[0] for s in FUSED])
+def test_fused_small_layers(gpu, name, spec, T):
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(spec, gpu)
+    assert moe.layer_path(layer.desc(), T) == "fused_decode"
+    for seed in (3, 4):
+        rep = run_case(spec, T, seed=seed, device=gpu, check_taps=False)
+        print(name, seed, rep)
+
+
+def test_fused_decode_full_size(gpu):
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(synth.GLM_LAYER, gpu)
+    assert moe.layer_path(layer.desc(), 1) == "fused_decode"
+    assert moe.layer_path(layer.desc(), 2) == "fused_decode"
+    assert moe.layer_path(layer.desc(), 3) == "multi_kernel"
+    for seed in (0, 1, 2, 3):
+        print("fused t1", seed, run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu,
+                                         check_taps=False))
+    for seed in (0, 1):
+        print("fused t2", seed, run_case(synth.GLM_LAYER, 2, seed=seed, device=gpu,
+                                         check_taps=False))
+
+
+def test_fused_matches_multi_kernel_and_repeats(gpu):
+    """The fused kernel and the multi-kernel path agree (same routing, same
+    int8 codes, y within fp32 summation order), and the fused kernel is
+    bit-identical from call to call."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = synth.GLM_LAYER
+    layer = device_layer(spec, gpu)
+    bias = torch.from_numpy(synth.bias(spec)).to(gpu)
+    for T in (1, 2):
+        logits, x = synth.token_inputs(spec, 40 + T, T)
+        args = [torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu), bias]
+        a = layer.forward(*args)
+        ya, ia, xa = a.y.clone(), a.idx.clone(), a.xq.clone()
+        b = layer.forward(*args)
+        assert torch.equal(b.y, ya)
+        m = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV)
+        torch.cuda.synchronize()
+        assert torch.equal(m.idx, ia) and torch.equal(m.xq, xa)
+        ym, yf = m.y.cpu().numpy(), ya.cpu().numpy()
+        err = np.abs(ym - yf).max(axis=1) / np.abs(ym).max(axis=1)
+        assert err.max() < 1e-4, err
+
+
+def test_fused_wait_timeout_is_reported(gpu):
+    """Failure detection without a GPU fault: with MOE_FLAG_TEST_STALL the router
+    never publishes its result, every bounded wait runs out (~10 ms), the call
+    reports MOE_ERR_TIMEOUT through the error word, and the next call works."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 5, 1)
+    args = [torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
+            torch.from_numpy(synth.bias(spec)).to(gpu)]
+    desc = layer.desc(moe.FLAG_TEST_STALL)
+    assert moe.layer_path(desc, 1) == "fused_decode"
+    ws = torch.zeros(moe.workspace_size(desc, 1), dtype=torch.uint8, device=gpu)
+    y = torch.empty((1, spec.d), dtype=torch.float32, device=gpu)
+    moe.layer(desc, layer.weights, args[0], args[1], args[2], y, ws)
+    assert moe.check_device_error(ws) == 5  # MOE_ERR_TIMEOUT
+    moe.layer(layer.desc(), layer.weights, args[0], args[1], args[2], y, ws)
+    assert moe.check_device_error(ws) == 0
+    ref = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV).y
+    torch.cuda.synchronize()
+    assert torch.allclose(y, ref, rtol=1e-4, atol=1e-6 * float(ref.abs().max()))
