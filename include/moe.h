@@ -89,6 +89,9 @@ typedef struct {
  * routing result, so its bounded waits run out (~10 ms) and the call's error
  * word reports MOE_ERR_TIMEOUT; nothing faults and the context stays usable. */
 #define MOE_FLAG_TEST_STALL 0x8u
+/* Tracing: the fused decode kernel writes 20 uint64 per CTA (timestamps and
+ * cycle counts of its waits and phases) into the workspace's trace region. */
+#define MOE_FLAG_TRACE 0x10u
 
 typedef struct {
   uint32_t n_expert; /* E, 1..1024 */
@@ -109,6 +112,14 @@ typedef struct {
   moe_mat s_gate, s_up, s_down;
 } moe_weights;
 
+/* The first MOE_WS_FIXED_BYTES of every workspace have a fixed layout: the
+ * device error word at offset 0 and, from offset 256, MOE_SYNC_BYTES of
+ * counters used by the fused decode kernel.  A workspace must be zero-filled
+ * once after it is allocated; every call leaves the counters zeroed again, so
+ * one workspace can serve calls of any desc and T. */
+#define MOE_SYNC_BYTES ((size_t)16384)
+#define MOE_WS_FIXED_BYTES ((size_t)256 + MOE_SYNC_BYTES)
+
 /* Regions of the workspace (byte offsets), for debug taps and tests.
  * Rows of the expert FFN are "slots": routed rows at p = pos[t*k+j] in [0, R),
  * shared rows at R + t, R = T*k.  Widths use fmax = max(f, f_shared). */
@@ -118,8 +129,9 @@ typedef struct {
   size_t hq, hs;                 /* int8 [R+T][fmax], fp32 [R+T][fmax/32] */
   size_t h, o;                   /* fp32 [R+T][fmax], fp32 [R+T][d] */
   size_t plan;                   /* internal work list */
-  size_t sync;                   /* counters of the fused decode kernel */
+  size_t sync;                   /* counters of the fused decode kernel (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
+  size_t trace;                  /* uint64 [1024][20] (MOE_FLAG_TRACE) */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
   uint32_t n_tap;                /* tapped features per row (gate/up and down) */
@@ -182,10 +194,12 @@ const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i);
  *   MOE_ERR_WORKSPACE (moe_last_error says why) and launch nothing.  For the
  *   E=256 / d=6144 / f=2048 layer with a shared expert that is T <= 48.
  * - All calls on a device share the array, which keeps the last call's
- *   contents; each call resets what must start at zero (the error word).
- *   Calls that overlap on the GPU race on the array: serialise them.
- * - The first call on each device looks up the array's device address and
- *   caches it; make that first call before any stream capture begins.
+ *   contents; what must start at zero (error word, counters) is zero-filled
+ *   at set-up and left zeroed by every call.  Calls that overlap on the GPU
+ *   race on the array: serialise them.
+ * - The first call on each device looks up the array's device address,
+ *   caches it and zero-fills the array's head on that call's stream; make
+ *   that first call before any stream capture begins.
  * - Allocates nothing (no cudaMalloc/cudaFree or allocating library call).
  * Inputs and outputs are the caller's device buffers, as for moe_layer. */
 #define MOE_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)

@@ -33,17 +33,50 @@
 namespace moe {
 namespace {
 
-constexpr int kConsumerWarps = 8;
+constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxT = 2;
-constexpr int kBFeat = 8;        // features per gate/up stage: one per consumer warp
+constexpr int kBFeat = 8;        // features per gate/up stage: two consumer warps each
+constexpr int kKSplit = kConsumerWarps / kBFeat;  // K parts per feature
 constexpr int kBItemFeat = 32;   // features per gate/up item: one quantisation block
 constexpr int kMaxStages = 4;
+constexpr uint32_t kSyncInts = MOE_SYNC_BYTES / 4;
 constexpr int kSpinIters = 1 << 26;                // iteration cap of every wait
 constexpr long long kWaitCycles = 4000000000ll;     // ~2 s at 2 GHz: a wait gives up after this
 constexpr long long kStallTestCycles = 20000000ll;  // ~10 ms under MOE_FLAG_TEST_STALL
 
 enum : int { kKindB = 0, kKindC = 1, kKindEnd = 2 };
+
+// MOE_FLAG_TRACE words per CTA (absolute times in ns of %globaltimer, durations
+// in SM clock cycles)
+enum : int {
+  kTrStart = 0,        // kernel entry (ns)
+  kTrXqDone = 1,       // x quantised (ns)
+  kTrFirstStage = 2,   // first stage ready for the consumers (ns)
+  kTrWaitFull = 3,     // consumers waiting for stage data (cycles)
+  kTrWaitReady = 4,    // consumers waiting for an expert's h (cycles)
+  kTrStagesB = 5,      // gate/up stages consumed
+  kTrStagesC = 6,      // down stages consumed
+  kTrConsEnd = 7,      // consumers leave (ns)
+  kTrWaitEmpty = 8,    // producer waiting for a free stage (cycles)
+  kTrWaitRoute = 9,    // producer waiting for the routing result (cycles)
+  kTrItems = 10,       // items taken by this CTA
+  kTrComputeB = 11,    // consumer cycles in gate/up stages
+  kTrComputeC = 12,    // consumer cycles in down stages
+  kTrCombine = 13,     // consumer cycles combining chunks
+  kTrRouteDone = 14,   // CTA 0: routing published (ns)
+  kTrProdEnd = 15,     // producer leaves (ns)
+  kTrRouteLoaded = 16, // CTA 0: logits and bias loaded (ns)
+  kTrRouteTopk = 17,   // CTA 0: top-k and weights done (ns)
+  kTrRoutePerm = 18,   // CTA 0: permutation and plan written (ns)
+  kTraceWords = 20
+};
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 
 struct StageDesc {
   int kind;
@@ -74,11 +107,31 @@ struct FusedArgs {
   float *hs;
   float *o;
   int *plan;
-  uint32_t *sync;  // [0] queue, [1] route flag, [4..4+E] expert ready, then chunk counters
+  uint32_t *sync;  // see SyncView
   uint32_t *err;
   uint32_t c_rows, n_chunks, n_stages, stage_bytes;
   long long wait_cycles;  // budget of every bounded wait
+  unsigned long long *trace;  // MOE_FLAG_TRACE: kTraceWords per CTA, else null
   int stall_test;         // MOE_FLAG_TEST_STALL: never publish the routing result
+};
+
+// Counters at a fixed workspace offset (moe.h: the first 32 KiB of a workspace).
+// They are zero before a call and the last CTA to finish zeroes them again, so
+// no per-call memset is needed (a workspace must be zero-filled once after it
+// is allocated).  diag[] keeps the first timeout's site for the host.
+struct SyncView {
+  uint32_t *queue, *route, *diag, *ready, *chunk, *owner, *done;
+  uint32_t n_clear;  // words from queue up to and including done (diag words are kept)
+  __device__ SyncView(uint32_t *base, uint32_t E, uint32_t n_chunks) {
+    queue = base;
+    route = base + 1;
+    diag = base + 2;  // [2], [3]
+    ready = base + 4;  // [E+1]
+    chunk = ready + E + 1;
+    owner = chunk + n_chunks;  // 1 + CTA that completes chunk c (combines it)
+    done = owner + n_chunks;
+    n_clear = 4 + E + 1 + 2 * n_chunks + 1;
+  }
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -92,6 +145,12 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// raise the phase's expected transaction bytes without arriving
+__device__ __forceinline__ void mbar_add_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
@@ -116,6 +175,18 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long l
     if (clock64() - t0 > budget) return false;
   }
   return false;
+}
+
+// non-blocking: has the phase with the given parity completed?
+__device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
 }
 
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
@@ -150,6 +221,19 @@ __device__ __forceinline__ bool wait_geq(const uint32_t *p, uint32_t target, lon
 
 __device__ __forceinline__ int ld_cg_i32(const int *p) { return __ldcg(p); }
 
+// one thread publishes the CTA's prior writes (made visible to it by a CTA
+// barrier) with a gpu-scope release reduction
+__device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t *p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
 // a bounded wait gave up: flag the error word (kErrTimeout plus the wait site in
 // bits 8..15) and keep the first site / CTA / detail in sync[2], sync[3]
 __device__ __noinline__ void report_timeout(const FusedArgs &a, uint32_t site, uint32_t detail) {
@@ -162,6 +246,15 @@ __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
+// gate/up item end: the requantising warps wait (bar.sync) for every consumer
+// warp's partial sums; the others only signal (bar.arrive) and move on
+__device__ __forceinline__ void item_barrier_wait() {
+  asm volatile("bar.sync 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+__device__ __forceinline__ void item_barrier_arrive() {
+  asm volatile("bar.arrive 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
 __device__ __forceinline__ W8 lds32(const int8_t *p) {
   const uint4 a = *reinterpret_cast<const uint4 *>(p);
   const uint4 b = *reinterpret_cast<const uint4 *>(p + 16);
@@ -169,6 +262,18 @@ __device__ __forceinline__ W8 lds32(const int8_t *p) {
   w.v[0] = a.x; w.v[1] = a.y; w.v[2] = a.z; w.v[3] = a.w;
   w.v[4] = b.x; w.v[5] = b.y; w.v[6] = b.z; w.v[7] = b.w;
   return w;
+}
+
+__device__ __forceinline__ uint4 lds16(const int8_t *p) {
+  return *reinterpret_cast<const uint4 *>(p);
+}
+
+// exact int32 dot of 16 int8 pairs
+__device__ __forceinline__ int dot16(const uint4 &a, const uint4 &b) {
+  int s = __dp4a((int)a.x, (int)b.x, 0);
+  s = __dp4a((int)a.y, (int)b.y, s);
+  s = __dp4a((int)a.z, (int)b.z, s);
+  return __dp4a((int)a.w, (int)b.w, s);
 }
 
 __device__ __forceinline__ int dot8(const W8 &a, const W8 &b) {
@@ -185,155 +290,155 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ---------------------------------------------------------------- routing (CTA 0)
-// Warp t routes token t; then the consumer threads build the stable permutation
-// (R <= 64 rows: rank by comparison), off[], and the active-expert list.
-__device__ void route_tokens(const FusedArgs &a, int *s_idx, float *s_w) {
+// Runs once per call on cold caches, so the code is kept short (no wide
+// unrolling): scores go to shared-memory scratch, warp t selects token t's
+// top_k by k rounds of a strided scan plus a butterfly argmax (score
+// descending, index ascending: ties go to the lower index), and the stable
+// permutation / offsets / active list are O(R) per thread (R <= 64 rows).
+__device__ void route_tokens(const FusedArgs &a, int *s_idx, float *s_w, float *scratch,
+                             unsigned long long *tr) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t E = a.E, k = a.k;
-  if (warp < (int)a.T) {
+  const uint32_t E = a.E, k = a.k, T = a.T;
+  float *c_s = scratch;               // [T][E] selection score (taken -> -inf)
+  float *sg_s = scratch + (size_t)T * E;  // [T][E] sigmoid(logit)
+  const int R = (int)a.R;
+  // scores: every consumer thread takes a share of the T*E (token, expert) pairs
+  for (uint32_t i = tid; i < T * E; i += kConsumerWarps * 32) {
+    const float sg = sigmoid_rn(__ldg(a.logits + i));
+    sg_s[i] = sg;
+    c_s[i] = __fadd_rn(sg, __ldg(a.bias + i % E));
+  }
+  consumer_sync();
+  if (tr && tid == 0) tr[kTrRouteLoaded] = global_ns();
+  if (warp < (int)T) {
     const int t = warp;
-    const float *l = a.logits + (size_t)t * E;
-    const int nper = (int)((E + 31) / 32);
-    float lv[32], bv[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {  // issue every load before any use
-      const uint32_t e = (uint32_t)lane + 32u * i;
-      const bool ok = i < nper && e < E;
-      lv[i] = ok ? l[e] : 0.0f;
-      bv[i] = ok ? a.bias[e] : 0.0f;
-    }
-    float c[32], sg[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const uint32_t e = (uint32_t)lane + 32u * i;
-      c[i] = -INFINITY;
-      sg[i] = 0.0f;
-      if (i < nper && e < E) {
-        sg[i] = sigmoid_rn(lv[i]);
-        c[i] = __fadd_rn(sg[i], bv[i]);
-      }
-    }
-    uint32_t taken = 0;
-    float my_sigma = 0.0f;
+    float *ct = c_s + (size_t)t * E;
+    float my_sigma = 0.0f;  // lane j keeps the sigma of slot j
+#pragma unroll 1
     for (uint32_t j = 0; j < k; ++j) {
-      float bc = -INFINITY, bs = 0.0f;
+      float bc = -INFINITY;
       int be = 0x7fffffff;
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        if (i < nper && !((taken >> i) & 1u) && c[i] > bc) {
-          bc = c[i];
-          be = lane + 32 * i;
-          bs = sg[i];
+#pragma unroll 1
+      for (uint32_t e = lane; e < E; e += 32) {
+        const float v = ct[e];
+        if (v > bc) {  // ascending e per lane: strict '>' keeps the lower index
+          bc = v;
+          be = (int)e;
         }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
         const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
         if (oc > bc || (oc == bc && oe < be)) {
           bc = oc;
           be = oe;
-          bs = os;
         }
       }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if ((uint32_t)lane == j) my_sigma = bs;
-      if (lane == 0) s_idx[t * k + j] = be;
+      __syncwarp();
+      if (lane == 0) {
+        ct[be] = -INFINITY;
+        s_idx[t * k + j] = be;
+      }
+      __syncwarp();
+      if ((uint32_t)lane == j) my_sigma = sg_s[(size_t)t * E + be];
     }
     float sum = 0.0f;
+#pragma unroll 1
     for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
     if ((uint32_t)lane < k) s_w[t * k + lane] = __fmul_rn(a.s, __fdiv_rn(my_sigma, sum));
   }
   consumer_sync();
-  const int R = (int)a.R;
+  if (tr && tid == 0) tr[kTrRouteTopk] = global_ns();
   PlanView P(a.plan, E);
-  // stable rank of each (token, slot) row by expert
+  int *rank_of = (int *)(c_s);            // [R] sorted position of row r (scores are done)
+  int *row_at = rank_of + 64;             // [R] row at sorted position p
   if (tid < R) {
     const int e = s_idx[tid];
     int rank = 0;
+#pragma unroll 1
     for (int r = 0; r < R; ++r) {
       const int er = s_idx[r];
       rank += (er < e || (er == e && r < tid)) ? 1 : 0;
     }
+    rank_of[tid] = rank;
+    row_at[rank] = tid;
     a.idx[tid] = e;
     a.w[tid] = s_w[tid];
     a.pos[tid] = rank;
     a.perm[rank] = tid;
   }
-  // off[e] = rows routed to experts below e
+#pragma unroll 1
   for (uint32_t e = tid; e <= E; e += kConsumerWarps * 32) {
     int c = 0;
+#pragma unroll 1
     for (int r = 0; r < R; ++r) c += s_idx[r] < (int)e ? 1 : 0;
     a.off[e] = c;
   }
-  // active list: one entry per distinct expert, ascending
-  if (tid < R) {
-    const int e = s_idx[tid];
-    bool first = true;
-    int below = 0, rows = 0;
-    for (int r = 0; r < R; ++r) {
-      const int er = s_idx[r];
-      if (er == e) {
-        ++rows;
-        if (r < tid) first = false;
-      }
-    }
-    if (first) {
-      // distinct experts smaller than e
-      for (int r = 0; r < R; ++r) {
-        const int er = s_idx[r];
-        if (er < e) {
-          bool first_r = true;
-          for (int q = 0; q < r; ++q)
-            if (s_idx[q] == er) first_r = false;
-          below += first_r ? 1 : 0;
-        }
-      }
-      int row0 = 0;
-      for (int r = 0; r < R; ++r) row0 += s_idx[r] < e ? 1 : 0;
-      P.act_e[below] = e;
-      P.act_row0[below] = row0;
-      P.act_rows[below] = rows;
-    }
-  }
-  if (tid == 0) {
-    int U = 0;
-    for (int r = 0; r < R; ++r) {
-      bool first_r = true;
-      for (int q = 0; q < r; ++q)
-        if (s_idx[q] == s_idx[r]) first_r = false;
-      U += first_r ? 1 : 0;
-    }
-    P.hdr[0] = U;  // routed experts only
-    P.hdr[4] = 1;
-  }
-  __threadfence();
   consumer_sync();
-  if (tid == 0 && !a.stall_test) st_release(&a.sync[1], 1u);
+  // active list from the sorted rows: a run of equal experts is one entry
+  if (tid < R) {
+    const int p = tid;
+    const int e = s_idx[row_at[p]];
+    const bool first = p == 0 || s_idx[row_at[p - 1]] != e;
+    if (first) {
+      int u = 0, rows = 0;
+#pragma unroll 1
+      for (int q = 1; q <= p; ++q) u += s_idx[row_at[q]] != s_idx[row_at[q - 1]] ? 1 : 0;
+#pragma unroll 1
+      for (int q = p; q < R && s_idx[row_at[q]] == e; ++q) ++rows;
+      P.act_e[u] = e;
+      P.act_row0[u] = p;
+      P.act_rows[u] = rows;
+    }
+    if (p == R - 1) {
+      int U = 1;
+#pragma unroll 1
+      for (int q = 1; q < R; ++q) U += s_idx[row_at[q]] != s_idx[row_at[q - 1]] ? 1 : 0;
+      P.hdr[0] = U;  // routed experts only
+      P.hdr[4] = 1;
+    }
+  }
+  consumer_sync();
+  if (tr && tid == 0) tr[kTrRoutePerm] = global_ns();
+  if (tid == 0 && !a.stall_test) red_release_add(&a.sync[1], 1u);
 }
 
 // ---------------------------------------------------------------- the kernel
+// Shared-memory carve-up (all offsets multiples of 16 bytes):
+//   stages[NS][stage_bytes] | xq_s[2][d] | xs_s[2][d/32] | hq_s[2][fmax] |
+//   hs_s[2][fmax/32] | part[32][2][2][2] | desc[4] | full[4] | empty[4] |
+//   misc[4] | s_idx[64] | producer plan (4 x 64) | s_w[64]
+// NT: token count known at compile time (1 or 2): the one-token kernel has no
+// second-row code.
+template <int NT>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t T = a.T, d = a.d, nb = d / 32, fmax = a.fmax;
+  const uint32_t T = NT, d = a.d, nb = d / 32, fmax = a.fmax;
   const uint32_t NS = a.n_stages;
-  // shared-memory carve-up
   uint8_t *stages = smem;
   int8_t *xq_s = (int8_t *)(stages + (size_t)NS * a.stage_bytes);
   float *xs_s = (float *)(xq_s + (size_t)kMaxT * d);
   int8_t *hq_s = (int8_t *)(xs_s + (size_t)kMaxT * nb);
   float *hs_s = (float *)(hq_s + (size_t)kMaxT * fmax);
-  float *h_tile = hs_s + (size_t)kMaxT * (fmax / 32);
-  StageDesc *desc = (StageDesc *)(h_tile + kMaxT * kBItemFeat);
+  float *part = hs_s + (size_t)kMaxT * (fmax / 32);  // [2][feature 32][K part][row 2][g,u]
+  StageDesc *desc = (StageDesc *)(part + 2 * kBItemFeat * kKSplit * kMaxT * 2);
   uint64_t *full = (uint64_t *)(desc + kMaxStages);
   uint64_t *empty = full + kMaxStages;
-  volatile int *s_misc = (volatile int *)(empty + kMaxStages);  // [0] abort, [1] chunk is last
+  volatile int *s_misc = (volatile int *)(empty + kMaxStages);  // [0] abort, [1] exit-last
   int *s_idx = (int *)(s_misc + 4);                             // [R]
-  float *s_w = (float *)(s_idx + 64);                           // [R]
+  float *s_w = (float *)(s_idx + 64 + 4 * 64);                  // [R]; producer plan before it
 
+  const SyncView SV(a.sync, a.E, a.n_chunks);
+  unsigned long long *tr = a.trace ? a.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+  if (tr && tid == 0) {
+    for (int i = 0; i < kTraceWords; ++i) tr[i] = 0;
+    tr[kTrStart] = global_ns();
+  }
   if (tid == 0) {
+    // any timeout report comes >= 10 ms later, after every CTA has started
+    if (blockIdx.x == 0) *a.err = 0u;
     for (uint32_t i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -344,68 +449,96 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   }
   __syncthreads();
 
-  const uint32_t n_sh = a.fs / kBItemFeat;          // shared-expert gate/up items
-  const uint32_t fb = a.f / kBItemFeat;              // gate/up items per routed expert
+  const uint32_t n_sh = a.fs / kBItemFeat;  // shared-expert gate/up items
+  const uint32_t fb = a.f / kBItemFeat;      // gate/up items per routed expert
   PlanView P(a.plan, a.E);
 
   if (warp == kConsumerWarps) {
-    // ============================ producer (one lane)
-    if (lane != 0) return;
-    uint32_t g = 0;  // stages issued
-    bool routed = false;
-    uint32_t U = 0, NB = 0, total = 0;
-    for (;;) {
-      const uint32_t item = atomicAdd(&a.sync[0], 1u);
-      if (!routed && item >= n_sh) {
-        if (!wait_geq(&a.sync[1], 1u, a.wait_cycles)) {
-          report_timeout(a, 1, item);
+    // ============================ producer (lane 0; the warp's other lanes wait at the end)
+    if (lane == 0) {
+      uint32_t g = 0;  // stages issued
+      bool routed = false;
+      uint32_t U = 0, NB = 0, total = 0;
+      // per ring slot: what completes when the consumers release it
+      //   ready_e >= 0: last stage of a gate/up item of that expert
+      //   chunk  >= 0: a down stage contributing to that output chunk (n_contrib)
+      int slot_ready_e[kMaxStages], slot_chunk[kMaxStages], slot_contrib[kMaxStages];
+      unsigned long long p_wait_empty = 0, p_wait_route = 0, p_items = 0, p_wait_ready = 0;
+      for (int i = 0; i < kMaxStages; ++i) slot_ready_e[i] = slot_chunk[i] = -1;
+      int *p_e = s_idx + 64, *p_row0 = p_e + 64, *p_rows = p_row0 + 64, *p_tok = p_rows + 64;
+      // queue order: shared gate/up | routed gate/up | shared down | routed down.
+      // Only the shared gate/up items are known before routing.
+      const uint32_t n_pre = n_sh;
+      // wait for CTA 0's routing result and copy the plan (U <= R <= 64 experts)
+      auto learn_routing = [&]() -> bool {
+        const long long t_rw = clock64();
+        const bool ok = wait_geq(SV.route, 1u, a.wait_cycles);
+        p_wait_route += clock64() - t_rw;
+        if (!ok) {
+          report_timeout(a, 1, 0);
           s_misc[0] = 1;
-        } else {
-          U = (uint32_t)ld_cg_i32(&P.hdr[0]);
-          NB = n_sh + U * fb;
-          total = NB + (U + (a.fs ? 1u : 0u)) * a.n_chunks;
-          routed = true;
+          return false;
         }
-      }
-      const bool end = s_misc[0] || (routed && item >= total);
-      StageDesc dsc;
-      dsc.kind = kKindEnd;
-      int nsub = 1;
-      if (!end) {
-        // shared-expert gate/up items come first and are known before routing (NB is
-        // only known after it), so test them against n_sh before NB
-        if (item < n_sh || item < NB) {  // gate/up item
-          dsc.kind = kKindB;
+        U = (uint32_t)ld_cg_i32(&P.hdr[0]);
+        for (uint32_t u = 0; u < U; ++u) {
+          p_e[u] = ld_cg_i32(&P.act_e[u]);
+          p_row0[u] = ld_cg_i32(&P.act_row0[u]);
+          p_rows[u] = ld_cg_i32(&P.act_rows[u]);
+        }
+        for (uint32_t p = 0; p < a.R; ++p) p_tok[p] = ld_cg_i32(&a.perm[p]) / (int)a.k;
+        NB = n_sh + U * fb;  // all gate/up items
+        total = NB + (U + (a.fs ? 1u : 0u)) * a.n_chunks;
+        routed = true;
+        return true;
+      };
+      // a stage was released by the consumers: publish what it completed
+      auto settle = [&](uint32_t st) {
+        if (slot_ready_e[st] >= 0) red_release_add(&SV.ready[slot_ready_e[st]], 1u);
+        if (slot_chunk[st] >= 0) {
+          // a shared-expert down stage issued before routing: the number of
+          // contributions per chunk (routed experts + 1) is learnt now
+          if (slot_contrib[st] < 0 && (routed || learn_routing())) slot_contrib[st] = (int)U + 1;
+          const uint32_t c = (uint32_t)slot_chunk[st];
+          if (slot_contrib[st] > 0 &&
+              atom_acq_rel_add(&SV.chunk[c], 1u) + 1 == (uint32_t)slot_contrib[st])
+            SV.owner[c] = blockIdx.x + 1;  // this CTA combines chunk c at its end
+        }
+        slot_ready_e[st] = slot_chunk[st] = -1;
+      };
+      // CTA 0's consumers route first, using the stage buffers as scratch: its
+      // producer starts once the routing result is out
+      if (blockIdx.x == 0 && !learn_routing()) s_misc[0] = 1;
+      uint32_t item = atomicAdd(SV.queue, 1u);
+      for (;;) {
+        // ticket for the following item, fetched while this one is issued
+        const uint32_t next_item = atomicAdd(SV.queue, 1u);
+        ++p_items;
+        if (!routed && item >= n_pre && !learn_routing()) {
+          s_misc[0] = 1;
+        }
+        const bool end = s_misc[0] || (routed && item >= total);
+        StageDesc dsc;
+        dsc.kind = kKindEnd;
+        int nsub = 1;
+        if (!end) {
+          // shared-expert gate/up items come first and are known before routing
+          // (NB is only known after it), so test them against n_sh before NB
+          bool is_b = false, shared = false;
+          uint32_t u = 0, chunk = 0;
           if (item < n_sh) {
-            dsc.e = (int)a.E;
+            is_b = shared = true;
             dsc.item_first = (int)(item * kBItemFeat);
-            dsc.nrows = (int)T;
-            for (uint32_t r = 0; r < T; ++r) {
-              dsc.slot[r] = (int)(a.R + r);
-              dsc.tok[r] = (int)r;
-            }
-          } else {
-            const uint32_t u = (item - n_sh) / fb;
-            dsc.e = ld_cg_i32(&P.act_e[u]);
+          } else if (item < NB) {
+            is_b = true;
+            u = (item - n_sh) / fb;
             dsc.item_first = (int)(((item - n_sh) % fb) * kBItemFeat);
-            const int row0 = ld_cg_i32(&P.act_row0[u]);
-            dsc.nrows = ld_cg_i32(&P.act_rows[u]);
-            for (int r = 0; r < dsc.nrows; ++r) {
-              dsc.slot[r] = row0 + r;
-              dsc.tok[r] = ld_cg_i32(&a.perm[row0 + r]) / (int)a.k;
-            }
+          } else {
+            uint32_t uc = (item - NB) / a.n_chunks;
+            chunk = (item - NB) % a.n_chunks;
+            if (a.fs && uc == 0) shared = true;
+            else u = a.fs ? uc - 1 : uc;
           }
-          nsub = kBItemFeat / kBFeat;
-        } else {  // down item
-          const uint32_t c = item - NB;
-          uint32_t uc = c / a.n_chunks;
-          const uint32_t chunk = c % a.n_chunks;
-          dsc.kind = kKindC;
-          dsc.item_first = (int)chunk;
-          dsc.first = (int)(chunk * a.c_rows);
-          dsc.count = (int)min(a.c_rows, d - chunk * a.c_rows);
-          dsc.n_contrib = (int)(U + (a.fs ? 1u : 0u));
-          if (a.fs && uc == 0) {
+          if (shared) {
             dsc.e = (int)a.E;
             dsc.nrows = (int)T;
             for (uint32_t r = 0; r < T; ++r) {
@@ -413,213 +546,422 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               dsc.tok[r] = (int)r;
             }
           } else {
-            if (a.fs) uc -= 1;
-            dsc.e = ld_cg_i32(&P.act_e[uc]);
-            const int row0 = ld_cg_i32(&P.act_row0[uc]);
-            dsc.nrows = ld_cg_i32(&P.act_rows[uc]);
+            dsc.e = p_e[u];
+            const int row0 = p_row0[u];
+            dsc.nrows = p_rows[u];
             for (int r = 0; r < dsc.nrows; ++r) {
               dsc.slot[r] = row0 + r;
-              dsc.tok[r] = ld_cg_i32(&a.perm[row0 + r]) / (int)a.k;
+              dsc.tok[r] = p_tok[row0 + r];
             }
           }
+          if (is_b) {
+            dsc.kind = kKindB;
+            nsub = kBItemFeat / kBFeat;
+          } else {
+            dsc.kind = kKindC;
+            dsc.item_first = (int)chunk;
+            dsc.first = (int)(chunk * a.c_rows);
+            dsc.count = (int)min(a.c_rows, d - chunk * a.c_rows);
+            dsc.n_contrib = routed ? (int)(U + (a.fs ? 1u : 0u)) : -1;
+          }
+        }
+        for (int sub = 0; sub < nsub; ++sub) {
+          const uint32_t st = g % NS, use = g / NS;
+          const long long t_we = clock64();
+          const bool empty_ok =
+              use == 0 || mbar_wait(&empty[st], (use - 1) & 1u, a.wait_cycles);
+          p_wait_empty += clock64() - t_we;
+          if (!empty_ok) {
+            report_timeout(a, 2, g);
+            s_misc[0] = 1;
+            dsc.kind = kKindEnd;
+          }
+          // the slot's previous contents were released: publish their effects once,
+          // normally after the new copy is on its way, but before a wait on expert
+          // readiness (the previous contents may complete that very expert)
+          bool prev_settled = !empty_ok;
+          auto settle_prev = [&]() {
+            if (!prev_settled) settle(st);
+            prev_settled = true;
+          };
+          dsc.sub = sub;
+          uint8_t *buf = stages + (size_t)st * a.stage_bytes;
+          if (dsc.kind == kKindB) {
+            dsc.first = dsc.item_first + sub * kBFeat;
+            dsc.count = kBFeat;
+            const bool sh = dsc.e == (int)a.E;
+            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * a.f + dsc.first;
+            const int8_t *g_src = (sh ? a.sgq : a.gq) + row * d;
+            const int8_t *u_src = (sh ? a.suq : a.uq) + row * d;
+            const uint16_t *gs_src = (sh ? a.sgs : a.gs) + row * nb;
+            const uint16_t *us_src = (sh ? a.sus : a.us) + row * nb;
+            const uint32_t qb = kBFeat * d, sb = kBFeat * nb * 2;
+            desc[st] = dsc;
+            mbar_expect_tx(&full[st], 2 * qb + 2 * sb);
+            bulk_g2s(buf, g_src, qb, &full[st]);
+            bulk_g2s(buf + qb, u_src, qb, &full[st]);
+            bulk_g2s(buf + 2 * qb, gs_src, sb, &full[st]);
+            bulk_g2s(buf + 2 * qb + sb, us_src, sb, &full[st]);
+          } else if (dsc.kind == kKindC) {
+            const bool sh = dsc.e == (int)a.E;
+            const uint32_t K = sh ? a.fs : a.f;
+            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * d + dsc.first;
+            const int8_t *q_src = (sh ? a.sdq : a.dq) + row * K;
+            const uint16_t *s_src = (sh ? a.sds : a.ds) + row * (K / 32);
+            const uint32_t qb = (uint32_t)dsc.count * K, sb = (uint32_t)dsc.count * (K / 32) * 2;
+            // the expert's h codes travel with its down weights.  The weights go
+            // first (expected bytes raised without arriving, so the phase cannot
+            // complete early); the h codes follow once every gate/up item of the
+            // expert is published, together with the stage's single arrival.
+            desc[st] = dsc;
+            mbar_add_tx(&full[st], qb + sb);
+            bulk_g2s(buf, q_src, qb, &full[st]);
+            bulk_g2s(buf + qb, s_src, sb, &full[st]);
+            settle_prev();
+            const long long t_wr = clock64();
+            const uint32_t need = (K / kBItemFeat);
+            // while waiting, publish whatever older stages the consumers have
+            // released: one of them may complete the very expert waited for
+            bool ready_ok = false;
+            for (int it = 0; it < kSpinIters; ++it) {
+              if (ld_acquire(&SV.ready[dsc.e]) >= need) {
+                ready_ok = true;
+                break;
+              }
+              for (uint32_t q = (g + 1 > NS ? g + 1 - NS : 0); q < g; ++q)
+                if ((slot_ready_e[q % NS] >= 0 || slot_chunk[q % NS] >= 0) &&
+                    mbar_test(&empty[q % NS], (q / NS) & 1u))
+                  settle(q % NS);
+              if (clock64() - t_wr > a.wait_cycles) break;
+              __nanosleep(64);
+            }
+            p_wait_ready += clock64() - t_wr;
+            if (!ready_ok) {
+              // the consumers get an END stage once the weights have landed
+              report_timeout(a, 4, ((uint32_t)dsc.e << 16) | __ldcg(&SV.ready[dsc.e]));
+              s_misc[0] = 1;
+              dsc.kind = kKindEnd;
+              desc[st] = dsc;
+              mbar_arrive(&full[st]);
+              ++g;
+              break;
+            }
+            // async-proxy reads of data that other CTAs wrote with generic stores
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            const uint32_t hb = K, hsb = (K / 32) * 4;
+            uint8_t *hq_dst = buf + qb + sb;
+            uint8_t *hs_dst = hq_dst + (size_t)kMaxT * hb;
+            mbar_expect_tx(&full[st], (uint32_t)dsc.nrows * (hb + hsb));
+            for (int r = 0; r < dsc.nrows; ++r) {
+              const size_t slot = (size_t)(r == 0 ? dsc.slot[0] : dsc.slot[kMaxT - 1]);
+              bulk_g2s(hq_dst + (size_t)r * hb, a.hq + slot * fmax, hb, &full[st]);
+              bulk_g2s(hs_dst + (size_t)r * hsb, a.hs + slot * (fmax / 32), hsb, &full[st]);
+            }
+          } else {
+            desc[st] = dsc;
+            mbar_arrive(&full[st]);
+          }
+          settle_prev();
+          if (dsc.kind == kKindB && sub == kBItemFeat / kBFeat - 1) slot_ready_e[st] = dsc.e;
+          if (dsc.kind == kKindC) {
+            slot_chunk[st] = dsc.item_first;
+            slot_contrib[st] = dsc.n_contrib;
+          }
+          ++g;
+          if (dsc.kind == kKindEnd) break;
+        }
+        if (dsc.kind == kKindEnd) break;
+        item = next_item;
+      }
+      // drain: wait for the consumers to release every stage still held and
+      // publish its effects (the END stage itself is never released)
+      if (!s_misc[0]) {
+        for (uint32_t q = (g > NS ? g - NS : 0); q + 1 < g; ++q) {
+          const uint32_t st = q % NS;
+          if (!mbar_wait(&empty[st], (q / NS) & 1u, a.wait_cycles)) {
+            report_timeout(a, 2, q);
+            break;
+          }
+          settle(st);
         }
       }
-      for (int sub = 0; sub < nsub; ++sub) {
-        const uint32_t st = g % NS, use = g / NS;
-        if (use > 0 && !mbar_wait(&empty[st], (use - 1) & 1u, a.wait_cycles)) {
-          report_timeout(a, 2, g);
-          s_misc[0] = 1;
-          dsc.kind = kKindEnd;
-        }
-        dsc.sub = sub;
-        uint8_t *buf = stages + (size_t)st * a.stage_bytes;
-        if (dsc.kind == kKindB) {
-          dsc.first = dsc.item_first + sub * kBFeat;
-          dsc.count = kBFeat;
-          const bool sh = dsc.e == (int)a.E;
-          const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * a.f + dsc.first;
-          const int8_t *g_src = (sh ? a.sgq : a.gq) + row * d;
-          const int8_t *u_src = (sh ? a.suq : a.uq) + row * d;
-          const uint16_t *gs_src = (sh ? a.sgs : a.gs) + row * nb;
-          const uint16_t *us_src = (sh ? a.sus : a.us) + row * nb;
-          const uint32_t qb = kBFeat * d, sb = kBFeat * nb * 2;
-          desc[st] = dsc;
-          mbar_expect_tx(&full[st], 2 * qb + 2 * sb);
-          bulk_g2s(buf, g_src, qb, &full[st]);
-          bulk_g2s(buf + qb, u_src, qb, &full[st]);
-          bulk_g2s(buf + 2 * qb, gs_src, sb, &full[st]);
-          bulk_g2s(buf + 2 * qb + sb, us_src, sb, &full[st]);
-        } else if (dsc.kind == kKindC) {
-          const bool sh = dsc.e == (int)a.E;
-          const uint32_t K = sh ? a.fs : a.f;
-          const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * d + dsc.first;
-          const int8_t *q_src = (sh ? a.sdq : a.dq) + row * K;
-          const uint16_t *s_src = (sh ? a.sds : a.ds) + row * (K / 32);
-          const uint32_t qb = dsc.count * K, sb = dsc.count * (K / 32) * 2;
-          desc[st] = dsc;
-          mbar_expect_tx(&full[st], qb + sb);
-          bulk_g2s(buf, q_src, qb, &full[st]);
-          bulk_g2s(buf + qb, s_src, sb, &full[st]);
-        } else {
-          desc[st] = dsc;
-          mbar_arrive(&full[st]);
-        }
-        ++g;
+      if (tr) {
+        tr[kTrProdEnd] = global_ns();
+        tr[kTrWaitEmpty] = p_wait_empty;
+        tr[kTrWaitRoute] = p_wait_route;
+        tr[kTrItems] = p_items;
+        tr[kTrWaitReady] = p_wait_ready;
       }
-      if (dsc.kind == kKindEnd) return;
     }
-  }
-
-  // ============================ consumers (warps 0..7)
-  if (blockIdx.x == 0) route_tokens(a, s_idx, s_w);
-  // quantise x for this CTA (identical in every CTA); CTA 0 also publishes it
-  for (uint32_t b = warp; b < T * nb; b += kConsumerWarps) {
-    const uint32_t t = b / nb, bb = b % nb;
-    const float v = a.x[(size_t)t * d + 32 * bb + lane];
-    float amax = fabsf(v);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    const float sc = __fdiv_rn(amax, 127.0f);
-    const int8_t q = (int8_t)quant_one(v, sc);
-    xq_s[(size_t)t * d + 32 * bb + lane] = q;
-    if (lane == 0) xs_s[t * nb + bb] = sc;
+    __syncwarp();
+  } else {
+    // ============================ consumers (warps 0..15)
     if (blockIdx.x == 0) {
-      a.xq[(size_t)t * d + 32 * bb + lane] = q;
-      if (lane == 0) a.xs[t * nb + bb] = sc;
+      route_tokens(a, s_idx, s_w, (float *)stages, tr);
+      if (tr && tid == 0) tr[kTrRouteDone] = global_ns();
+    }
+    // quantise x for this CTA (identical in every CTA; CTA 0 also publishes it):
+    // warp w takes blocks w, w+16, ...; each round issues 8 loads per lane first
+    for (uint32_t b0 = warp; b0 < T * nb; b0 += 8 * kConsumerWarps) {
+      float v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t b = b0 + i * kConsumerWarps;
+        v[i] = b < T * nb ? __ldg(a.x + (size_t)b * 32 + lane) : 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t b = b0 + i * kConsumerWarps;
+        float amax = fabsf(v[i]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (b < T * nb) {
+          const float sc = __fdiv_rn(amax, 127.0f);
+          const int8_t q = (int8_t)quant_one(v[i], sc);
+          xq_s[(size_t)b * 32 + lane] = q;
+          if (lane == 0) xs_s[b] = sc;
+          if (blockIdx.x == 0) {
+            a.xq[(size_t)b * 32 + lane] = q;
+            if (lane == 0) a.xs[b] = sc;
+          }
+        }
+      }
+    }
+    consumer_sync();
+    if (tr && tid == 0) tr[kTrXqDone] = global_ns();
+
+    // trace accumulators live in registers; written once when the consumers leave
+    unsigned long long c_wait_full = 0, c_b = 0, c_c = 0, n_b = 0, n_c = 0;
+    // gate/up: warp w takes feature w / kKSplit of the stage, K part w % kKSplit
+    const uint32_t half = warp % kKSplit, fw = warp / kKSplit;
+    const uint32_t nbh = nb / kKSplit;  // 32-blocks per K part
+    const uint32_t nc = d / (16 * kKSplit);  // 16-byte chunks per K part
+    uint32_t b_items = 0;  // gate/up items finished by this CTA (part[] buffer parity)
+    uint32_t g = 0;
+    for (;; ++g) {
+      const uint32_t st = g % NS, use = g / NS;
+      const long long t_wf = clock64();
+      const bool full_ok = mbar_wait(&full[st], use & 1u, a.wait_cycles);
+      const long long t_got = clock64();
+      c_wait_full += t_got - t_wf;
+      if (tr && tid == 0 && g == 0) tr[kTrFirstStage] = global_ns();
+      if (!full_ok) {
+        report_timeout(a, 3, g);
+        break;
+      }
+      const StageDesc dsc = desc[st];
+      if (dsc.kind == kKindEnd) break;
+      const uint8_t *buf = stages + (size_t)st * a.stage_bytes;
+      const int nr = NT == 1 ? 1 : dsc.nrows;
+      const int tok0 = dsc.tok[0], tok1 = dsc.tok[kMaxT - 1];
+      if (dsc.kind == kKindB) {
+        // ---- gate/up: kKSplit warps split feature first+f over K.  Lane l reads
+        // 16 contiguous bytes (conflict-free); lanes l and l^1 form one 32-block
+        // whose exact int32 sum is completed with one shuffle.
+        const size_t hoff = (size_t)half * (d / kKSplit);  // byte offset of this warp's K part
+        const int8_t *gc = (const int8_t *)buf + (size_t)fw * d + hoff;
+        const int8_t *uc = (const int8_t *)buf + (size_t)kBFeat * d + (size_t)fw * d + hoff;
+        const uint16_t *gsc =
+            (const uint16_t *)(buf + 2 * kBFeat * d) + (size_t)fw * nb + half * nbh;
+        const uint16_t *usc = (const uint16_t *)(buf + 2 * kBFeat * d) + (size_t)kBFeat * nb +
+                              (size_t)fw * nb + half * nbh;
+        const int8_t *x0p = xq_s + (size_t)tok0 * d + hoff;
+        const int8_t *x1p = xq_s + (size_t)tok1 * d + hoff;
+        const float *xs0p = xs_s + tok0 * nb + half * nbh;
+        const float *xs1p = xs_s + tok1 * nb + half * nbh;
+        const bool even = (lane & 1) == 0;
+        float g0 = 0.0f, u0 = 0.0f, g1 = 0.0f, u1 = 0.0f;
+        {
+        // every lane runs the same trip count (the shuffles need the full warp);
+        // chunk pairs never straddle nc (nc is even)
+#pragma unroll 2
+        for (uint32_t c0 = 0; c0 < nc; c0 += 32) {
+          const uint32_t c = c0 + lane;
+          const bool ok = c < nc;
+          const uint4 z = make_uint4(0, 0, 0, 0);
+          const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
+          const uint4 x0 = ok ? lds16(x0p + 16 * c) : z;
+          int pg = dot16(wg, x0), pu = dot16(wu, x0);
+          pg += __shfl_xor_sync(0xffffffffu, pg, 1);
+          pu += __shfl_xor_sync(0xffffffffu, pu, 1);
+          const uint32_t blk = ok ? c >> 1 : 0;
+          const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
+          if (even && ok) {
+            const float xs0 = xs0p[blk];
+            g0 = __fmaf_rn((float)pg, sg * xs0, g0);
+            u0 = __fmaf_rn((float)pu, su * xs0, u0);
+          }
+          if (nr > 1) {
+            const uint4 x1 = ok ? lds16(x1p + 16 * c) : z;
+            int qg = dot16(wg, x1), qu = dot16(wu, x1);
+            qg += __shfl_xor_sync(0xffffffffu, qg, 1);
+            qu += __shfl_xor_sync(0xffffffffu, qu, 1);
+            if (even && ok) {
+              const float xs1 = xs1p[blk];
+              g1 = __fmaf_rn((float)qg, sg * xs1, g1);
+              u1 = __fmaf_rn((float)qu, su * xs1, u1);
+            }
+          }
+        }
+        }
+        g0 = warp_sum(g0);
+        u0 = warp_sum(u0);
+        if (NT > 1 && nr > 1) {
+          g1 = warp_sum(g1);
+          u1 = warp_sum(u1);
+        }
+        // partial sums, double-buffered by item parity: the requant of item i reads
+        // buffer i&1 while the other warps may already fill buffer (i+1)&1 (the
+        // stage ring keeps them from reaching item i+2)
+        float *pbuf = part + (size_t)(b_items & 1) * kBItemFeat * kKSplit * kMaxT * 2;
+        if (lane == 0) {
+          float *pp =
+              pbuf + ((size_t)((dsc.first - dsc.item_first) + fw) * kKSplit + half) * kMaxT * 2;
+          pp[0] = g0;
+          pp[1] = u0;
+          pp[2] = g1;
+          pp[3] = u1;
+        }
+        if (dsc.sub == kBItemFeat / kBFeat - 1) {
+          ++b_items;
+          // the item's 32 features are done: h = silu(g)*u, requantised (warp r: row r)
+          if (warp < nr) item_barrier_wait(); else item_barrier_arrive();
+          if (warp < nr) {
+            const float *pp = pbuf + (size_t)lane * kKSplit * kMaxT * 2;
+            float gv = pp[warp * 2], uv = pp[warp * 2 + 1];
+#pragma unroll
+            for (int q = 1; q < kKSplit; ++q) {
+              gv = __fadd_rn(gv, pp[q * kMaxT * 2 + warp * 2]);
+              uv = __fadd_rn(uv, pp[q * kMaxT * 2 + warp * 2 + 1]);
+            }
+            const float v = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
+            float amax = fabsf(v);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1)
+              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            const float sc = __fdiv_rn(amax, 127.0f);
+            const size_t slot = (size_t)(warp == 0 ? dsc.slot[0] : dsc.slot[kMaxT - 1]);
+            a.hq[slot * fmax + dsc.item_first + lane] = (int8_t)quant_one(v, sc);
+            if (lane == 0) a.hs[slot * (fmax / 32) + dsc.item_first / 32] = sc;
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // the producer publishes h readiness
+        n_b += 1;
+        c_b += clock64() - t_got;
+      } else {
+        // ---- down: the stage holds the rows' weights and the expert's h codes
+        const bool sh = dsc.e == (int)a.E;
+        const uint32_t K = sh ? a.fs : a.f, kb = K / 32;
+        const int8_t *hq_st = (const int8_t *)buf + (size_t)dsc.count * (K + K / 16);
+        const float *hs_st = (const float *)(hq_st + (size_t)kMaxT * K);
+        const int8_t *qc = (const int8_t *)buf;
+        const uint16_t *scl = (const uint16_t *)(buf + (size_t)dsc.count * K);
+        const size_t slot0 = (size_t)dsc.slot[0], slot1 = (size_t)dsc.slot[kMaxT - 1];
+        const uint32_t ncr = K / 16;  // 16-byte chunks per down row
+        const bool even = (lane & 1) == 0;
+        // rows m0, m0+16, m0+32 of the stage: each h chunk is read once for three rows
+        for (int m0 = warp; m0 < dsc.count; m0 += 3 * kConsumerWarps) {
+          float acc[3][kMaxT];
+#pragma unroll
+          for (int j = 0; j < 3; ++j) acc[j][0] = acc[j][1] = 0.0f;
+          for (uint32_t c0 = 0; c0 < ncr; c0 += 32) {  // same trip count in every lane
+            const uint32_t c = c0 + lane;
+            const bool ok = c < ncr;
+            const uint32_t blk = ok ? c >> 1 : 0;
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 h0 = ok ? lds16(hq_st + 16 * c) : z;
+            const float hs0 = hs_st[blk];
+            uint4 h1 = z;
+            float hs1 = 0.0f;
+            if (nr > 1) {
+              h1 = ok ? lds16(hq_st + K + 16 * c) : z;
+              hs1 = hs_st[kb + blk];
+            }
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              const int m = m0 + j * kConsumerWarps;
+              const bool live = ok && m < dsc.count;
+              const uint4 wd = live ? lds16(qc + (size_t)m * K + 16 * c) : make_uint4(0, 0, 0, 0);
+              const float sw = live ? half_bits_to_float(scl[(size_t)m * kb + blk]) : 0.0f;
+              int p0 = dot16(wd, h0);
+              p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+              if (even) acc[j][0] = __fmaf_rn((float)p0, sw * hs0, acc[j][0]);
+              if (nr > 1) {
+                int p1 = dot16(wd, h1);
+                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                if (even) acc[j][1] = __fmaf_rn((float)p1, sw * hs1, acc[j][1]);
+              }
+            }
+          }
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const int m = m0 + j * kConsumerWarps;
+            const float v0 = warp_sum(acc[j][0]);
+            const float v1 = nr > 1 ? warp_sum(acc[j][1]) : 0.0f;
+            if (lane == 0 && m < dsc.count) {
+              a.o[slot0 * d + dsc.first + m] = v0;
+              if (nr > 1) a.o[slot1 * d + dsc.first + m] = v1;
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // the producer counts the contribution
+        n_c += 1;
+        c_c += clock64() - t_got;
+      }
+    }
+    if (tr && tid == 0) {
+      tr[kTrConsEnd] = global_ns();
+      tr[kTrWaitFull] = c_wait_full;
+      tr[kTrComputeB] = c_b;
+      tr[kTrComputeC] = c_c;
+      tr[kTrStagesB] = n_b;
+      tr[kTrStagesC] = n_c;
     }
   }
-  consumer_sync();
 
-  bool route_seen = blockIdx.x == 0;
-  uint32_t g = 0;
-  for (;; ++g) {
-    const uint32_t st = g % NS, use = g / NS;
-    if (!mbar_wait(&full[st], use & 1u, a.wait_cycles)) {
-      report_timeout(a, 3, g);
-      return;
+  // ============================ exit: combine the chunks this CTA completed last
+  __syncthreads();
+  const long long t_comb = clock64();
+  // owned chunks: every thread checks a share of owner[] (one L2 round trip),
+  // the matches go to a shared list
+  int *owned = s_idx + 64;  // the producer's plan arrays are no longer needed
+  volatile int *n_owned = s_misc + 3;
+  if (tid == 0) *n_owned = 0;
+  __syncthreads();
+  for (uint32_t c = tid; c < a.n_chunks; c += kThreads)
+    if (__ldcg(&SV.owner[c]) == blockIdx.x + 1) {
+      const int i = atomicAdd((int *)n_owned, 1);
+      if (i < 4 * 64) owned[i] = (int)c;
+      else atomicOr(a.err, kErrTimeout | (1u << 15));  // cannot happen: <= 4*64 down stages fit
     }
-    const StageDesc dsc = desc[st];
-    if (dsc.kind == kKindEnd) return;
-    const uint8_t *buf = stages + (size_t)st * a.stage_bytes;
-    const int nr = dsc.nrows;
-    if (dsc.kind == kKindB) {
-      // ---- gate/up: warp w owns feature first + w
-      const int8_t *gc = (const int8_t *)buf + (size_t)warp * d;
-      const int8_t *uc = (const int8_t *)buf + (size_t)kBFeat * d + (size_t)warp * d;
-      const uint16_t *gsc = (const uint16_t *)(buf + 2 * kBFeat * d) + (size_t)warp * nb;
-      const uint16_t *usc = (const uint16_t *)(buf + 2 * kBFeat * d) + (size_t)kBFeat * nb +
-                            (size_t)warp * nb;
-      float accg[kMaxT] = {0.0f, 0.0f}, accu[kMaxT] = {0.0f, 0.0f};
-      for (uint32_t b = lane; b < nb; b += 32) {
-        const W8 wg = lds32(gc + 32 * b), wu = lds32(uc + 32 * b);
-        const float sg = half_bits_to_float(gsc[b]), su = half_bits_to_float(usc[b]);
-#pragma unroll
-        for (int r = 0; r < kMaxT; ++r) {
-          if (r < nr) {
-            const int t = dsc.tok[r];
-            const W8 xv = lds32(xq_s + (size_t)t * d + 32 * b);
-            const float xsc = xs_s[t * nb + b];
-            accg[r] = __fmaf_rn((float)dot8(wg, xv), sg * xsc, accg[r]);
-            accu[r] = __fmaf_rn((float)dot8(wu, xv), su * xsc, accu[r]);
-          }
+  __syncthreads();
+  if (warp < kConsumerWarps && !s_misc[0]) {
+    for (int oi = 0; oi < min(*n_owned, 4 * 64); ++oi) {
+      const uint32_t c = (uint32_t)owned[oi];
+      const uint32_t first = c * a.c_rows, count = min(a.c_rows, d - first);
+      // y = o_shared + sum_j w_j o_j, shared first, then slots in order
+      for (uint32_t i = tid; i < T * count; i += kConsumerWarps * 32) {
+        const uint32_t t = i / count, m = first + i % count;
+        float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
+        for (uint32_t j = 0; j < a.k; ++j) {
+          const int p = __ldcg(a.pos + t * a.k + j);
+          acc = __fmaf_rn(__ldcg(a.w + t * a.k + j), __ldcg(a.o + (size_t)p * d + m), acc);
         }
-      }
-#pragma unroll
-      for (int r = 0; r < kMaxT; ++r) {
-        const float gv = warp_sum(accg[r]), uv = warp_sum(accu[r]);
-        if (lane == 0 && r < nr)
-          h_tile[r * kBItemFeat + (dsc.first - dsc.item_first) + warp] =
-              __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (dsc.sub == kBItemFeat / kBFeat - 1) {
-        // the item's 32 features are done: requantise h (one warp per row)
-        consumer_sync();
-        if (warp < nr) {
-          const float v = h_tile[warp * kBItemFeat + lane];
-          float amax = fabsf(v);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          const float sc = __fdiv_rn(amax, 127.0f);
-          const size_t slot = (size_t)dsc.slot[warp];
-          a.hq[slot * fmax + dsc.item_first + lane] = (int8_t)quant_one(v, sc);
-          if (lane == 0) a.hs[slot * (fmax / 32) + dsc.item_first / 32] = sc;
-          __threadfence();
-        }
-        consumer_sync();
-        if (tid == 0) atomicAdd(&a.sync[4 + dsc.e], 1u);
-      }
-    } else {
-      // ---- down: wait for the expert's h, stage its codes, dot, combine
-      const bool sh = dsc.e == (int)a.E;
-      const uint32_t K = sh ? a.fs : a.f, kb = K / 32;
-      if (tid == 0) {
-        if (!wait_geq(&a.sync[4 + dsc.e], K / kBItemFeat, a.wait_cycles)) {
-          report_timeout(a, 4, ((uint32_t)dsc.e << 16) | __ldcg(&a.sync[4 + dsc.e]));
-          s_misc[0] = 1;
-        } else if (!route_seen && !wait_geq(&a.sync[1], 1u, a.wait_cycles)) {
-          report_timeout(a, 5, 0);
-          s_misc[0] = 1;
-        }
-      }
-      consumer_sync();
-      route_seen = true;
-      if (s_misc[0]) return;  // the producer sees the flag and ends too
-      for (int r = 0; r < nr; ++r) {
-        const size_t slot = (size_t)dsc.slot[r];
-        const int4 *src = (const int4 *)(a.hq + slot * fmax);
-        int4 *dst = (int4 *)(hq_s + (size_t)r * fmax);
-        for (uint32_t i = tid; i < K / 16; i += kConsumerWarps * 32) dst[i] = __ldcg(src + i);
-        for (uint32_t i = tid; i < kb; i += kConsumerWarps * 32)
-          hs_s[r * (fmax / 32) + i] = __ldcg(a.hs + slot * (fmax / 32) + i);
-      }
-      consumer_sync();
-      const int8_t *qc = (const int8_t *)buf;
-      const uint16_t *sc = (const uint16_t *)(buf + (size_t)dsc.count * K);
-      for (int m = warp; m < dsc.count; m += kConsumerWarps) {
-        float acc[kMaxT] = {0.0f, 0.0f};
-        for (uint32_t b = lane; b < kb; b += 32) {
-          const W8 wd = lds32(qc + (size_t)m * K + 32 * b);
-          const float sw = half_bits_to_float(sc[(size_t)m * kb + b]);
-#pragma unroll
-          for (int r = 0; r < kMaxT; ++r)
-            if (r < nr) {
-              const W8 hv = lds32(hq_s + (size_t)r * fmax + 32 * b);
-              acc[r] = __fmaf_rn((float)dot8(wd, hv), sw * hs_s[r * (fmax / 32) + b], acc[r]);
-            }
-        }
-#pragma unroll
-        for (int r = 0; r < kMaxT; ++r) {
-          const float v = warp_sum(acc[r]);
-          if (lane == 0 && r < nr) a.o[(size_t)dsc.slot[r] * d + dsc.first + m] = v;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      __threadfence();
-      consumer_sync();
-      if (tid == 0) {
-        const uint32_t old = atomicAdd(&a.sync[4 + a.E + 1 + dsc.item_first], 1u);
-        const int last = old + 1 == (uint32_t)dsc.n_contrib;
-        if (last) __threadfence();
-        s_misc[1] = last;
-      }
-      consumer_sync();
-      if (s_misc[1]) {
-        // combine this chunk for every token: shared first, then slots in order
-        for (uint32_t i = tid; i < T * (uint32_t)dsc.count; i += kConsumerWarps * 32) {
-          const uint32_t t = i / dsc.count, m = dsc.first + i % dsc.count;
-          float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
-          for (uint32_t j = 0; j < a.k; ++j) {
-            const int p = __ldcg(a.pos + t * a.k + j);
-            acc = __fmaf_rn(__ldcg(a.w + t * a.k + j), __ldcg(a.o + (size_t)p * d + m), acc);
-          }
-          a.y[(size_t)t * d + m] = acc;
-        }
+        a.y[(size_t)t * d + m] = acc;
       }
     }
+  }
+  if (tr && tid == 0) tr[kTrCombine] += clock64() - t_comb;
+  __syncthreads();
+  // the last CTA out zeroes the counters for the next call
+  if (tid == 0) s_misc[1] = atom_acq_rel_add(SV.done, 1u) + 1 == gridDim.x;
+  __syncthreads();
+  if (s_misc[1]) {
+    for (uint32_t i = tid; i < SV.n_clear; i += kThreads)
+      if (i != 2 && i != 3) a.sync[i] = 0u;
   }
 }
 
@@ -639,19 +981,22 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (D.flags & (MOE_FLAG_DEBUG_TAPS | MOE_FLAG_FORCE_GEMV)) return false;
   if (D.flags & MOE_FLAG_FORCE_TC) return false;
   if (D.d % 256 || D.f % 256 || D.f_shared % 256) return false;
+  if (D.d % (32 * kKSplit * 2)) return false;  // whole, even chunk counts per K part
   if (c.R > 64) return false;
   const uint32_t d = D.d, fmax = c.fmax;
   const size_t b_bytes = (size_t)kBFeat * 2 * (d + d / 16);
   const uint32_t row_c = fmax + fmax / 16;
-  uint32_t c_rows = (uint32_t)(b_bytes / row_c) / 8 * 8;
+  // a down stage also carries the expert's h codes and scales (up to 2 rows)
+  const size_t h_bytes = (size_t)kMaxT * (fmax + (fmax / 32) * 4);
+  if (b_bytes <= h_bytes) return false;
+  uint32_t c_rows = (uint32_t)((b_bytes - h_bytes) / row_c) / 8 * 8;
   if (c_rows == 0) return false;
   if (c_rows > d) c_rows = d;
-  const size_t stage = ((b_bytes > (size_t)c_rows * row_c ? b_bytes : (size_t)c_rows * row_c) +
-                        127) / 128 * 128;
+  const size_t stage = (b_bytes + 127) / 128 * 128;
   const size_t rest = (size_t)kMaxT * d + (size_t)kMaxT * (d / 32) * 4 + (size_t)kMaxT * fmax +
-                      (size_t)kMaxT * (fmax / 32) * 4 + kMaxT * kBItemFeat * 4 +
-                      kMaxStages * sizeof(StageDesc) + 2 * kMaxStages * 8 + 16 + 64 * 4 +
-                      64 * 4 + 128;
+                      (size_t)kMaxT * (fmax / 32) * 4 + 2 * kBItemFeat * kKSplit * kMaxT * 2 * 4 +
+                      kMaxStages * sizeof(StageDesc) + 2 * kMaxStages * 8 + 16 + 6 * 64 * 4 +
+                      128;
   int dev = 0, max_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -660,8 +1005,11 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if ((size_t)max_smem < rest + 2 * stage) return false;
   uint32_t ns = (uint32_t)(((size_t)max_smem - rest) / stage);
   if (ns > (uint32_t)kMaxStages) ns = kMaxStages;
+  // CTA 0 routes with the stage buffers as scratch (scores + sigmoids, then 128 ints)
+  if ((size_t)c.T * D.n_expert * 8 + 512 > (size_t)ns * stage) return false;
   fp->c_rows = c_rows;
   fp->n_chunks = (d + c_rows - 1) / c_rows;
+  if (4 + D.n_expert + 1 + 2 * fp->n_chunks + 1 > kSyncInts) return false;
   fp->n_stages = ns;
   fp->stage_bytes = (uint32_t)stage;
   fp->smem = rest + ns * stage;
@@ -669,13 +1017,9 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
 }
 }  // namespace
 
-size_t fused_sync_ints(const moe_desc *d) { return 4 + (size_t)d->n_expert + 1 + (size_t)d->d / 8; }
-
-// counters start at zero every call; the error word is cleared with them
-cudaError_t zero_decode_fused(const Ctx &c) {
-  cudaError_t e = cudaMemsetAsync(c.ws + c.L.sync, 0, fused_sync_ints(&c.desc) * 4, c.stream);
-  if (e != cudaSuccess) return e;
-  return cudaMemsetAsync(c.ws + c.L.err, 0, 4, c.stream);
+size_t fused_sync_ints(const moe_desc *d) {
+  (void)d;
+  return kSyncInts;
 }
 
 bool fused_eligible(const Ctx &c) {
@@ -733,7 +1077,9 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.stage_bytes = fp.stage_bytes;
   a.stall_test = (D.flags & MOE_FLAG_TEST_STALL) ? 1 : 0;
   a.wait_cycles = a.stall_test ? kStallTestCycles : kWaitCycles;
-  cudaError_t e = cudaFuncSetAttribute(k_decode_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  a.trace = (D.flags & MOE_FLAG_TRACE) ? (unsigned long long *)(c.ws + c.L.trace) : nullptr;
+  auto kern = c.T == 1 ? k_decode_fused<1> : k_decode_fused<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)fp.smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
@@ -746,7 +1092,7 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, k_decode_fused, a);
+  return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
 }  // namespace moe

@@ -54,14 +54,14 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
   const size_t fmax = d->f > d->f_shared ? d->f : d->f_shared;
   size_t p = 0;
   L.err = p;
-  p = align_up(p + sizeof(uint32_t));
+  L.sync = 256;
+  p = align_up(MOE_WS_FIXED_BYTES);
   L.idx = p; p = align_up(p + R * 4);
   L.w = p; p = align_up(p + R * 4);
   L.off = p; p = align_up(p + (size_t)(d->n_expert + 1) * 4);
   L.perm = p; p = align_up(p + R * 4);
   L.pos = p; p = align_up(p + R * 4);
   L.plan = p; p = align_up(p + PlanView::ints(d->n_expert) * 4);
-  L.sync = p; p = align_up(p + fused_sync_ints(d) * 4);
   L.xq = p; p = align_up(p + (size_t)T * d->d);
   L.xs = p; p = align_up(p + (size_t)T * (d->d / 32) * 4);
   L.h = p; p = align_up(p + slots * fmax * 4);
@@ -74,6 +74,10 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
     L.tap_dn = p; p = align_up(p + slots * kNTap * (fmax / 32) * 4);
   } else {
     L.tap_gu = L.tap_dn = 0;
+  }
+  L.trace = 0;
+  if (d->flags & MOE_FLAG_TRACE) {
+    L.trace = p; p = align_up(p + (size_t)1024 * 20 * 8);
   }
   L.total = p;
   return L;
@@ -112,8 +116,8 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
 const char *const kStageNames[] = {"route", "permute", "plan",  "quant_x",
                                    "gateup", "requant", "down", "combine"};
 constexpr uint32_t kNumStages = sizeof(kStageNames) / sizeof(kStageNames[0]);
-const char *const kFusedStageNames[] = {"zero_sync", "decode_fused"};
-constexpr uint32_t kNumFusedStages = 2;
+const char *const kFusedStageNames[] = {"decode_fused"};
+constexpr uint32_t kNumFusedStages = 1;
 
 // optional timing markers: events[i] after stage i-1
 struct Marks {
@@ -174,10 +178,8 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   cudaError_t e;
   if (T > 0 && fused_eligible(c)) {
     if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
-    if ((e = zero_decode_fused(c)) != cudaSuccess) return from_cuda(e);
-    if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
     if ((e = launch_decode_fused(c, x, logits, bias, y)) != cudaSuccess) return from_cuda(e);
-    if ((e = mk.mark(2)) != cudaSuccess) return from_cuda(e);
+    if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
     return MOE_OK;
   }
   if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);

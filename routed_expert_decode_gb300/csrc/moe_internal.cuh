@@ -186,7 +186,6 @@ cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, flo
 // fused single-kernel decode (T <= 2): decode_fused.cu
 size_t fused_sync_ints(const moe_desc *d);
 bool fused_eligible(const Ctx &c);
-cudaError_t zero_decode_fused(const Ctx &c);
 cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logits,
                                 const float *bias, float *y);
 

@@ -13,13 +13,15 @@
 //    fit (moe_workspace_size(desc, T) > 16 MiB) is rejected with
 //    MOE_ERR_WORKSPACE before anything is launched;
 //  * every call on a device uses the same array and it keeps whatever the last
-//    call left there.  The only state that must start at zero -- the device
-//    error word -- is reset by the first kernel of each call; every other
-//    region is written before it is read.  Calls that overlap on the GPU (two
-//    streams, or two host threads) race on the array: serialise them;
+//    call left there.  What must start at zero -- the error word and the fused
+//    decode kernel's counters -- is zero-filled at set-up and left zeroed by
+//    every call (the error word is reset at the start of each call); every
+//    other region is written before it is read.  Calls that overlap on the GPU
+//    (two streams, or two host threads) race on the array: serialise them;
 //  * the first call on each device looks up the array's device address
-//    (cudaGetSymbolAddress, with that device current) and caches it; make that
-//    first call before any stream capture starts.
+//    (cudaGetSymbolAddress, with that device current), caches it and zero-fills
+//    the array's fixed head on the call's stream; make that first call before
+//    any stream capture starts.
 // Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 #include <mutex>
 
@@ -36,7 +38,9 @@ std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on the current device (looked up once).
-cudaError_t scratch_address(void **out) {
+// The first lookup on a device also zero-fills the workspace's fixed head (the
+// error word and the counters that every call leaves zeroed), on `stream`.
+cudaError_t scratch_address(void **out, cudaStream_t stream) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -45,6 +49,8 @@ cudaError_t scratch_address(void **out) {
   if (!g_scratch_addr[dev]) {
     void *p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(p, 0, MOE_WS_FIXED_BYTES, stream);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
   }
@@ -65,7 +71,7 @@ extern "C" moe_status moe_layer_noalloc(const moe_desc *desc, const moe_weights 
     return MOE_ERR_WORKSPACE;
   }
   void *scratch = nullptr;
-  const cudaError_t e = scratch_address(&scratch);
+  const cudaError_t e = scratch_address(&scratch, (cudaStream_t)stream);
   if (e != cudaSuccess) {
     moe::set_last_error(cudaGetErrorName(e));
     return MOE_ERR_CUDA;

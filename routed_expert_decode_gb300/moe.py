@@ -31,6 +31,11 @@ FLAG_DEBUG_TAPS = 0x1
 FLAG_FORCE_GEMV = 0x2
 FLAG_FORCE_TC = 0x4
 FLAG_TEST_STALL = 0x8
+FLAG_TRACE = 0x10
+TRACE_FIELDS = ("start_ns", "xq_done_ns", "first_stage_ns", "wait_full_cyc", "wait_ready_cyc",
+                "stages_b", "stages_c", "cons_end_ns", "wait_empty_cyc", "wait_route_cyc",
+                "items", "compute_b_cyc", "compute_c_cyc", "combine_cyc", "route_done_ns",
+                "prod_end_ns", "route_loaded_ns", "route_topk_ns", "route_perm_ns", "spare")
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -52,7 +57,7 @@ class MoeWeights(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "sync", "tap_gu", "tap_dn", "err", "total")
+                 "sync", "tap_gu", "tap_dn", "trace", "err", "total")
 
 
 class MoeWsLayout(ctypes.Structure):

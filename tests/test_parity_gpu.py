@@ -194,7 +194,7 @@ FUSED = [
     ("fused_e64_t2", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 2),
     ("fused_noshared_t2", _spec(E=32, k=8, d=768, f=512, f_shared=0), 2),
     ("fused_wide_shared_t1", _spec(E=384, k=6, d=1024, f=256, f_shared=512, s=1.5), 1),
-    ("fused_k32_t2", _spec(E=1024, k=32, d=256, f=256, f_shared=256), 2),
+    ("fused_k32_t2", _spec(E=1024, k=32, d=1024, f=256, f_shared=256), 2),
 ]
 
 
