@@ -132,6 +132,8 @@ typedef struct {
   size_t sync;                   /* counters of the fused decode kernel (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
   size_t trace;                  /* uint64 [1024][20] (MOE_FLAG_TRACE) */
+  size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales
+                                    [R+T][d/32], fp16 h codes [R+T][fmax], in slot order */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
   uint32_t n_tap;                /* tapped features per row (gate/up and down) */
@@ -192,7 +194,7 @@ const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i);
  * held by every GPU that loads the library until the process exits.
  * - Calls whose moe_workspace_size(desc, T) exceeds it return
  *   MOE_ERR_WORKSPACE (moe_last_error says why) and launch nothing.  For the
- *   E=256 / d=6144 / f=2048 layer with a shared expert that is T <= 48.
+ *   E=256 / d=6144 / f=2048 layer with a shared expert that is T <= 32.
  * - All calls on a device share the array, which keeps the last call's
  *   contents; what must start at zero (error word, counters) is zero-filled
  *   at set-up and left zeroed by every call.  Calls that overlap on the GPU

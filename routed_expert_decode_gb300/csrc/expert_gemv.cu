@@ -275,8 +275,12 @@ cudaError_t run_down(const Ctx &c, const DNArgs &a) {
   return cudaGetLastError();
 }
 
-// rows per pass: an expert has at most T rows
-int maxr_for(uint32_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16; }
+// rows per pass: an expert has at most T rows, and at most kTcMinRows when the
+// tensor-core path takes the larger experts
+int maxr_for(uint32_t T, bool tc) {
+  if (tc && T > kTcMinRows) T = kTcMinRows;
+  return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
+}
 
 template <int FMT, int MAXR>
 cudaError_t gu_taps(const Ctx &c, const GUArgs &a, bool taps) {
@@ -289,7 +293,7 @@ cudaError_t dn_taps(const Ctx &c, const DNArgs &a, bool taps) {
 
 template <int FMT>
 cudaError_t gu_maxr(const Ctx &c, const GUArgs &a, bool taps) {
-  switch (maxr_for(c.T)) {
+  switch (maxr_for(c.T, c.L.xperm != 0 && tc_supported(c.desc))) {
     case 1: return gu_taps<FMT, 1>(c, a, taps);
     case 2: return gu_taps<FMT, 2>(c, a, taps);
     case 4: return gu_taps<FMT, 4>(c, a, taps);
@@ -299,7 +303,7 @@ cudaError_t gu_maxr(const Ctx &c, const GUArgs &a, bool taps) {
 }
 template <int FMT>
 cudaError_t dn_maxr(const Ctx &c, const DNArgs &a, bool taps) {
-  switch (maxr_for(c.T)) {
+  switch (maxr_for(c.T, c.L.xperm != 0 && tc_supported(c.desc))) {
     case 1: return dn_taps<FMT, 1>(c, a, taps);
     case 2: return dn_taps<FMT, 2>(c, a, taps);
     case 4: return dn_taps<FMT, 4>(c, a, taps);

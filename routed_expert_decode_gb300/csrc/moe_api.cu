@@ -75,6 +75,12 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
   } else {
     L.tap_gu = L.tap_dn = 0;
   }
+  L.xperm = L.xsperm = L.hperm = 0;
+  if (tc_possible(*d, T)) {
+    L.xperm = p; p = align_up(p + slots * d->d * 2);
+    L.xsperm = p; p = align_up(p + slots * (d->d / 32) * 4);
+    L.hperm = p; p = align_up(p + slots * fmax * 2);
+  }
   L.trace = 0;
   if (d->flags & MOE_FLAG_TRACE) {
     L.trace = p; p = align_up(p + (size_t)1024 * 20 * 8);
@@ -113,8 +119,9 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
   return c;
 }
 
-const char *const kStageNames[] = {"route", "permute", "plan",  "quant_x",
-                                   "gateup", "requant", "down", "combine"};
+const char *const kStageNames[] = {"route",   "permute",   "plan", "quant_x", "tc_prepare",
+                                   "gateup",  "requant",   "gateup_tc", "down", "down_tc",
+                                   "combine"};
 constexpr uint32_t kNumStages = sizeof(kStageNames) / sizeof(kStageNames[0]);
 const char *const kFusedStageNames[] = {"decode_fused"};
 constexpr uint32_t kNumFusedStages = 1;
@@ -138,7 +145,7 @@ struct Marks {
   }
 };
 
-// FFN stages shared by moe_ffn and moe_layer (stage numbers 2..7)
+// FFN stages shared by moe_ffn and moe_layer (stage numbers 2..10)
 moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float *w,
                    const int32_t *off, const int32_t *perm, const int32_t *pos, float *y,
                    const Marks &mk) {
@@ -148,14 +155,23 @@ moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float
   if ((e = mk.mark(3)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_quant_x(c, x)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(4)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_gateup(c, perm)) != cudaSuccess) return from_cuda(e);
+  // tensor-core experts possible for this desc and T
+  const bool tc = c.L.xperm != 0 && tc_supported(c.desc);
+  if (tc && (e = launch_tc_prepare(c, perm)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(5)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_requant_h(c)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_gateup(c, perm)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(6)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_down(c)) != cudaSuccess) return from_cuda(e);
+  // requantises h of every slot; the tensor path then writes its own slots' codes
+  if ((e = launch_requant_h(c)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(7)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_combine(c, w, pos, y)) != cudaSuccess) return from_cuda(e);
+  if (tc && (e = launch_tc(c, 2)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(8)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_down(c)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(9)) != cudaSuccess) return from_cuda(e);
+  if (tc && (e = launch_tc(c, 1)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(10)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_combine(c, w, pos, y)) != cudaSuccess) return from_cuda(e);
+  if ((e = mk.mark(11)) != cudaSuccess) return from_cuda(e);
   return MOE_OK;
 }
 

@@ -22,22 +22,35 @@ constexpr uint32_t kErrTimeout = 4u;    // a bounded wait gave up
 
 // ---------------------------------------------------------------- plan layout
 // int32 array in the workspace describing the active experts of one call.
-//   [0] U (active experts incl. the shared one)   [1] gate/up work items
-//   [2] down work items   [3] largest routed row count   [4..7] reserved
-//   act_e[E+1]   expert id per active slot u (E = the shared expert)
-//   act_row0[E+1] first FFN slot of expert u; act_rows[E+1] its row count
-//   item_gu[E+2]  exclusive prefix of gate/up items (features) per u
+//   [0] U (experts on the dp4a path, incl. the shared one if there)
+//   [1] gate/up work items  [2] down work items  [3] largest routed row count
+//   [4] 1 once the routing arrays were validated
+//   [5] experts on the tensor-core path  [6] their gate/up tiles  [7] down tiles
+//   act_e / act_row0 / act_rows [E+1]: dp4a experts (id E = shared), first slot, rows
+//   item_gu[E+2]: exclusive prefix of dp4a gate/up items (features)
+//   tc_e / tc_row0 / tc_rows [E+1]: tensor-core experts
+//   tc_tile_gu / tc_tile_dn [E+2]: exclusive prefix of their 128x64 tiles
 struct PlanView {
   int *hdr, *act_e, *act_row0, *act_rows, *item_gu;
+  int *tc_e, *tc_row0, *tc_rows, *tc_tile_gu, *tc_tile_dn;
   __host__ __device__ PlanView(int *base, uint32_t E) {
     hdr = base;
     act_e = base + 8;
     act_row0 = act_e + (E + 1);
     act_rows = act_row0 + (E + 1);
     item_gu = act_rows + (E + 1);
+    tc_e = item_gu + (E + 2);
+    tc_row0 = tc_e + (E + 1);
+    tc_rows = tc_row0 + (E + 1);
+    tc_tile_gu = tc_rows + (E + 1);
+    tc_tile_dn = tc_tile_gu + (E + 2);
   }
-  __host__ __device__ static size_t ints(uint32_t E) { return 8 + 4 * (size_t)(E + 2); }
+  __host__ __device__ static size_t ints(uint32_t E) { return 8 + 9 * (size_t)(E + 2); }
 };
+
+// rows per expert above which an expert runs on the tensor-core path
+constexpr uint32_t kTcMinRows = 4;
+constexpr uint32_t kTcTileM = 128, kTcTileN = 64;
 
 // ---------------------------------------------------------------- spec-exp
 // e^x, bit-reproducible on any IEEE fp32 machine: clamp to [-86, 88];
@@ -177,6 +190,11 @@ cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32
                            int32_t *pos, uint32_t *err);
 cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
                         const int32_t *perm, const int32_t *pos, uint32_t *err);
+// tensor-core path (expert_tc.cu)
+bool tc_supported(const moe_desc &D);
+bool tc_possible(const moe_desc &D, uint32_t T);
+cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm);
+cudaError_t launch_tc(const Ctx &c, int mat);
 cudaError_t launch_quant_x(const Ctx &c, const float *x);
 cudaError_t launch_gateup(const Ctx &c, const int32_t *perm);
 cudaError_t launch_requant_h(const Ctx &c);

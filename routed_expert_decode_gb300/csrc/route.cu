@@ -160,16 +160,36 @@ __global__ void __launch_bounds__(kPermThreads)
   }
 }
 
+// block-wide exclusive scan of one int per thread (kPlanThreads threads);
+// returns the exclusive prefix, *total gets the block sum
+constexpr int kPlanThreads = 1024;
+
+__device__ int block_excl_scan(int v, int *scan, int *total) {
+  const int tid = threadIdx.x;
+  scan[tid] = v;
+  __syncthreads();
+  for (int o = 1; o < kPlanThreads; o <<= 1) {
+    const int add = tid >= o ? scan[tid - o] : 0;
+    __syncthreads();
+    scan[tid] += add;
+    __syncthreads();
+  }
+  const int incl = scan[tid];
+  *total = scan[kPlanThreads - 1];
+  __syncthreads();
+  return incl - v;
+}
+
 // Work plan from off[] (1 CTA).  Validates off, perm, pos and idx against one
 // another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
 // no work (so no kernel indexes with untrusted values).  Otherwise it lists the
-// active experts in ascending order, the shared expert last.
-constexpr int kPlanThreads = 1024;
-
+// active experts, ascending, the shared expert last, split between the dp4a
+// path and the tensor-core path (rows > tc_min_rows; every row with force_tc).
 __global__ void __launch_bounds__(kPlanThreads)
     k_plan(const int32_t *__restrict__ off, const int32_t *__restrict__ idx,
            const int32_t *__restrict__ perm, const int32_t *__restrict__ pos, uint32_t T,
-           uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int *plan, uint32_t *err) {
+           uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int tc_mode,
+           uint32_t tc_min_rows, int *plan, uint32_t *err) {
   __shared__ int scan[kPlanThreads];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -188,6 +208,7 @@ __global__ void __launch_bounds__(kPlanThreads)
       atomicOr(err, kErrBadOffsets);
       for (int i = 0; i < 8; ++i) P.hdr[i] = 0;  // hdr[4] = 0: nothing validated
       P.item_gu[0] = 0;
+      P.tc_tile_gu[0] = P.tc_tile_dn[0] = 0;
     }
     return;
   }
@@ -212,51 +233,87 @@ __global__ void __launch_bounds__(kPlanThreads)
       atomicOr(err, kErrBadIndex);
       for (int i = 0; i < 8; ++i) P.hdr[i] = 0;
       P.item_gu[0] = 0;
+      P.tc_tile_gu[0] = P.tc_tile_dn[0] = 0;
     }
     return;
   }
-  // active routed experts, ascending
-  int carry = 0, maxrows = 0;
+  auto on_tc = [&](int rows) -> bool {
+    if (tc_mode == 0 || rows <= 0) return false;
+    return tc_mode == 2 ? true : (uint32_t)rows > tc_min_rows;
+  };
+  const int ntile_n = (int)kTcTileN;
+  int ng = 0, ntc = 0, ntile_gu = 0, maxrows = 0, total;
   for (uint32_t base = 0; base < E; base += kPlanThreads) {
     const uint32_t e = base + tid;
     const int rows = e < E ? off[e + 1] - off[e] : 0;
-    const int flag = rows > 0 ? 1 : 0;
-    scan[tid] = flag;
-    __syncthreads();
-    for (int o = 1; o < kPlanThreads; o <<= 1) {
-      const int add = tid >= o ? scan[tid - o] : 0;
-      __syncthreads();
-      scan[tid] += add;
-      __syncthreads();
+    const bool tc = on_tc(rows);
+    const int gflag = rows > 0 && !tc ? 1 : 0, tflag = tc ? 1 : 0;
+    const int gu = ng + block_excl_scan(gflag, scan, &total);
+    const int gtotal = total;
+    const int tv = ntc + block_excl_scan(tflag, scan, &total);
+    const int ttotal = total;
+    const int tiles = tc ? (int)(f / kTcTileM) * ((rows + ntile_n - 1) / ntile_n) : 0;
+    const int tile0 = ntile_gu + block_excl_scan(tiles, scan, &total);
+    const int tiles_total = total;
+    if (gflag) {
+      P.act_e[gu] = (int)e;
+      P.act_row0[gu] = off[e];
+      P.act_rows[gu] = rows;
+      P.item_gu[gu] = gu * (int)f;
     }
-    if (flag) {
-      const int u = carry + scan[tid] - 1;
-      P.act_e[u] = (int)e;
-      P.act_row0[u] = off[e];
-      P.act_rows[u] = rows;
-      P.item_gu[u] = u * (int)f;
+    if (tflag) {
+      P.tc_e[tv] = (int)e;
+      P.tc_row0[tv] = off[e];
+      P.tc_rows[tv] = rows;
+      P.tc_tile_gu[tv] = tile0;
+      P.tc_tile_dn[tv] = (tile0 / (int)(f / kTcTileM)) * (int)(d / kTcTileM);
     }
-    carry += scan[kPlanThreads - 1];
-    __syncthreads();
+    ng += gtotal;
+    ntc += ttotal;
+    ntile_gu += tiles_total;
+    if (tid == 0)
+      for (uint32_t q = base; q < base + kPlanThreads && q < E; ++q)
+        maxrows = max(maxrows, off[q + 1] - off[q]);
   }
   if (tid == 0) {
-    for (uint32_t e = 0; e < E; ++e) maxrows = max(maxrows, off[e + 1] - off[e]);
-    int U = carry;
+    int U = ng;
     int items = U * (int)f;
+    int V = ntc;
+    int tiles_gu = ntile_gu;
+    const int mt = (int)(f / kTcTileM);
+    int tiles_dn = mt > 0 ? (ntile_gu / mt) * (int)(d / kTcTileM) : 0;
     if (fs > 0 && T > 0) {
-      P.act_e[U] = (int)E;
-      P.act_row0[U] = (int)R;
-      P.act_rows[U] = (int)T;
-      P.item_gu[U] = items;
-      items += (int)fs;
-      U += 1;
+      // the shared expert reads every token; the tensor path needs fs == f
+      if (on_tc((int)T) && fs == f) {
+        const int nt = ((int)T + ntile_n - 1) / ntile_n;
+        P.tc_e[V] = (int)E;
+        P.tc_row0[V] = (int)R;
+        P.tc_rows[V] = (int)T;
+        P.tc_tile_gu[V] = tiles_gu;
+        P.tc_tile_dn[V] = tiles_dn;
+        tiles_gu += (int)(fs / kTcTileM) * nt;
+        tiles_dn += (int)(d / kTcTileM) * nt;
+        V += 1;
+      } else {
+        P.act_e[U] = (int)E;
+        P.act_row0[U] = (int)R;
+        P.act_rows[U] = (int)T;
+        P.item_gu[U] = items;
+        items += (int)fs;
+        U += 1;
+      }
     }
     P.item_gu[U] = items;
+    P.tc_tile_gu[V] = tiles_gu;
+    P.tc_tile_dn[V] = tiles_dn;
     P.hdr[0] = U;
     P.hdr[1] = items;
     P.hdr[2] = U * (int)d;
     P.hdr[3] = maxrows;
     P.hdr[4] = 1;  // routing arrays validated: the combine may read pos[]
+    P.hdr[5] = V;
+    P.hdr[6] = tiles_gu;
+    P.hdr[7] = tiles_dn;
   }
 }
 
@@ -303,9 +360,13 @@ cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32
 cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
                              const int32_t *perm, const int32_t *pos, uint32_t *err) {
   int *plan = (int *)(c.ws + c.L.plan);
-  k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, c.desc.n_expert,
-                                           c.desc.top_k, c.desc.f, c.desc.f_shared, c.desc.d,
-                                           plan, err);
+  // tensor path: 0 off, 1 for experts with more than kTcMinRows rows, 2 forced
+  const moe_desc &D = c.desc;
+  int tc_mode = 0;
+  if (!(D.flags & MOE_FLAG_FORCE_GEMV) && tc_supported(D))
+    tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
+  k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, D.n_expert, D.top_k, D.f,
+                                           D.f_shared, D.d, tc_mode, kTcMinRows, plan, err);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,7 @@ class MoeWeights(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "sync", "tap_gu", "tap_dn", "trace", "err", "total")
+                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "err", "total")
 
 
 class MoeWsLayout(ctypes.Structure):

