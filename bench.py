@@ -79,14 +79,29 @@ def row_bytes(fmt: int, K: int) -> int:
     return (K if fmt == 0 else K // 4) + (K // 32) * 2
 
 
-def stage_bytes(spec, U_routed: int):
-    """Algorithmic HBM bytes of the selected experts' and the shared expert's weights."""
-    gu = U_routed * 2 * spec.f * row_bytes(spec.fmt, spec.d)
-    dn = U_routed * spec.d * row_bytes(spec.fmt, spec.f)
+def stage_bytes(spec, T: int, counts, tc_rows=None):
+    """Algorithmic HBM bytes per stage: each selected expert's weights and the
+    shared expert's, read once.  counts: rows per routed expert; experts with
+    more than tc_rows rows (None: no tensor path) are charged to the
+    tensor-core stages."""
+    out = {"gateup": 0, "down": 0, "gateup_tc": 0, "down_tc": 0}
+
+    def add(rows, fmt, f):
+        tc = "_tc" if tc_rows is not None and rows > tc_rows else ""
+        out["gateup" + tc] += 2 * f * row_bytes(fmt, spec.d)
+        out["down" + tc] += spec.d * row_bytes(fmt, f)
+
+    for c in counts:
+        if c > 0:
+            add(int(c), spec.fmt, spec.f)
     if spec.f_shared:
-        gu += 2 * spec.f_shared * row_bytes(0, spec.d)
-        dn += spec.d * row_bytes(0, spec.f_shared)
-    return {"gateup": gu, "down": dn, "total": gu + dn, "decode_fused": gu + dn}
+        add(T, 0, spec.f_shared)
+    out["total"] = sum(out.values())
+    out["decode_fused"] = out["total"]
+    return out
+
+
+ROOFLINE_STAGES = ("gateup", "down", "gateup_tc", "down_tc", "decode_fused")
 
 
 # ------------------------------------------------------------------ clocks
@@ -207,7 +222,7 @@ def run_ours(args):
     flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
 
     # unique routed experts per seed (setup pass through the library's router)
-    U_of = {}
+    U_of, counts_of = {}, {}
     off = torch.empty(spec.E + 1, dtype=torch.int32, device=dev)
     idx = torch.empty((T, spec.k), dtype=torch.int32, device=dev)
     wts = torch.empty((T, spec.k), dtype=torch.float32, device=dev)
@@ -215,7 +230,9 @@ def run_ours(args):
     pos = torch.empty(T * spec.k, dtype=torch.int32, device=dev)
     for s in seeds:
         moe.route(desc, dev_in[s][1], bias, idx, wts, off, perm, pos)
-        U_of[s] = int((off[1:] - off[:-1] > 0).sum().item())
+        counts_of[s] = (off[1:] - off[:-1]).cpu().tolist()
+        U_of[s] = sum(1 for c in counts_of[s] if c > 0)
+    tc_rows = moe.tc_min_rows(desc, T)
 
     names = moe.stage_names(desc, T)
     path = moe.layer_path(desc, T)
@@ -287,12 +304,12 @@ def run_ours(args):
 
     # roofline of the dominant kernel
     peak, peak_src = load_peaks()
-    bytes_steps = [stage_bytes(spec, U_of[s]) for s in step_seed]
+    bytes_steps = [stage_bytes(spec, T, counts_of[s], tc_rows) for s in step_seed]
     mean_stage = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(mean_stage, key=mean_stage.get)
     dom_bytes = sum(b.get(dom, 0) for b in bytes_steps) / K
     achieved = (dom_bytes / (mean_stage[dom] / 1e3) / 1e9
-                if dom in ("gateup", "down", "decode_fused") else None)
+                if dom in ROOFLINE_STAGES and dom_bytes > 0 else None)
     layer_gbs = sum(b["total"] for b in bytes_steps) / (sum(step_ms) / 1e3) / 1e9
 
     # end-to-end through the C ABI with host buffers: H2D inputs, layer, D2H output
@@ -419,15 +436,18 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
         stage = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
                  for j, nm in enumerate(names)}
         lay_off = lay.views(ws, T)["off"].cpu()
-        U = int((lay_off[1:] - lay_off[:-1] > 0).sum().item())
-        b = stage_bytes(spec, U)
+        counts = (lay_off[1:] - lay_off[:-1]).tolist()
+        U = sum(1 for c in counts if c > 0)
+        b = stage_bytes(spec, T, counts, moe.tc_min_rows(desc, T))
         ms = statistics.mean(step)
         out[name] = {"T": T, "unique_experts": U, "ms_per_step": round(ms, 4),
                      "tokens_per_s": round(T / (ms / 1e3), 1),
                      "algorithmic_bytes": b["total"],
                      "hbm_gbs": round(b["total"] / (ms / 1e3) / 1e9, 1),
                      "frac_of_measured": round(b["total"] / (ms / 1e3) / 1e9 / peak, 4),
-                     "stage_us": {k: round(v * 1e3, 1) for k, v in stage.items()}}
+                     "stage_us": {k: round(v * 1e3, 1) for k, v in stage.items()},
+                     "stage_gbs": {k: round(b[k] / (stage[k] / 1e3) / 1e9, 1)
+                                   for k in ROOFLINE_STAGES if k in stage and b[k] > 0}}
         assert moe.check_device_error(ws) == 0
     return out
 

@@ -134,6 +134,9 @@ typedef struct {
   size_t trace;                  /* uint64 [1024][20] (MOE_FLAG_TRACE) */
   size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales
                                     [R+T][d/32], fp16 h codes [R+T][fmax], in slot order */
+  size_t xt, ht;                 /* 2-bit routed weights: int8 x codes [T][d] and h codes
+                                    [R+T][fmax] with each 16-code group stored 4x4
+                                    transposed (byte 4i+j = code 4j+i); 0 otherwise */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
   uint32_t n_tap;                /* tapped features per row (gate/up and down) */
@@ -180,6 +183,14 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
 /* Which implementation moe_layer uses for (desc, T) on the current device:
  * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);
+
+/* Row threshold of the tensor-core path of moe_layer for (desc, T) on the
+ * current device: an expert (the shared expert included, with T rows) whose
+ * routed row count exceeds it runs its block dots on tcgen05 tensor cores,
+ * the rest on the dp4a GEMV.  -1 when no expert of such a call can take the
+ * tensor path (the fused decode path, 2-bit routed weights, dims not a
+ * multiple of 128, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
+int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);
 
 /* Name of stage i of that path (what moe_layer_timed's events bracket),
  * NULL past the last stage. */

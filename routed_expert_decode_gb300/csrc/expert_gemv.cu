@@ -22,7 +22,8 @@ struct GUArgs {
   uint32_t E, k, d, f, fs, R, fmax;
   const int8_t *gq, *uq, *sgq, *suq;
   const uint16_t *gs, *us, *sgs, *sus;
-  const int8_t *xq;
+  const int8_t *xq;  // x codes [T][d]
+  const int8_t *xt;  // 2-bit routed weights: x codes, 16-code groups transposed
   const float *xs;
   const int32_t *perm;
   float *h;
@@ -35,11 +36,29 @@ struct DNArgs {
   uint32_t E, d, f, fs, R, fmax;
   const int8_t *dq, *sdq;
   const uint16_t *ds, *sds;
-  const int8_t *hq;
+  const int8_t *hq;  // h codes [slots][fmax]
+  const int8_t *ht;  // 2-bit routed weights: h codes, 16-code groups transposed
   const float *hs;
   float *o;
   int32_t *tap;
 };
+
+// Shape of a warp work item: NF consecutive output features of one expert; a
+// pass over 32*J blocks gives lane l the blocks l, l+32, .., l+32(J-1) of each
+// of the NF rows of each of the NM matrices, all loaded before any use (about
+// 32 registers of weight codes in flight per lane, enough to cover HBM latency
+// with 16 warps per SM); one plan lookup per item.
+template <int FMT, int NM>
+__host__ __device__ constexpr int group_nf() {
+  return NM == 2 ? (FMT == MOE_FMT_Q2S ? 2 : 1) : (FMT == MOE_FMT_Q2S ? 4 : 2);
+}
+template <int FMT, int NM, int MAXR>
+__host__ __device__ constexpr int group_j() {
+  return FMT == MOE_FMT_Q2S && NM == 2 && MAXR < 4 ? 4 : 2;
+}
+
+template <int FMT, int MAXR>
+__host__ __device__ constexpr int min_ctas() { return FMT == MOE_FMT_Q8_0 && MAXR <= 2 ? 3 : 2; }
 
 __device__ __forceinline__ int find_slot(const int *prefix, int U, int item) {
   int lo = 0, hi = U;
@@ -66,20 +85,98 @@ __device__ __forceinline__ int tap_index(uint32_t n, uint32_t width) {
   return jt;
 }
 
-// g/u of feature n for rows [row0, row0 + nrows) of one expert; h = silu(g)*u
-template <int FMT, int MAXR, bool TAPS>
-__device__ __forceinline__ void gateup_feature(const GUArgs &a, const int8_t *gq,
-                                               const uint16_t *gs, const int8_t *uq,
-                                               const uint16_t *us, uint32_t width, int n,
-                                               int row0, int nrows, bool shared) {
+// The plan's dp4a expert list (act_e, act_row0, act_rows, item_gu: 4(E+1)+1
+// consecutive ints) copied into shared memory, so that the per-item lookups
+// cost no global round trips.
+struct SmemPlan {
+  const int *e, *row0, *rows, *item;
+  __device__ SmemPlan(int *sm, const PlanView &P, uint32_t E) {
+    const int n = 4 * (int)(E + 1) + 1;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = P.act_e[i];
+    __syncthreads();
+    e = sm;
+    row0 = sm + (E + 1);
+    rows = row0 + (E + 1);
+    item = rows + (E + 1);
+  }
+};
+inline size_t smem_plan_bytes(uint32_t E) { return sizeof(int) * (4 * (size_t)(E + 1) + 1); }
+
+// acc[m][f][r] += sum over the K/32 blocks b of
+//   dot(codes of row f of matrix m, codes of activation row r) * w-scale * x-scale
+// w[m] / ws[m]: first weight row / scale row of the group (rb bytes, nb scales
+// a row); activation row r at act + idx[r]*act_stride, its scales at
+// act_s + idx[r]*act_s_stride.  tap(m, f, r, b, dot) sees every block dot.
+template <int FMT, int NM, int NF, int J, int MAXR, typename Tap>
+__device__ __forceinline__ void group_dots(const int8_t *const (&w)[NM],
+                                           const uint16_t *const (&ws)[NM], size_t rb,
+                                           uint32_t nb, const int8_t *act, size_t act_stride,
+                                           const float *act_s, size_t act_s_stride,
+                                           const int (&idx)[MAXR], int nr,
+                                           float (&acc)[NM][NF][MAXR], Tap tap) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll 1
+  for (uint32_t b0 = 0; b0 < nb; b0 += 32 * J) {
+    // lanes past the last block load the last block again (valid memory, an
+    // L1/L2 hit) and add it with scale 0: no divergent branches, so that the
+    // unrolled loads stay in registers
+    WBlock<FMT> wb[NM][NF][J];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const uint32_t b = min(b0 + lane + 32 * j, nb - 1);
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int f = 0; f < NF; ++f) wb[m][f][j].load(w[m] + f * rb, b);
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const bool valid = b0 + lane + 32 * j < nb;
+      const uint32_t b = min(b0 + lane + 32 * j, nb - 1);
+      float sw[NM][NF];
+#pragma unroll
+      for (int m = 0; m < NM; ++m)
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+          sw[m][f] = valid ? half_bits_to_float(ws[m][(size_t)f * nb + b]) : 0.0f;
+          wb[m][f][j].prep();
+        }
+#pragma unroll
+      for (int r = 0; r < MAXR; ++r) {
+        if (r < nr) {  // warp-uniform
+          const W8 x = ld_cached32(act + (size_t)idx[r] * act_stride + 32 * b);
+          const float xsc = act_s[(size_t)idx[r] * act_s_stride + b];
+          const int sx = WBlock<FMT>::kNeedSum ? block_sum(x) : 0;
+#pragma unroll
+          for (int m = 0; m < NM; ++m)
+#pragma unroll
+            for (int f = 0; f < NF; ++f) {
+              const int v = wb[m][f][j].dot(x, sx);
+              acc[m][f][r] = __fmaf_rn((float)v, sw[m][f] * xsc, acc[m][f][r]);
+              if (valid) tap(m, f, r, b, v);
+            }
+        }
+      }
+    }
+  }
+}
+
+// g/u of features [n0, n0 + NF) for rows [row0, row0 + nrows) of one expert;
+// h = silu(g)*u.  Rows go in passes of at most MAXR (a later pass re-reads the
+// group's rows, which the first pass has just brought into L2).
+template <int FMT, int NF, int J, int MAXR, bool TAPS>
+__device__ __forceinline__ void gateup_group(const GUArgs &a, const int8_t *gq,
+                                             const uint16_t *gs, const int8_t *uq,
+                                             const uint16_t *us, uint32_t width, int n0,
+                                             int row0, int nrows, bool shared) {
   const int lane = threadIdx.x & 31;
   const uint32_t d = a.d, nb = d / 32;
   const size_t rb = row_bytes(FMT, d);
-  const int8_t *grow = gq + (size_t)n * rb;
-  const int8_t *urow = uq + (size_t)n * rb;
-  const uint16_t *gsr = gs + (size_t)n * nb;
-  const uint16_t *usr = us + (size_t)n * nb;
-  const int jt = tap_index<TAPS>((uint32_t)n, width);
+  const int8_t *const w[2] = {gq + (size_t)n0 * rb, uq + (size_t)n0 * rb};
+  const uint16_t *const ws[2] = {gs + (size_t)n0 * nb, us + (size_t)n0 * nb};
+  int jt[NF];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) jt[f] = tap_index<TAPS>((uint32_t)(n0 + f), width);
   for (int r0 = 0; r0 < nrows; r0 += MAXR) {
     const int nr = min(MAXR, nrows - r0);
     int tok[MAXR];
@@ -88,72 +185,79 @@ __device__ __forceinline__ void gateup_feature(const GUArgs &a, const int8_t *gq
       const int p = row0 + r0 + r;
       tok[r] = r < nr ? (shared ? p - (int)a.R : a.perm[p] / (int)a.k) : 0;
     }
-    float accg[MAXR], accu[MAXR];
+    float acc[2][NF][MAXR];
 #pragma unroll
-    for (int r = 0; r < MAXR; ++r) accg[r] = accu[r] = 0.0f;
-#pragma unroll 2
-    for (uint32_t b = lane; b < nb; b += 32) {
-      WBlock<FMT> wg, wu;
-      wg.load(grow, b);
-      wu.load(urow, b);
-      const float sg = half_bits_to_float(gsr[b]);
-      const float su = half_bits_to_float(usr[b]);
+    for (int m = 0; m < 2; ++m)
 #pragma unroll
-      for (int r = 0; r < MAXR; ++r) {
-        if (r < nr) {
-          const W8 x = ld_cached32(a.xq + (size_t)tok[r] * d + 32 * b);
-          const float xsc = a.xs[(size_t)tok[r] * nb + b];
-          const int ig = wg.dot(x);
-          const int iu = wu.dot(x);
-          accg[r] = __fmaf_rn((float)ig, sg * xsc, accg[r]);
-          accu[r] = __fmaf_rn((float)iu, su * xsc, accu[r]);
-          if (TAPS && jt >= 0) {
-            int32_t *tp = a.tap + ((size_t)(row0 + r0 + r) * 2 * kNTap + jt) * nb;
-            tp[b] = ig;
-            tp[(size_t)kNTap * nb + b] = iu;
-          }
-        }
-      }
-    }
+      for (int f = 0; f < NF; ++f)
+#pragma unroll
+        for (int r = 0; r < MAXR; ++r) acc[m][f][r] = 0.0f;
+    group_dots<FMT, 2, NF, J, MAXR>(
+        w, ws, rb, nb, FMT == MOE_FMT_Q2S ? a.xt : a.xq, d, a.xs, nb, tok, nr, acc,
+        [&](int m, int f, int r, uint32_t b, int v) {
+          if (TAPS && jt[f] >= 0)
+            a.tap[(((size_t)(row0 + r0 + r) * 2 + m) * kNTap + jt[f]) * nb + b] = v;
+        });
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
-      const float g = warp_sum(accg[r]);
-      const float u = warp_sum(accu[r]);
-      if (lane == 0 && r < nr) {
-        const float hv = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g))), u);
-        a.h[(size_t)(row0 + r0 + r) * a.fmax + n] = hv;
+      if (r < nr) {  // warp-uniform
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+          const float g = warp_sum(acc[0][f][r]);
+          const float u = warp_sum(acc[1][f][r]);
+          if (lane == f) {
+            const float hv = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g))), u);
+            a.h[(size_t)(row0 + r0 + r) * a.fmax + n0 + f] = hv;
+          }
+        }
       }
     }
   }
 }
 
 template <int FMT, int MAXR, bool TAPS>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, MAXR <= 2 ? 3 : 2) k_gateup(const GUArgs a) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>()))
+    k_gateup(const GUArgs a) {
+  constexpr int NF = group_nf<FMT, 2>(), J = group_j<FMT, 2, MAXR>();
+  constexpr int NFS = group_nf<MOE_FMT_Q8_0, 2>(), JS = group_j<MOE_FMT_Q8_0, 2, MAXR>();
+  static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
+  extern __shared__ int gsm[];
   PlanView P(const_cast<int *>(a.plan), a.E);
+  const SmemPlan S(gsm, P, a.E);
   const int U = P.hdr[0];
-  const int total = P.hdr[1];
+  const int groups = P.hdr[1] / NF;  // every width is a multiple of 32
   const int nwarps = gridDim.x * kWarpsPerCta;
-  for (int item = blockIdx.x * kWarpsPerCta + threadIdx.x / 32; item < total; item += nwarps) {
-    const int u = find_slot(P.item_gu, U, item);
-    const int e = P.act_e[u];
-    const int n = item - P.item_gu[u];
-    const int row0 = P.act_row0[u], nrows = P.act_rows[u];
+  for (int g = blockIdx.x * kWarpsPerCta + threadIdx.x / 32; g < groups; g += nwarps) {
+    const int item = g * NF;
+    const int u = find_slot(S.item, U, item);
+    const int e = S.e[u];
+    const int n0 = item - S.item[u];
+    const int row0 = S.row0[u], nrows = S.rows[u];
     if ((uint32_t)e == a.E) {
-      gateup_feature<MOE_FMT_Q8_0, MAXR, TAPS>(a, a.sgq, a.sgs, a.suq, a.sus, a.fs, n, row0,
-                                               nrows, true);
+#pragma unroll 1
+      for (int f = 0; f < NF; f += NFS)
+        gateup_group<MOE_FMT_Q8_0, NFS, JS, MAXR, TAPS>(a, a.sgq, a.sgs, a.suq, a.sus, a.fs,
+                                                        n0 + f, row0, nrows, true);
     } else {
       const size_t qoff = (size_t)e * a.f * row_bytes(FMT, a.d);
       const size_t soff = (size_t)e * a.f * (a.d / 32);
-      gateup_feature<FMT, MAXR, TAPS>(a, a.gq + qoff, a.gs + soff, a.uq + qoff, a.us + soff,
-                                      a.f, n, row0, nrows, false);
+      gateup_group<FMT, NF, J, MAXR, TAPS>(a, a.gq + qoff, a.gs + soff, a.uq + qoff,
+                                           a.us + soff, a.f, n0, row0, nrows, false);
     }
   }
+}
+
+// 16-code groups of a 32-code block transposed as 4x4 bytes: code 16g + 4j + i
+// moves to byte 16g + 4i + j (the order the 2-bit block dot consumes)
+__device__ __forceinline__ int transposed_lane(int lane) {
+  return (lane & 16) | ((lane & 3) << 2) | ((lane >> 2) & 3);
 }
 
 // requantise h per 32-block: one warp per (slot, block)
 __global__ void __launch_bounds__(256)
     k_requant(const float *__restrict__ h, uint32_t slots, uint32_t R, uint32_t f, uint32_t fs,
-              uint32_t fmax, int8_t *__restrict__ hq, float *__restrict__ hs) {
+              uint32_t fmax, int8_t *__restrict__ hq, float *__restrict__ hs,
+              int8_t *__restrict__ ht) {
   const int lane = threadIdx.x & 31;
   const uint32_t nbmax = fmax / 32;
   const uint64_t gw = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32;
@@ -167,66 +271,77 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
   const float sc = __fdiv_rn(amax, 127.0f);
-  hq[i] = (int8_t)quant_one(v, sc);
+  const int8_t q = (int8_t)quant_one(v, sc);
+  hq[i] = q;
+  if (ht && slot < R) ht[(size_t)slot * fmax + 32 * b + transposed_lane(lane)] = q;
   if (lane == 0) hs[(size_t)slot * nbmax + b] = sc;
 }
 
-// o[slot][m] for rows of one expert: the down row m (K = width) against hq
-template <int FMT, int MAXR, bool TAPS>
-__device__ __forceinline__ void down_feature(const DNArgs &a, const int8_t *dq,
-                                             const uint16_t *ds, uint32_t width, int m,
-                                             int row0, int nrows) {
+// o[slot][m] for m in [m0, m0 + NF), rows of one expert: down rows (K = width)
+// against the h codes
+template <int FMT, int NF, int J, int MAXR, bool TAPS>
+__device__ __forceinline__ void down_group(const DNArgs &a, const int8_t *dq, const uint16_t *ds,
+                                           uint32_t width, int m0, int row0, int nrows) {
   const int lane = threadIdx.x & 31;
   const uint32_t nb = width / 32, nbmax = a.fmax / 32;
-  const int8_t *row = dq + (size_t)m * row_bytes(FMT, width);
-  const uint16_t *srow = ds + (size_t)m * nb;
-  const int jt = tap_index<TAPS>((uint32_t)m, a.d);
+  const size_t rb = row_bytes(FMT, width);
+  const int8_t *const w[1] = {dq + (size_t)m0 * rb};
+  const uint16_t *const ws[1] = {ds + (size_t)m0 * nb};
+  int jt[NF];
+#pragma unroll
+  for (int f = 0; f < NF; ++f) jt[f] = tap_index<TAPS>((uint32_t)(m0 + f), a.d);
   for (int r0 = 0; r0 < nrows; r0 += MAXR) {
     const int nr = min(MAXR, nrows - r0);
-    float acc[MAXR];
+    int slot[MAXR];
 #pragma unroll
-    for (int r = 0; r < MAXR; ++r) acc[r] = 0.0f;
-#pragma unroll 2
-    for (uint32_t b = lane; b < nb; b += 32) {
-      WBlock<FMT> wd;
-      wd.load(row, b);
-      const float sw = half_bits_to_float(srow[b]);
+    for (int r = 0; r < MAXR; ++r) slot[r] = r < nr ? row0 + r0 + r : row0;
+    float acc[1][NF][MAXR];
 #pragma unroll
-      for (int r = 0; r < MAXR; ++r) {
-        if (r < nr) {
-          const size_t slot = (size_t)(row0 + r0 + r);
-          const W8 x = ld_cached32(a.hq + slot * a.fmax + 32 * b);
-          const float hsc = a.hs[slot * nbmax + b];
-          const int is = wd.dot(x);
-          acc[r] = __fmaf_rn((float)is, sw * hsc, acc[r]);
-          if (TAPS && jt >= 0) a.tap[(slot * kNTap + jt) * nbmax + b] = is;
-        }
-      }
-    }
+    for (int f = 0; f < NF; ++f)
+#pragma unroll
+      for (int r = 0; r < MAXR; ++r) acc[0][f][r] = 0.0f;
+    group_dots<FMT, 1, NF, J, MAXR>(
+        w, ws, rb, nb, FMT == MOE_FMT_Q2S ? a.ht : a.hq, a.fmax, a.hs, nbmax, slot, nr, acc,
+        [&](int, int f, int r, uint32_t b, int v) {
+          if (TAPS && jt[f] >= 0) a.tap[((size_t)slot[r] * kNTap + jt[f]) * nbmax + b] = v;
+        });
 #pragma unroll
     for (int r = 0; r < MAXR; ++r) {
-      const float v = warp_sum(acc[r]);
-      if (lane == 0 && r < nr) a.o[(size_t)(row0 + r0 + r) * a.d + m] = v;
+      if (r < nr) {  // warp-uniform
+#pragma unroll
+        for (int f = 0; f < NF; ++f) {
+          const float v = warp_sum(acc[0][f][r]);
+          if (lane == f) a.o[(size_t)slot[r] * a.d + m0 + f] = v;
+        }
+      }
     }
   }
 }
 
 template <int FMT, int MAXR, bool TAPS>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, MAXR <= 2 ? 3 : 2) k_down(const DNArgs a) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>())) k_down(const DNArgs a) {
+  constexpr int NF = group_nf<FMT, 1>(), J = group_j<FMT, 1, MAXR>();
+  constexpr int NFS = group_nf<MOE_FMT_Q8_0, 1>(), JS = group_j<MOE_FMT_Q8_0, 1, MAXR>();
+  static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
+  extern __shared__ int gsm[];
   PlanView P(const_cast<int *>(a.plan), a.E);
-  const int total = P.hdr[2];
+  const SmemPlan S(gsm, P, a.E);
+  const int per = (int)a.d / NF;  // groups per expert
+  const int groups = P.hdr[2] / NF;
   const int nwarps = gridDim.x * kWarpsPerCta;
-  for (int item = blockIdx.x * kWarpsPerCta + threadIdx.x / 32; item < total; item += nwarps) {
-    const int u = item / (int)a.d;
-    const int m = item - u * (int)a.d;
-    const int e = P.act_e[u];
-    const int row0 = P.act_row0[u], nrows = P.act_rows[u];
+  for (int g = blockIdx.x * kWarpsPerCta + threadIdx.x / 32; g < groups; g += nwarps) {
+    const int u = g / per;
+    const int m0 = (g - u * per) * NF;
+    const int e = S.e[u];
+    const int row0 = S.row0[u], nrows = S.rows[u];
     if ((uint32_t)e == a.E) {
-      down_feature<MOE_FMT_Q8_0, MAXR, TAPS>(a, a.sdq, a.sds, a.fs, m, row0, nrows);
+#pragma unroll 1
+      for (int f = 0; f < NF; f += NFS)
+        down_group<MOE_FMT_Q8_0, NFS, JS, MAXR, TAPS>(a, a.sdq, a.sds, a.fs, m0 + f, row0, nrows);
     } else {
       const size_t qoff = (size_t)e * a.d * row_bytes(FMT, a.f);
       const size_t soff = (size_t)e * a.d * (a.f / 32);
-      down_feature<FMT, MAXR, TAPS>(a, a.dq + qoff, a.ds + soff, a.f, m, row0, nrows);
+      down_group<FMT, NF, J, MAXR, TAPS>(a, a.dq + qoff, a.ds + soff, a.f, m0, row0, nrows);
     }
   }
 }
@@ -251,36 +366,48 @@ __global__ void __launch_bounds__(256)
   y[i] = acc;
 }
 
+// resident CTAs per SM of a persistent GEMV kernel with `smem` dynamic bytes
 template <typename K>
-int persistent_grid(K kernel, int sm_count) {
-  int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarpsPerCta * 32, 0) !=
+cudaError_t grid_for(K kernel, size_t smem, bool &big_smem, int &per_sm) {
+  if (smem > 48 * 1024 && !big_smem) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    big_smem = true;
+  }
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kWarpsPerCta * 32, smem) !=
           cudaSuccess ||
       per_sm < 1)
     per_sm = 1;
-  return per_sm * sm_count;
+  return cudaSuccess;
 }
 
 template <int FMT, int MAXR, bool TAPS>
 cudaError_t run_gateup(const Ctx &c, const GUArgs &a) {
+  static bool big_smem = false;
   auto kern = k_gateup<FMT, MAXR, TAPS>;
-  kern<<<persistent_grid(kern, c.sm_count), kWarpsPerCta * 32, 0, c.stream>>>(a);
+  const size_t smem = smem_plan_bytes(c.desc.n_expert);
+  int per_sm = 1;
+  cudaError_t e = grid_for(kern, smem, big_smem, per_sm);
+  if (e != cudaSuccess) return e;
+  kern<<<per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream>>>(a);
   return cudaGetLastError();
 }
 
 template <int FMT, int MAXR, bool TAPS>
 cudaError_t run_down(const Ctx &c, const DNArgs &a) {
+  static bool big_smem = false;
   auto kern = k_down<FMT, MAXR, TAPS>;
-  kern<<<persistent_grid(kern, c.sm_count), kWarpsPerCta * 32, 0, c.stream>>>(a);
+  const size_t smem = smem_plan_bytes(c.desc.n_expert);
+  int per_sm = 1;
+  cudaError_t e = grid_for(kern, smem, big_smem, per_sm);
+  if (e != cudaSuccess) return e;
+  kern<<<per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream>>>(a);
   return cudaGetLastError();
 }
 
-// rows per pass: an expert has at most T rows, and at most kTcMinRows when the
-// tensor-core path takes the larger experts
-int maxr_for(uint32_t T, bool tc) {
-  if (tc && T > kTcMinRows) T = kTcMinRows;
-  return T <= 1 ? 1 : T <= 2 ? 2 : T <= 4 ? 4 : T <= 8 ? 8 : 16;
-}
+// rows per pass: an expert has at most T rows; more than 4 take several passes
+int maxr_for(uint32_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : 4; }
 
 template <int FMT, int MAXR>
 cudaError_t gu_taps(const Ctx &c, const GUArgs &a, bool taps) {
@@ -293,22 +420,18 @@ cudaError_t dn_taps(const Ctx &c, const DNArgs &a, bool taps) {
 
 template <int FMT>
 cudaError_t gu_maxr(const Ctx &c, const GUArgs &a, bool taps) {
-  switch (maxr_for(c.T, c.L.xperm != 0 && tc_supported(c.desc))) {
+  switch (maxr_for(c.T)) {
     case 1: return gu_taps<FMT, 1>(c, a, taps);
     case 2: return gu_taps<FMT, 2>(c, a, taps);
-    case 4: return gu_taps<FMT, 4>(c, a, taps);
-    case 8: return gu_taps<FMT, 8>(c, a, taps);
-    default: return gu_taps<FMT, 16>(c, a, taps);
+    default: return gu_taps<FMT, 4>(c, a, taps);
   }
 }
 template <int FMT>
 cudaError_t dn_maxr(const Ctx &c, const DNArgs &a, bool taps) {
-  switch (maxr_for(c.T, c.L.xperm != 0 && tc_supported(c.desc))) {
+  switch (maxr_for(c.T)) {
     case 1: return dn_taps<FMT, 1>(c, a, taps);
     case 2: return dn_taps<FMT, 2>(c, a, taps);
-    case 4: return dn_taps<FMT, 4>(c, a, taps);
-    case 8: return dn_taps<FMT, 8>(c, a, taps);
-    default: return dn_taps<FMT, 16>(c, a, taps);
+    default: return dn_taps<FMT, 4>(c, a, taps);
   }
 }
 
@@ -334,6 +457,7 @@ cudaError_t launch_gateup(const Ctx &c, const int32_t *perm) {
   a.sgs = c.wts.s_gate.scale;
   a.sus = c.wts.s_up.scale;
   a.xq = (const int8_t *)(c.ws + c.L.xq);
+  a.xt = c.L.xt ? (const int8_t *)(c.ws + c.L.xt) : nullptr;
   a.xs = (const float *)(c.ws + c.L.xs);
   a.perm = perm;
   a.h = (float *)(c.ws + c.L.h);
@@ -350,7 +474,8 @@ cudaError_t launch_requant_h(const Ctx &c) {
   if (warps == 0) return cudaSuccess;
   k_requant<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
       (const float *)(c.ws + c.L.h), slots, c.R, c.desc.f, c.desc.f_shared, c.fmax,
-      (int8_t *)(c.ws + c.L.hq), (float *)(c.ws + c.L.hs));
+      (int8_t *)(c.ws + c.L.hq), (float *)(c.ws + c.L.hs),
+      c.L.ht ? (int8_t *)(c.ws + c.L.ht) : nullptr);
   return cudaGetLastError();
 }
 
@@ -369,6 +494,7 @@ cudaError_t launch_down(const Ctx &c) {
   a.sdq = (const int8_t *)c.wts.s_down.q;
   a.sds = c.wts.s_down.scale;
   a.hq = (const int8_t *)(c.ws + c.L.hq);
+  a.ht = c.L.ht ? (const int8_t *)(c.ws + c.L.ht) : nullptr;
   a.hs = (const float *)(c.ws + c.L.hs);
   a.o = (float *)(c.ws + c.L.o);
   a.tap = (int32_t *)(c.ws + c.L.tap_dn);

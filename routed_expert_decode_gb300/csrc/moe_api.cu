@@ -81,6 +81,11 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
     L.xsperm = p; p = align_up(p + slots * (d->d / 32) * 4);
     L.hperm = p; p = align_up(p + slots * fmax * 2);
   }
+  L.xt = L.ht = 0;
+  if (d->routed_fmt == MOE_FMT_Q2S) {
+    L.xt = p; p = align_up(p + (size_t)T * d->d);
+    L.ht = p; p = align_up(p + slots * fmax);
+  }
   L.trace = 0;
   if (d->flags & MOE_FLAG_TRACE) {
     L.trace = p; p = align_up(p + (size_t)1024 * 20 * 8);
@@ -281,6 +286,13 @@ const char *moe_layer_path(const moe_desc *desc, uint32_t T) {
   if (!desc_ok(desc)) return nullptr;
   Ctx c = make_ctx(desc, nullptr, T, nullptr, nullptr);
   return (T > 0 && fused_eligible(c)) ? "fused_decode" : "multi_kernel";
+}
+
+int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T) {
+  if (!desc_ok(desc)) return -1;
+  Ctx c = make_ctx(desc, nullptr, T, nullptr, nullptr);
+  if (T == 0 || fused_eligible(c) || !tc_possible(*desc, T) || !tc_supported(*desc)) return -1;
+  return (desc->flags & MOE_FLAG_FORCE_TC) ? 0 : (int32_t)kTcMinRows;
 }
 
 const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i) {

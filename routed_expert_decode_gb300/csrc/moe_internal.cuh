@@ -115,6 +115,17 @@ __device__ __forceinline__ W8 ld_cached32(const void *p) {
   return w;
 }
 
+// as ld_cached32, but issued exactly where written (volatile): keeps the
+// compiler from hoisting a whole unrolled loop's activation loads ahead of use
+__device__ __forceinline__ W8 ld_cached32_here(const void *p) {
+  W8 w;
+  asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(w.v[0]), "=r"(w.v[1]), "=r"(w.v[2]), "=r"(w.v[3]), "=r"(w.v[4]),
+                 "=r"(w.v[5]), "=r"(w.v[6]), "=r"(w.v[7])
+               : "l"(p));
+  return w;
+}
+
 __device__ __forceinline__ uint2 ld_stream8(const void *p) {
   uint2 w;
   asm("ld.global.nc.L1::no_allocate.v2.b32 {%0,%1}, [%2];" : "=r"(w.x), "=r"(w.y) : "l"(p));
@@ -131,8 +142,10 @@ template <>
 struct WBlock<MOE_FMT_Q8_0> {
   W8 w;
   static constexpr int kRowBytesPer32 = 32;
+  static constexpr bool kNeedSum = false;
   __device__ __forceinline__ void load(const int8_t *row, int b) { w = ld_stream32(row + 32 * b); }
-  __device__ __forceinline__ int dot(const W8 &x) const {
+  __device__ __forceinline__ void prep() {}
+  __device__ __forceinline__ int dot(const W8 &x, int /*sum_x*/) const {
     int s = 0;
 #pragma unroll
     for (int q = 0; q < 8; ++q) s = __dp4a((int)w.v[q], (int)x.v[q], s);
@@ -140,28 +153,41 @@ struct WBlock<MOE_FMT_Q8_0> {
   }
 };
 
-__device__ __forceinline__ uint32_t spread_codes(uint32_t byte) {
-  return (byte | (byte << 6) | (byte << 12) | (byte << 18)) & 0x03030303u;
-}
-
 template <>
 struct WBlock<MOE_FMT_Q2S> {
   uint2 c;
+  uint32_t t[8];
   static constexpr int kRowBytesPer32 = 8;
+  static constexpr bool kNeedSum = true;
   __device__ __forceinline__ void load(const int8_t *row, int b) { c = ld_stream8(row + 8 * b); }
-  // sum_i (2c_i - 3) x_i = 2 sum c_i x_i - 3 sum x_i, exact in int32
-  __device__ __forceinline__ int dot(const W8 &x) const {
-    int sc = 0, sx = 0;
+  // Byte j of code word g (codes 16g .. 16g+15, LSB first) holds codes
+  // 16g+4j .. 16g+4j+3; t[4g+i] = (word >> 2i) & 0x03030303 has code 16g+4j+i
+  // in byte j, which lines up with activations stored 16-code-group transposed
+  // (byte 4i+j of a group = code 4j+i).  Done once per block, reused by every row.
+  __device__ __forceinline__ void prep() {
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const uint32_t word = q < 4 ? c.x : c.y;
-      const uint32_t cw = spread_codes((word >> (8 * (q & 3))) & 0xFFu);
-      sc = __dp4a((int)cw, (int)x.v[q], sc);
-      sx = __dp4a(0x01010101, (int)x.v[q], sx);
+    for (int i = 0; i < 4; ++i) {
+      t[i] = (c.x >> (2 * i)) & 0x03030303u;
+      t[4 + i] = (c.y >> (2 * i)) & 0x03030303u;
     }
-    return 2 * sc - 3 * sx;
+  }
+  // sum_i (2c_i - 3) x_i = 2 sum c_i x_i - 3 sum x_i, exact in int32; x in the
+  // transposed order
+  __device__ __forceinline__ int dot(const W8 &xt, int sum_x) const {
+    int sc = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sc = __dp4a((int)t[q], (int)xt.v[q], sc);
+    return 2 * sc - 3 * sum_x;
   }
 };
+
+// sum of the 32 int8 codes of an activation block
+__device__ __forceinline__ int block_sum(const W8 &x) {
+  int s = 0;
+#pragma unroll
+  for (int q = 0; q < 8; ++q) s = __dp4a(0x01010101, (int)x.v[q], s);
+  return s;
+}
 
 __host__ __device__ inline size_t row_bytes(int fmt, uint32_t K) {
   return fmt == MOE_FMT_Q2S ? K / 4 : K;

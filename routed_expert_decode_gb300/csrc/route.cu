@@ -320,7 +320,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 // Activation quantiser: one warp per 32-block.
 __global__ void __launch_bounds__(256)
     k_quant(const float *__restrict__ x, uint32_t nblocks, int8_t *__restrict__ xq,
-            float *__restrict__ xs) {
+            float *__restrict__ xs, int8_t *__restrict__ xt) {
   const int lane = threadIdx.x & 31;
   const uint32_t b = blockIdx.x * 8 + threadIdx.x / 32;
   if (b >= nblocks) return;
@@ -329,7 +329,11 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
   const float sc = __fdiv_rn(a, 127.0f);
-  xq[(size_t)b * 32 + lane] = (int8_t)quant_one(v, sc);
+  const int8_t q = (int8_t)quant_one(v, sc);
+  xq[(size_t)b * 32 + lane] = q;
+  // 2-bit routed weights also read the codes with each 16-code group 4x4
+  // transposed: code 16g + 4j + i at byte 16g + 4i + j
+  if (xt) xt[(size_t)b * 32 + ((lane & 16) | ((lane & 3) << 2) | ((lane >> 2) & 3))] = q;
   if (lane == 0) xs[b] = sc;
 }
 
@@ -373,8 +377,9 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
 cudaError_t launch_quant_x(const Ctx &c, const float *x) {
   const uint32_t nblocks = c.T * (c.desc.d / 32);
   if (nblocks == 0) return cudaSuccess;
-  k_quant<<<(nblocks + 7) / 8, 256, 0, c.stream>>>(x, nblocks, (int8_t *)(c.ws + c.L.xq),
-                                                    (float *)(c.ws + c.L.xs));
+  k_quant<<<(nblocks + 7) / 8, 256, 0, c.stream>>>(
+      x, nblocks, (int8_t *)(c.ws + c.L.xq), (float *)(c.ws + c.L.xs),
+      c.L.xt ? (int8_t *)(c.ws + c.L.xt) : nullptr);
   return cudaGetLastError();
 }
 

@@ -57,7 +57,8 @@ class MoeWeights(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "err", "total")
+                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "xt", "ht", "err",
+                 "total")
 
 
 class MoeWsLayout(ctypes.Structure):
@@ -104,6 +105,8 @@ def lib():
         L.moe_layer_path.restype = ctypes.c_char_p
         L.moe_layer_path.argtypes = [ctypes.POINTER(MoeDesc), _u32]
         L.moe_layer_stage_name.restype = ctypes.c_char_p
+        L.moe_tc_min_rows.argtypes = [ctypes.POINTER(MoeDesc), _u32]
+        L.moe_tc_min_rows.restype = ctypes.c_int32
         L.moe_layer_stage_name.argtypes = [ctypes.POINTER(MoeDesc), _u32, _u32]
         L.moe_layer_noalloc.restype = ctypes.c_int
         L.moe_layer_noalloc.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
@@ -225,6 +228,12 @@ NOALLOC_SCRATCH_BYTES = 16 << 20
 
 def layer_path(desc: MoeDesc, T: int) -> str:
     return lib().moe_layer_path(ctypes.byref(desc), T).decode()
+
+
+def tc_min_rows(desc: MoeDesc, T: int):
+    """Experts with more rows than this run on the tensor cores; None: no tensor path."""
+    v = lib().moe_tc_min_rows(ctypes.byref(desc), T)
+    return None if v < 0 else v
 
 
 def stage_names(desc: MoeDesc, T: int) -> list:

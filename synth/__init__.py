@@ -150,6 +150,10 @@ Q2_LAYER = LayerSpec("e192_k8_d4096_f1536_q2", E=192, k=8, d=4096, f=1536, f_sha
 # read per token): the small case that profiler captures run on.
 GLM_LAYER_E32 = LayerSpec("e32_k8_d6144_f2048_q8", E=32, k=8, d=6144, f=2048, f_shared=2048,
                           fmt=FMT_Q8_0, s=2.5, zipf_beta=0.4)
+# 64 experts (2.4 GB): with T=128 an expert gets ~16 rows, as in a T=512 batch
+# over 256 experts -- the small case for captures of the tensor-core path.
+GLM_LAYER_E64 = LayerSpec("e64_k8_d6144_f2048_q8", E=64, k=8, d=6144, f=2048, f_shared=2048,
+                          fmt=FMT_Q8_0, s=2.5, zipf_beta=0.4)
 
 # workloads: (layer, tokens per step, token seeds)
 WORKLOADS = {
@@ -161,6 +165,7 @@ WORKLOADS = {
     "q2_t64": (Q2_LAYER, 64, (0,)),
     "profile_decode_t1": (GLM_LAYER_E32, 1, tuple(range(8))),
     "profile_prefill_t512": (GLM_LAYER_E32, 512, (0,)),
+    "profile_prefill_e64_t128": (GLM_LAYER_E64, 128, (0,)),
 }
 
 
