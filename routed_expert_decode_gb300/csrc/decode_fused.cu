@@ -6,25 +6,27 @@
 // launch gaps between small kernels, the router's latency, and the drain/ramp
 // between the gate/up and the down projection.  This kernel removes all three.
 //
-//  * One CTA per SM (cooperative launch, all CTAs co-resident), 8 consumer warps
-//    and 1 producer warp.  The producer lane streams weight rows with
+//  * One CTA per SM (cooperative launch, all CTAs co-resident), 16 consumer
+//    warps and 1 producer warp.  The producer lane streams weight rows with
 //    cp.async.bulk (the bulk-copy/TMA engine, one-CTA copies, no multicast) into
-//    a ring of shared-memory stages guarded by mbarriers; consumers compute from
-//    shared memory with dp4a.
+//    a ring of up to 8 shared-memory stages guarded by mbarriers; consumers
+//    compute from shared memory with dp4a.
+//  * Every CTA routes the tokens itself (sigmoid + bias, top-k in registers,
+//    stable permutation) from the same inputs, so no CTA waits on another for
+//    the routing; CTA 0 also writes the routing arrays to the workspace.  While
+//    the consumers route, the producer is already streaming the shared expert,
+//    whose items need no routing.
 //  * Work comes from one global queue, handed out in this order: gate/up items
-//    of the shared expert (they need no routing), gate/up items of the routed
-//    experts, then down items of every expert.  A gate/up item is 32 features
-//    of one expert (one int8 block of h, requantised by the CTA that computed
-//    it); a down item is a chunk of output rows of one expert.
-//  * CTA 0's consumer warps route the tokens first (sigmoid + bias, top-k,
-//    stable permutation) and publish the active-expert list with a release
-//    flag; meanwhile every other CTA is already streaming the shared expert.
-//  * A down item needs its expert's h complete: consumers wait on a per-expert
-//    counter, while the producer keeps prefetching weights (which do not depend
-//    on h).  Because every gate/up item is handed out before any down item and
-//    all CTAs are resident, every such wait ends.
+//    of the shared expert, gate/up items of the routed experts, then down items
+//    of every expert.  A gate/up item is 32 features of one expert (one int8
+//    block of h, requantised by the CTA that computed it) in stages of 8
+//    features; a down item is a chunk of output rows of one expert.
+//  * A down item needs its expert's h complete: the producer waits on a
+//    per-expert counter (after issuing the stage's weight copies) before it
+//    copies the h codes in.  Because every gate/up item is handed out before
+//    any down item and all CTAs are resident, every such wait ends.
 //  * The combine (y = o_shared + sum_j w_j o_j, fixed order) of an output chunk
-//    is done by the CTA that lands the chunk's last contribution.
+//    is done, at the end, by the CTA that landed the chunk's last contribution.
 //  * Every wait is bounded; on timeout the kernel flags kErrTimeout and exits.
 // Per-expert batches of the selected experts only, read once per call: the
 // indexed per-expert FFN of NeutronStar README, "MTP speculative decoding".
@@ -36,10 +38,11 @@ namespace {
 constexpr int kConsumerWarps = 16;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr int kMaxT = 2;
-constexpr int kBFeat = 8;        // features per gate/up stage: two consumer warps each
-constexpr int kKSplit = kConsumerWarps / kBFeat;  // K parts per feature
+constexpr int kMaxR = 64;        // routed rows (T * top_k)
+constexpr int kBFeat = 8;        // features per gate/up stage
+constexpr int kKSplit = kConsumerWarps / kBFeat;  // K parts per feature (one warp each)
 constexpr int kBItemFeat = 32;   // features per gate/up item: one quantisation block
-constexpr int kMaxStages = 4;
+constexpr int kMaxStages = 8;
 constexpr uint32_t kSyncInts = MOE_SYNC_BYTES / 4;
 constexpr int kSpinIters = 1 << 26;                // iteration cap of every wait
 constexpr long long kWaitCycles = 4000000000ll;     // ~2 s at 2 GHz: a wait gives up after this
@@ -64,11 +67,11 @@ enum : int {
   kTrComputeB = 11,    // consumer cycles in gate/up stages
   kTrComputeC = 12,    // consumer cycles in down stages
   kTrCombine = 13,     // consumer cycles combining chunks
-  kTrRouteDone = 14,   // CTA 0: routing published (ns)
+  kTrRouteDone = 14,   // routing known to the producer (ns)
   kTrProdEnd = 15,     // producer leaves (ns)
-  kTrRouteLoaded = 16, // CTA 0: logits and bias loaded (ns)
-  kTrRouteTopk = 17,   // CTA 0: top-k and weights done (ns)
-  kTrRoutePerm = 18,   // CTA 0: permutation and plan written (ns)
+  kTrRouteLoaded = 16, // routing inputs loaded (ns)
+  kTrRouteTopk = 17,   // top-k done (ns)
+  kTrRoutePerm = 18,   // permutation and active list done (ns)
   kTraceWords = 20
 };
 
@@ -115,23 +118,36 @@ struct FusedArgs {
   int stall_test;         // MOE_FLAG_TEST_STALL: never publish the routing result
 };
 
-// Counters at a fixed workspace offset (moe.h: the first 32 KiB of a workspace).
+// Counters at a fixed workspace offset (moe.h: MOE_SYNC_BYTES from offset 256).
 // They are zero before a call and the last CTA to finish zeroes them again, so
 // no per-call memset is needed (a workspace must be zero-filled once after it
 // is allocated).  diag[] keeps the first timeout's site for the host.
 struct SyncView {
-  uint32_t *queue, *route, *diag, *ready, *chunk, *owner, *done;
+  uint32_t *queue, *diag, *ready, *chunk, *done;
   uint32_t n_clear;  // words from queue up to and including done (diag words are kept)
   __device__ SyncView(uint32_t *base, uint32_t E, uint32_t n_chunks) {
-    queue = base;
-    route = base + 1;
-    diag = base + 2;  // [2], [3]
-    ready = base + 4;  // [E+1]
-    chunk = ready + E + 1;
-    owner = chunk + n_chunks;  // 1 + CTA that completes chunk c (combines it)
-    done = owner + n_chunks;
-    n_clear = 4 + E + 1 + 2 * n_chunks + 1;
+    queue = base;      // [0]; [1] unused
+    diag = base + 2;   // [2], [3]
+    ready = base + 4;  // [E+1] gate/up items finished per expert
+    chunk = ready + E + 1;  // [n_chunks] down contributions landed per chunk
+    done = chunk + n_chunks;
+    n_clear = 4 + E + 1 + n_chunks + 1;
   }
+};
+
+// Routing of the call, held in shared memory by every CTA.
+struct RouteSmem {
+  int idx[kMaxR];     // expert of row r = t*k + j
+  float w[kMaxR];     // its combine weight
+  int pos[kMaxR];     // slot of row r (stable sort by expert)
+  int tok[kMaxR];     // token of slot p
+  int act_e[kMaxR];   // active routed experts in id order, their first slot and rows
+  int act_row0[kMaxR];
+  int act_rows[kMaxR];
+  int row_at[kMaxR];  // row at slot p
+  uint32_t first_bits[2];  // slot p opens an expert's run (bit p)
+  int U;              // active routed experts
+  int pad;
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -204,22 +220,6 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
   return v;
 }
 
-__device__ __forceinline__ void st_release(uint32_t *p, uint32_t v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-// bounded wait until *p >= target (acquire); false on timeout
-__device__ __forceinline__ bool wait_geq(const uint32_t *p, uint32_t target, long long budget) {
-  const long long t0 = clock64();
-  for (int i = 0; i < kSpinIters; ++i) {
-    if (ld_acquire(p) >= target) return true;
-    if (clock64() - t0 > budget) return false;
-    __nanosleep(64);
-  }
-  return false;
-}
-
-__device__ __forceinline__ int ld_cg_i32(const int *p) { return __ldcg(p); }
 
 // one thread publishes the CTA's prior writes (made visible to it by a CTA
 // barrier) with a gpu-scope release reduction
@@ -255,15 +255,6 @@ __device__ __forceinline__ void item_barrier_arrive() {
   asm volatile("bar.arrive 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-__device__ __forceinline__ W8 lds32(const int8_t *p) {
-  const uint4 a = *reinterpret_cast<const uint4 *>(p);
-  const uint4 b = *reinterpret_cast<const uint4 *>(p + 16);
-  W8 w;
-  w.v[0] = a.x; w.v[1] = a.y; w.v[2] = a.z; w.v[3] = a.w;
-  w.v[4] = b.x; w.v[5] = b.y; w.v[6] = b.z; w.v[7] = b.w;
-  return w;
-}
-
 __device__ __forceinline__ uint4 lds16(const int8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
 }
@@ -276,139 +267,163 @@ __device__ __forceinline__ int dot16(const uint4 &a, const uint4 &b) {
   return __dp4a((int)a.w, (int)b.w, s);
 }
 
-__device__ __forceinline__ int dot8(const W8 &a, const W8 &b) {
-  int s = 0;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) s = __dp4a((int)a.v[q], (int)b.v[q], s);
-  return s;
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
   return v;
 }
 
-// ---------------------------------------------------------------- routing (CTA 0)
-// Runs once per call on cold caches, so the code is kept short (no wide
-// unrolling): scores go to shared-memory scratch, warp t selects token t's
-// top_k by k rounds of a strided scan plus a butterfly argmax (score
-// descending, index ascending: ties go to the lower index), and the stable
-// permutation / offsets / active list are O(R) per thread (R <= 64 rows).
-__device__ void route_tokens(const FusedArgs &a, int *s_idx, float *s_w, float *scratch,
-                             unsigned long long *tr) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+// ---------------------------------------------------------------- routing (every CTA)
+// Every CTA routes the tokens itself from the same inputs, so all CTAs hold the
+// same routing in shared memory without waiting on one another; CTA 0 also
+// writes idx, w, off, perm, pos and the plan's active list to the workspace.
+// This code runs once per call with a cold instruction cache (each new line of
+// code costs a round trip to L2 or HBM), so it is kept compact -- rolled loops,
+// no unrolled sorting network -- and only the T routing warps run it, while the
+// other consumer warps quantise x.
+
+// (score, expert) order of the selection: higher score first, ties to the lower
+// expert index
+__device__ __forceinline__ bool ranks_before(float s1, int e1, float s2, int e2) {
+  return s1 > s2 || (s1 == s2 && e1 < e2);
+}
+
+__device__ __forceinline__ void route_bar_sync(uint32_t T) {
+  asm volatile("bar.sync 3, %0;" ::"r"(T * 32) : "memory");
+}
+
+// selection scores sigmoid(logit) + bias of all T*E (token, expert) pairs
+// (every consumer thread; a consumer barrier follows)
+__device__ void route_scores(const FusedArgs &a, float *sc) {
+#pragma unroll 1
+  for (uint32_t i = threadIdx.x; i < a.T * a.E; i += kConsumerWarps * 32)
+    sc[i] = __fadd_rn(sigmoid_rn(__ldg(a.logits + i)), __ldg(a.bias + i % a.E));
+}
+
+// warps 0..T-1: warp t selects token t's top_k by k rounds of a strided scan
+// of the scores (ascending e per lane: strict '>' keeps the lower index) and a
+// butterfly argmax; then the stable permutation (rows by expert, then row
+// order) and the active list, with the T warps' threads as the R <= 64 rows
+__device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
+  const int tid = threadIdx.x, lane = tid & 31, t = tid >> 5;
   const uint32_t E = a.E, k = a.k, T = a.T;
-  float *c_s = scratch;               // [T][E] selection score (taken -> -inf)
-  float *sg_s = scratch + (size_t)T * E;  // [T][E] sigmoid(logit)
   const int R = (int)a.R;
-  // scores: every consumer thread takes a share of the T*E (token, expert) pairs
-  for (uint32_t i = tid; i < T * E; i += kConsumerWarps * 32) {
-    const float sg = sigmoid_rn(__ldg(a.logits + i));
-    sg_s[i] = sg;
-    c_s[i] = __fadd_rn(sg, __ldg(a.bias + i % E));
-  }
-  consumer_sync();
-  if (tr && tid == 0) tr[kTrRouteLoaded] = global_ns();
-  if (warp < (int)T) {
-    const int t = warp;
-    float *ct = c_s + (size_t)t * E;
-    float my_sigma = 0.0f;  // lane j keeps the sigma of slot j
+  float *ct = sc + (size_t)t * E;
 #pragma unroll 1
-    for (uint32_t j = 0; j < k; ++j) {
-      float bc = -INFINITY;
-      int be = 0x7fffffff;
+  for (uint32_t j = 0; j < k; ++j) {
+    float bs = -INFINITY;
+    int be = 0x7fffffff;
 #pragma unroll 1
-      for (uint32_t e = lane; e < E; e += 32) {
-        const float v = ct[e];
-        if (v > bc) {  // ascending e per lane: strict '>' keeps the lower index
-          bc = v;
-          be = (int)e;
-        }
+    for (uint32_t e = lane; e < E; e += 32) {
+      const float v = ct[e];
+      if (v > bs) {
+        bs = v;
+        be = (int)e;
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float oc = __shfl_xor_sync(0xffffffffu, bc, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (oc > bc || (oc == bc && oe < be)) {
-          bc = oc;
-          be = oe;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        ct[be] = -INFINITY;
-        s_idx[t * k + j] = be;
-      }
-      __syncwarp();
-      if ((uint32_t)lane == j) my_sigma = sg_s[(size_t)t * E + be];
     }
-    float sum = 0.0f;
 #pragma unroll 1
-    for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
-    if ((uint32_t)lane < k) s_w[t * k + lane] = __fmul_rn(a.s, __fdiv_rn(my_sigma, sum));
+    for (int o = 16; o > 0; o >>= 1) {
+      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ranks_before(os, oe, bs, be)) {
+        bs = os;
+        be = oe;
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      ct[be] = -INFINITY;
+      rs.idx[t * k + j] = be;
+    }
+    __syncwarp();
   }
-  consumer_sync();
-  if (tr && tid == 0) tr[kTrRouteTopk] = global_ns();
-  PlanView P(a.plan, E);
-  int *rank_of = (int *)(c_s);            // [R] sorted position of row r (scores are done)
-  int *row_at = rank_of + 64;             // [R] row at sorted position p
+  // lane j < k: the sigmoid of slot j; w = s * sigma_j / sum_j sigma_j (in order)
+  const float my_sigma =
+      (uint32_t)lane < k ? sigmoid_rn(__ldg(a.logits + (size_t)t * E + rs.idx[t * k + lane]))
+                         : 0.0f;
+  float sum = 0.0f;
+#pragma unroll 1
+  for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
+  if ((uint32_t)lane < k) rs.w[t * k + lane] = __fmul_rn(a.s, __fdiv_rn(my_sigma, sum));
+  route_bar_sync(T);
+  // slot of row r = rows before it in (expert, row) order
   if (tid < R) {
-    const int e = s_idx[tid];
+    const int e = rs.idx[tid];
     int rank = 0;
 #pragma unroll 1
     for (int r = 0; r < R; ++r) {
-      const int er = s_idx[r];
+      const int er = rs.idx[r];
       rank += (er < e || (er == e && r < tid)) ? 1 : 0;
     }
-    rank_of[tid] = rank;
-    row_at[rank] = tid;
-    a.idx[tid] = e;
-    a.w[tid] = s_w[tid];
-    a.pos[tid] = rank;
-    a.perm[rank] = tid;
+    rs.pos[tid] = rank;
+    rs.row_at[rank] = tid;
+    rs.tok[rank] = tid / (int)k;
+    if (blockIdx.x == 0) {
+      a.idx[tid] = e;
+      a.w[tid] = rs.w[tid];
+      a.pos[tid] = rank;
+      a.perm[rank] = tid;
+    }
   }
+  if (blockIdx.x == 0) {
 #pragma unroll 1
-  for (uint32_t e = tid; e <= E; e += kConsumerWarps * 32) {
-    int c = 0;
+    for (uint32_t e = tid; e <= E; e += T * 32) {
+      int c = 0;
 #pragma unroll 1
-    for (int r = 0; r < R; ++r) c += s_idx[r] < (int)e ? 1 : 0;
-    a.off[e] = c;
+      for (int r = 0; r < R; ++r) c += rs.idx[r] < (int)e ? 1 : 0;
+      a.off[e] = c;
+    }
   }
-  consumer_sync();
-  // active list from the sorted rows: a run of equal experts is one entry
+  route_bar_sync(T);
+  // active list: slot p opens an entry when its expert differs from slot p-1's;
+  // the entry's index is the number of openings before p
+  {
+    const int p = tid;
+    const int e = p < R ? rs.idx[rs.row_at[p]] : -1;
+    const bool first = p < R && (p == 0 || rs.idx[rs.row_at[p - 1]] != e);
+    const uint32_t bits = __ballot_sync(0xffffffffu, first);
+    if (lane == 0) rs.first_bits[t] = bits;
+    if (T == 1 && tid == 0) rs.first_bits[1] = 0u;
+  }
+  route_bar_sync(T);
   if (tid < R) {
     const int p = tid;
-    const int e = s_idx[row_at[p]];
-    const bool first = p == 0 || s_idx[row_at[p - 1]] != e;
-    if (first) {
-      int u = 0, rows = 0;
+    const int e = rs.idx[rs.row_at[p]];
+    const uint32_t b0 = rs.first_bits[0], b1 = rs.first_bits[1];
+    if (((p < 32 ? b0 : b1) >> (p & 31)) & 1u) {
+      const int u = p < 32 ? __popc(b0 & ((1u << p) - 1u))
+                           : __popc(b0) + __popc(b1 & ((1u << (p - 32)) - 1u));
+      int rows = 1;
 #pragma unroll 1
-      for (int q = 1; q <= p; ++q) u += s_idx[row_at[q]] != s_idx[row_at[q - 1]] ? 1 : 0;
-#pragma unroll 1
-      for (int q = p; q < R && s_idx[row_at[q]] == e; ++q) ++rows;
-      P.act_e[u] = e;
-      P.act_row0[u] = p;
-      P.act_rows[u] = rows;
+      for (int q = p + 1; q < R && rs.idx[rs.row_at[q]] == e; ++q) ++rows;
+      rs.act_e[u] = e;
+      rs.act_row0[u] = p;
+      rs.act_rows[u] = rows;
+      if (blockIdx.x == 0) {
+        PlanView P(a.plan, E);
+        P.act_e[u] = e;
+        P.act_row0[u] = p;
+        P.act_rows[u] = rows;
+      }
     }
-    if (p == R - 1) {
-      int U = 1;
-#pragma unroll 1
-      for (int q = 1; q < R; ++q) U += s_idx[row_at[q]] != s_idx[row_at[q - 1]] ? 1 : 0;
-      P.hdr[0] = U;  // routed experts only
-      P.hdr[4] = 1;
+    if (p == 0) {
+      const int U = __popc(b0) + __popc(b1);
+      rs.U = U;
+      if (blockIdx.x == 0) {
+        PlanView P(a.plan, E);
+        P.hdr[0] = U;  // routed experts only
+        P.hdr[4] = 1;
+      }
     }
   }
-  consumer_sync();
-  if (tr && tid == 0) tr[kTrRoutePerm] = global_ns();
-  if (tid == 0 && !a.stall_test) red_release_add(&a.sync[1], 1u);
+  route_bar_sync(T);
 }
 
 // ---------------------------------------------------------------- the kernel
 // Shared-memory carve-up (all offsets multiples of 16 bytes):
-//   stages[NS][stage_bytes] | xq_s[2][d] | xs_s[2][d/32] | hq_s[2][fmax] |
-//   hs_s[2][fmax/32] | part[32][2][2][2] | desc[4] | full[4] | empty[4] |
-//   misc[4] | s_idx[64] | producer plan (4 x 64) | s_w[64]
+//   stages[NS][stage_bytes] | xq_s[T][d] | xs_s[T][d/32] | part[2][32][KS][2][2] |
+//   desc[8] | full[8] | empty[8] | route_bar | misc[4] | RouteSmem | owned[n_chunks] |
+//   route scores[T][E]
 // NT: token count known at compile time (1 or 2): the one-token kernel has no
 // second-row code.
 template <int NT>
@@ -419,16 +434,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   const uint32_t NS = a.n_stages;
   uint8_t *stages = smem;
   int8_t *xq_s = (int8_t *)(stages + (size_t)NS * a.stage_bytes);
-  float *xs_s = (float *)(xq_s + (size_t)kMaxT * d);
-  int8_t *hq_s = (int8_t *)(xs_s + (size_t)kMaxT * nb);
-  float *hs_s = (float *)(hq_s + (size_t)kMaxT * fmax);
-  float *part = hs_s + (size_t)kMaxT * (fmax / 32);  // [2][feature 32][K part][row 2][g,u]
+  float *xs_s = (float *)(xq_s + (size_t)NT * d);
+  float *part = xs_s + (size_t)NT * nb;  // [2][feature 32][K part][row 2][g,u]
   StageDesc *desc = (StageDesc *)(part + 2 * kBItemFeat * kKSplit * kMaxT * 2);
   uint64_t *full = (uint64_t *)(desc + kMaxStages);
   uint64_t *empty = full + kMaxStages;
-  volatile int *s_misc = (volatile int *)(empty + kMaxStages);  // [0] abort, [1] exit-last
-  int *s_idx = (int *)(s_misc + 4);                             // [R]
-  float *s_w = (float *)(s_idx + 64 + 4 * 64);                  // [R]; producer plan before it
+  uint64_t *route_bar = empty + kMaxStages;  // the consumers' routing is in RouteSmem
+  volatile int *s_misc = (volatile int *)(route_bar + 2);  // [0] abort, [1] exit-last, [2] owned
+  RouteSmem &rs = *(RouteSmem *)(s_misc + 4);
+  int *owned = (int *)(&rs + 1);  // [n_chunks] chunks whose last contribution this CTA landed
+  float *route_scratch = (float *)(owned + (a.n_chunks + 3) / 4 * 4);  // [T][E] scores
 
   const SyncView SV(a.sync, a.E, a.n_chunks);
   unsigned long long *tr = a.trace ? a.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
@@ -443,15 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    mbar_init(route_bar, 1);
     s_misc[0] = 0;
     s_misc[1] = 0;
+    s_misc[2] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
 
   const uint32_t n_sh = a.fs / kBItemFeat;  // shared-expert gate/up items
   const uint32_t fb = a.f / kBItemFeat;      // gate/up items per routed expert
-  PlanView P(a.plan, a.E);
 
   if (warp == kConsumerWarps) {
     // ============================ producer (lane 0; the warp's other lanes wait at the end)
@@ -464,28 +480,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       //   chunk  >= 0: a down stage contributing to that output chunk (n_contrib)
       int slot_ready_e[kMaxStages], slot_chunk[kMaxStages], slot_contrib[kMaxStages];
       unsigned long long p_wait_empty = 0, p_wait_route = 0, p_items = 0, p_wait_ready = 0;
-      for (int i = 0; i < kMaxStages; ++i) slot_ready_e[i] = slot_chunk[i] = -1;
-      int *p_e = s_idx + 64, *p_row0 = p_e + 64, *p_rows = p_row0 + 64, *p_tok = p_rows + 64;
+      for (int i = 0; i < kMaxStages; ++i) slot_ready_e[i] = slot_chunk[i] = slot_contrib[i] = -1;
+      int n_owned = 0;
       // queue order: shared gate/up | routed gate/up | shared down | routed down.
       // Only the shared gate/up items are known before routing.
       const uint32_t n_pre = n_sh;
-      // wait for CTA 0's routing result and copy the plan (U <= R <= 64 experts)
+      // wait for this CTA's consumers to finish routing (RouteSmem)
       auto learn_routing = [&]() -> bool {
         const long long t_rw = clock64();
-        const bool ok = wait_geq(SV.route, 1u, a.wait_cycles);
+        const bool ok = mbar_wait(route_bar, 0u, a.wait_cycles);
         p_wait_route += clock64() - t_rw;
         if (!ok) {
           report_timeout(a, 1, 0);
           s_misc[0] = 1;
           return false;
         }
-        U = (uint32_t)ld_cg_i32(&P.hdr[0]);
-        for (uint32_t u = 0; u < U; ++u) {
-          p_e[u] = ld_cg_i32(&P.act_e[u]);
-          p_row0[u] = ld_cg_i32(&P.act_row0[u]);
-          p_rows[u] = ld_cg_i32(&P.act_rows[u]);
-        }
-        for (uint32_t p = 0; p < a.R; ++p) p_tok[p] = ld_cg_i32(&a.perm[p]) / (int)a.k;
+        if (tr) tr[kTrRouteDone] = global_ns();
+        U = (uint32_t)rs.U;
         NB = n_sh + U * fb;  // all gate/up items
         total = NB + (U + (a.fs ? 1u : 0u)) * a.n_chunks;
         routed = true;
@@ -501,13 +512,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           const uint32_t c = (uint32_t)slot_chunk[st];
           if (slot_contrib[st] > 0 &&
               atom_acq_rel_add(&SV.chunk[c], 1u) + 1 == (uint32_t)slot_contrib[st])
-            SV.owner[c] = blockIdx.x + 1;  // this CTA combines chunk c at its end
+            owned[n_owned++] = (int)c;  // this CTA combines chunk c at its end
         }
         slot_ready_e[st] = slot_chunk[st] = -1;
       };
-      // CTA 0's consumers route first, using the stage buffers as scratch: its
-      // producer starts once the routing result is out
-      if (blockIdx.x == 0 && !learn_routing()) s_misc[0] = 1;
       uint32_t item = atomicAdd(SV.queue, 1u);
       for (;;) {
         // ticket for the following item, fetched while this one is issued
@@ -546,12 +554,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               dsc.tok[r] = (int)r;
             }
           } else {
-            dsc.e = p_e[u];
-            const int row0 = p_row0[u];
-            dsc.nrows = p_rows[u];
+            dsc.e = rs.act_e[u];
+            const int row0 = rs.act_row0[u];
+            dsc.nrows = rs.act_rows[u];
             for (int r = 0; r < dsc.nrows; ++r) {
               dsc.slot[r] = row0 + r;
-              dsc.tok[r] = p_tok[row0 + r];
+              dsc.tok[r] = rs.tok[row0 + r];
             }
           }
           if (is_b) {
@@ -685,6 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           settle(st);
         }
       }
+      s_misc[2] = n_owned;
       if (tr) {
         tr[kTrProdEnd] = global_ns();
         tr[kTrWaitEmpty] = p_wait_empty;
@@ -696,36 +705,44 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     __syncwarp();
   } else {
     // ============================ consumers (warps 0..15)
-    if (blockIdx.x == 0) {
-      route_tokens(a, s_idx, s_w, (float *)stages, tr);
-      if (tr && tid == 0) tr[kTrRouteDone] = global_ns();
-    }
-    // quantise x for this CTA (identical in every CTA; CTA 0 also publishes it):
-    // warp w takes blocks w, w+16, ...; each round issues 8 loads per lane first
-    for (uint32_t b0 = warp; b0 < T * nb; b0 += 8 * kConsumerWarps) {
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t b = b0 + i * kConsumerWarps;
-        v[i] = b < T * nb ? __ldg(a.x + (size_t)b * 32 + lane) : 0.0f;
+    // x: every CTA quantises it for itself (CTA 0 also publishes xq/xs).  A warp
+    // load covers a quad of 4 blocks (lane l: floats 4l..4l+3, block l/8).  The
+    // warps that do not route take quads round-robin, loading the next quad
+    // before quantising the current one (a compact rolled loop: cold code).
+    const uint32_t n_quad = T * nb / 4;  // d % 256 == 0: whole quads per token
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.x);
+    auto quant_quad = [&](uint32_t q, float4 v) {
+      float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll 1
+      for (int o = 4; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+      const float sc = __fdiv_rn(amax, 127.0f);
+      const uint32_t packed = (uint32_t)(uint8_t)quant_one(v.x, sc) |
+                              ((uint32_t)(uint8_t)quant_one(v.y, sc) << 8) |
+                              ((uint32_t)(uint8_t)quant_one(v.z, sc) << 16) |
+                              ((uint32_t)(uint8_t)quant_one(v.w, sc) << 24);
+      const size_t e0 = (size_t)q * 128 + 4 * lane;  // first element of this lane
+      *reinterpret_cast<uint32_t *>(xq_s + e0) = packed;
+      if ((lane & 7) == 0) xs_s[q * 4 + lane / 8] = sc;
+      if (blockIdx.x == 0) {
+        *reinterpret_cast<uint32_t *>(a.xq + e0) = packed;
+        if ((lane & 7) == 0) a.xs[q * 4 + lane / 8] = sc;
       }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t b = b0 + i * kConsumerWarps;
-        float amax = fabsf(v[i]);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-          amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (b < T * nb) {
-          const float sc = __fdiv_rn(amax, 127.0f);
-          const int8_t q = (int8_t)quant_one(v[i], sc);
-          xq_s[(size_t)b * 32 + lane] = q;
-          if (lane == 0) xs_s[b] = sc;
-          if (blockIdx.x == 0) {
-            a.xq[(size_t)b * 32 + lane] = q;
-            if (lane == 0) a.xs[b] = sc;
-          }
-        }
+    };
+    const uint32_t xw = (uint32_t)kConsumerWarps - T;  // quantising warps
+    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
+    if ((uint32_t)warp >= T && warp - T < n_quad) xv = __ldg(x4 + (size_t)(warp - T) * 32 + lane);
+    route_scores(a, route_scratch);
+    consumer_sync();
+    if ((uint32_t)warp < T) {
+      route_select(a, rs, route_scratch);
+      if (tr && tid == 0) tr[kTrRoutePerm] = global_ns();
+      if (tid == 0 && !a.stall_test) mbar_arrive(route_bar);  // the producer may take routed items
+    } else {
+#pragma unroll 1
+      for (uint32_t q = warp - T; q < n_quad; q += xw) {
+        const float4 v = xv;
+        if (q + xw < n_quad) xv = __ldg(x4 + (size_t)(q + xw) * 32 + lane);
+        quant_quad(q, v);
       }
     }
     consumer_sync();
@@ -925,33 +942,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   // ============================ exit: combine the chunks this CTA completed last
   __syncthreads();
   const long long t_comb = clock64();
-  // owned chunks: every thread checks a share of owner[] (one L2 round trip),
-  // the matches go to a shared list
-  int *owned = s_idx + 64;  // the producer's plan arrays are no longer needed
-  volatile int *n_owned = s_misc + 3;
-  if (tid == 0) *n_owned = 0;
-  __syncthreads();
-  for (uint32_t c = tid; c < a.n_chunks; c += kThreads)
-    if (__ldcg(&SV.owner[c]) == blockIdx.x + 1) {
-      const int i = atomicAdd((int *)n_owned, 1);
-      if (i < 4 * 64) owned[i] = (int)c;
-      else atomicOr(a.err, kErrTimeout | (1u << 15));  // cannot happen: <= 4*64 down stages fit
-    }
-  __syncthreads();
   if (warp < kConsumerWarps && !s_misc[0]) {
-    for (int oi = 0; oi < min(*n_owned, 4 * 64); ++oi) {
-      const uint32_t c = (uint32_t)owned[oi];
-      const uint32_t first = c * a.c_rows, count = min(a.c_rows, d - first);
-      // y = o_shared + sum_j w_j o_j, shared first, then slots in order
-      for (uint32_t i = tid; i < T * count; i += kConsumerWarps * 32) {
-        const uint32_t t = i / count, m = first + i % count;
-        float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
-        for (uint32_t j = 0; j < a.k; ++j) {
-          const int p = __ldcg(a.pos + t * a.k + j);
-          acc = __fmaf_rn(__ldcg(a.w + t * a.k + j), __ldcg(a.o + (size_t)p * d + m), acc);
-        }
-        a.y[(size_t)t * d + m] = acc;
-      }
+    // y = o_shared + sum_j w_j o_j, shared first, then slots in order; all owned
+    // chunks in one pass (every load of a thread is independent: one round trip)
+    const uint32_t n_own = (uint32_t)s_misc[2], per = T * a.c_rows;
+    for (uint32_t i = tid; i < n_own * per; i += kConsumerWarps * 32) {
+      const uint32_t c = (uint32_t)owned[i / per], r = i % per;
+      const uint32_t t = r / a.c_rows, m = c * a.c_rows + r % a.c_rows;
+      if (m >= d) continue;  // the last chunk is shorter
+      float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
+      for (uint32_t j = 0; j < a.k; ++j)
+        acc = __fmaf_rn(rs.w[t * a.k + j], __ldcg(a.o + (size_t)rs.pos[t * a.k + j] * d + m), acc);
+      a.y[(size_t)t * d + m] = acc;
     }
   }
   if (tr && tid == 0) tr[kTrCombine] += clock64() - t_comb;
@@ -980,23 +982,27 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (D.routed_fmt != MOE_FMT_Q8_0) return false;
   if (D.flags & (MOE_FLAG_DEBUG_TAPS | MOE_FLAG_FORCE_GEMV)) return false;
   if (D.flags & MOE_FLAG_FORCE_TC) return false;
+  if (D.top_k > 32) return false;
   if (D.d % 256 || D.f % 256 || D.f_shared % 256) return false;
   if (D.d % (32 * kKSplit * 2)) return false;  // whole, even chunk counts per K part
-  if (c.R > 64) return false;
+  if (c.R > (uint32_t)kMaxR) return false;
   const uint32_t d = D.d, fmax = c.fmax;
   const size_t b_bytes = (size_t)kBFeat * 2 * (d + d / 16);
   const uint32_t row_c = fmax + fmax / 16;
   // a down stage also carries the expert's h codes and scales (up to 2 rows)
   const size_t h_bytes = (size_t)kMaxT * (fmax + (fmax / 32) * 4);
   if (b_bytes <= h_bytes) return false;
-  uint32_t c_rows = (uint32_t)((b_bytes - h_bytes) / row_c) / 8 * 8;
+  uint32_t c_rows = (uint32_t)((b_bytes - h_bytes) / row_c);
   if (c_rows == 0) return false;
   if (c_rows > d) c_rows = d;
+  const uint32_t n_chunks = (d + c_rows - 1) / c_rows;
+  if (4 + D.n_expert + 1 + n_chunks + 1 > kSyncInts) return false;
   const size_t stage = (b_bytes + 127) / 128 * 128;
-  const size_t rest = (size_t)kMaxT * d + (size_t)kMaxT * (d / 32) * 4 + (size_t)kMaxT * fmax +
-                      (size_t)kMaxT * (fmax / 32) * 4 + 2 * kBItemFeat * kKSplit * kMaxT * 2 * 4 +
-                      kMaxStages * sizeof(StageDesc) + 2 * kMaxStages * 8 + 16 + 6 * 64 * 4 +
-                      128;
+  const size_t rest = (size_t)c.T * d + (size_t)c.T * (d / 32) * 4 +
+                      2 * kBItemFeat * kKSplit * kMaxT * 2 * 4 + kMaxStages * sizeof(StageDesc) +
+                      2 * kMaxStages * 8 + 16 + 16 + sizeof(RouteSmem) +
+                      (size_t)(n_chunks + 3) / 4 * 16 +
+                      (size_t)c.T * D.n_expert * 4 + 128;
   int dev = 0, max_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -1005,11 +1011,8 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if ((size_t)max_smem < rest + 2 * stage) return false;
   uint32_t ns = (uint32_t)(((size_t)max_smem - rest) / stage);
   if (ns > (uint32_t)kMaxStages) ns = kMaxStages;
-  // CTA 0 routes with the stage buffers as scratch (scores + sigmoids, then 128 ints)
-  if ((size_t)c.T * D.n_expert * 8 + 512 > (size_t)ns * stage) return false;
   fp->c_rows = c_rows;
-  fp->n_chunks = (d + c_rows - 1) / c_rows;
-  if (4 + D.n_expert + 1 + 2 * fp->n_chunks + 1 > kSyncInts) return false;
+  fp->n_chunks = n_chunks;
   fp->n_stages = ns;
   fp->stage_bytes = (uint32_t)stage;
   fp->smem = rest + ns * stage;
