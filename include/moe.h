@@ -89,7 +89,7 @@ typedef struct {
  * routing result, so its bounded waits run out (~10 ms) and the call's error
  * word reports MOE_ERR_TIMEOUT; nothing faults and the context stays usable. */
 #define MOE_FLAG_TEST_STALL 0x8u
-/* Tracing: the fused decode kernel writes 20 uint64 per CTA (timestamps and
+/* Tracing: the fused decode kernel writes 24 uint64 per CTA (timestamps and
  * cycle counts of its waits and phases) into the workspace's trace region. */
 #define MOE_FLAG_TRACE 0x10u
 
@@ -131,7 +131,7 @@ typedef struct {
   size_t plan;                   /* internal work list */
   size_t sync;                   /* counters of the fused decode kernel (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
-  size_t trace;                  /* uint64 [1024][20] (MOE_FLAG_TRACE) */
+  size_t trace;                  /* uint64 [1024][24] (MOE_FLAG_TRACE) */
   size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales
                                     [R+T][d/32], fp16 h codes [R+T][fmax], in slot order */
   size_t xt, ht;                 /* 2-bit routed weights: int8 x codes [T][d] and h codes

@@ -17,8 +17,8 @@
 //    the consumers route, the producer is already streaming the shared expert,
 //    whose items need no routing.
 //  * Work comes from one global queue, handed out in this order: gate/up items
-//    of the shared expert, gate/up items of the routed experts, then down items
-//    of every expert.  A gate/up item is 32 features of one expert (one int8
+//    of the shared expert (known before the routing), gate/up items of the
+//    routed experts, then down items of every expert.  A gate/up item is 32 features of one expert (one int8
 //    block of h, requantised by the CTA that computed it) in stages of 8
 //    features; a down item is a chunk of output rows of one expert.
 //  * A down item needs its expert's h complete: the producer waits on a
@@ -36,15 +36,29 @@ namespace moe {
 namespace {
 
 constexpr int kConsumerWarps = 16;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kProducerWarp = kConsumerWarps;       // lane 0 issues the weight copies
+constexpr int kPublisherWarp = kConsumerWarps + 1;  // lane 0 does the gpu-scope atomics
+constexpr int kThreads = (kConsumerWarps + 2) * 32;
+constexpr int kPubCap = 64;
+constexpr int kRouteWarp0 = 1;   // first routing warp (not on the producer's SM sub-partition)      // events in flight from the CTA's warps to its publisher
 constexpr int kMaxT = 2;
 constexpr int kMaxR = 64;        // routed rows (T * top_k)
 constexpr int kBFeat = 8;        // features per gate/up stage
 constexpr int kKSplit = kConsumerWarps / kBFeat;  // K parts per feature (one warp each)
 constexpr int kBItemFeat = 32;   // features per gate/up item: one quantisation block
+constexpr int kDnRows = kBFeat == 8 ? 3 : 2;  // down rows per warp and pass (~43 / ~21 a stage)
+constexpr int kXRegs = kBFeat == 8 ? 6 : 4;   // x chunks per lane in registers (d <= 6144 / 8192)
 constexpr int kMaxStages = 8;
+// partial-sum buffers of gate/up items.  The warp that requantises item i reads
+// buffer i % kPartBufs after releasing the item's last stage; the other warps
+// can then run at most kMaxStages stages ahead, i.e. into item i + 2 at most
+// (items are 4 stages), so three buffers keep its buffer from being refilled.
+constexpr int kPartBufs = 3;
+static_assert(kMaxStages <= (kPartBufs - 1) * (kBItemFeat / kBFeat),
+              "the stage ring could let a warp reach an item whose buffer is still read");
 constexpr uint32_t kSyncInts = MOE_SYNC_BYTES / 4;
 constexpr int kSpinIters = 1 << 26;                // iteration cap of every wait
+constexpr int kSuspendNs = 20000;                  // mbarrier try_wait suspend-time hint
 constexpr long long kWaitCycles = 4000000000ll;     // ~2 s at 2 GHz: a wait gives up after this
 constexpr long long kStallTestCycles = 20000000ll;  // ~10 ms under MOE_FLAG_TEST_STALL
 
@@ -69,10 +83,15 @@ enum : int {
   kTrCombine = 13,     // consumer cycles combining chunks
   kTrRouteDone = 14,   // routing known to the producer (ns)
   kTrProdEnd = 15,     // producer leaves (ns)
-  kTrRouteLoaded = 16, // routing inputs loaded (ns)
-  kTrRouteTopk = 17,   // top-k done (ns)
+  kTrRouteLoaded = 16, // selection scores computed (ns)
+  kTrRouteTopk = 17,   // publisher: cycles in its gpu-scope atomics
   kTrRoutePerm = 18,   // permutation and active list done (ns)
-  kTraceWords = 20
+  kTrExit = 19,        // CTA leaves the kernel (ns)
+  kTrW5WaitFull = 20,  // consumer warp 5 (no requant duty): waiting for stage data (cycles)
+  kTrW5ComputeB = 21,  // consumer warp 5: cycles in gate/up stages
+  kTrW5ComputeC = 22,  // consumer warp 5: cycles in down stages
+  kTrItemEnd = 23,     // consumer warp 0: cycles at item ends (barrier + requant)
+  kTraceWords = 28
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -135,6 +154,21 @@ struct SyncView {
   }
 };
 
+// CTA-local control words and the publisher's event ring.  Events: an expert's
+// h is complete (e >= 0), or a down stage's contribution to chunk c landed
+// (INT_MIN | contributions << 16 | c).
+struct SharedCtl {
+  int abort;          // a wait gave up: stop issuing, skip the combine
+  int exit_last;      // this CTA is the last one out (zeroes the counters)
+  int n_owned;        // chunks this CTA combines (owned[])
+  int writers_done;   // consumer warps + producer that will post no more events
+  int item_cnt[kPartBufs];  // consumer warps done with an item, by b_items % kPartBufs
+  int pub_head;       // events reserved
+  int pub_tail;       // events taken by the publisher
+  int pub_ev[kPubCap];
+  int pub_seq[kPubCap];  // event i is valid when pub_seq[i % kPubCap] == i + 1
+};
+
 // Routing of the call, held in shared memory by every CTA.
 struct RouteSmem {
   int idx[kMaxR];     // expert of row r = t*k + j
@@ -175,17 +209,20 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                : "memory");
 }
 
-// bounded wait for completion of the phase with the given parity
+// bounded wait for completion of the phase with the given parity.  Each try_wait
+// may suspend the thread (up to kSuspendNs) until the phase completes, so a
+// waiting warp does not take issue slots from the warps sharing its SM
+// sub-partition.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, long long budget) {
   const uint32_t a = smem_u32(bar);
   const long long t0 = clock64();
   for (int i = 0; i < kSpinIters; ++i) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(a), "r"(parity)
+        : "r"(a), "r"(parity), "n"(kSuspendNs)
         : "memory");
     if (done) return true;
     if (clock64() - t0 > budget) return false;
@@ -242,18 +279,30 @@ __device__ __noinline__ void report_timeout(const FusedArgs &a, uint32_t site, u
     a.sync[3] = detail;
 }
 
+// hand an event to the CTA's publisher warp (any thread; bounded wait for room)
+__device__ __noinline__ void pub_post(const FusedArgs &a, SharedCtl &ctl, int ev) {
+  const int i = atomicAdd(&ctl.pub_head, 1);
+  const long long t0 = clock64();
+  while (i - *(volatile int *)&ctl.pub_tail >= kPubCap) {
+    if (clock64() - t0 > a.wait_cycles) {
+      report_timeout(a, 5, (uint32_t)i);
+      *(volatile int *)&ctl.abort = 1;
+      return;
+    }
+  }
+  ctl.pub_ev[i % kPubCap] = ev;
+  __threadfence_block();
+  *(volatile int *)&ctl.pub_seq[i % kPubCap] = i + 1;
+}
+
+__device__ __forceinline__ int chunk_event(uint32_t c, int contrib) {
+  return (int)(0x80000000u | ((uint32_t)contrib << 16) | c);
+}
+
 __device__ __forceinline__ void consumer_sync() {
   asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
 }
 
-// gate/up item end: the requantising warps wait (bar.sync) for every consumer
-// warp's partial sums; the others only signal (bar.arrive) and move on
-__device__ __forceinline__ void item_barrier_wait() {
-  asm volatile("bar.sync 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
-__device__ __forceinline__ void item_barrier_arrive() {
-  asm volatile("bar.arrive 2, %0;" ::"n"(kConsumerWarps * 32) : "memory");
-}
 
 __device__ __forceinline__ uint4 lds16(const int8_t *p) {
   return *reinterpret_cast<const uint4 *>(p);
@@ -304,8 +353,9 @@ __device__ void route_scores(const FusedArgs &a, float *sc) {
 // of the scores (ascending e per lane: strict '>' keeps the lower index) and a
 // butterfly argmax; then the stable permutation (rows by expert, then row
 // order) and the active list, with the T warps' threads as the R <= 64 rows
-__device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
-  const int tid = threadIdx.x, lane = tid & 31, t = tid >> 5;
+__device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc,
+                             unsigned long long *tr) {
+  const int tid = (int)threadIdx.x - kRouteWarp0 * 32, lane = tid & 31, t = tid >> 5;
   const uint32_t E = a.E, k = a.k, T = a.T;
   const int R = (int)a.R;
   float *ct = sc + (size_t)t * E;
@@ -337,6 +387,7 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
     }
     __syncwarp();
   }
+  if (tr && tid == 0) tr[24] = global_ns();
   // lane j < k: the sigmoid of slot j; w = s * sigma_j / sum_j sigma_j (in order)
   const float my_sigma =
       (uint32_t)lane < k ? sigmoid_rn(__ldg(a.logits + (size_t)t * E + rs.idx[t * k + lane]))
@@ -345,6 +396,7 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
 #pragma unroll 1
   for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
   if ((uint32_t)lane < k) rs.w[t * k + lane] = __fmul_rn(a.s, __fdiv_rn(my_sigma, sum));
+  if (tr && tid == 0) tr[25] = global_ns();
   route_bar_sync(T);
   // slot of row r = rows before it in (expert, row) order
   if (tid < R) {
@@ -374,6 +426,7 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
       a.off[e] = c;
     }
   }
+  if (tr && tid == 0) tr[26] = global_ns();
   route_bar_sync(T);
   // active list: slot p opens an entry when its expert differs from slot p-1's;
   // the entry's index is the number of openings before p
@@ -421,8 +474,8 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc) {
 
 // ---------------------------------------------------------------- the kernel
 // Shared-memory carve-up (all offsets multiples of 16 bytes):
-//   stages[NS][stage_bytes] | xq_s[T][d] | xs_s[T][d/32] | part[2][32][KS][2][2] |
-//   desc[8] | full[8] | empty[8] | route_bar | misc[4] | RouteSmem | owned[n_chunks] |
+//   stages[NS][stage_bytes] | xq_s[T][d] | xs_s[T][d/32] | part[3][32][KS][2][2] |
+//   desc[8] | full[8] | empty[8] | route_bar | SharedCtl | RouteSmem | owned[n_chunks] |
 //   route scores[T][E]
 // NT: token count known at compile time (1 or 2): the one-token kernel has no
 // second-row code.
@@ -436,12 +489,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   int8_t *xq_s = (int8_t *)(stages + (size_t)NS * a.stage_bytes);
   float *xs_s = (float *)(xq_s + (size_t)NT * d);
   float *part = xs_s + (size_t)NT * nb;  // [2][feature 32][K part][row 2][g,u]
-  StageDesc *desc = (StageDesc *)(part + 2 * kBItemFeat * kKSplit * kMaxT * 2);
+  StageDesc *desc = (StageDesc *)(part + kPartBufs * kBItemFeat * kKSplit * kMaxT * 2);
   uint64_t *full = (uint64_t *)(desc + kMaxStages);
   uint64_t *empty = full + kMaxStages;
   uint64_t *route_bar = empty + kMaxStages;  // the consumers' routing is in RouteSmem
-  volatile int *s_misc = (volatile int *)(route_bar + 2);  // [0] abort, [1] exit-last, [2] owned
-  RouteSmem &rs = *(RouteSmem *)(s_misc + 4);
+  SharedCtl &ctl = *(SharedCtl *)(route_bar + 2);
+  volatile int *s_abort = &ctl.abort;
+  int *item_cnt = ctl.item_cnt;
+  RouteSmem &rs = *(RouteSmem *)(&ctl + 1);
   int *owned = (int *)(&rs + 1);  // [n_chunks] chunks whose last contribution this CTA landed
   float *route_scratch = (float *)(owned + (a.n_chunks + 3) / 4 * 4);  // [T][E] scores
 
@@ -459,9 +514,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       mbar_init(&empty[i], kConsumerWarps);
     }
     mbar_init(route_bar, 1);
-    s_misc[0] = 0;
-    s_misc[1] = 0;
-    s_misc[2] = 0;
+    ctl.abort = ctl.exit_last = ctl.n_owned = ctl.writers_done = 0;
+    for (int i = 0; i < kPartBufs; ++i) ctl.item_cnt[i] = 0;
+    ctl.pub_head = ctl.pub_tail = 0;
+    for (int i = 0; i < kPubCap; ++i) ctl.pub_seq[i] = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -469,19 +525,18 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   const uint32_t n_sh = a.fs / kBItemFeat;  // shared-expert gate/up items
   const uint32_t fb = a.f / kBItemFeat;      // gate/up items per routed expert
 
-  if (warp == kConsumerWarps) {
+  if (warp == kProducerWarp) {
     // ============================ producer (lane 0; the warp's other lanes wait at the end)
     if (lane == 0) {
       uint32_t g = 0;  // stages issued
       bool routed = false;
       uint32_t U = 0, NB = 0, total = 0;
       // per ring slot: what completes when the consumers release it
-      //   ready_e >= 0: last stage of a gate/up item of that expert
-      //   chunk  >= 0: a down stage contributing to that output chunk (n_contrib)
-      int slot_ready_e[kMaxStages], slot_chunk[kMaxStages], slot_contrib[kMaxStages];
+      //   chunk >= 0: a down stage contributing to that output chunk (n_contrib)
+      // (an expert's h readiness is raised by the warps that requantise it)
+      int slot_chunk[kMaxStages], slot_contrib[kMaxStages];
       unsigned long long p_wait_empty = 0, p_wait_route = 0, p_items = 0, p_wait_ready = 0;
-      for (int i = 0; i < kMaxStages; ++i) slot_ready_e[i] = slot_chunk[i] = slot_contrib[i] = -1;
-      int n_owned = 0;
+      for (int i = 0; i < kMaxStages; ++i) slot_chunk[i] = slot_contrib[i] = -1;
       // queue order: shared gate/up | routed gate/up | shared down | routed down.
       // Only the shared gate/up items are known before routing.
       const uint32_t n_pre = n_sh;
@@ -492,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         p_wait_route += clock64() - t_rw;
         if (!ok) {
           report_timeout(a, 1, 0);
-          s_misc[0] = 1;
+          *s_abort = 1;
           return false;
         }
         if (tr) tr[kTrRouteDone] = global_ns();
@@ -504,17 +559,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       };
       // a stage was released by the consumers: publish what it completed
       auto settle = [&](uint32_t st) {
-        if (slot_ready_e[st] >= 0) red_release_add(&SV.ready[slot_ready_e[st]], 1u);
         if (slot_chunk[st] >= 0) {
           // a shared-expert down stage issued before routing: the number of
           // contributions per chunk (routed experts + 1) is learnt now
           if (slot_contrib[st] < 0 && (routed || learn_routing())) slot_contrib[st] = (int)U + 1;
-          const uint32_t c = (uint32_t)slot_chunk[st];
-          if (slot_contrib[st] > 0 &&
-              atom_acq_rel_add(&SV.chunk[c], 1u) + 1 == (uint32_t)slot_contrib[st])
-            owned[n_owned++] = (int)c;  // this CTA combines chunk c at its end
+          if (slot_contrib[st] > 0)
+            pub_post(a, ctl, chunk_event((uint32_t)slot_chunk[st], slot_contrib[st]));
         }
-        slot_ready_e[st] = slot_chunk[st] = -1;
+        slot_chunk[st] = -1;
       };
       uint32_t item = atomicAdd(SV.queue, 1u);
       for (;;) {
@@ -522,9 +574,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const uint32_t next_item = atomicAdd(SV.queue, 1u);
         ++p_items;
         if (!routed && item >= n_pre && !learn_routing()) {
-          s_misc[0] = 1;
+          *s_abort = 1;
         }
-        const bool end = s_misc[0] || (routed && item >= total);
+        const bool end = *s_abort || (routed && item >= total);
         StageDesc dsc;
         dsc.kind = kKindEnd;
         int nsub = 1;
@@ -581,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           p_wait_empty += clock64() - t_we;
           if (!empty_ok) {
             report_timeout(a, 2, g);
-            s_misc[0] = 1;
+            *s_abort = 1;
             dsc.kind = kKindEnd;
           }
           // the slot's previous contents were released: publish their effects once,
@@ -629,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             const long long t_wr = clock64();
             const uint32_t need = (K / kBItemFeat);
             // while waiting, publish whatever older stages the consumers have
-            // released: one of them may complete the very expert waited for
+            // released (chunk contributions)
             bool ready_ok = false;
             for (int it = 0; it < kSpinIters; ++it) {
               if (ld_acquire(&SV.ready[dsc.e]) >= need) {
@@ -637,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
                 break;
               }
               for (uint32_t q = (g + 1 > NS ? g + 1 - NS : 0); q < g; ++q)
-                if ((slot_ready_e[q % NS] >= 0 || slot_chunk[q % NS] >= 0) &&
+                if (slot_chunk[q % NS] >= 0 &&
                     mbar_test(&empty[q % NS], (q / NS) & 1u))
                   settle(q % NS);
               if (clock64() - t_wr > a.wait_cycles) break;
@@ -647,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             if (!ready_ok) {
               // the consumers get an END stage once the weights have landed
               report_timeout(a, 4, ((uint32_t)dsc.e << 16) | __ldcg(&SV.ready[dsc.e]));
-              s_misc[0] = 1;
+              *s_abort = 1;
               dsc.kind = kKindEnd;
               desc[st] = dsc;
               mbar_arrive(&full[st]);
@@ -670,7 +722,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             mbar_arrive(&full[st]);
           }
           settle_prev();
-          if (dsc.kind == kKindB && sub == kBItemFeat / kBFeat - 1) slot_ready_e[st] = dsc.e;
           if (dsc.kind == kKindC) {
             slot_chunk[st] = dsc.item_first;
             slot_contrib[st] = dsc.n_contrib;
@@ -683,7 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       }
       // drain: wait for the consumers to release every stage still held and
       // publish its effects (the END stage itself is never released)
-      if (!s_misc[0]) {
+      if (!*s_abort) {
         for (uint32_t q = (g > NS ? g - NS : 0); q + 1 < g; ++q) {
           const uint32_t st = q % NS;
           if (!mbar_wait(&empty[st], (q / NS) & 1u, a.wait_cycles)) {
@@ -693,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           settle(st);
         }
       }
-      s_misc[2] = n_owned;
+      atomicAdd(&ctl.writers_done, 1);  // no more events from the producer
       if (tr) {
         tr[kTrProdEnd] = global_ns();
         tr[kTrWaitEmpty] = p_wait_empty;
@@ -701,6 +752,53 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         tr[kTrItems] = p_items;
         tr[kTrWaitReady] = p_wait_ready;
       }
+    }
+    __syncwarp();
+  } else if (warp == kPublisherWarp) {
+    // ============================ publisher (lane 0): takes the CTA's events in
+    // order and does their gpu-scope atomics, so that no producer or consumer
+    // warp waits on them.  h readiness: a release add (the requantising warp's
+    // stores were ordered before the event by a CTA-scope fence).  A chunk
+    // contribution: an acq_rel add; the CTA landing the last one combines it.
+    if (lane == 0) {
+      int n_owned = 0;
+      const long long t_pub = clock64();
+      unsigned long long busy = 0;
+      for (int i = 0;; ++i) {
+        bool have = false;
+        const long long t0 = clock64();
+        for (int it = 0; it < kSpinIters; ++it) {
+          if (*(volatile int *)&ctl.pub_seq[i % kPubCap] == i + 1) {
+            have = true;
+            break;
+          }
+          if (*(volatile int *)&ctl.writers_done == kConsumerWarps + 1 &&
+              i >= *(volatile int *)&ctl.pub_head)
+            break;
+          if (clock64() - t0 > a.wait_cycles) {
+            report_timeout(a, 6, (uint32_t)i);
+            *s_abort = 1;
+            break;
+          }
+          __nanosleep(256);
+        }
+        if (!have) break;
+        __threadfence_block();
+        const long long t1 = clock64();
+        const int ev = ctl.pub_ev[i % kPubCap];
+        *(volatile int *)&ctl.pub_tail = i + 1;
+        if (ev >= 0) {
+          red_release_add(&SV.ready[ev], 1u);
+        } else {
+          const uint32_t c = (uint32_t)ev & 0xFFFFu;
+          const uint32_t contrib = ((uint32_t)ev >> 16) & 0x7FFFu;
+          if (atom_acq_rel_add(&SV.chunk[c], 1u) + 1 == contrib) owned[n_owned++] = (int)c;
+        }
+        busy += clock64() - t1;
+      }
+      ctl.n_owned = n_owned;
+      if (tr) tr[kTrRouteTopk] = busy;
+      (void)t_pub;
     }
     __syncwarp();
   } else {
@@ -730,16 +828,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     };
     const uint32_t xw = (uint32_t)kConsumerWarps - T;  // quantising warps
     float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-    if ((uint32_t)warp >= T && warp - T < n_quad) xv = __ldg(x4 + (size_t)(warp - T) * 32 + lane);
+    {
+      const uint32_t rw0 = (uint32_t)(warp - kRouteWarp0);
+      const uint32_t xi0 = (uint32_t)warp < (uint32_t)kRouteWarp0 ? warp : warp - T;
+      if (rw0 >= T && xi0 < n_quad) xv = __ldg(x4 + (size_t)xi0 * 32 + lane);
+    }
     route_scores(a, route_scratch);
     consumer_sync();
-    if ((uint32_t)warp < T) {
-      route_select(a, rs, route_scratch);
-      if (tr && tid == 0) tr[kTrRoutePerm] = global_ns();
-      if (tid == 0 && !a.stall_test) mbar_arrive(route_bar);  // the producer may take routed items
+    if (tr && tid == 0) tr[kTrRouteLoaded] = global_ns();
+    const uint32_t rw = (uint32_t)(warp - kRouteWarp0);  // routing warp index (token)
+    if (rw < T) {
+      route_select(a, rs, route_scratch, tr);
+      if (tr && rw == 0 && lane == 0) tr[kTrRoutePerm] = global_ns();
+      if (rw == 0 && lane == 0 && !a.stall_test) mbar_arrive(route_bar);  // routed items may go
     } else {
+      const uint32_t xi = (uint32_t)warp < (uint32_t)kRouteWarp0 ? warp : warp - T;  // 0..xw-1
 #pragma unroll 1
-      for (uint32_t q = warp - T; q < n_quad; q += xw) {
+      for (uint32_t q = xi; q < n_quad; q += xw) {
         const float4 v = xv;
         if (q + xw < n_quad) xv = __ldg(x4 + (size_t)(q + xw) * 32 + lane);
         quant_quad(q, v);
@@ -749,11 +854,24 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     if (tr && tid == 0) tr[kTrXqDone] = global_ns();
 
     // trace accumulators live in registers; written once when the consumers leave
-    unsigned long long c_wait_full = 0, c_b = 0, c_c = 0, n_b = 0, n_c = 0;
+    unsigned long long c_wait_full = 0, c_b = 0, c_c = 0, n_b = 0, n_c = 0, c_item = 0;
     // gate/up: warp w takes feature w / kKSplit of the stage, K part w % kKSplit
     const uint32_t half = warp % kKSplit, fw = warp / kKSplit;
     const uint32_t nbh = nb / kKSplit;  // 32-blocks per K part
     const uint32_t nc = d / (16 * kKSplit);  // 16-byte chunks per K part
+    // one token: the warp's K part of x never changes, so its codes and block
+    // scales stay in registers for every gate/up stage (lane: chunks lane + 32i)
+    uint4 xr[kXRegs];
+    float xsr[kXRegs];
+    if (NT == 1) {
+#pragma unroll
+      for (int i = 0; i < kXRegs; ++i) {
+        const uint32_t c = lane + 32u * i;
+        const bool ok = c < nc;
+        xr[i] = ok ? lds16(xq_s + (size_t)half * (d / kKSplit) + 16 * c) : make_uint4(0, 0, 0, 0);
+        xsr[i] = ok ? xs_s[half * nbh + (c >> 1)] : 0.0f;
+      }
+    }
     uint32_t b_items = 0;  // gate/up items finished by this CTA (part[] buffer parity)
     uint32_t g = 0;
     for (;; ++g) {
@@ -789,7 +907,27 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const float *xs1p = xs_s + tok1 * nb + half * nbh;
         const bool even = (lane & 1) == 0;
         float g0 = 0.0f, u0 = 0.0f, g1 = 0.0f, u1 = 0.0f;
-        {
+        if (NT == 1) {
+          // x from registers: only the weights and their scales come from the stage
+#pragma unroll
+          for (int i = 0; i < kXRegs; ++i) {
+            if (32u * i < nc) {  // warp-uniform
+              const uint32_t c = lane + 32u * i;
+              const bool ok = c < nc;
+              const uint4 z = make_uint4(0, 0, 0, 0);
+              const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
+              int pg = dot16(wg, xr[i]), pu = dot16(wu, xr[i]);
+              pg += __shfl_xor_sync(0xffffffffu, pg, 1);
+              pu += __shfl_xor_sync(0xffffffffu, pu, 1);
+              const uint32_t blk = ok ? c >> 1 : 0;
+              const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
+              if (even && ok) {
+                g0 = __fmaf_rn((float)pg, sg * xsr[i], g0);
+                u0 = __fmaf_rn((float)pu, su * xsr[i], u0);
+              }
+            }
+          }
+        } else {
         // every lane runs the same trip count (the shuffles need the full warp);
         // chunk pairs never straddle nc (nc is even)
 #pragma unroll 2
@@ -822,49 +960,82 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           }
         }
         }
-        g0 = warp_sum(g0);
-        u0 = warp_sum(u0);
+        // warp sums of (g0, u0) [, (g1, u1)] in one butterfly: the first step(s)
+        // hand each lane half (quarter) one of the values, then 4 (3) steps
+        // finish them; the sums land in lanes 0, 16 [, 8, 24]
+        float red;
         if (NT > 1 && nr > 1) {
-          g1 = warp_sum(g1);
-          u1 = warp_sum(u1);
+          const bool lo = lane < 16;
+          float x0 = (lo ? g0 : u0) + __shfl_xor_sync(0xffffffffu, lo ? u0 : g0, 16);
+          float x1 = (lo ? g1 : u1) + __shfl_xor_sync(0xffffffffu, lo ? u1 : g1, 16);
+          const bool lo8 = (lane & 8) == 0;
+          red = (lo8 ? x0 : x1) + __shfl_xor_sync(0xffffffffu, lo8 ? x1 : x0, 8);
+#pragma unroll
+          for (int o = 4; o > 0; o >>= 1) red += __shfl_xor_sync(0xffffffffu, red, o);
+        } else {
+          const bool lo = lane < 16;
+          red = (lo ? g0 : u0) + __shfl_xor_sync(0xffffffffu, lo ? u0 : g0, 16);
+#pragma unroll
+          for (int o = 8; o > 0; o >>= 1) red += __shfl_xor_sync(0xffffffffu, red, o);
         }
-        // partial sums, double-buffered by item parity: the requant of item i reads
-        // buffer i&1 while the other warps may already fill buffer (i+1)&1 (the
-        // stage ring keeps them from reaching item i+2)
-        float *pbuf = part + (size_t)(b_items & 1) * kBItemFeat * kKSplit * kMaxT * 2;
-        if (lane == 0) {
+        // partial sums [feature][K part][row][g, u] in buffer b_items % kPartBufs
+        // (see kPartBufs: the requant of an item never races the refill)
+        const uint32_t pb = b_items % kPartBufs;
+        float *pbuf = part + (size_t)pb * kBItemFeat * kKSplit * kMaxT * 2;
+        {
           float *pp =
               pbuf + ((size_t)((dsc.first - dsc.item_first) + fw) * kKSplit + half) * kMaxT * 2;
-          pp[0] = g0;
-          pp[1] = u0;
-          pp[2] = g1;
-          pp[3] = u1;
-        }
-        if (dsc.sub == kBItemFeat / kBFeat - 1) {
-          ++b_items;
-          // the item's 32 features are done: h = silu(g)*u, requantised (warp r: row r)
-          if (warp < nr) item_barrier_wait(); else item_barrier_arrive();
-          if (warp < nr) {
-            const float *pp = pbuf + (size_t)lane * kKSplit * kMaxT * 2;
-            float gv = pp[warp * 2], uv = pp[warp * 2 + 1];
-#pragma unroll
-            for (int q = 1; q < kKSplit; ++q) {
-              gv = __fadd_rn(gv, pp[q * kMaxT * 2 + warp * 2]);
-              uv = __fadd_rn(uv, pp[q * kMaxT * 2 + warp * 2 + 1]);
-            }
-            const float v = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
-            float amax = fabsf(v);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-              amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            const float sc = __fdiv_rn(amax, 127.0f);
-            const size_t slot = (size_t)(warp == 0 ? dsc.slot[0] : dsc.slot[kMaxT - 1]);
-            a.hq[slot * fmax + dsc.item_first + lane] = (int8_t)quant_one(v, sc);
-            if (lane == 0) a.hs[slot * (fmax / 32) + dsc.item_first / 32] = sc;
+          if (NT > 1 && nr > 1) {
+            // lane 0: g0, 8: g1, 16: u0, 24: u1
+            if ((lane & 7) == 0) pp[((lane >> 3) & 1) * 2 + (lane >> 4)] = red;
+          } else {
+            if ((lane & 15) == 0) pp[lane >> 4] = red;
           }
         }
+        // the stage's data is no longer needed: release it before the item's
+        // requant, so that the producer can refill the slot meanwhile
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);  // the producer publishes h readiness
+        if (lane == 0) mbar_arrive(&empty[st]);
+        if (dsc.sub == kBItemFeat / kBFeat - 1) {
+          const long long t_item = clock64();
+          // the item's 32 features: the last warp to finish its part computes
+          // h = silu(g)*u and requantises it (lane = feature), then raises the
+          // expert's readiness count (gpu-scope release) -- no warp waits
+          int last = 0;
+          if (lane == 0) {
+            __threadfence_block();
+            last = atomicAdd(&item_cnt[pb], 1) == kConsumerWarps - 1;
+            if (last) {
+              item_cnt[pb] = 0;
+              __threadfence_block();
+            }
+          }
+          if (__shfl_sync(0xffffffffu, last, 0)) {
+            __syncwarp();
+            const float *pp = pbuf + (size_t)lane * kKSplit * kMaxT * 2;
+            for (int r = 0; r < nr; ++r) {
+              float gv = pp[r * 2], uv = pp[r * 2 + 1];
+#pragma unroll
+              for (int q = 1; q < kKSplit; ++q) {
+                gv = __fadd_rn(gv, pp[q * kMaxT * 2 + r * 2]);
+                uv = __fadd_rn(uv, pp[q * kMaxT * 2 + r * 2 + 1]);
+              }
+              const float v = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
+              float amax = fabsf(v);
+#pragma unroll
+              for (int o = 16; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+              const float sc = __fdiv_rn(amax, 127.0f);
+              const size_t slot = (size_t)(r == 0 ? dsc.slot[0] : dsc.slot[kMaxT - 1]);
+              a.hq[slot * fmax + dsc.item_first + lane] = (int8_t)quant_one(v, sc);
+              if (lane == 0) a.hs[slot * (fmax / 32) + dsc.item_first / 32] = sc;
+            }
+            __syncwarp();
+            if (lane == 0) pub_post(a, ctl, dsc.e);  // the publisher raises ready[e]
+          }
+          ++b_items;
+          c_item += clock64() - t_item;
+        }
         n_b += 1;
         c_b += clock64() - t_got;
       } else {
@@ -878,11 +1049,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const size_t slot0 = (size_t)dsc.slot[0], slot1 = (size_t)dsc.slot[kMaxT - 1];
         const uint32_t ncr = K / 16;  // 16-byte chunks per down row
         const bool even = (lane & 1) == 0;
-        // rows m0, m0+16, m0+32 of the stage: each h chunk is read once for three rows
-        for (int m0 = warp; m0 < dsc.count; m0 += 3 * kConsumerWarps) {
-          float acc[3][kMaxT];
+        // rows m0, m0+16, .. of the stage: each h chunk is read once for kDnRows rows
+        for (int m0 = warp; m0 < dsc.count; m0 += kDnRows * kConsumerWarps) {
+          float acc[kDnRows][kMaxT];
 #pragma unroll
-          for (int j = 0; j < 3; ++j) acc[j][0] = acc[j][1] = 0.0f;
+          for (int j = 0; j < kDnRows; ++j) acc[j][0] = acc[j][1] = 0.0f;
           for (uint32_t c0 = 0; c0 < ncr; c0 += 32) {  // same trip count in every lane
             const uint32_t c = c0 + lane;
             const bool ok = c < ncr;
@@ -897,7 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               hs1 = hs_st[kb + blk];
             }
 #pragma unroll
-            for (int j = 0; j < 3; ++j) {
+            for (int j = 0; j < kDnRows; ++j) {
               const int m = m0 + j * kConsumerWarps;
               const bool live = ok && m < dsc.count;
               const uint4 wd = live ? lds16(qc + (size_t)m * K + 16 * c) : make_uint4(0, 0, 0, 0);
@@ -913,7 +1084,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             }
           }
 #pragma unroll
-          for (int j = 0; j < 3; ++j) {
+          for (int j = 0; j < kDnRows; ++j) {
             const int m = m0 + j * kConsumerWarps;
             const float v0 = warp_sum(acc[j][0]);
             const float v1 = nr > 1 ? warp_sum(acc[j][1]) : 0.0f;
@@ -929,23 +1100,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         c_c += clock64() - t_got;
       }
     }
+    if (lane == 0) atomicAdd(&ctl.writers_done, 1);  // this warp posts no more events
     if (tr && tid == 0) {
       tr[kTrConsEnd] = global_ns();
       tr[kTrWaitFull] = c_wait_full;
+      tr[kTrItemEnd] = c_item;
       tr[kTrComputeB] = c_b;
       tr[kTrComputeC] = c_c;
       tr[kTrStagesB] = n_b;
       tr[kTrStagesC] = n_c;
+    }
+    if (tr && warp == 5 && lane == 0) {
+      tr[kTrW5WaitFull] = c_wait_full;
+      tr[kTrW5ComputeB] = c_b;
+      tr[kTrW5ComputeC] = c_c;
     }
   }
 
   // ============================ exit: combine the chunks this CTA completed last
   __syncthreads();
   const long long t_comb = clock64();
-  if (warp < kConsumerWarps && !s_misc[0]) {
+  if (warp < kConsumerWarps && !*s_abort) {
     // y = o_shared + sum_j w_j o_j, shared first, then slots in order; all owned
     // chunks in one pass (every load of a thread is independent: one round trip)
-    const uint32_t n_own = (uint32_t)s_misc[2], per = T * a.c_rows;
+    const uint32_t n_own = (uint32_t)ctl.n_owned, per = T * a.c_rows;
     for (uint32_t i = tid; i < n_own * per; i += kConsumerWarps * 32) {
       const uint32_t c = (uint32_t)owned[i / per], r = i % per;
       const uint32_t t = r / a.c_rows, m = c * a.c_rows + r % a.c_rows;
@@ -959,12 +1137,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   if (tr && tid == 0) tr[kTrCombine] += clock64() - t_comb;
   __syncthreads();
   // the last CTA out zeroes the counters for the next call
-  if (tid == 0) s_misc[1] = atom_acq_rel_add(SV.done, 1u) + 1 == gridDim.x;
+  if (tid == 0) ctl.exit_last = atom_acq_rel_add(SV.done, 1u) + 1 == gridDim.x;
   __syncthreads();
-  if (s_misc[1]) {
+  if (*(volatile int *)&ctl.exit_last) {
     for (uint32_t i = tid; i < SV.n_clear; i += kThreads)
       if (i != 2 && i != 3) a.sync[i] = 0u;
   }
+  if (tr && tid == 0) tr[kTrExit] = global_ns();
 }
 
 }  // namespace
@@ -985,6 +1164,7 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (D.top_k > 32) return false;
   if (D.d % 256 || D.f % 256 || D.f_shared % 256) return false;
   if (D.d % (32 * kKSplit * 2)) return false;  // whole, even chunk counts per K part
+  if (D.d > 16u * kKSplit * 32 * kXRegs) return false;  // x of a K part fits the registers
   if (c.R > (uint32_t)kMaxR) return false;
   const uint32_t d = D.d, fmax = c.fmax;
   const size_t b_bytes = (size_t)kBFeat * 2 * (d + d / 16);
@@ -999,8 +1179,9 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (4 + D.n_expert + 1 + n_chunks + 1 > kSyncInts) return false;
   const size_t stage = (b_bytes + 127) / 128 * 128;
   const size_t rest = (size_t)c.T * d + (size_t)c.T * (d / 32) * 4 +
-                      2 * kBItemFeat * kKSplit * kMaxT * 2 * 4 + kMaxStages * sizeof(StageDesc) +
-                      2 * kMaxStages * 8 + 16 + 16 + sizeof(RouteSmem) +
+                      kPartBufs * kBItemFeat * kKSplit * kMaxT * 2 * 4 +
+                      kMaxStages * sizeof(StageDesc) +
+                      2 * kMaxStages * 8 + 16 + sizeof(SharedCtl) + sizeof(RouteSmem) +
                       (size_t)(n_chunks + 3) / 4 * 16 +
                       (size_t)c.T * D.n_expert * 4 + 128;
   int dev = 0, max_smem = 0;

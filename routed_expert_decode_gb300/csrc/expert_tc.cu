@@ -36,6 +36,7 @@ constexpr int kTcThreads = 14 * 32;
 constexpr int kEpiWarps = 8;
 constexpr long long kTcWaitCycles = 4000000000ll;  // ~2 s
 constexpr int kTcSpinIters = 1 << 26;
+constexpr int kSuspendNs = 20000;  // try_wait suspend-time hint: waiting warps sleep, not spin
 
 struct TcArgs {
   uint32_t E, d, f, fs, R, fmax, nb_in;  // nb_in: 32-blocks along K
@@ -81,10 +82,10 @@ __device__ __forceinline__ bool bar_wait(uint64_t *b, uint32_t parity) {
   for (int i = 0; i < kTcSpinIters; ++i) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(s32(b)), "r"(parity)
+        : "r"(s32(b)), "r"(parity), "n"(kSuspendNs)
         : "memory");
     if (done) return true;
     if (clock64() - t0 > kTcWaitCycles) return false;

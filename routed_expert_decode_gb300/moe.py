@@ -35,7 +35,8 @@ FLAG_TRACE = 0x10
 TRACE_FIELDS = ("start_ns", "xq_done_ns", "first_stage_ns", "wait_full_cyc", "wait_ready_cyc",
                 "stages_b", "stages_c", "cons_end_ns", "wait_empty_cyc", "wait_route_cyc",
                 "items", "compute_b_cyc", "compute_c_cyc", "combine_cyc", "route_done_ns",
-                "prod_end_ns", "route_loaded_ns", "route_topk_ns", "route_perm_ns", "spare")
+                "prod_end_ns", "route_loaded_ns", "route_topk_ns", "route_perm_ns", "exit_ns",
+                "w5_wait_full_cyc", "w5_compute_b_cyc", "w5_compute_c_cyc", "item_end_cyc")
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
