@@ -359,34 +359,71 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc,
   const uint32_t E = a.E, k = a.k, T = a.T;
   const int R = (int)a.R;
   float *ct = sc + (size_t)t * E;
+  if (E <= 256) {
+    // the lane's (up to) 8 scores in registers; each round takes the lane-local
+    // best, a butterfly argmax, and the winner's entry is retired
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) v[i] = (uint32_t)lane + 32u * i < E ? ct[lane + 32 * i] : -INFINITY;
 #pragma unroll 1
-  for (uint32_t j = 0; j < k; ++j) {
-    float bs = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll 1
-    for (uint32_t e = lane; e < E; e += 32) {
-      const float v = ct[e];
-      if (v > bs) {
-        bs = v;
-        be = (int)e;
+    for (uint32_t j = 0; j < k; ++j) {
+      float bs = v[0];
+      int bi = 0;
+#pragma unroll
+      for (int i = 1; i < 8; ++i)
+        if (v[i] > bs) {  // ascending e per lane: strict '>' keeps the lower index
+          bs = v[i];
+          bi = i;
+        }
+      int be = bs == -INFINITY ? 0x7fffffff : lane + 32 * bi;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ranks_before(os, oe, bs, be)) {
+          bs = os;
+          be = oe;
+        }
       }
-    }
-#pragma unroll 1
-    for (int o = 16; o > 0; o >>= 1) {
-      const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ranks_before(os, oe, bs, be)) {
-        bs = os;
-        be = oe;
+      if ((be & 31) == lane) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (i == (be >> 5)) v[i] = -INFINITY;
       }
+      if (lane == 0) rs.idx[t * k + j] = be;
     }
-    __syncwarp();
-    if (lane == 0) {
-      ct[be] = -INFINITY;
-      rs.idx[t * k + j] = be;
+  } else {
+    // larger E: k rounds of a strided scan of the scores in shared memory
+#pragma unroll 1
+    for (uint32_t j = 0; j < k; ++j) {
+      float bs = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll 1
+      for (uint32_t e = lane; e < E; e += 32) {
+        const float v = ct[e];
+        if (v > bs) {
+          bs = v;
+          be = (int)e;
+        }
+      }
+#pragma unroll 1
+      for (int o = 16; o > 0; o >>= 1) {
+        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+        if (ranks_before(os, oe, bs, be)) {
+          bs = os;
+          be = oe;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        ct[be] = -INFINITY;
+        rs.idx[t * k + j] = be;
+      }
+      __syncwarp();
     }
-    __syncwarp();
   }
+  __syncwarp();
   if (tr && tid == 0) tr[24] = global_ns();
   // lane j < k: the sigmoid of slot j; w = s * sigma_j / sum_j sigma_j (in order)
   const float my_sigma =
