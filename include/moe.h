@@ -189,7 +189,7 @@ const char *moe_layer_path(const moe_desc *desc, uint32_t T);
  * routed row count exceeds it runs its block dots on tcgen05 tensor cores,
  * the rest on the dp4a GEMV.  -1 when no expert of such a call can take the
  * tensor path (the fused decode path, 2-bit routed weights, dims not a
- * multiple of 128, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
+ * multiple of 256, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
 int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);
 
 /* Name of stage i of that path (what moe_layer_timed's events bracket),

@@ -36,6 +36,10 @@ constexpr int kTcThreads = 14 * 32;
 constexpr int kEpiWarps = 8;
 constexpr long long kTcWaitCycles = 4000000000ll;  // ~2 s
 constexpr int kTcSpinIters = 1 << 26;
+constexpr uint32_t kSG = 4;        // stages per scale group (8 blocks: a 16-byte fp16 box row)
+constexpr uint32_t kScSlots = 3;   // scale groups in flight
+// a scale slot: weight scales [MAT<=2][kBM rows][8] fp16 + activation scales [kBN rows][8] fp32
+constexpr uint32_t kScSlotBytes = 2 * kBM * kSG * 2 * 2 + kBN * kSG * 2 * 4;
 constexpr int kSuspendNs = 20000;  // try_wait suspend-time hint: waiting warps sleep, not spin
 
 struct TcArgs {
@@ -55,12 +59,29 @@ struct TcArgs {
   uint32_t tap_nb;                       // blocks per tap row
   uint32_t *err;
   uint32_t n_stages, stage_bytes;
+  unsigned long long *trace;  // MOE_FLAG_TRACE: kTcTraceWords per CTA, else null
+};
+
+// MOE_FLAG_TRACE words per CTA (cycles), gate/up at 0.., down at 8..
+enum : int {
+  kTcTrProdWaitEmpty = 0,  // producer waiting for a free stage
+  kTcTrMmaWaitA = 1,       // MMA issuer waiting for converted operands
+  kTcTrMmaWaitD = 2,       // MMA issuer waiting for a free accumulator buffer
+  kTcTrCvtWaitFull = 3,    // converters waiting for the TMA data
+  kTcTrEpiWaitD = 4,       // epilogue waiting for accumulators
+  kTcTrEpiOut = 5,         // epilogue writing tile outputs
+  kTcTrTotal = 6,          // kernel cycles (thread 0)
+  kTcTrStages = 7,         // stages processed
+  kTcTraceStride = 28      // words per CTA in the trace region
 };
 
 struct TcMaps {
-  CUtensorMap w[2];   // routed weights, [E * rows][K] int8
-  CUtensorMap sw[2];  // shared expert weights, [rows][K] int8
-  CUtensorMap act;    // activations, [slots][K] fp16, 128B swizzle
+  CUtensorMap w[2];    // routed weights, [E * rows][K] int8
+  CUtensorMap sw[2];   // shared expert weights, [rows][K] int8
+  CUtensorMap act;     // activations, [slots][K] fp16, 128B swizzle
+  CUtensorMap ws[2];   // routed weight scales, [E * rows][K/32] fp16, box 8 x 128
+  CUtensorMap sws[2];  // shared expert weight scales, [rows][K/32] fp16, box 8 x 128
+  CUtensorMap xs;      // activation scales, [slots][K/32] fp32, box 8 x 64
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -121,22 +142,19 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
           s32(bar))
       : "memory");
 }
-// 32 consecutive fp32 columns of this warp's 32 TMEM lanes
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes into v[0..15]
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
@@ -152,7 +170,14 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
 }
 
 // instruction descriptor: D f32, A and B f16, both K-major, M = 128, N = kBN
-constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(kBM >> 4) << 24);
+__device__ __forceinline__ uint32_t idesc_for(uint32_t n) { return kIdescBase | ((n >> 3) << 17); }
+
+// MMA width of a tile: its live rows rounded up to 16 (the MMA's N step at M = 128)
+__device__ __forceinline__ int tile_cols(int rows, int n0) {
+  const int live = min(kBN, rows - n0);
+  return (live + 15) & ~15;
+}
 
 // int8 x4 -> two half2, exact: bias to 0..255, place under exponent 2^10, subtract 1152
 __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t &hi) {
@@ -199,6 +224,189 @@ __device__ __forceinline__ TcTile tc_tile(const PlanView &P, const TcArgs &a, in
   return t;
 }
 
+// Stage geometry of a tile: MMA width ncol = live rows rounded up to 16, and
+// gstages = stages whose accumulators share one TMEM buffer (ncol * gstages =
+// kBN, so a buffer is always MAT * 2 * kBN columns).  The epilogue waits, reads
+// and releases once per buffer instead of once per stage.
+struct TileGeom {
+  int ncol, gstages;
+};
+__device__ __forceinline__ TileGeom tile_geom(int rows, int n0) {
+  TileGeom g;
+  const int c = tile_cols(rows, n0);
+  g.ncol = c <= 16 ? 16 : c <= 32 ? 32 : kBN;
+  g.gstages = kBN / g.ncol;
+  return g;
+}
+// TMEM column of (stage-in-buffer si, matrix mi, block bi) in buffer b
+template <int MAT>
+__device__ __forceinline__ uint32_t acc_col(uint32_t b, uint32_t half_cols, int si, int mi, int bi,
+                                            int ncol) {
+  return b * half_cols + (uint32_t)(((si * MAT + mi) * 2 + bi) * ncol);
+}
+
+// Epilogue of one tile.  NCM: columns per warp (16 or 32).  SPLIT (ncol <= 32):
+// warp half h takes the K blocks of parity h over all columns, the halves'
+// partial sums meeting in shared memory at the tile end; !SPLIT (ncol = 64):
+// half h takes columns [32h, 32h + 32) of both blocks.  Warp w reads TMEM lanes
+// 32*(w%4).. (= features).  Per block: acc += dot * (w-scale * x-scale), the
+// scales coming from the scale ring (one slot per kSG stages, filled by TMA).
+struct EpiState {
+  uint32_t tmem, half_cols, KS;
+  uint32_t bufs, scgroups;  // accumulator buffers / scale groups consumed so far
+  uint64_t *d_full, *d_empty, *sc_full, *sc_empty;
+  uint8_t *sc_ring;
+  float *red;
+  volatile int *abort_flag;
+  long long t_wait, t_out;
+};
+
+template <int MAT, bool TAPS, int NCM, bool SPLIT>
+__device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile &t,
+                                      const TileGeom &geo) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ew = warp - 6;               // 0..7
+  const int quarter = warp & 3;          // TMEM lane quarter this warp may read
+  const int half = ew >> 2;
+  const int feat = quarter * 32 + lane;  // feature within the tile (TMEM lane)
+  const bool sh = t.e == (int)a.E;
+  const int width = MAT == 2 ? (int)(sh ? a.fs : a.f) : (int)a.d;
+  const int col0 = SPLIT ? 0 : 32 * half;
+  float acc[MAT][NCM];
+#pragma unroll
+  for (int mi = 0; mi < MAT; ++mi)
+#pragma unroll
+    for (int j = 0; j < NCM; ++j) acc[mi][j] = 0.0f;
+  int jt = -1;  // tapped feature index of this thread, if any
+  if (TAPS) {
+    const int wf = t.m0 + feat;
+#pragma unroll
+    for (int j = kNTap - 1; j >= 0; --j)
+      if ((int)tap_feature(j, width) == wf) jt = j;
+  }
+  for (uint32_t ks0 = 0; ks0 < c.KS; ks0 += geo.gstages) {
+    const uint32_t b = c.bufs & 1u;
+    const long long tw = clock64();
+    if (!bar_wait(&c.d_full[b], (c.bufs >> 1) & 1u)) {
+      atomicOr(a.err, kErrTimeout);
+      *c.abort_flag = 1;
+      return;
+    }
+    c.t_wait += clock64() - tw;
+    tc_fence_after();
+    const uint32_t nst = min((uint32_t)geo.gstages, c.KS - ks0);
+    for (uint32_t si = 0; si < nst; ++si) {
+      const uint32_t ks = ks0 + si;
+      const uint32_t q = c.scgroups % kScSlots;  // scale slot of stage ks
+      if (ks % kSG == 0) {
+        if (!bar_wait(&c.sc_full[q], (c.scgroups / kScSlots) & 1u)) {
+          atomicOr(a.err, kErrTimeout);
+          *c.abort_flag = 1;
+          return;
+        }
+      }
+      const uint8_t *slot = c.sc_ring + (size_t)q * kScSlotBytes;
+      const uint16_t *wsl = (const uint16_t *)slot;                       // [MAT][kBM][8]
+      const float *xsl = (const float *)(slot + MAT * kBM * kSG * 2 * 2);  // [kBN][8]
+      const uint32_t blk0 = (ks % kSG) * 2;  // first block of this stage in the slot
+      float wsc[MAT][2];
+#pragma unroll
+      for (int mi = 0; mi < MAT; ++mi) {
+        const uint32_t pair =
+            *reinterpret_cast<const uint32_t *>(wsl + ((size_t)mi * kBM + feat) * 8 + blk0);
+        wsc[mi][0] = half_bits_to_float((uint16_t)(pair & 0xFFFFu));
+        wsc[mi][1] = half_bits_to_float((uint16_t)(pair >> 16));
+      }
+#pragma unroll
+      for (int bi = 0; bi < 2; ++bi) {
+        if (SPLIT && bi != half) continue;  // warp-uniform
+#pragma unroll
+        for (int mi = 0; mi < MAT; ++mi) {
+          const float ws_b = wsc[mi][bi];
+#pragma unroll
+          for (int c16 = 0; c16 < NCM / 16; ++c16) {
+            float v[32];
+            const uint32_t col = acc_col<MAT>(b, c.half_cols, (int)si, mi, bi, geo.ncol) + col0 +
+                                 16 * c16;
+            tc_ld16(c.tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float xsv = xsl[(col0 + 16 * c16 + j) * 8 + blk0 + bi];
+              acc[mi][16 * c16 + j] = __fmaf_rn(v[j], ws_b * xsv, acc[mi][16 * c16 + j]);
+            }
+            if (TAPS && jt >= 0) {
+              const uint32_t kb = ks * 2 + bi;
+              for (int j = 0; j < 16; ++j) {
+                const int n = col0 + 16 * c16 + j;
+                if (t.n0 + n < t.rows) {
+                  const size_t sl = (size_t)(t.slot0 + t.n0 + n);
+                  const size_t base = MAT == 2 ? ((sl * 2 + mi) * kNTap + jt) * a.tap_nb
+                                               : (sl * kNTap + jt) * a.tap_nb;
+                  a.tap[base + kb] = (int32_t)v[j];
+                }
+              }
+            }
+          }
+        }
+      }
+      if (ks % kSG == kSG - 1 || ks + 1 == c.KS) {  // the scale slot's last stage
+        __syncwarp();
+        if (lane == 0) bar_arrive(&c.sc_empty[q]);
+        ++c.scgroups;
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) bar_arrive(&c.d_empty[b]);
+    ++c.bufs;
+  }
+  const long long t_o = clock64();
+  if (SPLIT) {
+    // odd blocks' partial sums (half 1) join the even blocks' (half 0)
+    if (half == 1) {
+#pragma unroll
+      for (int mi = 0; mi < MAT; ++mi)
+#pragma unroll
+        for (int j = 0; j < NCM; ++j) c.red[((size_t)mi * kBM + feat) * 33 + j] = acc[mi][j];
+    }
+    epi_sync();
+    if (half == 0) {
+#pragma unroll
+      for (int mi = 0; mi < MAT; ++mi)
+#pragma unroll
+        for (int j = 0; j < NCM; ++j)
+          acc[mi][j] = __fadd_rn(acc[mi][j], c.red[((size_t)mi * kBM + feat) * 33 + j]);
+    }
+  }
+  // ---- tile output: this warp's columns (half 0 only when split)
+  if (!SPLIT || half == 0) {
+#pragma unroll
+    for (int j = 0; j < NCM; ++j) {
+      const int n = col0 + j;
+      if (t.n0 + n >= t.rows) break;  // warp-uniform: the tile's live rows end here
+      const size_t sl = (size_t)(t.slot0 + t.n0 + n);
+      if (MAT == 2) {
+        // h = silu(g)*u, requantised over this warp's 32 consecutive features
+        const float gv = acc[0][j], uv = acc[MAT - 1][j];
+        const float h = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
+        float amax = fabsf(h);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        const float sc = __fdiv_rn(amax, 127.0f);
+        const int qv = quant_one(h, sc);
+        const size_t fo = (size_t)t.m0 + feat;
+        a.hq[sl * a.fmax + fo] = (int8_t)qv;
+        a.hperm[sl * a.fmax + fo] = __int2half_rn(qv);
+        if (lane == 0) a.hs[sl * (a.fmax / 32) + fo / 32] = sc;
+      } else {
+        a.o[sl * a.d + t.m0 + feat] = acc[0][j];
+      }
+    }
+  }
+  if (SPLIT) epi_sync();  // red[] is free again
+  c.t_out += clock64() - t_o;
+}
+
 template <int MAT, bool TAPS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_expert_tc(const TcArgs a, const __grid_constant__ TcMaps maps) {
@@ -212,15 +420,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t KS = a.K / kBK;  // stages per tile
   // stage layout: [A16 mat0 16K][A16 mat1 16K][B 8K][A8 mat0 8K][A8 mat1 8K]
   constexpr uint32_t kA16 = kBM * kBK * 2, kB16 = kBN * kBK * 2, kA8 = kBM * kBK;
-  uint8_t *ctrl = tsm + (size_t)NS * a.stage_bytes;
+  uint8_t *sc_ring = tsm + (size_t)NS * a.stage_bytes;  // [kScSlots][kScSlotBytes]
+  uint8_t *ctrl = sc_ring + (size_t)kScSlots * kScSlotBytes;
   uint64_t *ld_full = (uint64_t *)ctrl;          // [NS]
   uint64_t *a_ready = ld_full + 8;               // [NS]
   uint64_t *st_empty = a_ready + 8;              // [NS]
   uint64_t *d_full = st_empty + 8;               // [2]
   uint64_t *d_empty = d_full + 2;                // [2]
-  uint32_t *tmem_holder = (uint32_t *)(d_empty + 2);
+  uint64_t *sc_full = d_empty + 2;               // [kScSlots]
+  uint64_t *sc_empty = sc_full + kScSlots;       // [kScSlots]
+  uint32_t *tmem_holder = (uint32_t *)(sc_empty + kScSlots);
   volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
-  float *xs_stage = (float *)(tmem_holder + 4);  // [2 buffers][2 blocks][kBN]
+  float *red = (float *)(ctrl + 1024);  // [MAT][kBM features][33]: split-K partial sums
   const uint32_t tmem_cols = MAT == 2 ? 512 : 256;
 
   if (tid == 0) {
@@ -232,6 +443,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int i = 0; i < 2; ++i) {
       bar_init(&d_full[i], 1);
       bar_init(&d_empty[i], kEpiWarps);
+    }
+    for (uint32_t i = 0; i < kScSlots; ++i) {
+      bar_init(&sc_full[i], 1);
+      bar_init(&sc_empty[i], kEpiWarps);
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -247,18 +462,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
+  const long long t_start = clock64();
+  long long t_wait0 = 0, t_wait1 = 0, t_out = 0;
+  unsigned long long *tr =
+      a.trace ? a.trace + (size_t)blockIdx.x * kTcTraceStride + (MAT == 2 ? 0 : 8) : nullptr;
 
   if (warp == 0) {
-    // ============================ TMA producer
+    // ============================ TMA producer: weights per stage, scales per kSG stages
     if (lane == 0) {
-      uint32_t g = 0;
+      uint32_t g = 0, scg = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
         const TcTile t = tc_tile<MAT>(P, a, tile);
         const bool sh = t.e == (int)a.E;
         const int wrow = sh ? t.m0 : (int)(t.e * (MAT == 2 ? (int)a.f : (int)a.d)) + t.m0;
         for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
+          if (ks % kSG == 0) {
+            // scales of stages ks .. ks+kSG-1: 8 blocks of the tile's weight rows
+            // and activation rows
+            const uint32_t q = scg % kScSlots, use = scg / kScSlots;
+            const long long tw = clock64();
+            const bool ok_s = use == 0 || bar_wait(&sc_empty[q], (use - 1) & 1u);
+            t_wait0 += clock64() - tw;
+            if (!ok_s) {
+              atomicOr(a.err, kErrTimeout);
+              *abort_flag = 1;
+              break;
+            }
+            uint8_t *slot = sc_ring + (size_t)q * kScSlotBytes;
+            bar_expect(&sc_full[q], MAT * kBM * kSG * 2 * 2 + kBN * kSG * 2 * 4);
+            for (int mi = 0; mi < MAT; ++mi)
+              tma_2d(slot + (size_t)mi * kBM * kSG * 2 * 2, sh ? &maps.sws[mi] : &maps.ws[mi],
+                     (int)(ks * 2), wrow, &sc_full[q]);
+            tma_2d(slot + MAT * kBM * kSG * 2 * 2, &maps.xs, (int)(ks * 2), t.slot0 + t.n0,
+                   &sc_full[q]);
+            ++scg;
+          }
           const uint32_t s = g % NS, use = g / NS;
-          if (use > 0 && !bar_wait(&st_empty[s], (use - 1) & 1u)) {
+          const long long tw = clock64();
+          const bool ok_e = use == 0 || bar_wait(&st_empty[s], (use - 1) & 1u);
+          t_wait0 += clock64() - tw;
+          if (!ok_e) {
             atomicOr(a.err, kErrTimeout);
             *abort_flag = 1;
             break;
@@ -273,14 +516,22 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ============================ MMA issuer
+    // ============================ MMA issuer: a buffer holds gstages stages
     if (lane == 0) {
-      uint32_t g = 0, dbuf_use[2] = {0, 0};
+      uint32_t g = 0, bufs = 0;
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+        const TcTile tt = tc_tile<MAT>(P, a, tile);
+        const TileGeom geo = tile_geom(tt.rows, tt.n0);
+        const uint32_t idesc = idesc_for((uint32_t)geo.ncol);
         for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
-          const uint32_t s = g % NS, use = g / NS, b = g & 1u;
+          const uint32_t s = g % NS, use = g / NS, b = bufs & 1u;
+          const uint32_t si = ks % (uint32_t)geo.gstages;
+          const long long tw = clock64();
           bool ok = bar_wait(&a_ready[s], use & 1u);
-          if (ok && dbuf_use[b] > 0) ok = bar_wait(&d_empty[b], (dbuf_use[b] - 1) & 1u);
+          const long long tw2 = clock64();
+          t_wait0 += tw2 - tw;
+          if (ok && si == 0 && bufs >= 2) ok = bar_wait(&d_empty[b], ((bufs >> 1) - 1) & 1u);
+          t_wait1 += clock64() - tw2;
           if (!ok) {
             atomicOr(a.err, kErrTimeout);
             *abort_flag = 1;
@@ -298,12 +549,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 const uint32_t koff = (uint32_t)(blk * 2 + k16) * 32;  // bytes along K
                 const uint64_t ad = sw128_desc(s32(st + mi * kA16) + koff);
                 const uint64_t bd = sw128_desc(b_addr + koff);
-                const uint32_t dcol = tmem + b * (tmem_cols / 2) + (uint32_t)(mi * 2 + blk) * kBN;
-                tc_mma(dcol, ad, bd, kIdesc, k16 > 0);
+                const uint32_t dcol = tmem + acc_col<MAT>(b, tmem_cols / 2, (int)si, mi, blk,
+                                                          geo.ncol);
+                tc_mma(dcol, ad, bd, idesc, k16 > 0);
               }
           tc_commit(&st_empty[s]);
-          tc_commit(&d_full[b]);
-          ++dbuf_use[b];
+          if (si + 1 == (uint32_t)geo.gstages || ks + 1 == KS) {
+            tc_commit(&d_full[b]);
+            ++bufs;
+          }
         }
       }
     }
@@ -314,7 +568,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
       for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
         const uint32_t s = g % NS, use = g / NS;
-        if (!bar_wait(&ld_full[s], use & 1u)) {
+        const long long tw = clock64();
+        const bool ok_f = bar_wait(&ld_full[s], use & 1u);
+        t_wait0 += clock64() - tw;
+        if (!ok_f) {
           atomicOr(a.err, kErrTimeout);
           *abort_flag = 1;
           break;
@@ -323,8 +580,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int mi = 0; mi < MAT; ++mi) {
           const uint4 *src = (const uint4 *)(st + 2 * kA16 + kB16 + mi * kA8 + r * kBK);
           uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
+          // rows are 64 B apart, so lanes r and r+2 share banks: each row starts
+          // at a different chunk (rotation by r/2) to keep the loads conflict-free
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {  // 16 int8 -> two 16-byte fp16 chunks
+          for (int qq = 0; qq < 4; ++qq) {  // 16 int8 -> two 16-byte fp16 chunks
+            const int q = (qq + (r >> 1)) & 3;
             const uint4 w = src[q];
             uint4 c0, c1;
             i8x4_to_h2x2(w.x, c0.x, c0.y);
@@ -344,126 +604,46 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
   } else {
     // ============================ epilogue
-    const int ew = warp - 6;                    // 0..7
-    const int quarter = warp & 3;               // TMEM lane quarter this warp may read
-    const int half = ew >> 2;                   // rows [32*half, 32*half+32) of the tile
-    const int et = ew * 32 + lane;              // 0..255
-    const int feat = quarter * 32 + lane;       // feature within the tile (TMEM lane)
-    uint32_t g = 0, dbuf_use[2] = {0, 0};
+    EpiState c;
+    c.tmem = tmem;
+    c.half_cols = tmem_cols / 2;
+    c.KS = KS;
+    c.bufs = 0;
+    c.scgroups = 0;
+    c.d_full = d_full;
+    c.d_empty = d_empty;
+    c.sc_full = sc_full;
+    c.sc_empty = sc_empty;
+    c.sc_ring = sc_ring;
+    c.red = red;
+    c.abort_flag = abort_flag;
+    c.t_wait = 0;
+    c.t_out = 0;
     for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
       const TcTile t = tc_tile<MAT>(P, a, tile);
-      const bool sh = t.e == (int)a.E;
-      const int width = MAT == 2 ? (int)(sh ? a.fs : a.f) : (int)a.d;
-      const int wrow = (sh ? 0 : t.e * width) + t.m0 + feat;  // weight row of this feature
-      float acc[MAT][32];
-#pragma unroll
-      for (int mi = 0; mi < MAT; ++mi)
-#pragma unroll
-        for (int j = 0; j < 32; ++j) acc[mi][j] = 0.0f;
-      int jt = -1;  // tapped feature index of this thread, if any
-      if (TAPS) {
-        const int wf = t.m0 + feat;
-#pragma unroll
-        for (int j = kNTap - 1; j >= 0; --j)
-          if ((int)tap_feature(j, width) == wf) jt = j;
-      }
-      // scales of stage ks are loaded one stage ahead (registers), so their
-      // latency hides behind the previous stage's drain
-      const int pblk = et / kBN, pn = et % kBN;
-      const bool prow = et < 2 * kBN && t.n0 + pn < t.rows;
-      const float *pxs = a.xs + (size_t)(t.slot0 + t.n0 + pn) * a.xs_stride + pblk;
-      const uint16_t *pws[MAT];
-#pragma unroll
-      for (int mi = 0; mi < MAT; ++mi)
-        pws[mi] = (sh ? a.sws[mi] : a.ws[mi]) + (size_t)wrow * a.ws_row_stride;
-      float nx_xs = prow ? __ldg(pxs) : 0.0f;
-      uint32_t nx_ws[MAT];
-#pragma unroll
-      for (int mi = 0; mi < MAT; ++mi) nx_ws[mi] = __ldg((const uint32_t *)pws[mi]);
-      for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
-        const uint32_t b = g & 1u;
-        // activation scales of this stage's two blocks for the tile's 64 rows
-        float *xsb = xs_stage + (size_t)(g & 1u) * 2 * kBN;
-        if (et < 2 * kBN) xsb[pblk * kBN + pn] = nx_xs;
-        float wsc[MAT][2];
-#pragma unroll
-        for (int mi = 0; mi < MAT; ++mi) {
-          wsc[mi][0] = half_bits_to_float((uint16_t)(nx_ws[mi] & 0xFFFFu));
-          wsc[mi][1] = half_bits_to_float((uint16_t)(nx_ws[mi] >> 16));
-        }
-        if (ks + 1 < KS) {
-          nx_xs = prow ? __ldg(pxs + (ks + 1) * 2) : 0.0f;
-#pragma unroll
-          for (int mi = 0; mi < MAT; ++mi)
-            nx_ws[mi] = __ldg((const uint32_t *)(pws[mi] + (ks + 1) * 2));
-        }
-        epi_sync();
-        if (!bar_wait(&d_full[b], dbuf_use[b] & 1u)) {
-          atomicOr(a.err, kErrTimeout);
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int blk = 0; blk < 2; ++blk)
-#pragma unroll
-          for (int mi = 0; mi < MAT; ++mi) {
-            float v[32];
-            const uint32_t col = b * (tmem_cols / 2) + (uint32_t)(mi * 2 + blk) * kBN + half * 32;
-            tc_ld32(tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
-            const float* xsr = xsb + blk * kBN + half * 32;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              acc[mi][j] = __fmaf_rn(v[j], wsc[mi][blk] * xsr[j], acc[mi][j]);
-            if (TAPS && jt >= 0) {
-              const uint32_t kb = ks * 2 + blk;
-              for (int j = 0; j < 32; ++j) {
-                const int n = half * 32 + j;
-                if (t.n0 + n < t.rows) {
-                  const size_t slot = (size_t)(t.slot0 + t.n0 + n);
-                  const size_t base = MAT == 2 ? ((slot * 2 + mi) * kNTap + jt) * a.tap_nb
-                                               : (slot * kNTap + jt) * a.tap_nb;
-                  a.tap[base + kb] = (int32_t)v[j];
-                }
-              }
-            }
-          }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) bar_arrive(&d_empty[b]);
-        ++dbuf_use[b];
-      }
-      if (*abort_flag) break;
-      // ---- tile output
-#pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int n = half * 32 + j;
-        const bool live = t.n0 + n < t.rows;
-        const size_t slot = (size_t)(t.slot0 + t.n0 + n);
-        if (MAT == 2) {
-          // h = silu(g)*u, requantised over this warp's 32 consecutive features
-          const float gv = acc[0][j], uv = acc[MAT - 1][j];
-          const float h = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
-          float amax = fabsf(h);
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-          const float sc = __fdiv_rn(amax, 127.0f);
-          const int q = quant_one(h, sc);
-          if (live) {
-            const size_t fo = (size_t)t.m0 + feat;
-            a.hq[slot * a.fmax + fo] = (int8_t)q;
-            a.hperm[slot * a.fmax + fo] = __int2half_rn(q);
-            if (lane == 0) a.hs[slot * (a.fmax / 32) + fo / 32] = sc;
-          }
-        } else {
-          if (live) a.o[slot * a.d + t.m0 + feat] = acc[0][j];
-        }
-      }
+      const TileGeom geo = tile_geom(t.rows, t.n0);
+      if (geo.ncol == 16) epi_tile<MAT, TAPS, 16, true>(a, c, t, geo);
+      else if (geo.ncol == 32) epi_tile<MAT, TAPS, 32, true>(a, c, t, geo);
+      else epi_tile<MAT, TAPS, 32, false>(a, c, t, geo);
+    }
+    t_wait0 = c.t_wait;
+    t_out = c.t_out;
+  }
+  if (tr && lane == 0) {
+    if (warp == 0) tr[kTcTrProdWaitEmpty] = t_wait0;
+    if (warp == 1) {
+      tr[kTcTrMmaWaitA] = t_wait0;
+      tr[kTcTrMmaWaitD] = t_wait1;
+    }
+    if (warp == 2) tr[kTcTrCvtWaitFull] = t_wait0;
+    if (warp == 6) {
+      tr[kTcTrEpiWaitD] = t_wait0;
+      tr[kTcTrEpiOut] = t_out;
     }
   }
   tc_fence_before();
   __syncthreads();
+  if (tr && threadIdx.x == 0) tr[kTcTrTotal] = clock64() - t_start;
   if (warp == 1) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
@@ -545,9 +725,10 @@ cudaError_t run_tc(const Ctx &c, const TcArgs &a, const TcMaps &maps, size_t sme
 
 }  // namespace
 
+// the scale rows (K/32 fp16) of every matrix must be whole 16-byte TMA rows
 bool tc_supported(const moe_desc &D) {
   if (D.routed_fmt != MOE_FMT_Q8_0) return false;
-  if (D.d % 128 || D.f % 128 || (D.f_shared && D.f_shared % 128)) return false;
+  if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   return encode_fn() != nullptr;
 }
 
@@ -555,7 +736,7 @@ bool tc_supported(const moe_desc &D) {
 bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.flags & MOE_FLAG_FORCE_GEMV) return false;
   if (D.routed_fmt != MOE_FMT_Q8_0) return false;
-  if (D.d % 128 || D.f % 128 || (D.f_shared && D.f_shared % 128)) return false;
+  if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T > kTcMinRows;
 }
 
@@ -589,6 +770,8 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   a.fmax = c.fmax;
   a.plan = (const int *)(c.ws + c.L.plan);
   a.err = (uint32_t *)(c.ws + c.L.err);
+  a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace ? (unsigned long long *)(c.ws + c.L.trace)
+                                                     : nullptr;
   const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
   bool ok = true;
   if (mat == 2) {
@@ -619,6 +802,22 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     }
     ok &= make_map(&maps.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, c.ws + c.L.xperm, D.d, slots,
                    (uint64_t)D.d * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    // scales: 8 blocks (kSG stages) of 128 weight rows / 64 activation rows per copy
+    ok &= make_map(&maps.ws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.gate.scale, D.d / 32,
+                   (uint64_t)D.n_expert * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&maps.ws[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.up.scale, D.d / 32,
+                   (uint64_t)D.n_expert * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (D.f_shared) {
+      ok &= make_map(&maps.sws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.s_gate.scale, D.d / 32,
+                     D.f_shared, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+      ok &= make_map(&maps.sws[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.s_up.scale, D.d / 32,
+                     D.f_shared, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    } else {
+      maps.sws[0] = maps.ws[0];
+      maps.sws[1] = maps.ws[1];
+    }
+    ok &= make_map(&maps.xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c.ws + c.L.xsperm, D.d / 32, slots,
+                   (uint64_t)(D.d / 32) * 4, kSG * 2, kBN, CU_TENSOR_MAP_SWIZZLE_NONE);
   } else {
     a.K = D.f;  // the shared expert is on this path only when f_shared == f
     a.ws[0] = c.wts.down.scale;
@@ -639,6 +838,18 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     maps.sw[1] = maps.sw[0];
     ok &= make_map(&maps.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, c.ws + c.L.hperm, c.fmax, slots,
                    (uint64_t)c.fmax * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
+    ok &= make_map(&maps.ws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.down.scale, D.f / 32,
+                   (uint64_t)D.n_expert * D.d, D.f / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (D.f_shared)
+      ok &= make_map(&maps.sws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.s_down.scale,
+                     D.f_shared / 32, D.d, D.f_shared / 16, kSG * 2, kBM,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
+    else
+      maps.sws[0] = maps.ws[0];
+    maps.ws[1] = maps.ws[0];
+    maps.sws[1] = maps.sws[0];
+    ok &= make_map(&maps.xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, c.ws + c.L.hs, c.fmax / 32, slots,
+                   (uint64_t)(c.fmax / 32) * 4, kSG * 2, kBN, CU_TENSOR_MAP_SWIZZLE_NONE);
   }
   if (!ok) return cudaErrorInvalidValue;
   a.ws_row_stride = a.K / 32;
@@ -646,7 +857,9 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   const uint32_t stage = mat == 2 ? (2 * 16384 + 8192 + 2 * 8192) : (2 * 16384 + 8192 + 2 * 8192);
   a.stage_bytes = stage;
   a.n_stages = mat == 2 ? 3 : 3;
-  const size_t smem = 1024 + (size_t)a.n_stages * stage + 2048;
+  // alignment slack | stages | scale ring | barriers and flags | split-K partial sums
+  const size_t smem = 1024 + (size_t)a.n_stages * stage + (size_t)kScSlots * kScSlotBytes + 1024 +
+                      (size_t)mat * kBM * 33 * 4;
   if (mat == 2)
     return taps ? run_tc<2, true>(c, a, maps, smem) : run_tc<2, false>(c, a, maps, smem);
   return taps ? run_tc<1, true>(c, a, maps, smem) : run_tc<1, false>(c, a, maps, smem);

@@ -274,7 +274,7 @@ def test_fused_wait_timeout_is_reported(gpu):
 
 # ---------------------------------------------------------------- tensor-core expert path
 TC_CASES = [
-    ("tc_small_forced", _spec(E=16, k=4, d=256, f=128, f_shared=128, s=2.5, zipf_beta=0.4), 9),
+    ("tc_small_forced", _spec(E=16, k=4, d=256, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 9),
     ("tc_ragged_rows", _spec(E=8, k=2, d=512, f=256, f_shared=256, s=1.0), 70),
     ("tc_d6144", _spec(E=16, k=4, d=6144, f=256, f_shared=256, s=2.5), 33),
 ]
