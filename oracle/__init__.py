@@ -22,6 +22,8 @@ LIB = os.path.join(_HERE, "liboracle.so")
 
 FMT_Q8_0 = 0
 FMT_Q2S = 1
+SCORE_SIGMOID = 0
+SCORE_SQRT_SOFTPLUS = 1
 
 _lib = None
 _p = ctypes.c_void_p
@@ -36,7 +38,8 @@ class _Expert(ctypes.Structure):
 
 class _Desc(ctypes.Structure):
     _fields_ = [("n_expert", _u32), ("top_k", _u32), ("d", _u32), ("f", _u32),
-                ("f_shared", _u32), ("routed_fmt", _i32), ("s", ctypes.c_float)]
+                ("f_shared", _u32), ("routed_fmt", _i32), ("s", ctypes.c_float),
+                ("score_fn", _i32)]
 
 
 class _Out(ctypes.Structure):
@@ -56,6 +59,13 @@ def load():
         lib.ora_f16_to_f64.restype = ctypes.c_double
         lib.ora_f16_to_f64.argtypes = [ctypes.c_uint16]
         lib.ora_score.argtypes = [_u32, _p, _p, _p, _p]
+        lib.ora_spec_log1p.restype = ctypes.c_float
+        lib.ora_spec_log1p.argtypes = [ctypes.c_float]
+        lib.ora_sqrt_softplus.restype = ctypes.c_float
+        lib.ora_sqrt_softplus.argtypes = [ctypes.c_float]
+        lib.ora_router_logits.argtypes = [_u32, _u32, _u32, _p, _p, _p]
+        lib.ora_score_fn.argtypes = [_i32, _u32, _p, _p, _p, _p]
+        lib.ora_route_fn.argtypes = [_i32, _u32, _u32, _u32, ctypes.c_float, _p, _p, _p, _p]
         lib.ora_topk.argtypes = [_u32, _u32, _p, _p]
         lib.ora_route.argtypes = [_u32, _u32, _u32, ctypes.c_float, _p, _p, _p, _p]
         lib.ora_permute.argtypes = [_u32, _u32, _u32, _p, _p, _p, _p]
@@ -104,6 +114,39 @@ def score(logit, bias):
     return sigma, c
 
 
+def spec_log1p(y) -> np.ndarray:
+    lib = load()
+    y = np.asarray(y, np.float32).ravel()
+    return np.array([lib.ora_spec_log1p(float(v)) for v in y], np.float32)
+
+
+def sqrt_softplus(logit) -> np.ndarray:
+    lib = load()
+    logit = np.asarray(logit, np.float32).ravel()
+    return np.array([lib.ora_sqrt_softplus(float(v)) for v in logit], np.float32)
+
+
+def router_logits(x, w_r) -> np.ndarray:
+    """logits[T][E] = x[T][d] . w_r[E][d]^T in the oracle's fixed fp32 order."""
+    x = _c(x, np.float32)
+    w_r = _c(w_r, np.float32)
+    T, d = x.shape
+    E = w_r.shape[0]
+    out = np.empty((T, E), np.float32)
+    load().ora_router_logits(T, E, d, _ptr(x), _ptr(w_r), _ptr(out))
+    return out
+
+
+def score_fn(fn: int, logit, bias):
+    logit = _c(logit, np.float32)
+    bias = _c(bias, np.float32)
+    E = logit.size
+    p = np.empty(E, np.float32)
+    c = np.empty(E, np.float32)
+    load().ora_score_fn(int(fn), E, _ptr(logit), _ptr(bias), _ptr(p), _ptr(c))
+    return p, c
+
+
 def topk(c, k: int) -> np.ndarray:
     c = _c(c, np.float32)
     idx = np.empty(k, np.int32)
@@ -111,13 +154,14 @@ def topk(c, k: int) -> np.ndarray:
     return idx
 
 
-def route(logits, bias, k: int, s: float):
+def route(logits, bias, k: int, s: float, score: int = SCORE_SIGMOID):
     logits = _c(logits, np.float32)
     bias = _c(bias, np.float32)
     T, E = logits.shape
     idx = np.empty((T, k), np.int32)
     w = np.empty((T, k), np.float32)
-    load().ora_route(T, E, k, float(s), _ptr(logits), _ptr(bias), _ptr(idx), _ptr(w))
+    load().ora_route_fn(int(score), T, E, k, float(s), _ptr(logits), _ptr(bias), _ptr(idx),
+                        _ptr(w))
     return idx, w
 
 
@@ -212,7 +256,7 @@ class LayerResult:
 
 
 def layer(E: int, k: int, d: int, f: int, f_shared: int, fmt: int, s: float,
-          experts, shared, x, logits, bias, want=None) -> LayerResult:
+          experts, shared, x, logits, bias, want=None, score: int = SCORE_SIGMOID) -> LayerResult:
     """Run the whole layer.  ``experts`` maps expert id -> dict of planar arrays
     (gate_q, gate_s, up_q, up_s, down_q, down_s); a missing id is allowed only if
     no wanted token selects it.  ``shared`` is such a dict, or None."""
@@ -229,7 +273,7 @@ def layer(E: int, k: int, d: int, f: int, f_shared: int, fmt: int, s: float,
         if ex is not None:
             arr[e] = _expert_struct(ex, keep)
     sh = _expert_struct(shared, keep) if (shared is not None and f_shared > 0) else _Expert()
-    desc = _Desc(E, k, d, f, f_shared, fmt, float(s))
+    desc = _Desc(E, k, d, f, f_shared, fmt, float(s), int(score))
     res = LayerResult(
         idx=np.empty((T, k), np.int32), w=np.empty((T, k), np.float32),
         off=np.empty(E + 1, np.int32), perm=np.empty(R, np.int32), pos=np.empty(R, np.int32),

@@ -73,6 +73,66 @@ double ora_f16_to_f64(uint16_t h) {
   return neg ? -v : v;
 }
 
+/* log(1+y) for 0 <= y <= 1, "spec-log1p", defined so that any IEEE-754 fp32
+ * machine gets the same bits: z = y/(2+y) (IEEE division), log1p(y) =
+ * 2 atanh(z) = 2z (1 + z^2/3 + z^4/5 + ... + z^14/15): the series of atanh in
+ * z^2 <= 1/9, coefficients fp32(1/(2n+1)), Horner with fmaf, then (2z) * p.
+ * Used by the softplus of the DeepSeek-style scoring sqrt(softplus(l)) ("256
+ * experts, 512 lines", section "The constant that always said 256"). */
+float ora_spec_log1p(float y) {
+  const float c7 = 0x1.111112p-4f; /* 1/15 */
+  const float c6 = 0x1.3b13b2p-4f; /* 1/13 */
+  const float c5 = 0x1.745d18p-4f; /* 1/11 */
+  const float c4 = 0x1.c71c72p-4f; /* 1/9  */
+  const float c3 = 0x1.24924ap-3f; /* 1/7  */
+  const float c2 = 0x1.99999ap-3f; /* 1/5  */
+  const float c1 = 0x1.555556p-2f; /* 1/3  */
+  const float c0 = 1.0f;
+  const float z = y / (2.0f + y);
+  const float z2 = z * z;
+  float p = c7;
+  p = fmaf(p, z2, c6);
+  p = fmaf(p, z2, c5);
+  p = fmaf(p, z2, c4);
+  p = fmaf(p, z2, c3);
+  p = fmaf(p, z2, c2);
+  p = fmaf(p, z2, c1);
+  p = fmaf(p, z2, c0);
+  return (2.0f * z) * p;
+}
+
+/* sqrt(softplus(l)) with softplus(l) = max(l, 0) + log1p(e(-|l|)): spec-exp,
+ * spec-log1p, IEEE add and sqrt */
+float ora_sqrt_softplus(float l) {
+  const float m = l > 0.0f ? l : 0.0f;
+  const float e = ora_spec_exp(-fabsf(l));
+  return sqrtf(m + ora_spec_log1p(e));
+}
+
+/* Router logits l[t][e] = sum_i x[t][i] * w_r[e][i] in fp32 in one fixed order
+ * (the router GEMM in front of the scoring; its precision is not given on the
+ * pages, so fp32 weights and this order define it): 32 partial sums,
+ * p_l = fmaf chain over i = l, l+32, l+64, ... ascending; then for
+ * o = 16, 8, 4, 2, 1: p_l <- p_l + p_(l xor o) for every l at once; l = p_0. */
+void ora_router_logits(uint32_t T, uint32_t E, uint32_t d, const float *x, const float *w_r,
+                       float *logits) {
+  for (uint32_t t = 0; t < T; ++t) {
+    for (uint32_t e = 0; e < E; ++e) {
+      float p[32], q[32];
+      for (uint32_t l = 0; l < 32; ++l) {
+        p[l] = 0.0f;
+        for (uint32_t i = l; i < d; i += 32)
+          p[l] = fmaf(x[(size_t)t * d + i], w_r[(size_t)e * d + i], p[l]);
+      }
+      for (uint32_t o = 16; o >= 1; o >>= 1) {
+        for (uint32_t l = 0; l < 32; ++l) q[l] = p[l] + p[l ^ o];
+        memcpy(p, q, sizeof p);
+      }
+      logits[(size_t)t * E + e] = p[0];
+    }
+  }
+}
+
 /* ------------------------------------------------------------------ A1 score */
 void ora_score(uint32_t E, const float *logit, const float *bias, float *sigma, float *c) {
   for (uint32_t i = 0; i < E; ++i) {
@@ -81,6 +141,28 @@ void ora_score(uint32_t E, const float *logit, const float *bias, float *sigma, 
     if (sigma) sigma[i] = sg;
     c[i] = sg + bias[i];
   }
+}
+
+/* per-expert score p_i of scoring function fn (ORA_SCORE_*) and selection score
+ * c_i = p_i + b_i */
+void ora_score_fn(int32_t fn, uint32_t E, const float *logit, const float *bias, float *p,
+                  float *c) {
+  if (fn == ORA_SCORE_SIGMOID) {
+    ora_score(E, logit, bias, p, c);
+    return;
+  }
+  for (uint32_t i = 0; i < E; ++i) {
+    const float v = ora_sqrt_softplus(logit[i]);
+    if (p) p[i] = v;
+    c[i] = v + bias[i];
+  }
+}
+
+/* the score in fp64 (routing weights): sigmoid, or sqrt(softplus) in its
+ * overflow-free form */
+static double score_f64(int32_t fn, double l) {
+  if (fn == ORA_SCORE_SIGMOID) return 1.0 / (1.0 + exp(-l));
+  return sqrt((l > 0.0 ? l : 0.0) + log1p(exp(-fabs(l))));
 }
 
 /* ------------------------------------------------------------------ A2 top-k
@@ -100,24 +182,31 @@ void ora_topk(uint32_t E, uint32_t k, const float *c, int32_t *idx) {
   free(taken);
 }
 
-/* router for T tokens; weights w_j = s * sigma_j / sum_j sigma_j in fp64 */
-void ora_route(uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
-               const float *bias, int32_t *idx, float *w) {
+/* router for T tokens with scoring function fn; weights w_j = s * p_j / sum_j
+ * p_j in fp64 */
+void ora_route_fn(int32_t fn, uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
+                  const float *bias, int32_t *idx, float *w) {
   float *c = (float *)malloc(sizeof(float) * E);
   for (uint32_t t = 0; t < T; ++t) {
     const float *l = logits + (size_t)t * E;
-    ora_score(E, l, bias, NULL, c);
+    ora_score_fn(fn, E, l, bias, NULL, c);
     ora_topk(E, k, c, idx + (size_t)t * k);
     if (w) {
       double sum = 0.0;
-      for (uint32_t j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
+      for (uint32_t j = 0; j < k; ++j) sum += score_f64(fn, (double)l[idx[t * k + j]]);
       for (uint32_t j = 0; j < k; ++j) {
-        double sg = 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
-        w[t * k + j] = (float)((double)s * sg / sum);
+        const double p = score_f64(fn, (double)l[idx[t * k + j]]);
+        w[t * k + j] = (float)((double)s * p / sum);
       }
     }
   }
   free(c);
+}
+
+/* sigmoid router (the GLM-5.2 / Hy3 scoring) */
+void ora_route(uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
+               const float *bias, int32_t *idx, float *w) {
+  ora_route_fn(ORA_SCORE_SIGMOID, T, E, k, s, logits, bias, idx, w);
 }
 
 /* ------------------------------------------------------------------ A3 permute
@@ -251,7 +340,7 @@ int ora_layer(const ora_desc *desc, const ora_expert *experts, const ora_expert 
   double *wd = (double *)malloc(sizeof(double) * k);
   for (uint32_t t = 0; t < T; ++t)
     ora_quantize(d, x + (size_t)t * d, xq + (size_t)t * d, xs + (size_t)t * d / 32);
-  ora_route(T, E, k, desc->s, logits, bias, idx, w32);
+  ora_route_fn(desc->score_fn, T, E, k, desc->s, logits, bias, idx, w32);
   ora_permute(T, E, k, idx, off, perm, pos);
   for (uint32_t t = 0; t < T && rc == ORA_OK; ++t) {
     if (want && !want[t]) continue;

@@ -12,6 +12,11 @@
  *               "Why GLM-5.2 in an engine built for DeepSeek"; NeutronStar main
  *               README, Hy3 paragraph ("192-expert top-8 sigmoid router with
  *               expert bias").
+ *  - DeepSeek : p_i = sqrt(softplus(l_i)) in place of sigma_i (spec-log1p below),
+ *               top-6, scale 1.5, E = 384 ("256 experts, 512 lines", section
+ *               "The constant that always said 256").
+ *  - router   : logits l = x . W_r^T in fp32 in one fixed summation order
+ *               (ora_router_logits).
  *  - top-k    : k indices of largest c; equal c -> lower index first; slots in
  *               order of c descending.  Weight w_j = s * sigma_j / sum_j sigma_j
  *               (fp64).  The parameterised n_expert/top_k/scale router:
@@ -48,6 +53,8 @@ extern "C" {
 #endif
 
 enum { ORA_FMT_Q8_0 = 0, ORA_FMT_Q2S = 1 };
+/* scoring of a logit: sigmoid (GLM-5.2, Hy3) or sqrt(softplus) (DeepSeek) */
+enum { ORA_SCORE_SIGMOID = 0, ORA_SCORE_SQRT_SOFTPLUS = 1 };
 enum { ORA_OK = 0, ORA_BAD_ARG = 1, ORA_MISSING_EXPERT = 2, ORA_NO_MEMORY = 3 };
 
 /* One expert's weights, planar: code plane + fp16 scale plane (bit patterns).
@@ -66,6 +73,7 @@ typedef struct {
   uint32_t n_expert, top_k, d, f, f_shared; /* f_shared == 0: no shared expert */
   int32_t routed_fmt;                       /* ORA_FMT_Q8_0 or ORA_FMT_Q2S */
   float s;                                  /* routing scale */
+  int32_t score_fn;                         /* ORA_SCORE_* */
 } ora_desc;
 
 /* Outputs of ora_layer; any pointer may be NULL.
@@ -89,7 +97,15 @@ typedef struct {
 float ora_spec_exp(float x);
 void ora_spec_exp_n(uint32_t n, const float *x, float *out);
 double ora_f16_to_f64(uint16_t h);
+float ora_spec_log1p(float y);
+float ora_sqrt_softplus(float l);
+void ora_router_logits(uint32_t T, uint32_t E, uint32_t d, const float *x, const float *w_r,
+                       float *logits);
 void ora_score(uint32_t E, const float *logit, const float *bias, float *sigma, float *c);
+void ora_score_fn(int32_t fn, uint32_t E, const float *logit, const float *bias, float *p,
+                  float *c);
+void ora_route_fn(int32_t fn, uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
+                  const float *bias, int32_t *idx, float *w);
 void ora_topk(uint32_t E, uint32_t k, const float *c, int32_t *idx);
 void ora_route(uint32_t T, uint32_t E, uint32_t k, float s, const float *logits,
                const float *bias, int32_t *idx, float *w);

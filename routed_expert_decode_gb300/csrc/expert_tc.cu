@@ -142,9 +142,9 @@ __device__ __forceinline__ void tc_commit(uint64_t *bar) {
           s32(bar))
       : "memory");
 }
-// 16 consecutive fp32 columns of this warp's 32 TMEM lanes into v[0..15]
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[16];
+// 16 consecutive fp32 columns of this warp's 32 TMEM lanes, no wait (tc_wait_ld)
+__device__ __forceinline__ void tc_ld16_issue(uint32_t taddr, float (&v)[16]) {
+  uint32_t *r = reinterpret_cast<uint32_t *>(v);
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15}, [%16];"
@@ -152,9 +152,9 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[32]) {
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
         "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // shared-memory matrix descriptor: K-major operand in the 128-byte swizzle
@@ -321,19 +321,25 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
       for (int bi = 0; bi < 2; ++bi) {
         if (SPLIT && bi != half) continue;  // warp-uniform
 #pragma unroll
-        for (int mi = 0; mi < MAT; ++mi) {
-          const float ws_b = wsc[mi][bi];
+        for (int c16 = 0; c16 < NCM / 16; ++c16) {
+          // both matrices' 16 columns in flight together, one wait
+          float v[MAT][16];
 #pragma unroll
-          for (int c16 = 0; c16 < NCM / 16; ++c16) {
-            float v[32];
-            const uint32_t col = acc_col<MAT>(b, c.half_cols, (int)si, mi, bi, geo.ncol) + col0 +
-                                 16 * c16;
-            tc_ld16(c.tmem + ((uint32_t)(quarter * 32) << 16) + col, v);
+          for (int mi = 0; mi < MAT; ++mi)
+            tc_ld16_issue(c.tmem + ((uint32_t)(quarter * 32) << 16) +
+                              acc_col<MAT>(b, c.half_cols, (int)si, mi, bi, geo.ncol) + col0 +
+                              16 * c16,
+                          v[mi]);
+          float xsv[16];  // the 16 rows' x scales of this block (shared by both matrices)
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float xsv = xsl[(col0 + 16 * c16 + j) * 8 + blk0 + bi];
-              acc[mi][16 * c16 + j] = __fmaf_rn(v[j], ws_b * xsv, acc[mi][16 * c16 + j]);
-            }
+          for (int j = 0; j < 16; ++j) xsv[j] = xsl[(col0 + 16 * c16 + j) * 8 + blk0 + bi];
+          tc_wait_ld();
+#pragma unroll
+          for (int mi = 0; mi < MAT; ++mi) {
+            const float ws_b = wsc[mi][bi];
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              acc[mi][16 * c16 + j] = __fmaf_rn(v[mi][j], ws_b * xsv[j], acc[mi][16 * c16 + j]);
             if (TAPS && jt >= 0) {
               const uint32_t kb = ks * 2 + bi;
               for (int j = 0; j < 16; ++j) {
@@ -342,7 +348,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
                   const size_t sl = (size_t)(t.slot0 + t.n0 + n);
                   const size_t base = MAT == 2 ? ((sl * 2 + mi) * kNTap + jt) * a.tap_nb
                                                : (sl * kNTap + jt) * a.tap_nb;
-                  a.tap[base + kb] = (int32_t)v[j];
+                  a.tap[base + kb] = (int32_t)v[mi][j];
                 }
               }
             }
