@@ -349,9 +349,9 @@ int ora_layer(const ora_desc *desc, const ora_expert *experts, const ora_expert 
     const float *l = logits + (size_t)t * E;
     /* routing weights in fp64 (the fp32 copy in w32 is only an output) */
     double sum = 0.0;
-    for (uint32_t j = 0; j < k; ++j) sum += 1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]));
+    for (uint32_t j = 0; j < k; ++j) sum += score_f64(desc->score_fn, (double)l[idx[t * k + j]]);
     for (uint32_t j = 0; j < k; ++j)
-      wd[j] = (double)desc->s * (1.0 / (1.0 + exp(-(double)l[idx[t * k + j]]))) / sum;
+      wd[j] = (double)desc->s * score_f64(desc->score_fn, (double)l[idx[t * k + j]]) / sum;
     for (uint32_t m = 0; m < d; ++m) acc[m] = 0.0;
     if (fs > 0) {
       rc = ora_expert_row(ORA_FMT_Q8_0, d, fs, shared, xqt, xst,

@@ -82,8 +82,14 @@ def stable_permutation(idx: np.ndarray, E: int):
     return off, perm, pos
 
 
-def layer(E, k, d, f, f_shared, fmt, s, experts, shared, x, idx, logits):
-    """Dense fp64 layer given the selected indices; returns y [T, d] (fp64)."""
+def sqrt_softplus64(v):
+    v = np.asarray(v, np.float64)
+    return np.sqrt(np.maximum(v, 0.0) + np.log1p(np.exp(-np.abs(v))))
+
+
+def layer(E, k, d, f, f_shared, fmt, s, experts, shared, x, idx, logits, score=0):
+    """Dense fp64 layer given the selected indices; returns y [T, d] (fp64).
+    score: 0 sigmoid, 1 sqrt(softplus) (the routing weights' p)."""
     T = x.shape[0]
     y = np.zeros((T, d), np.float64)
     for t in range(T):
@@ -91,7 +97,7 @@ def layer(E, k, d, f, f_shared, fmt, s, experts, shared, x, idx, logits):
         acc = np.zeros(d, np.float64)
         if f_shared > 0:
             acc += expert_ffn(shared, 0, d, f_shared, xq, xs)[2]
-        sg = sigmoid64(logits[t, idx[t]])
+        sg = (sqrt_softplus64 if score == 1 else sigmoid64)(logits[t, idx[t]])
         w = s * sg / sg.sum()
         for j in range(k):
             acc += w[j] * expert_ffn(experts[int(idx[t, j])], fmt, d, f, xq, xs)[2]

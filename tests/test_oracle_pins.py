@@ -294,7 +294,7 @@ def _run_layer(spec, T, seed, want=None, drop_shared=False):
     shared = synth.expert_host(spec, spec.E) if spec.f_shared else None
     fs = 0 if drop_shared else spec.f_shared
     res = oracle.layer(spec.E, spec.k, spec.d, spec.f, fs, spec.fmt, spec.s, experts, shared,
-                       x, logits, bias, want=want)
+                       x, logits, bias, want=want, score=spec.score)
     return res, experts, shared, x, logits, bias
 
 
@@ -302,18 +302,19 @@ def _run_layer(spec, T, seed, want=None, drop_shared=False):
     _spec(),                                                  # the tiny layer
     _spec(E=24, k=6, d=320, f=96, f_shared=64, s=2.5, zipf_beta=0.4),
     _spec(E=12, k=3, d=256, f=128, f_shared=96, fmt=1, s=1.0),
+    _spec(E=40, k=6, d=256, f=128, f_shared=128, s=1.5, score=1),  # DeepSeek scoring
 ])
 def test_layer_matches_dense_rederivation(spec):
     T = 6
     res, experts, shared, x, logits, bias = _run_layer(spec, T, 3)
     for t in range(T):
-        _, c = oracle.score(logits[t], bias)
+        _, c = oracle.score_fn(spec.score, logits[t], bias)
         assert np.array_equal(res.idx[t], refmath.brute_topk(c, spec.k))
     assert refmath.check_permutation(res.idx, res.off, res.perm, res.pos, spec.E) == []
     rq, rs = refmath.quantize(x)
     assert np.array_equal(res.xq.ravel(), rq) and np.array_equal(res.xs.ravel(), rs)
     y_ref = refmath.layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s,
-                          experts, shared, x, res.idx, logits)
+                          experts, shared, x, res.idx, logits, score=spec.score)
     err = np.abs(res.y - y_ref).max(axis=1) / np.abs(y_ref).max(axis=1)
     assert err.max() < 1e-5, err
 
