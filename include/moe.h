@@ -81,6 +81,19 @@ typedef struct {
   const uint16_t *scale;
 } moe_mat;
 
+/* Scoring of a router logit l (both with the spec-exp of moe_layer's router):
+ * MOE_SCORE_SIGMOID        p = 1/(1+e^-l)          (GLM-5.2 "sigmoid routing
+ *                          with top-8" and Hy3's sigmoid router: "256 experts,
+ *                          512 lines", section "Why GLM-5.2 in an engine built for
+ *                          DeepSeek"; NeutronStar README, Hy3 paragraph)
+ * MOE_SCORE_SQRT_SOFTPLUS  p = sqrt(softplus(l)), softplus(l) = max(l,0) +
+ *                          log1p(e^-|l|), log1p by the atanh series in
+ *                          z = y/(2+y) to z^15 (DeepSeek's scoring with top-6 and
+ *                          scale 1.5: "256 experts, 512 lines", section "The
+ *                          constant that always said 256").
+ * Selection uses c = p + bias; weights w_j = s * p_j / sum_j p_j. */
+typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score;
+
 /* flags */
 #define MOE_FLAG_DEBUG_TAPS 0x1u /* write sampled int32 block dots into the workspace */
 #define MOE_FLAG_FORCE_GEMV 0x2u /* every expert on the dp4a path (no tensor-core path) */
@@ -102,6 +115,7 @@ typedef struct {
   int32_t routed_fmt;/* moe_fmt of the routed experts (the shared expert is Q8_0) */
   float s;           /* routing scale */
   uint32_t flags;    /* MOE_FLAG_* */
+  uint32_t score;    /* moe_score: how a logit becomes the expert's score */
 } moe_desc;
 
 /* Routed experts, expert-major: gate, up [E][f][d]; down [E][d][f] (codes; for
@@ -179,6 +193,19 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
                            const float *logits, const float *bias, uint32_t T, float *y,
                            void *ws, size_t ws_bytes, void *stream, void *const *events,
                            uint32_t n_events);
+
+/* Router logits in front of the scoring: logits[t][e] = sum_i x[t][i] *
+ * w_router[e][i] in fp32 in one fixed order -- lane l (of 32) accumulates
+ * i = l, l+32, ... ascending with fused multiply-adds, then the 32 partial sums
+ * are combined pairwise over lane distances 16, 8, 4, 2, 1 -- so that any
+ * implementation of that order gets the same bits (the expert picks downstream
+ * depend on them).  The pages give no precision for the router GEMM; fp32
+ * weights and this order are this library's definition.
+ * x: [T][d] fp32, w_router: [E][d] fp32, logits: [T][E] fp32, all device
+ * pointers (caller-owned, 16-byte aligned).  Asynchronous on `stream`;
+ * MOE_ERR_INVALID_ARG on a bad desc or NULL pointer with T > 0. */
+moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const float *x,
+                             uint32_t T, float *logits, void *stream);
 
 /* Which implementation moe_layer uses for (desc, T) on the current device:
  * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */

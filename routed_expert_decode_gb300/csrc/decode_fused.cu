@@ -116,6 +116,7 @@ struct StageDesc {
 struct FusedArgs {
   uint32_t E, k, d, f, fs, T, R, fmax;
   float s;
+  uint32_t score;  // moe_score
   const float *x, *logits, *bias;
   const int8_t *gq, *uq, *dq, *sgq, *suq, *sdq;
   const uint16_t *gs, *us, *ds, *sgs, *sus, *sds;
@@ -346,7 +347,7 @@ __device__ __forceinline__ void route_bar_sync(uint32_t T) {
 __device__ void route_scores(const FusedArgs &a, float *sc) {
 #pragma unroll 1
   for (uint32_t i = threadIdx.x; i < a.T * a.E; i += kConsumerWarps * 32)
-    sc[i] = __fadd_rn(sigmoid_rn(__ldg(a.logits + i)), __ldg(a.bias + i % a.E));
+    sc[i] = __fadd_rn(score_rn(__ldg(a.logits + i), a.score), __ldg(a.bias + i % a.E));
 }
 
 // warps 0..T-1: warp t selects token t's top_k by k rounds of a strided scan
@@ -425,9 +426,9 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc,
   }
   __syncwarp();
   if (tr && tid == 0) tr[24] = global_ns();
-  // lane j < k: the sigmoid of slot j; w = s * sigma_j / sum_j sigma_j (in order)
+  // lane j < k: the score of slot j; w = s * p_j / sum_j p_j (in order)
   const float my_sigma =
-      (uint32_t)lane < k ? sigmoid_rn(__ldg(a.logits + (size_t)t * E + rs.idx[t * k + lane]))
+      (uint32_t)lane < k ? score_rn(__ldg(a.logits + (size_t)t * E + rs.idx[t * k + lane]), a.score)
                          : 0.0f;
   float sum = 0.0f;
 #pragma unroll 1
@@ -1263,6 +1264,7 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.R = c.R;
   a.fmax = c.fmax;
   a.s = D.s;
+  a.score = D.score;
   a.x = x;
   a.logits = logits;
   a.bias = bias;

@@ -21,6 +21,7 @@ bool desc_ok(const moe_desc *d) {
   if (d->d == 0 || d->d % 32 || d->f == 0 || d->f % 32 || d->f_shared % 32) return false;
   if (d->routed_fmt != MOE_FMT_Q8_0 && d->routed_fmt != MOE_FMT_Q2S) return false;
   if (!(d->s == d->s)) return false;  // NaN scale
+  if (d->score != MOE_SCORE_SIGMOID && d->score != MOE_SCORE_SQRT_SOFTPLUS) return false;
   // int32 indexing of rows and work items
   if ((uint64_t)d->n_expert * d->f > (1u << 30) || (uint64_t)d->n_expert * d->d > (1u << 30))
     return false;
@@ -300,6 +301,16 @@ const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i) {
   if (!path) return nullptr;
   if (path[0] == 'f') return i < kNumFusedStages ? kFusedStageNames[i] : nullptr;
   return i < kNumStages ? kStageNames[i] : nullptr;
+}
+
+moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const float *x,
+                             uint32_t T, float *logits, void *stream) {
+  if (!desc_ok(desc)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!w_router || !x || !logits || !aligned(w_router, 16) || !aligned(x, 16) ||
+      !aligned(logits, 4))
+    return MOE_ERR_INVALID_ARG;
+  return from_cuda(launch_router_logits(*desc, w_router, x, T, logits, (cudaStream_t)stream));
 }
 
 const char *moe_last_error(void) { return t_last_error; }

@@ -78,6 +78,33 @@ __device__ __forceinline__ float sigmoid_rn(float x) {
   return __fdiv_rn(1.0f, __fadd_rn(1.0f, spec_exp(-x)));
 }
 
+// log(1+y), 0 <= y <= 1: z = y/(2+y), 2z * (1 + z^2/3 + ... + z^14/15) with
+// fp32(1/(2n+1)) by Horner (fma) -- bit-reproducible like spec_exp
+__device__ __forceinline__ float spec_log1p(float y) {
+  const float z = __fdiv_rn(y, __fadd_rn(2.0f, y));
+  const float z2 = __fmul_rn(z, z);
+  float p = 0x1.111112p-4f;          // 1/15
+  p = __fmaf_rn(p, z2, 0x1.3b13b2p-4f);  // 1/13
+  p = __fmaf_rn(p, z2, 0x1.745d18p-4f);  // 1/11
+  p = __fmaf_rn(p, z2, 0x1.c71c72p-4f);  // 1/9
+  p = __fmaf_rn(p, z2, 0x1.24924ap-3f);  // 1/7
+  p = __fmaf_rn(p, z2, 0x1.99999ap-3f);  // 1/5
+  p = __fmaf_rn(p, z2, 0x1.555556p-2f);  // 1/3
+  p = __fmaf_rn(p, z2, 1.0f);
+  return __fmul_rn(__fmul_rn(2.0f, z), p);
+}
+
+// sqrt(softplus(l)), softplus(l) = max(l, 0) + log1p(e^-|l|)
+__device__ __forceinline__ float sqrt_softplus_rn(float l) {
+  const float m = l > 0.0f ? l : 0.0f;
+  return __fsqrt_rn(__fadd_rn(m, spec_log1p(spec_exp(-fabsf(l)))));
+}
+
+// the expert score p of a logit under moe_score `fn`
+__device__ __forceinline__ float score_rn(float l, uint32_t fn) {
+  return fn == MOE_SCORE_SQRT_SOFTPLUS ? sqrt_softplus_rn(l) : sigmoid_rn(l);
+}
+
 // one 32-element block: scale = amax/127, q = clamp(round_half_away(x/scale))
 __device__ __forceinline__ int quant_one(float x, float scale) {
   if (scale == 0.0f) return 0;
@@ -212,6 +239,8 @@ struct Ctx {
 
 cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, int32_t *idx,
                          float *w);
+cudaError_t launch_router_logits(const moe_desc &d, const float *w_router, const float *x,
+                                 uint32_t T, float *logits, cudaStream_t stream);
 cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32_t *perm,
                            int32_t *pos, uint32_t *err);
 cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,

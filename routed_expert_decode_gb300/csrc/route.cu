@@ -19,7 +19,8 @@ constexpr int kRouteWarps = 8;
 // lanes agree on a unique winner and ties go to the lower index.
 __global__ void __launch_bounds__(kRouteWarps * 32)
     k_route(const float *__restrict__ logits, const float *__restrict__ bias, uint32_t T,
-            uint32_t E, uint32_t k, float s, int32_t *__restrict__ idx, float *__restrict__ w) {
+            uint32_t E, uint32_t k, float s, uint32_t score, int32_t *__restrict__ idx,
+            float *__restrict__ w) {
   const int lane = threadIdx.x & 31;
   const uint32_t t = blockIdx.x * kRouteWarps + threadIdx.x / 32;
   if (t >= T) return;
@@ -32,7 +33,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     c[i] = -INFINITY;
     sg[i] = 0.0f;
     if (i < nper && e < E) {
-      const float sgm = sigmoid_rn(l[e]);
+      const float sgm = score_rn(l[e], score);
       sg[i] = sgm;
       c[i] = __fadd_rn(sgm, bias[e]);
     }
@@ -344,7 +345,36 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
   if (c.T == 0) return cudaSuccess;
   const unsigned grid = (c.T + kRouteWarps - 1) / kRouteWarps;
   k_route<<<grid, kRouteWarps * 32, 0, c.stream>>>(logits, bias, c.T, c.desc.n_expert,
-                                                   c.desc.top_k, c.desc.s, idx, w);
+                                                   c.desc.top_k, c.desc.s, c.desc.score, idx, w);
+  return cudaGetLastError();
+}
+
+// logits[t][e] = x[t] . w_router[e] in the library's fixed order (moe.h,
+// moe_router_logits): one warp per (t, e); lane l runs the fma chain over
+// i = l, l+32, ..; the lanes' sums meet over xor distances 16..1.
+__global__ void __launch_bounds__(256)
+    k_router_logits(const float *__restrict__ x, const float *__restrict__ wr, uint32_t T,
+                    uint32_t E, uint32_t d, float *__restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const uint64_t item = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32;
+  if (item >= (uint64_t)T * E) return;
+  const uint32_t t = (uint32_t)(item / E), e = (uint32_t)(item % E);
+  const float *xr = x + (size_t)t * d;
+  const float *wrow = wr + (size_t)e * d;
+  float p = 0.0f;
+#pragma unroll 8
+  for (uint32_t i = lane; i < d; i += 32) p = __fmaf_rn(__ldg(xr + i), __ldg(wrow + i), p);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
+  if (lane == 0) logits[item] = p;
+}
+
+cudaError_t launch_router_logits(const moe_desc &d, const float *w_router, const float *x,
+                                 uint32_t T, float *logits, cudaStream_t stream) {
+  const uint64_t items = (uint64_t)T * d.n_expert;
+  if (items == 0) return cudaSuccess;
+  k_router_logits<<<(unsigned)((items + 7) / 8), 256, 0, stream>>>(x, w_router, T, d.n_expert,
+                                                                   d.d, logits);
   return cudaGetLastError();
 }
 

@@ -50,7 +50,7 @@ class MoeMat(ctypes.Structure):
 class MoeDesc(ctypes.Structure):
     _fields_ = [("n_expert", _u32), ("top_k", _u32), ("d", _u32), ("f", _u32),
                 ("f_shared", _u32), ("routed_fmt", ctypes.c_int32), ("s", ctypes.c_float),
-                ("flags", _u32)]
+                ("flags", _u32), ("score", _u32)]
 
 
 class MoeWeights(ctypes.Structure):
@@ -105,6 +105,8 @@ def lib():
                                       ctypes.POINTER(_vp), _u32]
         L.moe_layer_path.restype = ctypes.c_char_p
         L.moe_layer_path.argtypes = [ctypes.POINTER(MoeDesc), _u32]
+        L.moe_router_logits.argtypes = [ctypes.POINTER(MoeDesc), _vp, _vp, _u32, _vp, _vp]
+        L.moe_router_logits.restype = ctypes.c_int
         L.moe_layer_stage_name.restype = ctypes.c_char_p
         L.moe_tc_min_rows.argtypes = [ctypes.POINTER(MoeDesc), _u32]
         L.moe_tc_min_rows.restype = ctypes.c_int32
@@ -151,8 +153,23 @@ def _check(fn: str, status: int):
         raise MoeError(fn, status)
 
 
-def make_desc(n_expert, top_k, d, f, f_shared, routed_fmt, s, flags=0) -> MoeDesc:
-    return MoeDesc(n_expert, top_k, d, f, f_shared, routed_fmt, float(s), flags)
+SCORE_SIGMOID = 0
+SCORE_SQRT_SOFTPLUS = 1
+
+
+def make_desc(n_expert, top_k, d, f, f_shared, routed_fmt, s, flags=0,
+              score=SCORE_SIGMOID) -> MoeDesc:
+    return MoeDesc(n_expert, top_k, d, f, f_shared, routed_fmt, float(s), flags, score)
+
+
+def router_logits(desc: MoeDesc, w_router: torch.Tensor, x: torch.Tensor,
+                  logits: torch.Tensor, stream=None) -> None:
+    """logits[T][E] = x[T][d] . w_router[E][d]^T in the library's fixed fp32 order."""
+    T = x.shape[0]
+    st = lib().moe_router_logits(ctypes.byref(desc), _dev_ptr(w_router, torch.float32, "w_router"),
+                                 _dev_ptr(x, torch.float32, "x"), T,
+                                 _dev_ptr(logits, torch.float32, "logits"), _stream(stream))
+    _check("moe_router_logits", st)
 
 
 def workspace_size(desc: MoeDesc, T: int) -> int:
@@ -278,9 +295,10 @@ class Layer:
     """
 
     def __init__(self, n_expert, top_k, d, f, f_shared, routed_fmt, s, tensors: dict,
-                 device=None):
+                 device=None, score=SCORE_SIGMOID):
         self.n_expert, self.top_k, self.d, self.f = n_expert, top_k, d, f
         self.f_shared, self.routed_fmt, self.s = f_shared, routed_fmt, float(s)
+        self.score = score
         self.tensors = tensors
         self.device = device or tensors["gate_q"].device
         self.weights = MoeWeights()
@@ -312,7 +330,7 @@ class Layer:
 
     def desc(self, flags=0) -> MoeDesc:
         return make_desc(self.n_expert, self.top_k, self.d, self.f, self.f_shared,
-                         self.routed_fmt, self.s, flags)
+                         self.routed_fmt, self.s, flags, self.score)
 
     def workspace(self, T: int, flags=0) -> torch.Tensor:
         key = (T, flags & FLAG_DEBUG_TAPS)

@@ -36,6 +36,7 @@ STREAM_LOGITS = 0
 STREAM_BIAS = 1
 STREAM_X = 2
 STREAM_ZIPF = 3
+STREAM_ROUTER = 4  # router weights W_r [E][d]
 STREAM_WEIGHTS = 16  # + 8 * expert + matrix (expert == E is the shared expert)
 MATS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s")
 
@@ -138,6 +139,7 @@ class LayerSpec:
     s: float         # routing scale
     zipf_beta: float  # popularity-offset strength (0: none)
     layer_seed: int = 0
+    score: int = 0    # logit scoring: 0 sigmoid, 1 sqrt(softplus)
 
 
 TINY = LayerSpec("tiny", E=16, k=4, d=256, f=128, f_shared=0, fmt=FMT_Q8_0, s=1.0, zipf_beta=0.0)
@@ -148,6 +150,12 @@ Q2_LAYER = LayerSpec("e192_k8_d4096_f1536_q2", E=192, k=8, d=4096, f=1536, f_sha
 
 # Same per-token shapes as GLM_LAYER with 32 experts (1.3 GB of weights, 361 MB
 # read per token): the small case that profiler captures run on.
+# DeepSeek-style routing (sqrt(softplus) scoring, top-6, scale 1.5, 384 experts:
+# "256 experts, 512 lines", section "The constant that always said 256") on the
+# same expert shapes; no Zipf offset (its logits come from the router GEMM).
+DS_LAYER = LayerSpec("e384_k6_d6144_f2048_q8_ds", E=384, k=6, d=6144, f=2048, f_shared=2048,
+                     fmt=FMT_Q8_0, s=1.5, zipf_beta=0.0, score=1)
+
 GLM_LAYER_E32 = LayerSpec("e32_k8_d6144_f2048_q8", E=32, k=8, d=6144, f=2048, f_shared=2048,
                           fmt=FMT_Q8_0, s=2.5, zipf_beta=0.4)
 # 64 experts (2.4 GB): with T=128 an expert gets ~16 rows, as in a T=512 batch
@@ -211,6 +219,13 @@ def expert_host(spec: LayerSpec, expert: int) -> dict:
 
 def bias(spec: LayerSpec) -> np.ndarray:
     return normal(spec.layer_seed, STREAM_BIAS, spec.E, 0.0, 0.1)
+
+
+def router_weights(spec: LayerSpec) -> np.ndarray:
+    """Router weights W_r [E][d] fp32, N(0, 1/d): with x ~ N(0, 1) the logits
+    x . W_r are ~N(0, 1), like the direct logits of token_inputs."""
+    return normal(spec.layer_seed, STREAM_ROUTER, spec.E * spec.d, 0.0,
+                  1.0 / float(np.sqrt(spec.d))).reshape(spec.E, spec.d)
 
 
 def token_inputs(spec: LayerSpec, seed: int, T: int):

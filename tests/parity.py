@@ -32,7 +32,7 @@ def device_layer(spec: synth.LayerSpec, device) -> moe.Layer:
         t = synth.fill_layer_device(spec, device)
         torch.cuda.synchronize()
         _LAYERS[key] = moe.Layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s,
-                                 t, device)
+                                 t, device, score=spec.score)
     return _LAYERS[key]
 
 
@@ -45,11 +45,22 @@ def host_expert(spec, e):
     return _HOST[key]
 
 
-def run_case(spec, T, seed, device, sample=None, flags=0, check_taps=True):
-    """Run one batch on the GPU and the oracle; assert parity; return a report."""
+def run_case(spec, T, seed, device, sample=None, flags=0, check_taps=True, router=False):
+    """Run one batch on the GPU and the oracle; assert parity; return a report.
+    router=True: the logits come from the router GEMM x . W_r (moe_router_logits
+    on the GPU, ora_router_logits on the CPU), which must agree bit for bit."""
     logits, x = synth.token_inputs(spec, seed, T)
     bias = synth.bias(spec)
     layer = device_layer(spec, device)
+    if router:
+        w_r = synth.router_weights(spec)
+        logits = oracle.router_logits(x, w_r)
+        l_dev = torch.empty((T, spec.E), dtype=torch.float32, device=device)
+        moe.router_logits(layer.desc(), torch.from_numpy(w_r).to(device),
+                          torch.from_numpy(x).to(device), l_dev)
+        torch.cuda.synchronize()
+        assert np.array_equal(l_dev.cpu().numpy().view(np.uint32), logits.view(np.uint32)), \
+            "router logits differ"
     taps = check_taps
     out = layer.forward(torch.from_numpy(x).to(device), torch.from_numpy(logits).to(device),
                         torch.from_numpy(bias).to(device), taps=taps, flags=flags)
@@ -60,12 +71,12 @@ def run_case(spec, T, seed, device, sample=None, flags=0, check_taps=True):
     if sample is None:
         sample = list(range(T))
     sample = sorted(set(int(t) for t in sample))
-    r_idx, _ = oracle.route(logits, bias, spec.k, spec.s)
+    r_idx, _ = oracle.route(logits, bias, spec.k, spec.s, score=spec.score)
     need = sorted(set(int(e) for t in sample for e in r_idx[t]))
     experts = {e: host_expert(spec, e) for e in need}
     shared = host_expert(spec, spec.E) if spec.f_shared else None
     ref = oracle.layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, experts,
-                       shared, x, logits, bias, want=sample)
+                       shared, x, logits, bias, want=sample, score=spec.score)
 
     g = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in vars(out).items()}
     R = T * spec.k

@@ -1,0 +1,75 @@
+"""Router front end on the GPU (pytest -m gpu): the router logits GEMM in the
+library's fixed fp32 order must equal the oracle's bit for bit, and the
+DeepSeek scoring sqrt(softplus(l)) (top-6, scale 1.5, E = 384: "256 experts,
+512 lines", section "The constant that always said 256") must pick the
+oracle's experts on both the fused decode path and the multi-kernel path."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from parity import device_layer, run_case
+from routed_expert_decode_gb300 import moe
+
+pytestmark = pytest.mark.gpu
+
+
+def _spec(**kw):
+    base = dict(name="r", E=64, k=8, d=512, f=256, f_shared=256, fmt=0, s=2.5, zipf_beta=0.0)
+    base.update(kw)
+    return synth.LayerSpec(**base)
+
+
+@pytest.mark.parametrize("T,E,d", [(1, 256, 6144), (5, 384, 1024), (3, 37, 96), (64, 192, 4096)])
+def test_router_logits_bit_exact(gpu, T, E, d):
+    spec = _spec(E=E, k=min(8, E), d=d)
+    rng = np.random.default_rng(T + E + d)
+    x = rng.normal(size=(T, d)).astype(np.float32)
+    w_r = (rng.normal(size=(E, d)) / np.sqrt(d)).astype(np.float32)
+    ref = oracle.router_logits(x, w_r)
+    out = torch.full((T, E), float("nan"), dtype=torch.float32, device=gpu)
+    desc = moe.make_desc(E, min(8, E), d, 256, 0, 0, 1.0)
+    moe.router_logits(desc, torch.from_numpy(w_r).to(gpu), torch.from_numpy(x).to(gpu), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+
+
+def test_router_logits_rejects_bad_args(gpu):
+    desc = moe.make_desc(16, 4, 64, 64, 0, 0, 1.0)
+    x = torch.zeros((2, 64), dtype=torch.float32, device=gpu)
+    w = torch.zeros((16, 64), dtype=torch.float32, device=gpu)
+    out = torch.zeros((2, 16), dtype=torch.float32, device=gpu)
+    bad = moe.make_desc(16, 4, 64, 64, 0, 0, 1.0, score=7)
+    with pytest.raises(moe.MoeError):
+        moe.router_logits(bad, w, x, out)
+    moe.router_logits(desc, w, x, out)  # well-formed call works
+    torch.cuda.synchronize()
+
+
+DS_SMALL = _spec(name="ds_small", E=384, k=6, d=1024, f=256, f_shared=256, s=1.5, score=1)
+
+
+@pytest.mark.parametrize("T", [1, 2, 9])
+def test_deepseek_scoring_layer(gpu, T):
+    """sqrt(softplus) routing with E=384, k=6, s=1.5: T <= 2 on the fused kernel,
+    T = 9 on the multi-kernel path; bit-exact picks, y within tolerance."""
+    layer = device_layer(DS_SMALL, gpu)
+    assert moe.layer_path(layer.desc(), T) == ("fused_decode" if T <= 2 else "multi_kernel")
+    for seed in (1, 2):
+        print("ds", T, seed, run_case(DS_SMALL, T, seed=seed, device=gpu, check_taps=T > 2))
+
+
+@pytest.mark.parametrize("spec,T", [(_spec(name="glm_router"), 1), (_spec(name="glm_router"), 6),
+                                    (DS_SMALL, 1)], ids=["sigmoid_t1", "sigmoid_t6", "ds_t1"])
+def test_router_front_end_layer(gpu, spec, T):
+    """x -> router GEMM -> scoring -> layer: logits bit-exact, then full parity."""
+    print("router", spec.name, T, run_case(spec, T, seed=4, device=gpu, check_taps=False,
+                                           router=True))
+
+
+def test_deepseek_full_size_decode(gpu):
+    """The full DeepSeek-style layer (E=384, k=6, d=6144, f=2048, shared 2048) at
+    T=1 through the router GEMM, on the fused kernel."""
+    print("ds_full", run_case(synth.DS_LAYER, 1, seed=0, device=gpu, check_taps=False,
+                              router=True))
