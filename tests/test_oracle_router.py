@@ -79,14 +79,15 @@ def test_route_sqrt_softplus_topk_and_weights(s):
 
 @pytest.mark.parametrize("T,E,d", [(1, 8, 64), (3, 37, 256), (2, 256, 6144)])
 def test_router_logits_within_fp32_bound(T, E, d):
-    """Against the exact fp64 dot: |err| <= (d/32 + 5) * 2^-24 * sum|x_i w_i|
-    (a d/32-long fma chain per lane, then a 5-level tree)."""
+    """Against the exact fp64 dot: |err| <= (32 + 5 + d/1024) * 2^-24 * sum|x_i w_i|
+    (a <= 32-long fma chain per lane and segment, a 5-level tree, then the
+    segment totals added in order)."""
     rng = np.random.default_rng(T * 1000 + E)
     x = rng.normal(size=(T, d)).astype(np.float32)
     w = (rng.normal(size=(E, d)) / math.sqrt(d)).astype(np.float32)
     got = oracle.router_logits(x, w).astype(np.float64)
     exact = x.astype(np.float64) @ w.T.astype(np.float64)
-    bound = (d / 32 + 5) * 2.0 ** -24 * (np.abs(x).astype(np.float64) @ np.abs(w).T.astype(np.float64))
+    bound = (32 + 5 + d / 1024) * 2.0 ** -24 * (np.abs(x).astype(np.float64) @ np.abs(w).T.astype(np.float64))
     assert np.all(np.abs(got - exact) <= bound + 1e-30)
 
 
@@ -103,6 +104,20 @@ def test_router_logits_closed_forms():
     xi = rng.integers(-8, 9, size=(3, d)).astype(np.float32)
     exact = (xi.astype(np.int64) @ wi.T.astype(np.int64)).astype(np.float64)
     assert np.array_equal(oracle.router_logits(xi, wi).astype(np.float64), exact)
+
+
+def test_router_logits_segment_order():
+    """Segments of 1024 are summed in ascending order after their own trees:
+    segment 0 totals 2^24, segment 1 totals 1.0 then segment 2 totals -2^24 -- in
+    that order the 1.0 is lost to rounding (2^24 + 1 = 2^24), so the logit is 0;
+    any order that cancels the big segments first would give 1."""
+    d = 3072
+    x = np.zeros((1, d), np.float32)
+    w = np.zeros((1, d), np.float32)
+    x[0, 0], w[0, 0] = 1.0, 2.0 ** 24
+    x[0, 1024], w[0, 1024] = 1.0, 1.0
+    x[0, 2048], w[0, 2048] = 1.0, -(2.0 ** 24)
+    assert oracle.router_logits(x, w)[0, 0] == 0.0
 
 
 def test_router_logits_tree_order():
