@@ -473,6 +473,59 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
                      "stage_gbs": {k: round(b[k] / (stage[k] / 1e3) / 1e9, 1)
                                    for k in ROOFLINE_STAGES if k in stage and b[k] > 0}}
         assert moe.check_device_error(ws) == 0
+    out.update(run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak))
+    return out
+
+
+def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
+    """The router front end at T=1: x -> router logits GEMM (fp32 W_r [E][d]) ->
+    layer, on the sigmoid layer and on the DeepSeek-scored 384-expert layer
+    (eager calls, 10 steps after 3 warm-ups, L2 flushed between)."""
+    out = {}
+    cases = [("router_decode_t1", synth.GLM_LAYER, layer), ("ds_router_decode_t1", synth.DS_LAYER, None)]
+    for name, spec, lay in cases:
+        if lay is None:
+            w = synth.fill_layer_device(spec, dev)
+            lay = moe.Layer(spec.E, spec.k, spec.d, spec.f, spec.f_shared, spec.fmt, spec.s, w, dev,
+                            score=spec.score)
+        T = 1
+        desc = lay.desc()
+        ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=dev)
+        bias = torch.from_numpy(synth.bias(spec)).to(dev)
+        w_r = torch.from_numpy(synth.router_weights(spec)).to(dev)
+        _, x = synth.token_inputs(spec, 0, T)
+        x_d = torch.from_numpy(x).to(dev)
+        l_d = torch.empty((T, spec.E), dtype=torch.float32, device=dev)
+        y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
+        n = 10
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+
+        def step(i):
+            ev[i][0].record()
+            moe.router_logits(desc, w_r, x_d, l_d)
+            ev[i][1].record()
+            moe.layer(desc, lay.weights, x_d, l_d, bias, y, ws)
+            ev[i][2].record()
+
+        for i in range(3):
+            step(0)
+        torch.cuda.synchronize()
+        for i in range(n):
+            flush_buf.zero_()
+            step(i)
+        torch.cuda.synchronize()
+        ms = statistics.mean(ev[i][0].elapsed_time(ev[i][2]) for i in range(n))
+        r_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n))
+        off = lay.views(ws, T)["off"].cpu()
+        counts = (off[1:] - off[:-1]).tolist()
+        b = stage_bytes(spec, T, counts, None)["total"] + spec.E * spec.d * 4
+        out[name] = {"T": T, "E": spec.E, "top_k": spec.k,
+                     "score": "sqrt_softplus" if spec.score else "sigmoid",
+                     "ms_per_step": round(ms, 4), "router_us": round(r_ms * 1e3, 1),
+                     "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": b,
+                     "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1),
+                     "frac_of_measured": round(b / (ms / 1e3) / 1e9 / peak, 4)}
+        assert moe.check_device_error(ws) == 0
     return out
 
 

@@ -195,15 +195,16 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
                            uint32_t n_events);
 
 /* Router logits in front of the scoring: logits[t][e] = sum_i x[t][i] *
- * w_router[e][i] in fp32 in one fixed order -- lane l (of 32) accumulates
- * i = l, l+32, ... ascending with fused multiply-adds, then the 32 partial sums
- * are combined pairwise over lane distances 16, 8, 4, 2, 1 -- so that any
- * implementation of that order gets the same bits (the expert picks downstream
- * depend on them).  The pages give no precision for the router GEMM; fp32
+ * w_router[e][i] in fp32 in one fixed order -- the inputs form segments of
+ * 1024; in each, lane l (of 32) accumulates i = l, l+32, ... ascending with
+ * fused multiply-adds, the 32 partial sums are combined pairwise over lane
+ * distances 16, 8, 4, 2, 1, and the segment totals are added in ascending
+ * order -- so that any implementation of that order gets the same bits (the
+ * expert picks downstream depend on them).  The pages give no precision for the router GEMM; fp32
  * weights and this order are this library's definition.
  * x: [T][d] fp32, w_router: [E][d] fp32, logits: [T][E] fp32, all device
  * pointers (caller-owned, 16-byte aligned).  Asynchronous on `stream`;
- * MOE_ERR_INVALID_ARG on a bad desc or NULL pointer with T > 0. */
+ * MOE_ERR_INVALID_ARG on a bad desc, d > 32768, or a NULL pointer with T > 0. */
 moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const float *x,
                              uint32_t T, float *logits, void *stream);
 

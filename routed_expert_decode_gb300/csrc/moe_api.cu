@@ -308,7 +308,7 @@ moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const 
   if (!desc_ok(desc)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!w_router || !x || !logits || !aligned(w_router, 16) || !aligned(x, 16) ||
-      !aligned(logits, 4))
+      !aligned(logits, 4) || desc->d > 32768 || (uint64_t)T * desc->n_expert > 0x7fffffffull)
     return MOE_ERR_INVALID_ARG;
   return from_cuda(launch_router_logits(*desc, w_router, x, T, logits, (cudaStream_t)stream));
 }

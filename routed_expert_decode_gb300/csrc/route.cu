@@ -350,31 +350,52 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
 }
 
 // logits[t][e] = x[t] . w_router[e] in the library's fixed order (moe.h,
-// moe_router_logits): one warp per (t, e); lane l runs the fma chain over
-// i = l, l+32, ..; the lanes' sums meet over xor distances 16..1.
-__global__ void __launch_bounds__(256)
+// moe_router_logits): one CTA per (t, e), warp g takes the 1024-input segment
+// g (lane l: fma chain over i = 1024g + l + 32j, all loads issued first), the
+// lanes' sums meet over xor distances 16..1, and warp 0 adds the segment totals
+// in ascending order.
+constexpr int kRouterSeg = 1024;
+__global__ void __launch_bounds__(1024)
     k_router_logits(const float *__restrict__ x, const float *__restrict__ wr, uint32_t T,
                     uint32_t E, uint32_t d, float *__restrict__ logits) {
-  const int lane = threadIdx.x & 31;
-  const uint64_t item = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32;
-  if (item >= (uint64_t)T * E) return;
-  const uint32_t t = (uint32_t)(item / E), e = (uint32_t)(item % E);
+  __shared__ float seg_total[32];
+  const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
+  const uint32_t t = blockIdx.x / E, e = blockIdx.x % E;
+  const uint32_t g0 = (uint32_t)g * kRouterSeg;
   const float *xr = x + (size_t)t * d;
   const float *wrow = wr + (size_t)e * d;
+  float xv[32], wv[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t i = g0 + lane + 32 * j;
+    const bool ok = i < d;
+    xv[j] = ok ? __ldg(xr + i) : 0.0f;
+    wv[j] = ok ? __ldg(wrow + i) : 0.0f;
+  }
   float p = 0.0f;
-#pragma unroll 8
-  for (uint32_t i = lane; i < d; i += 32) p = __fmaf_rn(__ldg(xr + i), __ldg(wrow + i), p);
+#pragma unroll
+  for (int j = 0; j < 32; ++j)
+    if (g0 + lane + 32 * j < d) p = __fmaf_rn(xv[j], wv[j], p);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
-  if (lane == 0) logits[item] = p;
+  if (lane == 0) seg_total[g] = p;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float total = seg_total[0];
+    const int nseg = (int)((d + kRouterSeg - 1) / kRouterSeg);
+    for (int s = 1; s < nseg; ++s) total = __fadd_rn(total, seg_total[s]);
+    logits[(size_t)t * E + e] = total;
+  }
 }
 
 cudaError_t launch_router_logits(const moe_desc &d, const float *w_router, const float *x,
                                  uint32_t T, float *logits, cudaStream_t stream) {
   const uint64_t items = (uint64_t)T * d.n_expert;
   if (items == 0) return cudaSuccess;
-  k_router_logits<<<(unsigned)((items + 7) / 8), 256, 0, stream>>>(x, w_router, T, d.n_expert,
-                                                                   d.d, logits);
+  if (items > 0x7fffffffull || d.d > 32u * kRouterSeg) return cudaErrorInvalidValue;
+  const unsigned warps = (d.d + kRouterSeg - 1) / kRouterSeg;
+  k_router_logits<<<(unsigned)items, warps * 32, 0, stream>>>(x, w_router, T, d.n_expert, d.d,
+                                                              logits);
   return cudaGetLastError();
 }
 
