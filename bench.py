@@ -479,10 +479,14 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
 
 def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
     """The router front end at T=1: x -> router logits GEMM (fp32 W_r [E][d]) ->
-    layer, on the sigmoid layer and on the DeepSeek-scored 384-expert layer
-    (eager calls, 10 steps after 3 warm-ups, L2 flushed between)."""
+    layer, on the sigmoid layer and on the DeepSeek-scored 384-expert layer.
+    Three CUDA graphs per case -- the logits GEMM kernel alone, that kernel
+    followed by moe_layer, and moe_layer_from_x (the GEMM inside the decode
+    kernel) -- each replayed 10 times after 3 warm-ups with L2 flushed before
+    every replay.  ms_per_step is moe_layer_from_x."""
     out = {}
     cases = [("router_decode_t1", synth.GLM_LAYER, layer), ("ds_router_decode_t1", synth.DS_LAYER, None)]
+    stream = torch.cuda.current_stream(dev)
     for name, spec, lay in cases:
         if lay is None:
             w = synth.fill_layer_device(spec, dev)
@@ -497,31 +501,55 @@ def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
         x_d = torch.from_numpy(x).to(dev)
         l_d = torch.empty((T, spec.E), dtype=torch.float32, device=dev)
         y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
-        n = 10
-        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
 
-        def step(i):
-            ev[i][0].record()
+        def router_only():
             moe.router_logits(desc, w_r, x_d, l_d)
-            ev[i][1].record()
-            moe.layer(desc, lay.weights, x_d, l_d, bias, y, ws)
-            ev[i][2].record()
 
-        for i in range(3):
-            step(0)
+        def separate():
+            moe.router_logits(desc, w_r, x_d, l_d)
+            moe.layer(desc, lay.weights, x_d, l_d, bias, y, ws)
+
+        def from_x():
+            moe.layer_from_x(desc, lay.weights, w_r, x_d, bias, l_d, y, ws)
+
+        for _ in range(3):
+            separate()
+            from_x()
         torch.cuda.synchronize()
-        for i in range(n):
-            flush_buf.zero_()
-            step(i)
-        torch.cuda.synchronize()
-        ms = statistics.mean(ev[i][0].elapsed_time(ev[i][2]) for i in range(n))
-        r_ms = statistics.mean(ev[i][0].elapsed_time(ev[i][1]) for i in range(n))
+        graphs = []
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            for fn in (router_only, separate, from_x):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    fn()
+                graphs.append(g)
+        stream.wait_stream(cap)
+        n = 10
+        times = []
+        for g in graphs:
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(n)]
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            for a, b in ev:
+                flush_buf.zero_()
+                a.record()
+                g.replay()
+                b.record()
+            torch.cuda.synchronize()
+            times.append(statistics.mean(a.elapsed_time(b) for a, b in ev))
+        r_ms, sep_ms, ms = times
         off = lay.views(ws, T)["off"].cpu()
         counts = (off[1:] - off[:-1]).tolist()
         b = stage_bytes(spec, T, counts, None)["total"] + spec.E * spec.d * 4
         out[name] = {"T": T, "E": spec.E, "top_k": spec.k,
                      "score": "sqrt_softplus" if spec.score else "sigmoid",
                      "ms_per_step": round(ms, 4), "router_us": round(r_ms * 1e3, 1),
+                     "separate_kernels_ms": round(sep_ms, 4),
+                     "router_gbs": round(spec.E * spec.d * 4 / (r_ms / 1e3) / 1e9, 1),
                      "tokens_per_s": round(T / (ms / 1e3), 1), "algorithmic_bytes": b,
                      "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1),
                      "frac_of_measured": round(b / (ms / 1e3) / 1e9 / peak, 4)}

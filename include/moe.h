@@ -145,12 +145,14 @@ typedef struct {
   size_t plan;                   /* internal work list */
   size_t sync;                   /* counters of the fused decode kernel (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
-  size_t trace;                  /* uint64 [1024][24] (MOE_FLAG_TRACE) */
+  size_t trace;                  /* uint64 [1024][28] (MOE_FLAG_TRACE) */
   size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales
                                     [R+T][d/32], fp16 h codes [R+T][fmax], in slot order */
   size_t xt, ht;                 /* 2-bit routed weights: int8 x codes [T][d] and h codes
                                     [R+T][fmax] with each 16-code group stored 4x4
                                     transposed (byte 4i+j = code 4j+i); 0 otherwise */
+  size_t rseg;                   /* router partial sums fp32 [T][E][ceil(d/1024)] of the
+                                    fused decode path (T <= 2); 0 otherwise */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
   uint32_t n_tap;                /* tapped features per row (gate/up and down) */
@@ -207,6 +209,24 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
  * MOE_ERR_INVALID_ARG on a bad desc, d > 32768, or a NULL pointer with T > 0. */
 moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const float *x,
                              uint32_t T, float *logits, void *stream);
+
+/* The layer from the hidden state: the router logits of moe_router_logits
+ * (same order, same bits), written to `logits` [T][E] fp32 (an output here,
+ * caller-owned), then moe_layer on them -- the router front end fused in front
+ * of the scoring and top-k ("256 experts, 512 lines", "The constant that
+ * always said 256": per token, n_expert logits feed the expert scores).
+ * On the fused decode path (moe_layer_path "fused_decode", T <= 2) the logits
+ * are computed inside the decode kernel: every CTA takes a share of the
+ * (expert, 1024-input segment) partial sums, writes them to the workspace
+ * (moe_ws_layout.rseg), and every CTA then adds each logit's segments in
+ * ascending order itself, while the shared expert's weights already stream.
+ * On the multi-kernel path the moe_router_logits kernel runs first.
+ * w_router [E][d] fp32 and x 16-byte aligned; d <= 32768; otherwise as
+ * moe_layer (workspace from moe_workspace_size, MOE_ERR_INVALID_ARG on a bad
+ * argument before anything is launched). */
+moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,
+                            const float *w_router, const float *x, const float *bias, uint32_t T,
+                            float *logits, float *y, void *ws, size_t ws_bytes, void *stream);
 
 /* Which implementation moe_layer uses for (desc, T) on the current device:
  * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */

@@ -49,6 +49,13 @@ constexpr int kBItemFeat = 32;   // features per gate/up item: one quantisation 
 constexpr int kDnRows = kBFeat == 8 ? 3 : 2;  // down rows per warp and pass (~43 / ~21 a stage)
 constexpr int kXRegs = kBFeat == 8 ? 6 : 4;   // x chunks per lane in registers (d <= 6144 / 8192)
 constexpr int kMaxStages = 8;
+// x quads (128 floats) a quantising warp takes at T tokens: d <= 16*kKSplit*32*kXRegs
+// = 6144 gives 48 quads per token, over 15 warps at T=1 and 14 at T=2
+constexpr int kMaxQuadsPerToken = 16 * kKSplit * 32 * kXRegs / 128;
+template <int NT>
+__host__ __device__ constexpr int x_quads() {
+  return (NT * kMaxQuadsPerToken + kConsumerWarps - NT - 1) / (kConsumerWarps - NT);
+}
 // partial-sum buffers of gate/up items.  The warp that requantises item i reads
 // buffer i % kPartBufs after releasing the item's last stage; the other warps
 // can then run at most kMaxStages stages ahead, i.e. into item i + 2 at most
@@ -91,6 +98,8 @@ enum : int {
   kTrW5ComputeB = 21,  // consumer warp 5: cycles in gate/up stages
   kTrW5ComputeC = 22,  // consumer warp 5: cycles in down stages
   kTrItemEnd = 23,     // consumer warp 0: cycles at item ends (barrier + requant)
+  // 24..26: routing warp 0 after its top-k, weights and permutation (ns);
+  // 27: the CTA's router partial sums written (ns)
   kTraceWords = 28
 };
 
@@ -118,6 +127,11 @@ struct FusedArgs {
   float s;
   uint32_t score;  // moe_score
   const float *x, *logits, *bias;
+  // router logits computed in the kernel (wr non-null): W_router [E][d] fp32, the
+  // segment partial sums rseg [T][E][nseg] (workspace), logits_out [T][E]
+  const float *wr;
+  float *rseg, *logits_out;
+  uint32_t nseg;
   const int8_t *gq, *uq, *dq, *sgq, *suq, *sdq;
   const uint16_t *gs, *us, *ds, *sgs, *sus, *sds;
   float *y;
@@ -133,6 +147,7 @@ struct FusedArgs {
   uint32_t *sync;  // see SyncView
   uint32_t *err;
   uint32_t c_rows, n_chunks, n_stages, stage_bytes;
+  uint32_t part_bytes;    // the part[] region, which also holds the routing scores
   long long wait_cycles;  // budget of every bounded wait
   unsigned long long *trace;  // MOE_FLAG_TRACE: kTraceWords per CTA, else null
   int stall_test;         // MOE_FLAG_TEST_STALL: never publish the routing result
@@ -146,7 +161,7 @@ struct SyncView {
   uint32_t *queue, *diag, *ready, *chunk, *done;
   uint32_t n_clear;  // words from queue up to and including done (diag words are kept)
   __device__ SyncView(uint32_t *base, uint32_t E, uint32_t n_chunks) {
-    queue = base;      // [0]; [1] unused
+    queue = base;      // [0]; [1]: CTAs whose router partial sums are written
     diag = base + 2;   // [2], [3]
     ready = base + 4;  // [E+1] gate/up items finished per expert
     chunk = ready + E + 1;  // [n_chunks] down contributions landed per chunk
@@ -332,104 +347,131 @@ __device__ __forceinline__ float warp_sum(float v) {
 // no unrolled sorting network -- and only the T routing warps run it, while the
 // other consumer warps quantise x.
 
-// (score, expert) order of the selection: higher score first, ties to the lower
-// expert index
-__device__ __forceinline__ bool ranks_before(float s1, int e1, float s2, int e2) {
-  return s1 > s2 || (s1 == s2 && e1 < e2);
-}
-
 __device__ __forceinline__ void route_bar_sync(uint32_t T) {
   asm volatile("bar.sync 3, %0;" ::"r"(T * 32) : "memory");
 }
 
-// selection scores sigmoid(logit) + bias of all T*E (token, expert) pairs
-// (every consumer thread; a consumer barrier follows)
-__device__ void route_scores(const FusedArgs &a, float *sc) {
+// scores p(l) (sigmoid or sqrt-softplus of the logit) and selection scores
+// c = p + bias of all T*E (token, expert) pairs, into sg and sc (every consumer
+// thread; a consumer barrier follows).  With the router in the kernel, the
+// logit is the sum of its segment partials in ascending order, read through L2
+// (other CTAs wrote them), and CTA 0 stores it for the caller.
+constexpr uint32_t kMaxSeg = 8;  // router segments: d <= 8192
+__device__ void route_scores(const FusedArgs &a, float *sc, float *sg, float pre_l, float pre_b) {
 #pragma unroll 1
-  for (uint32_t i = threadIdx.x; i < a.T * a.E; i += kConsumerWarps * 32)
-    sc[i] = __fadd_rn(score_rn(__ldg(a.logits + i), a.score), __ldg(a.bias + i % a.E));
+  for (uint32_t i = threadIdx.x; i < a.T * a.E; i += kConsumerWarps * 32) {
+    const bool first = i == threadIdx.x;  // its logit (if given) and bias came at entry
+    float l;
+    if (a.wr) {
+      const float *ps = a.rseg + (size_t)i * a.nseg;
+      float v[kMaxSeg];
+#pragma unroll
+      for (uint32_t g = 0; g < kMaxSeg; ++g) v[g] = g < a.nseg ? __ldcg(ps + g) : 0.0f;
+      l = v[0];
+#pragma unroll
+      for (uint32_t g = 1; g < kMaxSeg; ++g)
+        if (g < a.nseg) l = __fadd_rn(l, v[g]);
+      if (blockIdx.x == 0) a.logits_out[i] = l;
+    } else {
+      l = first ? pre_l : __ldg(a.logits + i);
+    }
+    const float p = score_rn(l, a.score);
+    sg[i] = p;
+    sc[i] = __fadd_rn(p, first ? pre_b : __ldg(a.bias + i % a.E));
+  }
 }
 
-// warps 0..T-1: warp t selects token t's top_k by k rounds of a strided scan
-// of the scores (ascending e per lane: strict '>' keeps the lower index) and a
-// butterfly argmax; then the stable permutation (rows by expert, then row
-// order) and the active list, with the T warps' threads as the R <= 64 rows
-__device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc,
+// order-preserving unsigned key of a selection score (scores are never NaN; -0
+// takes +0's key).  Key 0 is below every score's key: it marks an absent or
+// already selected entry.
+__device__ __forceinline__ uint32_t score_key(float c) {
+  uint32_t b = __float_as_uint(c);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// top-k of one token by one warp, E <= 32*NV: lane l holds the keys of experts
+// l + 32i (ct: the token's selection scores).  Each round takes the lane's
+// best key (strict '>' over ascending i keeps the lower expert), the warp's
+// largest key (redux) and the lowest expert holding it (redux), and the
+// winning lane retires that entry.
+template <int NV>
+__device__ __forceinline__ void topk_regs(const float *ct, uint32_t E, uint32_t k, int lane,
+                                          int *out) {
+  uint32_t v[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const uint32_t e = (uint32_t)lane + 32u * i;
+    v[i] = e < E ? score_key(ct[e]) : 0u;
+  }
+#pragma unroll 1
+  for (uint32_t j = 0; j < k; ++j) {
+    uint32_t bk = v[0];
+    int bi = 0;
+#pragma unroll
+    for (int i = 1; i < NV; ++i)
+      if (v[i] > bk) {
+        bk = v[i];
+        bi = i;
+      }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t be =
+        __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)lane + 32u * bi : 0xffffffffu);
+    if ((int)(be & 31u) == lane) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (i == (int)(be >> 5)) v[i] = 0u;
+    }
+    if (lane == 0) out[j] = (int)be;
+  }
+}
+
+// the same selection for E > 512: the keys replace the selection scores in
+// shared memory, and each round scans them with a stride of 32
+__device__ __noinline__ void topk_scan(float *ct, uint32_t E, uint32_t k, int lane, int *out) {
+  uint32_t *kt = reinterpret_cast<uint32_t *>(ct);
+#pragma unroll 1
+  for (uint32_t e = lane; e < E; e += 32) kt[e] = score_key(ct[e]);
+#pragma unroll 1
+  for (uint32_t j = 0; j < k; ++j) {
+    uint32_t bk = 0u, be_l = 0xffffffffu;
+#pragma unroll 1
+    for (uint32_t e = lane; e < E; e += 32) {
+      const uint32_t v = kt[e];
+      if (v > bk) {
+        bk = v;
+        be_l = e;
+      }
+    }
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
+    const uint32_t be = __reduce_min_sync(0xffffffffu, bk == m ? be_l : 0xffffffffu);
+    if ((int)(be & 31u) == lane) kt[be] = 0u;
+    if (lane == 0) out[j] = (int)be;
+  }
+}
+
+// warps 0..T-1: warp t selects token t's top_k (keys in registers for E <= 512,
+// else k rounds of a strided scan of the scores); then the stable permutation
+// (rows by expert, then row order) and the active list, with the T warps'
+// threads as the R <= 64 rows.  route_scores has filled sc and sg.
+__device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const float *sg,
                              unsigned long long *tr) {
   const int tid = (int)threadIdx.x - kRouteWarp0 * 32, lane = tid & 31, t = tid >> 5;
   const uint32_t E = a.E, k = a.k, T = a.T;
   const int R = (int)a.R;
   float *ct = sc + (size_t)t * E;
+  const float *gt = sg + (size_t)t * E;
   if (E <= 256) {
-    // the lane's (up to) 8 scores in registers; each round takes the lane-local
-    // best, a butterfly argmax, and the winner's entry is retired
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) v[i] = (uint32_t)lane + 32u * i < E ? ct[lane + 32 * i] : -INFINITY;
-#pragma unroll 1
-    for (uint32_t j = 0; j < k; ++j) {
-      float bs = v[0];
-      int bi = 0;
-#pragma unroll
-      for (int i = 1; i < 8; ++i)
-        if (v[i] > bs) {  // ascending e per lane: strict '>' keeps the lower index
-          bs = v[i];
-          bi = i;
-        }
-      int be = bs == -INFINITY ? 0x7fffffff : lane + 32 * bi;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ranks_before(os, oe, bs, be)) {
-          bs = os;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-          if (i == (be >> 5)) v[i] = -INFINITY;
-      }
-      if (lane == 0) rs.idx[t * k + j] = be;
-    }
+    topk_regs<8>(ct, E, k, lane, rs.idx + t * k);
+  } else if (E <= 512) {
+    topk_regs<16>(ct, E, k, lane, rs.idx + t * k);
   } else {
-    // larger E: k rounds of a strided scan of the scores in shared memory
-#pragma unroll 1
-    for (uint32_t j = 0; j < k; ++j) {
-      float bs = -INFINITY;
-      int be = 0x7fffffff;
-#pragma unroll 1
-      for (uint32_t e = lane; e < E; e += 32) {
-        const float v = ct[e];
-        if (v > bs) {
-          bs = v;
-          be = (int)e;
-        }
-      }
-#pragma unroll 1
-      for (int o = 16; o > 0; o >>= 1) {
-        const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ranks_before(os, oe, bs, be)) {
-          bs = os;
-          be = oe;
-        }
-      }
-      __syncwarp();
-      if (lane == 0) {
-        ct[be] = -INFINITY;
-        rs.idx[t * k + j] = be;
-      }
-      __syncwarp();
-    }
+    topk_scan(ct, E, k, lane, rs.idx + t * k);
   }
   __syncwarp();
   if (tr && tid == 0) tr[24] = global_ns();
   // lane j < k: the score of slot j; w = s * p_j / sum_j p_j (in order)
-  const float my_sigma =
-      (uint32_t)lane < k ? score_rn(__ldg(a.logits + (size_t)t * E + rs.idx[t * k + lane]), a.score)
-                         : 0.0f;
+  const float my_sigma = (uint32_t)lane < k ? gt[rs.idx[t * k + lane]] : 0.0f;
   float sum = 0.0f;
 #pragma unroll 1
   for (uint32_t j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xffffffffu, my_sigma, j));
@@ -513,8 +555,10 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc,
 // ---------------------------------------------------------------- the kernel
 // Shared-memory carve-up (all offsets multiples of 16 bytes):
 //   stages[NS][stage_bytes] | xq_s[T][d] | xs_s[T][d/32] | part[3][32][KS][2][2] |
-//   desc[8] | full[8] | empty[8] | route_bar | SharedCtl | RouteSmem | owned[n_chunks] |
-//   route scores[T][E]
+//   desc[8] | full[8] | empty[8] | route_bar | SharedCtl | RouteSmem | owned[n_chunks]
+// The routing scores (selection scores and p(l), [T][E] each) live in the part[]
+// region, which is sized for both: they are read only before the consumer
+// barrier that ends the routing, and part[] is written only after it.
 // NT: token count known at compile time (1 or 2): the one-token kernel has no
 // second-row code.
 template <int NT>
@@ -527,19 +571,45 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   int8_t *xq_s = (int8_t *)(stages + (size_t)NS * a.stage_bytes);
   float *xs_s = (float *)(xq_s + (size_t)NT * d);
   float *part = xs_s + (size_t)NT * nb;  // [2][feature 32][K part][row 2][g,u]
-  StageDesc *desc = (StageDesc *)(part + kPartBufs * kBItemFeat * kKSplit * kMaxT * 2);
+  StageDesc *desc = (StageDesc *)((uint8_t *)part + a.part_bytes);
   uint64_t *full = (uint64_t *)(desc + kMaxStages);
   uint64_t *empty = full + kMaxStages;
   uint64_t *route_bar = empty + kMaxStages;  // the consumers' routing is in RouteSmem
+  uint64_t *go_bar = route_bar + 1;          // the CTA's routing inputs are loaded
   SharedCtl &ctl = *(SharedCtl *)(route_bar + 2);
   volatile int *s_abort = &ctl.abort;
   int *item_cnt = ctl.item_cnt;
   RouteSmem &rs = *(RouteSmem *)(&ctl + 1);
   int *owned = (int *)(&rs + 1);  // [n_chunks] chunks whose last contribution this CTA landed
-  float *route_scratch = (float *)(owned + (a.n_chunks + 3) / 4 * 4);  // [T][E] scores
+  float *route_scratch = part;                           // [T][E] selection scores
+  float *route_sig = route_scratch + (size_t)NT * a.E;  // [T][E] scores p(l)
 
   const SyncView SV(a.sync, a.E, a.n_chunks);
   unsigned long long *tr = a.trace ? a.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
+  // The consumers' inputs are loaded first, before the set-up barrier: the
+  // routing inputs (a consumer thread's first logit and bias) and every x quad
+  // a quantising warp will take (lane l: floats 4l..4l+3 of quad q), so that
+  // each is one round trip from the kernel's start.
+  const uint32_t n_quad = NT * nb / 4;  // d % 256 == 0: whole quads per token
+  const uint32_t xw = (uint32_t)kConsumerWarps - NT;  // quantising warps
+  const uint32_t rw = (uint32_t)(warp - kRouteWarp0);  // routing warp index (token)
+  const uint32_t xi = (uint32_t)warp < (uint32_t)kRouteWarp0 ? warp : warp - NT;  // 0..xw-1
+  float pre_l = 0.0f, pre_b = 0.0f;
+  constexpr int kXQuads = x_quads<NT>();
+  float4 xa[kXQuads];
+  if (warp < kConsumerWarps) {
+    if ((uint32_t)tid < NT * a.E) {
+      if (!a.wr) pre_l = __ldg(a.logits + tid);
+      pre_b = __ldg(a.bias + (uint32_t)tid % a.E);
+    }
+    const float4 *x4 = reinterpret_cast<const float4 *>(a.x);
+#pragma unroll
+    for (int i = 0; i < kXQuads; ++i) {
+      const uint32_t q = xi + (uint32_t)i * xw;
+      xa[i] = rw >= NT && q < n_quad ? __ldg(x4 + (size_t)q * 32 + lane)
+                                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
   if (tr && tid == 0) {
     for (int i = 0; i < kTraceWords; ++i) tr[i] = 0;
     tr[kTrStart] = global_ns();
@@ -552,6 +622,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       mbar_init(&empty[i], kConsumerWarps);
     }
     mbar_init(route_bar, 1);
+    mbar_init(go_bar, 1);
     ctl.abort = ctl.exit_last = ctl.n_owned = ctl.writers_done = 0;
     for (int i = 0; i < kPartBufs; ++i) ctl.item_cnt[i] = 0;
     ctl.pub_head = ctl.pub_tail = 0;
@@ -607,6 +678,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         slot_chunk[st] = -1;
       };
       uint32_t item = atomicAdd(SV.queue, 1u);
+      // with the router in the kernel, the weight stream starts once this CTA's
+      // router loads have landed, so that they do not queue behind the stream's
+      // copies in the memory system (the grid waits for the slowest CTA's)
+      if (a.wr && !mbar_wait(go_bar, 0u, a.wait_cycles)) {
+        report_timeout(a, 1, 1);
+        *s_abort = 1;
+      }
       for (;;) {
         // ticket for the following item, fetched while this one is issued
         const uint32_t next_item = atomicAdd(SV.queue, 1u);
@@ -842,11 +920,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   } else {
     // ============================ consumers (warps 0..15)
     // x: every CTA quantises it for itself (CTA 0 also publishes xq/xs).  A warp
-    // load covers a quad of 4 blocks (lane l: floats 4l..4l+3, block l/8).  The
-    // warps that do not route take quads round-robin, loading the next quad
-    // before quantising the current one (a compact rolled loop: cold code).
-    const uint32_t n_quad = T * nb / 4;  // d % 256 == 0: whole quads per token
-    const float4 *x4 = reinterpret_cast<const float4 *>(a.x);
+    // load covers a quad of 4 blocks (lane l: floats 4l..4l+3, block l/8); the
+    // warps that do not route take quads round-robin (loaded at entry) in a
+    // compact rolled loop (the code runs once per call, with a cold cache).
     auto quant_quad = [&](uint32_t q, float4 v) {
       float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 #pragma unroll 1
@@ -864,28 +940,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         if ((lane & 7) == 0) a.xs[q * 4 + lane / 8] = sc;
       }
     };
-    const uint32_t xw = (uint32_t)kConsumerWarps - T;  // quantising warps
-    float4 xv = make_float4(0.f, 0.f, 0.f, 0.f);
-    {
-      const uint32_t rw0 = (uint32_t)(warp - kRouteWarp0);
-      const uint32_t xi0 = (uint32_t)warp < (uint32_t)kRouteWarp0 ? warp : warp - T;
-      if (rw0 >= T && xi0 < n_quad) xv = __ldg(x4 + (size_t)xi0 * 32 + lane);
+    if (a.wr) {
+      // router logits: the (expert, segment) units are spread over every
+      // consumer warp of the grid, each writing its segment's partial sums for
+      // the T tokens; then the CTA counts itself in and waits for all CTAs
+      // (all are resident and each arrives before it waits, so the wait ends)
+      const uint32_t units = a.E * a.nseg, n_warps = gridDim.x * kConsumerWarps;
+      const float *xr[NT];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) xr[t] = a.x + (size_t)t * d;
+#pragma unroll 1
+      for (uint32_t u = (uint32_t)warp * gridDim.x + blockIdx.x; u < units; u += n_warps) {
+        const uint32_t e = u / a.nseg, g = u % a.nseg;
+        float p[NT];
+        router_seg_sums<NT, NT == 1 ? 32 : 16>(xr, a.wr + (size_t)e * d, g, d, lane, p);
+        if (lane == 0) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) a.rseg[((size_t)t * a.E + e) * a.nseg + g] = p[t];
+        }
+      }
+      consumer_sync();
+      if (tid == 0) {
+        mbar_arrive(go_bar);
+        red_release_add(SV.queue + 1, 1u);
+        if (tr) tr[27] = global_ns();
+        const long long t0 = clock64();
+        for (int i = 0;; ++i) {
+          const uint32_t n = ld_acquire(SV.queue + 1);
+          if (n >= gridDim.x) break;
+          if (i >= kSpinIters || clock64() - t0 > a.wait_cycles) {
+            report_timeout(a, 7, n);
+            *s_abort = 1;
+            break;
+          }
+        }
+      }
+      consumer_sync();
     }
-    route_scores(a, route_scratch);
+    // every consumer thread scores a share of the T*E pairs (one compact
+    // rolled loop: this code runs once per call with a cold instruction cache,
+    // where a warp scoring a whole token in unrolled code was slower)
+    route_scores(a, route_scratch, route_sig, pre_l, pre_b);
     consumer_sync();
     if (tr && tid == 0) tr[kTrRouteLoaded] = global_ns();
-    const uint32_t rw = (uint32_t)(warp - kRouteWarp0);  // routing warp index (token)
     if (rw < T) {
-      route_select(a, rs, route_scratch, tr);
+      route_select(a, rs, route_scratch, route_sig, tr);
       if (tr && rw == 0 && lane == 0) tr[kTrRoutePerm] = global_ns();
       if (rw == 0 && lane == 0 && !a.stall_test) mbar_arrive(route_bar);  // routed items may go
     } else {
-      const uint32_t xi = (uint32_t)warp < (uint32_t)kRouteWarp0 ? warp : warp - T;  // 0..xw-1
+      // rolled; the quads shift down one register each pass (static indices
+      // keep them in registers)
 #pragma unroll 1
       for (uint32_t q = xi; q < n_quad; q += xw) {
-        const float4 v = xv;
-        if (q + xw < n_quad) xv = __ldg(x4 + (size_t)(q + xw) * 32 + lane);
-        quant_quad(q, v);
+        quant_quad(q, xa[0]);
+#pragma unroll
+        for (int i = 0; i + 1 < kXQuads; ++i) xa[i] = xa[i + 1];
       }
     }
     consumer_sync();
@@ -1189,7 +1298,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
 // host side --------------------------------------------------------------------
 namespace {
 struct FusedPlan {
-  uint32_t c_rows, n_chunks, n_stages, stage_bytes;
+  uint32_t c_rows, n_chunks, n_stages, stage_bytes, part_bytes;
   size_t smem;
 };
 
@@ -1204,6 +1313,7 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (D.d % (32 * kKSplit * 2)) return false;  // whole, even chunk counts per K part
   if (D.d > 16u * kKSplit * 32 * kXRegs) return false;  // x of a K part fits the registers
   if (c.R > (uint32_t)kMaxR) return false;
+  if ((D.d + kRouterSeg - 1) / kRouterSeg > kMaxSeg) return false;
   const uint32_t d = D.d, fmax = c.fmax;
   const size_t b_bytes = (size_t)kBFeat * 2 * (d + d / 16);
   const uint32_t row_c = fmax + fmax / 16;
@@ -1216,12 +1326,13 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   const uint32_t n_chunks = (d + c_rows - 1) / c_rows;
   if (4 + D.n_expert + 1 + n_chunks + 1 > kSyncInts) return false;
   const size_t stage = (b_bytes + 127) / 128 * 128;
-  const size_t rest = (size_t)c.T * d + (size_t)c.T * (d / 32) * 4 +
-                      kPartBufs * kBItemFeat * kKSplit * kMaxT * 2 * 4 +
+  size_t part = (size_t)kPartBufs * kBItemFeat * kKSplit * kMaxT * 2 * 4;
+  const size_t scores = 2 * (size_t)c.T * D.n_expert * 4;
+  part = (part > scores ? part : scores + 15) / 16 * 16;
+  const size_t rest = (size_t)c.T * d + (size_t)c.T * (d / 32) * 4 + part +
                       kMaxStages * sizeof(StageDesc) +
                       2 * kMaxStages * 8 + 16 + sizeof(SharedCtl) + sizeof(RouteSmem) +
-                      (size_t)(n_chunks + 3) / 4 * 16 +
-                      (size_t)c.T * D.n_expert * 4 + 128;
+                      (size_t)(n_chunks + 3) / 4 * 16 + 128;
   int dev = 0, max_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
@@ -1234,6 +1345,7 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   fp->n_chunks = n_chunks;
   fp->n_stages = ns;
   fp->stage_bytes = (uint32_t)stage;
+  fp->part_bytes = (uint32_t)part;
   fp->smem = rest + ns * stage;
   return true;
 }
@@ -1250,7 +1362,8 @@ bool fused_eligible(const Ctx &c) {
 }
 
 cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logits,
-                                const float *bias, float *y) {
+                                const float *bias, float *y, const float *w_router,
+                                float *logits_out) {
   FusedPlan fp;
   if (!fused_plan(c, &fp)) return cudaErrorNotSupported;
   const moe_desc &D = c.desc;
@@ -1266,8 +1379,13 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.s = D.s;
   a.score = D.score;
   a.x = x;
-  a.logits = logits;
+  a.logits = w_router ? nullptr : logits;
   a.bias = bias;
+  a.wr = w_router;
+  a.logits_out = logits_out;
+  a.rseg = (float *)(c.ws + c.L.rseg);
+  a.nseg = (D.d + kRouterSeg - 1) / kRouterSeg;
+  if (w_router && (!c.L.rseg || !logits_out)) return cudaErrorInvalidValue;
   a.gq = (const int8_t *)c.wts.gate.q;
   a.uq = (const int8_t *)c.wts.up.q;
   a.dq = (const int8_t *)c.wts.down.q;
@@ -1298,6 +1416,7 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.n_chunks = fp.n_chunks;
   a.n_stages = fp.n_stages;
   a.stage_bytes = fp.stage_bytes;
+  a.part_bytes = fp.part_bytes;
   a.stall_test = (D.flags & MOE_FLAG_TEST_STALL) ? 1 : 0;
   a.wait_cycles = a.stall_test ? kStallTestCycles : kWaitCycles;
   a.trace = (D.flags & MOE_FLAG_TRACE) ? (unsigned long long *)(c.ws + c.L.trace) : nullptr;

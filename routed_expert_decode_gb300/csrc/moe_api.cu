@@ -87,6 +87,10 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
     L.xt = p; p = align_up(p + (size_t)T * d->d);
     L.ht = p; p = align_up(p + slots * fmax);
   }
+  L.rseg = 0;
+  if (T >= 1 && T <= 2) {
+    L.rseg = p; p = align_up(p + (size_t)T * d->n_expert * ((d->d + kRouterSeg - 1) / kRouterSeg) * 4);
+  }
   L.trace = 0;
   if (d->flags & MOE_FLAG_TRACE) {
     L.trace = p; p = align_up(p + (size_t)1024 * 28 * 8);
@@ -181,12 +185,19 @@ moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float
   return MOE_OK;
 }
 
+// w_router non-null: the router logits are computed from x into `logits`
+// (an output then); else `logits` is the caller's input
 moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
                      const float *logits, const float *bias, uint32_t T, float *y, void *ws,
-                     size_t ws_bytes, void *stream, void *const *events, uint32_t n_events) {
+                     size_t ws_bytes, void *stream, void *const *events, uint32_t n_events,
+                     const float *w_router = nullptr) {
   if (!desc_ok(desc) || !weights_ok(desc, wts)) return MOE_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !logits || !bias || !y)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && w_router &&
+      (!aligned(w_router, 16) || !aligned(x, 16) || !aligned(logits, 4) || desc->d > 32768 ||
+       (uint64_t)T * desc->n_expert > 0x7fffffffull))
+    return MOE_ERR_INVALID_ARG;
   if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
   Ctx c = make_ctx(desc, wts, T, ws, stream);
@@ -198,13 +209,18 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   int32_t *pos = (int32_t *)(c.ws + c.L.pos);
   uint32_t *err = (uint32_t *)(c.ws + c.L.err);
   cudaError_t e;
+  float *logits_out = const_cast<float *>(w_router ? logits : nullptr);
   if (T > 0 && fused_eligible(c)) {
     if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
-    if ((e = launch_decode_fused(c, x, logits, bias, y)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_decode_fused(c, x, logits, bias, y, w_router, logits_out)) != cudaSuccess)
+      return from_cuda(e);
     if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
     return MOE_OK;
   }
   if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
+  if (w_router && T > 0 &&
+      (e = launch_router_logits(c.desc, w_router, x, T, logits_out, c.stream)) != cudaSuccess)
+    return from_cuda(e);
   if ((e = launch_route(c, logits, bias, idx, w)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_permute(c, idx, off, perm, pos, err)) != cudaSuccess) return from_cuda(e);
@@ -281,6 +297,14 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
                            void *ws, size_t ws_bytes, void *stream, void *const *events,
                            uint32_t n_events) {
   return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, events, n_events);
+}
+
+moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,
+                            const float *w_router, const float *x, const float *bias, uint32_t T,
+                            float *logits, float *y, void *ws, size_t ws_bytes, void *stream) {
+  if (T > 0 && !w_router) return MOE_ERR_INVALID_ARG;
+  return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0,
+                   T > 0 ? w_router : nullptr);
 }
 
 const char *moe_layer_path(const moe_desc *desc, uint32_t T) {

@@ -105,6 +105,47 @@ __device__ __forceinline__ float score_rn(float l, uint32_t fn) {
   return fn == MOE_SCORE_SQRT_SOFTPLUS ? sqrt_softplus_rn(l) : sigmoid_rn(l);
 }
 
+// Router logits order (moe_router_logits): the d inputs form segments of
+// kRouterSeg; the partial sum of segment g is an fma chain per lane l over
+// i = kRouterSeg*g + l + 32j, j ascending (i < d), followed by the lanes'
+// pairwise sums over xor distances 16, 8, 4, 2, 1; a logit is the segment sums
+// added in ascending g.  router_seg_sums gives every lane of the warp the sums
+// of segment g for NT tokens (x rows xr[t]) against one router row, issuing
+// the loads of JB consecutive j at a time (the chain order does not change).
+constexpr int kRouterSeg = 1024;
+
+template <int NT, int JB>
+__device__ __forceinline__ void router_seg_sums(const float *const (&xr)[NT], const float *wrow,
+                                                uint32_t g, uint32_t d, int lane, float (&p)[NT]) {
+  static_assert(32 % JB == 0, "JB divides the 32 steps of a lane");
+  const uint32_t i0 = g * kRouterSeg + (uint32_t)lane;
+#pragma unroll
+  for (int t = 0; t < NT; ++t) p[t] = 0.0f;
+#pragma unroll
+  for (int j0 = 0; j0 < 32; j0 += JB) {
+    float wv[JB], xv[NT][JB];
+#pragma unroll
+    for (int j = 0; j < JB; ++j) {
+      const uint32_t i = i0 + 32u * (uint32_t)(j0 + j);
+      const bool ok = i < d;
+      wv[j] = ok ? __ldg(wrow + i) : 0.0f;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) xv[t][j] = ok ? __ldg(xr[t] + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < JB; ++j)
+      if (i0 + 32u * (uint32_t)(j0 + j) < d) {
+#pragma unroll
+        for (int t = 0; t < NT; ++t) p[t] = __fmaf_rn(xv[t][j], wv[j], p[t]);
+      }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+    for (int t = 0; t < NT; ++t) p[t] = __fadd_rn(p[t], __shfl_xor_sync(0xffffffffu, p[t], o));
+  }
+}
+
 // one 32-element block: scale = amax/127, q = clamp(round_half_away(x/scale))
 __device__ __forceinline__ int quant_one(float x, float scale) {
   if (scale == 0.0f) return 0;
@@ -259,8 +300,11 @@ cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, flo
 // fused single-kernel decode (T <= 2): decode_fused.cu
 size_t fused_sync_ints(const moe_desc *d);
 bool fused_eligible(const Ctx &c);
+// w_router non-null: the kernel computes the router logits itself from x and
+// stores them to logits_out (`logits` is unused); else `logits` is the input
 cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logits,
-                                const float *bias, float *y);
+                                const float *bias, float *y, const float *w_router,
+                                float *logits_out);
 
 moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, const float *x,
                               const float *logits, const float *bias, uint32_t T, float *y,

@@ -352,33 +352,18 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
 // logits[t][e] = x[t] . w_router[e] in the library's fixed order (moe.h,
 // moe_router_logits): one CTA per (t, e), warp g takes the 1024-input segment
 // g (lane l: fma chain over i = 1024g + l + 32j, all loads issued first), the
-// lanes' sums meet over xor distances 16..1, and warp 0 adds the segment totals
+// lanes' sums meet over xor distances 16..1, and thread 0 adds the segment totals
 // in ascending order.
-constexpr int kRouterSeg = 1024;
 __global__ void __launch_bounds__(1024)
     k_router_logits(const float *__restrict__ x, const float *__restrict__ wr, uint32_t T,
                     uint32_t E, uint32_t d, float *__restrict__ logits) {
   __shared__ float seg_total[32];
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
   const uint32_t t = blockIdx.x / E, e = blockIdx.x % E;
-  const uint32_t g0 = (uint32_t)g * kRouterSeg;
-  const float *xr = x + (size_t)t * d;
-  const float *wrow = wr + (size_t)e * d;
-  float xv[32], wv[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const uint32_t i = g0 + lane + 32 * j;
-    const bool ok = i < d;
-    xv[j] = ok ? __ldg(xr + i) : 0.0f;
-    wv[j] = ok ? __ldg(wrow + i) : 0.0f;
-  }
-  float p = 0.0f;
-#pragma unroll
-  for (int j = 0; j < 32; ++j)
-    if (g0 + lane + 32 * j < d) p = __fmaf_rn(xv[j], wv[j], p);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) p = __fadd_rn(p, __shfl_xor_sync(0xffffffffu, p, o));
-  if (lane == 0) seg_total[g] = p;
+  const float *const xr[1] = {x + (size_t)t * d};
+  float p[1];
+  router_seg_sums<1, 32>(xr, wr + (size_t)e * d, (uint32_t)g, d, lane, p);
+  if (lane == 0) seg_total[g] = p[0];
   __syncthreads();
   if (threadIdx.x == 0) {
     float total = seg_total[0];

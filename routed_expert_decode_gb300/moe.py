@@ -36,7 +36,8 @@ TRACE_FIELDS = ("start_ns", "xq_done_ns", "first_stage_ns", "wait_full_cyc", "wa
                 "stages_b", "stages_c", "cons_end_ns", "wait_empty_cyc", "wait_route_cyc",
                 "items", "compute_b_cyc", "compute_c_cyc", "combine_cyc", "route_done_ns",
                 "prod_end_ns", "route_loaded_ns", "route_topk_ns", "route_perm_ns", "exit_ns",
-                "w5_wait_full_cyc", "w5_compute_b_cyc", "w5_compute_c_cyc", "item_end_cyc")
+                "w5_wait_full_cyc", "w5_compute_b_cyc", "w5_compute_c_cyc", "item_end_cyc",
+                "select_topk_ns", "select_weights_ns", "select_perm_ns", "router_written_ns")
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
@@ -58,7 +59,7 @@ class MoeWeights(ctypes.Structure):
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "xt", "ht", "err",
+                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "xt", "ht", "rseg", "err",
                  "total")
 
 
@@ -107,6 +108,9 @@ def lib():
         L.moe_layer_path.argtypes = [ctypes.POINTER(MoeDesc), _u32]
         L.moe_router_logits.argtypes = [ctypes.POINTER(MoeDesc), _vp, _vp, _u32, _vp, _vp]
         L.moe_router_logits.restype = ctypes.c_int
+        L.moe_layer_from_x.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
+                                       _vp, _vp, _u32, _vp, _vp, _vp, _sz, _vp]
+        L.moe_layer_from_x.restype = ctypes.c_int
         L.moe_layer_stage_name.restype = ctypes.c_char_p
         L.moe_tc_min_rows.argtypes = [ctypes.POINTER(MoeDesc), _u32]
         L.moe_tc_min_rows.restype = ctypes.c_int32
@@ -210,6 +214,21 @@ def layer(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, stream=Non
                          _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
                          ws.numel(), _stream(stream))
     _check("moe_layer", st)
+
+
+def layer_from_x(desc: MoeDesc, weights: MoeWeights, w_router, x, bias, logits, y, ws,
+                 stream=None):
+    """moe_layer_from_x: router logits from x (written to ``logits``), then the
+    layer on them; on the fused decode path the logits GEMM runs inside the
+    decode kernel."""
+    st = lib().moe_layer_from_x(ctypes.byref(desc), ctypes.byref(weights),
+                                _dev_ptr(w_router, torch.float32, "w_router"),
+                                _dev_ptr(x, torch.float32, "x"),
+                                _dev_ptr(bias, torch.float32, "bias"), x.shape[0],
+                                _dev_ptr(logits, torch.float32, "logits"),
+                                _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
+                                ws.numel(), _stream(stream))
+    _check("moe_layer_from_x", st)
 
 
 def layer_timed(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, events,
@@ -376,5 +395,19 @@ class Layer:
         if y is None:
             y = torch.empty((T, self.d), dtype=torch.float32, device=self.device)
         layer(self.desc(flags), self.weights, x, logits, bias, y, ws, stream)
+        v = self.views(ws, T, flags)
+        return LayerOutput(y=y, **v)
+
+    def forward_from_x(self, x: torch.Tensor, w_router: torch.Tensor, bias: torch.Tensor,
+                       logits: torch.Tensor, taps: bool = False, flags: int = 0,
+                       y: Optional[torch.Tensor] = None, stream=None) -> LayerOutput:
+        """moe_layer_from_x: the router logits of x (written to ``logits``
+        [T][E]) and the layer on them, in one call."""
+        flags = flags | (FLAG_DEBUG_TAPS if taps else 0)
+        T = x.shape[0]
+        ws = self.workspace(T, flags)
+        if y is None:
+            y = torch.empty((T, self.d), dtype=torch.float32, device=self.device)
+        layer_from_x(self.desc(flags), self.weights, w_router, x, bias, logits, y, ws, stream)
         v = self.views(ws, T, flags)
         return LayerOutput(y=y, **v)

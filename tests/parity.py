@@ -48,22 +48,29 @@ def host_expert(spec, e):
 def run_case(spec, T, seed, device, sample=None, flags=0, check_taps=True, router=False):
     """Run one batch on the GPU and the oracle; assert parity; return a report.
     router=True: the logits come from the router GEMM x . W_r (moe_router_logits
-    on the GPU, ora_router_logits on the CPU), which must agree bit for bit."""
+    on the GPU, ora_router_logits on the CPU), which must agree bit for bit;
+    router="fused": the same through moe_layer_from_x, which computes the logits
+    and runs the layer in one call."""
     logits, x = synth.token_inputs(spec, seed, T)
     bias = synth.bias(spec)
     layer = device_layer(spec, device)
+    taps = check_taps
     if router:
         w_r = synth.router_weights(spec)
         logits = oracle.router_logits(x, w_r)
-        l_dev = torch.empty((T, spec.E), dtype=torch.float32, device=device)
-        moe.router_logits(layer.desc(), torch.from_numpy(w_r).to(device),
-                          torch.from_numpy(x).to(device), l_dev)
+        l_dev = torch.full((T, spec.E), float("nan"), dtype=torch.float32, device=device)
+        w_dev, x_dev = torch.from_numpy(w_r).to(device), torch.from_numpy(x).to(device)
+        if router == "fused":
+            out = layer.forward_from_x(x_dev, w_dev, torch.from_numpy(bias).to(device), l_dev,
+                                       taps=taps, flags=flags)
+        else:
+            moe.router_logits(layer.desc(), w_dev, x_dev, l_dev)
         torch.cuda.synchronize()
         assert np.array_equal(l_dev.cpu().numpy().view(np.uint32), logits.view(np.uint32)), \
             "router logits differ"
-    taps = check_taps
-    out = layer.forward(torch.from_numpy(x).to(device), torch.from_numpy(logits).to(device),
-                        torch.from_numpy(bias).to(device), taps=taps, flags=flags)
+    if router != "fused":
+        out = layer.forward(torch.from_numpy(x).to(device), torch.from_numpy(logits).to(device),
+                            torch.from_numpy(bias).to(device), taps=taps, flags=flags)
     torch.cuda.synchronize()
     assert moe.check_device_error(layer.workspace(T, flags | (moe.FLAG_DEBUG_TAPS if taps else 0))) == 0
 

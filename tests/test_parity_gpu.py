@@ -52,6 +52,36 @@ def test_tie_logits_pick_lower_index(gpu):
     assert np.allclose(out.w.cpu().numpy(), 0.25)
 
 
+@pytest.mark.parametrize("E,k,T", [(32, 4, 1), (300, 8, 2), (600, 4, 2)])
+def test_fused_selection_ties_and_infinite_bias(gpu, E, k, T):
+    """The fused decode kernel's top-k (register keys for E <= 512, a shared
+    memory scan above): equal scores go to the lower expert, and with all but two
+    biases at -inf the two finite experts come first, then the lowest-indexed
+    -inf ones -- the oracle's order in both cases."""
+    import oracle
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=E, k=k, d=256, f=256)
+    layer = device_layer(spec, gpu)
+    assert moe.layer_path(layer.desc(), T) == "fused_decode"
+    rng = np.random.default_rng(E)
+    x = torch.from_numpy(rng.normal(size=(T, spec.d)).astype(np.float32)).to(gpu)
+    logits = np.zeros((T, E), dtype=np.float32)
+    bias = np.zeros(E, dtype=np.float32)
+    out = layer.forward(x, torch.from_numpy(logits).to(gpu), torch.from_numpy(bias).to(gpu))
+    torch.cuda.synchronize()
+    assert out.idx.cpu().tolist() == [list(range(k))] * T
+    bias[:] = -np.inf
+    bias[[E // 2, E - 1]] = 0.0
+    logits = rng.normal(size=(T, E)).astype(np.float32)
+    out = layer.forward(x, torch.from_numpy(logits).to(gpu), torch.from_numpy(bias).to(gpu))
+    torch.cuda.synchronize()
+    ref_idx, ref_w = oracle.route(logits, bias, k, spec.s)
+    assert np.array_equal(out.idx.cpu().numpy(), ref_idx)
+    assert np.allclose(out.w.cpu().numpy(), ref_w, rtol=4e-6, atol=0)
+    assert moe.check_device_error(layer.workspace(T, 0)) == 0
+
+
 def test_zero_tokens(gpu):
     spec = synth.TINY
     layer = device_layer(spec, gpu)

@@ -2,7 +2,10 @@
 library's fixed fp32 order must equal the oracle's bit for bit, and the
 DeepSeek scoring sqrt(softplus(l)) (top-6, scale 1.5, E = 384: "256 experts,
 512 lines", section "The constant that always said 256") must pick the
-oracle's experts on both the fused decode path and the multi-kernel path."""
+oracle's experts on both the fused decode path and the multi-kernel path.
+moe_layer_from_x (router GEMM inside the fused decode kernel at T <= 2, a
+separate kernel before the multi-kernel path) must give the same logits bits
+and the same layer results."""
 import numpy as np
 import pytest
 import torch
@@ -68,8 +71,59 @@ def test_router_front_end_layer(gpu, spec, T):
                                            router=True))
 
 
-def test_deepseek_full_size_decode(gpu):
+@pytest.mark.parametrize("router", [True, "fused"], ids=["separate", "fused"])
+def test_deepseek_full_size_decode(gpu, router):
     """The full DeepSeek-style layer (E=384, k=6, d=6144, f=2048, shared 2048) at
     T=1 through the router GEMM, on the fused kernel."""
     print("ds_full", run_case(synth.DS_LAYER, 1, seed=0, device=gpu, check_taps=False,
-                              router=True))
+                              router=router))
+
+
+@pytest.mark.parametrize("spec,T", [(_spec(name="glm_router"), 1), (_spec(name="glm_router"), 2),
+                                    (_spec(name="glm_router"), 6), (DS_SMALL, 1), (DS_SMALL, 2),
+                                    (_spec(name="odd_router", E=37, k=5, d=768, f=512), 2)],
+                         ids=["sigmoid_t1", "sigmoid_t2", "sigmoid_t6", "ds_t1", "ds_t2",
+                              "e37_t2"])
+def test_layer_from_x(gpu, spec, T):
+    """moe_layer_from_x: logits bit-exact against the oracle's router GEMM, then
+    full parity of the layer on them (fused kernel at T <= 2)."""
+    layer = device_layer(spec, gpu)
+    assert moe.layer_path(layer.desc(), T) == ("fused_decode" if T <= 2 else "multi_kernel")
+    for seed in (4, 5):
+        print("from_x", spec.name, T, run_case(spec, T, seed=seed, device=gpu, check_taps=False,
+                                               router="fused"))
+
+
+def test_layer_from_x_repeated_calls(gpu):
+    """The fused kernel's router arrival counter is left zeroed by every call:
+    back-to-back calls on one workspace give identical logits and y."""
+    spec = _spec(name="glm_router")
+    layer = device_layer(spec, gpu)
+    w_r = torch.from_numpy(synth.router_weights(spec)).to(gpu)
+    bias = torch.from_numpy(synth.bias(spec)).to(gpu)
+    outs = []
+    for _ in range(3):
+        _, x = synth.token_inputs(spec, 7, 1)
+        l_dev = torch.empty((1, spec.E), dtype=torch.float32, device=gpu)
+        out = layer.forward_from_x(torch.from_numpy(x).to(gpu), w_r, bias, l_dev)
+        torch.cuda.synchronize()
+        outs.append((l_dev.cpu().numpy().copy(), out.y.cpu().numpy().copy()))
+    assert moe.check_device_error(layer.workspace(1, 0)) == 0
+    for l_, y_ in outs[1:]:
+        assert np.array_equal(l_.view(np.uint32), outs[0][0].view(np.uint32))
+        assert np.array_equal(y_.view(np.uint32), outs[0][1].view(np.uint32))
+
+
+def test_layer_from_x_rejects_bad_args(gpu):
+    spec = _spec(name="glm_router")
+    layer = device_layer(spec, gpu)
+    x = torch.zeros((1, spec.d), dtype=torch.float32, device=gpu)
+    bias = torch.zeros((spec.E,), dtype=torch.float32, device=gpu)
+    l_dev = torch.zeros((1, spec.E), dtype=torch.float32, device=gpu)
+    ws = layer.workspace(1, 0)
+    y = torch.zeros((1, spec.d), dtype=torch.float32, device=gpu)
+    with pytest.raises(moe.MoeError):
+        moe.layer_from_x(layer.desc(), layer.weights, None, x, bias, l_dev, y, ws)
+    w_r = torch.zeros((spec.E, spec.d), dtype=torch.float32, device=gpu)
+    moe.layer_from_x(layer.desc(), layer.weights, w_r, x, bias, l_dev, y, ws)
+    torch.cuda.synchronize()
