@@ -25,8 +25,8 @@
 //    per-expert counter (after issuing the stage's weight copies) before it
 //    copies the h codes in.  Because every gate/up item is handed out before
 //    any down item and all CTAs are resident, every such wait ends.
-//  * The combine (y = o_shared + sum_j w_j o_j, fixed order) of an output chunk
-//    is done, at the end, by the CTA that landed the chunk's last contribution.
+//  * The combine (y = o_shared + sum_j w_j o_j, fixed order) runs at the end,
+//    after a grid barrier on the expert outputs o, split over all threads.
 //  * Every wait is bounded; on timeout the kernel flags kErrTimeout and exits.
 // Per-expert batches of the selected experts only, read once per call: the
 // indexed per-expert FFN of NeutronStar README, "MTP speculative decoding".
@@ -64,6 +64,10 @@ constexpr int kPartBufs = 3;
 static_assert(kMaxStages <= (kPartBufs - 1) * (kBItemFeat / kBFeat),
               "the stage ring could let a warp reach an item whose buffer is still read");
 constexpr uint32_t kSyncInts = MOE_SYNC_BYTES / 4;
+// true: the two lanes of a 32-block add their int32 half sums (one shuffle)
+// before the block's scale is applied; false: each lane scales its exact
+// half-block sum itself (a different fp32 summation order of the same terms)
+constexpr bool kPairShuffle = false;
 constexpr int kSpinIters = 1 << 26;                // iteration cap of every wait
 constexpr int kSuspendNs = 20000;                  // mbarrier try_wait suspend-time hint
 constexpr long long kWaitCycles = 4000000000ll;     // ~2 s at 2 GHz: a wait gives up after this
@@ -87,7 +91,7 @@ enum : int {
   kTrItems = 10,       // items taken by this CTA
   kTrComputeB = 11,    // consumer cycles in gate/up stages
   kTrComputeC = 12,    // consumer cycles in down stages
-  kTrCombine = 13,     // consumer cycles combining chunks
+  kTrCombine = 13,     // cycles in the final combine
   kTrRouteDone = 14,   // routing known to the producer (ns)
   kTrProdEnd = 15,     // producer leaves (ns)
   kTrRouteLoaded = 16, // selection scores computed (ns)
@@ -117,7 +121,6 @@ struct StageDesc {
   int sub;         // B: sub-stage in the item (0..3)
   int item_first;  // B: first feature of the item; C: chunk index
   int nrows;       // token rows of this expert
-  int n_contrib;   // C: experts contributing to each chunk
   int slot[kMaxT];
   int tok[kMaxT];
 };
@@ -158,25 +161,23 @@ struct FusedArgs {
 // no per-call memset is needed (a workspace must be zero-filled once after it
 // is allocated).  diag[] keeps the first timeout's site for the host.
 struct SyncView {
-  uint32_t *queue, *diag, *ready, *chunk, *done;
+  uint32_t *queue, *diag, *ready, *fin, *done;
   uint32_t n_clear;  // words from queue up to and including done (diag words are kept)
-  __device__ SyncView(uint32_t *base, uint32_t E, uint32_t n_chunks) {
+  __device__ SyncView(uint32_t *base, uint32_t E) {
     queue = base;      // [0]; [1]: CTAs whose router partial sums are written
     diag = base + 2;   // [2], [3]
     ready = base + 4;  // [E+1] gate/up items finished per expert
-    chunk = ready + E + 1;  // [n_chunks] down contributions landed per chunk
-    done = chunk + n_chunks;
-    n_clear = 4 + E + 1 + n_chunks + 1;
+    fin = ready + E + 1;  // CTAs whose expert outputs o are all written
+    done = fin + 1;       // CTAs that finished the combine
+    n_clear = 4 + E + 1 + 2;
   }
 };
 
-// CTA-local control words and the publisher's event ring.  Events: an expert's
-// h is complete (e >= 0), or a down stage's contribution to chunk c landed
-// (INT_MIN | contributions << 16 | c).
+// CTA-local control words and the publisher's event ring.  An event: expert e's
+// h rows of one gate/up item are written.
 struct SharedCtl {
   int abort;          // a wait gave up: stop issuing, skip the combine
   int exit_last;      // this CTA is the last one out (zeroes the counters)
-  int n_owned;        // chunks this CTA combines (owned[])
   int writers_done;   // consumer warps + producer that will post no more events
   int item_cnt[kPartBufs];  // consumer warps done with an item, by b_items % kPartBufs
   int pub_head;       // events reserved
@@ -309,10 +310,6 @@ __device__ __noinline__ void pub_post(const FusedArgs &a, SharedCtl &ctl, int ev
   ctl.pub_ev[i % kPubCap] = ev;
   __threadfence_block();
   *(volatile int *)&ctl.pub_seq[i % kPubCap] = i + 1;
-}
-
-__device__ __forceinline__ int chunk_event(uint32_t c, int contrib) {
-  return (int)(0x80000000u | ((uint32_t)contrib << 16) | c);
 }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -555,7 +552,7 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
 // ---------------------------------------------------------------- the kernel
 // Shared-memory carve-up (all offsets multiples of 16 bytes):
 //   stages[NS][stage_bytes] | xq_s[T][d] | xs_s[T][d/32] | part[3][32][KS][2][2] |
-//   desc[8] | full[8] | empty[8] | route_bar | SharedCtl | RouteSmem | owned[n_chunks]
+//   desc[8] | full[8] | empty[8] | route_bar, go_bar | SharedCtl | RouteSmem
 // The routing scores (selection scores and p(l), [T][E] each) live in the part[]
 // region, which is sized for both: they are read only before the consumer
 // barrier that ends the routing, and part[] is written only after it.
@@ -580,11 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   volatile int *s_abort = &ctl.abort;
   int *item_cnt = ctl.item_cnt;
   RouteSmem &rs = *(RouteSmem *)(&ctl + 1);
-  int *owned = (int *)(&rs + 1);  // [n_chunks] chunks whose last contribution this CTA landed
   float *route_scratch = part;                           // [T][E] selection scores
   float *route_sig = route_scratch + (size_t)NT * a.E;  // [T][E] scores p(l)
 
-  const SyncView SV(a.sync, a.E, a.n_chunks);
+  const SyncView SV(a.sync, a.E);
   unsigned long long *tr = a.trace ? a.trace + (size_t)blockIdx.x * kTraceWords : nullptr;
   // The consumers' inputs are loaded first, before the set-up barrier: the
   // routing inputs (a consumer thread's first logit and bias) and every x quad
@@ -623,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     }
     mbar_init(route_bar, 1);
     mbar_init(go_bar, 1);
-    ctl.abort = ctl.exit_last = ctl.n_owned = ctl.writers_done = 0;
+    ctl.abort = ctl.exit_last = ctl.writers_done = 0;
     for (int i = 0; i < kPartBufs; ++i) ctl.item_cnt[i] = 0;
     ctl.pub_head = ctl.pub_tail = 0;
     for (int i = 0; i < kPubCap; ++i) ctl.pub_seq[i] = 0;
@@ -640,12 +636,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       uint32_t g = 0;  // stages issued
       bool routed = false;
       uint32_t U = 0, NB = 0, total = 0;
-      // per ring slot: what completes when the consumers release it
-      //   chunk >= 0: a down stage contributing to that output chunk (n_contrib)
-      // (an expert's h readiness is raised by the warps that requantise it)
-      int slot_chunk[kMaxStages], slot_contrib[kMaxStages];
       unsigned long long p_wait_empty = 0, p_wait_route = 0, p_items = 0, p_wait_ready = 0;
-      for (int i = 0; i < kMaxStages; ++i) slot_chunk[i] = slot_contrib[i] = -1;
       // queue order: shared gate/up | routed gate/up | shared down | routed down.
       // Only the shared gate/up items are known before routing.
       const uint32_t n_pre = n_sh;
@@ -665,17 +656,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         total = NB + (U + (a.fs ? 1u : 0u)) * a.n_chunks;
         routed = true;
         return true;
-      };
-      // a stage was released by the consumers: publish what it completed
-      auto settle = [&](uint32_t st) {
-        if (slot_chunk[st] >= 0) {
-          // a shared-expert down stage issued before routing: the number of
-          // contributions per chunk (routed experts + 1) is learnt now
-          if (slot_contrib[st] < 0 && (routed || learn_routing())) slot_contrib[st] = (int)U + 1;
-          if (slot_contrib[st] > 0)
-            pub_post(a, ctl, chunk_event((uint32_t)slot_chunk[st], slot_contrib[st]));
-        }
-        slot_chunk[st] = -1;
       };
       uint32_t item = atomicAdd(SV.queue, 1u);
       // with the router in the kernel, the weight stream starts once this CTA's
@@ -738,7 +718,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             dsc.item_first = (int)chunk;
             dsc.first = (int)(chunk * a.c_rows);
             dsc.count = (int)min(a.c_rows, d - chunk * a.c_rows);
-            dsc.n_contrib = routed ? (int)(U + (a.fs ? 1u : 0u)) : -1;
           }
         }
         for (int sub = 0; sub < nsub; ++sub) {
@@ -752,14 +731,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             *s_abort = 1;
             dsc.kind = kKindEnd;
           }
-          // the slot's previous contents were released: publish their effects once,
-          // normally after the new copy is on its way, but before a wait on expert
-          // readiness (the previous contents may complete that very expert)
-          bool prev_settled = !empty_ok;
-          auto settle_prev = [&]() {
-            if (!prev_settled) settle(st);
-            prev_settled = true;
-          };
           dsc.sub = sub;
           uint8_t *buf = stages + (size_t)st * a.stage_bytes;
           if (dsc.kind == kKindB) {
@@ -793,21 +764,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             mbar_add_tx(&full[st], qb + sb);
             bulk_g2s(buf, q_src, qb, &full[st]);
             bulk_g2s(buf + qb, s_src, sb, &full[st]);
-            settle_prev();
             const long long t_wr = clock64();
             const uint32_t need = (K / kBItemFeat);
-            // while waiting, publish whatever older stages the consumers have
-            // released (chunk contributions)
             bool ready_ok = false;
             for (int it = 0; it < kSpinIters; ++it) {
               if (ld_acquire(&SV.ready[dsc.e]) >= need) {
                 ready_ok = true;
                 break;
               }
-              for (uint32_t q = (g + 1 > NS ? g + 1 - NS : 0); q < g; ++q)
-                if (slot_chunk[q % NS] >= 0 &&
-                    mbar_test(&empty[q % NS], (q / NS) & 1u))
-                  settle(q % NS);
               if (clock64() - t_wr > a.wait_cycles) break;
               __nanosleep(64);
             }
@@ -837,30 +801,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             desc[st] = dsc;
             mbar_arrive(&full[st]);
           }
-          settle_prev();
-          if (dsc.kind == kKindC) {
-            slot_chunk[st] = dsc.item_first;
-            slot_contrib[st] = dsc.n_contrib;
-          }
           ++g;
           if (dsc.kind == kKindEnd) break;
         }
         if (dsc.kind == kKindEnd) break;
         item = next_item;
       }
-      // drain: wait for the consumers to release every stage still held and
-      // publish its effects (the END stage itself is never released)
-      if (!*s_abort) {
-        for (uint32_t q = (g > NS ? g - NS : 0); q + 1 < g; ++q) {
-          const uint32_t st = q % NS;
-          if (!mbar_wait(&empty[st], (q / NS) & 1u, a.wait_cycles)) {
-            report_timeout(a, 2, q);
-            break;
-          }
-          settle(st);
-        }
-      }
-      atomicAdd(&ctl.writers_done, 1);  // no more events from the producer
+      atomicAdd(&ctl.writers_done, 1);  // the producer posts no events
       if (tr) {
         tr[kTrProdEnd] = global_ns();
         tr[kTrWaitEmpty] = p_wait_empty;
@@ -872,12 +819,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     __syncwarp();
   } else if (warp == kPublisherWarp) {
     // ============================ publisher (lane 0): takes the CTA's events in
-    // order and does their gpu-scope atomics, so that no producer or consumer
-    // warp waits on them.  h readiness: a release add (the requantising warp's
-    // stores were ordered before the event by a CTA-scope fence).  A chunk
-    // contribution: an acq_rel add; the CTA landing the last one combines it.
+    // order and does their gpu-scope release adds to the experts' readiness
+    // counts (the requantising warp's stores were ordered before the event by a
+    // CTA-scope fence), so that no producer or consumer warp waits on them
     if (lane == 0) {
-      int n_owned = 0;
       const long long t_pub = clock64();
       unsigned long long busy = 0;
       for (int i = 0;; ++i) {
@@ -903,16 +848,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const long long t1 = clock64();
         const int ev = ctl.pub_ev[i % kPubCap];
         *(volatile int *)&ctl.pub_tail = i + 1;
-        if (ev >= 0) {
-          red_release_add(&SV.ready[ev], 1u);
-        } else {
-          const uint32_t c = (uint32_t)ev & 0xFFFFu;
-          const uint32_t contrib = ((uint32_t)ev >> 16) & 0x7FFFu;
-          if (atom_acq_rel_add(&SV.chunk[c], 1u) + 1 == contrib) owned[n_owned++] = (int)c;
-        }
+        red_release_add(&SV.ready[ev], 1u);
         busy += clock64() - t1;
       }
-      ctl.n_owned = n_owned;
       if (tr) tr[kTrRouteTopk] = busy;
       (void)t_pub;
     }
@@ -1064,11 +1002,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const uint4 z = make_uint4(0, 0, 0, 0);
               const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
               int pg = dot16(wg, xr[i]), pu = dot16(wu, xr[i]);
-              pg += __shfl_xor_sync(0xffffffffu, pg, 1);
-              pu += __shfl_xor_sync(0xffffffffu, pu, 1);
+              if (kPairShuffle) {
+                pg += __shfl_xor_sync(0xffffffffu, pg, 1);
+                pu += __shfl_xor_sync(0xffffffffu, pu, 1);
+              }
               const uint32_t blk = ok ? c >> 1 : 0;
               const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
-              if (even && ok) {
+              if ((even || !kPairShuffle) && ok) {
                 g0 = __fmaf_rn((float)pg, sg * xsr[i], g0);
                 u0 = __fmaf_rn((float)pu, su * xsr[i], u0);
               }
@@ -1221,12 +1161,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const uint4 wd = live ? lds16(qc + (size_t)m * K + 16 * c) : make_uint4(0, 0, 0, 0);
               const float sw = live ? half_bits_to_float(scl[(size_t)m * kb + blk]) : 0.0f;
               int p0 = dot16(wd, h0);
-              p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-              if (even) acc[j][0] = __fmaf_rn((float)p0, sw * hs0, acc[j][0]);
+              if (kPairShuffle) p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
+              if (even || !kPairShuffle) acc[j][0] = __fmaf_rn((float)p0, sw * hs0, acc[j][0]);
               if (nr > 1) {
                 int p1 = dot16(wd, h1);
-                p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-                if (even) acc[j][1] = __fmaf_rn((float)p1, sw * hs1, acc[j][1]);
+                if (kPairShuffle) p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
+                if (even || !kPairShuffle) acc[j][1] = __fmaf_rn((float)p1, sw * hs1, acc[j][1]);
               }
             }
           }
@@ -1242,7 +1182,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);  // the producer counts the contribution
+        if (lane == 0) mbar_arrive(&empty[st]);
         n_c += 1;
         c_c += clock64() - t_got;
       }
@@ -1264,26 +1204,51 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     }
   }
 
-  // ============================ exit: combine the chunks this CTA completed last
+  // ============================ exit: combine, after every CTA's o rows are written
+  // A grid barrier (all CTAs are resident and each arrives before it waits, so
+  // the wait ends), then the T*d outputs are split over all threads of the
+  // grid: y = o_shared + sum_j w_j o_j, shared first, then slots in order, the
+  // k loads of an output issued together (one round trip).
+  __syncthreads();
+  if (tid == 0) {
+    red_release_add(SV.fin, 1u);  // this CTA's o stores, ordered by the barrier
+    const long long t0 = clock64();
+    for (int i = 0;; ++i) {
+      const uint32_t n = ld_acquire(SV.fin);
+      if (n >= gridDim.x) break;
+      if (i >= kSpinIters || clock64() - t0 > a.wait_cycles) {
+        report_timeout(a, 0, n);
+        *s_abort = 1;
+        break;
+      }
+      __nanosleep(32);
+    }
+  }
   __syncthreads();
   const long long t_comb = clock64();
-  if (warp < kConsumerWarps && !*s_abort) {
-    // y = o_shared + sum_j w_j o_j, shared first, then slots in order; all owned
-    // chunks in one pass (every load of a thread is independent: one round trip)
-    const uint32_t n_own = (uint32_t)ctl.n_owned, per = T * a.c_rows;
-    for (uint32_t i = tid; i < n_own * per; i += kConsumerWarps * 32) {
-      const uint32_t c = (uint32_t)owned[i / per], r = i % per;
-      const uint32_t t = r / a.c_rows, m = c * a.c_rows + r % a.c_rows;
-      if (m >= d) continue;  // the last chunk is shorter
+  if (!*s_abort) {
+    constexpr uint32_t kJ = 8;
+#pragma unroll 1
+    for (uint32_t i = blockIdx.x * kThreads + tid; i < T * d; i += gridDim.x * kThreads) {
+      const uint32_t t = i / d, m = i % d;
       float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
-      for (uint32_t j = 0; j < a.k; ++j)
-        acc = __fmaf_rn(rs.w[t * a.k + j], __ldcg(a.o + (size_t)rs.pos[t * a.k + j] * d + m), acc);
+#pragma unroll 1
+      for (uint32_t j0 = 0; j0 < a.k; j0 += kJ) {
+        float v[kJ];
+#pragma unroll
+        for (uint32_t jj = 0; jj < kJ; ++jj)
+          v[jj] = j0 + jj < a.k ? __ldcg(a.o + (size_t)rs.pos[t * a.k + j0 + jj] * d + m) : 0.0f;
+#pragma unroll
+        for (uint32_t jj = 0; jj < kJ; ++jj)
+          if (j0 + jj < a.k) acc = __fmaf_rn(rs.w[t * a.k + j0 + jj], v[jj], acc);
+      }
       a.y[(size_t)t * d + m] = acc;
     }
   }
   if (tr && tid == 0) tr[kTrCombine] += clock64() - t_comb;
   __syncthreads();
-  // the last CTA out zeroes the counters for the next call
+  // the last CTA out zeroes the counters for the next call (every CTA has
+  // passed the barrier above before it counts itself out here)
   if (tid == 0) ctl.exit_last = atom_acq_rel_add(SV.done, 1u) + 1 == gridDim.x;
   __syncthreads();
   if (*(volatile int *)&ctl.exit_last) {
@@ -1324,15 +1289,14 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (c_rows == 0) return false;
   if (c_rows > d) c_rows = d;
   const uint32_t n_chunks = (d + c_rows - 1) / c_rows;
-  if (4 + D.n_expert + 1 + n_chunks + 1 > kSyncInts) return false;
+  if (4 + D.n_expert + 1 + 2 > kSyncInts) return false;
   const size_t stage = (b_bytes + 127) / 128 * 128;
   size_t part = (size_t)kPartBufs * kBItemFeat * kKSplit * kMaxT * 2 * 4;
   const size_t scores = 2 * (size_t)c.T * D.n_expert * 4;
   part = (part > scores ? part : scores + 15) / 16 * 16;
   const size_t rest = (size_t)c.T * d + (size_t)c.T * (d / 32) * 4 + part +
                       kMaxStages * sizeof(StageDesc) +
-                      2 * kMaxStages * 8 + 16 + sizeof(SharedCtl) + sizeof(RouteSmem) +
-                      (size_t)(n_chunks + 3) / 4 * 16 + 128;
+                      2 * kMaxStages * 8 + 16 + sizeof(SharedCtl) + sizeof(RouteSmem) + 128;
   int dev = 0, max_smem = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   if (cudaDeviceGetAttribute(&max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
