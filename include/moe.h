@@ -145,7 +145,7 @@ typedef struct {
   size_t plan;                   /* internal work list */
   size_t sync;                   /* counters of the fused decode kernel (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
-  size_t trace;                  /* uint64 [1024][28] (MOE_FLAG_TRACE) */
+  size_t trace;                  /* uint64 [1024][32] (MOE_FLAG_TRACE) */
   size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales
                                     [R+T][d/32], fp16 h codes [R+T][fmax], in slot order */
   size_t xt, ht;                 /* 2-bit routed weights: int8 x codes [T][d] and h codes

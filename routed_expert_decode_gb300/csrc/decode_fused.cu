@@ -104,7 +104,11 @@ enum : int {
   kTrItemEnd = 23,     // consumer warp 0: cycles at item ends (barrier + requant)
   // 24..26: routing warp 0 after its top-k, weights and permutation (ns);
   // 27: the CTA's router partial sums written (ns)
-  kTraceWords = 28
+  kTrLatIssueGot = 28, // producer, over reused slots: cycles from issuing a stage to
+  kTrLatGotRel = 29,   //   consumer warp 0 having its data, from then to warp 0's
+  kTrLatRelEmpty = 30, //   release, and from that to the producer seeing the slot
+  kTrLatSamples = 31,  //   empty; and the number of such stages
+  kTraceWords = 32
 };
 
 __device__ __forceinline__ unsigned long long global_ns() {
@@ -184,6 +188,7 @@ struct SharedCtl {
   int pub_tail;       // events taken by the publisher
   int pub_ev[kPubCap];
   int pub_seq[kPubCap];  // event i is valid when pub_seq[i % kPubCap] == i + 1
+  long long t_issue[kMaxStages], t_got[kMaxStages], t_rel[kMaxStages];  // MOE_FLAG_TRACE
 };
 
 // Routing of the call, held in shared memory by every CTA.
@@ -637,6 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       bool routed = false;
       uint32_t U = 0, NB = 0, total = 0;
       unsigned long long p_wait_empty = 0, p_wait_route = 0, p_items = 0, p_wait_ready = 0;
+      long long lat_ig = 0, lat_gr = 0, lat_re = 0, lat_n = 0;
       // queue order: shared gate/up | routed gate/up | shared down | routed down.
       // Only the shared gate/up items are known before routing.
       const uint32_t n_pre = n_sh;
@@ -726,6 +732,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           const bool empty_ok =
               use == 0 || mbar_wait(&empty[st], (use - 1) & 1u, a.wait_cycles);
           p_wait_empty += clock64() - t_we;
+          if (tr && use > 0 && empty_ok) {
+            lat_ig += ctl.t_got[st] - ctl.t_issue[st];
+            lat_gr += ctl.t_rel[st] - ctl.t_got[st];
+            lat_re += clock64() - ctl.t_rel[st];
+            ++lat_n;
+          }
           if (!empty_ok) {
             report_timeout(a, 2, g);
             *s_abort = 1;
@@ -749,6 +761,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             bulk_g2s(buf + qb, u_src, qb, &full[st]);
             bulk_g2s(buf + 2 * qb, gs_src, sb, &full[st]);
             bulk_g2s(buf + 2 * qb + sb, us_src, sb, &full[st]);
+            if (tr) ctl.t_issue[st] = clock64();
           } else if (dsc.kind == kKindC) {
             const bool sh = dsc.e == (int)a.E;
             const uint32_t K = sh ? a.fs : a.f;
@@ -764,6 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             mbar_add_tx(&full[st], qb + sb);
             bulk_g2s(buf, q_src, qb, &full[st]);
             bulk_g2s(buf + qb, s_src, sb, &full[st]);
+            if (tr) ctl.t_issue[st] = clock64();
             const long long t_wr = clock64();
             const uint32_t need = (K / kBItemFeat);
             bool ready_ok = false;
@@ -814,6 +828,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         tr[kTrWaitRoute] = p_wait_route;
         tr[kTrItems] = p_items;
         tr[kTrWaitReady] = p_wait_ready;
+        tr[kTrLatIssueGot] = lat_ig;
+        tr[kTrLatGotRel] = lat_gr;
+        tr[kTrLatRelEmpty] = lat_re;
+        tr[kTrLatSamples] = lat_n;
       }
     }
     __syncwarp();
@@ -964,6 +982,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       const long long t_wf = clock64();
       const bool full_ok = mbar_wait(&full[st], use & 1u, a.wait_cycles);
       const long long t_got = clock64();
+      if (tr && tid == 0) ctl.t_got[st] = t_got;
       c_wait_full += t_got - t_wf;
       if (tr && tid == 0 && g == 0) tr[kTrFirstStage] = global_ns();
       if (!full_ok) {
@@ -1082,6 +1101,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         // the stage's data is no longer needed: release it before the item's
         // requant, so that the producer can refill the slot meanwhile
         __syncwarp();
+        if (tr && tid == 0) ctl.t_rel[st] = clock64();
         if (lane == 0) mbar_arrive(&empty[st]);
         if (dsc.sub == kBItemFeat / kBFeat - 1) {
           const long long t_item = clock64();
@@ -1182,6 +1202,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           }
         }
         __syncwarp();
+        if (tr && tid == 0) ctl.t_rel[st] = clock64();
         if (lane == 0) mbar_arrive(&empty[st]);
         n_c += 1;
         c_c += clock64() - t_got;

@@ -93,7 +93,7 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
   }
   L.trace = 0;
   if (d->flags & MOE_FLAG_TRACE) {
-    L.trace = p; p = align_up(p + (size_t)1024 * 28 * 8);
+    L.trace = p; p = align_up(p + (size_t)1024 * 32 * 8);
   }
   L.total = p;
   return L;

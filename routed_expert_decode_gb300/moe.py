@@ -37,7 +37,8 @@ TRACE_FIELDS = ("start_ns", "xq_done_ns", "first_stage_ns", "wait_full_cyc", "wa
                 "items", "compute_b_cyc", "compute_c_cyc", "combine_cyc", "route_done_ns",
                 "prod_end_ns", "route_loaded_ns", "route_topk_ns", "route_perm_ns", "exit_ns",
                 "w5_wait_full_cyc", "w5_compute_b_cyc", "w5_compute_c_cyc", "item_end_cyc",
-                "select_topk_ns", "select_weights_ns", "select_perm_ns", "router_written_ns")
+                "select_topk_ns", "select_weights_ns", "select_perm_ns", "router_written_ns",
+                "lat_issue_got_cyc", "lat_got_rel_cyc", "lat_rel_empty_cyc", "lat_samples")
 
 _vp = ctypes.c_void_p
 _sz = ctypes.c_size_t
