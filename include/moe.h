@@ -120,10 +120,21 @@ typedef struct {
 
 /* Routed experts, expert-major: gate, up [E][f][d]; down [E][d][f] (codes; for
  * Q2S the last dimension is in bytes = K/4), scales [E][rows][K/32].
- * Shared expert (Q8_0): s_gate, s_up [f_shared][d]; s_down [d][f_shared]. */
+ * Shared expert (Q8_0): s_gate, s_up [f_shared][d]; s_down [d][f_shared].
+ *
+ * Optional expert -> slot indirection, for routed experts cached in HBM from a
+ * host tier (moe_cache_*): expert_slot (device int32 [E], 4-byte aligned, caller-
+ * owned) gives the slot whose weights expert e uses, and gate/up/down then hold
+ * n_slots expert-sized slots ([n_slots][f][d], ...) instead of E experts.
+ * expert_slot == NULL: slot = expert, n_slots is ignored.  Every expert a call
+ * selects must map to a slot in [0, n_slots): one that does not fails the call's
+ * device check (MOE_ERR_DEVICE_CHECK via moe_check_device_error) before any of
+ * its weights are read; the entries of unselected experts are not read. */
 typedef struct {
   moe_mat gate, up, down;
   moe_mat s_gate, s_up, s_down;
+  const int32_t *expert_slot;
+  uint32_t n_slots;
 } moe_weights;
 
 /* The first MOE_WS_FIXED_BYTES of every workspace have a fixed layout: the
@@ -153,6 +164,7 @@ typedef struct {
                                     transposed (byte 4i+j = code 4j+i); 0 otherwise */
   size_t rseg;                   /* router partial sums fp32 [T][E][ceil(d/1024)] of the
                                     fused decode path (T <= 2); 0 otherwise */
+  size_t lidx, lw;               /* moe_stream_layer's lookahead picks [T][k] int32, fp32 */
   size_t err;                    /* uint32 device error word: always offset 0 */
   size_t total;
   uint32_t n_tap;                /* tapped features per row (gate/up and down) */
@@ -243,6 +255,98 @@ int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);
 /* Name of stage i of that path (what moe_layer_timed's events bracket),
  * NULL past the last stage. */
 const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i);
+
+/* ---- Host-tier expert streaming: an HBM expert cache over host memory ----
+ * The pages stream routed experts per token from a slower tier into a GPU-side
+ * expert cache, keep the hottest experts in an LFU cache, load the union of a
+ * batch's experts once, and prefetch the next layer's experts by running its
+ * router early (NeutronStar glm-local README, "SSD streaming optimizations":
+ * the host expert cache with LFU eviction and the cross-layer router-lookahead
+ * prefetch; "Long-prompt prefill": one union read serves a chunk).  Here the
+ * slow tier is host memory (pinned; on GB300 the Grace LPDDR across NVLink-C2C)
+ * holding every layer's routed experts, and the cache is an arena of n_slots
+ * expert-sized slots in HBM shared by all layers; moe_weights.expert_slot
+ * points the layer kernels at the slots.
+ *
+ * Policy (deterministic): each moe_cache_ensure call counts one lookup for every
+ * distinct expert it names (the LFU frequency, kept while the expert is evicted)
+ * and stamps it as the most recent use.  A missing expert takes the lowest free
+ * slot, else evicts the resident expert with the fewest lookups, ties to the
+ * least recent use, then to the lower (layer, expert).  Never evicted: the
+ * experts of the call itself and, for a prefetch, those of the latest ensure
+ * (their layer may still be running).  A call whose union exceeds what it may
+ * evict fails with MOE_ERR_WORKSPACE before copying anything.
+ * Ordering: ensure copies on its stream (the compute stream), so they follow
+ * every kernel enqueued there before; prefetch copies on its own stream wait for
+ * the compute work enqueued before the latest ensure, and an ensure that needs a
+ * prefetched expert makes its stream wait for that copy. */
+typedef struct moe_cache moe_cache;
+
+typedef struct {
+  uint64_t lookups;        /* distinct experts named by moe_cache_ensure calls */
+  uint64_t hits;           /* ... already resident (loaded before, or prefetched) */
+  uint64_t misses;         /* ... loaded by the ensure call itself */
+  uint64_t prefetch_loads; /* experts loaded by moe_cache_prefetch */
+  uint64_t prefetch_hits;  /* prefetched experts later named by an ensure while resident */
+  uint64_t evictions;
+  uint64_t bytes_h2d;      /* weight bytes copied host -> HBM */
+} moe_cache_stats;
+
+#define MOE_CACHE_POLICY_ONLY 1u /* no device work: moe_cache_plan only (tests, planning) */
+
+/* host_layers[n_layers]: each layer's routed gate/up/down planes in pinned host
+ * memory, expert-major as in moe_weights (shared-expert fields and expert_slot
+ * ignored).  arena: gate/up/down planes of n_slots expert slots in device memory
+ * (same per-expert layout).  slot_table: device int32 [n_layers][E], written by
+ * the cache (layer l's moe_weights.expert_slot = slot_table + l*E).  All memory
+ * is caller-owned and must outlive the cache; the cache itself allocates host
+ * memory and CUDA events only.  MOE_ERR_INVALID_ARG on a bad argument. */
+moe_status moe_cache_create(const moe_desc *desc, uint32_t n_layers,
+                            const moe_weights *host_layers, const moe_weights *arena,
+                            uint32_t n_slots, int32_t *slot_table, uint32_t flags,
+                            moe_cache **out);
+void moe_cache_destroy(moe_cache *cache);
+
+/* Make the distinct experts of experts[0..n) of `layer` resident, copying
+ * misses host -> HBM on `stream`, and upload the layer's slot table on `stream`.
+ * Experts outside [0, E) are MOE_ERR_INVALID_ARG. */
+moe_status moe_cache_ensure(moe_cache *cache, uint32_t layer, const int32_t *experts,
+                            uint32_t n, void *stream);
+
+/* Load what of experts[0..n) of `layer` is missing on `stream` (a side stream),
+ * without counting lookups; stops quietly when nothing may be evicted. */
+moe_status moe_cache_prefetch(moe_cache *cache, uint32_t layer, const int32_t *experts,
+                              uint32_t n, void *stream);
+
+/* The policy step of ensure (prefetch != 0: of prefetch) with no device work:
+ * updates the cache state as the call would and reports the experts it would
+ * load, their slots and the (layer*E + expert) each evicts (-1: a free slot);
+ * the arrays hold n entries, n_loaded receives the count. */
+moe_status moe_cache_plan(moe_cache *cache, uint32_t layer, const int32_t *experts, uint32_t n,
+                          int prefetch, int32_t *loaded, int32_t *slots, int64_t *evicted,
+                          uint32_t *n_loaded);
+
+/* Layers the cache was created for (0 for NULL). */
+uint32_t moe_cache_layers(const moe_cache *cache);
+
+/* Slot of (layer, expert), -1 when not resident or out of range. */
+int32_t moe_cache_slot(const moe_cache *cache, uint32_t layer, int32_t expert);
+moe_status moe_cache_get_stats(const moe_cache *cache, moe_cache_stats *out);
+
+/* One decode/prefill step of one layer with its routed experts served by the
+ * cache: route x's logits on the device, read the picks back (the stream is
+ * synchronised once), make their union resident (moe_cache_ensure on `stream`),
+ * then moe_layer on the slot weights.  wts: the layer's shared-expert planes
+ * (routed fields and expert_slot ignored: the arena and the layer's slot table
+ * are used).  next_logits / next_bias (optional, device, [T][E] / [E]): the next
+ * layer's router applied early to this layer's x -- their top-k picks are
+ * read back with this layer's and prefetched for layer + 1 on prefetch_stream
+ * while this layer runs.  Workspace as moe_layer. */
+moe_status moe_stream_layer(moe_cache *cache, uint32_t layer, const moe_desc *desc,
+                            const moe_weights *wts, const float *x, const float *logits,
+                            const float *bias, uint32_t T, const float *next_logits,
+                            const float *next_bias, float *y, void *ws, size_t ws_bytes,
+                            void *stream, void *prefetch_stream);
 
 /* ---- Allocation-free variant (the pages have no counterpart of this) ----
  * moe_layer without a workspace argument, for callers that cannot allocate

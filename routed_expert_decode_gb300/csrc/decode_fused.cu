@@ -120,6 +120,7 @@ __device__ __forceinline__ unsigned long long global_ns() {
 struct StageDesc {
   int kind;
   int e;           // expert id, E = shared expert
+  int we;          // routed: the expert's weight slot
   int first;       // B: first feature of the stage; C: first output row
   int count;       // B: features (8); C: output rows
   int sub;         // B: sub-stage in the item (0..3)
@@ -141,6 +142,8 @@ struct FusedArgs {
   uint32_t nseg;
   const int8_t *gq, *uq, *dq, *sgq, *suq, *sdq;
   const uint16_t *gs, *us, *ds, *sgs, *sus, *sds;
+  const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
+  uint32_t n_slots;      // slots in the routed weight planes
   float *y;
   int32_t *idx;
   float *w;
@@ -197,13 +200,14 @@ struct RouteSmem {
   float w[kMaxR];     // its combine weight
   int pos[kMaxR];     // slot of row r (stable sort by expert)
   int tok[kMaxR];     // token of slot p
-  int act_e[kMaxR];   // active routed experts in id order, their first slot and rows
+  int act_e[kMaxR];   // active routed experts in id order, their weight slot, first row slot and rows
+  int act_w[kMaxR];
   int act_row0[kMaxR];
   int act_rows[kMaxR];
   int row_at[kMaxR];  // row at slot p
   uint32_t first_bits[2];  // slot p opens an expert's run (bit p)
   int U;              // active routed experts
-  int pad;
+  int bad_slot;       // an active expert's weight slot is outside [0, n_slots)
 };
 
 // ---------------------------------------------------------------- PTX helpers
@@ -463,6 +467,7 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
   const int R = (int)a.R;
   float *ct = sc + (size_t)t * E;
   const float *gt = sg + (size_t)t * E;
+  if (tid == 0) rs.bad_slot = 0;  // read after the barriers below
   if (E <= 256) {
     topk_regs<8>(ct, E, k, lane, rs.idx + t * k);
   } else if (E <= 512) {
@@ -534,6 +539,9 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
       rs.act_e[u] = e;
       rs.act_row0[u] = p;
       rs.act_rows[u] = rows;
+      const int w = a.eslot ? __ldg(a.eslot + e) : e;
+      rs.act_w[u] = w;
+      if ((uint32_t)w >= a.n_slots) rs.bad_slot = 1;
       if (blockIdx.x == 0) {
         PlanView P(a.plan, E);
         P.act_e[u] = e;
@@ -541,14 +549,19 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
         P.act_rows[u] = rows;
       }
     }
-    if (p == 0) {
-      const int U = __popc(b0) + __popc(b1);
-      rs.U = U;
-      if (blockIdx.x == 0) {
-        PlanView P(a.plan, E);
-        P.hdr[0] = U;  // routed experts only
-        P.hdr[4] = 1;
-      }
+  }
+  route_bar_sync(T);
+  if (tid == 0) {
+    const int U = __popc(rs.first_bits[0]) + __popc(rs.first_bits[1]);
+    rs.U = U;
+    if (rs.bad_slot) {  // plan no routed work: every weight row read stays in range
+      rs.U = 0;
+      atomicOr(a.err, kErrBadSlot);
+    }
+    if (blockIdx.x == 0) {
+      PlanView P(a.plan, E);
+      P.hdr[0] = U;  // routed experts only
+      P.hdr[4] = 1;
     }
   }
   route_bar_sync(T);
@@ -709,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             }
           } else {
             dsc.e = rs.act_e[u];
+            dsc.we = rs.act_w[u];
             const int row0 = rs.act_row0[u];
             dsc.nrows = rs.act_rows[u];
             for (int r = 0; r < dsc.nrows; ++r) {
@@ -749,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
             dsc.first = dsc.item_first + sub * kBFeat;
             dsc.count = kBFeat;
             const bool sh = dsc.e == (int)a.E;
-            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * a.f + dsc.first;
+            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.we * a.f + dsc.first;
             const int8_t *g_src = (sh ? a.sgq : a.gq) + row * d;
             const int8_t *u_src = (sh ? a.suq : a.uq) + row * d;
             const uint16_t *gs_src = (sh ? a.sgs : a.gs) + row * nb;
@@ -765,7 +779,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           } else if (dsc.kind == kKindC) {
             const bool sh = dsc.e == (int)a.E;
             const uint32_t K = sh ? a.fs : a.f;
-            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.e * d + dsc.first;
+            const size_t row = sh ? (size_t)dsc.first : (size_t)dsc.we * d + dsc.first;
             const int8_t *q_src = (sh ? a.sdq : a.dq) + row * K;
             const uint16_t *s_src = (sh ? a.sds : a.ds) + row * (K / 32);
             const uint32_t qb = (uint32_t)dsc.count * K, sb = (uint32_t)dsc.count * (K / 32) * 2;
@@ -1383,6 +1397,8 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.sgs = c.wts.s_gate.scale;
   a.sus = c.wts.s_up.scale;
   a.sds = c.wts.s_down.scale;
+  a.eslot = c.wts.expert_slot;
+  a.n_slots = c.wexp;
   a.y = y;
   a.idx = (int32_t *)(c.ws + c.L.idx);
   a.w = (float *)(c.ws + c.L.w);

@@ -22,6 +22,7 @@ struct GUArgs {
   uint32_t E, k, d, f, fs, R, fmax;
   const int8_t *gq, *uq, *sgq, *suq;
   const uint16_t *gs, *us, *sgs, *sus;
+  const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
   const int8_t *xq;  // x codes [T][d]
   const int8_t *xt;  // 2-bit routed weights: x codes, 16-code groups transposed
   const float *xs;
@@ -36,6 +37,7 @@ struct DNArgs {
   uint32_t E, d, f, fs, R, fmax;
   const int8_t *dq, *sdq;
   const uint16_t *ds, *sds;
+  const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
   const int8_t *hq;  // h codes [slots][fmax]
   const int8_t *ht;  // 2-bit routed weights: h codes, 16-code groups transposed
   const float *hs;
@@ -239,8 +241,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>()))
         gateup_group<MOE_FMT_Q8_0, NFS, JS, MAXR, TAPS>(a, a.sgq, a.sgs, a.suq, a.sus, a.fs,
                                                         n0 + f, row0, nrows, true);
     } else {
-      const size_t qoff = (size_t)e * a.f * row_bytes(FMT, a.d);
-      const size_t soff = (size_t)e * a.f * (a.d / 32);
+      const size_t we = (size_t)weight_slot(a.eslot, e);  // validated by k_plan
+      const size_t qoff = we * a.f * row_bytes(FMT, a.d);
+      const size_t soff = we * a.f * (a.d / 32);
       gateup_group<FMT, NF, J, MAXR, TAPS>(a, a.gq + qoff, a.gs + soff, a.uq + qoff,
                                            a.us + soff, a.f, n0, row0, nrows, false);
     }
@@ -339,8 +342,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>())) k_
       for (int f = 0; f < NF; f += NFS)
         down_group<MOE_FMT_Q8_0, NFS, JS, MAXR, TAPS>(a, a.sdq, a.sds, a.fs, m0 + f, row0, nrows);
     } else {
-      const size_t qoff = (size_t)e * a.d * row_bytes(FMT, a.f);
-      const size_t soff = (size_t)e * a.d * (a.f / 32);
+      const size_t we = (size_t)weight_slot(a.eslot, e);  // validated by k_plan
+      const size_t qoff = we * a.d * row_bytes(FMT, a.f);
+      const size_t soff = we * a.d * (a.f / 32);
       down_group<FMT, NF, J, MAXR, TAPS>(a, a.dq + qoff, a.ds + soff, a.f, m0, row0, nrows);
     }
   }
@@ -456,6 +460,7 @@ cudaError_t launch_gateup(const Ctx &c, const int32_t *perm) {
   a.suq = (const int8_t *)c.wts.s_up.q;
   a.sgs = c.wts.s_gate.scale;
   a.sus = c.wts.s_up.scale;
+  a.eslot = c.wts.expert_slot;
   a.xq = (const int8_t *)(c.ws + c.L.xq);
   a.xt = c.L.xt ? (const int8_t *)(c.ws + c.L.xt) : nullptr;
   a.xs = (const float *)(c.ws + c.L.xs);
@@ -491,6 +496,7 @@ cudaError_t launch_down(const Ctx &c) {
   a.fmax = c.fmax;
   a.dq = (const int8_t *)c.wts.down.q;
   a.ds = c.wts.down.scale;
+  a.eslot = c.wts.expert_slot;
   a.sdq = (const int8_t *)c.wts.s_down.q;
   a.sds = c.wts.s_down.scale;
   a.hq = (const int8_t *)(c.ws + c.L.hq);

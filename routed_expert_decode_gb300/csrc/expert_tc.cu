@@ -58,6 +58,7 @@ struct TcArgs {
   int32_t *tap;                          // taps (null when off)
   uint32_t tap_nb;                       // blocks per tap row
   uint32_t *err;
+  const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
   uint32_t n_stages, stage_bytes;
   unsigned long long *trace;  // MOE_FLAG_TRACE: kTcTraceWords per CTA, else null
 };
@@ -480,7 +481,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
         const TcTile t = tc_tile<MAT>(P, a, tile);
         const bool sh = t.e == (int)a.E;
-        const int wrow = sh ? t.m0 : (int)(t.e * (MAT == 2 ? (int)a.f : (int)a.d)) + t.m0;
+        // routed weights from the expert's slot (validated by k_plan)
+        const int wrow =
+            sh ? t.m0 : weight_slot(a.eslot, t.e) * (MAT == 2 ? (int)a.f : (int)a.d) + t.m0;
         for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
           if (ks % kSG == 0) {
             // scales of stages ks .. ks+kSG-1: 8 blocks of the tile's weight rows
@@ -774,6 +777,7 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   a.fs = D.f_shared;
   a.R = c.R;
   a.fmax = c.fmax;
+  a.eslot = c.wts.expert_slot;
   a.plan = (const int *)(c.ws + c.L.plan);
   a.err = (uint32_t *)(c.ws + c.L.err);
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace ? (unsigned long long *)(c.ws + c.L.trace)
@@ -794,9 +798,9 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     a.tap = taps ? (int32_t *)(c.ws + c.L.tap_gu) : nullptr;
     a.tap_nb = D.d / 32;
     ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.gate.q, D.d,
-                   (uint64_t)D.n_expert * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     ok &= make_map(&maps.w[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.up.q, D.d,
-                   (uint64_t)D.n_expert * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared) {
       ok &= make_map(&maps.sw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.s_gate.q, D.d, D.f_shared,
                      D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -810,9 +814,9 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
                    (uint64_t)D.d * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
     // scales: 8 blocks (kSG stages) of 128 weight rows / 64 activation rows per copy
     ok &= make_map(&maps.ws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.gate.scale, D.d / 32,
-                   (uint64_t)D.n_expert * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     ok &= make_map(&maps.ws[1], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.up.scale, D.d / 32,
-                   (uint64_t)D.n_expert * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.f, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared) {
       ok &= make_map(&maps.sws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.s_gate.scale, D.d / 32,
                      D.f_shared, D.d / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -834,7 +838,7 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     a.tap = taps ? (int32_t *)(c.ws + c.L.tap_dn) : nullptr;
     a.tap_nb = c.fmax / 32;
     ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.down.q, D.f,
-                   (uint64_t)D.n_expert * D.d, D.f, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.d, D.f, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared)
       ok &= make_map(&maps.sw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.s_down.q, D.f_shared,
                      D.d, D.f_shared, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -845,7 +849,7 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     ok &= make_map(&maps.act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, c.ws + c.L.hperm, c.fmax, slots,
                    (uint64_t)c.fmax * 2, kBK, kBN, CU_TENSOR_MAP_SWIZZLE_128B);
     ok &= make_map(&maps.ws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.down.scale, D.f / 32,
-                   (uint64_t)D.n_expert * D.d, D.f / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+                   (uint64_t)c.wexp * D.d, D.f / 16, kSG * 2, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared)
       ok &= make_map(&maps.sws[0], CU_TENSOR_MAP_DATA_TYPE_UINT16, c.wts.s_down.scale,
                      D.f_shared / 32, D.d, D.f_shared / 16, kSG * 2, kBM,

@@ -39,6 +39,11 @@ bool weights_ok(const moe_desc *d, const moe_weights *w) {
   if (!w) return false;
   const int f = d->routed_fmt;
   if (!mat_ok(w->gate, f) || !mat_ok(w->up, f) || !mat_ok(w->down, f)) return false;
+  if (w->expert_slot) {
+    if (!aligned(w->expert_slot, 4) || w->n_slots < 1) return false;
+    if ((uint64_t)w->n_slots * d->f > (1u << 30) || (uint64_t)w->n_slots * d->d > (1u << 30))
+      return false;
+  }
   if (d->f_shared) {
     if (!mat_ok(w->s_gate, MOE_FMT_Q8_0) || !mat_ok(w->s_up, MOE_FMT_Q8_0) ||
         !mat_ok(w->s_down, MOE_FMT_Q8_0))
@@ -91,6 +96,8 @@ moe_ws_layout make_layout(const moe_desc *d, uint32_t T) {
   if (T >= 1 && T <= 2) {
     L.rseg = p; p = align_up(p + (size_t)T * d->n_expert * ((d->d + kRouterSeg - 1) / kRouterSeg) * 4);
   }
+  L.lidx = p; p = align_up(p + R * 4);
+  L.lw = p; p = align_up(p + R * 4);
   L.trace = 0;
   if (d->flags & MOE_FLAG_TRACE) {
     L.trace = p; p = align_up(p + (size_t)1024 * 32 * 8);
@@ -122,6 +129,7 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
   c.T = T;
   c.R = T * d->top_k;
   c.fmax = d->f > d->f_shared ? d->f : d->f_shared;
+  c.wexp = (w && w->expert_slot) ? w->n_slots : d->n_expert;
   c.ws = (uint8_t *)ws;
   c.L = make_layout(d, T);
   c.stream = (cudaStream_t)stream;
@@ -305,6 +313,54 @@ moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,
   if (T > 0 && !w_router) return MOE_ERR_INVALID_ARG;
   return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0,
                    T > 0 ? w_router : nullptr);
+}
+
+moe_status moe_stream_layer(moe_cache *cache, uint32_t layer, const moe_desc *desc,
+                            const moe_weights *wts, const float *x, const float *logits,
+                            const float *bias, uint32_t T, const float *next_logits,
+                            const float *next_bias, float *y, void *ws, size_t ws_bytes,
+                            void *stream, void *prefetch_stream) {
+  const moe_desc *cd = cache_desc(cache);
+  if (!cd || !desc_ok(desc) || !wts) return MOE_ERR_INVALID_ARG;
+  if (cd->n_expert != desc->n_expert || cd->d != desc->d || cd->f != desc->f ||
+      cd->routed_fmt != desc->routed_fmt)
+    return MOE_ERR_INVALID_ARG;
+  if (next_logits && !next_bias) return MOE_ERR_INVALID_ARG;
+  moe_weights w = *wts;
+  if (!cache_layer_routed(cache, layer, &w)) return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(desc, &w)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !logits || !bias || !y)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  Ctx c = make_ctx(desc, &w, T, ws, stream);
+  int32_t *idx = (int32_t *)(c.ws + c.L.idx);
+  int32_t *lidx = (int32_t *)(c.ws + c.L.lidx);
+  const bool look = next_logits != nullptr && layer + 1 < moe_cache_layers(cache);
+  const size_t R = c.R;
+  int32_t *host = cache_pinned(cache, 2 * R);
+  if (!host) {
+    set_last_error("moe_stream_layer: cudaHostAlloc failed");
+    return MOE_ERR_CUDA;
+  }
+  // the picks of this layer (and of the next layer's router, run early), read back
+  cudaError_t e = launch_route(c, logits, bias, idx, (float *)(c.ws + c.L.w));
+  if (e == cudaSuccess && look)
+    e = launch_route(c, next_logits, next_bias, lidx, (float *)(c.ws + c.L.lw));
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(host, idx, R * 4, cudaMemcpyDeviceToHost, c.stream);
+  if (e == cudaSuccess && look)
+    e = cudaMemcpyAsync(host + R, lidx, R * 4, cudaMemcpyDeviceToHost, c.stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(c.stream);
+  if (e != cudaSuccess) return from_cuda(e);
+  moe_status st = moe_cache_ensure(cache, layer, host, (uint32_t)R, stream);
+  if (st != MOE_OK) return st;
+  if (look) {
+    st = moe_cache_prefetch(cache, layer + 1, host + R, (uint32_t)R, prefetch_stream);
+    if (st != MOE_OK) return st;
+  }
+  return run_layer(desc, &w, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0);
 }
 
 const char *moe_layer_path(const moe_desc *desc, uint32_t T) {

@@ -19,6 +19,12 @@ constexpr int kSmCount = 152;
 constexpr uint32_t kErrBadIndex = 1u;   // expert index outside [0, E)
 constexpr uint32_t kErrBadOffsets = 2u; // off[] not a valid prefix of R rows
 constexpr uint32_t kErrTimeout = 4u;    // a bounded wait gave up
+constexpr uint32_t kErrBadSlot = 8u;    // a selected expert's weight slot outside [0, n_slots)
+
+// the weight slot of routed expert e (moe_weights.expert_slot; identity without one)
+__device__ __forceinline__ int weight_slot(const int32_t *eslot, int e) {
+  return eslot ? __ldg(eslot + e) : e;
+}
 
 // ---------------------------------------------------------------- plan layout
 // int32 array in the workspace describing the active experts of one call.
@@ -272,6 +278,7 @@ struct Ctx {
   moe_weights wts;
   uint32_t T, R;
   uint32_t fmax;
+  uint32_t wexp;  // expert-sized slots in the routed weight planes (E without a slot table)
   uint8_t *ws;
   moe_ws_layout L;
   cudaStream_t stream;
@@ -310,5 +317,10 @@ moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, cons
                               const float *logits, const float *bias, uint32_t T, float *y,
                               void *ws, size_t ws_bytes, void *stream);
 void set_last_error(const char *msg);
+
+// expert cache internals for moe_stream_layer (expert_cache.cu)
+bool cache_layer_routed(const moe_cache *c, uint32_t layer, moe_weights *w);
+const moe_desc *cache_desc(const moe_cache *c);
+int32_t *cache_pinned(moe_cache *c, size_t n);
 
 }  // namespace moe

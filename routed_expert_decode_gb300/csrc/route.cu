@@ -190,7 +190,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     k_plan(const int32_t *__restrict__ off, const int32_t *__restrict__ idx,
            const int32_t *__restrict__ perm, const int32_t *__restrict__ pos, uint32_t T,
            uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int tc_mode,
-           uint32_t tc_min_rows, int *plan, uint32_t *err) {
+           uint32_t tc_min_rows, const int32_t *__restrict__ eslot, uint32_t n_slots,
+           int *plan, uint32_t *err) {
   __shared__ int scan[kPlanThreads];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -237,6 +238,21 @@ __global__ void __launch_bounds__(kPlanThreads)
       P.tc_tile_gu[0] = P.tc_tile_dn[0] = 0;
     }
     return;
+  }
+  // with a slot table, every selected expert's weights must be in a slot
+  if (eslot) {
+    for (uint32_t e = tid; e < E; e += kPlanThreads)
+      if (off[e + 1] > off[e] && (uint32_t)eslot[e] >= n_slots) bad = 3;
+    __syncthreads();
+    if (bad) {
+      if (tid == 0) {
+        atomicOr(err, kErrBadSlot);
+        for (int i = 0; i < 8; ++i) P.hdr[i] = 0;
+        P.item_gu[0] = 0;
+        P.tc_tile_gu[0] = P.tc_tile_dn[0] = 0;
+      }
+      return;
+    }
   }
   auto on_tc = [&](int rows) -> bool {
     if (tc_mode == 0 || rows <= 0) return false;
@@ -406,7 +422,8 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
   if (!(D.flags & MOE_FLAG_FORCE_GEMV) && tc_supported(D))
     tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
   k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, D.n_expert, D.top_k, D.f,
-                                           D.f_shared, D.d, tc_mode, kTcMinRows, plan, err);
+                                           D.f_shared, D.d, tc_mode, kTcMinRows,
+                                           c.wts.expert_slot, c.wexp, plan, err);
   return cudaGetLastError();
 }
 

@@ -56,16 +56,26 @@ class MoeDesc(ctypes.Structure):
 
 
 class MoeWeights(ctypes.Structure):
-    _fields_ = [(n, MoeMat) for n in ("gate", "up", "down", "s_gate", "s_up", "s_down")]
+    _fields_ = [(n, MoeMat) for n in ("gate", "up", "down", "s_gate", "s_up", "s_down")] + \
+        [("expert_slot", _vp), ("n_slots", _u32)]
 
 
 LAYOUT_FIELDS = ("idx", "w", "off", "perm", "pos", "xq", "xs", "hq", "hs", "h", "o", "plan",
-                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "xt", "ht", "rseg", "err",
+                 "sync", "tap_gu", "tap_dn", "trace", "xperm", "xsperm", "hperm", "xt", "ht", "rseg",
+                 "lidx", "lw", "err",
                  "total")
 
 
 class MoeWsLayout(ctypes.Structure):
     _fields_ = [(n, _sz) for n in LAYOUT_FIELDS] + [("n_tap", _u32)]
+
+
+class MoeCacheStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("lookups", "hits", "misses", "prefetch_loads",
+                                               "prefetch_hits", "evictions", "bytes_h2d")]
+
+
+CACHE_POLICY_ONLY = 1
 
 
 class MoeError(RuntimeError):
@@ -119,6 +129,29 @@ def lib():
         L.moe_layer_noalloc.restype = ctypes.c_int
         L.moe_layer_noalloc.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
                                         _vp, _vp, _u32, _vp, _vp]
+        _pc = ctypes.POINTER(ctypes.c_void_p)
+        L.moe_cache_create.restype = ctypes.c_int
+        L.moe_cache_create.argtypes = [ctypes.POINTER(MoeDesc), _u32, ctypes.POINTER(MoeWeights),
+                                       ctypes.POINTER(MoeWeights), _u32, _vp, _u32, _pc]
+        L.moe_cache_destroy.restype = None
+        L.moe_cache_destroy.argtypes = [_vp]
+        L.moe_cache_ensure.restype = ctypes.c_int
+        L.moe_cache_ensure.argtypes = [_vp, _u32, _vp, _u32, _vp]
+        L.moe_cache_prefetch.restype = ctypes.c_int
+        L.moe_cache_prefetch.argtypes = [_vp, _u32, _vp, _u32, _vp]
+        L.moe_cache_plan.restype = ctypes.c_int
+        L.moe_cache_plan.argtypes = [_vp, _u32, _vp, _u32, ctypes.c_int, _vp, _vp, _vp,
+                                     ctypes.POINTER(_u32)]
+        L.moe_cache_slot.restype = ctypes.c_int32
+        L.moe_cache_slot.argtypes = [_vp, _u32, ctypes.c_int32]
+        L.moe_cache_layers.restype = _u32
+        L.moe_cache_layers.argtypes = [_vp]
+        L.moe_cache_get_stats.restype = ctypes.c_int
+        L.moe_cache_get_stats.argtypes = [_vp, ctypes.POINTER(MoeCacheStats)]
+        L.moe_stream_layer.restype = ctypes.c_int
+        L.moe_stream_layer.argtypes = [_vp, _u32, ctypes.POINTER(MoeDesc),
+                                       ctypes.POINTER(MoeWeights), _vp, _vp, _vp, _u32, _vp, _vp,
+                                       _vp, _vp, _sz, _vp, _vp]
         L.moe_check_device_error.restype = ctypes.c_int
         L.moe_check_device_error.argtypes = [_vp, _sz, _vp]
         L.moe_last_error.restype = ctypes.c_char_p
@@ -262,6 +295,107 @@ def layer_noalloc(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, stream
 
 
 NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def _host_ptr(t, name="tensor"):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be host memory")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _i32_host(a):
+    """A host int32 array (numpy or CPU tensor) as (keep-alive object, pointer, n)."""
+    import numpy as np
+
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32).reshape(-1))
+    return arr, arr.ctypes.data, int(arr.size)
+
+
+class ExpertCache:
+    """moe_cache_*: an HBM cache of expert slots over host-resident routed experts.
+
+    ``host_layers``: one MoeWeights per layer whose gate/up/down point at pinned
+    host planes; ``arena``: MoeWeights whose gate/up/down point at device planes
+    of ``n_slots`` experts; ``slot_table``: device int32 [n_layers, E].  With
+    ``policy_only`` the cache does no device work (plan / slot / stats only), and
+    the pointers are not dereferenced."""
+
+    def __init__(self, desc: MoeDesc, host_layers, arena: MoeWeights, n_slots: int,
+                 slot_table_ptr: int, policy_only: bool = False):
+        arr = (MoeWeights * len(host_layers))(*host_layers)
+        h = ctypes.c_void_p()
+        st = lib().moe_cache_create(ctypes.byref(desc), len(host_layers), arr, ctypes.byref(arena),
+                                    n_slots, slot_table_ptr,
+                                    CACHE_POLICY_ONLY if policy_only else 0, ctypes.byref(h))
+        _check("moe_cache_create", st)
+        self._h = h
+        self._keep = (arr, arena)
+        self.n_slots = n_slots
+
+    def close(self):
+        if self._h:
+            lib().moe_cache_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self):
+        return self._h
+
+    def ensure(self, layer: int, experts, stream=None):
+        arr, ptr, n = _i32_host(experts)
+        _check("moe_cache_ensure", lib().moe_cache_ensure(self._h, layer, ptr, n, _stream(stream)))
+
+    def prefetch(self, layer: int, experts, stream=None):
+        arr, ptr, n = _i32_host(experts)
+        _check("moe_cache_prefetch", lib().moe_cache_prefetch(self._h, layer, ptr, n,
+                                                              _stream(stream)))
+
+    def plan(self, layer: int, experts, prefetch: bool = False):
+        """Policy step only: returns [(expert, slot, evicted layer*E+expert or -1)]."""
+        import numpy as np
+
+        arr, ptr, n = _i32_host(experts)
+        m = max(n, 1)
+        loaded = np.zeros(m, np.int32)
+        slots = np.zeros(m, np.int32)
+        evicted = np.zeros(m, np.int64)
+        cnt = _u32(0)
+        _check("moe_cache_plan", lib().moe_cache_plan(
+            self._h, layer, ptr, n, 1 if prefetch else 0, loaded.ctypes.data, slots.ctypes.data,
+            evicted.ctypes.data, ctypes.byref(cnt)))
+        return [(int(loaded[i]), int(slots[i]), int(evicted[i])) for i in range(cnt.value)]
+
+    def slot(self, layer: int, expert: int) -> int:
+        return int(lib().moe_cache_slot(self._h, layer, expert))
+
+    def stats(self) -> dict:
+        out = MoeCacheStats()
+        _check("moe_cache_get_stats", lib().moe_cache_get_stats(self._h, ctypes.byref(out)))
+        return {n: int(getattr(out, n)) for n, _ in MoeCacheStats._fields_}
+
+
+def stream_layer(cache: ExpertCache, layer: int, desc: MoeDesc, shared: MoeWeights, x, logits,
+                 bias, y, ws, next_logits=None, next_bias=None, stream=None,
+                 prefetch_stream=None):
+    """moe_stream_layer: route, make the picks resident in the cache, run the layer
+    on the slot weights; with next_logits, prefetch the next layer's picks."""
+    st = lib().moe_stream_layer(cache.handle, layer, ctypes.byref(desc), ctypes.byref(shared),
+                                _dev_ptr(x, torch.float32, "x"),
+                                _dev_ptr(logits, torch.float32, "logits"),
+                                _dev_ptr(bias, torch.float32, "bias"), x.shape[0],
+                                _dev_ptr(next_logits, torch.float32, "next_logits"),
+                                _dev_ptr(next_bias, torch.float32, "next_bias"),
+                                _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
+                                ws.numel(), _stream(stream), _stream(prefetch_stream))
+    _check("moe_stream_layer", st)
 
 
 def layer_path(desc: MoeDesc, T: int) -> str:

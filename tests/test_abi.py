@@ -54,6 +54,8 @@ int main(void) {
          sizeof(moe_ws_layout));
   printf("%zu %zu %zu\n", offsetof(moe_desc, s), offsetof(moe_desc, flags),
          offsetof(moe_ws_layout, n_tap));
+  printf("%zu %zu %zu\n", sizeof(moe_cache_stats), offsetof(moe_weights, expert_slot),
+         offsetof(moe_weights, n_slots));
   return 0;
 }
 ''')
@@ -65,6 +67,9 @@ int main(void) {
     assert sizes == [ctypes.sizeof(moe.MoeMat), ctypes.sizeof(moe.MoeDesc),
                      ctypes.sizeof(moe.MoeWeights), ctypes.sizeof(moe.MoeWsLayout)]
     assert offs == [moe.MoeDesc.s.offset, moe.MoeDesc.flags.offset, moe.MoeWsLayout.n_tap.offset]
+    cache = [int(v) for v in lines[2].split()]
+    assert cache == [ctypes.sizeof(moe.MoeCacheStats), moe.MoeWeights.expert_slot.offset,
+                     moe.MoeWeights.n_slots.offset]
 
 
 def _desc(moe, **kw):
