@@ -474,6 +474,7 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
                                    for k in ROOFLINE_STAGES if k in stage and b[k] > 0}}
         assert moe.check_device_error(ws) == 0
     out.update(run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak))
+    out.update(run_stream_sweep(torch, moe, synth, dev, layer))
     return out
 
 
@@ -554,6 +555,122 @@ def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
                      "hbm_gbs": round(b / (ms / 1e3) / 1e9, 1),
                      "frac_of_measured": round(b / (ms / 1e3) / 1e9 / peak, 4)}
         assert moe.check_device_error(ws) == 0
+    return out
+
+
+def h2d_peak_gbs(torch, dev, nbytes=1 << 30):
+    """Pinned host -> HBM copy bandwidth (one cudaMemcpyAsync of 1 GiB, best of 5)."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = None
+    for _ in range(6):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        dst.copy_(src, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        best = ms if best is None else min(best, ms)
+    del src, dst
+    return nbytes / (best / 1e3) / 1e9
+
+
+def run_stream_sweep(torch, moe, synth, dev, layer, n_layers=8, n_slots=512, warm=24, timed=40):
+    """Host-tier expert streaming: a decode stack of n_layers layers of the headline
+    shape whose routed experts live in pinned host memory (every layer reuses the
+    headline layer's routed weights: the cache keys (layer, expert) differ, so each
+    miss is a real 40 MB copy), an HBM cache of n_slots expert slots, resident
+    shared experts.  Per token and layer: router GEMM on rmsnorm(x) plus the
+    layer's popularity offset -> moe_stream_layer -> x += y.  With lookahead the
+    next layer's router also runs on this layer's input and its picks are
+    prefetched on a side stream.  Cold cache, `warm` tokens, then `timed` tokens
+    timed with CUDA events; weights far exceed L2 (no flush needed)."""
+    import dataclasses
+    import numpy as np
+
+    spec = synth.GLM_LAYER
+    out = {}
+    t = layer.tensors
+    host_t = {}
+    for n in ("gate", "up", "down"):
+        for sfx in ("_q", "_s"):
+            host_t[n + sfx] = t[n + sfx].cpu().pin_memory()
+    host_w = moe.MoeWeights()
+    for n in ("gate", "up", "down"):
+        setattr(host_w, n, moe.MoeMat(host_t[n + "_q"].data_ptr(), host_t[n + "_s"].data_ptr()))
+    arena_t = {k: torch.empty((n_slots,) + tuple(v.shape[1:]), dtype=v.dtype, device=dev)
+               for k, v in host_t.items()}
+    arena = moe.MoeWeights()
+    for n in ("gate", "up", "down"):
+        setattr(arena, n, moe.MoeMat(arena_t[n + "_q"].data_ptr(), arena_t[n + "_s"].data_ptr()))
+    shared = moe.MoeWeights()
+    for n in ("s_gate", "s_up", "s_down"):
+        setattr(shared, n, getattr(layer.weights, n))
+    desc = layer.desc()
+    specs = [dataclasses.replace(spec, layer_seed=1000 + l) for l in range(n_layers)]
+    w_r = [torch.from_numpy(synth.router_weights(s)).to(dev) for s in specs]
+    offs = [torch.from_numpy(synth.zipf_offset(s.layer_seed, synth.STREAM_ZIPF, s.E,
+                                               s.zipf_beta)).to(dev) for s in specs]
+    bias = [torch.from_numpy(synth.bias(s)).to(dev) for s in specs]
+    ws = torch.zeros(moe.workspace_size(desc, 1), dtype=torch.uint8, device=dev)
+    peak = h2d_peak_gbs(torch, dev)
+    expert_bytes = spec.f * spec.d * 2 * 1.0625 + spec.d * spec.f * 1.0625
+    side = torch.cuda.Stream(dev)
+
+    def logits_of(l, xn):
+        lg = torch.empty((1, spec.E), dtype=torch.float32, device=dev)
+        moe.router_logits(desc, w_r[l], xn, lg)
+        return lg + offs[l]
+
+    for lookahead in (False, True):
+        table = torch.full((n_layers, spec.E), -1, dtype=torch.int32, device=dev)
+        cache = moe.ExpertCache(desc, [host_w] * n_layers, arena, n_slots, table.data_ptr())
+        evs = []
+        y = torch.empty((1, spec.d), dtype=torch.float32, device=dev)
+        for tok in range(warm + timed):
+            if tok == warm:
+                torch.cuda.synchronize()
+                s0 = cache.stats()
+            _, x0 = synth.token_inputs(spec, 7000 + tok, 1)
+            x = torch.from_numpy(x0).to(dev)
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            for l in range(n_layers):
+                xn = x * torch.rsqrt((x * x).mean(dim=1, keepdim=True) + 1e-6)
+                lg = logits_of(l, xn)
+                nl = logits_of(l + 1, xn) if lookahead and l + 1 < n_layers else None
+                moe.stream_layer(cache, l, desc, shared, xn, lg, bias[l], y, ws, next_logits=nl,
+                                 next_bias=bias[l + 1] if nl is not None else None,
+                                 prefetch_stream=side)
+                x = x + y
+            b.record()
+            if tok >= warm:
+                evs.append((a, b))
+        torch.cuda.synchronize()
+        assert moe.check_device_error(ws) == 0
+        s1 = cache.stats()
+        cache.close()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+        d = {k: s1[k] - s0[k] for k in s1}
+        link = d["bytes_h2d"] / timed
+        name = "stream_decode_t1" + ("_lookahead" if lookahead else "")
+        out[name] = {
+            "layers": n_layers, "cache_slots": n_slots,
+            "cache_fraction": round(n_slots / (n_layers * spec.E), 4),
+            "ms_per_token": round(ms, 4), "tokens_per_s": round(1e3 / ms, 2),
+            "hit_rate": round(d["hits"] / max(d["lookups"], 1), 4),
+            "misses_per_token": round(d["misses"] / timed, 2),
+            "prefetch_loads_per_token": round(d["prefetch_loads"] / timed, 2),
+            "prefetch_hit_rate": round(d["prefetch_hits"] / max(d["prefetch_loads"], 1), 4),
+            "h2d_bytes_per_token": int(link),
+            "h2d_gbs": round(link / (ms / 1e3) / 1e9, 1),
+            "h2d_peak_gbs": round(peak, 1),
+            "h2d_frac_of_measured": round(link / (ms / 1e3) / 1e9 / peak, 4),
+            "hbm_bytes_per_token": int(n_layers * 9 * expert_bytes),
+        }
+    del arena_t, host_t
+    torch.cuda.empty_cache()
     return out
 
 
