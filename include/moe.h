@@ -277,9 +277,10 @@ const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i);
  * (their layer may still be running).  A call whose union exceeds what it may
  * evict fails with MOE_ERR_WORKSPACE before copying anything.
  * Ordering: ensure copies on its stream (the compute stream), so they follow
- * every kernel enqueued there before; prefetch copies on its own stream wait for
- * the compute work enqueued before the latest ensure, and an ensure that needs a
- * prefetched expert makes its stream wait for that copy. */
+ * every kernel enqueued there before; prefetch copies on their own stream start
+ * after the latest ensure's copies (which go first on the link, and follow every
+ * earlier use of an evicted slot), and an ensure that needs a prefetched expert
+ * makes its stream wait for that copy. */
 typedef struct moe_cache moe_cache;
 
 typedef struct {

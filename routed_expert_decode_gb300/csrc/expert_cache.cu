@@ -38,7 +38,7 @@ struct moe_cache {
   std::vector<cudaEvent_t> ready;  // [S]: recorded after a prefetch's copies into the slot
   std::vector<uint8_t> busy;       // [L*E]: named by the latest ensure
   std::vector<int64_t> busy_list;
-  cudaEvent_t before_latest = nullptr;  // compute stream, before the latest ensure's copies
+  cudaEvent_t after_latest = nullptr;  // compute stream, after the latest ensure's copies
   bool have_latest = false;
   uint64_t stamp = 0;
   moe_cache_stats st;
@@ -278,7 +278,7 @@ moe_status moe_cache_create(const moe_desc *desc, uint32_t n_layers,
   memset(&c->st, 0, sizeof c->st);
   if (!(flags & MOE_CACHE_POLICY_ONLY)) {
     c->ready.assign(n_slots, nullptr);
-    bool ok = cudaEventCreateWithFlags(&c->before_latest, cudaEventDisableTiming) == cudaSuccess;
+    bool ok = cudaEventCreateWithFlags(&c->after_latest, cudaEventDisableTiming) == cudaSuccess;
     for (uint32_t s = 0; s < n_slots && ok; ++s)
       ok = cudaEventCreateWithFlags(&c->ready[s], cudaEventDisableTiming) == cudaSuccess;
     if (!ok) {
@@ -295,7 +295,7 @@ void moe_cache_destroy(moe_cache *c) {
   if (!c) return;
   for (cudaEvent_t ev : c->ready)
     if (ev) cudaEventDestroy(ev);
-  if (c->before_latest) cudaEventDestroy(c->before_latest);
+  if (c->after_latest) cudaEventDestroy(c->after_latest);
   if (c->pinned) cudaFreeHost(c->pinned);
   delete c;
 }
@@ -326,8 +326,7 @@ moe_status moe_cache_ensure(moe_cache *c, uint32_t layer, const int32_t *experts
   std::vector<int32_t> wait_slots;
   moe_status s = decide(*c, layer, experts, n, false, &loads, &wait_slots);
   if (s != MOE_OK) return s;
-  cudaError_t e = cudaEventRecord(c->before_latest, st);
-  c->have_latest = e == cudaSuccess;
+  cudaError_t e = cudaSuccess;
   // hits still arriving by a prefetch, and slots a prefetch may still be writing
   for (int32_t slot : wait_slots)
     if (e == cudaSuccess) {
@@ -342,6 +341,10 @@ moe_status moe_cache_ensure(moe_cache *c, uint32_t layer, const int32_t *experts
     if (e == cudaSuccess) e = copy_expert(*c, layer, ld.expert, ld.slot, st);
   }
   if (e == cudaSuccess) e = upload_table(*c, layer, st);
+  // later prefetches start after these copies: the layer's own misses get the
+  // link first, and every compute use of a slot enqueued before is behind them
+  if (e == cudaSuccess) e = cudaEventRecord(c->after_latest, st);
+  c->have_latest = e == cudaSuccess;
   if (e != cudaSuccess) {
     set_last_error(cudaGetErrorName(e));
     return MOE_ERR_CUDA;
@@ -358,11 +361,9 @@ moe_status moe_cache_prefetch(moe_cache *c, uint32_t layer, const int32_t *exper
   moe_status s = decide(*c, layer, experts, n, true, &loads, nullptr);
   if (s != MOE_OK) return s;
   cudaError_t e = cudaSuccess;
-  // an evicted expert's slot may be read by compute work enqueued before the
-  // latest ensure: wait for that point first
-  bool evicts = false;
-  for (const Load &ld : loads) evicts |= ld.evicted >= 0;
-  if (evicts && c->have_latest) e = cudaStreamWaitEvent(st, c->before_latest, 0);
+  // start after the latest ensure's copies: its misses go first on the link, and
+  // an evicted expert's slot is no longer read by compute work enqueued before it
+  if (!loads.empty() && c->have_latest) e = cudaStreamWaitEvent(st, c->after_latest, 0);
   for (const Load &ld : loads) {
     if (e == cudaSuccess && c->pending[ld.slot]) e = cudaStreamWaitEvent(st, c->ready[ld.slot], 0);
     if (e == cudaSuccess) e = copy_expert(*c, layer, ld.expert, ld.slot, st);
