@@ -589,11 +589,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         for (int mi = 0; mi < MAT; ++mi) {
           const uint4 *src = (const uint4 *)(st + 2 * kA16 + kB16 + mi * kA8 + r * kBK);
           uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
-          // rows are 64 B apart, so lanes r and r+2 share banks: each row starts
-          // at a different chunk (rotation by r/2) to keep the loads conflict-free
+          // Chunk order per row pair s = (r/2)%4: q = qq ^ g(s), g = (0, 2, 3, 1).
+          // Loads: the staging rows are 64 B apart, so in a quarter-warp (rows
+          // r..r+7) even rows use 16-byte bank groups q and odd rows 4 + q:
+          // distinct because g is a permutation.  Stores: chunk 2q (2q+1) lands
+          // at position 2q ^ (r&7) of its 128-byte swizzled row, i.e. 2(q ^ s)
+          // (+1): distinct because s -> g(s) ^ s is a permutation too.  Both are
+          // conflict-free.
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {  // 16 int8 -> two 16-byte fp16 chunks
-            const int q = (qq + (r >> 1)) & 3;
+            const int q = qq ^ (int)((0x78u >> (2 * ((r >> 1) & 3))) & 3u);
             const uint4 w = src[q];
             uint4 c0, c1;
             i8x4_to_h2x2(w.x, c0.x, c0.y);
