@@ -58,6 +58,21 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
+def max_over_ranks(torch, dist, value: float, device) -> float:
+    """MAX of a per-rank float over the process group (the value itself on one
+    rank): the job's time is its slowest replica's."""
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_rank: float, world: int, max_ms: float) -> float:
+    """Whole-job units per second: every rank's units over the slowest rank's time."""
+    return units_per_rank * world / (max_ms / 1e3)
+
+
 def rank_seeds(seeds, rank: int):
     """Token seeds of one replica: rank 0 keeps the workload's seeds, rank r
     shifts them by 1000*r so that replicas decode different tokens."""
@@ -315,14 +330,10 @@ def run_ours(args):
                 for j, n in enumerate(names)}
     if nst == 1:  # a single kernel: its duration is the timed step
         stage_ms = {names[0]: list(step_ms)}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(torch, dist, sum(step_ms), dev)
     ms_per_step = total_ms / K
     tokens = T * K * world
-    value = tokens / (total_ms / 1e3)
+    value = job_throughput(T * K, world, total_ms)
 
     # roofline of the dominant kernel
     peak, peak_src = load_peaks()
@@ -355,12 +366,8 @@ def run_ours(args):
             if i >= 0:
                 e1[i].record()
         torch.cuda.synchronize()
-        e2e_ms = sum(e0[i].elapsed_time(e1[i]) for i in range(K))
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": round(tokens / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+        e2e_ms = max_over_ranks(torch, dist, sum(e0[i].elapsed_time(e1[i]) for i in range(K)), dev)
+        e2e = {"value": round(job_throughput(T * K, world, e2e_ms), 2), "unit": "tokens/s",
                "h2d_bytes_per_step": T * spec.d * 4 + T * spec.E * 4,
                "d2h_bytes_per_step": T * spec.d * 4}
     assert moe.check_device_error(ws) == 0
