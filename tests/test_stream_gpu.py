@@ -180,3 +180,46 @@ def test_streamed_layers_match_resident(gpu, lookahead):
     if lookahead:
         assert stats["prefetch_loads"] > 0 and stats["prefetch_hits"] > 0
     st.cache.close()
+
+
+def test_streamed_full_size_decode_matches_resident(gpu):
+    """The full-size layer (E=256, top-8, d=6144, f=2048, shared 2048, Q8_0)
+    streamed from pinned host memory through an 18-slot cache, two layers
+    sharing the routed bytes as in the bench's stack, one token per call, with
+    the lookahead prefetch: bit-identical to the same layer resident in HBM."""
+    spec = synth.GLM_LAYER
+    layer = device_layer(spec, gpu)
+    host_t = {n + sfx: layer.tensors[n + sfx].cpu().pin_memory()
+              for n in ROUTED for sfx in ("_q", "_s")}
+    host_w = _mats(host_t, ROUTED)
+    n_slots = 18
+    arena_t = {k: torch.zeros((n_slots,) + tuple(v.shape[1:]), dtype=v.dtype, device=gpu)
+               for k, v in host_t.items()}
+    arena = _mats(arena_t, ROUTED)
+    table = torch.full((2, spec.E), -1, dtype=torch.int32, device=gpu)
+    desc = layer.desc()
+    cache = moe.ExpertCache(desc, [host_w, host_w], arena, n_slots, table.data_ptr())
+    shared = moe.MoeWeights()
+    for n in ("s_gate", "s_up", "s_down"):
+        setattr(shared, n, getattr(layer.weights, n))
+    bias = torch.from_numpy(synth.bias(spec)).to(gpu)
+    ws = torch.zeros(moe.workspace_size(desc, 1), dtype=torch.uint8, device=gpu)
+    ws_ref = torch.zeros_like(ws)
+    side = torch.cuda.Stream(gpu)
+    for tok in range(3):
+        ins = [synth.token_inputs(spec, 300 + tok + 100 * l, 1) for l in range(2)]
+        lg = [torch.from_numpy(i[0]).to(gpu) for i in ins]
+        xs = [torch.from_numpy(i[1]).to(gpu) for i in ins]
+        for l in range(2):
+            y = torch.empty((1, spec.d), dtype=torch.float32, device=gpu)
+            y_ref = torch.empty_like(y)
+            moe.stream_layer(cache, l, desc, shared, xs[l], lg[l], bias, y, ws,
+                             next_logits=lg[1] if l == 0 else None,
+                             next_bias=bias if l == 0 else None, prefetch_stream=side)
+            moe.layer(desc, layer.weights, xs[l], lg[l], bias, y_ref, ws_ref)
+            torch.cuda.synchronize()
+            assert moe.check_device_error(ws) == 0
+            assert torch.equal(y, y_ref), f"token {tok} layer {l}"
+    st = cache.stats()
+    assert st["misses"] > 0 and st["lookups"] == st["hits"] + st["misses"]
+    cache.close()
