@@ -140,8 +140,10 @@ typedef struct {
 /* The first MOE_WS_FIXED_BYTES of every workspace have a fixed layout: the
  * device error word at offset 0 and, from offset 256, MOE_SYNC_BYTES of
  * counters used by the fused decode kernel.  A workspace must be zero-filled
- * once after it is allocated; every call leaves the counters zeroed again, so
- * one workspace can serve calls of any desc and T. */
+ * once after it is allocated; every call leaves the counters ready for the next
+ * (most zeroed again, two counting calls), so one workspace can serve calls of
+ * any desc and T.  After a call that reported MOE_ERR_TIMEOUT, zero-fill the
+ * first MOE_WS_FIXED_BYTES again before reusing the workspace. */
 #define MOE_SYNC_BYTES ((size_t)16384)
 #define MOE_WS_FIXED_BYTES ((size_t)256 + MOE_SYNC_BYTES)
 

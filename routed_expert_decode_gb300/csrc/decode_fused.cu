@@ -168,15 +168,17 @@ struct FusedArgs {
 // no per-call memset is needed (a workspace must be zero-filled once after it
 // is allocated).  diag[] keeps the first timeout's site for the host.
 struct SyncView {
-  uint32_t *queue, *diag, *ready, *fin, *done;
-  uint32_t n_clear;  // words from queue up to and including done (diag words are kept)
+  uint32_t *queue, *diag, *ready, *fin, *gen;
+  uint32_t n_clear;  // words from queue through ready[] (diag words are kept)
   __device__ SyncView(uint32_t *base, uint32_t E) {
     queue = base;      // [0]; [1]: CTAs whose router partial sums are written
     diag = base + 2;   // [2], [3]
     ready = base + 4;  // [E+1] gate/up items finished per expert
-    fin = ready + E + 1;  // CTAs whose expert outputs o are all written
-    done = fin + 1;       // CTAs that finished the combine
-    n_clear = 4 + E + 1 + 2;
+    // the two counters that carry over between calls sit at the end of the area,
+    // clear of ready[] for any E, so calls of different E may share a workspace
+    fin = base + kSyncInts - 2;  // CTAs whose expert outputs o are written, counting up
+    gen = base + kSyncInts - 1;  // calls completed: this call's fin target is (gen+1)*grid
+    n_clear = 4 + E + 1;
   }
 };
 
@@ -184,7 +186,7 @@ struct SyncView {
 // h rows of one gate/up item are written.
 struct SharedCtl {
   int abort;          // a wait gave up: stop issuing, skip the combine
-  int exit_last;      // this CTA is the last one out (zeroes the counters)
+  uint32_t gen;       // SyncView::gen at the call's start
   int writers_done;   // consumer warps + producer that will post no more events
   int item_cnt[kPartBufs];  // consumer warps done with an item, by b_items % kPartBufs
   int pub_head;       // events reserved
@@ -290,12 +292,6 @@ __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-__device__ __forceinline__ uint32_t atom_acq_rel_add(uint32_t *p, uint32_t v) {
-  uint32_t old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
 
 // a bounded wait gave up: flag the error word (kErrTimeout plus the wait site in
 // bits 8..15) and keep the first site / CTA / detail in sync[2], sync[3]
@@ -637,7 +633,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     }
     mbar_init(route_bar, 1);
     mbar_init(go_bar, 1);
-    ctl.abort = ctl.exit_last = ctl.writers_done = 0;
+    ctl.abort = ctl.writers_done = 0;
+    ctl.gen = __ldcg(SV.gen);  // every CTA reads it before any can pass the exit barrier
     for (int i = 0; i < kPartBufs; ++i) ctl.item_cnt[i] = 0;
     ctl.pub_head = ctl.pub_tail = 0;
     for (int i = 0; i < kPubCap; ++i) ctl.pub_seq[i] = 0;
@@ -1247,9 +1244,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   __syncthreads();
   if (tid == 0) {
     red_release_add(SV.fin, 1u);  // this CTA's o stores, ordered by the barrier
+    const uint32_t base = ctl.gen * gridDim.x;  // fin before this call (mod 2^32)
     const long long t0 = clock64();
     for (int i = 0;; ++i) {
-      const uint32_t n = ld_acquire(SV.fin);
+      const uint32_t n = ld_acquire(SV.fin) - base;
       if (n >= gridDim.x) break;
       if (i >= kSpinIters || clock64() - t0 > a.wait_cycles) {
         report_timeout(a, 0, n);
@@ -1281,14 +1279,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     }
   }
   if (tr && tid == 0) tr[kTrCombine] += clock64() - t_comb;
-  __syncthreads();
-  // the last CTA out zeroes the counters for the next call (every CTA has
-  // passed the barrier above before it counts itself out here)
-  if (tid == 0) ctl.exit_last = atom_acq_rel_add(SV.done, 1u) + 1 == gridDim.x;
-  __syncthreads();
-  if (*(volatile int *)&ctl.exit_last) {
+  // Every CTA has passed the barrier above, so no CTA uses the queue, router
+  // and readiness counters any more: CTA 0 zeroes them for the next call and
+  // counts the call (fin is not cleared: it counts up, and the next call's
+  // target follows from gen), with no atomic round trip at any CTA's exit.
+  if (blockIdx.x == 0) {
     for (uint32_t i = tid; i < SV.n_clear; i += kThreads)
       if (i != 2 && i != 3) a.sync[i] = 0u;
+    if (tid == 0) *(volatile uint32_t *)SV.gen = ctl.gen + 1u;
   }
   if (tr && tid == 0) tr[kTrExit] = global_ns();
 }
@@ -1324,7 +1322,7 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   if (c_rows == 0) return false;
   if (c_rows > d) c_rows = d;
   const uint32_t n_chunks = (d + c_rows - 1) / c_rows;
-  if (4 + D.n_expert + 1 + 2 > kSyncInts) return false;
+  if (4 + D.n_expert + 1 + 2 > kSyncInts) return false;  // ready[E+1] clear of fin, gen
   const size_t stage = (b_bytes + 127) / 128 * 128;
   size_t part = (size_t)kPartBufs * kBItemFeat * kKSplit * kMaxT * 2 * 4;
   const size_t scores = 2 * (size_t)c.T * D.n_expert * 4;

@@ -328,3 +328,32 @@ def test_prefill_tensor_core_dispatch(gpu):
     layer = device_layer(synth.GLM_LAYER, gpu)
     print("prefill_t512 dispatch", run_case(synth.GLM_LAYER, 512, seed=1, device=gpu,
                                             sample=[3, 200, 509]))
+
+
+def test_fused_workspace_shared_across_descs_and_calls(gpu):
+    """One workspace serves fused calls of different E in any order: the counters
+    the kernel carries between calls (a call-counting barrier) never overlap
+    another call's readiness counters, so every result equals the one on a fresh
+    workspace."""
+    from routed_expert_decode_gb300 import moe
+
+    specs = [_spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4),
+             _spec(E=16, k=4, d=256, f=256, f_shared=0)]
+    layers = [device_layer(s, gpu) for s in specs[:1]]
+    ws = torch.zeros(1 << 24, dtype=torch.uint8, device=gpu)
+    order = [0, 1, 0, 0, 1, 1, 0]
+    for call, i in enumerate(order):
+        spec = specs[i]
+        layer = device_layer(spec, gpu)  # one resident layer at a time
+        assert moe.layer_path(layer.desc(), 1) == "fused_decode"
+        logits, x = synth.token_inputs(spec, 40 + call, 1)
+        args = [torch.from_numpy(a).to(gpu) for a in (x, logits, synth.bias(spec))]
+        y = torch.empty((1, spec.d), dtype=torch.float32, device=gpu)
+        y_ref = torch.empty_like(y)
+        moe.layer(layer.desc(), layer.weights, *args, y, ws)
+        fresh = torch.zeros(moe.workspace_size(layer.desc(), 1), dtype=torch.uint8, device=gpu)
+        moe.layer(layer.desc(), layer.weights, *args, y_ref, fresh)
+        torch.cuda.synchronize()
+        assert moe.check_device_error(ws) == 0
+        assert torch.equal(y, y_ref), f"call {call} (E={spec.E})"
+    del layers
