@@ -94,11 +94,24 @@ def row_bytes(fmt: int, K: int) -> int:
     return (K if fmt == 0 else K // 4) + (K // 32) * 2
 
 
-def stage_bytes(spec, T: int, counts, tc_rows=None):
+def tc_tiles(spec, T: int, counts, tc_rows) -> int:
+    """Gate/up tiles (128 features x 64 rows) the row rule sends to the tensor
+    cores: routed experts with more than tc_rows rows, and the shared expert when
+    its width equals f."""
+    n = sum((spec.f // 128) * ((int(c) + 63) // 64) for c in counts if int(c) > tc_rows)
+    if spec.f_shared and spec.f_shared == spec.f and T > tc_rows:
+        n += (spec.f_shared // 128) * ((T + 63) // 64)
+    return n
+
+
+def stage_bytes(spec, T: int, counts, tc_rows=None, sm_count=None):
     """Algorithmic HBM bytes per stage: each selected expert's weights and the
     shared expert's, read once.  counts: rows per routed expert; experts with
     more than tc_rows rows (None: no tensor path) are charged to the
-    tensor-core stages."""
+    tensor-core stages -- unless their gate/up tiles number fewer than sm_count,
+    when the library runs every expert on the GEMV."""
+    if tc_rows is not None and sm_count is not None and tc_tiles(spec, T, counts, tc_rows) < sm_count:
+        tc_rows = None
     out = {"gateup": 0, "down": 0, "gateup_tc": 0, "down_tc": 0}
 
     def add(rows, fmt, f):
@@ -337,7 +350,8 @@ def run_ours(args):
 
     # roofline of the dominant kernel
     peak, peak_src = load_peaks()
-    bytes_steps = [stage_bytes(spec, T, counts_of[s], tc_rows) for s in step_seed]
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    bytes_steps = [stage_bytes(spec, T, counts_of[s], tc_rows, sms) for s in step_seed]
     mean_stage = {n: statistics.mean(v) for n, v in stage_ms.items()}
     dom = max(mean_stage, key=mean_stage.get)
     dom_bytes = sum(b.get(dom, 0) for b in bytes_steps) / K
@@ -469,7 +483,8 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
         lay_off = lay.views(ws, T)["off"].cpu()
         counts = (lay_off[1:] - lay_off[:-1]).tolist()
         U = sum(1 for c in counts if c > 0)
-        b = stage_bytes(spec, T, counts, moe.tc_min_rows(desc, T))
+        b = stage_bytes(spec, T, counts, moe.tc_min_rows(desc, T),
+                        torch.cuda.get_device_properties(dev).multi_processor_count)
         ms = statistics.mean(step)
         out[name] = {"T": T, "unique_experts": U, "ms_per_step": round(ms, 4),
                      "tokens_per_s": round(T / (ms / 1e3), 1),

@@ -247,9 +247,13 @@ moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);
 
 /* Row threshold of the tensor-core path of moe_layer for (desc, T) on the
- * current device: an expert (the shared expert included, with T rows) whose
- * routed row count exceeds it runs its block dots on tcgen05 tensor cores,
- * the rest on the dp4a GEMV.  -1 when no expert of such a call can take the
+ * current device: an expert (the shared expert included, with T rows, when
+ * f_shared == f) whose routed row count exceeds it runs its block dots on
+ * tcgen05 tensor cores, the rest on the dp4a GEMV -- provided those experts'
+ * gate/up tiles (128 features x 64 rows each) number at least the device's SM
+ * count; with fewer, every expert of the call runs on the GEMV (a nearly empty
+ * tensor kernel would leave most SMs idle).  MOE_FLAG_FORCE_TC sends every
+ * expert to the tensor cores.  -1 when no expert of such a call can take the
  * tensor path (the fused decode path, 2-bit routed weights, dims not a
  * multiple of 256, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
 int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);

@@ -424,6 +424,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t NS = a.n_stages;
   PlanView P(const_cast<int *>(a.plan), a.E);
   const int total = MAT == 2 ? P.hdr[6] : P.hdr[7];
+  if (total == 0) return;  // no tensor-core tiles in this call's plan
   const uint32_t KS = a.K / kBK;  // stages per tile
   // stage layout: [A16 mat0 16K][A16 mat1 16K][B 8K][A8 mat0 8K][A8 mat1 8K]
   constexpr uint32_t kA16 = kBM * kBK * 2, kB16 = kBN * kBK * 2, kA8 = kBM * kBK;
@@ -666,10 +667,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// activations for the tensor path: fp16 copy of x codes in slot order
+// activations for the tensor path: fp16 copy of x codes in slot order (nothing
+// when the plan sends no expert to the tensor cores)
 __global__ void __launch_bounds__(256)
     k_perm_x(const int8_t *__restrict__ xq, const int32_t *__restrict__ perm, uint32_t R,
-             uint32_t slots, uint32_t k, uint32_t d, __half *__restrict__ xperm) {
+             uint32_t slots, uint32_t k, uint32_t d, const int *plan, uint32_t E,
+             __half *__restrict__ xperm) {
+  if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element chunks
   const uint64_t chunks = (uint64_t)slots * (d / 8);
   if (i >= chunks) return;
@@ -685,7 +689,9 @@ __global__ void __launch_bounds__(256)
 // activation scales in slot order
 __global__ void __launch_bounds__(256)
     k_perm_xs(const float *__restrict__ xs, const int32_t *__restrict__ perm, uint32_t R,
-              uint32_t slots, uint32_t k, uint32_t nb, float *__restrict__ xsperm) {
+              uint32_t slots, uint32_t k, uint32_t nb, const int *plan, uint32_t E,
+              float *__restrict__ xsperm) {
+  if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)slots * nb) return;
   const uint32_t slot = (uint32_t)(i / nb), b = (uint32_t)(i % nb);
@@ -760,11 +766,11 @@ cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm) {
   if (n1 == 0) return cudaSuccess;
   k_perm_x<<<(unsigned)((n1 + 255) / 256), 256, 0, c.stream>>>(
       (const int8_t *)(c.ws + c.L.xq), perm, c.R, slots, c.desc.top_k, c.desc.d,
-      (__half *)(c.ws + c.L.xperm));
+      (const int *)(c.ws + c.L.plan), c.desc.n_expert, (__half *)(c.ws + c.L.xperm));
   const uint64_t n2 = (uint64_t)slots * (c.desc.d / 32);
   k_perm_xs<<<(unsigned)((n2 + 255) / 256), 256, 0, c.stream>>>(
       (const float *)(c.ws + c.L.xs), perm, c.R, slots, c.desc.top_k, c.desc.d / 32,
-      (float *)(c.ws + c.L.xsperm));
+      (const int *)(c.ws + c.L.plan), c.desc.n_expert, (float *)(c.ws + c.L.xsperm));
   return cudaGetLastError();
 }
 

@@ -185,13 +185,16 @@ __device__ int block_excl_scan(int v, int *scan, int *total) {
 // another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
 // no work (so no kernel indexes with untrusted values).  Otherwise it lists the
 // active experts, ascending, the shared expert last, split between the dp4a
-// path and the tensor-core path (rows > tc_min_rows; every row with force_tc).
+// path and the tensor-core path: experts with more than tc_min_rows rows, when
+// their gate/up tiles number at least tc_min_tiles (one per SM: fewer would
+// leave most SMs idle while the GEMV kernels wait behind the tensor kernel),
+// else none; every row with force_tc.
 __global__ void __launch_bounds__(kPlanThreads)
     k_plan(const int32_t *__restrict__ off, const int32_t *__restrict__ idx,
            const int32_t *__restrict__ perm, const int32_t *__restrict__ pos, uint32_t T,
            uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int tc_mode,
-           uint32_t tc_min_rows, const int32_t *__restrict__ eslot, uint32_t n_slots,
-           int *plan, uint32_t *err) {
+           uint32_t tc_min_rows, uint32_t tc_min_tiles, const int32_t *__restrict__ eslot,
+           uint32_t n_slots, int *plan, uint32_t *err) {
   __shared__ int scan[kPlanThreads];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -253,6 +256,25 @@ __global__ void __launch_bounds__(kPlanThreads)
       }
       return;
     }
+  }
+  if (tc_mode == 1) {
+    // gate/up tiles the row rule would send to the tensor cores
+    __shared__ int tc_tiles;
+    if (tid == 0) {
+      tc_tiles = 0;
+      if (fs > 0 && fs == f && T > tc_min_rows)
+        tc_tiles = (int)(fs / kTcTileM) * (int)((T + kTcTileN - 1) / kTcTileN);
+    }
+    __syncthreads();
+    int mine = 0;
+    for (uint32_t e = tid; e < E; e += kPlanThreads) {
+      const int rows = off[e + 1] - off[e];
+      if (rows > (int)tc_min_rows)
+        mine += (int)(f / kTcTileM) * ((rows + (int)kTcTileN - 1) / (int)kTcTileN);
+    }
+    if (mine) atomicAdd(&tc_tiles, mine);
+    __syncthreads();
+    if ((uint32_t)tc_tiles < tc_min_tiles) tc_mode = 0;
   }
   auto on_tc = [&](int rows) -> bool {
     if (tc_mode == 0 || rows <= 0) return false;
@@ -423,7 +445,8 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
     tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
   k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, D.n_expert, D.top_k, D.f,
                                            D.f_shared, D.d, tc_mode, kTcMinRows,
-                                           c.wts.expert_slot, c.wexp, plan, err);
+                                           (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
+                                           plan, err);
   return cudaGetLastError();
 }
 

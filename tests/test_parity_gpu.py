@@ -357,3 +357,32 @@ def test_fused_workspace_shared_across_descs_and_calls(gpu):
         assert moe.check_device_error(ws) == 0
         assert torch.equal(y, y_ref), f"call {call} (E={spec.E})"
     del layers
+
+
+@pytest.mark.parametrize("T", [8, 16, 64])
+def test_tensor_core_dispatch_needs_a_tile_per_sm(gpu, T):
+    """Auto dispatch on the full layer: the tensor-core path is taken only when
+    the experts above the row threshold bring at least one gate/up tile per SM
+    (else every expert runs on the GEMV); the plan's tensor-expert count agrees
+    with the rule restated on the host, and the output matches the oracle."""
+    import os
+    import sys
+
+    from routed_expert_decode_gb300 import moe
+
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+
+    spec = synth.GLM_LAYER
+    layer = device_layer(spec, gpu)
+    rep = run_case(spec, T, seed=2, device=gpu, sample=[0, T - 1], check_taps=False)
+    ws = layer.workspace(T, 0)
+    L = moe.workspace_layout(layer.desc(), T)
+    hdr = ws[L.plan:L.plan + 32].view(torch.int32).cpu().tolist()
+    off = layer.views(ws, T)["off"].cpu().numpy()
+    counts = (off[1:] - off[:-1]).tolist()
+    sms = torch.cuda.get_device_properties(gpu).multi_processor_count
+    thr = moe.tc_min_rows(layer.desc(), T)
+    want_tc = thr is not None and thr >= 0 and bench.tc_tiles(spec, T, counts, thr) >= sms
+    assert (hdr[5] > 0) == want_tc, (T, hdr[5], bench.tc_tiles(spec, T, counts, thr), sms)
+    print("dispatch", T, hdr[5], rep)
