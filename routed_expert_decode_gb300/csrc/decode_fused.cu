@@ -39,8 +39,8 @@ constexpr int kConsumerWarps = 16;
 constexpr int kProducerWarp = kConsumerWarps;       // lane 0 issues the weight copies
 constexpr int kPublisherWarp = kConsumerWarps + 1;  // lane 0 does the gpu-scope atomics
 constexpr int kThreads = (kConsumerWarps + 2) * 32;
-constexpr int kPubCap = 64;
-constexpr int kRouteWarp0 = 1;   // first routing warp (not on the producer's SM sub-partition)      // events in flight from the CTA's warps to its publisher
+constexpr int kPubCap = 64;      // events in flight from the CTA's warps to its publisher
+constexpr int kRouteWarp0 = 1;   // first routing warp (not on the producer's SM sub-partition)
 constexpr int kMaxT = 2;
 constexpr int kMaxR = 64;        // routed rows (T * top_k)
 constexpr int kBFeat = 8;        // features per gate/up stage
@@ -64,10 +64,6 @@ constexpr int kPartBufs = 3;
 static_assert(kMaxStages <= (kPartBufs - 1) * (kBItemFeat / kBFeat),
               "the stage ring could let a warp reach an item whose buffer is still read");
 constexpr uint32_t kSyncInts = MOE_SYNC_BYTES / 4;
-// true: the two lanes of a 32-block add their int32 half sums (one shuffle)
-// before the block's scale is applied; false: each lane scales its exact
-// half-block sum itself (a different fp32 summation order of the same terms)
-constexpr bool kPairShuffle = false;
 constexpr int kSpinIters = 1 << 26;                // iteration cap of every wait
 constexpr int kSuspendNs = 20000;                  // mbarrier try_wait suspend-time hint
 constexpr long long kWaitCycles = 4000000000ll;     // ~2 s at 2 GHz: a wait gives up after this
@@ -1007,8 +1003,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
       const int tok0 = dsc.tok[0], tok1 = dsc.tok[kMaxT - 1];
       if (dsc.kind == kKindB) {
         // ---- gate/up: kKSplit warps split feature first+f over K.  Lane l reads
-        // 16 contiguous bytes (conflict-free); lanes l and l^1 form one 32-block
-        // whose exact int32 sum is completed with one shuffle.
+        // 16 contiguous bytes (conflict-free): half of a 32-block, whose exact
+        // int32 sum the lane scales itself (the pair's halves meet in the warp
+        // sum: the same terms as a whole-block sum, another fp32 order).
         const size_t hoff = (size_t)half * (d / kKSplit);  // byte offset of this warp's K part
         const int8_t *gc = (const int8_t *)buf + (size_t)fw * d + hoff;
         const int8_t *uc = (const int8_t *)buf + (size_t)kBFeat * d + (size_t)fw * d + hoff;
@@ -1020,7 +1017,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const int8_t *x1p = xq_s + (size_t)tok1 * d + hoff;
         const float *xs0p = xs_s + tok0 * nb + half * nbh;
         const float *xs1p = xs_s + tok1 * nb + half * nbh;
-        const bool even = (lane & 1) == 0;
         float g0 = 0.0f, u0 = 0.0f, g1 = 0.0f, u1 = 0.0f;
         if (NT == 1) {
           // x from registers: only the weights and their scales come from the stage
@@ -1031,49 +1027,30 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const bool ok = c < nc;
               const uint4 z = make_uint4(0, 0, 0, 0);
               const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
-              int pg = dot16(wg, xr[i]), pu = dot16(wu, xr[i]);
-              if (kPairShuffle) {
-                pg += __shfl_xor_sync(0xffffffffu, pg, 1);
-                pu += __shfl_xor_sync(0xffffffffu, pu, 1);
-              }
+              const int pg = dot16(wg, xr[i]), pu = dot16(wu, xr[i]);
               const uint32_t blk = ok ? c >> 1 : 0;
               const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
-              if ((even || !kPairShuffle) && ok) {
+              if (ok) {
                 g0 = __fmaf_rn((float)pg, sg * xsr[i], g0);
                 u0 = __fmaf_rn((float)pu, su * xsr[i], u0);
               }
             }
           }
         } else {
-        // every lane runs the same trip count (the shuffles need the full warp);
-        // chunk pairs never straddle nc (nc is even)
 #pragma unroll 2
-        for (uint32_t c0 = 0; c0 < nc; c0 += 32) {
-          const uint32_t c = c0 + lane;
-          const bool ok = c < nc;
-          const uint4 z = make_uint4(0, 0, 0, 0);
-          const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
-          const uint4 x0 = ok ? lds16(x0p + 16 * c) : z;
-          int pg = dot16(wg, x0), pu = dot16(wu, x0);
-          pg += __shfl_xor_sync(0xffffffffu, pg, 1);
-          pu += __shfl_xor_sync(0xffffffffu, pu, 1);
-          const uint32_t blk = ok ? c >> 1 : 0;
+        for (uint32_t c = lane; c < nc; c += 32) {
+          const uint4 wg = lds16(gc + 16 * c), wu = lds16(uc + 16 * c);
+          const uint32_t blk = c >> 1;
           const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
-          if (even && ok) {
-            const float xs0 = xs0p[blk];
-            g0 = __fmaf_rn((float)pg, sg * xs0, g0);
-            u0 = __fmaf_rn((float)pu, su * xs0, u0);
-          }
+          const uint4 x0 = lds16(x0p + 16 * c);
+          const float xs0 = xs0p[blk];
+          g0 = __fmaf_rn((float)dot16(wg, x0), sg * xs0, g0);
+          u0 = __fmaf_rn((float)dot16(wu, x0), su * xs0, u0);
           if (nr > 1) {
-            const uint4 x1 = ok ? lds16(x1p + 16 * c) : z;
-            int qg = dot16(wg, x1), qu = dot16(wu, x1);
-            qg += __shfl_xor_sync(0xffffffffu, qg, 1);
-            qu += __shfl_xor_sync(0xffffffffu, qu, 1);
-            if (even && ok) {
-              const float xs1 = xs1p[blk];
-              g1 = __fmaf_rn((float)qg, sg * xs1, g1);
-              u1 = __fmaf_rn((float)qu, su * xs1, u1);
-            }
+            const uint4 x1 = lds16(x1p + 16 * c);
+            const float xs1 = xs1p[blk];
+            g1 = __fmaf_rn((float)dot16(wg, x1), sg * xs1, g1);
+            u1 = __fmaf_rn((float)dot16(wu, x1), su * xs1, u1);
           }
         }
         }
@@ -1166,13 +1143,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const uint16_t *scl = (const uint16_t *)(buf + (size_t)dsc.count * K);
         const size_t slot0 = (size_t)dsc.slot[0], slot1 = (size_t)dsc.slot[kMaxT - 1];
         const uint32_t ncr = K / 16;  // 16-byte chunks per down row
-        const bool even = (lane & 1) == 0;
         // rows m0, m0+16, .. of the stage: each h chunk is read once for kDnRows rows
         for (int m0 = warp; m0 < dsc.count; m0 += kDnRows * kConsumerWarps) {
           float acc[kDnRows][kMaxT];
 #pragma unroll
           for (int j = 0; j < kDnRows; ++j) acc[j][0] = acc[j][1] = 0.0f;
-          for (uint32_t c0 = 0; c0 < ncr; c0 += 32) {  // same trip count in every lane
+          for (uint32_t c0 = 0; c0 < ncr; c0 += 32) {
             const uint32_t c = c0 + lane;
             const bool ok = c < ncr;
             const uint32_t blk = ok ? c >> 1 : 0;
@@ -1191,14 +1167,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const bool live = ok && m < dsc.count;
               const uint4 wd = live ? lds16(qc + (size_t)m * K + 16 * c) : make_uint4(0, 0, 0, 0);
               const float sw = live ? half_bits_to_float(scl[(size_t)m * kb + blk]) : 0.0f;
-              int p0 = dot16(wd, h0);
-              if (kPairShuffle) p0 += __shfl_xor_sync(0xffffffffu, p0, 1);
-              if (even || !kPairShuffle) acc[j][0] = __fmaf_rn((float)p0, sw * hs0, acc[j][0]);
-              if (nr > 1) {
-                int p1 = dot16(wd, h1);
-                if (kPairShuffle) p1 += __shfl_xor_sync(0xffffffffu, p1, 1);
-                if (even || !kPairShuffle) acc[j][1] = __fmaf_rn((float)p1, sw * hs1, acc[j][1]);
-              }
+              // each lane scales its exact half-block sum (the halves meet in
+              // the warp sum below)
+              acc[j][0] = __fmaf_rn((float)dot16(wd, h0), sw * hs0, acc[j][0]);
+              if (nr > 1) acc[j][1] = __fmaf_rn((float)dot16(wd, h1), sw * hs1, acc[j][1]);
             }
           }
 #pragma unroll
