@@ -225,6 +225,14 @@ __device__ __forceinline__ TcTile tc_tile(const PlanView &P, const TcArgs &a, in
   return t;
 }
 
+// This CTA's tile in round rd: round rd deals tiles rd*G .. rd*G+G-1 out one per
+// CTA, from CTA 0 up in even rounds and from CTA G-1 down in odd ones; with the
+// plan listing the widest (costliest) tiles first, the CTAs' totals stay close.
+__device__ __forceinline__ int tile_of_round(int rd) {
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
+  return rd * G + ((rd & 1) ? G - 1 - b : b);
+}
+
 // Stage geometry of a tile: MMA width ncol = live rows rounded up to 16, and
 // gstages = stages whose accumulators share one TMEM buffer (ncol * gstages =
 // kBN, so a buffer is always MAT * 2 * kBN columns).  The epilogue waits, reads
@@ -426,7 +434,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int total = MAT == 2 ? P.hdr[6] : P.hdr[7];
   if (total == 0) return;  // no tensor-core tiles in this call's plan
   const uint32_t KS = a.K / kBK;  // stages per tile
-  // stage layout: [A16 mat0 16K][A16 mat1 16K][B 8K][A8 mat0 8K][A8 mat1 8K]
+  // stage layout: [A16 per matrix 16K][B 8K][A8 per matrix 8K]
   constexpr uint32_t kA16 = kBM * kBK * 2, kB16 = kBN * kBK * 2, kA8 = kBM * kBK;
   uint8_t *sc_ring = tsm + (size_t)NS * a.stage_bytes;  // [kScSlots][kScSlotBytes]
   uint8_t *ctrl = sc_ring + (size_t)kScSlots * kScSlotBytes;
@@ -479,7 +487,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ TMA producer: weights per stage, scales per kSG stages
     if (lane == 0) {
       uint32_t g = 0, scg = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
         const TcTile t = tc_tile<MAT>(P, a, tile);
         const bool sh = t.e == (int)a.E;
         // routed weights from the expert's slot (validated by k_plan)
@@ -519,9 +527,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           uint8_t *st = tsm + (size_t)s * a.stage_bytes;
           bar_expect(&ld_full[s], MAT * kA8 + kB16);
           for (int mi = 0; mi < MAT; ++mi)
-            tma_2d(st + 2 * kA16 + kB16 + mi * kA8, sh ? &maps.sw[mi] : &maps.w[mi],
+            tma_2d(st + MAT * kA16 + kB16 + mi * kA8, sh ? &maps.sw[mi] : &maps.w[mi],
                    (int)(ks * kBK), wrow, &ld_full[s]);
-          tma_2d(st + 2 * kA16, &maps.act, (int)(ks * kBK), t.slot0 + t.n0, &ld_full[s]);
+          tma_2d(st + MAT * kA16, &maps.act, (int)(ks * kBK), t.slot0 + t.n0, &ld_full[s]);
         }
       }
     }
@@ -529,7 +537,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ MMA issuer: a buffer holds gstages stages
     if (lane == 0) {
       uint32_t g = 0, bufs = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+      for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
         const TcTile tt = tc_tile<MAT>(P, a, tile);
         const TileGeom geo = tile_geom(tt.rows, tt.n0);
         const uint32_t idesc = idesc_for((uint32_t)geo.ncol);
@@ -549,7 +557,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           tc_fence_after();
           uint8_t *st = tsm + (size_t)s * a.stage_bytes;
-          const uint32_t b_addr = s32(st + 2 * kA16);
+          const uint32_t b_addr = s32(st + MAT * kA16);
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
@@ -575,7 +583,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ converters: row r = tid - 64 of the tile
     const int r = tid - 64;
     uint32_t g = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+    for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
       for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
         const uint32_t s = g % NS, use = g / NS;
         const long long tw = clock64();
@@ -588,7 +596,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         uint8_t *st = tsm + (size_t)s * a.stage_bytes;
         for (int mi = 0; mi < MAT; ++mi) {
-          const uint4 *src = (const uint4 *)(st + 2 * kA16 + kB16 + mi * kA8 + r * kBK);
+          const uint4 *src = (const uint4 *)(st + MAT * kA16 + kB16 + mi * kA8 + r * kBK);
           uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
           // Chunk order per row pair s = (r/2)%4: q = qq ^ g(s), g = (0, 2, 3, 1).
           // Loads: the staging rows are 64 B apart, so in a quarter-warp (rows
@@ -634,7 +642,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     c.abort_flag = abort_flag;
     c.t_wait = 0;
     c.t_out = 0;
-    for (int tile = blockIdx.x; tile < total && !*abort_flag; tile += gridDim.x) {
+    for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
       const TcTile t = tc_tile<MAT>(P, a, tile);
       const TileGeom geo = tile_geom(t.rows, t.n0);
       if (geo.ncol == 16) epi_tile<MAT, TAPS, 16, true>(a, c, t, geo);
@@ -875,9 +883,10 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   if (!ok) return cudaErrorInvalidValue;
   a.ws_row_stride = a.K / 32;
   a.nb_in = a.K / 32;
-  const uint32_t stage = mat == 2 ? (2 * 16384 + 8192 + 2 * 8192) : (2 * 16384 + 8192 + 2 * 8192);
+  // stage: [fp16 A per matrix 16 KB][fp16 B 8 KB][int8 A per matrix 8 KB]
+  const uint32_t stage = (uint32_t)mat * (16384 + 8192) + 8192;
   a.stage_bytes = stage;
-  a.n_stages = mat == 2 ? 3 : 3;
+  a.n_stages = mat == 2 ? 3 : 5;
   // alignment slack | stages | scale ring | barriers and flags | split-K partial sums
   const size_t smem = 1024 + (size_t)a.n_stages * stage + (size_t)kScSlots * kScSlotBytes + 1024 +
                       (size_t)mat * kBM * 33 * 4;

@@ -184,8 +184,9 @@ __device__ int block_excl_scan(int v, int *scan, int *total) {
 // Work plan from off[] (1 CTA).  Validates off, perm, pos and idx against one
 // another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
 // no work (so no kernel indexes with untrusted values).  Otherwise it lists the
-// active experts, ascending, the shared expert last, split between the dp4a
-// path and the tensor-core path: experts with more than tc_min_rows rows, when
+// active experts (dp4a list: ascending, the shared expert last; tensor-core
+// list: by rows, descending), split between the dp4a path and the tensor-core
+// path: experts with more than tc_min_rows rows, when
 // their gate/up tiles number at least tc_min_tiles (one per SM: fewer would
 // leave most SMs idle while the GEMV kernels wait behind the tensor kernel),
 // else none; every row with force_tc.
@@ -353,6 +354,54 @@ __global__ void __launch_bounds__(kPlanThreads)
     P.hdr[5] = V;
     P.hdr[6] = tiles_gu;
     P.hdr[7] = tiles_dn;
+  }
+  __syncthreads();
+  // Tensor-core experts by rows, descending (lower expert index first on equal
+  // rows; the shared expert, with every token, leads).  The tensor kernels deal
+  // tiles out in rounds of one per CTA, so the widest and costliest tiles go out
+  // first and the narrow ones even out the CTAs' totals at the end.
+  const int V = P.hdr[5];
+  if (V > 1) {
+    // (rows, expert) of every entry in shared memory while it fits
+    __shared__ int key_rows[kPlanThreads], key_e[kPlanThreads];
+    const bool in_smem = V <= kPlanThreads;
+    if (in_smem && tid < V) {
+      key_rows[tid] = P.tc_rows[tid];
+      key_e[tid] = P.tc_e[tid];
+    }
+    __syncthreads();
+    const int *rows_of = in_smem ? key_rows : P.tc_rows;
+    const int *e_of = in_smem ? key_e : P.tc_e;
+    for (int v = tid; v < V; v += kPlanThreads) {
+      const int rv = rows_of[v], ev = e_of[v];
+      int rank = 0;
+      for (int u = 0; u < V; ++u) {
+        const int ru = rows_of[u];
+        rank += (ru > rv || (ru == rv && e_of[u] < ev)) ? 1 : 0;
+      }
+      P.tc_tile_dn[rank] = ev;  // scratch: the expert at its new position
+    }
+    __syncthreads();
+    for (int r = tid; r < V; r += kPlanThreads) {
+      const int e = P.tc_tile_dn[r];
+      P.tc_e[r] = e;
+      P.tc_row0[r] = e == (int)E ? (int)R : off[e];
+      P.tc_rows[r] = e == (int)E ? (int)T : off[e + 1] - off[e];
+    }
+    __syncthreads();
+    // tile prefixes in the new order (the totals do not change)
+    const int mt = (int)(f / kTcTileM), dt = (int)(d / kTcTileM);
+    int done = 0;
+    for (int base = 0; base < V; base += kPlanThreads) {
+      const int r = base + tid;
+      const int tiles = r < V ? mt * ((P.tc_rows[r] + ntile_n - 1) / ntile_n) : 0;
+      const int tile0 = done + block_excl_scan(tiles, scan, &total);
+      if (r < V) {
+        P.tc_tile_gu[r] = tile0;
+        P.tc_tile_dn[r] = (tile0 / mt) * dt;
+      }
+      done += total;
+    }
   }
 }
 
