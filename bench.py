@@ -6,8 +6,10 @@ experts, top-8, d=6144, f=2048, shared expert 2048, Q8_0 weights, s=2.5,
 Zipf-skewed router logits), one token per step, token seeds 0..99.  A step is
 one moe_layer call (route -> permute -> quantise -> expert FFN -> shared
 expert -> combine), captured as a CUDA graph per step.  Inputs and weights are
-resident in HBM; L2 (129 MB) is flushed by writing a 2x-L2 buffer between
-steps, outside the per-step CUDA-event timing.
+resident in HBM; between steps, outside the per-step CUDA-event timing, L2
+(129 MB) is flushed by writing a 2x-L2 buffer and reading it back (the read
+pass evicts the written lines, so the timed step does not pay for writing the
+flush buffer's dirty lines back to HBM; the write-only figure is reported too).
 
 --gpus N (under torchrun) runs N replicas: each rank decodes its own tokens on
 its own copy of the weights with no data-path collective (token-parallel
@@ -218,6 +220,29 @@ def traffic_for(kernel_stage: str, workload: str):
     return None
 
 
+class L2Flush:
+    """Evicts the previous step's data from L2 between timed steps: write a
+    2x-L2 buffer, then read it back.  Writing alone leaves up to a full L2 of
+    dirty lines whose write-back to HBM would then land inside the next timed
+    step; the read pass evicts them (and the written data) before the timer
+    starts.  ``write_only`` is the plain write flush, kept for the side
+    measurement that shows the difference."""
+
+    def __init__(self, torch, dev):
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+        self.buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        self.words = self.buf.view(torch.int64)
+        self.acc = torch.zeros(1, dtype=torch.int64, device=dev)
+        self.torch = torch
+
+    def __call__(self):
+        self.buf.zero_()
+        self.torch.sum(self.words, dim=0, out=self.acc[0])
+
+    def write_only(self):
+        self.buf.zero_()
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -246,8 +271,7 @@ def run_ours(args):
     dev_in = {s: (torch.from_numpy(host_in[s][1]).to(dev), torch.from_numpy(host_in[s][0]).to(dev))
               for s in seeds}
     y = torch.empty((T, spec.d), dtype=torch.float32, device=dev)
-    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush_buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = L2Flush(torch, dev)
 
     # unique routed experts per seed (setup pass through the library's router)
     U_of, counts_of = {}, {}
@@ -315,7 +339,7 @@ def run_ours(args):
     t_wall = time.perf_counter()
     torch.cuda.nvtx.range_push("timed_steps")  # lets a profiler select these launches
     for i in range(K):
-        flush_buf.zero_()  # evict the previous step's weights from L2 (not timed)
+        flush()  # evict the previous step's weights from L2 (not timed)
         ev0[i].record()
         if graphs is not None:
             graphs[i].replay()
@@ -331,7 +355,7 @@ def run_ours(args):
 
     # stage split (not part of the timed steps)
     for i in range(K):
-        flush_buf.zero_()
+        flush()
         if staged_graphs is not None:
             staged_graphs[i].replay()
         else:
@@ -339,6 +363,24 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     step_ms = [ev0[i].elapsed_time(ev1[i]) for i in range(K)]
+
+    # side check (not the reported number): the same steps after a write-only
+    # flush, whose dirty lines are written back inside the step, and with no
+    # flush at all (the weights alone exceed L2)
+    flush_check = {}
+    for mode, fl in (("write_only_flush", flush.write_only), ("no_flush", lambda: None)):
+        n = min(K, 20)
+        for i in range(n):
+            fl()
+            ev0[i].record()
+            if graphs is not None:
+                graphs[i].replay()
+            else:
+                plain(i, step_seed[i])
+            ev1[i].record()
+        torch.cuda.synchronize()
+        flush_check[mode + "_ms_per_step"] = round(
+            statistics.mean(ev0[i].elapsed_time(ev1[i]) for i in range(n)), 5)
     stage_ms = {n: [stage_ev[i][j].elapsed_time(stage_ev[i][j + 1]) for i in range(K)]
                 for j, n in enumerate(names)}
     if nst == 1:  # a single kernel: its duration is the timed step
@@ -361,60 +403,87 @@ def run_ours(args):
 
     # end-to-end through the C ABI with host buffers: every step copies its inputs
     # in from pinned host memory and its result out, K steps back to back with the
-    # copies on a second stream (step i+1's inputs and step i's result move while
-    # a layer computes; double-buffered device copies).  No L2 flush here: a
-    # step reads 361 MB of weights, far more than L2.
-    if True:
-        pin_in = {s: (torch.from_numpy(host_in[s][1]).pin_memory(),
-                      torch.from_numpy(host_in[s][0]).pin_memory()) for s in seeds}
-        x_d = [torch.empty((T, spec.d), dtype=torch.float32, device=dev) for _ in range(2)]
-        l_d = [torch.empty((T, spec.E), dtype=torch.float32, device=dev) for _ in range(2)]
-        y_d = [torch.empty((T, spec.d), dtype=torch.float32, device=dev) for _ in range(2)]
-        y_h = [torch.empty((T, spec.d), dtype=torch.float32).pin_memory() for _ in range(2)]
-        cs = torch.cuda.Stream(dev)
-        comp = torch.cuda.current_stream(dev)
+    # copies in and the copies out on two more streams (step i+1's inputs and
+    # step i-1's result move while layer i computes; double-buffered device
+    # buffers; one copy stream for both directions would queue step i+1's inputs
+    # behind step i's result, between the two layers).  The K steps run as one
+    # CUDA graph (the steps as eager calls are reported beside it).  No L2 flush
+    # here: a step reads 361 MB of weights, far more than L2.
+    pin_in = {s: (torch.from_numpy(host_in[s][1]).pin_memory(),
+                  torch.from_numpy(host_in[s][0]).pin_memory()) for s in seeds}
+    x_d = [torch.empty((T, spec.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    l_d = [torch.empty((T, spec.E), dtype=torch.float32, device=dev) for _ in range(2)]
+    y_d = [torch.empty((T, spec.d), dtype=torch.float32, device=dev) for _ in range(2)]
+    y_h = [torch.empty((T, spec.d), dtype=torch.float32).pin_memory() for _ in range(2)]
+    cs_in, cs_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    n_ev = max(W, K)
+    in_ok, done, out_ok = ([torch.cuda.Event() for _ in range(n_ev)] for _ in range(3))
 
-        def run_steps(n, first):
-            ev = lambda: torch.cuda.Event()
-            in_ok, done, out_ok = [ev() for _ in range(n)], [ev() for _ in range(n)], \
-                [ev() for _ in range(n)]
-            for i in range(n):
-                b = i % 2
-                s_ = step_seed[(first + i) % K]
-                with torch.cuda.stream(cs):
-                    if i >= 2:
-                        cs.wait_event(done[i - 2])  # layer i-2 has read x_d[b], l_d[b]
-                    x_d[b].copy_(pin_in[s_][0], non_blocking=True)
-                    l_d[b].copy_(pin_in[s_][1], non_blocking=True)
-                    in_ok[i].record(cs)
-                comp.wait_event(in_ok[i])
+    def run_steps(n, comp):
+        cs_in.wait_stream(comp)  # brings the copy streams into a capture on comp
+        cs_out.wait_stream(comp)
+        for i in range(n):
+            b = i % 2
+            s_ = step_seed[i % K]
+            with torch.cuda.stream(cs_in):
                 if i >= 2:
-                    comp.wait_event(out_ok[i - 2])  # y_d[b] of step i-2 is copied out
-                moe.layer(desc, layer.weights, x_d[b], l_d[b], bias, y_d[b], ws)
-                done[i].record(comp)
-                with torch.cuda.stream(cs):
-                    cs.wait_event(done[i])
-                    y_h[b].copy_(y_d[b], non_blocking=True)
-                    out_ok[i].record(cs)
-            comp.wait_event(out_ok[n - 1])
+                    cs_in.wait_event(done[i - 2])  # layer i-2 has read x_d[b], l_d[b]
+                x_d[b].copy_(pin_in[s_][0], non_blocking=True)
+                l_d[b].copy_(pin_in[s_][1], non_blocking=True)
+                in_ok[i].record(cs_in)
+            comp.wait_event(in_ok[i])
+            if i >= 2:
+                comp.wait_event(out_ok[i - 2])  # y_d[b] of step i-2 is copied out
+            moe.layer(desc, layer.weights, x_d[b], l_d[b], bias, y_d[b], ws)
+            done[i].record(comp)
+            with torch.cuda.stream(cs_out):
+                cs_out.wait_event(done[i])
+                y_h[b].copy_(y_d[b], non_blocking=True)
+                out_ok[i].record(cs_out)
+        comp.wait_event(in_ok[n - 1])  # joins both copy streams
+        comp.wait_event(out_ok[n - 1])
 
-        run_steps(W, 0)
-        torch.cuda.synchronize()
+    def timed_ms(go):
         ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ea.record(comp)
-        run_steps(K, 0)
-        eb.record(comp)
+        ea.record()
+        go()
+        eb.record()
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(torch, dist, ea.elapsed_time(eb), dev)
-        e2e = {"value": round(job_throughput(T * K, world, e2e_ms), 2), "unit": "tokens/s",
-               "h2d_bytes_per_step": T * spec.d * 4 + T * spec.E * 4,
-               "d2h_bytes_per_step": T * spec.d * 4}
+        return ea.elapsed_time(eb)
+
+    main = torch.cuda.current_stream(dev)
+    run_steps(W, main)
+    torch.cuda.synchronize()
+    eager_ms = max_over_ranks(torch, dist, timed_ms(lambda: run_steps(K, main)), dev)
+    e2e_ms, e2e_how = eager_ms, "eager moe_layer calls"
+    if not args.no_graph:
+        cap = torch.cuda.Stream(dev)
+        cap.wait_stream(main)
+        g_e2e = []
+        with torch.cuda.stream(cap):
+            for n in (W, K):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cap):
+                    run_steps(n, cap)
+                g_e2e.append(g)
+        main.wait_stream(cap)
+        g_e2e[0].replay()
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(torch, dist, timed_ms(g_e2e[1].replay), dev)
+        e2e_how = "the K steps captured as one CUDA graph"
+    e2e = {"value": round(job_throughput(T * K, world, e2e_ms), 2), "unit": "tokens/s",
+           "h2d_bytes_per_step": T * spec.d * 4 + T * spec.E * 4,
+           "d2h_bytes_per_step": T * spec.d * 4,
+           "method": e2e_how + "; per step x and router logits in from pinned host memory, "
+                     "moe_layer, y out to pinned host memory (copies in and copies out on "
+                     "two more streams, double-buffered device buffers)",
+           "eager_calls_value": round(job_throughput(T * K, world, eager_ms), 2)}
     assert moe.check_device_error(ws) == 0
 
     sweep = None
     if not args.no_sweep and world == 1 and args.workload == "decode_t1":
         del graphs
-        sweep = run_sweep(torch, moe, synth, dev, layer, flush_buf, peak)
+        sweep = run_sweep(torch, moe, synth, dev, layer, flush, peak)
 
     cpu = None
     if rank == 0 and world == 1:
@@ -443,8 +512,9 @@ def run_ours(args):
                         f"s={spec.s}, zipf_beta={spec.zipf_beta}",
             "token_seeds": f"{seeds[0]}..{seeds[-1]}",
             "tokens_per_step": T,
-            "l2": "flushed between steps (2x L2 write), outside the per-step CUDA-event time; "
-                  "e2e: K steps back to back, each reading 361 MB of weights (> L2), no flush",
+            "l2": "flushed between steps (2x L2 write, then read back), outside the per-step "
+                  "CUDA-event time; e2e: K steps back to back, each reading 361 MB of weights "
+                  "(> L2), no flush",
             "timing": ("eager moe_layer calls" if args.no_graph
                        else "one CUDA graph of one moe_layer call per step")
                       + "; CUDA events around each step; stage split from a second, "
@@ -468,6 +538,7 @@ def run_ours(args):
         "path": path,
         "clocks": clk,
         "e2e": e2e,
+        "l2_flush_check": flush_check,
         "cpu_baseline": cpu,
         "wall_s_timed_region": round(t_wall, 4),
     }
@@ -476,7 +547,7 @@ def run_ours(args):
     return line
 
 
-def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
+def run_sweep(torch, moe, synth, dev, layer, flush, peak):
     """Side measurements at T=2/16/512 on the same layer and T=64 on the 2-bit
     layer (eager calls, 10 steps each after 3 warm-ups, L2 flushed between)."""
     out = {}
@@ -500,7 +571,7 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
             moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[0])
         torch.cuda.synchronize()
         for i in range(n):
-            flush_buf.zero_()
+            flush()
             moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[i])
         torch.cuda.synchronize()
         step = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(n)]
@@ -521,12 +592,12 @@ def run_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
                      "stage_gbs": {k: round(b[k] / (stage[k] / 1e3) / 1e9, 1)
                                    for k in ROOFLINE_STAGES if k in stage and b[k] > 0}}
         assert moe.check_device_error(ws) == 0
-    out.update(run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak))
+    out.update(run_router_sweep(torch, moe, synth, dev, layer, flush, peak))
     out.update(run_stream_sweep(torch, moe, synth, dev, layer))
     return out
 
 
-def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
+def run_router_sweep(torch, moe, synth, dev, layer, flush, peak):
     """The router front end at T=1: x -> router logits GEMM (fp32 W_r [E][d]) ->
     layer, on the sigmoid layer and on the DeepSeek-scored 384-expert layer.
     Three CUDA graphs per case -- the logits GEMM kernel alone, that kernel
@@ -584,7 +655,7 @@ def run_router_sweep(torch, moe, synth, dev, layer, flush_buf, peak):
                 g.replay()
             torch.cuda.synchronize()
             for a, b in ev:
-                flush_buf.zero_()
+                flush()
                 a.record()
                 g.replay()
                 b.record()
