@@ -281,11 +281,14 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
   const bool sh = t.e == (int)a.E;
   const int width = MAT == 2 ? (int)(sh ? a.fs : a.f) : (int)a.d;
   const int col0 = SPLIT ? 0 : 32 * half;
-  float acc[MAT][NCM];
+  // accumulator pairs (columns 2i, 2i+1): the scale products and FMAs run as
+  // packed fp32x2 operations, each lane rounded as the scalar operation would be
+  float2 acc2[MAT][NCM / 2];
+#define ACC(mi, j) (((j) & 1) ? acc2[mi][(j) >> 1].y : acc2[mi][(j) >> 1].x)
 #pragma unroll
   for (int mi = 0; mi < MAT; ++mi)
 #pragma unroll
-    for (int j = 0; j < NCM; ++j) acc[mi][j] = 0.0f;
+    for (int j = 0; j < NCM / 2; ++j) acc2[mi][j] = make_float2(0.0f, 0.0f);
   int jt = -1;  // tapped feature index of this thread, if any
   if (TAPS) {
     const int wf = t.m0 + feat;
@@ -293,28 +296,44 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
     for (int j = kNTap - 1; j >= 0; --j)
       if ((int)tap_feature(j, width) == wf) jt = j;
   }
-  for (uint32_t ks0 = 0; ks0 < c.KS; ks0 += geo.gstages) {
-    const uint32_t b = c.bufs & 1u;
+  // The loop's counters and the TMEM base in registers for the whole tile (a
+  // reference into the caller's frame is reloaded from local memory after
+  // every asm with a memory clobber); the barriers, the scale ring and the
+  // abort flag are fixed offsets from one base (the kernel's control block).
+  const uint32_t KS = c.KS, tmem = c.tmem;
+  constexpr uint32_t half_cols = MAT == 2 ? 256 : 128;
+  uint32_t bufs = c.bufs, scgroups = c.scgroups;
+  uint64_t *const d_full = c.d_full;
+  uint64_t *const d_empty = d_full + 2;
+  uint64_t *const sc_full = d_empty + 2;
+  uint64_t *const sc_empty = sc_full + kScSlots;
+  const uint8_t *const sc_ring = (const uint8_t *)(d_full - 24) - kScSlots * kScSlotBytes;
+  volatile int *const abort_flag = (volatile int *)((uint32_t *)(sc_empty + kScSlots) + 1);
+  long long t_wait = c.t_wait;
+  for (uint32_t ks0 = 0; ks0 < KS; ks0 += geo.gstages) {
+    const uint32_t b = bufs & 1u;
     const long long tw = clock64();
-    if (!bar_wait(&c.d_full[b], (c.bufs >> 1) & 1u)) {
+    if (!bar_wait(&d_full[b], (bufs >> 1) & 1u)) {
       atomicOr(a.err, kErrTimeout);
-      *c.abort_flag = 1;
+      *abort_flag = 1;
+      c.bufs = bufs, c.scgroups = scgroups, c.t_wait = t_wait;
       return;
     }
-    c.t_wait += clock64() - tw;
+    t_wait += clock64() - tw;
     tc_fence_after();
-    const uint32_t nst = min((uint32_t)geo.gstages, c.KS - ks0);
+    const uint32_t nst = min((uint32_t)geo.gstages, KS - ks0);
     for (uint32_t si = 0; si < nst; ++si) {
       const uint32_t ks = ks0 + si;
-      const uint32_t q = c.scgroups % kScSlots;  // scale slot of stage ks
+      const uint32_t q = scgroups % kScSlots;  // scale slot of stage ks
       if (ks % kSG == 0) {
-        if (!bar_wait(&c.sc_full[q], (c.scgroups / kScSlots) & 1u)) {
+        if (!bar_wait(&sc_full[q], (scgroups / kScSlots) & 1u)) {
           atomicOr(a.err, kErrTimeout);
-          *c.abort_flag = 1;
+          *abort_flag = 1;
+          c.bufs = bufs, c.scgroups = scgroups, c.t_wait = t_wait;
           return;
         }
       }
-      const uint8_t *slot = c.sc_ring + (size_t)q * kScSlotBytes;
+      const uint8_t *slot = sc_ring + (size_t)q * kScSlotBytes;
       const uint16_t *wsl = (const uint16_t *)slot;                       // [MAT][kBM][8]
       const float *xsl = (const float *)(slot + MAT * kBM * kSG * 2 * 2);  // [kBN][8]
       const uint32_t blk0 = (ks % kSG) * 2;  // first block of this stage in the slot
@@ -335,8 +354,8 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
           float v[MAT][16];
 #pragma unroll
           for (int mi = 0; mi < MAT; ++mi)
-            tc_ld16_issue(c.tmem + ((uint32_t)(quarter * 32) << 16) +
-                              acc_col<MAT>(b, c.half_cols, (int)si, mi, bi, geo.ncol) + col0 +
+            tc_ld16_issue(tmem + ((uint32_t)(quarter * 32) << 16) +
+                              acc_col<MAT>(b, half_cols, (int)si, mi, bi, geo.ncol) + col0 +
                               16 * c16,
                           v[mi]);
           float xsv[16];  // the 16 rows' x scales of this block (shared by both matrices)
@@ -346,9 +365,13 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
 #pragma unroll
           for (int mi = 0; mi < MAT; ++mi) {
             const float ws_b = wsc[mi][bi];
+            const float2 ws2 = make_float2(ws_b, ws_b);
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              acc[mi][16 * c16 + j] = __fmaf_rn(v[mi][j], ws_b * xsv[j], acc[mi][16 * c16 + j]);
+            for (int j = 0; j < 16; j += 2) {
+              const float2 sc2 = __fmul2_rn(ws2, make_float2(xsv[j], xsv[j + 1]));
+              float2 &a2 = acc2[mi][(16 * c16 + j) >> 1];
+              a2 = __ffma2_rn(make_float2(v[mi][j], v[mi][j + 1]), sc2, a2);
+            }
             if (TAPS && jt >= 0) {
               const uint32_t kb = ks * 2 + bi;
               for (int j = 0; j < 16; ++j) {
@@ -364,17 +387,20 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
           }
         }
       }
-      if (ks % kSG == kSG - 1 || ks + 1 == c.KS) {  // the scale slot's last stage
+      if (ks % kSG == kSG - 1 || ks + 1 == KS) {  // the scale slot's last stage
         __syncwarp();
-        if (lane == 0) bar_arrive(&c.sc_empty[q]);
-        ++c.scgroups;
+        if (lane == 0) bar_arrive(&sc_empty[q]);
+        ++scgroups;
       }
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) bar_arrive(&c.d_empty[b]);
-    ++c.bufs;
+    if (lane == 0) bar_arrive(&d_empty[b]);
+    ++bufs;
   }
+  c.bufs = bufs;
+  c.scgroups = scgroups;
+  c.t_wait = t_wait;
   const long long t_o = clock64();
   if (SPLIT) {
     // odd blocks' partial sums (half 1) join the even blocks' (half 0)
@@ -382,7 +408,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
 #pragma unroll
       for (int mi = 0; mi < MAT; ++mi)
 #pragma unroll
-        for (int j = 0; j < NCM; ++j) c.red[((size_t)mi * kBM + feat) * 33 + j] = acc[mi][j];
+        for (int j = 0; j < NCM; ++j) c.red[((size_t)mi * kBM + feat) * 33 + j] = ACC(mi, j);
     }
     epi_sync();
     if (half == 0) {
@@ -390,7 +416,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
       for (int mi = 0; mi < MAT; ++mi)
 #pragma unroll
         for (int j = 0; j < NCM; ++j)
-          acc[mi][j] = __fadd_rn(acc[mi][j], c.red[((size_t)mi * kBM + feat) * 33 + j]);
+          ACC(mi, j) = __fadd_rn(ACC(mi, j), c.red[((size_t)mi * kBM + feat) * 33 + j]);
     }
   }
   // ---- tile output: this warp's columns (half 0 only when split)
@@ -402,7 +428,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
       const size_t sl = (size_t)(t.slot0 + t.n0 + n);
       if (MAT == 2) {
         // h = silu(g)*u, requantised over this warp's 32 consecutive features
-        const float gv = acc[0][j], uv = acc[MAT - 1][j];
+        const float gv = ACC(0, j), uv = ACC(MAT - 1, j);
         const float h = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
         float amax = fabsf(h);
 #pragma unroll
@@ -414,13 +440,14 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
         a.hperm[sl * a.fmax + fo] = __int2half_rn(qv);
         if (lane == 0) a.hs[sl * (a.fmax / 32) + fo / 32] = sc;
       } else {
-        a.o[sl * a.d + t.m0 + feat] = acc[0][j];
+        a.o[sl * a.d + t.m0 + feat] = ACC(0, j);
       }
     }
   }
   if (SPLIT) epi_sync();  // red[] is free again
   c.t_out += clock64() - t_o;
 }
+#undef ACC
 
 template <int MAT, bool TAPS>
 __global__ void __launch_bounds__(kTcThreads, 1)
