@@ -47,12 +47,12 @@ struct DNArgs {
 
 // Shape of a warp work item: NF consecutive output features of one expert; a
 // pass over 32*J blocks gives lane l the blocks l, l+32, .., l+32(J-1) of each
-// of the NF rows of each of the NM matrices, all loaded before any use (about
-// 32 registers of weight codes in flight per lane, enough to cover HBM latency
-// with 16 warps per SM); one plan lookup per item.
+// of the NF rows of each of the NM matrices, all loaded before any use (32 to
+// 64 registers of weight codes in flight per lane, to cover HBM latency with
+// 16-24 warps per SM); one plan lookup per item.
 template <int FMT, int NM>
 __host__ __device__ constexpr int group_nf() {
-  return NM == 2 ? (FMT == MOE_FMT_Q2S ? 2 : 1) : (FMT == MOE_FMT_Q2S ? 4 : 2);
+  return NM == 2 ? (FMT == MOE_FMT_Q2S ? 2 : 1) : 4;
 }
 template <int FMT, int NM, int MAXR>
 __host__ __device__ constexpr int group_j() {
@@ -61,6 +61,10 @@ __host__ __device__ constexpr int group_j() {
 
 template <int FMT, int MAXR>
 __host__ __device__ constexpr int min_ctas() { return FMT == MOE_FMT_Q8_0 && MAXR <= 2 ? 3 : 2; }
+// down items are 4 features of a 2048-wide row (one pass each): the 4 rows' codes
+// in flight need the registers of 2 CTAs per SM
+template <int FMT, int MAXR>
+__host__ __device__ constexpr int min_ctas_dn() { return 2; }
 
 __device__ __forceinline__ int find_slot(const int *prefix, int U, int item) {
   int lo = 0, hi = U;
@@ -322,7 +326,7 @@ __device__ __forceinline__ void down_group(const DNArgs &a, const int8_t *dq, co
 }
 
 template <int FMT, int MAXR, bool TAPS>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>())) k_down(const DNArgs a) {
+__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas_dn<FMT, MAXR>())) k_down(const DNArgs a) {
   constexpr int NF = group_nf<FMT, 1>(), J = group_j<FMT, 1, MAXR>();
   constexpr int NFS = group_nf<MOE_FMT_Q8_0, 1>(), JS = group_j<MOE_FMT_Q8_0, 1, MAXR>();
   static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
