@@ -50,17 +50,22 @@ struct DNArgs {
 // of the NF rows of each of the NM matrices, all loaded before any use (32 to
 // 64 registers of weight codes in flight per lane, to cover HBM latency with
 // 16-24 warps per SM); one plan lookup per item.
-template <int FMT, int NM>
+// WIDE (gate/up, many tokens): 2 features per item for both formats -- twice the
+// codes in flight per warp; it pays when the call streams many experts' rows
+// (prefill) and costs a little on small batches, whose items are already few.
+template <int FMT, int NM, bool WIDE = false>
 __host__ __device__ constexpr int group_nf() {
-  return NM == 2 ? (FMT == MOE_FMT_Q2S ? 2 : 1) : 4;
+  return NM == 2 ? (FMT == MOE_FMT_Q2S || WIDE ? 2 : 1) : 4;
 }
 template <int FMT, int NM, int MAXR>
 __host__ __device__ constexpr int group_j() {
   return FMT == MOE_FMT_Q2S && NM == 2 && MAXR < 4 ? 4 : 2;
 }
 
-template <int FMT, int MAXR>
-__host__ __device__ constexpr int min_ctas() { return FMT == MOE_FMT_Q8_0 && MAXR <= 2 ? 3 : 2; }
+template <int FMT, int MAXR, bool WIDE = false>
+__host__ __device__ constexpr int min_ctas() {
+  return FMT == MOE_FMT_Q8_0 && MAXR <= 2 && !WIDE ? 3 : 2;
+}
 // down items are 4 features of a 2048-wide row (one pass each): the 4 rows' codes
 // in flight need the registers of 2 CTAs per SM
 template <int FMT, int MAXR>
@@ -221,11 +226,11 @@ __device__ __forceinline__ void gateup_group(const GUArgs &a, const int8_t *gq,
   }
 }
 
-template <int FMT, int MAXR, bool TAPS>
-__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR>()))
+template <int FMT, int MAXR, bool TAPS, bool WIDE>
+__global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR, WIDE>()))
     k_gateup(const GUArgs a) {
-  constexpr int NF = group_nf<FMT, 2>(), J = group_j<FMT, 2, MAXR>();
-  constexpr int NFS = group_nf<MOE_FMT_Q8_0, 2>(), JS = group_j<MOE_FMT_Q8_0, 2, MAXR>();
+  constexpr int NF = group_nf<FMT, 2, WIDE>(), J = group_j<FMT, 2, MAXR>();
+  constexpr int NFS = group_nf<MOE_FMT_Q8_0, 2, WIDE>(), JS = group_j<MOE_FMT_Q8_0, 2, MAXR>();
   static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
   extern __shared__ int gsm[];
   PlanView P(const_cast<int *>(a.plan), a.E);
@@ -390,10 +395,10 @@ cudaError_t grid_for(K kernel, size_t smem, bool &big_smem, int &per_sm) {
   return cudaSuccess;
 }
 
-template <int FMT, int MAXR, bool TAPS>
+template <int FMT, int MAXR, bool TAPS, bool WIDE>
 cudaError_t run_gateup(const Ctx &c, const GUArgs &a) {
   static bool big_smem = false;
-  auto kern = k_gateup<FMT, MAXR, TAPS>;
+  auto kern = k_gateup<FMT, MAXR, TAPS, WIDE>;
   const size_t smem = smem_plan_bytes(c.desc.n_expert);
   int per_sm = 1;
   cudaError_t e = grid_for(kern, smem, big_smem, per_sm);
@@ -416,10 +421,14 @@ cudaError_t run_down(const Ctx &c, const DNArgs &a) {
 
 // rows per pass: an expert has at most T rows; more than 4 take several passes
 int maxr_for(uint32_t T) { return T <= 1 ? 1 : T <= 2 ? 2 : 4; }
+// tokens per call from which the gate/up items are 2 features wide (gate/up
+// GEMV on the 256-expert layer, 1 -> 2 features: T=16 401 -> 426 us, T=32
+// 481 -> 446, T=64 713 -> 637, T=128 807 -> 700, T=512 598 -> 512)
+constexpr uint32_t kWideGateupT = 32;
 
-template <int FMT, int MAXR>
+template <int FMT, int MAXR, bool WIDE = false>
 cudaError_t gu_taps(const Ctx &c, const GUArgs &a, bool taps) {
-  return taps ? run_gateup<FMT, MAXR, true>(c, a) : run_gateup<FMT, MAXR, false>(c, a);
+  return taps ? run_gateup<FMT, MAXR, true, WIDE>(c, a) : run_gateup<FMT, MAXR, false, WIDE>(c, a);
 }
 template <int FMT, int MAXR>
 cudaError_t dn_taps(const Ctx &c, const DNArgs &a, bool taps) {
@@ -431,7 +440,8 @@ cudaError_t gu_maxr(const Ctx &c, const GUArgs &a, bool taps) {
   switch (maxr_for(c.T)) {
     case 1: return gu_taps<FMT, 1>(c, a, taps);
     case 2: return gu_taps<FMT, 2>(c, a, taps);
-    default: return gu_taps<FMT, 4>(c, a, taps);
+    default:
+      return c.T >= kWideGateupT ? gu_taps<FMT, 4, true>(c, a, taps) : gu_taps<FMT, 4>(c, a, taps);
   }
 }
 template <int FMT>
