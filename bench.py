@@ -5,7 +5,8 @@ Default workload: single-token decode of a GLM-5.2-shaped layer (E=256
 experts, top-8, d=6144, f=2048, shared expert 2048, Q8_0 weights, s=2.5,
 Zipf-skewed router logits), one token per step, token seeds 0..99.  A step is
 one moe_layer call (route -> permute -> quantise -> expert FFN -> shared
-expert -> combine), captured as a CUDA graph per step.  Inputs and weights are
+expert -> combine), launched eagerly (--graph: a CUDA graph per step; its
+GPU-side launch adds ~1.5 us to the decode step).  Inputs and weights are
 resident in HBM; between steps, outside the per-step CUDA-event timing, L2
 (129 MB) is flushed by writing a 2x-L2 buffer and reading it back (the read
 pass evicts the written lines, so the timed step does not pay for writing the
@@ -50,7 +51,10 @@ def parse_args(argv=None):
                     help="budget of the oracle CPU-baseline sample")
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the T=2/16/512 and 2-bit side measurements")
-    ap.add_argument("--no-graph", action="store_true", help="time eager calls, no CUDA graphs")
+    ap.add_argument("--graph", action="store_true",
+                    help="time each step as a replay of a CUDA graph of its moe_layer call "
+                         "(default: eager moe_layer calls)")
+    ap.add_argument("--no-graph", action="store_true", help="no CUDA graphs anywhere (e2e too)")
     ap.add_argument("--flags", type=int, default=0, help="moe_desc.flags for the timed calls")
     return ap.parse_args(argv)
 
@@ -314,7 +318,8 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     graphs = staged_graphs = None
-    if not args.no_graph:
+    graphed = args.graph and not args.no_graph
+    if graphed:
         graphs, staged_graphs = [], []
         cap = torch.cuda.Stream(dev)
         cap.wait_stream(stream)
@@ -515,8 +520,9 @@ def run_ours(args):
             "l2": "flushed between steps (2x L2 write, then read back), outside the per-step "
                   "CUDA-event time; e2e: K steps back to back, each reading 361 MB of weights "
                   "(> L2), no flush",
-            "timing": ("eager moe_layer calls" if args.no_graph
-                       else "one CUDA graph of one moe_layer call per step")
+            "timing": ("one CUDA graph of one moe_layer call per step" if graphed
+                       else "eager moe_layer calls (the flush kernels between steps keep the "
+                            "launches ahead of the GPU)")
                       + "; CUDA events around each step; stage split from a second, "
                         "untimed pass with per-stage events",
             "parallelism": f"replicas x{world} (token-parallel decode, no collective)",
