@@ -192,8 +192,10 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t 
   hi = *reinterpret_cast<uint32_t *>(&b);
 }
 
-__device__ __forceinline__ void epi_sync() {
-  asm volatile("bar.sync 3, %0;" ::"n"(kEpiWarps * 32) : "memory");
+// the two epilogue warps that read TMEM lane quarter q (one of each half) meet at
+// named barrier 4 + q; they alone share rows of the split-K partial sums
+__device__ __forceinline__ void epi_pair_sync(int quarter) {
+  asm volatile("bar.sync %0, 64;" ::"r"(4 + quarter) : "memory");
 }
 
 // tile list of the plan: v -> (expert, slot0, rows); tile t -> (v, m-tile, n-tile)
@@ -410,7 +412,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
 #pragma unroll
         for (int j = 0; j < NCM; ++j) c.red[((size_t)mi * kBM + feat) * 33 + j] = ACC(mi, j);
     }
-    epi_sync();
+    epi_pair_sync(quarter);
     if (half == 0) {
 #pragma unroll
       for (int mi = 0; mi < MAT; ++mi)
@@ -444,7 +446,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
       }
     }
   }
-  if (SPLIT) epi_sync();  // red[] is free again
+  if (SPLIT) epi_pair_sync(quarter);  // this quarter's red[] rows are free again
   c.t_out += clock64() - t_o;
 }
 #undef ACC
