@@ -432,9 +432,9 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
         // h = silu(g)*u, requantised over this warp's 32 consecutive features
         const float gv = ACC(0, j), uv = ACC(MAT - 1, j);
         const float h = __fmul_rn(__fdiv_rn(gv, __fadd_rn(1.0f, spec_exp(-gv))), uv);
-        float amax = fabsf(h);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        // |h| of finite values orders as its bit pattern: one warp max reduction
+        const float amax =
+            __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h))));
         const float sc = __fdiv_rn(amax, 127.0f);
         const int qv = quant_one(h, sc);
         const size_t fo = (size_t)t.m0 + feat;
