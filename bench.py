@@ -739,6 +739,23 @@ def run_stream_sweep(torch, moe, synth, dev, layer, n_layers=8, n_slots=512, war
     bias = [torch.from_numpy(synth.bias(s)).to(dev) for s in specs]
     ws = torch.zeros(moe.workspace_size(desc, 1), dtype=torch.uint8, device=dev)
     peak = h2d_peak_gbs(torch, dev)
+    # the link rate from where the expert tier itself sits in host memory (its
+    # pinned pages may land on another NUMA node than the 1 GiB probe's): 16
+    # experts' gate codes, one copy each, best of 3
+    n_probe = 16
+    src_rows = host_t["gate_q"].view(spec.E, -1)
+    dst_probe = torch.empty((n_probe, src_rows.shape[1]), dtype=torch.int8, device=dev)
+    tier_gbs = None
+    for _ in range(3):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n_probe):
+            dst_probe[i].copy_(src_rows[(37 * i) % spec.E], non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        gbs = n_probe * src_rows.shape[1] / (a.elapsed_time(b) / 1e3) / 1e9
+        tier_gbs = gbs if tier_gbs is None else max(tier_gbs, gbs)
+    del dst_probe
     expert_bytes = spec.f * spec.d * 2 * 1.0625 + spec.d * spec.f * 1.0625
     side = torch.cuda.Stream(dev)
 
@@ -791,6 +808,7 @@ def run_stream_sweep(torch, moe, synth, dev, layer, n_layers=8, n_slots=512, war
             "h2d_bytes_per_token": int(link),
             "h2d_gbs": round(link / (ms / 1e3) / 1e9, 1),
             "h2d_peak_gbs": round(peak, 1),
+            "h2d_expert_tier_gbs": round(tier_gbs, 1),
             "h2d_frac_of_measured": round(link / (ms / 1e3) / 1e9 / peak, 4),
             "hbm_bytes_per_token": int(n_layers * 9 * expert_bytes),
         }
