@@ -279,9 +279,8 @@ __global__ void __launch_bounds__(256)
   if (b >= width / 32) return;
   const size_t i = (size_t)slot * fmax + 32 * b + lane;
   const float v = h[i];
-  float amax = fabsf(v);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  // |h| of finite values orders as its bit pattern: one warp max reduction
+  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
   const float sc = __fdiv_rn(amax, 127.0f);
   const int8_t q = (int8_t)quant_one(v, sc);
   hq[i] = q;

@@ -263,12 +263,11 @@ __device__ __forceinline__ uint32_t acc_col(uint32_t b, uint32_t half_cols, int 
 // 32*(w%4).. (= features).  Per block: acc += dot * (w-scale * x-scale), the
 // scales coming from the scale ring (one slot per kSG stages, filled by TMA).
 struct EpiState {
-  uint32_t tmem, half_cols, KS;
+  uint32_t tmem, KS;
   uint32_t bufs, scgroups;  // accumulator buffers / scale groups consumed so far
-  uint64_t *d_full, *d_empty, *sc_full, *sc_empty;
-  uint8_t *sc_ring;
+  uint64_t *d_full;         // the control block's other barriers, the scale ring and
+                            // the abort flag sit at fixed offsets from it
   float *red;
-  volatile int *abort_flag;
   long long t_wait, t_out;
 };
 
@@ -658,17 +657,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ epilogue
     EpiState c;
     c.tmem = tmem;
-    c.half_cols = tmem_cols / 2;
     c.KS = KS;
     c.bufs = 0;
     c.scgroups = 0;
     c.d_full = d_full;
-    c.d_empty = d_empty;
-    c.sc_full = sc_full;
-    c.sc_empty = sc_empty;
-    c.sc_ring = sc_ring;
     c.red = red;
-    c.abort_flag = abort_flag;
     c.t_wait = 0;
     c.t_out = 0;
     for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
