@@ -386,3 +386,50 @@ def test_tensor_core_dispatch_needs_a_tile_per_sm(gpu, T):
     want_tc = thr is not None and thr >= 0 and bench.tc_tiles(spec, T, counts, thr) >= sms
     assert (hdr[5] > 0) == want_tc, (T, hdr[5], bench.tc_tiles(spec, T, counts, thr), sms)
     print("dispatch", T, hdr[5], rep)
+
+
+def test_tensor_core_plan_lists_widest_experts_first(gpu):
+    """The plan's tensor-core list (the order the tensor kernels deal tiles out
+    in) holds exactly the experts with rows plus the shared expert, sorted by
+    rows, descending, the lower expert index first on equal rows; each entry's
+    first slot and rows agree with the routing offsets, and the tile prefixes
+    count (f/128) x ceil(rows/64) gate/up and (d/128) x ceil(rows/64) down tiles
+    per entry in that order."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=32, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    T, E = 64, 32
+    fl = moe.FLAG_FORCE_TC
+    layer = device_layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 5, T)
+    out = layer.forward(torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
+                        torch.from_numpy(synth.bias(spec)).to(gpu), flags=fl)
+    torch.cuda.synchronize()
+    ws = layer.workspace(T, fl)
+    L = moe.workspace_layout(layer.desc(fl), T)
+    n_int = 8 + 9 * (E + 2)
+    plan = ws[L.plan:L.plan + 4 * n_int].view(torch.int32).cpu().numpy()
+    item_gu = 8 + 3 * (E + 1)
+    tc_e = item_gu + (E + 2)
+    tc_row0, tc_rows = tc_e + (E + 1), tc_e + 2 * (E + 1)
+    tc_tile_gu = tc_e + 3 * (E + 1)
+    tc_tile_dn = tc_tile_gu + (E + 2)
+    V = int(plan[5])
+    off = out.off.cpu().numpy()
+    rows_of = {e: int(off[e + 1] - off[e]) for e in range(E) if off[e + 1] > off[e]}
+    rows_of[E] = T
+    es = [int(v) for v in plan[tc_e:tc_e + V]]
+    rows = [int(v) for v in plan[tc_rows:tc_rows + V]]
+    assert sorted(es) == sorted(rows_of), (es, rows_of)
+    assert rows == [rows_of[e] for e in es]
+    for i in range(V - 1):
+        assert rows[i] > rows[i + 1] or (rows[i] == rows[i + 1] and es[i] < es[i + 1]), (i, es, rows)
+    R = T * spec.k
+    assert [int(v) for v in plan[tc_row0:tc_row0 + V]] == [R if e == E else int(off[e]) for e in es]
+    mt, dt = spec.f // 128, spec.d // 128
+    gu, dn = 0, 0
+    for i, r in enumerate(rows):
+        assert plan[tc_tile_gu + i] == gu and plan[tc_tile_dn + i] == dn, i
+        gu += mt * ((r + 63) // 64)
+        dn += dt * ((r + 63) // 64)
+    assert plan[tc_tile_gu + V] == gu == plan[6] and plan[tc_tile_dn + V] == dn == plan[7]
