@@ -127,7 +127,8 @@ def sqrt_softplus(logit) -> np.ndarray:
 
 
 def router_logits(x, w_r) -> np.ndarray:
-    """logits[T][E] = x[T][d] . w_r[E][d]^T in the oracle's fixed fp32 order."""
+    """logits[T][E] = x[T][d] . w_r[E][d]^T: exact products summed in fp64,
+    rounded once to fp32."""
     x = _c(x, np.float32)
     w_r = _c(w_r, np.float32)
     T, d = x.shape

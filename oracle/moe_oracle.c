@@ -109,34 +109,20 @@ float ora_sqrt_softplus(float l) {
   return sqrtf(m + ora_spec_log1p(e));
 }
 
-/* Router logits l[t][e] = sum_i x[t][i] * w_r[e][i] in fp32 in one fixed order
- * (the router GEMM in front of the scoring; its precision is not given on the
- * pages, so fp32 weights and this order define it).  The d inputs form
- * segments of 1024 (the last one may be shorter); in segment g, 32 partial sums
- * p_l are fmaf chains over i = 1024 g + l + 32 j, j ascending; then for
- * o = 16, 8, 4, 2, 1: p_l <- p_l + p_(l xor o) for every l at once; the segment
- * total is p_0; the logit is the sum of the segment totals in ascending g,
- * starting from the first. */
+/* Router logits l[t][e] = sum_i x[t][i] * w_r[e][i] (the router GEMM in front
+ * of the scoring: per token, n_expert logits feed the expert scores -- "256
+ * experts, 512 lines", "The constant that always said 256").  The pages give
+ * no precision or order for it, so the plain definition is taken: every
+ * product of the fp32 inputs (exact in double: 24 + 24 significand bits), the
+ * products summed in double in ascending i, and the sum rounded once to fp32. */
 void ora_router_logits(uint32_t T, uint32_t E, uint32_t d, const float *x, const float *w_r,
                        float *logits) {
   for (uint32_t t = 0; t < T; ++t) {
     for (uint32_t e = 0; e < E; ++e) {
-      float total = 0.0f;
-      for (uint32_t g0 = 0; g0 < d; g0 += 1024) {
-        const uint32_t g1 = g0 + 1024 < d ? g0 + 1024 : d;
-        float p[32], q[32];
-        for (uint32_t l = 0; l < 32; ++l) {
-          p[l] = 0.0f;
-          for (uint32_t i = g0 + l; i < g1; i += 32)
-            p[l] = fmaf(x[(size_t)t * d + i], w_r[(size_t)e * d + i], p[l]);
-        }
-        for (uint32_t o = 16; o >= 1; o >>= 1) {
-          for (uint32_t l = 0; l < 32; ++l) q[l] = p[l] + p[l ^ o];
-          memcpy(p, q, sizeof p);
-        }
-        total = g0 == 0 ? p[0] : total + p[0];
-      }
-      logits[(size_t)t * E + e] = total;
+      double sum = 0.0;
+      for (uint32_t i = 0; i < d; ++i)
+        sum += (double)x[(size_t)t * d + i] * (double)w_r[(size_t)e * d + i];
+      logits[(size_t)t * E + e] = (float)sum;
     }
   }
 }

@@ -15,8 +15,9 @@
  *  - DeepSeek : p_i = sqrt(softplus(l_i)) in place of sigma_i (spec-log1p below),
  *               top-6, scale 1.5, E = 384 ("256 experts, 512 lines", section
  *               "The constant that always said 256").
- *  - router   : logits l = x . W_r^T in fp32 in one fixed summation order
- *               (ora_router_logits).
+ *  - router   : logits l = x . W_r^T: exact products of the fp32 inputs summed
+ *               in fp64, rounded once to fp32 (ora_router_logits; the pages give
+ *               no precision or order for the router GEMM).
  *  - top-k    : k indices of largest c; equal c -> lower index first; slots in
  *               order of c descending.  Weight w_j = s * sigma_j / sum_j sigma_j
  *               (fp64).  The parameterised n_expert/top_k/scale router:
@@ -34,7 +35,8 @@
  *  - expert   : g_n = sum_b isum_b(Wg[n], xq) * wsg[n][b] * xs[b] with isum_b an
  *               exact int32 dot of 32 int8 pairs (the dp4a technique: NeutronStar
  *               README, "What this branch adds over upstream"); same for u;
- *               h = g*sigmoid(g)*u; h rounded to fp32 and requantised as above;
+ *               h = g/(1+exp(-g))*u in fp64 (libm exp); h rounded to fp32 and
+ *               requantised as above;
  *               o_m = sum_b isum_b(Wd[m], hq) * wsd[m][b] * hs[b].  fp64 sums in
  *               block order.  Q8_0 weights ("everything that makes decisions
  *               stays at Q8_0/F32": NeutronStar README, "The model").

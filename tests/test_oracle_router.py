@@ -1,7 +1,7 @@
 """Pins of the oracle's router front end (no GPU): spec-log1p, the DeepSeek
 scoring sqrt(softplus(l)) ("256 experts, 512 lines", section "The constant that
-always said 256": top-6, scale 1.5, E = 384) and the router logits GEMM in its
-fixed fp32 summation order.  Each is checked against the mathematics -- libm in
+always said 256": top-6, scale 1.5, E = 384) and the router logits GEMM (the
+dot product of the fp32 inputs rounded once).  Each is checked against the mathematics -- libm in
 fp64, closed forms, error bounds -- not against a retyped copy of itself."""
 import math
 
@@ -77,18 +77,32 @@ def test_route_sqrt_softplus_topk_and_weights(s):
         assert abs(float(w[t].astype(np.float64).sum()) - s) <= k * 2 ** -23 * s
 
 
-@pytest.mark.parametrize("T,E,d", [(1, 8, 64), (3, 37, 256), (2, 256, 6144)])
-def test_router_logits_within_fp32_bound(T, E, d):
-    """Against the exact fp64 dot: |err| <= (32 + 5 + d/1024) * 2^-24 * sum|x_i w_i|
-    (a <= 32-long fma chain per lane and segment, a 5-level tree, then the
-    segment totals added in order)."""
+def _exact_dot(x, w):
+    """The exact value of sum_i x_i w_i for fp32 inputs (math.fsum of products
+    that are exact in double), as a Python float."""
+    return math.fsum(float(a) * float(b) for a, b in zip(x.astype(np.float64), w.astype(np.float64)))
+
+
+@pytest.mark.parametrize("T,E,d", [(1, 8, 64), (3, 37, 256), (2, 24, 6144)])
+def test_router_logits_are_the_dot_rounded_once(T, E, d):
+    """Against the exact dot (fsum): the oracle's logit is within half an fp32
+    ulp of it plus the fp64 accumulation error (d * 2^-53 * sum|x_i w_i|), i.e.
+    the exact value rounded once; in practice it equals fp32(exact) almost
+    always (a double-rounding miss needs the fp64 sum within 2^-29 of a tie)."""
     rng = np.random.default_rng(T * 1000 + E)
     x = rng.normal(size=(T, d)).astype(np.float32)
     w = (rng.normal(size=(E, d)) / math.sqrt(d)).astype(np.float32)
-    got = oracle.router_logits(x, w).astype(np.float64)
-    exact = x.astype(np.float64) @ w.T.astype(np.float64)
-    bound = (32 + 5 + d / 1024) * 2.0 ** -24 * (np.abs(x).astype(np.float64) @ np.abs(w).T.astype(np.float64))
-    assert np.all(np.abs(got - exact) <= bound + 1e-30)
+    got = oracle.router_logits(x, w)
+    same = 0
+    for t in range(T):
+        for e in range(E):
+            ex = _exact_dot(x[t], w[e])
+            mag = float(np.abs(x[t].astype(np.float64)) @ np.abs(w[e].astype(np.float64)))
+            g = float(got[t, e])
+            half_ulp = float(np.spacing(np.float32(abs(ex)))) / 2
+            assert abs(g - ex) <= half_ulp + d * 2.0 ** -53 * mag + 1e-300, (t, e)
+            same += g == float(np.float32(ex))
+    assert same >= T * E - 1
 
 
 def test_router_logits_closed_forms():
@@ -106,28 +120,32 @@ def test_router_logits_closed_forms():
     assert np.array_equal(oracle.router_logits(xi, wi).astype(np.float64), exact)
 
 
-def test_router_logits_segment_order():
-    """Segments of 1024 are summed in ascending order after their own trees:
-    segment 0 totals 2^24, segment 1 totals 1.0 then segment 2 totals -2^24 -- in
-    that order the 1.0 is lost to rounding (2^24 + 1 = 2^24), so the logit is 0;
-    any order that cancels the big segments first would give 1."""
+def test_router_logits_cancellation_is_exact():
+    """Large terms that cancel do not swallow small ones: 2^24 + 1 - 2^24 = 1
+    (an fp32 running sum would give 0) wherever the terms sit, and 2^24 - 2^24
+    plus thirty ones is 30."""
     d = 3072
-    x = np.zeros((1, d), np.float32)
-    w = np.zeros((1, d), np.float32)
-    x[0, 0], w[0, 0] = 1.0, 2.0 ** 24
-    x[0, 1024], w[0, 1024] = 1.0, 1.0
-    x[0, 2048], w[0, 2048] = 1.0, -(2.0 ** 24)
-    assert oracle.router_logits(x, w)[0, 0] == 0.0
-
-
-def test_router_logits_tree_order():
-    """The fixed order: 32 lane sums, then pairwise xor-16..1 reductions.  Values
-    chosen so that a different association loses the small terms: lane 0 holds
-    2^24 and lane 16 holds -2^24, every other lane 1.0 -- the xor-16 step cancels
-    the big pair first, so the total is exactly 30."""
-    d = 32
-    x = np.ones((1, d), np.float32)
-    w = np.ones((1, d), np.float32)
-    w[0, 0] = 2.0 ** 24
-    w[0, 16] = -(2.0 ** 24)
+    for i0, i1, i2 in ((0, 1024, 2048), (5, 6, 7), (2048, 0, 1024)):
+        x = np.zeros((1, d), np.float32)
+        w = np.zeros((1, d), np.float32)
+        x[0, [i0, i1, i2]] = 1.0
+        w[0, i0], w[0, i1], w[0, i2] = 2.0 ** 24, 1.0, -(2.0 ** 24)
+        assert oracle.router_logits(x, w)[0, 0] == 1.0
+    x = np.ones((1, 32), np.float32)
+    w = np.ones((1, 32), np.float32)
+    w[0, 0], w[0, 16] = 2.0 ** 24, -(2.0 ** 24)
     assert oracle.router_logits(x, w)[0, 0] == 30.0
+
+
+def test_router_logits_products_are_not_rounded():
+    """(1 + 2^-12)^2 = 1 + 2^-11 + 2^-24 is not an fp32 number; with a second
+    product 2^-24 the exact dot is 1 + 2^-11 + 2^-23, which is.  Rounding the
+    first product to fp32 (a tie, to even: 1 + 2^-11) before adding would give
+    1 + 2^-11 instead."""
+    a = np.float32(1.0 + 2.0 ** -12)
+    b = np.float32(2.0 ** -12)
+    x = np.array([[a, b]], np.float32)
+    w = np.array([[a, b]], np.float32)
+    want = np.float32(1.0 + 2.0 ** -11 + 2.0 ** -23)
+    assert float(want) == 1.0 + 2.0 ** -11 + 2.0 ** -23
+    assert oracle.router_logits(x, w)[0, 0] == want
