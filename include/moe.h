@@ -42,8 +42,9 @@
  * (a cudaStream_t; NULL = legacy default stream), stateless and re-entrant as
  * long as concurrent calls use different workspaces.  Arguments are checked on
  * the host before anything is enqueued; nothing aborts or exits.  Device-side
- * argument faults (an expert index out of range in moe_ffn's inputs) set an
- * error word in the workspace, read by moe_check_device_error.
+ * argument faults (an expert index out of range in moe_ffn's inputs) and
+ * timed-out waits set bits in an error word in the workspace; kernels only ever
+ * set bits, and moe_check_device_error reads and clears them.
  * NaN or infinite inputs are unsupported.
  */
 #ifndef MOE_H
@@ -95,14 +96,17 @@ typedef struct {
 typedef enum { MOE_SCORE_SIGMOID = 0, MOE_SCORE_SQRT_SOFTPLUS = 1 } moe_score;
 
 /* flags */
-#define MOE_FLAG_DEBUG_TAPS 0x1u /* write sampled int32 block dots into the workspace */
+/* Write sampled int32 block dots into the workspace (moe_ws_layout.tap_gu /
+ * tap_dn) on every path, the fused decode kernel included, from the same dp4a
+ * or tensor-core results the outputs are built from; y is unchanged. */
+#define MOE_FLAG_DEBUG_TAPS 0x1u
 #define MOE_FLAG_FORCE_GEMV 0x2u /* every expert on the dp4a path (no tensor-core path) */
 #define MOE_FLAG_FORCE_TC 0x4u   /* every routed expert with >= 1 row on the tensor path */
 /* Failure-detection test only: the fused decode kernel never publishes its
  * routing result, so its bounded waits run out (~10 ms) and the call's error
  * word reports MOE_ERR_TIMEOUT; nothing faults and the context stays usable. */
 #define MOE_FLAG_TEST_STALL 0x8u
-/* Tracing: the fused decode kernel writes 24 uint64 per CTA (timestamps and
+/* Tracing: the fused decode kernel writes 32 uint64 per CTA (timestamps and
  * cycle counts of its waits and phases) into the workspace's trace region. */
 #define MOE_FLAG_TRACE 0x10u
 
@@ -140,10 +144,12 @@ typedef struct {
 /* The first MOE_WS_FIXED_BYTES of every workspace have a fixed layout: the
  * device error word at offset 0 and, from offset 256, MOE_SYNC_BYTES of
  * counters used by the fused decode kernel.  A workspace must be zero-filled
- * once after it is allocated; every call leaves the counters ready for the next
- * (most zeroed again, two counting calls), so one workspace can serve calls of
- * any desc and T.  After a call that reported MOE_ERR_TIMEOUT, zero-fill the
- * first MOE_WS_FIXED_BYTES again before reusing the workspace. */
+ * once after it is allocated; every call that completes leaves the counters
+ * ready for the next (most zeroed again, two counting calls), so one workspace
+ * can serve calls of any desc and T.  A call whose waits timed out may leave
+ * them mid-count: moe_check_device_error, reporting MOE_ERR_TIMEOUT, zeroes
+ * the whole fixed head, after which the workspace serves calls again.  Every
+ * byte past the fixed head is written by a call before that call reads it. */
 #define MOE_SYNC_BYTES ((size_t)16384)
 #define MOE_WS_FIXED_BYTES ((size_t)256 + MOE_SYNC_BYTES)
 
@@ -253,9 +259,10 @@ const char *moe_layer_path(const moe_desc *desc, uint32_t T);
  * gate/up tiles (128 features x 64 rows each) number at least the device's SM
  * count; with fewer, every expert of the call runs on the GEMV (a nearly empty
  * tensor kernel would leave most SMs idle).  MOE_FLAG_FORCE_TC sends every
- * expert to the tensor cores.  -1 when no expert of such a call can take the
- * tensor path (the fused decode path, 2-bit routed weights, dims not a
- * multiple of 256, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
+ * expert to the tensor cores.  2-bit routed weights take the same path: their
+ * codes are decoded to fp16 (2c - 3, exact) on the way to the MMA.  -1 when no
+ * expert of such a call can take the tensor path (the fused decode path, dims
+ * not a multiple of 256, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
 int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);
 
 /* Name of stage i of that path (what moe_layer_timed's events bracket),
@@ -367,7 +374,10 @@ moe_status moe_stream_layer(moe_cache *cache, uint32_t layer, const moe_desc *de
  *   E=256 / d=6144 / f=2048 layer with a shared expert that is T <= 32.
  * - All calls on a device share the array, which keeps the last call's
  *   contents; what must start at zero (error word, counters) is zero-filled
- *   at set-up and left zeroed by every call.  Calls that overlap on the GPU
+ *   at set-up and the counters are left zeroed by every call that completes.
+ *   The device error word (bad weight slots, timed-out waits) keeps its bits
+ *   until moe_check_device_error(NULL, 0, stream) reads and clears it; after a
+ *   timeout that call also zeroes the counters.  Calls that overlap on the GPU
  *   race on the array: serialise them.
  * - The first call on each device looks up the array's device address,
  *   caches it and zero-fills the array's head on that call's stream; make
@@ -380,8 +390,15 @@ moe_status moe_layer_noalloc(const moe_desc *desc, const moe_weights *wts, const
                              void *stream);
 
 /* Synchronise `stream` and read (then clear) the workspace's device error word
- * (the first 4 bytes of any workspace).
- * MOE_OK if no kernel flagged a fault; MOE_ERR_DEVICE_CHECK otherwise. */
+ * (the first 4 bytes of any workspace), which holds every bit the calls on that
+ * workspace set since it was last cleared.  MOE_OK if no kernel flagged a
+ * fault; MOE_ERR_TIMEOUT if a bounded wait gave up (the whole fixed head, the
+ * counters included, is then zeroed: ws_bytes >= MOE_WS_FIXED_BYTES);
+ * MOE_ERR_DEVICE_CHECK for bad routing inputs or weight slots.
+ * ws == NULL with ws_bytes == 0: the same for moe_layer_noalloc's static
+ * scratch on the current device (MOE_OK, with no CUDA call, before the first
+ * moe_layer_noalloc call there).  ws == NULL with ws_bytes != 0, or
+ * ws_bytes < 4: MOE_ERR_INVALID_ARG. */
 moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream);
 
 const char *moe_status_string(moe_status st);

@@ -150,6 +150,9 @@ struct FusedArgs {
   float *hs;
   float *o;
   int *plan;
+  // MOE_FLAG_DEBUG_TAPS: the int32 block dots of the tapped features and outputs
+  // (moe.h tap layout: tap_gu[slot][2][kNTap][d/32], tap_dn[slot][kNTap][fmax/32])
+  int32_t *tap_gu, *tap_dn;
   uint32_t *sync;  // see SyncView
   uint32_t *err;
   uint32_t c_rows, n_chunks, n_stages, stage_bytes;
@@ -328,6 +331,22 @@ __device__ __forceinline__ int dot16(const uint4 &a, const uint4 &b) {
   s = __dp4a((int)a.y, (int)b.y, s);
   s = __dp4a((int)a.z, (int)b.z, s);
   return __dp4a((int)a.w, (int)b.w, s);
+}
+
+// MOE_FLAG_DEBUG_TAPS: index j of tapped feature n of a row of `width` outputs
+// (n == tap_feature(j, width)), or -1
+__device__ __forceinline__ int tapped(uint32_t n, uint32_t width) {
+  int jt = -1;
+#pragma unroll
+  for (int j = 0; j < kNTap; ++j)
+    if (tap_feature((uint32_t)j, width) == n) jt = j;
+  return jt;
+}
+
+// the exact int32 dot of a 32-block whose two 16-byte halves lanes 2i and 2i+1
+// hold (chunk counts are even, so both lanes of a pair always run together)
+__device__ __forceinline__ int pair_sum(int v, int lane) {
+  return v + __shfl_xor_sync(3u << (lane & 30), v, 1);
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -567,8 +586,9 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
 // region, which is sized for both: they are read only before the consumer
 // barrier that ends the routing, and part[] is written only after it.
 // NT: token count known at compile time (1 or 2): the one-token kernel has no
-// second-row code.
-template <int NT>
+// second-row code.  TAPS: also store the block dots of the tapped features
+// (MOE_FLAG_DEBUG_TAPS), from the same dp4a results the outputs are built from.
+template <int NT, bool TAPS>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -621,8 +641,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
     tr[kTrStart] = global_ns();
   }
   if (tid == 0) {
-    // any timeout report comes >= 10 ms later, after every CTA has started
-    if (blockIdx.x == 0) *a.err = 0u;
+    // the error word is never cleared here: kernels only set bits in it and
+    // moe_check_device_error clears it (a clear by one CTA could erase a bit
+    // another CTA of the same call had already set)
     for (uint32_t i = 0; i < NS; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
@@ -1018,6 +1039,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         const float *xs0p = xs_s + tok0 * nb + half * nbh;
         const float *xs1p = xs_s + tok1 * nb + half * nbh;
         float g0 = 0.0f, u0 = 0.0f, g1 = 0.0f, u1 = 0.0f;
+        // taps: this warp's feature, if tapped; rows' tap entries of block b at
+        // tg0 / tg1 + b (gate), + kNTap * nb (up)
+        int jt = -1;
+        int32_t *tg0 = nullptr, *tg1 = nullptr;
+        if (TAPS) {
+          jt = tapped((uint32_t)(dsc.first + (int)fw), dsc.e == (int)a.E ? a.fs : a.f);
+          if (jt >= 0) {
+            tg0 = a.tap_gu + ((size_t)dsc.slot[0] * 2 * kNTap + jt) * nb + half * nbh;
+            tg1 = a.tap_gu + ((size_t)dsc.slot[kMaxT - 1] * 2 * kNTap + jt) * nb + half * nbh;
+          }
+        }
         if (NT == 1) {
           // x from registers: only the weights and their scales come from the stage
 #pragma unroll
@@ -1029,6 +1061,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const uint4 wg = ok ? lds16(gc + 16 * c) : z, wu = ok ? lds16(uc + 16 * c) : z;
               const int pg = dot16(wg, xr[i]), pu = dot16(wu, xr[i]);
               const uint32_t blk = ok ? c >> 1 : 0;
+              if (TAPS && jt >= 0) {
+                const int bg = pair_sum(pg, lane), bu = pair_sum(pu, lane);
+                if (ok && !(lane & 1)) {
+                  tg0[blk] = bg;
+                  tg0[blk + (size_t)kNTap * nb] = bu;
+                }
+              }
               const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
               if (ok) {
                 g0 = __fmaf_rn((float)pg, sg * xsr[i], g0);
@@ -1044,13 +1083,29 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           const float sg = half_bits_to_float(gsc[blk]), su = half_bits_to_float(usc[blk]);
           const uint4 x0 = lds16(x0p + 16 * c);
           const float xs0 = xs0p[blk];
-          g0 = __fmaf_rn((float)dot16(wg, x0), sg * xs0, g0);
-          u0 = __fmaf_rn((float)dot16(wu, x0), su * xs0, u0);
+          const int pg0 = dot16(wg, x0), pu0 = dot16(wu, x0);
+          g0 = __fmaf_rn((float)pg0, sg * xs0, g0);
+          u0 = __fmaf_rn((float)pu0, su * xs0, u0);
+          if (TAPS && jt >= 0) {
+            const int bg = pair_sum(pg0, lane), bu = pair_sum(pu0, lane);
+            if (!(lane & 1)) {
+              tg0[blk] = bg;
+              tg0[blk + (size_t)kNTap * nb] = bu;
+            }
+          }
           if (nr > 1) {
             const uint4 x1 = lds16(x1p + 16 * c);
             const float xs1 = xs1p[blk];
-            g1 = __fmaf_rn((float)dot16(wg, x1), sg * xs1, g1);
-            u1 = __fmaf_rn((float)dot16(wu, x1), su * xs1, u1);
+            const int pg1 = dot16(wg, x1), pu1 = dot16(wu, x1);
+            g1 = __fmaf_rn((float)pg1, sg * xs1, g1);
+            u1 = __fmaf_rn((float)pu1, su * xs1, u1);
+            if (TAPS && jt >= 0) {
+              const int bg = pair_sum(pg1, lane), bu = pair_sum(pu1, lane);
+              if (!(lane & 1)) {
+                tg1[blk] = bg;
+                tg1[blk + (size_t)kNTap * nb] = bu;
+              }
+            }
           }
         }
         }
@@ -1148,6 +1203,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           float acc[kDnRows][kMaxT];
 #pragma unroll
           for (int j = 0; j < kDnRows; ++j) acc[j][0] = acc[j][1] = 0.0f;
+          // taps: the tap index of each of the warp's rows (-1: not tapped)
+          int jtd[kDnRows];
+#pragma unroll
+          for (int j = 0; j < kDnRows; ++j) {
+            const int m = m0 + j * kConsumerWarps;
+            jtd[j] = TAPS && m < dsc.count ? tapped((uint32_t)(dsc.first + m), d) : -1;
+          }
           for (uint32_t c0 = 0; c0 < ncr; c0 += 32) {
             const uint32_t c = c0 + lane;
             const bool ok = c < ncr;
@@ -1169,8 +1231,22 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
               const float sw = live ? half_bits_to_float(scl[(size_t)m * kb + blk]) : 0.0f;
               // each lane scales its exact half-block sum (the halves meet in
               // the warp sum below)
-              acc[j][0] = __fmaf_rn((float)dot16(wd, h0), sw * hs0, acc[j][0]);
-              if (nr > 1) acc[j][1] = __fmaf_rn((float)dot16(wd, h1), sw * hs1, acc[j][1]);
+              const int p0 = dot16(wd, h0);
+              acc[j][0] = __fmaf_rn((float)p0, sw * hs0, acc[j][0]);
+              if (TAPS && jtd[j] >= 0) {
+                const int b0 = pair_sum(p0, lane);
+                if (ok && !(lane & 1))
+                  a.tap_dn[(slot0 * kNTap + jtd[j]) * (fmax / 32) + blk] = b0;
+              }
+              if (nr > 1) {
+                const int p1 = dot16(wd, h1);
+                acc[j][1] = __fmaf_rn((float)p1, sw * hs1, acc[j][1]);
+                if (TAPS && jtd[j] >= 0) {
+                  const int b1 = pair_sum(p1, lane);
+                  if (ok && !(lane & 1))
+                    a.tap_dn[(slot1 * kNTap + jtd[j]) * (fmax / 32) + blk] = b1;
+                }
+              }
             }
           }
 #pragma unroll
@@ -1276,7 +1352,7 @@ bool fused_plan(const Ctx &c, FusedPlan *fp) {
   const moe_desc &D = c.desc;
   if (c.T < 1 || c.T > (uint32_t)kMaxT) return false;
   if (D.routed_fmt != MOE_FMT_Q8_0) return false;
-  if (D.flags & (MOE_FLAG_DEBUG_TAPS | MOE_FLAG_FORCE_GEMV)) return false;
+  if (D.flags & MOE_FLAG_FORCE_GEMV) return false;
   if (D.flags & MOE_FLAG_FORCE_TC) return false;
   if (D.top_k > 32) return false;
   if (D.d % 256 || D.f % 256 || D.f_shared % 256) return false;
@@ -1391,7 +1467,12 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.stall_test = (D.flags & MOE_FLAG_TEST_STALL) ? 1 : 0;
   a.wait_cycles = a.stall_test ? kStallTestCycles : kWaitCycles;
   a.trace = (D.flags & MOE_FLAG_TRACE) ? (unsigned long long *)(c.ws + c.L.trace) : nullptr;
-  auto kern = c.T == 1 ? k_decode_fused<1> : k_decode_fused<2>;
+  const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
+  if (taps && (!c.L.tap_gu || !c.L.tap_dn)) return cudaErrorInvalidValue;
+  a.tap_gu = taps ? (int32_t *)(c.ws + c.L.tap_gu) : nullptr;
+  a.tap_dn = taps ? (int32_t *)(c.ws + c.L.tap_dn) : nullptr;
+  auto kern = c.T == 1 ? (taps ? k_decode_fused<1, true> : k_decode_fused<1, false>)
+                       : (taps ? k_decode_fused<2, true> : k_decode_fused<2, false>);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)fp.smem);
   if (e != cudaSuccess) return e;

@@ -21,6 +21,10 @@
 //          warp w reads TMEM lanes 32*(w%4).. (= features)
 // MAT = 2: gate and up, epilogue h = silu(g)*u requantised per 32 features;
 // MAT = 1: down, epilogue o.
+// RFMT: format of the routed experts' weights.  2-bit routed weights (code c in
+// {0..3} meaning 2c - 3) are decoded by the converters into fp16 as exactly as
+// int8 codes are, so the MMA computes the same exact integer block dots; the
+// shared expert is always Q8_0.
 #include <cuda.h>
 #include <string.h>
 
@@ -190,6 +194,39 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t 
   __half2 b = __hsub2(*reinterpret_cast<__half2 *>(&hi), k);
   lo = *reinterpret_cast<uint32_t *>(&a);
   hi = *reinterpret_cast<uint32_t *>(&b);
+}
+
+// prmt.b32 in its generic mode: byte n of the result is byte (c >> 4n) & 7 of
+// {b, a} -- or, when bit 4n+3 of c is set, that byte's sign bit replicated
+// (the CUDA intrinsic __byte_perm ignores that bit)
+__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// 16 2-bit codes (byte b: codes 4b..4b+3, LSB first) -> eight half2 of 2c - 3,
+// in K order: out[2b] = codes (4b, 4b+1), out[2b+1] = codes (4b+2, 4b+3).
+// t_i holds code 4b+i in the low bits of byte b, under 0x3C; a byte permute puts
+// each code's byte (0x3C | c) above a zero byte (the sign-replicated 0x3C|c),
+// which is the fp16 1 + c/4; then 8 * (1 + c/4) - 11 = 2c - 3, exact.
+__device__ __forceinline__ void q2x16_to_h2x8(uint32_t w, uint32_t (&out)[8]) {
+  uint32_t t[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) t[i] = ((w >> (2 * i)) & 0x03030303u) | 0x3C3C3C3Cu;
+  const __half2 k8 = __halves2half2(__ushort_as_half(0x4800), __ushort_as_half(0x4800));   // 8
+  const __half2 km11 = __halves2half2(__ushort_as_half(0xC980), __ushort_as_half(0xC980));  // -11
+#pragma unroll
+  for (int b = 0; b < 4; ++b) {
+    // bytes: [sign(t_lo.b) = 0, t_lo.b, sign(t_hi.b) = 0, t_hi.b]
+    const uint32_t sel = (8u | b) | ((uint32_t)b << 4) | ((8u | b) << 8) | ((4u + b) << 12);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v = prmt_sx(t[2 * h], t[2 * h + 1], sel);
+      __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&v), k8, km11);
+      out[2 * b + h] = *reinterpret_cast<uint32_t *>(&r);
+    }
+  }
 }
 
 // the two epilogue warps that read TMEM lane quarter q (one of each half) meet at
@@ -450,7 +487,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
 }
 #undef ACC
 
-template <int MAT, bool TAPS>
+template <int MAT, bool TAPS, int RFMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_expert_tc(const TcArgs a, const __grid_constant__ TcMaps maps) {
   extern __shared__ __align__(1024) uint8_t tsm_raw[];
@@ -462,8 +499,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int total = MAT == 2 ? P.hdr[6] : P.hdr[7];
   if (total == 0) return;  // no tensor-core tiles in this call's plan
   const uint32_t KS = a.K / kBK;  // stages per tile
-  // stage layout: [A16 per matrix 16K][B 8K][A8 per matrix 8K]
+  // stage layout: [A16 per matrix 16K][B 8K][A8 per matrix 8K]; a 2-bit tile
+  // stages 16 code bytes per row (kA2 per matrix) at the start of each A8 area
   constexpr uint32_t kA16 = kBM * kBK * 2, kB16 = kBN * kBK * 2, kA8 = kBM * kBK;
+  constexpr uint32_t kA2 = kBM * kBK / 4;
   uint8_t *sc_ring = tsm + (size_t)NS * a.stage_bytes;  // [kScSlots][kScSlotBytes]
   uint8_t *ctrl = sc_ring + (size_t)kScSlots * kScSlotBytes;
   uint64_t *ld_full = (uint64_t *)ctrl;          // [NS]
@@ -553,10 +592,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           uint8_t *st = tsm + (size_t)s * a.stage_bytes;
-          bar_expect(&ld_full[s], MAT * kA8 + kB16);
+          const bool q2 = RFMT == MOE_FMT_Q2S && !sh;  // 2-bit codes: K/4 bytes a row
+          bar_expect(&ld_full[s], MAT * (q2 ? kA2 : kA8) + kB16);
           for (int mi = 0; mi < MAT; ++mi)
             tma_2d(st + MAT * kA16 + kB16 + mi * kA8, sh ? &maps.sw[mi] : &maps.w[mi],
-                   (int)(ks * kBK), wrow, &ld_full[s]);
+                   (int)(ks * (q2 ? kBK / 4 : kBK)), wrow, &ld_full[s]);
           tma_2d(st + MAT * kA16, &maps.act, (int)(ks * kBK), t.slot0 + t.n0, &ld_full[s]);
         }
       }
@@ -612,6 +652,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = tid - 64;
     uint32_t g = 0;
     for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
+      // 2-bit routed tile (the shared expert is Q8_0)
+      const bool q2 = RFMT == MOE_FMT_Q2S && tc_tile<MAT>(P, a, tile).e != (int)a.E;
       for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
         const uint32_t s = g % NS, use = g / NS;
         const long long tw = clock64();
@@ -623,6 +665,28 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         uint8_t *st = tsm + (size_t)s * a.stage_bytes;
+        if (q2) {
+          // row r's 16 code bytes (rows 16 B apart: a quarter-warp reads 128
+          // contiguous bytes) -> 8 fp16 chunks; chunk j lands at position
+          // j ^ (r&7) of its swizzled row (distinct over a quarter-warp)
+          for (int mi = 0; mi < MAT; ++mi) {
+            const uint4 w = *(const uint4 *)(st + MAT * kA16 + kB16 + mi * kA8 + r * (kBK / 4));
+            uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
+            const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {  // codes 16v .. 16v+15 = chunks 2v, 2v+1
+              uint32_t h[8];
+              q2x16_to_h2x8(wv[v], h);
+              const int j0 = 2 * v, j1 = 2 * v + 1;
+              *(uint4 *)(dst_row + ((j0 ^ (r & 7)) << 4)) = make_uint4(h[0], h[1], h[2], h[3]);
+              *(uint4 *)(dst_row + ((j1 ^ (r & 7)) << 4)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) bar_arrive(&a_ready[s]);
+          continue;
+        }
         for (int mi = 0; mi < MAT; ++mi) {
           const uint4 *src = (const uint4 *)(st + MAT * kA16 + kB16 + mi * kA8 + r * kBK);
           uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
@@ -764,9 +828,9 @@ bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MAT, bool TAPS>
+template <int MAT, bool TAPS, int RFMT>
 cudaError_t run_tc(const Ctx &c, const TcArgs &a, const TcMaps &maps, size_t smem) {
-  auto kern = k_expert_tc<MAT, TAPS>;
+  auto kern = k_expert_tc<MAT, TAPS, RFMT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   kern<<<c.sm_count, kTcThreads, smem, c.stream>>>(a, maps);
@@ -775,9 +839,10 @@ cudaError_t run_tc(const Ctx &c, const TcArgs &a, const TcMaps &maps, size_t sme
 
 }  // namespace
 
-// the scale rows (K/32 fp16) of every matrix must be whole 16-byte TMA rows
+// the scale rows (K/32 fp16) of every matrix must be whole 16-byte TMA rows (and
+// a 2-bit code row, K/4 bytes, a multiple of 16 bytes: K % 256 covers both)
 bool tc_supported(const moe_desc &D) {
-  if (D.routed_fmt != MOE_FMT_Q8_0) return false;
+  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S) return false;
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   return encode_fn() != nullptr;
 }
@@ -785,7 +850,7 @@ bool tc_supported(const moe_desc &D) {
 // can any expert of a T-token call land on the tensor path (workspace sizing)?
 bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.flags & MOE_FLAG_FORCE_GEMV) return false;
-  if (D.routed_fmt != MOE_FMT_Q8_0) return false;
+  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S) return false;
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T > kTcMinRows;
 }
@@ -824,6 +889,9 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace ? (unsigned long long *)(c.ws + c.L.trace)
                                                      : nullptr;
   const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
+  const bool q2 = D.routed_fmt == MOE_FMT_Q2S;
+  // routed code planes: int8 [rows][K], box 64 x 128; 2-bit [rows][K/4] bytes, box 16 x 128
+  const uint32_t qdiv = q2 ? 4 : 1;
   bool ok = true;
   if (mat == 2) {
     a.K = D.d;
@@ -838,10 +906,10 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     a.hperm = (__half *)(c.ws + c.L.hperm);
     a.tap = taps ? (int32_t *)(c.ws + c.L.tap_gu) : nullptr;
     a.tap_nb = D.d / 32;
-    ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.gate.q, D.d,
-                   (uint64_t)c.wexp * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
-    ok &= make_map(&maps.w[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.up.q, D.d,
-                   (uint64_t)c.wexp * D.f, D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.gate.q, D.d / qdiv,
+                   (uint64_t)c.wexp * D.f, D.d / qdiv, kBK / qdiv, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&maps.w[1], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.up.q, D.d / qdiv,
+                   (uint64_t)c.wexp * D.f, D.d / qdiv, kBK / qdiv, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared) {
       ok &= make_map(&maps.sw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.s_gate.q, D.d, D.f_shared,
                      D.d, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -878,8 +946,8 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
     a.o = (float *)(c.ws + c.L.o);
     a.tap = taps ? (int32_t *)(c.ws + c.L.tap_dn) : nullptr;
     a.tap_nb = c.fmax / 32;
-    ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.down.q, D.f,
-                   (uint64_t)c.wexp * D.d, D.f, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok &= make_map(&maps.w[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.down.q, D.f / qdiv,
+                   (uint64_t)c.wexp * D.d, D.f / qdiv, kBK / qdiv, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (D.f_shared)
       ok &= make_map(&maps.sw[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, c.wts.s_down.q, D.f_shared,
                      D.d, D.f_shared, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -912,9 +980,18 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   // alignment slack | stages | scale ring | barriers and flags | split-K partial sums
   const size_t smem = 1024 + (size_t)a.n_stages * stage + (size_t)kScSlots * kScSlotBytes + 1024 +
                       (size_t)mat * kBM * 33 * 4;
+  if (q2) {
+    if (mat == 2)
+      return taps ? run_tc<2, true, MOE_FMT_Q2S>(c, a, maps, smem)
+                  : run_tc<2, false, MOE_FMT_Q2S>(c, a, maps, smem);
+    return taps ? run_tc<1, true, MOE_FMT_Q2S>(c, a, maps, smem)
+                : run_tc<1, false, MOE_FMT_Q2S>(c, a, maps, smem);
+  }
   if (mat == 2)
-    return taps ? run_tc<2, true>(c, a, maps, smem) : run_tc<2, false>(c, a, maps, smem);
-  return taps ? run_tc<1, true>(c, a, maps, smem) : run_tc<1, false>(c, a, maps, smem);
+    return taps ? run_tc<2, true, MOE_FMT_Q8_0>(c, a, maps, smem)
+                : run_tc<2, false, MOE_FMT_Q8_0>(c, a, maps, smem);
+  return taps ? run_tc<1, true, MOE_FMT_Q8_0>(c, a, maps, smem)
+              : run_tc<1, false, MOE_FMT_Q8_0>(c, a, maps, smem);
 }
 
 }  // namespace moe

@@ -396,15 +396,29 @@ moe_status moe_router_logits(const moe_desc *desc, const float *w_router, const 
 const char *moe_last_error(void) { return t_last_error; }
 
 moe_status moe_check_device_error(void *ws, size_t ws_bytes, void *stream) {
-  if (!ws || ws_bytes < sizeof(uint32_t)) return MOE_ERR_INVALID_ARG;
+  if (!ws) {
+    // moe_layer_noalloc's static scratch on the current device (none before the
+    // first such call there: then no kernel can have flagged anything)
+    if (ws_bytes != 0) return MOE_ERR_INVALID_ARG;
+    ws = noalloc_scratch_current();
+    if (!ws) return MOE_OK;
+    ws_bytes = MOE_NOALLOC_SCRATCH_BYTES;
+  }
+  if (ws_bytes < sizeof(uint32_t)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = (cudaStream_t)stream;
   uint32_t word = 0;
-  if (cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaError_t e = cudaMemcpyAsync(&word, ws, sizeof word, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e);
   if (word == 0) return MOE_OK;
-  if (cudaMemsetAsync(ws, 0, sizeof word, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the calls on `stream` have finished.  After a timeout the fused decode
+  // kernel's counters may be left mid-count: zero the whole fixed head so the
+  // workspace serves the next call; otherwise the error word alone
+  const size_t clear =
+      (word & kErrTimeout) && ws_bytes >= MOE_WS_FIXED_BYTES ? MOE_WS_FIXED_BYTES : sizeof word;
+  e = cudaMemsetAsync(ws, 0, clear, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return from_cuda(e);
   return (word & kErrTimeout) ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE_CHECK;
 }
 

@@ -317,6 +317,9 @@ moe_status layer_on_workspace(const moe_desc *desc, const moe_weights *wts, cons
                               const float *logits, const float *bias, uint32_t T, float *y,
                               void *ws, size_t ws_bytes, void *stream);
 void set_last_error(const char *msg);
+// moe_layer_noalloc's static scratch on the current device, or null when no such
+// call has set it up there (moe_noalloc.cu); never touches CUDA before that
+void *noalloc_scratch_current();
 
 // expert cache internals for moe_stream_layer (expert_cache.cu)
 bool cache_layer_routed(const moe_cache *c, uint32_t layer, moe_weights *w);

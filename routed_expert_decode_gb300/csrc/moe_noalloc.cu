@@ -14,10 +14,12 @@
 //    MOE_ERR_WORKSPACE before anything is launched;
 //  * every call on a device uses the same array and it keeps whatever the last
 //    call left there.  What must start at zero -- the error word and the fused
-//    decode kernel's counters -- is zero-filled at set-up and left zeroed by
-//    every call (the error word is reset at the start of each call); every
-//    other region is written before it is read.  Calls that overlap on the GPU
-//    (two streams, or two host threads) race on the array: serialise them;
+//    decode kernel's counters -- is zero-filled at set-up; the counters are left
+//    zeroed by every call that completes, and the error word keeps the bits any
+//    call set until moe_check_device_error(NULL, 0, stream) reads and clears it
+//    (after a timeout that also zeroes the counters).  Every other region is
+//    written before it is read.  Calls that overlap on the GPU (two streams, or
+//    two host threads) race on the array: serialise them;
 //  * the first call on each device looks up the array's device address
 //    (cudaGetSymbolAddress, with that device current), caches it and zero-fills
 //    the array's fixed head on the call's stream; make that first call before
@@ -36,6 +38,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kScratchBytes];
 
 std::mutex g_scratch_mu;
 void *g_scratch_addr[kMaxDevices] = {};
+bool g_any_setup = false;  // some device has been set up (read under the mutex)
 
 // Device address of g_noalloc_scratch on the current device (looked up once).
 // The first lookup on a device also zero-fills the workspace's fixed head (the
@@ -53,12 +56,26 @@ cudaError_t scratch_address(void **out, cudaStream_t stream) {
     e = cudaMemsetAsync(p, 0, MOE_WS_FIXED_BYTES, stream);
     if (e != cudaSuccess) return e;
     g_scratch_addr[dev] = p;
+    g_any_setup = true;
   }
   *out = g_scratch_addr[dev];
   return cudaSuccess;
 }
 
 }  // namespace
+
+namespace moe {
+// The array's address on the current device for moe_check_device_error, or null
+// when no moe_layer_noalloc call has set it up there.  Before the first set-up
+// on any device this makes no CUDA call at all.
+void *noalloc_scratch_current() {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_any_setup) return nullptr;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  return g_scratch_addr[dev];
+}
+}  // namespace moe
 
 extern "C" moe_status moe_layer_noalloc(const moe_desc *desc, const moe_weights *wts,
                                         const float *x, const float *logits, const float *bias,

@@ -201,10 +201,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   const int tid = threadIdx.x;
   const uint32_t R = T * k;
   PlanView P(plan, E);
-  if (tid == 0) {
-    *err = 0u;
-    bad = (off[0] != 0 || off[E] != (int)R) ? 1 : 0;
-  }
+  if (tid == 0) bad = (off[0] != 0 || off[E] != (int)R) ? 1 : 0;
   __syncthreads();
   for (uint32_t e = tid; e < E; e += kPlanThreads)
     if (off[e + 1] < off[e]) bad = 1;

@@ -285,7 +285,8 @@ def layer_timed(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, even
 def layer_noalloc(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, stream=None):
     """moe_layer_noalloc: the layer without a workspace, for callers that cannot
     allocate device memory; scratch comes from the library's fixed 16 MiB device
-    array (calls on one device must not overlap)."""
+    array (calls on one device must not overlap).  Its device error word is read
+    (and cleared) by check_device_error(None)."""
     st = lib().moe_layer_noalloc(ctypes.byref(desc), ctypes.byref(weights),
                                  _dev_ptr(x, torch.float32, "x"),
                                  _dev_ptr(logits, torch.float32, "logits"),
@@ -418,7 +419,11 @@ def stage_names(desc: MoeDesc, T: int) -> list:
 
 
 def check_device_error(ws, stream=None) -> int:
-    """Returns the moe_status of the workspace's device error word (and clears it)."""
+    """Returns the moe_status of the workspace's device error word (and clears
+    it; after a timeout also the workspace's counters).  ws=None: the static
+    scratch of layer_noalloc on the current device."""
+    if ws is None:
+        return int(lib().moe_check_device_error(None, 0, _stream(stream)))
     return int(lib().moe_check_device_error(_dev_ptr(ws, torch.uint8, "ws"), ws.numel(),
                                             _stream(stream)))
 

@@ -130,7 +130,12 @@ def test_host_checks_before_launch(moe):
                          need, None) == 1
     assert lib.moe_ffn(ctypes.byref(d), ctypes.byref(good), fake, 4, None, fake, fake, fake,
                        fake, fake, fake, need, None) == 1
-    assert lib.moe_check_device_error(None, 0, None) == 1
+    # a NULL workspace names moe_layer_noalloc's static scratch: before any such
+    # call nothing can have been flagged (and no CUDA call is made); a NULL
+    # workspace with a size is a bad argument
+    assert lib.moe_check_device_error(None, 0, None) == 0
+    assert lib.moe_check_device_error(None, 4, None) == 1
+    assert lib.moe_check_device_error(fake, 2, None) == 1
 
 
 def test_workspace_layout_regions(moe):

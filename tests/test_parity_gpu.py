@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import synth
-from parity import run_case, device_layer
+from parity import run_case, device_layer, poison_workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -199,9 +199,24 @@ def test_device_fill_matches_host_generator(gpu):
 
 # ---------------------------------------------------------------- full-size layers, sampled
 def test_decode_t1_full_size(gpu):
+    """The headline decode step on the fused kernel, with its block-dot taps:
+    gate/up and down int32 block dots bit-exact against the oracle."""
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(synth.GLM_LAYER, gpu)
+    assert moe.layer_path(layer.desc(moe.FLAG_DEBUG_TAPS), 1) == "fused_decode"
     for seed in (0, 1, 2):
         rep = run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu)
         print("decode_t1", seed, rep)
+
+
+def test_decode_t1_full_size_multi_kernel(gpu):
+    """The same tokens through the multi-kernel (dp4a GEMV) path."""
+    from routed_expert_decode_gb300 import moe
+
+    for seed in (0, 1):
+        rep = run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu, flags=moe.FLAG_FORCE_GEMV)
+        print("decode_t1 gemv", seed, rep)
 
 
 def test_small_batch_t2_t16_full_size(gpu):
@@ -215,7 +230,15 @@ def test_prefill_t512_full_size(gpu):
 
 
 def test_q2_t64_full_size(gpu):
+    """The 2-bit layer at T=64 (auto dispatch: the shared expert and the 2-bit
+    experts with more than 4 rows on the tensor cores, when they fill the SMs)."""
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(synth.Q2_LAYER, gpu)
+    assert moe.tc_min_rows(layer.desc(), 64) == 4
     print("q2_t64", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 33, 63]))
+    print("q2_t64 gemv", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 63],
+                                  flags=moe.FLAG_FORCE_GEMV))
 
 
 # ---------------------------------------------------------------- fused decode kernel (T <= 2)
@@ -234,8 +257,9 @@ def test_fused_small_layers(gpu, name, spec, T):
 
     layer = device_layer(spec, gpu)
     assert moe.layer_path(layer.desc(), T) == "fused_decode"
+    assert moe.layer_path(layer.desc(moe.FLAG_DEBUG_TAPS), T) == "fused_decode"
     for seed in (3, 4):
-        rep = run_case(spec, T, seed=seed, device=gpu, check_taps=False)
+        rep = run_case(spec, T, seed=seed, device=gpu)
         print(name, seed, rep)
 
 
@@ -246,18 +270,18 @@ def test_fused_decode_full_size(gpu):
     assert moe.layer_path(layer.desc(), 1) == "fused_decode"
     assert moe.layer_path(layer.desc(), 2) == "fused_decode"
     assert moe.layer_path(layer.desc(), 3) == "multi_kernel"
+    assert moe.layer_path(layer.desc(moe.FLAG_DEBUG_TAPS), 2) == "fused_decode"
     for seed in (0, 1, 2, 3):
-        print("fused t1", seed, run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu,
-                                         check_taps=False))
+        print("fused t1", seed, run_case(synth.GLM_LAYER, 1, seed=seed, device=gpu))
     for seed in (0, 1):
-        print("fused t2", seed, run_case(synth.GLM_LAYER, 2, seed=seed, device=gpu,
-                                         check_taps=False))
+        print("fused t2", seed, run_case(synth.GLM_LAYER, 2, seed=seed, device=gpu))
 
 
 def test_fused_matches_multi_kernel_and_repeats(gpu):
     """The fused kernel and the multi-kernel path agree (same routing, same
-    int8 codes, y within fp32 summation order), and the fused kernel is
-    bit-identical from call to call."""
+    int8 codes, y within fp32 summation order), the fused kernel is
+    bit-identical from call to call, and its tapped variant (block dots stored
+    on the side) gives the untapped kernel's y bit for bit."""
     from routed_expert_decode_gb300 import moe
 
     spec = synth.GLM_LAYER
@@ -270,6 +294,8 @@ def test_fused_matches_multi_kernel_and_repeats(gpu):
         ya, ia, xa = a.y.clone(), a.idx.clone(), a.xq.clone()
         b = layer.forward(*args)
         assert torch.equal(b.y, ya)
+        tp = layer.forward(*args, taps=True)
+        assert torch.equal(tp.y, ya) and torch.equal(tp.hq, a.hq)
         m = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV)
         torch.cuda.synchronize()
         assert torch.equal(m.idx, ia) and torch.equal(m.xq, xa)
@@ -307,6 +333,11 @@ TC_CASES = [
     ("tc_small_forced", _spec(E=16, k=4, d=256, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 9),
     ("tc_ragged_rows", _spec(E=8, k=2, d=512, f=256, f_shared=256, s=1.0), 70),
     ("tc_d6144", _spec(E=16, k=4, d=6144, f=256, f_shared=256, s=2.5), 33),
+    # 2-bit routed weights decoded to fp16 by the converters; the shared expert Q8_0
+    ("tc_q2_forced", _spec(E=16, k=4, d=512, f=256, f_shared=256, fmt=1, s=1.0,
+                           zipf_beta=0.4), 9),
+    ("tc_q2_d4096", _spec(E=24, k=8, d=4096, f=512, f_shared=512, fmt=1, s=1.0), 33),
+    ("tc_q2_noshared", _spec(E=8, k=2, d=1024, f=768, f_shared=0, fmt=1, s=1.0), 21),
 ]
 
 
@@ -433,3 +464,31 @@ def test_tensor_core_plan_lists_widest_experts_first(gpu):
         gu += mt * ((r + 63) // 64)
         dn += dt * ((r + 63) // 64)
     assert plan[tc_tile_gu + V] == gu == plan[6] and plan[tc_tile_dn + V] == dn == plan[7]
+
+
+# ---------------------------------------------------------------- uninitialised-memory guard
+POISON = [
+    ("fused_t1", synth.GLM_LAYER_E32, 1, 0),
+    ("fused_t2", synth.GLM_LAYER_E32, 2, 0),
+    ("gemv_t16", synth.GLM_LAYER_E32, 16, 0),
+    ("tc_forced_t40", _spec(E=16, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 40, "tc"),
+    ("tc_auto_t512", synth.GLM_LAYER_E32, 512, 0),
+    ("q2_t13", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=1, zipf_beta=0.4), 13, 0),
+]
+
+
+@pytest.mark.parametrize("name,spec,T,fl", POISON, ids=[p[0] for p in POISON])
+def test_poisoned_workspace(gpu, name, spec, T, fl):
+    """Every workspace byte past the fixed head set to 0xFF before the call: a
+    kernel that reads scratch it has not written (the class of bug behind the
+    pages' streaming regressions: NeutronStar glm-local README, "Latent
+    CUDA-streaming bugs") would see NaN floats and out-of-range indices and fail
+    parity.  Run twice, so the second call also starts from poison, not from the
+    first call's leftovers."""
+    from routed_expert_decode_gb300 import moe
+
+    flags = moe.FLAG_FORCE_TC if fl == "tc" else 0
+    sample = None if T <= 16 else [0, T // 2, T - 1]
+    for seed in (31, 32):
+        rep = run_case(spec, T, seed=seed, device=gpu, flags=flags, sample=sample, poison=True)
+        print(name, seed, rep)

@@ -4,8 +4,9 @@ Routed experts served from an HBM cache over pinned host memory (the pages'
 expert streaming with an LFU cache and router-lookahead prefetch: NeutronStar
 glm-local README, "SSD streaming optimizations") must give the same layer output,
 bit for bit, as the same experts resident in HBM: the kernels read the same
-bytes through the expert -> slot table (moe_weights.expert_slot).  The resident
-layer is itself pinned to the oracle by the parity tests."""
+bytes through the expert -> slot table (moe_weights.expert_slot); and a streamed
+decode token and a streamed 16-row batch are also compared with the CPU oracle
+directly."""
 import dataclasses
 
 import numpy as np
@@ -13,7 +14,7 @@ import pytest
 import torch
 
 import synth
-from parity import device_layer
+from parity import compare_with_oracle, device_layer
 from routed_expert_decode_gb300 import moe
 
 pytestmark = pytest.mark.gpu
@@ -80,10 +81,13 @@ def test_slot_table_gives_identical_output(gpu, T, flags):
     assert torch.equal(y_ref, y_slot)
 
 
-@pytest.mark.parametrize("T", [1, 6])
+@pytest.mark.parametrize("T", [1, 2, 6])
 def test_selected_expert_outside_the_slots_is_a_device_error(gpu, T):
     """A selected expert whose slot is >= n_slots fails the device check; no
-    weight row outside the slots is read (the kernels plan no routed work)."""
+    weight row outside the slots is read (the kernels plan no routed work).
+    On the fused decode kernel (T <= 2) every CTA routes and may flag the bad
+    slot before any other has started, so the call is repeated 50 times: the
+    flag must never be lost."""
     spec = _spec()
     layer = device_layer(spec, gpu)
     desc = layer.desc()
@@ -95,10 +99,12 @@ def test_selected_expert_outside_the_slots_is_a_device_error(gpu, T):
     keep["table"][int(picks[0, 0])] = n_slots  # out of range for a selected expert
     ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
     y = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
-    moe.layer(desc, w_slot, torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
-              torch.from_numpy(synth.bias(spec)).to(gpu), y, ws)
-    torch.cuda.synchronize()
-    assert moe.STATUS_NAMES[moe.check_device_error(ws)] == "MOE_ERR_DEVICE_CHECK"
+    assert moe.layer_path(desc, T) == ("fused_decode" if T <= 2 else "multi_kernel")
+    for _ in range(50 if T <= 2 else 1):
+        moe.layer(desc, w_slot, torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
+                  torch.from_numpy(synth.bias(spec)).to(gpu), y, ws)
+        torch.cuda.synchronize()
+        assert moe.STATUS_NAMES[moe.check_device_error(ws)] == "MOE_ERR_DEVICE_CHECK"
     # the workspace stays usable
     keep["table"][int(picks[0, 0])] = int(perm[int(picks[0, 0])])
     moe.layer(desc, w_slot, torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu),
@@ -222,4 +228,44 @@ def test_streamed_full_size_decode_matches_resident(gpu):
             assert torch.equal(y, y_ref), f"token {tok} layer {l}"
     st = cache.stats()
     assert st["misses"] > 0 and st["lookups"] == st["hits"] + st["misses"]
+    cache.close()
+
+
+@pytest.mark.parametrize("T", [1, 16])
+def test_streamed_layer_matches_oracle(gpu, T):
+    """The decode-shaped layer (d=6144, f=2048, shared 2048, Q8_0; 32 experts)
+    with its routed experts in pinned host memory, served through a cold HBM
+    cache: idx, off, perm, xq exact and y within tolerance against the CPU
+    oracle (T=1 on the fused kernel, T=16 on the multi-kernel path)."""
+    spec = synth.GLM_LAYER_E32
+    layer = device_layer(spec, gpu)
+    host_t = {n + sfx: layer.tensors[n + sfx].cpu().pin_memory()
+              for n in ROUTED for sfx in ("_q", "_s")}
+    n_slots = spec.E
+    arena_t = {k: torch.zeros((n_slots,) + tuple(v.shape[1:]), dtype=v.dtype, device=gpu)
+               for k, v in host_t.items()}
+    table = torch.full((1, spec.E), -1, dtype=torch.int32, device=gpu)
+    desc = layer.desc()
+    cache = moe.ExpertCache(desc, [_mats(host_t, ROUTED)], _mats(arena_t, ROUTED), n_slots,
+                            table.data_ptr())
+    shared = moe.MoeWeights()
+    for n in ("s_gate", "s_up", "s_down"):
+        setattr(shared, n, getattr(layer.weights, n))
+    bias = synth.bias(spec)
+    ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
+    for seed in (61, 62):
+        logits, x = synth.token_inputs(spec, seed, T)
+        y = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
+        moe.stream_layer(cache, 0, desc, shared, torch.from_numpy(x).to(gpu),
+                         torch.from_numpy(logits).to(gpu), torch.from_numpy(bias).to(gpu), y, ws)
+        torch.cuda.synchronize()
+        assert moe.check_device_error(ws) == 0
+        v = layer.views(ws, T)
+        g = {k: (t.cpu().numpy() if isinstance(t, torch.Tensor) else t) for k, t in v.items()}
+        g["y"] = y.cpu().numpy()
+        rep = compare_with_oracle(spec, T, x, logits, bias, g,
+                                  sample=None if T == 1 else [0, 7, 15])
+        print("streamed", T, seed, rep)
+    st = cache.stats()
+    assert st["misses"] > 0
     cache.close()

@@ -2,7 +2,8 @@
 (an engine that reserved its whole device arena up front, plugins and plain-C
 hosts without an allocator, paths that must not touch the allocator).  Its
 scratch is the library's fixed 16 MiB device array, so these checks call it
-through the C ABI and compare it with moe_layer on a caller workspace.
+through the C ABI, compare it bit for bit with moe_layer on a caller
+workspace, and read its device error word with moe_check_device_error(NULL).
 
 This file is collected last on purpose (its name sorts last)."""
 import numpy as np
@@ -31,6 +32,8 @@ def _layer(spec, dev):
                      zipf_beta=0.4), 5),
 ], ids=["e64_t9", "decode_shape_t1", "decode_shape_t16", "q2_t5"])
 def test_noalloc_matches_workspace_entry_twice(gpu, spec, T):
+    """Same kernels, same inputs: the output equals moe_layer's bit for bit, on
+    two calls in a row, and the static scratch's error word stays clear."""
     from routed_expert_decode_gb300 import moe
 
     layer = _layer(spec, gpu)
@@ -44,11 +47,42 @@ def test_noalloc_matches_workspace_entry_twice(gpu, spec, T):
         moe.layer(desc, layer.weights, x_d, l_d, bias, y_ref, ws)
         y = torch.full((T, spec.d), float("nan"), dtype=torch.float32, device=gpu)
         moe.layer_noalloc(desc, layer.weights, x_d, l_d, bias, y)
+        assert moe.check_device_error(None) == 0
         torch.cuda.synchronize()
         a, b = y.cpu().numpy(), y_ref.cpu().numpy()
         assert np.isfinite(a).all()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
         err = np.abs(a - b).max(axis=1) / np.abs(b).max(axis=1)
         assert err.max() <= Y_TOL, err.max()
+
+
+def test_noalloc_reports_device_errors_and_recovers(gpu):
+    """A caller with no workspace can still read the device error word: a
+    stalled fused call (the failure-detection switch: its bounded waits run
+    out, nothing faults) reports MOE_ERR_TIMEOUT through
+    check_device_error(None), which also zeroes the scratch's counters, so the
+    next call on the same static scratch is correct again."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = synth.LayerSpec("na_stall", E=64, k=4, d=512, f=256, f_shared=256, fmt=0, s=2.5,
+                           zipf_beta=0.4)
+    layer = _layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 5, 1)
+    x_d, l_d = torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu)
+    bias = torch.from_numpy(synth.bias(spec)).to(gpu)
+    stall = layer.desc(moe.FLAG_TEST_STALL)
+    assert moe.layer_path(stall, 1) == "fused_decode"
+    y = torch.empty((1, spec.d), dtype=torch.float32, device=gpu)
+    moe.layer_noalloc(stall, layer.weights, x_d, l_d, bias, y)
+    assert moe.check_device_error(None) == 5  # MOE_ERR_TIMEOUT
+    ws = torch.zeros(moe.workspace_size(layer.desc(), 1), dtype=torch.uint8, device=gpu)
+    y_ref = torch.empty_like(y)
+    moe.layer(layer.desc(), layer.weights, x_d, l_d, bias, y_ref, ws)
+    for _ in range(2):
+        moe.layer_noalloc(layer.desc(), layer.weights, x_d, l_d, bias, y)
+        assert moe.check_device_error(None) == 0
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref)
 
 
 def test_noalloc_rejects_oversized_batches(gpu):
