@@ -506,6 +506,8 @@ def run_ours(args):
         "steps": K,
         "warmup": W,
         "ms_per_step": round(ms_per_step, 5),
+        "ms_per_step_median": round(statistics.median(step_ms), 5),
+        "ms_per_step_p90": round(percentile(step_ms, 90), 5),
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -515,7 +517,7 @@ def run_ours(args):
             "workload": f"{args.workload}: T={T}, E={spec.E}, top_k={spec.k}, d={spec.d}, f={spec.f}, "
                         f"f_shared={spec.f_shared}, fmt={'Q8_0' if spec.fmt == 0 else 'Q2S'}, "
                         f"s={spec.s}, zipf_beta={spec.zipf_beta}",
-            "token_seeds": f"{seeds[0]}..{seeds[-1]}",
+            "token_seeds": seeds_run(step_seed),
             "tokens_per_step": T,
             "l2": "flushed between steps (2x L2 write, then read back), outside the per-step "
                   "CUDA-event time; e2e: K steps back to back, each reading 361 MB of weights "
@@ -553,9 +555,30 @@ def run_ours(args):
     return line
 
 
+def seeds_run(step_seed) -> str:
+    """The token seeds the timed steps used (each step takes the next seed)."""
+    u = sorted(set(step_seed))
+    if u == list(range(u[0], u[-1] + 1)):
+        return f"{u[0]}..{u[-1]} ({len(u)} seeds)"
+    return ",".join(str(v) for v in u)
+
+
+def percentile(v, q: float) -> float:
+    """q-th percentile by linear interpolation between order statistics."""
+    a = sorted(v)
+    if len(a) == 1:
+        return a[0]
+    x = (len(a) - 1) * q / 100.0
+    i = int(x)
+    j = min(i + 1, len(a) - 1)
+    return a[i] + (a[j] - a[i]) * (x - i)
+
+
 def run_sweep(torch, moe, synth, dev, layer, flush, peak):
     """Side measurements at T=2/16/512 on the same layer and T=64 on the 2-bit
-    layer (eager calls, 10 steps each after 3 warm-ups, L2 flushed between)."""
+    layer: 10 eager moe_layer calls each after 3 warm-ups, L2 flushed between,
+    CUDA events around each call (ms_per_step); then 10 more calls with events
+    between the stages (stage_us)."""
     out = {}
     cases = [("batch_t2", layer), ("batch_t16", layer), ("prefill_t512", layer), ("q2_t64", None)]
     for name, lay in cases:
@@ -573,14 +596,23 @@ def run_sweep(torch, moe, synth, dev, layer, flush, peak):
         n = 10
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)]
                for _ in range(n)]
+        e0 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+        e1 = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
         for i in range(3):
+            moe.layer(desc, lay.weights, x_d, l_d, bias, y, ws)
             moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[0])
         torch.cuda.synchronize()
         for i in range(n):
             flush()
+            e0[i].record()
+            moe.layer(desc, lay.weights, x_d, l_d, bias, y, ws)
+            e1[i].record()
+        torch.cuda.synchronize()
+        step = [e0[i].elapsed_time(e1[i]) for i in range(n)]
+        for i in range(n):
+            flush()
             moe.layer_timed(desc, lay.weights, x_d, l_d, bias, y, ws, evs[i])
         torch.cuda.synchronize()
-        step = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(n)]
         stage = {nm: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(n))
                  for j, nm in enumerate(names)}
         lay_off = lay.views(ws, T)["off"].cpu()
