@@ -248,6 +248,38 @@ moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,
                             const float *w_router, const float *x, const float *bias, uint32_t T,
                             float *logits, float *y, void *ws, size_t ws_bytes, void *stream);
 
+/* ---- Expert-parallel split ----
+ * The layer restricted to one rank's share of the experts: routing over all
+ * n_expert as in moe_layer (every rank routes every token the same way), then
+ *   y[t] = [with_shared] o_shared[t] + sum over slots j with
+ *          expert_begin <= idx[t][j] < expert_end of w[t][j] * o[t][j]
+ * (shared first, then the owned slots in slot order).  Ranks whose ranges
+ * partition [0, n_expert), with with_shared set on exactly one of them, give
+ * partial outputs whose sum is the layer (a sum all-reduce of y: the
+ * expert-parallel residency the pages name as the next multi-GPU lever,
+ * NeutronStar README, next-levers paragraph, and the two-worker split of
+ * NeutronStar glm-local README, "Roadmap"); the sum's fp32 order differs from
+ * moe_layer's, so it matches within the output tolerance, not bit for bit.
+ * Only the owned experts' weights are read: with moe_weights.expert_slot a
+ * rank holds its own experts only (the slots of unowned experts are never
+ * read, and need not be valid).  Workspace as moe_layer.  An empty range
+ * (expert_begin == expert_end) computes the shared expert alone (or y = 0).
+ * MOE_ERR_INVALID_ARG unless expert_begin <= expert_end <= n_expert. */
+moe_status moe_layer_experts(const moe_desc *desc, const moe_weights *wts, const float *x,
+                             const float *logits, const float *bias, uint32_t T,
+                             uint32_t expert_begin, uint32_t expert_end, int32_t with_shared,
+                             float *y, void *ws, size_t ws_bytes, void *stream);
+
+/* moe_ffn restricted the same way: the expert FFN and combine of the owned
+ * experts (and the shared expert if with_shared) for routing results computed
+ * elsewhere -- the compute step of an all-to-all dispatch, where a rank receives
+ * the rows (x and their full routing) that name at least one of its experts. */
+moe_status moe_ffn_experts(const moe_desc *desc, const moe_weights *wts, const float *x,
+                           uint32_t T, const int32_t *idx, const float *w, const int32_t *off,
+                           const int32_t *perm, const int32_t *pos, uint32_t expert_begin,
+                           uint32_t expert_end, int32_t with_shared, float *y, void *ws,
+                           size_t ws_bytes, void *stream);
+
 /* Which implementation moe_layer uses for (desc, T) on the current device:
  * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);

@@ -128,6 +128,9 @@ struct StageDesc {
 
 struct FusedArgs {
   uint32_t E, k, d, f, fs, T, R, fmax;
+  // the routed experts this call computes, [e_lo, e_hi), and the shared
+  // expert's width if the call adds it, else 0 (an expert-parallel rank's share)
+  uint32_t e_lo, e_hi, fs_on;
   float s;
   uint32_t score;  // moe_score
   const float *x, *logits, *bias;
@@ -550,28 +553,40 @@ __device__ void route_select(const FusedArgs &a, RouteSmem &rs, float *sc, const
       rs.act_e[u] = e;
       rs.act_row0[u] = p;
       rs.act_rows[u] = rows;
-      const int w = a.eslot ? __ldg(a.eslot + e) : e;
-      rs.act_w[u] = w;
-      if ((uint32_t)w >= a.n_slots) rs.bad_slot = 1;
-      if (blockIdx.x == 0) {
-        PlanView P(a.plan, E);
-        P.act_e[u] = e;
-        P.act_row0[u] = p;
-        P.act_rows[u] = rows;
-      }
+      rs.act_w[u] = a.eslot ? __ldg(a.eslot + e) : e;
     }
   }
   route_bar_sync(T);
   if (tid == 0) {
+    // keep the experts this call computes, in order; only their weight slots
+    // must be valid
     const int U = __popc(rs.first_bits[0]) + __popc(rs.first_bits[1]);
-    rs.U = U;
+    int V = 0;
+#pragma unroll 1
+    for (int u = 0; u < U; ++u) {
+      const int e = rs.act_e[u];
+      if ((uint32_t)e < a.e_lo || (uint32_t)e >= a.e_hi) continue;
+      rs.act_e[V] = e;
+      rs.act_w[V] = rs.act_w[u];
+      rs.act_row0[V] = rs.act_row0[u];
+      rs.act_rows[V] = rs.act_rows[u];
+      if ((uint32_t)rs.act_w[V] >= a.n_slots) rs.bad_slot = 1;
+      if (blockIdx.x == 0) {
+        PlanView P(a.plan, E);
+        P.act_e[V] = e;
+        P.act_row0[V] = rs.act_row0[V];
+        P.act_rows[V] = rs.act_rows[V];
+      }
+      ++V;
+    }
+    rs.U = V;
     if (rs.bad_slot) {  // plan no routed work: every weight row read stays in range
       rs.U = 0;
       atomicOr(a.err, kErrBadSlot);
     }
     if (blockIdx.x == 0) {
       PlanView P(a.plan, E);
-      P.hdr[0] = U;  // routed experts only
+      P.hdr[0] = V;  // routed experts only
       P.hdr[4] = 1;
     }
   }
@@ -659,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
   }
   __syncthreads();
 
-  const uint32_t n_sh = a.fs / kBItemFeat;  // shared-expert gate/up items
+  const uint32_t n_sh = a.fs_on / kBItemFeat;  // shared-expert gate/up items
   const uint32_t fb = a.f / kBItemFeat;      // gate/up items per routed expert
 
   if (warp == kProducerWarp) {
@@ -686,7 +701,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
         if (tr) tr[kTrRouteDone] = global_ns();
         U = (uint32_t)rs.U;
         NB = n_sh + U * fb;  // all gate/up items
-        total = NB + (U + (a.fs ? 1u : 0u)) * a.n_chunks;
+        total = NB + (U + (a.fs_on ? 1u : 0u)) * a.n_chunks;
         routed = true;
         return true;
       };
@@ -724,8 +739,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
           } else {
             uint32_t uc = (item - NB) / a.n_chunks;
             chunk = (item - NB) % a.n_chunks;
-            if (a.fs && uc == 0) shared = true;
-            else u = a.fs ? uc - 1 : uc;
+            if (a.fs_on && uc == 0) shared = true;
+            else u = a.fs_on ? uc - 1 : uc;
           }
           if (shared) {
             dsc.e = (int)a.E;
@@ -1312,16 +1327,20 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_fused(const FusedArgs a)
 #pragma unroll 1
     for (uint32_t i = blockIdx.x * kThreads + tid; i < T * d; i += gridDim.x * kThreads) {
       const uint32_t t = i / d, m = i % d;
-      float acc = a.fs ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
+      float acc = a.fs_on ? __ldcg(a.o + ((size_t)a.R + t) * d + m) : 0.0f;
 #pragma unroll 1
       for (uint32_t j0 = 0; j0 < a.k; j0 += kJ) {
         float v[kJ];
+        bool own[kJ];
+#pragma unroll
+        for (uint32_t jj = 0; jj < kJ; ++jj) {
+          const uint32_t r = t * a.k + j0 + jj;
+          own[jj] = j0 + jj < a.k && (uint32_t)rs.idx[r] >= a.e_lo && (uint32_t)rs.idx[r] < a.e_hi;
+          v[jj] = own[jj] ? __ldcg(a.o + (size_t)rs.pos[r] * d + m) : 0.0f;
+        }
 #pragma unroll
         for (uint32_t jj = 0; jj < kJ; ++jj)
-          v[jj] = j0 + jj < a.k ? __ldcg(a.o + (size_t)rs.pos[t * a.k + j0 + jj] * d + m) : 0.0f;
-#pragma unroll
-        for (uint32_t jj = 0; jj < kJ; ++jj)
-          if (j0 + jj < a.k) acc = __fmaf_rn(rs.w[t * a.k + j0 + jj], v[jj], acc);
+          if (own[jj]) acc = __fmaf_rn(rs.w[t * a.k + j0 + jj], v[jj], acc);
       }
       a.y[(size_t)t * d + m] = acc;
     }
@@ -1418,6 +1437,9 @@ cudaError_t launch_decode_fused(const Ctx &c, const float *x, const float *logit
   a.d = D.d;
   a.f = D.f;
   a.fs = D.f_shared;
+  a.e_lo = c.e_lo;
+  a.e_hi = c.e_hi;
+  a.fs_on = c.shared_on ? D.f_shared : 0u;
   a.T = c.T;
   a.R = c.R;
   a.fmax = c.fmax;

@@ -359,10 +359,13 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas_dn<FMT, MAXR>()))
 }
 
 // y[t][m] = o_shared[t][m] + sum_j w[t,j] * o[pos[t,j]][m], in that order
+// (only the slots of experts in [e_lo, e_hi), and the shared term if `shared`:
+// an expert-parallel rank's share of the sum)
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ o, const float *__restrict__ w,
-              const int32_t *__restrict__ pos, uint32_t T, uint32_t k, uint32_t d, uint32_t R,
-              bool shared, const int *__restrict__ plan, float *__restrict__ y) {
+              const int32_t *__restrict__ pos, const int32_t *__restrict__ idx, uint32_t T,
+              uint32_t k, uint32_t d, uint32_t R, bool shared, uint32_t e_lo, uint32_t e_hi,
+              bool all_experts, const int *__restrict__ plan, float *__restrict__ y) {
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)T * d) return;
   if (plan[4] != 1) {  // rejected routing arrays: no expert ran, pos[] is not trusted
@@ -372,6 +375,10 @@ __global__ void __launch_bounds__(256)
   const uint32_t t = (uint32_t)(i / d), m = (uint32_t)(i % d);
   float acc = shared ? o[((size_t)R + t) * d + m] : 0.0f;
   for (uint32_t j = 0; j < k; ++j) {
+    if (!all_experts) {
+      const uint32_t e = (uint32_t)idx[(size_t)t * k + j];
+      if (e < e_lo || e >= e_hi) continue;
+    }
     const int p = pos[(size_t)t * k + j];
     acc = __fmaf_rn(w[(size_t)t * k + j], o[(size_t)p * d + m], acc);
   }
@@ -522,12 +529,15 @@ cudaError_t launch_down(const Ctx &c) {
                                           : dn_maxr<MOE_FMT_Q8_0>(c, a, taps);
 }
 
-cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, float *y) {
+cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,
+                           const int32_t *idx, float *y) {
   const uint64_t n = (uint64_t)c.T * c.desc.d;
   if (n == 0) return cudaSuccess;
+  const bool all = c.e_lo == 0 && c.e_hi >= c.desc.n_expert;
   k_combine<<<(unsigned)((n + 255) / 256), 256, 0, c.stream>>>(
-      (const float *)(c.ws + c.L.o), w, pos, c.T, c.desc.top_k, c.desc.d, c.R,
-      c.desc.f_shared > 0, (const int *)(c.ws + c.L.plan), y);
+      (const float *)(c.ws + c.L.o), w, pos, idx, c.T, c.desc.top_k, c.desc.d, c.R,
+      c.desc.f_shared > 0 && c.shared_on, c.e_lo, c.e_hi, all, (const int *)(c.ws + c.L.plan),
+      y);
   return cudaGetLastError();
 }
 

@@ -134,6 +134,9 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
   c.L = make_layout(d, T);
   c.stream = (cudaStream_t)stream;
   c.sm_count = sm_count_of_current_device();
+  c.e_lo = 0;
+  c.e_hi = d->n_expert;
+  c.shared_on = true;
   return c;
 }
 
@@ -188,17 +191,20 @@ moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float
   if ((e = mk.mark(9)) != cudaSuccess) return from_cuda(e);
   if (tc && (e = launch_tc(c, 1)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(10)) != cudaSuccess) return from_cuda(e);
-  if ((e = launch_combine(c, w, pos, y)) != cudaSuccess) return from_cuda(e);
+  if ((e = launch_combine(c, w, pos, idx, y)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(11)) != cudaSuccess) return from_cuda(e);
   return MOE_OK;
 }
 
 // w_router non-null: the router logits are computed from x into `logits`
 // (an output then); else `logits` is the caller's input
+// e_lo, e_hi, shared_on: the routed experts [e_lo, e_hi) and the shared expert
+// (if shared_on) are the ones computed; e_hi == 0 means all experts
 moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *x,
                      const float *logits, const float *bias, uint32_t T, float *y, void *ws,
                      size_t ws_bytes, void *stream, void *const *events, uint32_t n_events,
-                     const float *w_router = nullptr) {
+                     const float *w_router = nullptr, uint32_t e_lo = 0, uint32_t e_hi = 0,
+                     bool shared_on = true, bool no_routed = false) {
   if (!desc_ok(desc) || !weights_ok(desc, wts)) return MOE_ERR_INVALID_ARG;
   if (!ws || !aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
   if (T > 0 && (!x || !logits || !bias || !y)) return MOE_ERR_INVALID_ARG;
@@ -209,6 +215,12 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
   if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
   Ctx c = make_ctx(desc, wts, T, ws, stream);
+  if (e_hi) {
+    c.e_lo = e_lo;
+    c.e_hi = e_hi;
+  }
+  if (no_routed) c.e_lo = c.e_hi = 0;  // an empty range: the shared expert alone
+  c.shared_on = shared_on;
   Marks mk(events, n_events, c.stream);
   int32_t *idx = (int32_t *)(c.ws + c.L.idx);
   float *w = (float *)(c.ws + c.L.w);
@@ -305,6 +317,36 @@ moe_status moe_layer_timed(const moe_desc *desc, const moe_weights *wts, const f
                            void *ws, size_t ws_bytes, void *stream, void *const *events,
                            uint32_t n_events) {
   return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, events, n_events);
+}
+
+moe_status moe_layer_experts(const moe_desc *desc, const moe_weights *wts, const float *x,
+                             const float *logits, const float *bias, uint32_t T,
+                             uint32_t expert_begin, uint32_t expert_end, int32_t with_shared,
+                             float *y, void *ws, size_t ws_bytes, void *stream) {
+  if (!desc_ok(desc) || expert_begin > expert_end || expert_end > desc->n_expert)
+    return MOE_ERR_INVALID_ARG;
+  return run_layer(desc, wts, x, logits, bias, T, y, ws, ws_bytes, stream, nullptr, 0, nullptr,
+                   expert_begin, expert_end == expert_begin ? 0 : expert_end, with_shared != 0,
+                   expert_end == expert_begin);
+}
+
+moe_status moe_ffn_experts(const moe_desc *desc, const moe_weights *wts, const float *x,
+                           uint32_t T, const int32_t *idx, const float *w, const int32_t *off,
+                           const int32_t *perm, const int32_t *pos, uint32_t expert_begin,
+                           uint32_t expert_end, int32_t with_shared, float *y, void *ws,
+                           size_t ws_bytes, void *stream) {
+  if (!desc_ok(desc) || expert_begin > expert_end || expert_end > desc->n_expert)
+    return MOE_ERR_INVALID_ARG;
+  if (!weights_ok(desc, wts)) return MOE_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, kAlign) || !off) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !idx || !w || !perm || !pos || !y)) return MOE_ERR_INVALID_ARG;
+  if ((uint64_t)T * desc->top_k > (1u << 30)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < make_layout(desc, T).total) return MOE_ERR_WORKSPACE;
+  Ctx c = make_ctx(desc, wts, T, ws, stream);
+  c.e_lo = expert_begin;
+  c.e_hi = expert_end;
+  c.shared_on = with_shared != 0;
+  return run_ffn(c, x, idx, w, off, perm, pos, y, Marks(nullptr, 0, c.stream));
 }
 
 moe_status moe_layer_from_x(const moe_desc *desc, const moe_weights *wts,

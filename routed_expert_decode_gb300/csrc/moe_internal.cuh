@@ -283,6 +283,10 @@ struct Ctx {
   moe_ws_layout L;
   cudaStream_t stream;
   int sm_count;
+  // routed experts this call computes, [e_lo, e_hi), and whether it adds the
+  // shared expert (an expert-parallel rank's share; [0, E) and true otherwise)
+  uint32_t e_lo, e_hi;
+  bool shared_on;
 };
 
 cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, int32_t *idx,
@@ -302,7 +306,8 @@ cudaError_t launch_quant_x(const Ctx &c, const float *x);
 cudaError_t launch_gateup(const Ctx &c, const int32_t *perm);
 cudaError_t launch_requant_h(const Ctx &c);
 cudaError_t launch_down(const Ctx &c);
-cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos, float *y);
+cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,
+                           const int32_t *idx, float *y);
 
 // fused single-kernel decode (T <= 2): decode_fused.cu
 size_t fused_sync_ints(const moe_desc *d);

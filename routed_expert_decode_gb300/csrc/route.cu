@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kPlanThreads)
            const int32_t *__restrict__ perm, const int32_t *__restrict__ pos, uint32_t T,
            uint32_t E, uint32_t k, uint32_t f, uint32_t fs, uint32_t d, int tc_mode,
            uint32_t tc_min_rows, uint32_t tc_min_tiles, const int32_t *__restrict__ eslot,
-           uint32_t n_slots, int *plan, uint32_t *err) {
+           uint32_t n_slots, uint32_t e_lo, uint32_t e_hi, int shared_on, int *plan,
+           uint32_t *err) {
   __shared__ int scan[kPlanThreads];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -240,10 +241,16 @@ __global__ void __launch_bounds__(kPlanThreads)
     }
     return;
   }
-  // with a slot table, every selected expert's weights must be in a slot
+  // rows of expert e this call computes: only the experts in [e_lo, e_hi) (the
+  // share of one rank in an expert-parallel split; all of them by default)
+  auto own_rows = [&](uint32_t e) -> int {
+    return e >= e_lo && e < e_hi ? off[e + 1] - off[e] : 0;
+  };
+  // with a slot table, every selected expert this call computes must have its
+  // weights in a slot
   if (eslot) {
     for (uint32_t e = tid; e < E; e += kPlanThreads)
-      if (off[e + 1] > off[e] && (uint32_t)eslot[e] >= n_slots) bad = 3;
+      if (own_rows(e) > 0 && (uint32_t)eslot[e] >= n_slots) bad = 3;
     __syncthreads();
     if (bad) {
       if (tid == 0) {
@@ -260,13 +267,13 @@ __global__ void __launch_bounds__(kPlanThreads)
     __shared__ int tc_tiles;
     if (tid == 0) {
       tc_tiles = 0;
-      if (fs > 0 && fs == f && T > tc_min_rows)
+      if (shared_on && fs > 0 && fs == f && T > tc_min_rows)
         tc_tiles = (int)(fs / kTcTileM) * (int)((T + kTcTileN - 1) / kTcTileN);
     }
     __syncthreads();
     int mine = 0;
     for (uint32_t e = tid; e < E; e += kPlanThreads) {
-      const int rows = off[e + 1] - off[e];
+      const int rows = own_rows(e);
       if (rows > (int)tc_min_rows)
         mine += (int)(f / kTcTileM) * ((rows + (int)kTcTileN - 1) / (int)kTcTileN);
     }
@@ -282,7 +289,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   int ng = 0, ntc = 0, ntile_gu = 0, maxrows = 0, total;
   for (uint32_t base = 0; base < E; base += kPlanThreads) {
     const uint32_t e = base + tid;
-    const int rows = e < E ? off[e + 1] - off[e] : 0;
+    const int rows = e < E ? own_rows(e) : 0;
     const bool tc = on_tc(rows);
     const int gflag = rows > 0 && !tc ? 1 : 0, tflag = tc ? 1 : 0;
     const int gu = ng + block_excl_scan(gflag, scan, &total);
@@ -310,7 +317,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     ntile_gu += tiles_total;
     if (tid == 0)
       for (uint32_t q = base; q < base + kPlanThreads && q < E; ++q)
-        maxrows = max(maxrows, off[q + 1] - off[q]);
+        maxrows = max(maxrows, own_rows(q));
   }
   if (tid == 0) {
     int U = ng;
@@ -319,7 +326,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     int tiles_gu = ntile_gu;
     const int mt = (int)(f / kTcTileM);
     int tiles_dn = mt > 0 ? (ntile_gu / mt) * (int)(d / kTcTileM) : 0;
-    if (fs > 0 && T > 0) {
+    if (shared_on && fs > 0 && T > 0) {
       // the shared expert reads every token; the tensor path needs fs == f
       if (on_tc((int)T) && fs == f) {
         const int nt = ((int)T + ntile_n - 1) / ntile_n;
@@ -492,7 +499,7 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
   k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, D.n_expert, D.top_k, D.f,
                                            D.f_shared, D.d, tc_mode, kTcMinRows,
                                            (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
-                                           plan, err);
+                                           c.e_lo, c.e_hi, c.shared_on ? 1 : 0, plan, err);
   return cudaGetLastError();
 }
 

@@ -126,6 +126,14 @@ def lib():
         L.moe_tc_min_rows.argtypes = [ctypes.POINTER(MoeDesc), _u32]
         L.moe_tc_min_rows.restype = ctypes.c_int32
         L.moe_layer_stage_name.argtypes = [ctypes.POINTER(MoeDesc), _u32, _u32]
+        L.moe_layer_experts.restype = ctypes.c_int
+        L.moe_layer_experts.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
+                                        _vp, _vp, _u32, _u32, _u32, ctypes.c_int32, _vp, _vp, _sz,
+                                        _vp]
+        L.moe_ffn_experts.restype = ctypes.c_int
+        L.moe_ffn_experts.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
+                                      _u32, _vp, _vp, _vp, _vp, _vp, _u32, _u32, ctypes.c_int32,
+                                      _vp, _vp, _sz, _vp]
         L.moe_layer_noalloc.restype = ctypes.c_int
         L.moe_layer_noalloc.argtypes = [ctypes.POINTER(MoeDesc), ctypes.POINTER(MoeWeights), _vp,
                                         _vp, _vp, _u32, _vp, _vp]
@@ -280,6 +288,34 @@ def layer_timed(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, even
                                _dev_ptr(y, torch.float32, "y"), _dev_ptr(ws, torch.uint8, "ws"),
                                ws.numel(), _stream(stream), handles, len(events))
     _check("moe_layer_timed", st)
+
+
+def layer_experts(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, ws, begin: int,
+                  end: int, with_shared: bool, stream=None):
+    """moe_layer_experts: the layer restricted to routed experts [begin, end) and,
+    if with_shared, the shared expert (one rank's share of an expert-parallel
+    split; the ranks' outputs sum to the layer)."""
+    st = lib().moe_layer_experts(ctypes.byref(desc), ctypes.byref(weights),
+                                 _dev_ptr(x, torch.float32, "x"),
+                                 _dev_ptr(logits, torch.float32, "logits"),
+                                 _dev_ptr(bias, torch.float32, "bias"), x.shape[0], begin, end,
+                                 1 if with_shared else 0, _dev_ptr(y, torch.float32, "y"),
+                                 _dev_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check("moe_layer_experts", st)
+
+
+def ffn_experts(desc: MoeDesc, weights: MoeWeights, x, idx, w, off, perm, pos, y, ws,
+                begin: int, end: int, with_shared: bool, stream=None):
+    """moe_ffn_experts: moe_ffn restricted like layer_experts."""
+    st = lib().moe_ffn_experts(ctypes.byref(desc), ctypes.byref(weights),
+                               _dev_ptr(x, torch.float32, "x"), x.shape[0],
+                               _dev_ptr(idx, torch.int32, "idx"), _dev_ptr(w, torch.float32, "w"),
+                               _dev_ptr(off, torch.int32, "off"),
+                               _dev_ptr(perm, torch.int32, "perm"),
+                               _dev_ptr(pos, torch.int32, "pos"), begin, end,
+                               1 if with_shared else 0, _dev_ptr(y, torch.float32, "y"),
+                               _dev_ptr(ws, torch.uint8, "ws"), ws.numel(), _stream(stream))
+    _check("moe_ffn_experts", st)
 
 
 def layer_noalloc(desc: MoeDesc, weights: MoeWeights, x, logits, bias, y, stream=None):
