@@ -94,6 +94,22 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+FALLBACK_TENSOR_TFLOPS = 1900.0  # dense 16-bit, one earlier GB300 measurement
+SM_MHZ_MAX = 2070.0              # the GB300's maximum SM clock
+
+
+def load_tensor_peak() -> float:
+    """Dense 16-bit tensor peak (TFLOP/s) of a kernel timed alone: the measured
+    bf16 burst figure (fp16 runs at the same dense rate), else the fallback."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        if p.get("bf16_tflops"):
+            return float(p["bf16_tflops"])
+    return FALLBACK_TENSOR_TFLOPS
+
+
 # ------------------------------------------------------------------ bytes model
 def row_bytes(fmt: int, K: int) -> int:
     """Bytes of one quantised weight row of K weights: codes + fp16 block scales."""
@@ -136,6 +152,47 @@ def stage_bytes(spec, T: int, counts, tc_rows=None, sm_count=None):
 
 
 ROOFLINE_STAGES = ("gateup", "down", "gateup_tc", "down_tc", "decode_fused")
+
+# dp4a issue rate of one SM per clock: half the 128 fp32 lanes (a probe kernel
+# of independent dp4a chains measured 60.2 per SM per clock on this GB300)
+DP4A_PER_SM_CLK = 64
+
+
+def stage_macs(spec, T: int, counts, tc_rows=None, sm_count=None):
+    """int8 (or 2-bit x int8) multiply-adds of the gate/up and down stages: each
+    selected expert's rows times its weights, split like stage_bytes between the
+    dp4a GEMV and the tensor cores."""
+    if tc_rows is not None and sm_count is not None and tc_tiles(spec, T, counts, tc_rows) < sm_count:
+        tc_rows = None
+    out = {"gateup": 0, "down": 0, "gateup_tc": 0, "down_tc": 0}
+
+    def add(rows, f):
+        tc = "_tc" if tc_rows is not None and rows > tc_rows else ""
+        out["gateup" + tc] += 2 * f * spec.d * rows
+        out["down" + tc] += spec.d * f * rows
+
+    for c in counts:
+        if c > 0:
+            add(int(c), spec.f)
+    if spec.f_shared:
+        add(T, spec.f_shared)
+    return out
+
+
+def unit_fractions(macs, stage_ms, sm_count, sm_mhz, tensor_tflops):
+    """Which unit binds each expert stage: the dp4a stages' dp4a issue rate
+    against SMs x 64 / clock x SM clock, the tensor-core stages' fp16 MMA rate
+    (2 flops a multiply-add) against the measured dense 16-bit peak."""
+    out = {}
+    dp4a_peak = sm_count * DP4A_PER_SM_CLK * sm_mhz * 1e6
+    for st in ("gateup", "down"):
+        if st in stage_ms and macs[st]:
+            out[st + "_dp4a_frac"] = round(macs[st] / 4 / (stage_ms[st] / 1e3) / dp4a_peak, 4)
+    for st in ("gateup_tc", "down_tc"):
+        if st in stage_ms and macs[st] and tensor_tflops:
+            out[st + "_tensor_frac"] = round(2 * macs[st] / (stage_ms[st] / 1e3) /
+                                            (tensor_tflops * 1e12), 4)
+    return out
 
 
 # ------------------------------------------------------------------ clocks
@@ -618,8 +675,9 @@ def run_sweep(torch, moe, synth, dev, layer, flush, peak):
         lay_off = lay.views(ws, T)["off"].cpu()
         counts = (lay_off[1:] - lay_off[:-1]).tolist()
         U = sum(1 for c in counts if c > 0)
-        b = stage_bytes(spec, T, counts, moe.tc_min_rows(desc, T),
-                        torch.cuda.get_device_properties(dev).multi_processor_count)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        b = stage_bytes(spec, T, counts, moe.tc_min_rows(desc, T), sms)
+        macs = stage_macs(spec, T, counts, moe.tc_min_rows(desc, T), sms)
         ms = statistics.mean(step)
         out[name] = {"T": T, "unique_experts": U, "ms_per_step": round(ms, 4),
                      "tokens_per_s": round(T / (ms / 1e3), 1),
@@ -628,7 +686,12 @@ def run_sweep(torch, moe, synth, dev, layer, flush, peak):
                      "frac_of_measured": round(b["total"] / (ms / 1e3) / 1e9 / peak, 4),
                      "stage_us": {k: round(v * 1e3, 1) for k, v in stage.items()},
                      "stage_gbs": {k: round(b[k] / (stage[k] / 1e3) / 1e9, 1)
-                                   for k in ROOFLINE_STAGES if k in stage and b[k] > 0}}
+                                   for k in ROOFLINE_STAGES if k in stage and b[k] > 0},
+                     "stage_hbm_frac": {k: round(b[k] / (stage[k] / 1e3) / 1e9 / peak, 4)
+                                        for k in ROOFLINE_STAGES if k in stage and b[k] > 0},
+                     "stage_unit_frac": unit_fractions(macs, stage, sms, SM_MHZ_MAX,
+                                                       load_tensor_peak()),
+                     "ms_per_step_median": round(statistics.median(step), 4)}
         assert moe.check_device_error(ws) == 0
     out.update(run_router_sweep(torch, moe, synth, dev, layer, flush, peak))
     out.update(run_stream_sweep(torch, moe, synth, dev, layer))

@@ -294,7 +294,8 @@ const char *moe_layer_path(const moe_desc *desc, uint32_t T);
  * expert to the tensor cores.  2-bit routed weights take the same path: their
  * codes are decoded to fp16 (2c - 3, exact) on the way to the MMA.  -1 when no
  * expert of such a call can take the tensor path (the fused decode path, dims
- * not a multiple of 256, MOE_FLAG_FORCE_GEMV, or T at most the threshold). */
+ * not a multiple of 256, MOE_FLAG_FORCE_GEMV, fewer than 32 tokens without
+ * MOE_FLAG_FORCE_TC, or T at most the threshold). */
 int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T);
 
 /* Name of stage i of that path (what moe_layer_timed's events bracket),

@@ -229,6 +229,8 @@ __device__ __forceinline__ void gateup_group(const GUArgs &a, const int8_t *gq,
 template <int FMT, int MAXR, bool TAPS, bool WIDE>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas<FMT, MAXR, WIDE>()))
     k_gateup(const GUArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NF = group_nf<FMT, 2, WIDE>(), J = group_j<FMT, 2, MAXR>();
   constexpr int NFS = group_nf<MOE_FMT_Q8_0, 2, WIDE>(), JS = group_j<MOE_FMT_Q8_0, 2, MAXR>();
   static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
@@ -270,6 +272,8 @@ __global__ void __launch_bounds__(256)
     k_requant(const float *__restrict__ h, uint32_t slots, uint32_t R, uint32_t f, uint32_t fs,
               uint32_t fmax, int8_t *__restrict__ hq, float *__restrict__ hs,
               int8_t *__restrict__ ht) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const uint32_t nbmax = fmax / 32;
   const uint64_t gw = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32;
@@ -331,6 +335,8 @@ __device__ __forceinline__ void down_group(const DNArgs &a, const int8_t *dq, co
 
 template <int FMT, int MAXR, bool TAPS>
 __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas_dn<FMT, MAXR>())) k_down(const DNArgs a) {
+  pdl_trigger();
+  pdl_wait();
   constexpr int NF = group_nf<FMT, 1>(), J = group_j<FMT, 1, MAXR>();
   constexpr int NFS = group_nf<MOE_FMT_Q8_0, 1>(), JS = group_j<MOE_FMT_Q8_0, 1, MAXR>();
   static_assert(NF % NFS == 0, "the shared expert's groups must tile the routed ones");
@@ -366,6 +372,8 @@ __global__ void __launch_bounds__(256)
               const int32_t *__restrict__ pos, const int32_t *__restrict__ idx, uint32_t T,
               uint32_t k, uint32_t d, uint32_t R, bool shared, uint32_t e_lo, uint32_t e_hi,
               bool all_experts, const int *__restrict__ plan, float *__restrict__ y) {
+  pdl_trigger();
+  pdl_wait();
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)T * d) return;
   if (plan[4] != 1) {  // rejected routing arrays: no expert ran, pos[] is not trusted
@@ -409,8 +417,9 @@ cudaError_t run_gateup(const Ctx &c, const GUArgs &a) {
   int per_sm = 1;
   cudaError_t e = grid_for(kern, smem, big_smem, per_sm);
   if (e != cudaSuccess) return e;
-  kern<<<per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream>>>(a);
-  return cudaGetLastError();
+  e = launch_k(kern, per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream, c.chained, a);
+  c.chained = true;
+  return e;
 }
 
 template <int FMT, int MAXR, bool TAPS>
@@ -421,8 +430,9 @@ cudaError_t run_down(const Ctx &c, const DNArgs &a) {
   int per_sm = 1;
   cudaError_t e = grid_for(kern, smem, big_smem, per_sm);
   if (e != cudaSuccess) return e;
-  kern<<<per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream>>>(a);
-  return cudaGetLastError();
+  e = launch_k(kern, per_sm * c.sm_count, kWarpsPerCta * 32, smem, c.stream, c.chained, a);
+  c.chained = true;
+  return e;
 }
 
 // rows per pass: an expert has at most T rows; more than 4 take several passes
@@ -497,11 +507,13 @@ cudaError_t launch_requant_h(const Ctx &c) {
   const uint32_t slots = c.R + (c.desc.f_shared ? c.T : 0);
   const uint64_t warps = (uint64_t)slots * (c.fmax / 32);
   if (warps == 0) return cudaSuccess;
-  k_requant<<<(unsigned)((warps + 7) / 8), 256, 0, c.stream>>>(
+  const cudaError_t e = launch_k(
+      k_requant, (unsigned)((warps + 7) / 8), 256, 0, c.stream, c.chained,
       (const float *)(c.ws + c.L.h), slots, c.R, c.desc.f, c.desc.f_shared, c.fmax,
       (int8_t *)(c.ws + c.L.hq), (float *)(c.ws + c.L.hs),
       c.L.ht ? (int8_t *)(c.ws + c.L.ht) : nullptr);
-  return cudaGetLastError();
+  c.chained = true;
+  return e;
 }
 
 cudaError_t launch_down(const Ctx &c) {
@@ -534,11 +546,13 @@ cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,
   const uint64_t n = (uint64_t)c.T * c.desc.d;
   if (n == 0) return cudaSuccess;
   const bool all = c.e_lo == 0 && c.e_hi >= c.desc.n_expert;
-  k_combine<<<(unsigned)((n + 255) / 256), 256, 0, c.stream>>>(
+  const cudaError_t e = launch_k(
+      k_combine, (unsigned)((n + 255) / 256), 256, 0, c.stream, c.chained,
       (const float *)(c.ws + c.L.o), w, pos, idx, c.T, c.desc.top_k, c.desc.d, c.R,
       c.desc.f_shared > 0 && c.shared_on, c.e_lo, c.e_hi, all, (const int *)(c.ws + c.L.plan),
       y);
-  return cudaGetLastError();
+  c.chained = true;
+  return e;
 }
 
 }  // namespace moe

@@ -490,6 +490,8 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
 template <int MAT, bool TAPS, int RFMT>
 __global__ void __launch_bounds__(kTcThreads, 1)
     k_expert_tc(const TcArgs a, const __grid_constant__ TcMaps maps) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ __align__(1024) uint8_t tsm_raw[];
   // 1024-byte alignment for the swizzled operands
   uint8_t *tsm = (uint8_t *)(((uintptr_t)tsm_raw + 1023) & ~(uintptr_t)1023);
@@ -767,6 +769,8 @@ __global__ void __launch_bounds__(256)
     k_perm_x(const int8_t *__restrict__ xq, const int32_t *__restrict__ perm, uint32_t R,
              uint32_t slots, uint32_t k, uint32_t d, const int *plan, uint32_t E,
              __half *__restrict__ xperm) {
+  pdl_trigger();
+  pdl_wait();
   if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;  // 8-element chunks
   const uint64_t chunks = (uint64_t)slots * (d / 8);
@@ -785,6 +789,8 @@ __global__ void __launch_bounds__(256)
     k_perm_xs(const float *__restrict__ xs, const int32_t *__restrict__ perm, uint32_t R,
               uint32_t slots, uint32_t k, uint32_t nb, const int *plan, uint32_t E,
               float *__restrict__ xsperm) {
+  pdl_trigger();
+  pdl_wait();
   if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= (uint64_t)slots * nb) return;
@@ -833,8 +839,9 @@ cudaError_t run_tc(const Ctx &c, const TcArgs &a, const TcMaps &maps, size_t sme
   auto kern = k_expert_tc<MAT, TAPS, RFMT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  kern<<<c.sm_count, kTcThreads, smem, c.stream>>>(a, maps);
-  return cudaGetLastError();
+  e = launch_k(kern, c.sm_count, kTcThreads, smem, c.stream, c.chained, a, maps);
+  c.chained = true;
+  return e;
 }
 
 }  // namespace
@@ -852,21 +859,26 @@ bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.flags & MOE_FLAG_FORCE_GEMV) return false;
   if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S) return false;
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
-  return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T > kTcMinRows;
+  // unforced, only from kTcMinTokens tokens: below that no expert brings enough
+  // tiles to pay for the tensor kernels and their activation copies
+  return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T >= kTcMinTokens && T > kTcMinRows;
 }
 
 cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm) {
   const uint32_t slots = c.R + (c.desc.f_shared ? c.T : 0);
   const uint64_t n1 = (uint64_t)slots * (c.desc.d / 8);
   if (n1 == 0) return cudaSuccess;
-  k_perm_x<<<(unsigned)((n1 + 255) / 256), 256, 0, c.stream>>>(
-      (const int8_t *)(c.ws + c.L.xq), perm, c.R, slots, c.desc.top_k, c.desc.d,
-      (const int *)(c.ws + c.L.plan), c.desc.n_expert, (__half *)(c.ws + c.L.xperm));
+  cudaError_t e = launch_k(k_perm_x, (unsigned)((n1 + 255) / 256), 256, 0, c.stream, c.chained,
+                           (const int8_t *)(c.ws + c.L.xq), perm, c.R, slots, c.desc.top_k,
+                           c.desc.d, (const int *)(c.ws + c.L.plan), c.desc.n_expert,
+                           (__half *)(c.ws + c.L.xperm));
+  c.chained = true;
+  if (e != cudaSuccess) return e;
   const uint64_t n2 = (uint64_t)slots * (c.desc.d / 32);
-  k_perm_xs<<<(unsigned)((n2 + 255) / 256), 256, 0, c.stream>>>(
-      (const float *)(c.ws + c.L.xs), perm, c.R, slots, c.desc.top_k, c.desc.d / 32,
-      (const int *)(c.ws + c.L.plan), c.desc.n_expert, (float *)(c.ws + c.L.xsperm));
-  return cudaGetLastError();
+  e = launch_k(k_perm_xs, (unsigned)((n2 + 255) / 256), 256, 0, c.stream, true,
+               (const float *)(c.ws + c.L.xs), perm, c.R, slots, c.desc.top_k, c.desc.d / 32,
+               (const int *)(c.ws + c.L.plan), c.desc.n_expert, (float *)(c.ws + c.L.xsperm));
+  return e;
 }
 
 cudaError_t launch_tc(const Ctx &c, int mat) {

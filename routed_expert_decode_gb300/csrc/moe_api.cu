@@ -137,6 +137,7 @@ Ctx make_ctx(const moe_desc *d, const moe_weights *w, uint32_t T, void *ws, void
   c.e_lo = 0;
   c.e_hi = d->n_expert;
   c.shared_on = true;
+  c.chained = false;
   return c;
 }
 
@@ -241,6 +242,7 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   if (w_router && T > 0 &&
       (e = launch_router_logits(c.desc, w_router, x, T, logits_out, c.stream)) != cudaSuccess)
     return from_cuda(e);
+  if (w_router && T > 0) c.chained = true;  // the router kernel is on the stream
   if ((e = launch_route(c, logits, bias, idx, w)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(1)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_permute(c, idx, off, perm, pos, err)) != cudaSuccess) return from_cuda(e);

@@ -56,6 +56,11 @@ struct PlanView {
 
 // rows per expert above which an expert runs on the tensor-core path
 constexpr uint32_t kTcMinRows = 4;
+// calls with fewer tokens run every expert on the dp4a GEMV (no tensor kernel,
+// no activation copies launched): measured on the 256-expert layer, the GEMV
+// alone was as fast or faster up to 16 tokens a call, the tensor path faster
+// from 32
+constexpr uint32_t kTcMinTokens = 32;
 constexpr uint32_t kTcTileM = 128, kTcTileN = 64;
 
 // ---------------------------------------------------------------- spec-exp
@@ -272,6 +277,38 @@ __host__ __device__ inline uint32_t tap_feature(uint32_t j, uint32_t width) {
   return (uint32_t)(((uint64_t)j * width / kNTap + j) % width);
 }
 
+// ---------------------------------------------------------------- dependent launch
+// The multi-kernel path is a chain of kernels on one stream.  Each kernel after
+// the first is launched with programmatic stream serialization: it may start
+// (and be scheduled onto free SM resources) once every CTA of its predecessor
+// has started and triggered, so its launch overlaps the predecessor's tail.
+// Every such kernel calls pdl_wait() -- which returns once the predecessor grid
+// has completed and its writes are visible -- before reading what the chain
+// produced, and in any case before it exits, so each kernel's completion
+// still implies its predecessors' (the dependency stays transitive).
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// launch `kern` on `stream`, as a programmatic dependent of the stream's
+// previous kernel when `dep`
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                     cudaStream_t stream, bool dep, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = dep ? attr : nullptr;
+  cfg.numAttrs = dep ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------- launchers
 struct Ctx {
   moe_desc desc;
@@ -287,6 +324,9 @@ struct Ctx {
   // shared expert (an expert-parallel rank's share; [0, E) and true otherwise)
   uint32_t e_lo, e_hi;
   bool shared_on;
+  // a kernel of this call is already on the stream: the next one is launched as
+  // its programmatic dependent (launch_k)
+  mutable bool chained;
 };
 
 cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, int32_t *idx,

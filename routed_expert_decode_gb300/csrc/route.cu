@@ -21,6 +21,8 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     k_route(const float *__restrict__ logits, const float *__restrict__ bias, uint32_t T,
             uint32_t E, uint32_t k, float s, uint32_t score, int32_t *__restrict__ idx,
             float *__restrict__ w) {
+  pdl_trigger();
+  pdl_wait();  // the logits may come from the router kernel before it
   const int lane = threadIdx.x & 31;
   const uint32_t t = blockIdx.x * kRouteWarps + threadIdx.x / 32;
   if (t >= T) return;
@@ -84,6 +86,8 @@ __global__ void __launch_bounds__(kPermThreads)
     k_permute(const int32_t *__restrict__ idx, uint32_t T, uint32_t E, uint32_t k,
               int32_t *__restrict__ off, int32_t *__restrict__ perm, int32_t *__restrict__ pos,
               uint32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   extern __shared__ int smem[];
   int *hist = smem;                       // [kPermWarps][E]
   int *cnt = hist + (size_t)kPermWarps * E;  // [E]
@@ -197,6 +201,8 @@ __global__ void __launch_bounds__(kPlanThreads)
            uint32_t tc_min_rows, uint32_t tc_min_tiles, const int32_t *__restrict__ eslot,
            uint32_t n_slots, uint32_t e_lo, uint32_t e_hi, int shared_on, int *plan,
            uint32_t *err) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ int scan[kPlanThreads];
   __shared__ int bad;
   const int tid = threadIdx.x;
@@ -413,6 +419,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 __global__ void __launch_bounds__(256)
     k_quant(const float *__restrict__ x, uint32_t nblocks, int8_t *__restrict__ xq,
             float *__restrict__ xs, int8_t *__restrict__ xt) {
+  pdl_trigger();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const uint32_t b = blockIdx.x * 8 + threadIdx.x / 32;
   if (b >= nblocks) return;
@@ -435,9 +443,11 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
                          float *w) {
   if (c.T == 0) return cudaSuccess;
   const unsigned grid = (c.T + kRouteWarps - 1) / kRouteWarps;
-  k_route<<<grid, kRouteWarps * 32, 0, c.stream>>>(logits, bias, c.T, c.desc.n_expert,
-                                                   c.desc.top_k, c.desc.s, c.desc.score, idx, w);
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(k_route, grid, kRouteWarps * 32, 0, c.stream, c.chained, logits,
+                                 bias, c.T, c.desc.n_expert, c.desc.top_k, c.desc.s,
+                                 c.desc.score, idx, w);
+  c.chained = true;
+  return e;
 }
 
 // logits[t][e] = x[t] . w_router[e] in the library's fixed order (moe.h,
@@ -448,6 +458,8 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
 __global__ void __launch_bounds__(1024)
     k_router_logits(const float *__restrict__ x, const float *__restrict__ wr, uint32_t T,
                     uint32_t E, uint32_t d, float *__restrict__ logits) {
+  pdl_trigger();
+  pdl_wait();
   __shared__ float seg_total[32];
   const int lane = threadIdx.x & 31, g = threadIdx.x >> 5;
   const uint32_t t = blockIdx.x / E, e = blockIdx.x % E;
@@ -484,8 +496,10 @@ cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32
                                          (int)smem);
     if (e != cudaSuccess) return e;
   }
-  k_permute<<<1, kPermThreads, smem, c.stream>>>(idx, c.T, E, c.desc.top_k, off, perm, pos, err);
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(k_permute, 1, kPermThreads, smem, c.stream, c.chained, idx, c.T,
+                                 E, c.desc.top_k, off, perm, pos, err);
+  c.chained = true;
+  return e;
 }
 
 cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
@@ -494,22 +508,24 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
   // tensor path: 0 off, 1 for experts with more than kTcMinRows rows, 2 forced
   const moe_desc &D = c.desc;
   int tc_mode = 0;
-  if (!(D.flags & MOE_FLAG_FORCE_GEMV) && tc_supported(D))
-    tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
-  k_plan<<<1, kPlanThreads, 0, c.stream>>>(off, idx, perm, pos, c.T, D.n_expert, D.top_k, D.f,
-                                           D.f_shared, D.d, tc_mode, kTcMinRows,
-                                           (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
-                                           c.e_lo, c.e_hi, c.shared_on ? 1 : 0, plan, err);
-  return cudaGetLastError();
+  // the same condition under which run_ffn launches the tensor kernels
+  if (c.L.xperm && tc_supported(D)) tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
+  const cudaError_t e = launch_k(k_plan, 1, kPlanThreads, 0, c.stream, c.chained, off, idx, perm,
+                                 pos, c.T, D.n_expert, D.top_k, D.f, D.f_shared, D.d, tc_mode,
+                                 kTcMinRows, (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
+                                 c.e_lo, c.e_hi, c.shared_on ? 1 : 0, plan, err);
+  c.chained = true;
+  return e;
 }
 
 cudaError_t launch_quant_x(const Ctx &c, const float *x) {
   const uint32_t nblocks = c.T * (c.desc.d / 32);
   if (nblocks == 0) return cudaSuccess;
-  k_quant<<<(nblocks + 7) / 8, 256, 0, c.stream>>>(
-      x, nblocks, (int8_t *)(c.ws + c.L.xq), (float *)(c.ws + c.L.xs),
-      c.L.xt ? (int8_t *)(c.ws + c.L.xt) : nullptr);
-  return cudaGetLastError();
+  const cudaError_t e = launch_k(k_quant, (nblocks + 7) / 8, 256, 0, c.stream, c.chained, x,
+                                 nblocks, (int8_t *)(c.ws + c.L.xq), (float *)(c.ws + c.L.xs),
+                                 c.L.xt ? (int8_t *)(c.ws + c.L.xt) : nullptr);
+  c.chained = true;
+  return e;
 }
 
 }  // namespace moe

@@ -172,6 +172,7 @@ WORKLOADS = {
     "prefill_t512": (GLM_LAYER, 512, (0,)),
     "q2_t64": (Q2_LAYER, 64, (0,)),
     "profile_decode_t1": (GLM_LAYER_E32, 1, tuple(range(8))),
+    "profile_batch_t16": (GLM_LAYER_E32, 16, (0,)),
     "profile_prefill_t512": (GLM_LAYER_E32, 512, (0,)),
     "profile_prefill_e64_t128": (GLM_LAYER_E64, 128, (0,)),
 }
