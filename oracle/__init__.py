@@ -22,6 +22,7 @@ LIB = os.path.join(_HERE, "liboracle.so")
 
 FMT_Q8_0 = 0
 FMT_Q2S = 1
+FMT_E2M1 = 2
 SCORE_SIGMOID = 0
 SCORE_SQRT_SOFTPLUS = 1
 
@@ -71,6 +72,7 @@ def load():
         lib.ora_permute.argtypes = [_u32, _u32, _u32, _p, _p, _p, _p]
         lib.ora_quantize.argtypes = [_u32, _p, _p, _p]
         lib.ora_decode_q2.argtypes = [_u32, _p, _p]
+        lib.ora_decode_e2m1.argtypes = [_u32, _p, _p]
         lib.ora_block_dots.argtypes = [_i32, _u32, _p, _p, _p]
         lib.ora_matvec.argtypes = [_i32, _u32, _u32, _p, _p, _p, _p, _p]
         lib.ora_expert_row.argtypes = [_i32, _u32, _u32, ctypes.POINTER(_Expert), _p, _p, _p,
@@ -191,6 +193,14 @@ def decode_q2(codes, K: int) -> np.ndarray:
     return out
 
 
+def decode_e2m1(codes, K: int) -> np.ndarray:
+    """4-bit e2m1 codes (two a byte, low nibble first) -> int8 TWICE the value."""
+    codes = _c(codes, np.uint8)
+    out = np.empty(K, np.int8)
+    load().ora_decode_e2m1(K, _ptr(codes), _ptr(out))
+    return out
+
+
 def block_dots(fmt: int, K: int, wq_row, xq) -> np.ndarray:
     wq_row = _c(wq_row, np.int8 if fmt == FMT_Q8_0 else np.uint8)
     xq = _c(xq, np.int8)
@@ -204,7 +214,7 @@ def matvec(fmt: int, wq, ws, xq, xs) -> np.ndarray:
     ws = _c(np.asarray(ws).view(np.uint16) if np.asarray(ws).dtype == np.float16 else ws,
             np.uint16)
     rows = wq.shape[0]
-    K = wq.shape[1] * (4 if fmt == FMT_Q2S else 1)
+    K = wq.shape[1] * {FMT_Q8_0: 1, FMT_Q2S: 4, FMT_E2M1: 2}[fmt]
     xq = _c(xq, np.int8)
     xs = _c(xs, np.float32)
     out = np.empty(rows, np.float64)

@@ -253,12 +253,30 @@ void ora_decode_q2(uint32_t K, const uint8_t *codes, int8_t *out) {
   }
 }
 
+/* ------------------------------------------------------------------ 4-bit e2m1 */
+/* e2m1 (the OCP microscaling 4-bit float: 1 sign, 2 exponent bits with bias
+ * 1, 1 mantissa bit, no infinities or NaN): code c = s e1 e0 m, value
+ * (-1)^s * (e == 0 ? m / 2 : 2^(e-1) * (1 + m/2)), i.e. 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6.  Weight i of a row sits at bits 4(i%2) of byte i/2 (low nibble first).
+ * Decoded to int8 as TWICE the value (0, 1, 2, 3, 4, 6, 8, 12), so that block
+ * dots stay exact integers; the matvec halves the weight scale. */
+void ora_decode_e2m1(uint32_t K, const uint8_t *codes, int8_t *out) {
+  for (uint32_t i = 0; i < K; ++i) {
+    const int c = (codes[i / 2] >> (4 * (i % 2))) & 15;
+    const int sgn = c >> 3, e = (c >> 1) & 3, m = c & 1;
+    const int twice = e == 0 ? m : (1 << e) + m * (1 << (e - 1)); /* 2 * value */
+    out[i] = (int8_t)(sgn ? -twice : twice);
+  }
+}
+
 /* ------------------------------------------------------------------ A5/A7 dots */
 void ora_block_dots(int32_t fmt, uint32_t K, const void *wq_row, const int8_t *xq,
                     int32_t *isum) {
   int8_t *w = (int8_t *)malloc(K);
   if (fmt == ORA_FMT_Q2S)
     ora_decode_q2(K, (const uint8_t *)wq_row, w);
+  else if (fmt == ORA_FMT_E2M1)
+    ora_decode_e2m1(K, (const uint8_t *)wq_row, w);
   else
     memcpy(w, wq_row, K);
   for (uint32_t b = 0; b < K / 32; ++b) {
@@ -269,18 +287,23 @@ void ora_block_dots(int32_t fmt, uint32_t K, const void *wq_row, const int8_t *x
   free(w);
 }
 
-static size_t row_bytes(int32_t fmt, uint32_t K) { return fmt == ORA_FMT_Q2S ? K / 4 : K; }
+static size_t row_bytes(int32_t fmt, uint32_t K) {
+  return fmt == ORA_FMT_Q2S ? K / 4 : fmt == ORA_FMT_E2M1 ? K / 2 : K;
+}
 
 void ora_matvec(int32_t fmt, uint32_t rows, uint32_t K, const void *wq, const uint16_t *ws,
                 const int8_t *xq, const float *xs, double *out) {
   uint32_t nb = K / 32;
   int32_t *isum = (int32_t *)malloc(sizeof(int32_t) * nb);
+  /* e2m1 block dots are of twice the weights: half the scale (exact) */
+  const double wmul = fmt == ORA_FMT_E2M1 ? 0.5 : 1.0;
   for (uint32_t n = 0; n < rows; ++n) {
     const char *row = (const char *)wq + (size_t)n * row_bytes(fmt, K);
     ora_block_dots(fmt, K, row, xq, isum);
     double acc = 0.0;
     for (uint32_t b = 0; b < nb; ++b)
-      acc += (double)isum[b] * (ora_f16_to_f64(ws[(size_t)n * nb + b]) * (double)xs[b]);
+      acc += (double)isum[b] *
+             (wmul * ora_f16_to_f64(ws[(size_t)n * nb + b]) * (double)xs[b]);
     out[n] = acc;
   }
   free(isum);
@@ -319,7 +342,9 @@ int ora_layer(const ora_desc *desc, const ora_expert *experts, const ora_expert 
   uint32_t E = desc->n_expert, k = desc->top_k, d = desc->d, f = desc->f, fs = desc->f_shared;
   if (E == 0 || k == 0 || k > E || d == 0 || f == 0 || d % 32 || f % 32 || fs % 32)
     return ORA_BAD_ARG;
-  if (desc->routed_fmt != ORA_FMT_Q8_0 && desc->routed_fmt != ORA_FMT_Q2S) return ORA_BAD_ARG;
+  if (desc->routed_fmt != ORA_FMT_Q8_0 && desc->routed_fmt != ORA_FMT_Q2S &&
+      desc->routed_fmt != ORA_FMT_E2M1)
+    return ORA_BAD_ARG;
   uint32_t R = T * k;
   int rc = ORA_OK;
   int32_t *idx = (int32_t *)malloc(sizeof(int32_t) * (R + 1));

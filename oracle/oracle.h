@@ -54,14 +54,15 @@
 extern "C" {
 #endif
 
-enum { ORA_FMT_Q8_0 = 0, ORA_FMT_Q2S = 1 };
+enum { ORA_FMT_Q8_0 = 0, ORA_FMT_Q2S = 1, ORA_FMT_E2M1 = 2 };
 /* scoring of a logit: sigmoid (GLM-5.2, Hy3) or sqrt(softplus) (DeepSeek) */
 enum { ORA_SCORE_SIGMOID = 0, ORA_SCORE_SQRT_SOFTPLUS = 1 };
 enum { ORA_OK = 0, ORA_BAD_ARG = 1, ORA_MISSING_EXPERT = 2, ORA_NO_MEMORY = 3 };
 
 /* One expert's weights, planar: code plane + fp16 scale plane (bit patterns).
- * gate/up: [width][d] (Q2S: [width][d/4] bytes), scales [width][d/32];
- * down: [d][width] (Q2S: [d][width/4]), scales [d][width/32]. */
+ * gate/up: [width][d] (Q2S: [width][d/4] bytes, E2M1: [width][d/2] bytes),
+ * scales [width][d/32]; down: [d][width] (Q2S: [d][width/4], E2M1:
+ * [d][width/2]), scales [d][width/32]. */
 typedef struct {
   const void *gate_q;
   const uint16_t *gate_s;
@@ -73,7 +74,7 @@ typedef struct {
 
 typedef struct {
   uint32_t n_expert, top_k, d, f, f_shared; /* f_shared == 0: no shared expert */
-  int32_t routed_fmt;                       /* ORA_FMT_Q8_0 or ORA_FMT_Q2S */
+  int32_t routed_fmt;                       /* ORA_FMT_Q8_0, ORA_FMT_Q2S or ORA_FMT_E2M1 */
   float s;                                  /* routing scale */
   int32_t score_fn;                         /* ORA_SCORE_* */
 } ora_desc;
@@ -115,6 +116,7 @@ void ora_permute(uint32_t T, uint32_t E, uint32_t k, const int32_t *idx, int32_t
                  int32_t *perm, int32_t *pos);
 void ora_quantize(uint32_t n, const float *x, int8_t *q, float *scale);
 void ora_decode_q2(uint32_t K, const uint8_t *codes, int8_t *out);
+void ora_decode_e2m1(uint32_t K, const uint8_t *codes, int8_t *out);
 void ora_block_dots(int32_t fmt, uint32_t K, const void *wq_row, const int8_t *xq,
                     int32_t *isum);
 void ora_matvec(int32_t fmt, uint32_t rows, uint32_t K, const void *wq, const uint16_t *ws,

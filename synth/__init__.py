@@ -12,8 +12,9 @@ Workload recipe (stand-ins for the GLM-5.2 / Hy3 MoE layers the pages run):
             -beta * 1.1 * ln(rank_e) over a seeded rank permutation
   bias    : N(0, 0.1) per expert (0.1 read as the standard deviation)
   x       : N(0,1) per (token, hidden)
-  weights : int8 uniform on [-127, 127] (or uniform 2-bit codes), fp16 block
-            scale (0.5 + U[0,1)) / (127 * sqrt(K)) (or / (3 * sqrt(K)) for codes)
+  weights : int8 uniform on [-127, 127] (or uniform 2-bit codes, or uniform
+            4-bit e2m1 codes), fp16 block scale (0.5 + U[0,1)) / (m * sqrt(K))
+            with m = 127, 3 or 6, the largest magnitude the codes stand for
 """
 from __future__ import annotations
 
@@ -30,6 +31,7 @@ DEV_LIB = os.path.join(_HERE, "libsynth_dev.so")
 
 FMT_Q8_0 = 0
 FMT_Q2S = 1
+FMT_E2M1 = 2
 
 # stream ids: token-level streams use the token seed, layer-level ones the layer seed
 STREAM_LOGITS = 0
@@ -135,7 +137,7 @@ class LayerSpec:
     d: int           # hidden size
     f: int           # routed expert width
     f_shared: int    # shared expert width (0: no shared expert)
-    fmt: int         # routed weight format: FMT_Q8_0 or FMT_Q2S
+    fmt: int         # routed weight format: FMT_Q8_0, FMT_Q2S or FMT_E2M1
     s: float         # routing scale
     zipf_beta: float  # popularity-offset strength (0: none)
     layer_seed: int = 0
@@ -147,6 +149,10 @@ GLM_LAYER = LayerSpec("e256_k8_d6144_f2048_q8", E=256, k=8, d=6144, f=2048, f_sh
                       fmt=FMT_Q8_0, s=2.5, zipf_beta=0.4)
 Q2_LAYER = LayerSpec("e192_k8_d4096_f1536_q2", E=192, k=8, d=4096, f=1536, f_shared=1536,
                      fmt=FMT_Q2S, s=1.0, zipf_beta=0.4)
+# the 2-bit layer's shape with 4-bit e2m1 routed experts (the same Hy3-sized
+# layer in a format GB300's tensor cores take natively)
+E2M1_LAYER = LayerSpec("e192_k8_d4096_f1536_e2m1", E=192, k=8, d=4096, f=1536, f_shared=1536,
+                       fmt=FMT_E2M1, s=1.0, zipf_beta=0.4)
 
 # Same per-token shapes as GLM_LAYER with 32 experts (1.3 GB of weights, 361 MB
 # read per token): the small case that profiler captures run on.
@@ -171,6 +177,7 @@ WORKLOADS = {
     "batch_t2": (GLM_LAYER, 2, (0,)),
     "prefill_t512": (GLM_LAYER, 512, (0,)),
     "q2_t64": (Q2_LAYER, 64, (0,)),
+    "fp4_t64": (E2M1_LAYER, 64, (0,)),
     "profile_decode_t1": (GLM_LAYER_E32, 1, tuple(range(8))),
     "profile_batch_t16": (GLM_LAYER_E32, 16, (0,)),
     "profile_prefill_t512": (GLM_LAYER_E32, 512, (0,)),
@@ -190,12 +197,12 @@ def expert_dims(spec: LayerSpec, expert: int):
 
 
 def scale_denom(fmt: int, K: int) -> float:
-    return (127.0 if fmt == FMT_Q8_0 else 3.0) * math.sqrt(K)
+    return {FMT_Q8_0: 127.0, FMT_Q2S: 3.0, FMT_E2M1: 6.0}[fmt] * math.sqrt(K)
 
 
 def matrix_shapes(fmt: int, rows: int, K: int):
     """(code-plane shape, scale-plane shape) of a [rows, K] matrix in planar layout."""
-    qcols = K if fmt == FMT_Q8_0 else K // 4
+    qcols = {FMT_Q8_0: K, FMT_Q2S: K // 4, FMT_E2M1: K // 2}[fmt]
     return (rows, qcols), (rows, K // 32)
 
 

@@ -23,8 +23,26 @@ def decode_q2(codes: np.ndarray, K: int) -> np.ndarray:
     return (2 * c.reshape(codes.shape[:-1] + (K,)).astype(np.int16) - 3).astype(np.int8)
 
 
+def decode_e2m1_value(codes: np.ndarray, K: int) -> np.ndarray:
+    """4-bit e2m1 codes (byte i//2, bits 4*(i%2)) -> fp64 values, through
+    numpy's float16 decoding: a normal code (e > 0) is the float16 with the
+    same sign, exponent e - 1 (float16 field e + 14) and its mantissa bit as the
+    top mantissa bit; a subnormal code (e == 0) is m * 0.5."""
+    codes = np.asarray(codes, np.uint8)
+    c = (codes[..., :, None] >> np.array([0, 4], np.uint8)) & 15
+    c = c.reshape(codes.shape[:-1] + (K,)).astype(np.uint16)
+    s, e, m = c >> 3, (c >> 1) & 3, c & 1
+    bits = (s << 15) | ((e + 14) << 10) | (m << 9)
+    v = bits.astype(np.uint16).view(np.float16).astype(np.float64)
+    sub = np.where(s == 1, -0.5, 0.5) * m
+    return np.where(e == 0, sub, v)
+
+
 def dequant(wq, ws, fmt: int, K: int) -> np.ndarray:
     """Planar weights -> fp64 matrix [rows, K]."""
+    if fmt == 2:
+        s = f16_bits_to_f64(np.asarray(ws).view(np.uint16))
+        return decode_e2m1_value(wq, K) * np.repeat(s, 32, axis=1)
     q = decode_q2(wq, K) if fmt == 1 else np.asarray(wq, np.int8)
     s = f16_bits_to_f64(np.asarray(ws).view(np.uint16))  # [rows, K/32]
     return q.astype(np.float64) * np.repeat(s, 32, axis=1)

@@ -203,8 +203,40 @@ def test_decode_q2_mapping_and_order():
     assert np.array_equal(oracle.decode_q2(codes, 256), refmath.decode_q2(codes, 256))
 
 
+# ------------------------------------------------------------------ 4-bit e2m1
+def test_decode_e2m1_table_and_order():
+    """The e2m1 value set (OCP microscaling FP4: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and
+    their negatives, sign in bit 3), decoded as twice the value; low nibble
+    first.  Pinned against the table and against numpy's float16 decoding of
+    the same sign / exponent / mantissa fields."""
+    nib = np.arange(16, dtype=np.uint8)
+    packed = (nib[0::2] | (nib[1::2] << 4)).astype(np.uint8)  # codes 0..15 in order
+    got = oracle.decode_e2m1(packed, 16).astype(np.float64) / 2
+    table = [0, 0.5, 1, 1.5, 2, 3, 4, 6]
+    assert list(got[:8]) == table and list(got[8:]) == [-v for v in table]
+    assert list(oracle.decode_e2m1(np.array([0x71], np.uint8), 2)) == [1, 12]  # low nibble first
+    codes = synth.code2(0, 98, 512)
+    assert np.array_equal(oracle.decode_e2m1(codes, 1024).astype(np.float64) / 2,
+                          refmath.decode_e2m1_value(codes, 1024))
+
+
+def test_matvec_e2m1_halves_the_doubled_dots():
+    """Rows of code 2 (the value 1.0) with scale 1: g = sum of the activations,
+    x codes times their scales, exactly; the block dots are of twice the values."""
+    K = 128
+    rng = np.random.default_rng(23)
+    xq = rng.integers(-127, 128, size=K).astype(np.int8)
+    xs = (rng.random(K // 32) + 0.5).astype(np.float32)
+    wq = np.full((3, K // 2), 0x22, np.uint8)
+    ws = np.full((3, K // 32), np.float16(1.0))
+    want = float((xq.astype(np.float64) * np.repeat(xs.astype(np.float64), 32)).sum())
+    assert np.array_equal(oracle.matvec(2, wq, ws, xq, xs), np.full(3, want))
+    dots = oracle.block_dots(2, K, wq[0], xq)
+    assert np.array_equal(dots, 2 * xq.astype(np.int32).reshape(-1, 32).sum(axis=1))
+
+
 # ------------------------------------------------------------------ A5/A7 block dots
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_block_dots_vs_int64(fmt):
     rng = np.random.default_rng(13 + fmt)
     K = 6144
@@ -212,9 +244,12 @@ def test_block_dots_vs_int64(fmt):
     if fmt == 0:
         w = rng.integers(-127, 128, size=K).astype(np.int8)
         wi = w.astype(np.int64)
-    else:
+    elif fmt == 1:
         w = rng.integers(0, 256, size=K // 4).astype(np.uint8)
         wi = refmath.decode_q2(w, K).astype(np.int64)
+    else:  # twice the e2m1 values, from numpy's float16 decoding
+        w = rng.integers(0, 256, size=K // 2).astype(np.uint8)
+        wi = (2 * refmath.decode_e2m1_value(w, K)).astype(np.int64)
     got = oracle.block_dots(fmt, K, w, xq)
     ref = (wi * xq.astype(np.int64)).reshape(-1, 32).sum(axis=1)
     assert np.array_equal(got.astype(np.int64), ref)
@@ -259,7 +294,7 @@ def _spec(**kw):
     return synth.LayerSpec(**base)
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
 def test_expert_row_matches_dense_fp64(fmt):
     spec = _spec(fmt=fmt, d=512, f=256)
     ex = synth.expert_host(spec, 3)
@@ -302,6 +337,7 @@ def _run_layer(spec, T, seed, want=None, drop_shared=False):
     _spec(),                                                  # the tiny layer
     _spec(E=24, k=6, d=320, f=96, f_shared=64, s=2.5, zipf_beta=0.4),
     _spec(E=12, k=3, d=256, f=128, f_shared=96, fmt=1, s=1.0),
+    _spec(E=12, k=3, d=256, f=128, f_shared=96, fmt=2, s=1.0),     # 4-bit e2m1 experts
     _spec(E=40, k=6, d=256, f=128, f_shared=128, s=1.5, score=1),  # DeepSeek scoring
 ])
 def test_layer_matches_dense_rederivation(spec):
