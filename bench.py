@@ -113,7 +113,7 @@ def load_tensor_peak() -> float:
 # ------------------------------------------------------------------ bytes model
 def row_bytes(fmt: int, K: int) -> int:
     """Bytes of one quantised weight row of K weights: codes + fp16 block scales."""
-    return (K if fmt == 0 else K // 4) + (K // 32) * 2
+    return {0: K, 1: K // 4, 2: K // 2}[fmt] + (K // 32) * 2
 
 
 def tc_tiles(spec, T: int, counts, tc_rows) -> int:
@@ -639,11 +639,12 @@ def percentile(v, q: float) -> float:
 
 def run_sweep(torch, moe, synth, dev, layer, flush, peak):
     """Side measurements at T=2/16/512 on the same layer and T=64 on the 2-bit
-    layer: 10 eager moe_layer calls each after 3 warm-ups, L2 flushed between,
+    and the e2m1 layers: 10 eager moe_layer calls each after 3 warm-ups, L2 flushed between,
     CUDA events around each call (ms_per_step); then 10 more calls with events
     between the stages (stage_us)."""
     out = {}
-    cases = [("batch_t2", layer), ("batch_t16", layer), ("prefill_t512", layer), ("q2_t64", None)]
+    cases = [("batch_t2", layer), ("batch_t16", layer), ("prefill_t512", layer), ("q2_t64", None),
+             ("fp4_t64", None)]
     for name, lay in cases:
         spec, T, seeds = synth.WORKLOADS[name]
         if lay is None:

@@ -72,8 +72,16 @@ typedef enum {
  *   MOE_FMT_Q8_0: int8 codes, row of K weights = K bytes + K/32 fp16.
  *   MOE_FMT_Q2S : 2-bit codes c in {0,1,2,3} meaning {-3,-1,+1,+3}; weight i of
  *                 a row sits at bits 2(i%4) of byte i/4 (LSB first); a row of K
- *                 weights = K/4 bytes + K/32 fp16. */
-typedef enum { MOE_FMT_Q8_0 = 0, MOE_FMT_Q2S = 1 } moe_fmt;
+ *                 weights = K/4 bytes + K/32 fp16.
+ *   MOE_FMT_E2M1: 4-bit e2m1 codes (the OCP microscaling FP4 element: sign bit
+ *                 3, exponent bits 1-2 with bias 1, mantissa bit 0; values 0,
+ *                 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives); weight i at bits
+ *                 4(i%2) of byte i/2 (low nibble first); a row of K weights =
+ *                 K/2 bytes + K/32 fp16.  Its int32 block dots are of TWICE the
+ *                 values (exact integers), so the weight scale enters halved.
+ *                 (The pages' own low-bit formats are not defined on them; this
+ *                 is a 4-bit format GB300's tensor cores take natively.) */
+typedef enum { MOE_FMT_Q8_0 = 0, MOE_FMT_Q2S = 1, MOE_FMT_E2M1 = 2 } moe_fmt;
 
 /* One quantised matrix of all experts: q = code plane, scale = fp16 bits.
  * q must be 32-byte aligned, scale 16-byte aligned. */

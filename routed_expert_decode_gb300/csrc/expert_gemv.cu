@@ -149,7 +149,8 @@ __device__ __forceinline__ void group_dots(const int8_t *const (&w)[NM],
       for (int m = 0; m < NM; ++m)
 #pragma unroll
         for (int f = 0; f < NF; ++f) {
-          sw[m][f] = valid ? half_bits_to_float(ws[m][(size_t)f * nb + b]) : 0.0f;
+          sw[m][f] = valid ? half_bits_to_float(ws[m][(size_t)f * nb + b]) * scale_mul<FMT>()
+                           : 0.0f;
           wb[m][f][j].prep();
         }
 #pragma unroll
@@ -499,8 +500,11 @@ cudaError_t launch_gateup(const Ctx &c, const int32_t *perm) {
   a.tap = (int32_t *)(c.ws + c.L.tap_gu);
   a.routed_fmt = c.desc.routed_fmt;
   const bool taps = (c.desc.flags & MOE_FLAG_DEBUG_TAPS) != 0;
-  return c.desc.routed_fmt == MOE_FMT_Q2S ? gu_maxr<MOE_FMT_Q2S>(c, a, taps)
-                                          : gu_maxr<MOE_FMT_Q8_0>(c, a, taps);
+  switch (c.desc.routed_fmt) {
+    case MOE_FMT_Q2S: return gu_maxr<MOE_FMT_Q2S>(c, a, taps);
+    case MOE_FMT_E2M1: return gu_maxr<MOE_FMT_E2M1>(c, a, taps);
+    default: return gu_maxr<MOE_FMT_Q8_0>(c, a, taps);
+  }
 }
 
 cudaError_t launch_requant_h(const Ctx &c) {
@@ -537,8 +541,11 @@ cudaError_t launch_down(const Ctx &c) {
   a.o = (float *)(c.ws + c.L.o);
   a.tap = (int32_t *)(c.ws + c.L.tap_dn);
   const bool taps = (c.desc.flags & MOE_FLAG_DEBUG_TAPS) != 0;
-  return c.desc.routed_fmt == MOE_FMT_Q2S ? dn_maxr<MOE_FMT_Q2S>(c, a, taps)
-                                          : dn_maxr<MOE_FMT_Q8_0>(c, a, taps);
+  switch (c.desc.routed_fmt) {
+    case MOE_FMT_Q2S: return dn_maxr<MOE_FMT_Q2S>(c, a, taps);
+    case MOE_FMT_E2M1: return dn_maxr<MOE_FMT_E2M1>(c, a, taps);
+    default: return dn_maxr<MOE_FMT_Q8_0>(c, a, taps);
+  }
 }
 
 cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,

@@ -22,8 +22,9 @@
 // MAT = 2: gate and up, epilogue h = silu(g)*u requantised per 32 features;
 // MAT = 1: down, epilogue o.
 // RFMT: format of the routed experts' weights.  2-bit routed weights (code c in
-// {0..3} meaning 2c - 3) are decoded by the converters into fp16 as exactly as
-// int8 codes are, so the MMA computes the same exact integer block dots; the
+// {0..3} meaning 2c - 3) and 4-bit e2m1 weights (as twice their values, the
+// integers 0, +-1, .., +-12) are decoded by the converters into fp16 as exactly
+// as int8 codes are, so the MMA computes the same exact integer block dots; the
 // shared expert is always Q8_0.
 #include <cuda.h>
 #include <string.h>
@@ -63,6 +64,7 @@ struct TcArgs {
   uint32_t tap_nb;                       // blocks per tap row
   uint32_t *err;
   const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
+  float routed_wmul;     // factor of the routed weight scales (0.5: e2m1 dots are of 2v)
   uint32_t n_stages, stage_bytes;
   unsigned long long *trace;  // MOE_FLAG_TRACE: kTcTraceWords per CTA, else null
 };
@@ -196,15 +198,6 @@ __device__ __forceinline__ void i8x4_to_h2x2(uint32_t w, uint32_t &lo, uint32_t 
   hi = *reinterpret_cast<uint32_t *>(&b);
 }
 
-// prmt.b32 in its generic mode: byte n of the result is byte (c >> 4n) & 7 of
-// {b, a} -- or, when bit 4n+3 of c is set, that byte's sign bit replicated
-// (the CUDA intrinsic __byte_perm ignores that bit)
-__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t c) {
-  uint32_t d;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
-  return d;
-}
-
 // 16 2-bit codes (byte b: codes 4b..4b+3, LSB first) -> eight half2 of 2c - 3,
 // in K order: out[2b] = codes (4b, 4b+1), out[2b+1] = codes (4b+2, 4b+3).
 // t_i holds code 4b+i in the low bits of byte b, under 0x3C; a byte permute puts
@@ -318,6 +311,7 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
   const int feat = quarter * 32 + lane;  // feature within the tile (TMEM lane)
   const bool sh = t.e == (int)a.E;
   const int width = MAT == 2 ? (int)(sh ? a.fs : a.f) : (int)a.d;
+  const float wmul = sh ? 1.0f : a.routed_wmul;  // exact (a power of two)
   const int col0 = SPLIT ? 0 : 32 * half;
   // accumulator pairs (columns 2i, 2i+1): the scale products and FMAs run as
   // packed fp32x2 operations, each lane rounded as the scalar operation would be
@@ -380,8 +374,8 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
       for (int mi = 0; mi < MAT; ++mi) {
         const uint32_t pair =
             *reinterpret_cast<const uint32_t *>(wsl + ((size_t)mi * kBM + feat) * 8 + blk0);
-        wsc[mi][0] = half_bits_to_float((uint16_t)(pair & 0xFFFFu));
-        wsc[mi][1] = half_bits_to_float((uint16_t)(pair >> 16));
+        wsc[mi][0] = half_bits_to_float((uint16_t)(pair & 0xFFFFu)) * wmul;
+        wsc[mi][1] = half_bits_to_float((uint16_t)(pair >> 16)) * wmul;
       }
 #pragma unroll
       for (int bi = 0; bi < 2; ++bi) {
@@ -594,11 +588,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             break;
           }
           uint8_t *st = tsm + (size_t)s * a.stage_bytes;
-          const bool q2 = RFMT == MOE_FMT_Q2S && !sh;  // 2-bit codes: K/4 bytes a row
-          bar_expect(&ld_full[s], MAT * (q2 ? kA2 : kA8) + kB16);
+          // code bytes a row per stage: 64 (int8), 16 (2-bit), 32 (e2m1)
+          const uint32_t rb = sh || RFMT == MOE_FMT_Q8_0 ? kBK
+                              : RFMT == MOE_FMT_Q2S     ? kBK / 4
+                                                        : kBK / 2;
+          bar_expect(&ld_full[s], MAT * kBM * rb + kB16);
           for (int mi = 0; mi < MAT; ++mi)
             tma_2d(st + MAT * kA16 + kB16 + mi * kA8, sh ? &maps.sw[mi] : &maps.w[mi],
-                   (int)(ks * (q2 ? kBK / 4 : kBK)), wrow, &ld_full[s]);
+                   (int)(ks * rb), wrow, &ld_full[s]);
           tma_2d(st + MAT * kA16, &maps.act, (int)(ks * kBK), t.slot0 + t.n0, &ld_full[s]);
         }
       }
@@ -654,8 +651,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int r = tid - 64;
     uint32_t g = 0;
     for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
-      // 2-bit routed tile (the shared expert is Q8_0)
-      const bool q2 = RFMT == MOE_FMT_Q2S && tc_tile<MAT>(P, a, tile).e != (int)a.E;
+      // a 2-bit or e2m1 routed tile (the shared expert is Q8_0)
+      const bool routed = RFMT != MOE_FMT_Q8_0 && tc_tile<MAT>(P, a, tile).e != (int)a.E;
+      const bool q2 = RFMT == MOE_FMT_Q2S && routed;
+      const bool f4 = RFMT == MOE_FMT_E2M1 && routed;
       for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
         const uint32_t s = g % NS, use = g / NS;
         const long long tw = clock64();
@@ -667,6 +666,41 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         uint8_t *st = tsm + (size_t)s * a.stage_bytes;
+        if (f4) {
+          // row r's 32 code bytes = 64 e2m1 codes, 8 a word: word j -> fp16
+          // chunk j (K 8j..8j+7) as the biased bytes 2v + 12 under 2^10, minus
+          // 1036 (exact), at position j ^ (r&7) of its swizzled row
+          const __half2 k1036 = __halves2half2(__ushort_as_half(0x640C), __ushort_as_half(0x640C));
+          for (int mi = 0; mi < MAT; ++mi) {
+            const uint4 *src = (const uint4 *)(st + MAT * kA16 + kB16 + mi * kA8 + r * (kBK / 2));
+            uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
+#pragma unroll
+            for (int hq = 0; hq < 2; ++hq) {
+              const uint4 cw = src[hq];
+              const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const int j = 4 * hq + v;
+                uint32_t hh[4];
+#pragma unroll
+                for (int hw = 0; hw < 2; ++hw) {
+                  const uint32_t t = e2m1x4_biased(wv[v] >> (16 * hw));
+                  uint32_t lo = __byte_perm(t, 0x64646464u, 0x5140);
+                  uint32_t hi = __byte_perm(t, 0x64646464u, 0x7362);
+                  __half2 a0 = __hsub2(*reinterpret_cast<__half2 *>(&lo), k1036);
+                  __half2 a1 = __hsub2(*reinterpret_cast<__half2 *>(&hi), k1036);
+                  hh[2 * hw] = *reinterpret_cast<uint32_t *>(&a0);
+                  hh[2 * hw + 1] = *reinterpret_cast<uint32_t *>(&a1);
+                }
+                *(uint4 *)(dst_row + ((j ^ (r & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
+              }
+            }
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) bar_arrive(&a_ready[s]);
+          continue;
+        }
         if (q2) {
           // row r's 16 code bytes (rows 16 B apart: a quarter-warp reads 128
           // contiguous bytes) -> 8 fp16 chunks; chunk j lands at position
@@ -847,9 +881,12 @@ cudaError_t run_tc(const Ctx &c, const TcArgs &a, const TcMaps &maps, size_t sme
 }  // namespace
 
 // the scale rows (K/32 fp16) of every matrix must be whole 16-byte TMA rows (and
-// a 2-bit code row, K/4 bytes, a multiple of 16 bytes: K % 256 covers both)
+// a 2-bit or e2m1 code row, K/4 or K/2 bytes, a multiple of 16 bytes: K % 256
+// covers all)
 bool tc_supported(const moe_desc &D) {
-  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S) return false;
+  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S &&
+      D.routed_fmt != MOE_FMT_E2M1)
+    return false;
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   return encode_fn() != nullptr;
 }
@@ -857,7 +894,9 @@ bool tc_supported(const moe_desc &D) {
 // can any expert of a T-token call land on the tensor path (workspace sizing)?
 bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.flags & MOE_FLAG_FORCE_GEMV) return false;
-  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S) return false;
+  if (D.routed_fmt != MOE_FMT_Q8_0 && D.routed_fmt != MOE_FMT_Q2S &&
+      D.routed_fmt != MOE_FMT_E2M1)
+    return false;
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   // unforced, only from kTcMinTokens tokens: below that no expert brings enough
   // tiles to pay for the tensor kernels and their activation copies
@@ -902,8 +941,11 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
                                                      : nullptr;
   const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
   const bool q2 = D.routed_fmt == MOE_FMT_Q2S;
-  // routed code planes: int8 [rows][K], box 64 x 128; 2-bit [rows][K/4] bytes, box 16 x 128
-  const uint32_t qdiv = q2 ? 4 : 1;
+  const bool f4 = D.routed_fmt == MOE_FMT_E2M1;
+  // routed code planes: int8 [rows][K], box 64 x 128; 2-bit [rows][K/4] bytes,
+  // box 16 x 128; e2m1 [rows][K/2] bytes, box 32 x 128
+  const uint32_t qdiv = q2 ? 4 : f4 ? 2 : 1;
+  a.routed_wmul = f4 ? 0.5f : 1.0f;
   bool ok = true;
   if (mat == 2) {
     a.K = D.d;
@@ -998,6 +1040,13 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
                   : run_tc<2, false, MOE_FMT_Q2S>(c, a, maps, smem);
     return taps ? run_tc<1, true, MOE_FMT_Q2S>(c, a, maps, smem)
                 : run_tc<1, false, MOE_FMT_Q2S>(c, a, maps, smem);
+  }
+  if (f4) {
+    if (mat == 2)
+      return taps ? run_tc<2, true, MOE_FMT_E2M1>(c, a, maps, smem)
+                  : run_tc<2, false, MOE_FMT_E2M1>(c, a, maps, smem);
+    return taps ? run_tc<1, true, MOE_FMT_E2M1>(c, a, maps, smem)
+                : run_tc<1, false, MOE_FMT_E2M1>(c, a, maps, smem);
   }
   if (mat == 2)
     return taps ? run_tc<2, true, MOE_FMT_Q8_0>(c, a, maps, smem)

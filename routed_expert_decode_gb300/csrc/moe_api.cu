@@ -19,7 +19,9 @@ bool desc_ok(const moe_desc *d) {
   if (d->n_expert < 1 || d->n_expert > 1024) return false;
   if (d->top_k < 1 || d->top_k > d->n_expert || d->top_k > 32) return false;
   if (d->d == 0 || d->d % 32 || d->f == 0 || d->f % 32 || d->f_shared % 32) return false;
-  if (d->routed_fmt != MOE_FMT_Q8_0 && d->routed_fmt != MOE_FMT_Q2S) return false;
+  if (d->routed_fmt != MOE_FMT_Q8_0 && d->routed_fmt != MOE_FMT_Q2S &&
+      d->routed_fmt != MOE_FMT_E2M1)
+    return false;
   if (!(d->s == d->s)) return false;  // NaN scale
   if (d->score != MOE_SCORE_SIGMOID && d->score != MOE_SCORE_SQRT_SOFTPLUS) return false;
   // int32 indexing of rows and work items
@@ -30,7 +32,7 @@ bool desc_ok(const moe_desc *d) {
 
 bool mat_ok(const moe_mat &m, int fmt) {
   if (!m.q || !m.scale) return false;
-  if (!aligned(m.q, fmt == MOE_FMT_Q2S ? 8 : 32)) return false;
+  if (!aligned(m.q, fmt == MOE_FMT_Q2S ? 8 : fmt == MOE_FMT_E2M1 ? 16 : 32)) return false;
   if (!aligned(m.scale, 2)) return false;
   return true;
 }

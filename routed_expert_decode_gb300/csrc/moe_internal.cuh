@@ -260,6 +260,70 @@ struct WBlock<MOE_FMT_Q2S> {
   }
 };
 
+// prmt.b32 in its generic mode: byte n of the result is byte (c >> 4n) & 7 of
+// {b, a} -- or, when bit 4n+3 of c is set, that byte's sign bit replicated
+// (the CUDA intrinsic __byte_perm ignores that bit)
+__device__ __forceinline__ uint32_t prmt_sx(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
+// Four 4-bit e2m1 codes (the low 16 bits of w, code j at bits 4j..4j+3: sign
+// bit 3, exponent bits 1-2 with bias 1, mantissa bit 0) -> four bytes holding
+// TWICE the value plus 12: 2v is one of 0, 1, 2, 3, 4, 6, 8, 12 or its
+// negative, so every byte is 0..24.  One byte permute looks up the positive
+// and one the negative table (indexed by the code's low 3 bits); a third, with
+// the sign bit as its sign-replicate flag over bytes 0x80, gives 0xFF for a
+// negative code and 0x80 for a positive one, and since both tables' bytes are
+// below 128 that word selects between them bit by bit.
+__device__ __forceinline__ uint32_t e2m1x4_biased(uint32_t w) {
+  const uint32_t sel = w & 0x7777u;
+  const uint32_t pos = __byte_perm(0x0F0E0D0Cu, 0x18141210u, sel);  // 12 + (0,1,2,3,4,6,8,12)
+  const uint32_t neg = __byte_perm(0x090A0B0Cu, 0x00040608u, sel);  // 12 - (0,1,2,3,4,6,8,12)
+  const uint32_t m = prmt_sx(0x80808080u, 0x80808080u, w & 0xFFFFu);
+  return (m & neg) | (~m & pos);
+}
+
+// e2m1: 16 bytes = 32 codes (low nibble first); prep() decodes them once per
+// block into 8 words of biased bytes 2v + 12 (natural order, like the int8
+// activation codes), and dot = sum (2v + 12) x - 12 sum x = sum 2v x, exact.
+// The block dot is of twice the weights: kScaleMul halves the weight scale.
+__device__ __forceinline__ uint4 ld_stream16(const void *p) {
+  uint4 w;
+  asm("ld.global.nc.L1::no_allocate.v4.b32 {%0,%1,%2,%3}, [%4];"
+      : "=r"(w.x), "=r"(w.y), "=r"(w.z), "=r"(w.w)
+      : "l"(p));
+  return w;
+}
+
+template <>
+struct WBlock<MOE_FMT_E2M1> {
+  uint4 c;
+  uint32_t t[8];
+  static constexpr int kRowBytesPer32 = 16;
+  static constexpr bool kNeedSum = true;
+  __device__ __forceinline__ void load(const int8_t *row, int b) { c = ld_stream16(row + 16 * b); }
+  __device__ __forceinline__ void prep() {
+    const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      t[2 * q] = e2m1x4_biased(w[q]);
+      t[2 * q + 1] = e2m1x4_biased(w[q] >> 16);
+    }
+  }
+  __device__ __forceinline__ int dot(const W8 &x, int sum_x) const {
+    int s = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) s = __dp4a((int)t[q], (int)x.v[q], s);
+    return s - 12 * sum_x;
+  }
+};
+
+// weight-scale factor of a format's block dots (e2m1 dots are of twice the values)
+template <int FMT>
+__host__ __device__ constexpr float scale_mul() { return FMT == MOE_FMT_E2M1 ? 0.5f : 1.0f; }
+
 // sum of the 32 int8 codes of an activation block
 __device__ __forceinline__ int block_sum(const W8 &x) {
   int s = 0;
@@ -269,7 +333,7 @@ __device__ __forceinline__ int block_sum(const W8 &x) {
 }
 
 __host__ __device__ inline size_t row_bytes(int fmt, uint32_t K) {
-  return fmt == MOE_FMT_Q2S ? K / 4 : K;
+  return fmt == MOE_FMT_Q2S ? K / 4 : fmt == MOE_FMT_E2M1 ? K / 2 : K;
 }
 
 // tapped feature j of a row of `width` outputs

@@ -27,6 +27,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 6: "MOE_ERR_DEVICE_CHECK"}
 FMT_Q8_0 = 0
 FMT_Q2S = 1
+FMT_E2M1 = 2
 FLAG_DEBUG_TAPS = 0x1
 FLAG_FORCE_GEMV = 0x2
 FLAG_FORCE_TC = 0x4

@@ -65,6 +65,7 @@ CASES = [
     ("gemv_t9", _spec(), 9, 0),
     ("tc_t40", _spec(E=16, k=4, d=512, f=256, f_shared=256), 40, "tc"),
     ("q2_t13", _spec(E=48, k=8, d=1024, f=256, f_shared=256, fmt=1, s=1.0), 13, 0),
+    ("fp4_tc_t40", _spec(E=16, k=4, d=512, f=256, f_shared=256, fmt=2, s=1.0), 40, "tc"),
     ("decode_shape_t1", synth.GLM_LAYER_E32, 1, 0),
     ("decode_shape_t16", synth.GLM_LAYER_E32, 16, 0),
 ]

@@ -21,6 +21,7 @@ SMALL = [
     ("tiny_ragged_t37", synth.TINY, 37),
     ("shared_e64", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 9),
     ("e192_q2", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=1, zipf_beta=0.4), 13),
+    ("e192_fp4", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=2, zipf_beta=0.4), 13),
     ("e384_k6", _spec(E=384, k=6, d=256, f=96, f_shared=64, s=1.5), 7),
     ("e256_d6144", _spec(E=256, k=8, d=6144, f=64, f_shared=96, s=2.5, zipf_beta=0.4), 3),
     ("k1_s1", _spec(E=16, k=1, d=256, f=128), 6),
@@ -241,6 +242,18 @@ def test_q2_t64_full_size(gpu):
                                   flags=moe.FLAG_FORCE_GEMV))
 
 
+def test_fp4_t64_full_size(gpu):
+    """The e2m1 layer (the 2-bit layer's shape) at T=64, auto dispatch and
+    dp4a-only: the same exact block dots on both paths."""
+    from routed_expert_decode_gb300 import moe
+
+    layer = device_layer(synth.E2M1_LAYER, gpu)
+    assert moe.tc_min_rows(layer.desc(), 64) == 4
+    print("fp4_t64", run_case(synth.E2M1_LAYER, 64, seed=0, device=gpu, sample=[0, 33, 63]))
+    print("fp4_t64 gemv", run_case(synth.E2M1_LAYER, 64, seed=0, device=gpu, sample=[0, 63],
+                                   flags=moe.FLAG_FORCE_GEMV))
+
+
 # ---------------------------------------------------------------- fused decode kernel (T <= 2)
 FUSED = [
     ("fused_e64_t1", _spec(E=64, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 1),
@@ -338,6 +351,11 @@ TC_CASES = [
                            zipf_beta=0.4), 9),
     ("tc_q2_d4096", _spec(E=24, k=8, d=4096, f=512, f_shared=512, fmt=1, s=1.0), 33),
     ("tc_q2_noshared", _spec(E=8, k=2, d=1024, f=768, f_shared=0, fmt=1, s=1.0), 21),
+    # e2m1 routed weights decoded to fp16 as twice their values (scale halved)
+    ("tc_fp4_forced", _spec(E=16, k=4, d=512, f=256, f_shared=256, fmt=2, s=1.0,
+                            zipf_beta=0.4), 9),
+    ("tc_fp4_d4096", _spec(E=24, k=8, d=4096, f=512, f_shared=512, fmt=2, s=1.0), 33),
+    ("tc_fp4_noshared", _spec(E=8, k=2, d=1024, f=768, f_shared=0, fmt=2, s=1.0), 21),
 ]
 
 
@@ -474,6 +492,8 @@ POISON = [
     ("tc_forced_t40", _spec(E=16, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4), 40, "tc"),
     ("tc_auto_t512", synth.GLM_LAYER_E32, 512, 0),
     ("q2_t13", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=1, zipf_beta=0.4), 13, 0),
+    ("fp4_t13", _spec(E=192, k=8, d=512, f=192, f_shared=160, fmt=2, zipf_beta=0.4), 13, 0),
+    ("fp4_tc_t40", _spec(E=16, k=4, d=512, f=256, f_shared=256, fmt=2, s=1.0), 40, "tc"),
 ]
 
 

@@ -30,7 +30,9 @@ def _layer(spec, dev):
     (synth.GLM_LAYER_E32, 16),
     (synth.LayerSpec("na_q2", E=48, k=8, d=1024, f=384, f_shared=256, fmt=1, s=1.0,
                      zipf_beta=0.4), 5),
-], ids=["e64_t9", "decode_shape_t1", "decode_shape_t16", "q2_t5"])
+    (synth.LayerSpec("na_fp4", E=16, k=4, d=512, f=256, f_shared=256, fmt=2, s=1.0,
+                     zipf_beta=0.4), 40),
+], ids=["e64_t9", "decode_shape_t1", "decode_shape_t16", "q2_t5", "fp4_t40"])
 def test_noalloc_matches_workspace_entry_twice(gpu, spec, T):
     """Same kernels, same inputs: the output equals moe_layer's bit for bit, on
     two calls in a row, and the static scratch's error word stays clear."""
