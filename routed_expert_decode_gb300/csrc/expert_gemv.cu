@@ -71,15 +71,6 @@ __host__ __device__ constexpr int min_ctas() {
 template <int FMT, int MAXR>
 __host__ __device__ constexpr int min_ctas_dn() { return 2; }
 
-__device__ __forceinline__ int find_slot(const int *prefix, int U, int item) {
-  int lo = 0, hi = U;
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (prefix[mid] <= item) lo = mid; else hi = mid;
-  }
-  return lo;
-}
-
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
@@ -95,23 +86,6 @@ __device__ __forceinline__ int tap_index(uint32_t n, uint32_t width) {
     if (tap_feature(j, width) == n) jt = j;
   return jt;
 }
-
-// The plan's dp4a expert list (act_e, act_row0, act_rows, item_gu: 4(E+1)+1
-// consecutive ints) copied into shared memory, so that the per-item lookups
-// cost no global round trips.
-struct SmemPlan {
-  const int *e, *row0, *rows, *item;
-  __device__ SmemPlan(int *sm, const PlanView &P, uint32_t E) {
-    const int n = 4 * (int)(E + 1) + 1;
-    for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = P.act_e[i];
-    __syncthreads();
-    e = sm;
-    row0 = sm + (E + 1);
-    rows = row0 + (E + 1);
-    item = rows + (E + 1);
-  }
-};
-inline size_t smem_plan_bytes(uint32_t E) { return sizeof(int) * (4 * (size_t)(E + 1) + 1); }
 
 // acc[m][f][r] += sum over the K/32 blocks b of
 //   dot(codes of row f of matrix m, codes of activation row r) * w-scale * x-scale
@@ -474,6 +448,7 @@ cudaError_t dn_maxr(const Ctx &c, const DNArgs &a, bool taps) {
 
 cudaError_t launch_gateup(const Ctx &c, const int32_t *perm) {
   if (c.T == 0) return cudaSuccess;
+  if (stream_gateup_ok(c)) return launch_gateup_stream(c, perm);
   GUArgs a;
   a.plan = (const int *)(c.ws + c.L.plan);
   a.E = c.desc.n_expert;
@@ -522,6 +497,7 @@ cudaError_t launch_requant_h(const Ctx &c) {
 
 cudaError_t launch_down(const Ctx &c) {
   if (c.T == 0) return cudaSuccess;
+  if (stream_down_ok(c)) return launch_down_stream(c);
   DNArgs a;
   a.plan = (const int *)(c.ws + c.L.plan);
   a.E = c.desc.n_expert;

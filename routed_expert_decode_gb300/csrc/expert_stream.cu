@@ -1,0 +1,733 @@
+// expert_stream.cu -- dp4a expert FFN for small batches, the weights streamed
+// into shared memory by the bulk-copy engine.
+//
+// The multi-kernel path's experts with few rows (every expert below 32 tokens a
+// call, the experts with at most 4 rows above) are bound by the weight stream:
+// each selected expert's rows are read once per call and applied to all of its
+// rows (the union-of-experts read of NeutronStar README, "MTP speculative
+// decoding"; the indexed per-expert FFN).  Rather than every warp loading its
+// weight codes into registers (a few KB in flight per warp), one producer lane
+// per CTA streams each work item's slice of one expert's weight rows with
+// cp.async.bulk (one-CTA copies, no multicast) into a ring of four ~52 KB
+// shared-memory stages, ~200 KB per SM in flight, and 12 consumer warps compute
+// from shared memory with dp4a (the dp4a expert kernels of "What this branch
+// adds over upstream").
+//
+//  * One CTA per SM, persistent; no CTA waits on another.  The routed experts'
+//    items go out in chunks of 8 consecutive ones (slices of one expert,
+//    mostly, whose activation rows then stay in L1), chunk c to CTA c % G (G
+//    CTAs), so that a hot expert's items -- more rows, more passes -- spread
+//    over many CTAs; then the shared expert's items one by one, item j to CTA
+//    j % G: the shared expert has a row per token, its items cost the most.
+//  * The CTA's i-th item goes to stage i % 4 and is read by consumer group
+//    i % 3 (4 warps).  Each group takes its items in order, and item i waits
+//    only for item i - 4 to leave its stage, so the ring always moves.  13
+//    warps: at most 4 on each of the SM's four sub-partitions, so a thread may
+//    hold 128 registers.
+//  * The stage's previous item i - 4 belongs to another group, so a group
+//    reaching item i can find that item still in flight: its full barrier is
+//    then two phases behind, where a parity wait would pass at once.  A
+//    consumer therefore first waits for the release of item i - 4 (the empty
+//    barrier, at most one phase behind: the producer issued item i - 4 only
+//    after item i - 8 was released), then for item i's bytes.
+//  * The producer looks one item ahead: the next item's plan lookup and its
+//    first rows' tokens (the permutation) are in flight while it issues the
+//    current item's copies, and each stage starts with a header (expert rows,
+//    first output, the first rows' activation rows) that the consumers read
+//    instead of repeating the lookup.
+//  * Gate/up item: 4 consecutive features of one expert, their gate and up rows
+//    (K int8 codes + K/32 fp16 scales each).  Warp q of the group takes K
+//    quarter q of all four features for every row of the expert, in passes of
+//    2 rows whose activation chunks it loads at once; the quarters' partial
+//    sums meet in shared memory, summed in quarter order, and h = silu(g)*u
+//    goes out in fp32; the requantisation kernel follows.
+//  * Down item: 4*RW consecutive output rows of one expert's down matrix; warp
+//    w takes RW of them against the h codes of every row (slot) of the expert,
+//    in passes of 2 slots whose h chunks it loads at once.
+//  * Lane l holds 16-byte chunks: half of a 32-block each, whose exact int32
+//    sum the lane scales itself (w-scale * x-scale); the block's two halves
+//    meet in the warp sum (the same terms as a whole-block sum, another fp32
+//    order).  The block-dot taps join the halves with one shuffle.
+//  * Every wait is bounded; on timeout the kernel flags kErrTimeout, stops
+//    issuing, waits (bounded) for the copies it has in flight and exits.
+#include "stream_ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kStStages = 4;                           // shared-memory stages
+constexpr int kStGroups = 3;                           // consumer groups
+constexpr int kStGroupWarps = 4;                       // consumer warps per group
+constexpr int kStConsWarps = kStGroups * kStGroupWarps;
+constexpr int kStProdWarp = kStConsWarps;              // lane 0 issues the copies
+constexpr int kStThreads = (kStConsWarps + 1) * 32;
+constexpr int kStRows = 2;                             // activation rows per pass
+constexpr int kHdrRows = 8;                            // rows whose activation row a header holds
+constexpr long long kStWaitCycles = 4000000000ll;      // ~2 s at 2 GHz
+constexpr uint32_t kStBarBytes = 128;                  // 11 mbarriers + the abort flag
+constexpr uint32_t kStSmemMax = 227u * 1024u;          // opt-in dynamic shared memory a CTA
+constexpr uint32_t kStHdrBytes = 64;                   // stage header
+// gate/up partial sums: [group][2 pass parities][4 quarters][16 values] fp32
+constexpr int kGuVals = 2 * kStGroupWarps * kStRows;  // gate/up x feature x row
+constexpr uint32_t kStPartFloats = kStGroups * 2 * kStGroupWarps * kGuVals;
+// largest stage: the dynamic shared memory of one CTA (227 KB) less the plan
+// of a 1024-expert layer, the barriers and the partial sums, over the stages
+constexpr uint32_t kStStageMax =
+    (kStSmemMax - (uint32_t)(sizeof(int) * (4 * 1025 + 1)) - kStBarBytes - 4 * kStPartFloats) /
+    kStStages / 16 * 16;
+// x chunks per lane per row: K/64 chunks a quarter, d <= 6144
+constexpr int kGuJ = 3;
+// h chunks per lane per row and segment in the down stage
+constexpr int kDnJ = 2;
+
+struct StArgs {
+  const int *plan;
+  uint32_t E, k, d, f, fs, R;
+  uint32_t K, Ks;             // reduction length of a routed / shared row
+  uint32_t out_per_e;         // down: output rows per expert (d)
+  const int8_t *q[2], *sq[2];        // routed / shared codes (gate/up: gate, up; down: down)
+  const uint16_t *sc[2], *ssc[2];    // their block scales
+  uint32_t rows_per_slot;     // routed weight rows per expert slot (gate/up: f; down: d)
+  const int32_t *eslot;       // expert -> weight slot, or null
+  const int8_t *act;          // activation codes: x [T][d] (gate/up), h [slots][fmax] (down)
+  const float *act_s;         // their block scales
+  uint32_t act_stride, act_s_stride;
+  const int32_t *perm;        // gate/up: slot -> row (token = row / k)
+  float *out;                 // gate/up: h [slots][out_stride]; down: o [slots][out_stride]
+  uint32_t out_stride;
+  int32_t *tap;               // MOE_FLAG_DEBUG_TAPS, else null
+  uint32_t tap_nb;            // blocks per tap row
+  uint32_t *err;
+  uint32_t stage_bytes;
+  unsigned long long *trace;  // MOE_FLAG_TRACE: this kernel's words of the trace region, else null
+};
+
+// MOE_FLAG_TRACE words per CTA (SM cycles), at kStTraceBase + (down ? kStTraceDown : 0)
+// + CTA * kStTraceStride of the workspace's trace region
+enum : int {
+  kStTrProdWait = 0,    // producer waiting for a free stage
+  kStTrItems = 1,       // items issued
+  kStTrProdTotal = 2,   // producer: kernel entry to its last copy landed
+  kStTrSetup = 3,       // kernel entry to the first copy issued
+  kStTrConsWait = 4,    // + warp: consumer warp waiting for a full stage
+  kStTrConsWork = 16,   // + warp: consumer warp computing
+  kStTraceStride = 32,
+  kStTraceBase = 16384,
+  kStTraceDown = 8192,
+  kStTraceCtas = 256
+};
+
+__device__ __forceinline__ uint4 ldg16(const int8_t *p) {
+  return __ldg(reinterpret_cast<const uint4 *>(p));
+}
+
+// stage header, written by the producer before it arms the stage's barrier
+struct StageHdr {
+  int row0, nrows, n0, sh;  // expert's first slot, its rows, first output, shared expert?
+  int K;                    // reduction length
+  int act_row[kHdrRows];    // gate/up: the tokens of its first rows
+  int pad[3];
+};
+static_assert(sizeof(StageHdr) == kStHdrBytes, "stage header size");
+
+// one work item: rows [n0, n0 + rows) of each of the MAT matrices of an expert
+struct Item {
+  int row0, nrows, n0;
+  bool sh;
+  uint32_t K;
+  const int8_t *q[2];
+  const uint16_t *s[2];
+};
+
+// item g of the call: gate/up items are 4 features (prefix S.item in features);
+// down items are NROWS output rows, out_per_e / NROWS of them per expert
+template <int MAT, int NROWS>
+__device__ __forceinline__ Item item_at(const StArgs &a, const SmemPlan &S, int U, int g) {
+  Item it;
+  int u, n0;
+  if (MAT == 2) {
+    const int feat = g * NROWS;
+    u = find_slot(S.item, U, feat);
+    n0 = feat - S.item[u];
+  } else {
+    const int per = (int)(a.out_per_e / NROWS);
+    u = g / per;
+    n0 = (g - u * per) * NROWS;
+  }
+  const int e = S.e[u];
+  it.row0 = S.row0[u];
+  it.nrows = S.rows[u];
+  it.n0 = n0;
+  it.sh = e == (int)a.E;
+  it.K = it.sh ? a.Ks : a.K;
+  // first weight row of the item in its matrix (k_plan validated the slot)
+  const size_t r = it.sh ? (size_t)n0
+                         : (size_t)weight_slot(a.eslot, e) * a.rows_per_slot + (size_t)n0;
+#pragma unroll
+  for (int m = 0; m < MAT; ++m) {
+    it.q[m] = (it.sh ? a.sq[m] : a.q[m]) + r * it.K;
+    it.s[m] = (it.sh ? a.ssc[m] : a.sc[m]) + r * (it.K / 32);
+  }
+  return it;
+}
+
+// The CTA's items in order: chunks of kChunk consecutive routed items (slices
+// of one expert, mostly), chunk b, b + G, b + 2G, .., then every G-th item of
+// the shared expert's (which come last in the plan).
+constexpr int kChunk = 8;
+struct Schedule {
+  int b, G;
+  int r_n;    // routed items of this CTA
+  int s0;     // its first shared item; then every G-th
+  int count;
+  __device__ __forceinline__ int item(int i) const {
+    return i < r_n ? (b + (i / kChunk) * G) * kChunk + i % kChunk : s0 + (i - r_n) * G;
+  }
+};
+
+template <int MAT, int NROWS>
+__device__ __forceinline__ Schedule schedule_of(const StArgs &a, const SmemPlan &S, int U,
+                                                int items, int b, int G) {
+  // items of the routed experts: all but the shared expert's, when it is on this list
+  int routed = items;
+  if (U > 0 && S.e[U - 1] == (int)a.E)
+    routed = MAT == 2 ? S.item[U - 1] / NROWS : (U - 1) * (int)(a.out_per_e / NROWS);
+  Schedule sc;
+  sc.b = b;
+  sc.G = G;
+  // chunks b, b + G, ..; only the call's last chunk can be short, and it is
+  // the last one of the CTA that holds it
+  const int nch = (routed + kChunk - 1) / kChunk;
+  const int mine = b < nch ? (nch - 1 - b) / G + 1 : 0;
+  sc.r_n = mine * kChunk;
+  if (mine > 0 && b + (mine - 1) * G == nch - 1) sc.r_n -= nch * kChunk - routed;
+  const int shared = items - routed;
+  sc.s0 = routed + b;
+  sc.count = sc.r_n + (b < shared ? (shared - 1 - b) / G + 1 : 0);
+  return sc;
+}
+
+// activation row of slot p: its token (gate/up: the shared expert's slots R..
+// are the tokens in order, a routed slot's row comes from the permutation) or
+// the slot itself (down: h rows are per slot)
+template <int MAT>
+__device__ __forceinline__ int act_row_of(const StArgs &a, bool sh, int p) {
+  if (MAT == 1) return p;
+  return sh ? p - (int)a.R : a.perm[p] / (int)a.k;
+}
+
+// N (16 or 32) values of every lane summed over the warp, transposed: on
+// return lane l holds the warp total of value l % N (31 shuffles; a fixed order
+// of fp32 adds)
+template <int N>
+__device__ __forceinline__ float transpose_sum(float (&v)[N], int lane) {
+#pragma unroll
+  for (int s = 16; s >= N; s >>= 1)
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], s);
+#pragma unroll
+  for (int s = N / 2; s >= 1; s >>= 1) {
+    const bool upper = (lane & s) != 0;
+#pragma unroll
+    for (int i = 0; i < s; ++i) {
+      const float send = upper ? v[i] : v[i + s];
+      const float keep = upper ? v[i + s] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, s);
+    }
+  }
+  return v[0];
+}
+
+// barrier of one consumer group's four warps: an mbarrier of count 4 (lane 0 of
+// each warp arrives after a __syncwarp, so the warp's shared-memory writes are
+// released), passed with a bounded wait on the phase of parity `par`
+__device__ __forceinline__ bool group_sync(uint64_t *gbar, uint32_t par, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(gbar);
+  return mbar_wait(gbar, par, kStWaitCycles);
+}
+
+// gate/up of the item's 4 features for every row of its expert.  Warp q takes
+// K quarter q (chunks [q K/64, (q+1) K/64)) of all four features; a pass of 2
+// rows loads its activation chunks (at most 3 per lane and row) before any
+// use.  Each lane's 16 partial sums (gate/up x feature x row) are summed over
+// the warp, and the four quarters in quarter order through shared memory
+// (part: [2 pass parities][4 quarters][16]).  Stage layout after the header:
+// gate codes [4][K], up codes [4][K], gate scales [4][K/32], up scales
+// [4][K/32].  Returns false if the group barrier's wait gave up.
+template <bool TAPS>
+__device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
+                                             const int *hdr_rows, const uint8_t *w, int q,
+                                             int lane, float *part, uint64_t *gbar, uint32_t &par,
+                                             uint64_t *empty_bar) {
+  const uint32_t K = (uint32_t)h.K, nb = K / 32, C4 = K / 64;
+  const int8_t *gcode = (const int8_t *)w;
+  const int8_t *ucode = gcode + (size_t)kStGroupWarps * K;
+  const uint16_t *gsc = (const uint16_t *)(w + (size_t)2 * kStGroupWarps * K);
+  const uint16_t *usc = gsc + (size_t)kStGroupWarps * nb;
+  const uint32_t width = h.sh ? a.fs : a.f;
+  int jt[kStGroupWarps];
+#pragma unroll
+  for (int f = 0; f < kStGroupWarps; ++f) jt[f] = TAPS ? tapped((uint32_t)(h.n0 + f), width) : -1;
+  for (int r0 = 0; r0 < h.nrows; r0 += kStRows) {
+    const int nr = min(kStRows, h.nrows - r0);
+    uint4 xr[kStRows][kGuJ];
+    float xsr[kStRows][kGuJ];
+#pragma unroll
+    for (int r = 0; r < kStRows; ++r) {
+      const int rr = r0 + (r < nr ? r : 0);
+      const int tok = rr < kHdrRows ? hdr_rows[rr] : act_row_of<2>(a, h.sh != 0, h.row0 + rr);
+      const int8_t *xp = a.act + (size_t)tok * a.act_stride;
+      const float *xsp = a.act_s + (size_t)tok * a.act_s_stride;
+#pragma unroll
+      for (int j = 0; j < kGuJ; ++j) {
+        const uint32_t cl = lane + 32u * j, c = q * C4 + cl;
+        const bool ok = r < nr && cl < C4;
+        xr[r][j] = ok ? ldg16(xp + 16 * c) : make_uint4(0, 0, 0, 0);
+        xsr[r][j] = ok ? __ldg(xsp + (c >> 1)) : 0.0f;
+      }
+    }
+    float v[kGuVals];  // [m = gate, up][feature][row]
+#pragma unroll
+    for (int i = 0; i < kGuVals; ++i) v[i] = 0.0f;
+    constexpr int kU = kStGroupWarps * kStRows;  // offset of the up values
+#pragma unroll
+    for (int f = 0; f < kStGroupWarps; ++f) {
+#pragma unroll
+      for (int j = 0; j < kGuJ; ++j) {
+        const uint32_t cl = lane + 32u * j, c = q * C4 + cl;
+        if (cl < C4) {  // both lanes of a block pair agree (C4 is even)
+          const uint4 wg = lds16(gcode + (size_t)f * K + 16 * c);
+          const uint4 wu = lds16(ucode + (size_t)f * K + 16 * c);
+          const uint32_t blk = c >> 1;
+          const float sg = half_bits_to_float(gsc[(size_t)f * nb + blk]);
+          const float su = half_bits_to_float(usc[(size_t)f * nb + blk]);
+#pragma unroll
+          for (int r = 0; r < kStRows; ++r) {
+            if (r < nr) {  // warp-uniform
+              const int pg = dot16(wg, xr[r][j]), pu = dot16(wu, xr[r][j]);
+              const int ig = f * kStRows + r;
+              v[ig] = __fmaf_rn((float)pg, sg * xsr[r][j], v[ig]);
+              v[kU + ig] = __fmaf_rn((float)pu, su * xsr[r][j], v[kU + ig]);
+              if (TAPS && jt[f] >= 0) {
+                const int bg = pair_sum(pg, lane), bu = pair_sum(pu, lane);
+                if (!(lane & 1)) {
+                  int32_t *t = a.tap +
+                               ((size_t)(h.row0 + r0 + r) * 2 * kNTap + (size_t)jt[f]) * a.tap_nb +
+                               blk;
+                  t[0] = bg;
+                  t[(size_t)kNTap * a.tap_nb] = bu;
+                }
+              }
+            }
+          }
+        }
+      }
+    }
+    // the stage is no longer read once its last pass has its dot products
+    if (r0 + kStRows >= h.nrows) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    const float tot = transpose_sum<kGuVals>(v, lane);
+    float *pp = part + (size_t)par * kStGroupWarps * kGuVals;
+    if (lane < kGuVals) pp[q * kGuVals + lane] = tot;
+    if (!group_sync(gbar, par, lane)) return false;
+    // warp q finishes feature q: lane r < nr sums its gate and up values over
+    // the quarters in quarter order
+    if (lane < nr) {
+      const int ig = q * kStRows + lane;
+      float g = pp[ig], u = pp[kU + ig];
+#pragma unroll
+      for (int qq = 1; qq < kStGroupWarps; ++qq) {
+        g = __fadd_rn(g, pp[qq * kGuVals + ig]);
+        u = __fadd_rn(u, pp[qq * kGuVals + kU + ig]);
+      }
+      const float hv = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g))), u);
+      a.out[(size_t)(h.row0 + r0 + lane) * a.out_stride + h.n0 + q] = hv;
+    }
+    par ^= 1u;
+  }
+  return true;
+}
+
+// down rows n0 + wi*RW .. + RW - 1 for every row (slot) of the item's expert,
+// in passes of 2 slots and segments of 32*kDnJ chunks, every h chunk of a
+// segment loaded before any use.  Stage layout after the header: codes
+// [4*RW][K], scales [4*RW][K/32].  Arrives on the stage's empty barrier after
+// its last read.
+template <int RW, bool TAPS>
+__device__ __forceinline__ void down_stage(const StArgs &a, const StageHdr &h, const uint8_t *w,
+                                           int wi, int lane, uint64_t *empty_bar) {
+  static_assert(RW * kStRows <= 16, "one transposed warp sum per pass");
+  constexpr int kRows = kStGroupWarps * RW;
+  const uint32_t K = (uint32_t)h.K, nb = K / 32, nc = K / 16;
+  const int8_t *wc = (const int8_t *)w + (size_t)wi * RW * K;
+  const uint16_t *wsc = (const uint16_t *)(w + (size_t)kRows * K) + (size_t)wi * RW * nb;
+  const int m0 = h.n0 + wi * RW;
+  int jt[RW];
+#pragma unroll
+  for (int q = 0; q < RW; ++q) jt[q] = TAPS ? tapped((uint32_t)(m0 + q), a.d) : -1;
+  for (int r0 = 0; r0 < h.nrows; r0 += kStRows) {
+    const int nr = min(kStRows, h.nrows - r0);
+    int slot[kStRows];
+    const int8_t *hp[kStRows];
+    const float *hsp[kStRows];
+#pragma unroll
+    for (int r = 0; r < kStRows; ++r) {
+      slot[r] = h.row0 + r0 + (r < nr ? r : 0);
+      hp[r] = a.act + (size_t)slot[r] * a.act_stride;
+      hsp[r] = a.act_s + (size_t)slot[r] * a.act_s_stride;
+    }
+    float v[16];  // [row q][slot r] at q * kStRows + r
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+#pragma unroll 1
+    for (uint32_t c0 = 0; c0 < nc; c0 += 32 * kDnJ) {
+      uint4 hx[kStRows][kDnJ];
+      float hsc[kStRows][kDnJ];
+#pragma unroll
+      for (int r = 0; r < kStRows; ++r)
+#pragma unroll
+        for (int j = 0; j < kDnJ; ++j) {
+          const uint32_t c = c0 + lane + 32u * j;
+          const bool ok = r < nr && c < nc;
+          hx[r][j] = ok ? ldg16(hp[r] + 16 * c) : make_uint4(0, 0, 0, 0);
+          hsc[r][j] = ok ? __ldg(hsp[r] + (c >> 1)) : 0.0f;
+        }
+#pragma unroll
+      for (int q = 0; q < RW; ++q)
+#pragma unroll
+        for (int j = 0; j < kDnJ; ++j) {
+          const uint32_t c = c0 + lane + 32u * j;
+          if (c < nc) {  // both lanes of a block pair agree (nc is even)
+            const uint4 wv = lds16(wc + (size_t)q * K + 16 * c);
+            const uint32_t blk = c >> 1;
+            const float sw = half_bits_to_float(wsc[(size_t)q * nb + blk]);
+#pragma unroll
+            for (int r = 0; r < kStRows; ++r) {
+              if (r < nr) {
+                const int p = dot16(wv, hx[r][j]);
+                v[q * kStRows + r] = __fmaf_rn((float)p, sw * hsc[r][j], v[q * kStRows + r]);
+                if (TAPS && jt[q] >= 0) {
+                  const int bd = pair_sum(p, lane);
+                  if (!(lane & 1))
+                    a.tap[((size_t)slot[r] * kNTap + (size_t)jt[q]) * a.tap_nb + blk] = bd;
+                }
+              }
+            }
+          }
+        }
+    }
+    if (r0 + kStRows >= h.nrows) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    const float tot = transpose_sum<16>(v, lane);
+    const int q = lane / kStRows, r = lane % kStRows;
+    if (lane < 16 && q < RW && r < nr) a.out[(size_t)slot[r] * a.out_stride + m0 + q] = tot;
+  }
+}
+
+// MAT = 2: gate/up (RW = 1: four features a stage); MAT = 1: down (RW rows a warp)
+template <int MAT, int RW, bool TAPS>
+__global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
+  constexpr int kRows = kStGroupWarps * RW;  // rows of each matrix per stage
+  pdl_trigger();
+  pdl_wait();
+  extern __shared__ __align__(128) uint8_t ssm[];
+  const uint32_t SB = a.stage_bytes;
+  uint64_t *full = (uint64_t *)(ssm + (size_t)kStStages * SB);
+  uint64_t *empty = full + kStStages;
+  uint64_t *gbar = empty + kStStages;  // one per consumer group
+  volatile int *abort_flag = (volatile int *)(gbar + kStGroups);
+  float *part = (float *)(ssm + (size_t)kStStages * SB + kStBarBytes);  // gate/up quarter sums
+  int *plan_sm = (int *)(part + kStPartFloats);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const long long t_entry = clock64();
+  unsigned long long *tr = a.trace && blockIdx.x < kStTraceCtas
+                               ? a.trace + (size_t)blockIdx.x * kStTraceStride
+                               : nullptr;
+  if (tid == 0) {
+    for (int s = 0; s < kStStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStGroupWarps);
+    }
+    for (int g = 0; g < kStGroups; ++g) mbar_init(&gbar[g], kStGroupWarps);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  PlanView P(const_cast<int *>(a.plan), a.E);
+  const SmemPlan S(plan_sm, P, a.E);  // ends in a CTA barrier: the mbarriers are ready
+  const int U = P.hdr[0];
+  const int items = MAT == 2 ? P.hdr[1] / kRows : P.hdr[2] / kRows;
+  const Schedule sc = schedule_of<MAT, kRows>(a, S, U, items, (int)blockIdx.x, (int)gridDim.x);
+  if (warp == kStProdWarp) {
+    if (lane != 0 || sc.count == 0) return;
+    // activation rows the header carries: gate/up tokens (down: the slots, which
+    // the consumers compute)
+    constexpr int kAR = MAT == 2 ? kHdrRows : 0;
+    int issued = 0;
+    long long t_wait = 0;
+    // the current item and its first rows' activation rows, one item ahead
+    Item cur = item_at<MAT, kRows>(a, S, U, sc.item(0));
+    int arow[kAR + 1];
+#pragma unroll
+    for (int r = 0; r < kAR; ++r)
+      arow[r] = r < cur.nrows ? act_row_of<MAT>(a, cur.sh, cur.row0 + r) : 0;
+    for (int i = 0;; ++i) {
+      if (*abort_flag) break;
+      const int s = i % kStStages;
+      const uint32_t use = (uint32_t)(i / kStStages);
+      const long long tw = clock64();
+      if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, kStWaitCycles)) {
+        atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+      t_wait += clock64() - tw;
+      if (tr && i == 0) tr[kStTrSetup] = (unsigned long long)(clock64() - t_entry);
+      // the next item's lookup and permutation reads, in flight meanwhile
+      const bool more = i + 1 < sc.count;
+      Item nxt = cur;
+      int arow_n[kAR + 1];
+#pragma unroll
+      for (int r = 0; r < kAR; ++r) arow_n[r] = 0;
+      if (more) {
+        nxt = item_at<MAT, kRows>(a, S, U, sc.item(i + 1));
+        const bool same = nxt.row0 == cur.row0 && nxt.sh == cur.sh;  // the same expert
+#pragma unroll
+        for (int r = 0; r < kAR; ++r)
+          arow_n[r] = same ? arow[r]
+                           : r < nxt.nrows ? act_row_of<MAT>(a, nxt.sh, nxt.row0 + r) : 0;
+      }
+      // header, then the weight copies
+      uint8_t *st = ssm + (size_t)s * SB;
+      StageHdr *hd = (StageHdr *)st;
+      hd->row0 = cur.row0;
+      hd->nrows = cur.nrows;
+      hd->n0 = cur.n0;
+      hd->sh = cur.sh ? 1 : 0;
+      hd->K = (int)cur.K;
+#pragma unroll
+      for (int r = 0; r < kAR; ++r) hd->act_row[r] = arow[r];
+      const uint32_t qb = (uint32_t)kRows * cur.K, sb = (uint32_t)kRows * (cur.K / 16);
+      uint8_t *w = st + kStHdrBytes;
+      mbar_expect_tx(&full[s], MAT * (qb + sb));
+#pragma unroll
+      for (int m = 0; m < MAT; ++m) {
+        bulk_g2s(w + (size_t)m * qb, cur.q[m], qb, &full[s]);
+        bulk_g2s(w + (size_t)MAT * qb + (size_t)m * sb, cur.s[m], sb, &full[s]);
+      }
+      issued = i + 1;
+      if (!more) break;
+      cur = nxt;
+#pragma unroll
+      for (int r = 0; r < kAR; ++r) arow[r] = arow_n[r];
+    }
+    // no copy may still be landing when the CTA exits: wait (bounded) for the
+    // last item issued to each stage (at once in a normal run: consumed)
+    for (int i = max(0, issued - kStStages); i < issued; ++i)
+      if (!mbar_wait(&full[i % kStStages], (uint32_t)(i / kStStages) & 1u, kStWaitCycles))
+        atomicOr(a.err, kErrTimeout);
+    if (tr) {
+      tr[kStTrProdWait] = (unsigned long long)t_wait;
+      tr[kStTrItems] = (unsigned long long)issued;
+      tr[kStTrProdTotal] = (unsigned long long)(clock64() - t_entry);
+    }
+    return;
+  }
+  const int gi = warp / kStGroupWarps, wi = warp % kStGroupWarps;
+  uint32_t par = 0;  // gate/up: pass parity (partial-sum buffer, group barrier phase)
+  long long c_wait = 0, c_work = 0;
+  for (int i = gi; i < sc.count && !*abort_flag; i += kStGroups) {
+    const int s = i % kStStages;
+    const uint32_t use = (uint32_t)(i / kStStages);
+    const long long tw = clock64();
+    // item i - 4 released (one phase behind at most), then item i's bytes
+    if ((use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, kStWaitCycles)) ||
+        !mbar_wait(&full[s], use & 1u, kStWaitCycles)) {
+      atomicOr(a.err, kErrTimeout);
+      *abort_flag = 1;
+      break;
+    }
+    const long long tg = clock64();
+    c_wait += tg - tw;
+    const uint8_t *st = ssm + (size_t)s * SB;
+    // the header's scalars in registers; gate/up reads its token list in place
+    const StageHdr *hp = (const StageHdr *)st;
+    StageHdr h;
+    h.row0 = hp->row0;
+    h.nrows = hp->nrows;
+    h.n0 = hp->n0;
+    h.sh = hp->sh;
+    h.K = hp->K;
+    if (MAT == 2) {
+      if (!gateup_stage<TAPS>(a, h, hp->act_row, st + kStHdrBytes, wi, lane,
+                              part + (size_t)gi * 2 * kStGroupWarps * kGuVals, &gbar[gi], par,
+                              &empty[s])) {
+        atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
+      }
+    } else {
+      down_stage<RW, TAPS>(a, h, st + kStHdrBytes, wi, lane, &empty[s]);
+    }
+    c_work += clock64() - tg;
+  }
+  if (tr && lane == 0) {
+    tr[kStTrConsWait + warp] = (unsigned long long)c_wait;
+    tr[kStTrConsWork + warp] = (unsigned long long)c_work;
+  }
+}
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+size_t stream_smem(uint32_t stage_bytes, uint32_t E) {
+  return (size_t)kStStages * stage_bytes + kStBarBytes + 4 * kStPartFloats + smem_plan_bytes(E);
+}
+
+// bytes of a stage: header, MAT matrices of `rows` weight rows of K codes and
+// K/32 fp16 scales
+uint64_t stage_bytes_for(int mat, uint32_t rows, uint32_t K) {
+  return kStHdrBytes + (uint64_t)mat * rows * (K + K / 16);
+}
+
+// down rows a warp takes per stage: the most of 6, 4, 2, 1 whose stage fits and
+// whose items tile d
+int down_rw(const moe_desc &D) {
+  const uint32_t kmax = D.f > D.f_shared ? D.f : D.f_shared;
+  for (int rw : {6, 4, 2, 1}) {
+    const uint32_t rows = (uint32_t)kStGroupWarps * rw;
+    if (D.d % rows || stage_bytes_for(1, rows, kmax) > kStStageMax) continue;
+    if ((rw * D.f / 4) % 16 || (rw * D.f_shared / 4) % 16) continue;
+    return rw;
+  }
+  return 0;
+}
+
+template <int MAT, int RW, bool TAPS>
+cudaError_t run_stream(const Ctx &c, const StArgs &a) {
+  static bool big_smem = false;
+  auto kern = k_stream<MAT, RW, TAPS>;
+  const size_t smem = stream_smem(a.stage_bytes, c.desc.n_expert);
+  if (!big_smem) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kStSmemMax);
+    if (e != cudaSuccess) return e;
+    big_smem = true;
+  }
+  const cudaError_t e = launch_k(kern, c.sm_count, kStThreads, smem, c.stream, c.chained, a);
+  c.chained = true;
+  return e;
+}
+
+}  // namespace
+
+// gate/up on the streamed GEMV: Q8_0 routed weights; d a multiple of 128 (K
+// quarters of whole block pairs; a 4-feature scale slice is a whole number of
+// 16-byte copies) and at most 6144; 16-byte aligned scale planes
+bool stream_gateup_ok(const Ctx &c) {
+  const moe_desc &D = c.desc;
+  if (D.routed_fmt != MOE_FMT_Q8_0 || D.d % 128 || D.d > 64u * 32u * kGuJ) return false;
+  if (stage_bytes_for(2, kStGroupWarps, D.d) > kStStageMax) return false;
+  if (!aligned16(c.wts.gate.scale) || !aligned16(c.wts.up.scale)) return false;
+  if (D.f_shared && (!aligned16(c.wts.s_gate.scale) || !aligned16(c.wts.s_up.scale))) return false;
+  return true;
+}
+
+// down: Q8_0 routed weights; an item shape that tiles d with 16-byte scale
+// copies (RW * K / 4 bytes a stage and a row offset); 16-byte aligned scale
+// planes
+bool stream_down_ok(const Ctx &c) {
+  const moe_desc &D = c.desc;
+  if (D.routed_fmt != MOE_FMT_Q8_0 || down_rw(D) == 0) return false;
+  if (!aligned16(c.wts.down.scale)) return false;
+  if (D.f_shared && !aligned16(c.wts.s_down.scale)) return false;
+  return true;
+}
+
+cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm) {
+  const moe_desc &D = c.desc;
+  StArgs a;
+  memset(&a, 0, sizeof a);
+  a.plan = (const int *)(c.ws + c.L.plan);
+  a.E = D.n_expert;
+  a.k = D.top_k;
+  a.d = D.d;
+  a.f = D.f;
+  a.fs = D.f_shared;
+  a.R = c.R;
+  a.K = a.Ks = D.d;
+  a.q[0] = (const int8_t *)c.wts.gate.q;
+  a.q[1] = (const int8_t *)c.wts.up.q;
+  a.sc[0] = c.wts.gate.scale;
+  a.sc[1] = c.wts.up.scale;
+  a.sq[0] = (const int8_t *)c.wts.s_gate.q;
+  a.sq[1] = (const int8_t *)c.wts.s_up.q;
+  a.ssc[0] = c.wts.s_gate.scale;
+  a.ssc[1] = c.wts.s_up.scale;
+  a.rows_per_slot = D.f;
+  a.eslot = c.wts.expert_slot;
+  a.act = (const int8_t *)(c.ws + c.L.xq);
+  a.act_s = (const float *)(c.ws + c.L.xs);
+  a.act_stride = D.d;
+  a.act_s_stride = D.d / 32;
+  a.perm = perm;
+  a.out = (float *)(c.ws + c.L.h);
+  a.out_stride = c.fmax;
+  const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
+  a.tap = taps ? (int32_t *)(c.ws + c.L.tap_gu) : nullptr;
+  a.tap_nb = D.d / 32;
+  a.err = (uint32_t *)(c.ws + c.L.err);
+  a.stage_bytes = (uint32_t)stage_bytes_for(2, kStGroupWarps, D.d);
+  a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
+                ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase
+                : nullptr;
+  return taps ? run_stream<2, 1, true>(c, a) : run_stream<2, 1, false>(c, a);
+}
+
+cudaError_t launch_down_stream(const Ctx &c) {
+  const moe_desc &D = c.desc;
+  const int rw = down_rw(D);
+  StArgs a;
+  memset(&a, 0, sizeof a);
+  a.plan = (const int *)(c.ws + c.L.plan);
+  a.E = D.n_expert;
+  a.k = D.top_k;
+  a.d = D.d;
+  a.f = D.f;
+  a.fs = D.f_shared;
+  a.R = c.R;
+  a.K = D.f;
+  a.Ks = D.f_shared;
+  a.out_per_e = D.d;
+  a.q[0] = (const int8_t *)c.wts.down.q;
+  a.sc[0] = c.wts.down.scale;
+  a.sq[0] = (const int8_t *)c.wts.s_down.q;
+  a.ssc[0] = c.wts.s_down.scale;
+  a.rows_per_slot = D.d;
+  a.eslot = c.wts.expert_slot;
+  a.act = (const int8_t *)(c.ws + c.L.hq);
+  a.act_s = (const float *)(c.ws + c.L.hs);
+  a.act_stride = c.fmax;
+  a.act_s_stride = c.fmax / 32;
+  a.out = (float *)(c.ws + c.L.o);
+  a.out_stride = D.d;
+  const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;
+  a.tap = taps ? (int32_t *)(c.ws + c.L.tap_dn) : nullptr;
+  a.tap_nb = c.fmax / 32;
+  a.err = (uint32_t *)(c.ws + c.L.err);
+  a.stage_bytes = (uint32_t)stage_bytes_for(1, (uint32_t)kStGroupWarps * rw, c.fmax);
+  a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
+                ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase + kStTraceDown
+                : nullptr;
+  switch (rw) {
+    case 6: return taps ? run_stream<1, 6, true>(c, a) : run_stream<1, 6, false>(c, a);
+    case 4: return taps ? run_stream<1, 4, true>(c, a) : run_stream<1, 4, false>(c, a);
+    case 2: return taps ? run_stream<1, 2, true>(c, a) : run_stream<1, 2, false>(c, a);
+    default: return taps ? run_stream<1, 1, true>(c, a) : run_stream<1, 1, false>(c, a);
+  }
+}
+
+}  // namespace moe

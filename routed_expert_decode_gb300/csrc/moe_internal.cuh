@@ -54,6 +54,33 @@ struct PlanView {
   __host__ __device__ static size_t ints(uint32_t E) { return 8 + 9 * (size_t)(E + 2); }
 };
 
+// index u of the dp4a expert whose items [prefix[u], prefix[u+1]) hold `item`
+__device__ __forceinline__ int find_slot(const int *prefix, int U, int item) {
+  int lo = 0, hi = U;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= item) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// The plan's dp4a expert list (act_e, act_row0, act_rows, item_gu: 4(E+1)+1
+// consecutive ints) copied into shared memory, so that the per-item lookups
+// cost no global round trips.
+struct SmemPlan {
+  const int *e, *row0, *rows, *item;
+  __device__ SmemPlan(int *sm, const PlanView &P, uint32_t E) {
+    const int n = 4 * (int)(E + 1) + 1;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) sm[i] = P.act_e[i];
+    __syncthreads();
+    e = sm;
+    row0 = sm + (E + 1);
+    rows = row0 + (E + 1);
+    item = rows + (E + 1);
+  }
+};
+inline size_t smem_plan_bytes(uint32_t E) { return sizeof(int) * (4 * (size_t)(E + 1) + 1); }
+
 // rows per expert above which an expert runs on the tensor-core path
 constexpr uint32_t kTcMinRows = 4;
 // calls with fewer tokens run every expert on the dp4a GEMV (no tensor kernel,
@@ -408,6 +435,12 @@ cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm);
 cudaError_t launch_tc(const Ctx &c, int mat);
 cudaError_t launch_quant_x(const Ctx &c, const float *x);
 cudaError_t launch_gateup(const Ctx &c, const int32_t *perm);
+// the streamed GEMV (weights through shared memory by bulk copies): eligible
+// calls, and its gate/up and down launches
+bool stream_gateup_ok(const Ctx &c);
+bool stream_down_ok(const Ctx &c);
+cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm);
+cudaError_t launch_down_stream(const Ctx &c);
 cudaError_t launch_requant_h(const Ctx &c);
 cudaError_t launch_down(const Ctx &c);
 cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,

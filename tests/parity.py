@@ -164,6 +164,7 @@ def compare_with_oracle(spec, T, x, logits, bias, g, sample=None, taps=False):
         slots += [(R + t, t, spec.E, spec.f_shared, True) for t in sample]
     flips = 0
     total = 0
+    flipped = set()  # sampled tokens with a one-step h flip in one of their rows
     for slot, t, e, width, is_shared in slots:
         ghq = g["hq"][slot, :width].astype(np.int32)
         rhq = (ref.hq_s[t] if is_shared else ref.hq_r[slot]).astype(np.int32)
@@ -171,6 +172,8 @@ def compare_with_oracle(spec, T, x, logits, bias, g, sample=None, taps=False):
         assert diff.max() <= 1, f"h codes differ by {diff.max()} in slot {slot}"
         flips += int((diff > 0).sum())
         total += width
+        if diff.max() > 0:
+            flipped.add(t)
     flip_frac = flips / max(total, 1)
     assert flip_frac <= HQ_FLIP_FRAC, f"h code flips {flip_frac:.2e}"
     # ---- int32 block dots (taps): gate/up exactly; down conditionally on the GPU's hq
@@ -189,13 +192,17 @@ def compare_with_oracle(spec, T, x, logits, bias, g, sample=None, taps=False):
                 ref_dn = oracle.block_dots(fmt, width, ex["down_q"][m], g["hq"][slot, :width])
                 assert np.array_equal(g["tap_dn"][slot, j, :width // 32], ref_dn), \
                     f"down block dots differ (slot {slot}, output {m})"
-    # ---- y: normwise per token (the bar); elementwise above a floor, against
-    # the oracle's down projection (fp64 sums of the exact block dots) and
-    # combine on the GPU's own h codes and scales
-    y_err, y_elem, y_elem_unc = [], [], []
+    # ---- y: normwise per token (the bar) against the oracle's y for a token
+    # whose h codes all equal the oracle's; for a token with a one-step h flip
+    # (allowed above: the fp32 sums of g and u sit on a rounding boundary),
+    # against y_c, the oracle's down projection (fp64 sums of the exact block
+    # dots) and combine on the GPU's own h codes and scales -- at small widths
+    # one flip alone moves y by ~1/(127 sqrt(f)) of its size.  Elementwise above
+    # a floor, always against y_c.
+    y_err, y_err_c, y_elem, y_elem_unc = [], [], [], []
     for t in sample:
         den = np.abs(ref.y[t]).max()
-        y_err.append(float(np.abs(g["y"][t] - ref.y[t]).max() / den))
+        err_t = float(np.abs(g["y"][t] - ref.y[t]).max() / den)
         big = np.abs(ref.y[t]) >= Y_ELEM_FLOOR * den
         rel = np.abs(g["y"][t][big] - ref.y[t][big]) / np.abs(ref.y[t][big])
         y_elem_unc.append(float(rel.max()) if rel.size else 0.0)
@@ -211,9 +218,14 @@ def compare_with_oracle(spec, T, x, logits, bias, g, sample=None, taps=False):
         bigc = np.abs(yc) >= Y_ELEM_FLOOR * np.abs(yc).max()
         relc = np.abs(g["y"][t][bigc] - yc[bigc]) / np.abs(yc[bigc])
         y_elem.append(float(relc.max()) if relc.size else 0.0)
-    assert max(y_err) <= Y_TOL, f"y normwise relative error {max(y_err):.3e}"
+        err_c = float(np.abs(g["y"][t] - yc).max() / np.abs(yc).max())
+        y_err_c.append(err_c)
+        assert (err_c if t in flipped else err_t) <= Y_TOL, \
+            f"y normwise relative error {err_t:.3e} (token {t}; given the GPU's h codes {err_c:.3e})"
+        y_err.append(err_t)
     assert max(y_elem) <= Y_ELEM_TOL, \
         f"y elementwise relative error {max(y_elem):.3e} (given the GPU's h codes)"
-    return dict(max_y_err=max(y_err), max_y_elem_err_given_h=max(y_elem),
-                max_y_elem_err=max(y_elem_unc), hq_flip_frac=flip_frac,
+    return dict(max_y_err=max(y_err), max_y_err_given_h=max(y_err_c),
+                max_y_elem_err_given_h=max(y_elem), max_y_elem_err=max(y_elem_unc),
+                hq_flip_frac=flip_frac, tokens_with_flips=len(flipped),
                 U=int((np.diff(ref.off) > 0).sum()))

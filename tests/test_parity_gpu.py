@@ -28,6 +28,8 @@ SMALL = [
     ("k_eq_E", _spec(E=8, k=8, d=128, f=64, f_shared=32), 5),
     ("e1024_k32", _spec(E=1024, k=32, d=128, f=32, f_shared=0), 3),
     ("many_rows_per_expert", _spec(E=4, k=2, d=256, f=128, f_shared=64), 40),
+    # d not a multiple of 64: gate/up on the register-streaming GEMV, down streamed
+    ("d224_gemv_gateup", _spec(E=16, k=4, d=224, f=96, f_shared=64, s=2.5), 7),
 ]
 
 
@@ -117,6 +119,29 @@ def test_deterministic_across_runs(gpu):
     y2 = layer.forward(*args).y.clone()
     torch.cuda.synchronize()
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("T", [16, 40])
+def test_streamed_gemv_repeatable_with_flushes(gpu, T):
+    """The streamed GEMV's shared-memory ring (four stages read by three consumer
+    groups in turn) under varying timing: 12 calls, each after an L2 flush,
+    give the h codes and y of the first call bit for bit (every expert on the
+    dp4a path: at T=40 FORCE_GEMV keeps the tensor cores off)."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = synth.GLM_LAYER_E32
+    layer = device_layer(spec, gpu)
+    logits, x = synth.token_inputs(spec, 70 + T, T)
+    args = [torch.from_numpy(a).to(gpu) for a in (x, logits, synth.bias(spec))]
+    flush = torch.empty(2 * torch.cuda.get_device_properties(gpu).L2_cache_size,
+                        dtype=torch.uint8, device=gpu)
+    ref = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV)
+    y0, h0 = ref.y.clone(), ref.hq.clone()
+    for i in range(12):
+        flush.fill_(i)
+        out = layer.forward(*args, flags=moe.FLAG_FORCE_GEMV)
+        torch.cuda.synchronize()
+        assert torch.equal(out.hq, h0) and torch.equal(out.y, y0), i
 
 
 def test_ffn_entry_matches_layer(gpu):
