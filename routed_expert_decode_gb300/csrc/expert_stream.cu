@@ -36,18 +36,18 @@
 //    first output, the first rows' activation rows) that the consumers read
 //    instead of repeating the lookup.
 //  * Gate/up item: 4 consecutive features of one expert, their gate and up rows
-//    (K int8 codes + K/32 fp16 scales each).  Warp q of the group takes K
-//    quarter q of all four features for every row of the expert, in passes of
-//    2 rows whose activation chunks it loads at once; the quarters' partial
-//    sums meet in shared memory, summed in quarter order, and h = silu(g)*u
-//    goes out in fp32; the requantisation kernel follows.
+//    (K int8 codes + K/32 fp16 scales each).  The group's warps take a pair of
+//    features over one K half each, for every row of the expert, in passes of
+//    2 rows whose activation blocks they load at once; the halves' partial
+//    sums meet in shared memory, summed in half order, and h = silu(g)*u goes
+//    out in fp32; the requantisation kernel follows.
 //  * Down item: 4*RW consecutive output rows of one expert's down matrix; warp
 //    w takes RW of them against the h codes of every row (slot) of the expert,
-//    in passes of 2 slots whose h chunks it loads at once.
-//  * Lane l holds 16-byte chunks: half of a 32-block each, whose exact int32
-//    sum the lane scales itself (w-scale * x-scale); the block's two halves
-//    meet in the warp sum (the same terms as a whole-block sum, another fp32
-//    order).  The block-dot taps join the halves with one shuffle.
+//    in passes of 2 slots whose h blocks it loads at once.
+//  * Lane l holds whole 32-blocks l, l+32, ..: their exact int32 dots (the
+//    block-dot taps) scaled by w-scale * x-scale into fp32 sums that meet in
+//    the warp sum.  A block's two 16-byte halves are read from shared memory
+//    in an order that keeps each quarter-warp on distinct banks.
 //  * Every wait is bounded; on timeout the kernel flags kErrTimeout, stops
 //    issuing, waits (bounded) for the copies it has in flight and exits.
 #include "stream_ptx.cuh"
@@ -67,17 +67,17 @@ constexpr long long kStWaitCycles = 4000000000ll;      // ~2 s at 2 GHz
 constexpr uint32_t kStBarBytes = 128;                  // 11 mbarriers + the abort flag
 constexpr uint32_t kStSmemMax = 227u * 1024u;          // opt-in dynamic shared memory a CTA
 constexpr uint32_t kStHdrBytes = 64;                   // stage header
-// gate/up partial sums: [group][2 pass parities][4 quarters][16 values] fp32
-constexpr int kGuVals = 2 * kStGroupWarps * kStRows;  // gate/up x feature x row
+// gate/up partial sums: [group][2 pass parities][4 warps][8 values] fp32
+constexpr int kGuVals = 2 * 2 * kStRows;  // gate/up x feature of the pair x row
 constexpr uint32_t kStPartFloats = kStGroups * 2 * kStGroupWarps * kGuVals;
 // largest stage: the dynamic shared memory of one CTA (227 KB) less the plan
 // of a 1024-expert layer, the barriers and the partial sums, over the stages
 constexpr uint32_t kStStageMax =
     (kStSmemMax - (uint32_t)(sizeof(int) * (4 * 1025 + 1)) - kStBarBytes - 4 * kStPartFloats) /
     kStStages / 16 * 16;
-// x chunks per lane per row: K/64 chunks a quarter, d <= 6144
+// x blocks per lane per row: K/64 blocks a half, d <= 6144
 constexpr int kGuJ = 3;
-// h chunks per lane per row and segment in the down stage
+// h blocks per lane per row and segment in the down stage
 constexpr int kDnJ = 2;
 
 struct StArgs {
@@ -116,10 +116,6 @@ enum : int {
   kStTraceDown = 8192,
   kStTraceCtas = 256
 };
-
-__device__ __forceinline__ uint4 ldg16(const int8_t *p) {
-  return __ldg(reinterpret_cast<const uint4 *>(p));
-}
 
 // stage header, written by the producer before it arms the stage's barrier
 struct StageHdr {
@@ -247,31 +243,45 @@ __device__ __forceinline__ bool group_sync(uint64_t *gbar, uint32_t par, int lan
   return mbar_wait(gbar, par, kStWaitCycles);
 }
 
-// gate/up of the item's 4 features for every row of its expert.  Warp q takes
-// K quarter q (chunks [q K/64, (q+1) K/64)) of all four features; a pass of 2
-// rows loads its activation chunks (at most 3 per lane and row) before any
-// use.  Each lane's 16 partial sums (gate/up x feature x row) are summed over
-// the warp, and the four quarters in quarter order through shared memory
-// (part: [2 pass parities][4 quarters][16]).  Stage layout after the header:
-// gate codes [4][K], up codes [4][K], gate scales [4][K/32], up scales
-// [4][K/32].  Returns false if the group barrier's wait gave up.
+// exact int32 dot of the 32-byte block at `w` (shared memory) with the
+// activation block x.  The two 16-byte halves are read in the order `swap`
+// (lanes with bit 2 set read the upper half first), so that a quarter-warp's
+// eight 16-byte reads of eight consecutive blocks fall on distinct banks.
+__device__ __forceinline__ int block_dot(const int8_t *w, const W8 &x, bool swap) {
+  const uint4 a = lds16(w + (swap ? 16 : 0)), b = lds16(w + (swap ? 0 : 16));
+  const uint4 xl = make_uint4(x.v[0], x.v[1], x.v[2], x.v[3]);
+  const uint4 xh = make_uint4(x.v[4], x.v[5], x.v[6], x.v[7]);
+  return dot16(a, swap ? xh : xl) + dot16(b, swap ? xl : xh);
+}
+
+// gate/up of the item's 4 features for every row of its expert.  Warp w takes
+// features 2(w/2), 2(w/2)+1 over K half w%2; lane l holds whole 32-blocks
+// l, l+32, .. of the half (at most 3 for d <= 6144).  A pass of 2 rows loads its
+// activation blocks before any use.  Each lane's 8 partial sums (gate/up x
+// feature x row) are summed over the warp, and the two halves of a feature in
+// half order through shared memory (part: [2 pass parities][4 warps][8]); warp
+// w then finishes feature 2(w/2) + w%2.  Stage layout after the header: gate
+// codes [4][K], up codes [4][K], gate scales [4][K/32], up scales [4][K/32].
+// Returns false if the group barrier's wait gave up.
 template <bool TAPS>
 __device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
-                                             const int *hdr_rows, const uint8_t *w, int q,
+                                             const int *hdr_rows, const uint8_t *w, int wi,
                                              int lane, float *part, uint64_t *gbar, uint32_t &par,
                                              uint64_t *empty_bar) {
-  const uint32_t K = (uint32_t)h.K, nb = K / 32, C4 = K / 64;
+  const uint32_t K = (uint32_t)h.K, nb = K / 32, nb2 = nb / 2;
+  const int fp = wi >> 1, hk = wi & 1;  // feature pair, K half
   const int8_t *gcode = (const int8_t *)w;
   const int8_t *ucode = gcode + (size_t)kStGroupWarps * K;
   const uint16_t *gsc = (const uint16_t *)(w + (size_t)2 * kStGroupWarps * K);
   const uint16_t *usc = gsc + (size_t)kStGroupWarps * nb;
   const uint32_t width = h.sh ? a.fs : a.f;
-  int jt[kStGroupWarps];
+  const bool swap = (lane >> 2) & 1;
+  int jt[2];
 #pragma unroll
-  for (int f = 0; f < kStGroupWarps; ++f) jt[f] = TAPS ? tapped((uint32_t)(h.n0 + f), width) : -1;
+  for (int f = 0; f < 2; ++f) jt[f] = TAPS ? tapped((uint32_t)(h.n0 + 2 * fp + f), width) : -1;
   for (int r0 = 0; r0 < h.nrows; r0 += kStRows) {
     const int nr = min(kStRows, h.nrows - r0);
-    uint4 xr[kStRows][kGuJ];
+    W8 xr[kStRows][kGuJ];
     float xsr[kStRows][kGuJ];
 #pragma unroll
     for (int r = 0; r < kStRows; ++r) {
@@ -281,43 +291,44 @@ __device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
       const float *xsp = a.act_s + (size_t)tok * a.act_s_stride;
 #pragma unroll
       for (int j = 0; j < kGuJ; ++j) {
-        const uint32_t cl = lane + 32u * j, c = q * C4 + cl;
-        const bool ok = r < nr && cl < C4;
-        xr[r][j] = ok ? ldg16(xp + 16 * c) : make_uint4(0, 0, 0, 0);
-        xsr[r][j] = ok ? __ldg(xsp + (c >> 1)) : 0.0f;
+        const uint32_t bl = lane + 32u * j, b = hk * nb2 + bl;
+        const bool ok = r < nr && bl < nb2;
+        if (ok) {
+          xr[r][j] = ld_cached32(xp + 32 * b);
+          xsr[r][j] = __ldg(xsp + b);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xr[r][j].v[q] = 0u;
+          xsr[r][j] = 0.0f;
+        }
       }
     }
-    float v[kGuVals];  // [m = gate, up][feature][row]
+    float v[kGuVals];  // [m = gate, up][feature of the pair][row]
 #pragma unroll
     for (int i = 0; i < kGuVals; ++i) v[i] = 0.0f;
-    constexpr int kU = kStGroupWarps * kStRows;  // offset of the up values
+    constexpr int kU = 2 * kStRows;  // offset of the up values
 #pragma unroll
-    for (int f = 0; f < kStGroupWarps; ++f) {
+    for (int f = 0; f < 2; ++f) {
+      const int fr = 2 * fp + f;  // feature row within the stage
 #pragma unroll
       for (int j = 0; j < kGuJ; ++j) {
-        const uint32_t cl = lane + 32u * j, c = q * C4 + cl;
-        if (cl < C4) {  // both lanes of a block pair agree (C4 is even)
-          const uint4 wg = lds16(gcode + (size_t)f * K + 16 * c);
-          const uint4 wu = lds16(ucode + (size_t)f * K + 16 * c);
-          const uint32_t blk = c >> 1;
-          const float sg = half_bits_to_float(gsc[(size_t)f * nb + blk]);
-          const float su = half_bits_to_float(usc[(size_t)f * nb + blk]);
+        const uint32_t bl = lane + 32u * j, b = hk * nb2 + bl;
+        if (bl < nb2) {
+          const float sg = half_bits_to_float(gsc[(size_t)fr * nb + b]);
+          const float su = half_bits_to_float(usc[(size_t)fr * nb + b]);
 #pragma unroll
           for (int r = 0; r < kStRows; ++r) {
             if (r < nr) {  // warp-uniform
-              const int pg = dot16(wg, xr[r][j]), pu = dot16(wu, xr[r][j]);
+              const int pg = block_dot(gcode + (size_t)fr * K + 32 * b, xr[r][j], swap);
+              const int pu = block_dot(ucode + (size_t)fr * K + 32 * b, xr[r][j], swap);
               const int ig = f * kStRows + r;
               v[ig] = __fmaf_rn((float)pg, sg * xsr[r][j], v[ig]);
               v[kU + ig] = __fmaf_rn((float)pu, su * xsr[r][j], v[kU + ig]);
               if (TAPS && jt[f] >= 0) {
-                const int bg = pair_sum(pg, lane), bu = pair_sum(pu, lane);
-                if (!(lane & 1)) {
-                  int32_t *t = a.tap +
-                               ((size_t)(h.row0 + r0 + r) * 2 * kNTap + (size_t)jt[f]) * a.tap_nb +
-                               blk;
-                  t[0] = bg;
-                  t[(size_t)kNTap * a.tap_nb] = bu;
-                }
+                int32_t *t = a.tap +
+                             ((size_t)(h.row0 + r0 + r) * 2 * kNTap + (size_t)jt[f]) * a.tap_nb + b;
+                t[0] = pg;
+                t[(size_t)kNTap * a.tap_nb] = pu;
               }
             }
           }
@@ -331,20 +342,16 @@ __device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
     }
     const float tot = transpose_sum<kGuVals>(v, lane);
     float *pp = part + (size_t)par * kStGroupWarps * kGuVals;
-    if (lane < kGuVals) pp[q * kGuVals + lane] = tot;
+    if (lane < kGuVals) pp[wi * kGuVals + lane] = tot;
     if (!group_sync(gbar, par, lane)) return false;
-    // warp q finishes feature q: lane r < nr sums its gate and up values over
-    // the quarters in quarter order
+    // warp wi finishes feature 2 fp + hk: lane r < nr adds the K halves (half 0
+    // first) of its gate and up values
     if (lane < nr) {
-      const int ig = q * kStRows + lane;
-      float g = pp[ig], u = pp[kU + ig];
-#pragma unroll
-      for (int qq = 1; qq < kStGroupWarps; ++qq) {
-        g = __fadd_rn(g, pp[qq * kGuVals + ig]);
-        u = __fadd_rn(u, pp[qq * kGuVals + kU + ig]);
-      }
+      const int ig = hk * kStRows + lane;
+      const float *p0 = pp + (2 * fp) * kGuVals, *p1 = p0 + kGuVals;
+      const float g = __fadd_rn(p0[ig], p1[ig]), u = __fadd_rn(p0[kU + ig], p1[kU + ig]);
       const float hv = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g))), u);
-      a.out[(size_t)(h.row0 + r0 + lane) * a.out_stride + h.n0 + q] = hv;
+      a.out[(size_t)(h.row0 + r0 + lane) * a.out_stride + h.n0 + 2 * fp + hk] = hv;
     }
     par ^= 1u;
   }
@@ -352,19 +359,20 @@ __device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
 }
 
 // down rows n0 + wi*RW .. + RW - 1 for every row (slot) of the item's expert,
-// in passes of 2 slots and segments of 32*kDnJ chunks, every h chunk of a
-// segment loaded before any use.  Stage layout after the header: codes
-// [4*RW][K], scales [4*RW][K/32].  Arrives on the stage's empty barrier after
-// its last read.
+// in passes of 2 slots and segments of 32*kDnJ blocks (lane l: whole 32-blocks
+// l, l+32, ..), every h block of a segment loaded before any use.  Stage layout
+// after the header: codes [4*RW][K], scales [4*RW][K/32].  Arrives on the
+// stage's empty barrier after its last read.
 template <int RW, bool TAPS>
 __device__ __forceinline__ void down_stage(const StArgs &a, const StageHdr &h, const uint8_t *w,
                                            int wi, int lane, uint64_t *empty_bar) {
   static_assert(RW * kStRows <= 16, "one transposed warp sum per pass");
   constexpr int kRows = kStGroupWarps * RW;
-  const uint32_t K = (uint32_t)h.K, nb = K / 32, nc = K / 16;
+  const uint32_t K = (uint32_t)h.K, nb = K / 32;
   const int8_t *wc = (const int8_t *)w + (size_t)wi * RW * K;
   const uint16_t *wsc = (const uint16_t *)(w + (size_t)kRows * K) + (size_t)wi * RW * nb;
   const int m0 = h.n0 + wi * RW;
+  const bool swap = (lane >> 2) & 1;
   int jt[RW];
 #pragma unroll
   for (int q = 0; q < RW; ++q) jt[q] = TAPS ? tapped((uint32_t)(m0 + q), a.d) : -1;
@@ -383,37 +391,37 @@ __device__ __forceinline__ void down_stage(const StArgs &a, const StageHdr &h, c
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.0f;
 #pragma unroll 1
-    for (uint32_t c0 = 0; c0 < nc; c0 += 32 * kDnJ) {
-      uint4 hx[kStRows][kDnJ];
+    for (uint32_t b0 = 0; b0 < nb; b0 += 32 * kDnJ) {
+      W8 hx[kStRows][kDnJ];
       float hsc[kStRows][kDnJ];
 #pragma unroll
       for (int r = 0; r < kStRows; ++r)
 #pragma unroll
         for (int j = 0; j < kDnJ; ++j) {
-          const uint32_t c = c0 + lane + 32u * j;
-          const bool ok = r < nr && c < nc;
-          hx[r][j] = ok ? ldg16(hp[r] + 16 * c) : make_uint4(0, 0, 0, 0);
-          hsc[r][j] = ok ? __ldg(hsp[r] + (c >> 1)) : 0.0f;
+          const uint32_t b = b0 + lane + 32u * j;
+          if (r < nr && b < nb) {
+            hx[r][j] = ld_cached32(hp[r] + 32 * b);
+            hsc[r][j] = __ldg(hsp[r] + b);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hx[r][j].v[q] = 0u;
+            hsc[r][j] = 0.0f;
+          }
         }
 #pragma unroll
       for (int q = 0; q < RW; ++q)
 #pragma unroll
         for (int j = 0; j < kDnJ; ++j) {
-          const uint32_t c = c0 + lane + 32u * j;
-          if (c < nc) {  // both lanes of a block pair agree (nc is even)
-            const uint4 wv = lds16(wc + (size_t)q * K + 16 * c);
-            const uint32_t blk = c >> 1;
-            const float sw = half_bits_to_float(wsc[(size_t)q * nb + blk]);
+          const uint32_t b = b0 + lane + 32u * j;
+          if (b < nb) {
+            const float sw = half_bits_to_float(wsc[(size_t)q * nb + b]);
 #pragma unroll
             for (int r = 0; r < kStRows; ++r) {
               if (r < nr) {
-                const int p = dot16(wv, hx[r][j]);
+                const int p = block_dot(wc + (size_t)q * K + 32 * b, hx[r][j], swap);
                 v[q * kStRows + r] = __fmaf_rn((float)p, sw * hsc[r][j], v[q * kStRows + r]);
-                if (TAPS && jt[q] >= 0) {
-                  const int bd = pair_sum(p, lane);
-                  if (!(lane & 1))
-                    a.tap[((size_t)slot[r] * kNTap + (size_t)jt[q]) * a.tap_nb + blk] = bd;
-                }
+                if (TAPS && jt[q] >= 0)
+                  a.tap[((size_t)slot[r] * kNTap + (size_t)jt[q]) * a.tap_nb + b] = p;
               }
             }
           }
@@ -441,7 +449,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   uint64_t *empty = full + kStStages;
   uint64_t *gbar = empty + kStStages;  // one per consumer group
   volatile int *abort_flag = (volatile int *)(gbar + kStGroups);
-  float *part = (float *)(ssm + (size_t)kStStages * SB + kStBarBytes);  // gate/up quarter sums
+  float *part = (float *)(ssm + (size_t)kStStages * SB + kStBarBytes);  // gate/up half sums
   int *plan_sm = (int *)(part + kStPartFloats);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const long long t_entry = clock64();
@@ -624,9 +632,10 @@ cudaError_t run_stream(const Ctx &c, const StArgs &a) {
 
 }  // namespace
 
-// gate/up on the streamed GEMV: Q8_0 routed weights; d a multiple of 128 (K
-// quarters of whole block pairs; a 4-feature scale slice is a whole number of
-// 16-byte copies) and at most 6144; 16-byte aligned scale planes
+// gate/up on the streamed GEMV: Q8_0 routed weights; d a multiple of 128 (a
+// 4-feature scale slice is a whole number of 16-byte copies; K halves of whole
+// blocks) and at most 6144 (3 blocks a lane and row); 16-byte aligned scale
+// planes
 bool stream_gateup_ok(const Ctx &c) {
   const moe_desc &D = c.desc;
   if (D.routed_fmt != MOE_FMT_Q8_0 || D.d % 128 || D.d > 64u * 32u * kGuJ) return false;
