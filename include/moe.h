@@ -151,7 +151,8 @@ typedef struct {
 
 /* The first MOE_WS_FIXED_BYTES of every workspace have a fixed layout: the
  * device error word at offset 0 and, from offset 256, MOE_SYNC_BYTES of
- * counters used by the fused decode kernel.  A workspace must be zero-filled
+ * counters used by the fused decode kernel and by the streamed GEMV's chunk
+ * queues (words 2048..2051).  A workspace must be zero-filled
  * once after it is allocated; every call that completes leaves the counters
  * ready for the next (most zeroed again, two counting calls), so one workspace
  * can serve calls of any desc and T.  A call whose waits timed out may leave
@@ -170,7 +171,8 @@ typedef struct {
   size_t hq, hs;                 /* int8 [R+T][fmax], fp32 [R+T][fmax/32] */
   size_t h, o;                   /* fp32 [R+T][fmax], fp32 [R+T][d] */
   size_t plan;                   /* internal work list */
-  size_t sync;                   /* counters of the fused decode kernel (offset 256) */
+  size_t sync;                   /* counters of the fused decode kernel and the streamed
+                                    GEMV's chunk queues (offset 256) */
   size_t tap_gu, tap_dn;         /* int32 taps (MOE_FLAG_DEBUG_TAPS) */
   size_t trace;                  /* uint64 [1024][32] (MOE_FLAG_TRACE) */
   size_t xperm, xsperm, hperm;   /* tensor-core path: fp16 x codes [R+T][d], fp32 x scales

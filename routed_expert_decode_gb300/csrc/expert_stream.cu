@@ -13,17 +13,20 @@
 // from shared memory with dp4a (the dp4a expert kernels of "What this branch
 // adds over upstream").
 //
-//  * One CTA per SM, persistent; no CTA waits on another.  The routed experts'
-//    items go out in chunks of 8 consecutive ones (slices of one expert,
-//    mostly, whose activation rows then stay in L1), chunk c to CTA c % G (G
-//    CTAs), so that a hot expert's items -- more rows, more passes -- spread
-//    over many CTAs; then the shared expert's items one by one, item j to CTA
-//    j % G: the shared expert has a row per token, its items cost the most.
+//  * One CTA per SM, persistent; no CTA waits on another.  Work items go out
+//    in chunks of 8 consecutive ones from a queue (a counter in the
+//    workspace's fixed head that each CTA's producer takes chunks from), the
+//    shared expert's first -- a row per token, its items cost the most -- then
+//    the routed experts' (slices of one expert, mostly, whose activation rows
+//    then stay in L1): hot experts' items (more rows, more passes) and the
+//    shared expert's no longer leave some CTAs working long after the rest.
+//    The last producer to finish zeroes the counter for the next call.
 //  * The CTA's i-th item goes to stage i % 4 and is read by consumer group
-//    i % 3 (4 warps).  Each group takes its items in order, and item i waits
-//    only for item i - 4 to leave its stage, so the ring always moves.  13
-//    warps: at most 4 on each of the SM's four sub-partitions, so a thread may
-//    hold 128 registers.
+//    i % 3 (4 warps), which learns the item from the stage header (an empty
+//    header ends its loop).  Each group takes its items in order, and item i
+//    waits only for item i - 4 to leave its stage, so the ring always moves.
+//    13 warps: at most 4 on each of the SM's four sub-partitions, so a thread
+//    may hold 128 registers.
 //  * The stage's previous item i - 4 belongs to another group, so a group
 //    reaching item i can find that item still in flight: its full barrier is
 //    then two phases behind, where a parity wait would pass at once.  A
@@ -99,8 +102,15 @@ struct StArgs {
   uint32_t tap_nb;            // blocks per tap row
   uint32_t *err;
   uint32_t stage_bytes;
+  uint32_t *queue;            // [0] chunks taken, [1] producers done (fixed head, zero between calls)
   unsigned long long *trace;  // MOE_FLAG_TRACE: this kernel's words of the trace region, else null
 };
+
+// the chunk queues' words in the workspace's fixed sync area (moe.h): clear of
+// the fused decode kernel's counters (words [0, 4 + E + 1) and the last two)
+constexpr uint32_t kStQueueGateup = 2048, kStQueueDown = 2050;
+static_assert(4 + 1024 + 1 <= kStQueueGateup && kStQueueDown + 2 <= MOE_SYNC_BYTES / 4 - 2,
+              "chunk queues overlap the fused kernel's counters");
 
 // MOE_FLAG_TRACE words per CTA (SM cycles), at kStTraceBase + (down ? kStTraceDown : 0)
 // + CTA * kStTraceStride of the workspace's trace region
@@ -167,40 +177,37 @@ __device__ __forceinline__ Item item_at(const StArgs &a, const SmemPlan &S, int 
   return it;
 }
 
-// The CTA's items in order: chunks of kChunk consecutive routed items (slices
-// of one expert, mostly), chunk b, b + G, b + 2G, .., then every G-th item of
-// the shared expert's (which come last in the plan).
+// The call's items in the order a chunk queue hands them out: chunks of
+// kChunk consecutive items, the shared expert's first (the costliest: a row per
+// token), then the routed experts' (slices of one expert, mostly, whose
+// activation rows then stay in L1).  Each CTA's producer takes the next chunk
+// from a counter in the workspace's fixed head when it needs one, so the CTAs
+// finish together whatever their items cost.
 constexpr int kChunk = 8;
-struct Schedule {
-  int b, G;
-  int r_n;    // routed items of this CTA
-  int s0;     // its first shared item; then every G-th
-  int count;
-  __device__ __forceinline__ int item(int i) const {
-    return i < r_n ? (b + (i / kChunk) * G) * kChunk + i % kChunk : s0 + (i - r_n) * G;
+struct Chunks {
+  int routed, items, n_shared, n;  // routed items, all items, shared chunks, chunks
+  __device__ __forceinline__ int first(int c) const {
+    return c < n_shared ? routed + c * kChunk : (c - n_shared) * kChunk;
+  }
+  __device__ __forceinline__ int end(int c) const {
+    return c < n_shared ? min(routed + (c + 1) * kChunk, items)
+                        : min((c - n_shared + 1) * kChunk, routed);
   }
 };
 
 template <int MAT, int NROWS>
-__device__ __forceinline__ Schedule schedule_of(const StArgs &a, const SmemPlan &S, int U,
-                                                int items, int b, int G) {
+__device__ __forceinline__ Chunks chunks_of(const StArgs &a, const SmemPlan &S, int U,
+                                            int items) {
   // items of the routed experts: all but the shared expert's, when it is on this list
   int routed = items;
   if (U > 0 && S.e[U - 1] == (int)a.E)
     routed = MAT == 2 ? S.item[U - 1] / NROWS : (U - 1) * (int)(a.out_per_e / NROWS);
-  Schedule sc;
-  sc.b = b;
-  sc.G = G;
-  // chunks b, b + G, ..; only the call's last chunk can be short, and it is
-  // the last one of the CTA that holds it
-  const int nch = (routed + kChunk - 1) / kChunk;
-  const int mine = b < nch ? (nch - 1 - b) / G + 1 : 0;
-  sc.r_n = mine * kChunk;
-  if (mine > 0 && b + (mine - 1) * G == nch - 1) sc.r_n -= nch * kChunk - routed;
-  const int shared = items - routed;
-  sc.s0 = routed + b;
-  sc.count = sc.r_n + (b < shared ? (shared - 1 - b) / G + 1 : 0);
-  return sc;
+  Chunks ch;
+  ch.routed = routed;
+  ch.items = items;
+  ch.n_shared = (items - routed + kChunk - 1) / kChunk;
+  ch.n = ch.n_shared + (routed + kChunk - 1) / kChunk;
+  return ch;
 }
 
 // activation row of slot p: its token (gate/up: the shared expert's slots R..
@@ -469,20 +476,37 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   const SmemPlan S(plan_sm, P, a.E);  // ends in a CTA barrier: the mbarriers are ready
   const int U = P.hdr[0];
   const int items = MAT == 2 ? P.hdr[1] / kRows : P.hdr[2] / kRows;
-  const Schedule sc = schedule_of<MAT, kRows>(a, S, U, items, (int)blockIdx.x, (int)gridDim.x);
+  const Chunks ch = chunks_of<MAT, kRows>(a, S, U, items);
   if (warp == kStProdWarp) {
-    if (lane != 0 || sc.count == 0) return;
+    if (lane != 0) return;
     // activation rows the header carries: gate/up tokens (down: the slots, which
     // the consumers compute)
     constexpr int kAR = MAT == 2 ? kHdrRows : 0;
-    int issued = 0;
+    int issued = 0, uses = 0, ends = 0;
     long long t_wait = 0;
+    // g: the item being prepared, of chunk c (items up to gend)
+    int c = 0, g = 0, gend = 0;
+    auto advance = [&]() -> bool {
+      if (g + 1 < gend) {
+        ++g;
+        return true;
+      }
+      c = (int)atomicAdd(a.queue, 1u);
+      if (c >= ch.n) return false;
+      g = ch.first(c);
+      gend = ch.end(c);
+      return true;
+    };
     // the current item and its first rows' activation rows, one item ahead
-    Item cur = item_at<MAT, kRows>(a, S, U, sc.item(0));
+    bool have = advance();
+    Item cur;
     int arow[kAR + 1];
+    if (have) {
+      cur = item_at<MAT, kRows>(a, S, U, g);
 #pragma unroll
-    for (int r = 0; r < kAR; ++r)
-      arow[r] = r < cur.nrows ? act_row_of<MAT>(a, cur.sh, cur.row0 + r) : 0;
+      for (int r = 0; r < kAR; ++r)
+        arow[r] = r < cur.nrows ? act_row_of<MAT>(a, cur.sh, cur.row0 + r) : 0;
+    }
     for (int i = 0;; ++i) {
       if (*abort_flag) break;
       const int s = i % kStStages;
@@ -494,24 +518,34 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
         break;
       }
       t_wait += clock64() - tw;
+      uses = i + 1;
+      uint8_t *st = ssm + (size_t)s * SB;
+      StageHdr *hd = (StageHdr *)st;
+      if (!have) {
+        // an empty header ends the loop of the group that reads item i; one for
+        // each group
+        hd->nrows = 0;
+        mbar_arrive(&full[s]);
+        if (++ends == kStGroups) break;
+        continue;
+      }
       if (tr && i == 0) tr[kStTrSetup] = (unsigned long long)(clock64() - t_entry);
       // the next item's lookup and permutation reads, in flight meanwhile
-      const bool more = i + 1 < sc.count;
+      const int g_cur = g;
+      const bool more = advance();
       Item nxt = cur;
       int arow_n[kAR + 1];
 #pragma unroll
       for (int r = 0; r < kAR; ++r) arow_n[r] = 0;
       if (more) {
-        nxt = item_at<MAT, kRows>(a, S, U, sc.item(i + 1));
-        const bool same = nxt.row0 == cur.row0 && nxt.sh == cur.sh;  // the same expert
+        nxt = item_at<MAT, kRows>(a, S, U, g);
+        const bool same = g == g_cur + 1 && nxt.row0 == cur.row0 && nxt.sh == cur.sh;
 #pragma unroll
         for (int r = 0; r < kAR; ++r)
           arow_n[r] = same ? arow[r]
                            : r < nxt.nrows ? act_row_of<MAT>(a, nxt.sh, nxt.row0 + r) : 0;
       }
       // header, then the weight copies
-      uint8_t *st = ssm + (size_t)s * SB;
-      StageHdr *hd = (StageHdr *)st;
       hd->row0 = cur.row0;
       hd->nrows = cur.nrows;
       hd->n0 = cur.n0;
@@ -527,17 +561,25 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
         bulk_g2s(w + (size_t)m * qb, cur.q[m], qb, &full[s]);
         bulk_g2s(w + (size_t)MAT * qb + (size_t)m * sb, cur.s[m], sb, &full[s]);
       }
-      issued = i + 1;
-      if (!more) break;
+      ++issued;
+      have = more;
       cur = nxt;
 #pragma unroll
       for (int r = 0; r < kAR; ++r) arow[r] = arow_n[r];
     }
     // no copy may still be landing when the CTA exits: wait (bounded) for the
-    // last item issued to each stage (at once in a normal run: consumed)
-    for (int i = max(0, issued - kStStages); i < issued; ++i)
+    // last use of each stage (at once in a normal run: consumed or an empty
+    // header)
+    for (int i = max(0, uses - kStStages); i < uses; ++i)
       if (!mbar_wait(&full[i % kStStages], (uint32_t)(i / kStStages) & 1u, kStWaitCycles))
         atomicOr(a.err, kErrTimeout);
+    // the last producer out zeroes the queue for the next call (every other
+    // producer has taken its last chunk before it counts itself out)
+    __threadfence();
+    if (atomicAdd(a.queue + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.queue, 0u);
+      atomicExch(a.queue + 1, 0u);
+    }
     if (tr) {
       tr[kStTrProdWait] = (unsigned long long)t_wait;
       tr[kStTrItems] = (unsigned long long)issued;
@@ -548,7 +590,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   const int gi = warp / kStGroupWarps, wi = warp % kStGroupWarps;
   uint32_t par = 0;  // gate/up: pass parity (partial-sum buffer, group barrier phase)
   long long c_wait = 0, c_work = 0;
-  for (int i = gi; i < sc.count && !*abort_flag; i += kStGroups) {
+  for (int i = gi; !*abort_flag; i += kStGroups) {
     const int s = i % kStStages;
     const uint32_t use = (uint32_t)(i / kStStages);
     const long long tw = clock64();
@@ -564,6 +606,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
     const uint8_t *st = ssm + (size_t)s * SB;
     // the header's scalars in registers; gate/up reads its token list in place
     const StageHdr *hp = (const StageHdr *)st;
+    if (hp->nrows == 0) break;  // no more items for this group
     StageHdr h;
     h.row0 = hp->row0;
     h.nrows = hp->nrows;
@@ -690,6 +733,7 @@ cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm) {
   a.tap_nb = D.d / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
   a.stage_bytes = (uint32_t)stage_bytes_for(2, kStGroupWarps, D.d);
+  a.queue = (uint32_t *)(c.ws + c.L.sync) + kStQueueGateup;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase
                 : nullptr;
@@ -728,6 +772,7 @@ cudaError_t launch_down_stream(const Ctx &c) {
   a.tap_nb = c.fmax / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
   a.stage_bytes = (uint32_t)stage_bytes_for(1, (uint32_t)kStGroupWarps * rw, c.fmax);
+  a.queue = (uint32_t *)(c.ws + c.L.sync) + kStQueueDown;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase + kStTraceDown
                 : nullptr;
