@@ -106,11 +106,7 @@ struct StArgs {
   unsigned long long *trace;  // MOE_FLAG_TRACE: this kernel's words of the trace region, else null
 };
 
-// the chunk queues' words in the workspace's fixed sync area (moe.h): clear of
-// the fused decode kernel's counters (words [0, 4 + E + 1) and the last two)
-constexpr uint32_t kStQueueGateup = 2048, kStQueueDown = 2050;
-static_assert(4 + 1024 + 1 <= kStQueueGateup && kStQueueDown + 2 <= MOE_SYNC_BYTES / 4 - 2,
-              "chunk queues overlap the fused kernel's counters");
+
 
 // MOE_FLAG_TRACE words per CTA (SM cycles), at kStTraceBase + (down ? kStTraceDown : 0)
 // + CTA * kStTraceStride of the workspace's trace region
@@ -733,7 +729,7 @@ cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm) {
   a.tap_nb = D.d / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
   a.stage_bytes = (uint32_t)stage_bytes_for(2, kStGroupWarps, D.d);
-  a.queue = (uint32_t *)(c.ws + c.L.sync) + kStQueueGateup;
+  a.queue = (uint32_t *)(c.ws + c.L.sync) + kQueueStreamGateup;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase
                 : nullptr;
@@ -772,7 +768,7 @@ cudaError_t launch_down_stream(const Ctx &c) {
   a.tap_nb = c.fmax / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
   a.stage_bytes = (uint32_t)stage_bytes_for(1, (uint32_t)kStGroupWarps * rw, c.fmax);
-  a.queue = (uint32_t *)(c.ws + c.L.sync) + kStQueueDown;
+  a.queue = (uint32_t *)(c.ws + c.L.sync) + kQueueStreamDown;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase + kStTraceDown
                 : nullptr;

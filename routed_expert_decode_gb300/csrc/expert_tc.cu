@@ -65,6 +65,7 @@ struct TcArgs {
   uint32_t *err;
   const int32_t *eslot;  // expert -> weight slot (moe_weights.expert_slot), or null
   float routed_wmul;     // factor of the routed weight scales (0.5: e2m1 dots are of 2v)
+  uint32_t *queue;       // [0] tiles taken, [1] CTAs done (fixed head, zero between calls)
   uint32_t n_stages, stage_bytes;
   unsigned long long *trace;  // MOE_FLAG_TRACE: kTcTraceWords per CTA, else null
 };
@@ -257,13 +258,14 @@ __device__ __forceinline__ TcTile tc_tile(const PlanView &P, const TcArgs &a, in
   return t;
 }
 
-// This CTA's tile in round rd: round rd deals tiles rd*G .. rd*G+G-1 out one per
-// CTA, from CTA 0 up in even rounds and from CTA G-1 down in odd ones; with the
-// plan listing the widest (costliest) tiles first, the CTAs' totals stay close.
-__device__ __forceinline__ int tile_of_round(int rd) {
-  const int G = (int)gridDim.x, b = (int)blockIdx.x;
-  return rd * G + ((rd & 1) ? G - 1 - b : b);
-}
+// Tiles go out from a queue: the producer takes the CTA's next tile from a
+// counter in the workspace's fixed head (the plan lists the widest, costliest
+// tiles first) and publishes it to the CTA's other roles in a ring of
+// kTileRing entries, each with an mbarrier of count 1 (a tile >= the total
+// ends every role's loop).  The roles lag the producer by a few tiles at most
+// (every tile has K/64 >= 4 stages, and the stage and accumulator rings hold
+// fewer than 3 tiles' worth), so an entry is read before it is written again.
+constexpr int kTileRing = 8;
 
 // Stage geometry of a tile: MMA width ncol = live rows rounded up to 16, and
 // gstages = stages whose accumulators share one TMEM buffer (ncol * gstages =
@@ -495,10 +497,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const int total = MAT == 2 ? P.hdr[6] : P.hdr[7];
   if (total == 0) return;  // no tensor-core tiles in this call's plan
   const uint32_t KS = a.K / kBK;  // stages per tile
-  // stage layout: [A16 per matrix 16K][B 8K][A8 per matrix 8K]; a 2-bit tile
-  // stages 16 code bytes per row (kA2 per matrix) at the start of each A8 area
+  // stage layout: [A16 per matrix 16K][B 8K][A8 per matrix 8K]; a 2-bit or e2m1
+  // tile stages its 16 or 32 code bytes per row at the start of each A8 area
   constexpr uint32_t kA16 = kBM * kBK * 2, kB16 = kBN * kBK * 2, kA8 = kBM * kBK;
-  constexpr uint32_t kA2 = kBM * kBK / 4;
   uint8_t *sc_ring = tsm + (size_t)NS * a.stage_bytes;  // [kScSlots][kScSlotBytes]
   uint8_t *ctrl = sc_ring + (size_t)kScSlots * kScSlotBytes;
   uint64_t *ld_full = (uint64_t *)ctrl;          // [NS]
@@ -510,6 +511,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   uint64_t *sc_empty = sc_full + kScSlots;       // [kScSlots]
   uint32_t *tmem_holder = (uint32_t *)(sc_empty + kScSlots);
   volatile int *abort_flag = (volatile int *)(tmem_holder + 1);
+  volatile int *tile_ring = (volatile int *)(ctrl + 512);  // [kTileRing]
+  uint64_t *tile_bar = (uint64_t *)(ctrl + 576);           // [kTileRing]
   float *red = (float *)(ctrl + 1024);  // [MAT][kBM features][33]: split-K partial sums
   const uint32_t tmem_cols = MAT == 2 ? 512 : 256;
 
@@ -527,6 +530,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bar_init(&sc_full[i], 1);
       bar_init(&sc_empty[i], kEpiWarps);
     }
+    for (int i = 0; i < kTileRing; ++i) bar_init(&tile_bar[i], 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -545,12 +549,25 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   long long t_wait0 = 0, t_wait1 = 0, t_out = 0;
   unsigned long long *tr =
       a.trace ? a.trace + (size_t)blockIdx.x * kTcTraceStride + (MAT == 2 ? 0 : 8) : nullptr;
+  // round rd's tile, as the producer published it (total: none left)
+  auto next_tile = [&](int rd) -> int {
+    if (!bar_wait(&tile_bar[rd % kTileRing], (uint32_t)(rd / kTileRing) & 1u)) {
+      atomicOr(a.err, kErrTimeout);
+      *abort_flag = 1;
+      return total;
+    }
+    return tile_ring[rd % kTileRing];
+  };
 
   if (warp == 0) {
     // ============================ TMA producer: weights per stage, scales per kSG stages
     if (lane == 0) {
       uint32_t g = 0, scg = 0;
-      for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
+      for (int rd = 0; !*abort_flag; ++rd) {
+        const int tile = (int)atomicAdd(a.queue, 1u);
+        tile_ring[rd % kTileRing] = tile < total ? tile : total;
+        bar_arrive(&tile_bar[rd % kTileRing]);
+        if (tile >= total) break;
         const TcTile t = tc_tile<MAT>(P, a, tile);
         const bool sh = t.e == (int)a.E;
         // routed weights from the expert's slot (validated by k_plan)
@@ -604,7 +621,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ MMA issuer: a buffer holds gstages stages
     if (lane == 0) {
       uint32_t g = 0, bufs = 0;
-      for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
+      for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
         const TcTile tt = tc_tile<MAT>(P, a, tile);
         const TileGeom geo = tile_geom(tt.rows, tt.n0);
         const uint32_t idesc = idesc_for((uint32_t)geo.ncol);
@@ -650,7 +667,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ============================ converters: row r = tid - 64 of the tile
     const int r = tid - 64;
     uint32_t g = 0;
-    for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
+    for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
       // a 2-bit or e2m1 routed tile (the shared expert is Q8_0)
       const bool routed = RFMT != MOE_FMT_Q8_0 && tc_tile<MAT>(P, a, tile).e != (int)a.E;
       const bool q2 = RFMT == MOE_FMT_Q2S && routed;
@@ -764,7 +781,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     c.red = red;
     c.t_wait = 0;
     c.t_out = 0;
-    for (int rd = 0, tile; (tile = tile_of_round(rd)) < total && !*abort_flag; ++rd) {
+    for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
       const TcTile t = tc_tile<MAT>(P, a, tile);
       const TileGeom geo = tile_geom(t.rows, t.n0);
       if (geo.ncol == 16) epi_tile<MAT, TAPS, 16, true>(a, c, t, geo);
@@ -773,6 +790,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     t_wait0 = c.t_wait;
     t_out = c.t_out;
+  }
+  if (warp == 0 && lane == 0) {
+    // the last producer out zeroes the queue for the next call (every other
+    // producer has taken its last tile before it counts itself out)
+    __threadfence();
+    if (atomicAdd(a.queue + 1, 1u) == gridDim.x - 1) {
+      atomicExch(a.queue, 0u);
+      atomicExch(a.queue + 1, 0u);
+    }
   }
   if (tr && lane == 0) {
     if (warp == 0) tr[kTcTrProdWaitEmpty] = t_wait0;
@@ -937,6 +963,7 @@ cudaError_t launch_tc(const Ctx &c, int mat) {
   a.eslot = c.wts.expert_slot;
   a.plan = (const int *)(c.ws + c.L.plan);
   a.err = (uint32_t *)(c.ws + c.L.err);
+  a.queue = (uint32_t *)(c.ws + c.L.sync) + (mat == 2 ? kQueueTcGateup : kQueueTcDown);
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace ? (unsigned long long *)(c.ws + c.L.trace)
                                                      : nullptr;
   const bool taps = (D.flags & MOE_FLAG_DEBUG_TAPS) != 0;

@@ -81,6 +81,15 @@ struct SmemPlan {
 };
 inline size_t smem_plan_bytes(uint32_t E) { return sizeof(int) * (4 * (size_t)(E + 1) + 1); }
 
+// Work queues of the persistent expert kernels: pairs of words (items taken,
+// CTAs done) in the workspace's fixed sync area (moe.h), zero between calls
+// (the last CTA out of a kernel zeroes its pair), clear of the fused decode
+// kernel's counters (words [0, 4 + E + 1) and the last two).
+constexpr uint32_t kQueueStreamGateup = 2048, kQueueStreamDown = 2050;
+constexpr uint32_t kQueueTcGateup = 2052, kQueueTcDown = 2054;
+static_assert(4 + 1024 + 1 <= kQueueStreamGateup && kQueueTcDown + 2 <= MOE_SYNC_BYTES / 4 - 2,
+              "work queues overlap the fused kernel's counters");
+
 // rows per expert above which an expert runs on the tensor-core path
 constexpr uint32_t kTcMinRows = 4;
 // calls with fewer tokens run every expert on the dp4a GEMV (no tensor kernel,
