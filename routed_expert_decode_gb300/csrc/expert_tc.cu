@@ -22,10 +22,16 @@
 // MAT = 2: gate and up, epilogue h = silu(g)*u requantised per 32 features;
 // MAT = 1: down, epilogue o.
 // RFMT: format of the routed experts' weights.  2-bit routed weights (code c in
-// {0..3} meaning 2c - 3) and 4-bit e2m1 weights (as twice their values, the
-// integers 0, +-1, .., +-12) are decoded by the converters into fp16 as exactly
-// as int8 codes are, so the MMA computes the same exact integer block dots; the
-// shared expert is always Q8_0.
+// {0..3} meaning 2c - 3) are decoded by the converters into fp16 as exactly as
+// int8 codes are, so the MMA computes the same exact integer block dots.  4-bit
+// e2m1 routed weights go to the tensor cores as they are: tcgen05.mma
+// kind::f8f6f4 with A = e2m1 (the converters only spread the packed codes into
+// the operand layout: 16 codes in the first 8 bytes of each 16-byte chunk) and
+// B = e4m3, the activation codes q carried as the two exact e4m3 digits of
+// 2q = 32 hi + 2 lo (hi = floor(q/16) in [-8, 7], lo in [0, 15]), one MMA per
+// digit into the same accumulator: the block dot sum(v * 2q) = sum(2v * q), the
+// same exact integer as for the other formats (the block-dot taps check it).
+// The shared expert is always Q8_0.
 #include <cuda.h>
 #include <string.h>
 
@@ -144,6 +150,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
+// kind::f8f6f4: A e2m1, B e4m3, D f32
+__device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, bool accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
+      : "memory");
+}
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -177,9 +192,30 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
   return desc;
 }
 
-// instruction descriptor: D f32, A and B f16, both K-major, M = 128, N = kBN
+// instruction descriptor: D f32 (bit 4), A and B f16 (bits 7-9, 10-12: 0), both
+// K-major, N >> 3 at bit 17, M >> 4 at bit 24
 constexpr uint32_t kIdescBase = (1u << 4) | ((uint32_t)(kBM >> 4) << 24);
 __device__ __forceinline__ uint32_t idesc_for(uint32_t n) { return kIdescBase | ((n >> 3) << 17); }
+// kind::f8f6f4: A e2m1 (5), B e4m3 (0)
+__device__ __forceinline__ uint32_t idesc_f4_for(uint32_t n) {
+  return idesc_for(n) | (5u << 7) | (0u << 10);
+}
+
+// The e4m3 byte of an integer v with at most 4 significant bits and |v| <= 256
+// (exactly representable): sign, biased exponent floor(log2 |v|) + 7, the 3
+// bits below the leading one.
+__device__ __forceinline__ uint32_t e4m3_of_int(int v) {
+  if (v == 0) return 0u;
+  const uint32_t a = (uint32_t)(v < 0 ? -v : v);
+  const int e = 31 - __clz((int)a);
+  return (v < 0 ? 0x80u : 0u) | ((uint32_t)(e + 7) << 3) | (((a << 3) >> e) & 7u);
+}
+// the two e4m3 digits of 2q for an int8 code q: 32 hi and 2 lo, hi = floor(q/16)
+__device__ __forceinline__ void e4m3_digits(int q, uint32_t &dhi, uint32_t &dlo) {
+  const int hi = q >> 4;  // floor(q / 16), -8 .. 7
+  dhi = e4m3_of_int(32 * hi);
+  dlo = e4m3_of_int(2 * (q - 16 * hi));
+}
 
 // MMA width of a tile: its live rows rounded up to 16 (the MMA's N step at M = 128)
 __device__ __forceinline__ int tile_cols(int rows, int n0) {
@@ -303,7 +339,7 @@ struct EpiState {
   long long t_wait, t_out;
 };
 
-template <int MAT, bool TAPS, int NCM, bool SPLIT>
+template <int MAT, bool TAPS, int NCM, bool SPLIT, int RFMT>
 __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile &t,
                                       const TileGeom &geo) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -471,7 +507,17 @@ __device__ __noinline__ void epi_tile(const TcArgs &a, EpiState &c, const TcTile
         const int qv = quant_one(h, sc);
         const size_t fo = (size_t)t.m0 + feat;
         a.hq[sl * a.fmax + fo] = (int8_t)qv;
-        a.hperm[sl * a.fmax + fo] = __int2half_rn(qv);
+        if (RFMT == MOE_FMT_E2M1 && !sh) {
+          // the down tiles' B operand: per 64-feature stage, the 32-hi digits of
+          // 2q in the stage's first 64 bytes, the 2-lo digits in the next 64
+          uint32_t dhi, dlo;
+          e4m3_digits(qv, dhi, dlo);
+          uint8_t *row = (uint8_t *)a.hperm + sl * a.fmax * 2 + (fo / 64) * 128 + fo % 64;
+          row[0] = (uint8_t)dhi;
+          row[64] = (uint8_t)dlo;
+        } else {
+          a.hperm[sl * a.fmax + fo] = __int2half_rn(qv);
+        }
         if (lane == 0) a.hs[sl * (a.fmax / 32) + fo / 32] = sc;
       } else {
         a.o[sl * a.d + t.m0 + feat] = ACC(0, j);
@@ -624,7 +670,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
         const TcTile tt = tc_tile<MAT>(P, a, tile);
         const TileGeom geo = tile_geom(tt.rows, tt.n0);
-        const uint32_t idesc = idesc_for((uint32_t)geo.ncol);
+        // e2m1 routed tile: kind::f8f6f4 on the packed codes and the e4m3 digits
+        const bool f4 = RFMT == MOE_FMT_E2M1 && tt.e != (int)a.E;
+        const uint32_t idesc =
+            f4 ? idesc_f4_for((uint32_t)geo.ncol) : idesc_for((uint32_t)geo.ncol);
         for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
           const uint32_t s = g % NS, use = g / NS, b = bufs & 1u;
           const uint32_t si = ks % (uint32_t)geo.gstages;
@@ -645,16 +694,24 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-            for (int mi = 0; mi < MAT; ++mi)
+            for (int mi = 0; mi < MAT; ++mi) {
+              const uint32_t dcol = tmem + acc_col<MAT>(b, tmem_cols / 2, (int)si, mi, blk,
+                                                        geo.ncol);
+              if (f4) {
+                // K = 32 a block: A chunks 2blk, 2blk+1; B's 32-hi digits in the
+                // row's first 64 bytes, its 2-lo digits in the next 64
+                const uint64_t ad = sw128_desc(s32(st + mi * kA16) + 32u * blk);
+                tc_mma_f4(dcol, ad, sw128_desc(b_addr + 32u * blk), idesc, false);
+                tc_mma_f4(dcol, ad, sw128_desc(b_addr + 64u + 32u * blk), idesc, true);
+              } else {
 #pragma unroll
-              for (int k16 = 0; k16 < 2; ++k16) {
-                const uint32_t koff = (uint32_t)(blk * 2 + k16) * 32;  // bytes along K
-                const uint64_t ad = sw128_desc(s32(st + mi * kA16) + koff);
-                const uint64_t bd = sw128_desc(b_addr + koff);
-                const uint32_t dcol = tmem + acc_col<MAT>(b, tmem_cols / 2, (int)si, mi, blk,
-                                                          geo.ncol);
-                tc_mma(dcol, ad, bd, idesc, k16 > 0);
+                for (int k16 = 0; k16 < 2; ++k16) {
+                  const uint32_t koff = (uint32_t)(blk * 2 + k16) * 32;  // bytes along K
+                  tc_mma(dcol, sw128_desc(s32(st + mi * kA16) + koff),
+                         sw128_desc(b_addr + koff), idesc, k16 > 0);
+                }
               }
+            }
           tc_commit(&st_empty[s]);
           if (si + 1 == (uint32_t)geo.gstages || ks + 1 == KS) {
             tc_commit(&d_full[b]);
@@ -684,34 +741,18 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         uint8_t *st = tsm + (size_t)s * a.stage_bytes;
         if (f4) {
-          // row r's 32 code bytes = 64 e2m1 codes, 8 a word: word j -> fp16
-          // chunk j (K 8j..8j+7) as the biased bytes 2v + 12 under 2^10, minus
-          // 1036 (exact), at position j ^ (r&7) of its swizzled row
-          const __half2 k1036 = __halves2half2(__ushort_as_half(0x640C), __ushort_as_half(0x640C));
+          // row r's 32 code bytes = 64 e2m1 codes: codes 16j .. 16j+15 (8 bytes)
+          // into the first half of 16-byte chunk j of the operand row, at
+          // position j ^ (r&7) of its 128-byte swizzled row; the MMA reads
+          // chunks 0..3 (K 0..63)
           for (int mi = 0; mi < MAT; ++mi) {
             const uint4 *src = (const uint4 *)(st + MAT * kA16 + kB16 + mi * kA8 + r * (kBK / 2));
             uint8_t *dst_row = st + mi * kA16 + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-            for (int hq = 0; hq < 2; ++hq) {
-              const uint4 cw = src[hq];
-              const uint32_t wv[4] = {cw.x, cw.y, cw.z, cw.w};
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
-                const int j = 4 * hq + v;
-                uint32_t hh[4];
-#pragma unroll
-                for (int hw = 0; hw < 2; ++hw) {
-                  const uint32_t t = e2m1x4_biased(wv[v] >> (16 * hw));
-                  uint32_t lo = __byte_perm(t, 0x64646464u, 0x5140);
-                  uint32_t hi = __byte_perm(t, 0x64646464u, 0x7362);
-                  __half2 a0 = __hsub2(*reinterpret_cast<__half2 *>(&lo), k1036);
-                  __half2 a1 = __hsub2(*reinterpret_cast<__half2 *>(&hi), k1036);
-                  hh[2 * hw] = *reinterpret_cast<uint32_t *>(&a0);
-                  hh[2 * hw + 1] = *reinterpret_cast<uint32_t *>(&a1);
-                }
-                *(uint4 *)(dst_row + ((j ^ (r & 7)) << 4)) = make_uint4(hh[0], hh[1], hh[2], hh[3]);
-              }
-            }
+            const uint4 c0 = src[0], c1 = src[1];
+            *(uint4 *)(dst_row + ((0 ^ (r & 7)) << 4)) = make_uint4(c0.x, c0.y, 0u, 0u);
+            *(uint4 *)(dst_row + ((1 ^ (r & 7)) << 4)) = make_uint4(c0.z, c0.w, 0u, 0u);
+            *(uint4 *)(dst_row + ((2 ^ (r & 7)) << 4)) = make_uint4(c1.x, c1.y, 0u, 0u);
+            *(uint4 *)(dst_row + ((3 ^ (r & 7)) << 4)) = make_uint4(c1.z, c1.w, 0u, 0u);
           }
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           __syncwarp();
@@ -784,9 +825,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
       const TcTile t = tc_tile<MAT>(P, a, tile);
       const TileGeom geo = tile_geom(t.rows, t.n0);
-      if (geo.ncol == 16) epi_tile<MAT, TAPS, 16, true>(a, c, t, geo);
-      else if (geo.ncol == 32) epi_tile<MAT, TAPS, 32, true>(a, c, t, geo);
-      else epi_tile<MAT, TAPS, 32, false>(a, c, t, geo);
+      if (geo.ncol == 16) epi_tile<MAT, TAPS, 16, true, RFMT>(a, c, t, geo);
+      else if (geo.ncol == 32) epi_tile<MAT, TAPS, 32, true, RFMT>(a, c, t, geo);
+      else epi_tile<MAT, TAPS, 32, false, RFMT>(a, c, t, geo);
     }
     t_wait0 = c.t_wait;
     t_out = c.t_out;
@@ -823,12 +864,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   }
 }
 
-// activations for the tensor path: fp16 copy of x codes in slot order (nothing
-// when the plan sends no expert to the tensor cores)
+// activations for the tensor path in slot order (nothing when the plan sends no
+// expert to the tensor cores): an fp16 copy of the x codes, or for the routed
+// slots of an e2m1 layer (`digits`) the e4m3 digits of 2q, per 64-element
+// stage 64 bytes of 32-hi digits then 64 of 2-lo digits (the same 128 bytes)
 __global__ void __launch_bounds__(256)
     k_perm_x(const int8_t *__restrict__ xq, const int32_t *__restrict__ perm, uint32_t R,
              uint32_t slots, uint32_t k, uint32_t d, const int *plan, uint32_t E,
-             __half *__restrict__ xperm) {
+             __half *__restrict__ xperm, int digits) {
   pdl_trigger();
   pdl_wait();
   if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
@@ -838,6 +881,21 @@ __global__ void __launch_bounds__(256)
   const uint32_t slot = (uint32_t)(i / (d / 8)), c = (uint32_t)(i % (d / 8));
   const uint32_t t = slot < R ? (uint32_t)perm[slot] / k : slot - R;
   const uint2 w = *(const uint2 *)(xq + (size_t)t * d + 8 * c);
+  if (digits && slot < R) {
+    uint32_t hi[2] = {0u, 0u}, lo[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int q = (int)(int8_t)(((i < 4 ? w.x : w.y) >> (8 * (i & 3))) & 0xFFu);
+      uint32_t dh, dl;
+      e4m3_digits(q, dh, dl);
+      hi[i >> 2] |= dh << (8 * (i & 3));
+      lo[i >> 2] |= dl << (8 * (i & 3));
+    }
+    uint8_t *row = (uint8_t *)xperm + (size_t)slot * d * 2 + (8 * c / 64) * 128 + (8 * c) % 64;
+    *(uint2 *)row = make_uint2(hi[0], hi[1]);
+    *(uint2 *)(row + 64) = make_uint2(lo[0], lo[1]);
+    return;
+  }
   uint4 out;
   i8x4_to_h2x2(w.x, out.x, out.y);
   i8x4_to_h2x2(w.y, out.z, out.w);
@@ -936,7 +994,8 @@ cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm) {
   cudaError_t e = launch_k(k_perm_x, (unsigned)((n1 + 255) / 256), 256, 0, c.stream, c.chained,
                            (const int8_t *)(c.ws + c.L.xq), perm, c.R, slots, c.desc.top_k,
                            c.desc.d, (const int *)(c.ws + c.L.plan), c.desc.n_expert,
-                           (__half *)(c.ws + c.L.xperm));
+                           (__half *)(c.ws + c.L.xperm),
+                           c.desc.routed_fmt == MOE_FMT_E2M1 ? 1 : 0);
   c.chained = true;
   if (e != cudaSuccess) return e;
   const uint64_t n2 = (uint64_t)slots * (c.desc.d / 32);
