@@ -38,8 +38,9 @@
 //    current item's copies, and each stage starts with a header (expert rows,
 //    first output, the first rows' activation rows) that the consumers read
 //    instead of repeating the lookup.
-//  * Gate/up item: 4 consecutive features of one expert, their gate and up rows
-//    (K int8 codes + K/32 fp16 scales each).  The group's warps take a pair of
+//  * Gate/up item: 4 consecutive Q8_0 features of one expert (16 of 2-bit or 8
+//    of e2m1 routed weights, whose blocks a lane decodes once for every row),
+//    their gate and up rows (codes + K/32 fp16 scales each).  The group's warps take a pair of
 //    features over one K half each, for every row of the expert, in passes of
 //    2 rows whose activation blocks they load at once; the halves' partial
 //    sums meet in shared memory, summed in half order, and h = silu(g)*u goes
@@ -53,6 +54,8 @@
 //    in an order that keeps each quarter-warp on distinct banks.
 //  * Every wait is bounded; on timeout the kernel flags kErrTimeout, stops
 //    issuing, waits (bounded) for the copies it has in flight and exits.
+#include <algorithm>
+
 #include "stream_ptx.cuh"
 
 namespace moe {
@@ -72,14 +75,25 @@ constexpr uint32_t kStSmemMax = 227u * 1024u;          // opt-in dynamic shared 
 constexpr uint32_t kStHdrBytes = 64;                   // stage header
 // gate/up partial sums: [group][2 pass parities][4 warps][8 values] fp32
 constexpr int kGuVals = 2 * 2 * kStRows;  // gate/up x feature of the pair x row
-constexpr uint32_t kStPartFloats = kStGroups * 2 * kStGroupWarps * kGuVals;
+// routed features per gate/up item by weight format: Q8_0 4, 2-bit 16, e2m1 8
+// (stages of 35-52 KB at the layers' widths); the shared expert's items are
+// always 4 Q8_0 features
+template <int FMT>
+__host__ __device__ constexpr int fpi_of() {
+  return FMT == MOE_FMT_Q2S ? 16 : FMT == MOE_FMT_E2M1 ? 8 : 4;
+}
+constexpr int kGuValsMax = 2 * (16 / 2) * kStRows;  // the low-bit consumer's, 2-bit
+constexpr uint32_t kStPartPerGroup = 2 * kStGroupWarps * kGuValsMax;  // floats
+constexpr uint32_t kStPartFloats = kStGroups * kStPartPerGroup;
 // largest stage: the dynamic shared memory of one CTA (227 KB) less the plan
 // of a 1024-expert layer, the barriers and the partial sums, over the stages
 constexpr uint32_t kStStageMax =
     (kStSmemMax - (uint32_t)(sizeof(int) * (4 * 1025 + 1)) - kStBarBytes - 4 * kStPartFloats) /
     kStStages / 16 * 16;
-// x blocks per lane per row: K/64 blocks a half, d <= 6144
+// x blocks per lane per row: K/64 blocks a half, d <= 6144 (Q8_0 items) or
+// d <= 4096 (2-bit and e2m1 items: fewer registers beside their decoded blocks)
 constexpr int kGuJ = 3;
+constexpr int kGuJLowBit = 2;
 // h blocks per lane per row and segment in the down stage
 constexpr int kDnJ = 2;
 
@@ -93,6 +107,7 @@ struct StArgs {
   uint32_t rows_per_slot;     // routed weight rows per expert slot (gate/up: f; down: d)
   const int32_t *eslot;       // expert -> weight slot, or null
   const int8_t *act;          // activation codes: x [T][d] (gate/up), h [slots][fmax] (down)
+  const int8_t *act_t;        // gate/up, 2-bit routed weights: x codes, 16-code groups transposed
   const float *act_s;         // their block scales
   uint32_t act_stride, act_s_stride;
   const int32_t *perm;        // gate/up: slot -> row (token = row / k)
@@ -136,25 +151,57 @@ static_assert(sizeof(StageHdr) == kStHdrBytes, "stage header size");
 struct Item {
   int row0, nrows, n0;
   bool sh;
+  int nf;      // weight rows of each matrix in the item
   uint32_t K;
+  uint32_t rb;  // code bytes of one weight row
   const int8_t *q[2];
   const uint16_t *s[2];
 };
 
-// item g of the call: gate/up items are 4 features (prefix S.item in features);
-// down items are NROWS output rows, out_per_e / NROWS of them per expert
-template <int MAT, int NROWS>
-__device__ __forceinline__ Item item_at(const StArgs &a, const SmemPlan &S, int U, int g) {
+// The call's items: the routed experts' first, then the shared expert's (the
+// last expert of the plan's list, when it is there).  Gate/up: routed items of
+// fpi_of<RFMT> features, shared items of 4 (Q8_0); down: NROWS output rows
+// throughout (Q8_0 weights only), out_per_e / NROWS per expert.
+struct ItemCount {
+  int routed, items;
+};
+template <int MAT, int NROWS, int RFMT>
+__device__ __forceinline__ ItemCount item_count(const StArgs &a, const SmemPlan &S, int U) {
+  const bool shared = U > 0 && S.e[U - 1] == (int)a.E;
+  ItemCount n;
+  if (MAT == 2) {
+    const int routed_feats = S.item[shared ? U - 1 : U];
+    n.routed = routed_feats / fpi_of<RFMT>();
+    n.items = n.routed + (shared ? (S.item[U] - routed_feats) / 4 : 0);
+  } else {
+    const int per = (int)(a.out_per_e / NROWS);
+    n.routed = (shared ? U - 1 : U) * per;
+    n.items = U * per;
+  }
+  return n;
+}
+
+template <int MAT, int NROWS, int RFMT>
+__device__ __forceinline__ Item item_at(const StArgs &a, const SmemPlan &S, int U,
+                                        const ItemCount &n, int g) {
   Item it;
   int u, n0;
   if (MAT == 2) {
-    const int feat = g * NROWS;
-    u = find_slot(S.item, U, feat);
-    n0 = feat - S.item[u];
+    if (g < n.routed) {
+      const int feat = g * fpi_of<RFMT>();
+      u = find_slot(S.item, U, feat);
+      n0 = feat - S.item[u];
+      it.nf = fpi_of<RFMT>();
+    } else {
+      u = U - 1;
+      n0 = (g - n.routed) * 4;
+      it.nf = 4;
+    }
   } else {
     const int per = (int)(a.out_per_e / NROWS);
     u = g / per;
     n0 = (g - u * per) * NROWS;
+    it.nf = NROWS;
   }
   const int e = S.e[u];
   it.row0 = S.row0[u];
@@ -162,12 +209,13 @@ __device__ __forceinline__ Item item_at(const StArgs &a, const SmemPlan &S, int 
   it.n0 = n0;
   it.sh = e == (int)a.E;
   it.K = it.sh ? a.Ks : a.K;
+  it.rb = (uint32_t)row_bytes(it.sh ? MOE_FMT_Q8_0 : RFMT, it.K);
   // first weight row of the item in its matrix (k_plan validated the slot)
   const size_t r = it.sh ? (size_t)n0
                          : (size_t)weight_slot(a.eslot, e) * a.rows_per_slot + (size_t)n0;
 #pragma unroll
   for (int m = 0; m < MAT; ++m) {
-    it.q[m] = (it.sh ? a.sq[m] : a.q[m]) + r * it.K;
+    it.q[m] = (it.sh ? a.sq[m] : a.q[m]) + r * it.rb;
     it.s[m] = (it.sh ? a.ssc[m] : a.sc[m]) + r * (it.K / 32);
   }
   return it;
@@ -191,18 +239,12 @@ struct Chunks {
   }
 };
 
-template <int MAT, int NROWS>
-__device__ __forceinline__ Chunks chunks_of(const StArgs &a, const SmemPlan &S, int U,
-                                            int items) {
-  // items of the routed experts: all but the shared expert's, when it is on this list
-  int routed = items;
-  if (U > 0 && S.e[U - 1] == (int)a.E)
-    routed = MAT == 2 ? S.item[U - 1] / NROWS : (U - 1) * (int)(a.out_per_e / NROWS);
+__device__ __forceinline__ Chunks chunks_of(const ItemCount &n) {
   Chunks ch;
-  ch.routed = routed;
-  ch.items = items;
-  ch.n_shared = (items - routed + kChunk - 1) / kChunk;
-  ch.n = ch.n_shared + (routed + kChunk - 1) / kChunk;
+  ch.routed = n.routed;
+  ch.items = n.items;
+  ch.n_shared = (n.items - n.routed + kChunk - 1) / kChunk;
+  ch.n = ch.n_shared + (n.routed + kChunk - 1) / kChunk;
   return ch;
 }
 
@@ -361,6 +403,117 @@ __device__ __forceinline__ bool gateup_stage(const StArgs &a, const StageHdr &h,
   return true;
 }
 
+// gate/up of a routed item of 2-bit or e2m1 weights: fpi_of<RFMT> features
+// (FP = half of them a warp pair) for every row of the expert.  Warp w takes
+// features (w/2) FP .. + FP - 1 over K half w%2; lane l holds whole 32-blocks
+// l, l+32, .. of the half: 8 code bytes (2-bit) or 16 (e2m1) from the stage,
+// decoded once per block and dotted with every row's activation block (2-bit:
+// activations 16-code-group transposed) -- the register GEMV's exact block
+// dots.  The 2 FP x 2 partial sums of each lane are summed over the warp, the
+// two K halves of a feature in half order through shared memory; warp w then
+// finishes FP/2 features.  Stage layout after the header: gate codes
+// [fpi][rb], up codes [fpi][rb], gate scales [fpi][K/32], up scales [fpi][K/32].
+template <int RFMT, bool TAPS>
+__device__ __forceinline__ bool gateup_stage_lb(const StArgs &a, const StageHdr &h,
+                                                const int *hdr_rows, const uint8_t *w, int wi,
+                                                int lane, float *part, uint64_t *gbar,
+                                                uint32_t &par, uint64_t *empty_bar) {
+  constexpr int FPI = fpi_of<RFMT>(), FP = FPI / 2;
+  constexpr int NV = 2 * FP * kStRows;  // [m][feature of the pair][row]
+  constexpr int BB = RFMT == MOE_FMT_Q2S ? 8 : 16;  // code bytes a block
+  const uint32_t K = (uint32_t)h.K, nb = K / 32, nb2 = nb / 2, rb = nb * BB;
+  const int fp = wi >> 1, hk = wi & 1;
+  const int8_t *gcode = (const int8_t *)w;
+  const int8_t *ucode = gcode + (size_t)FPI * rb;
+  const uint16_t *gsc = (const uint16_t *)(w + (size_t)2 * FPI * rb);
+  const uint16_t *usc = gsc + (size_t)FPI * nb;
+  const int8_t *act = RFMT == MOE_FMT_Q2S ? a.act_t : a.act;
+  int jt[FP];
+#pragma unroll
+  for (int f = 0; f < FP; ++f) jt[f] = TAPS ? tapped((uint32_t)(h.n0 + fp * FP + f), a.f) : -1;
+  for (int r0 = 0; r0 < h.nrows; r0 += kStRows) {
+    const int nr = min(kStRows, h.nrows - r0);
+    W8 xr[kStRows][kGuJLowBit];
+    float xsr[kStRows][kGuJLowBit];
+    int sx[kStRows][kGuJLowBit];
+#pragma unroll
+    for (int r = 0; r < kStRows; ++r) {
+      const int rr = r0 + (r < nr ? r : 0);
+      const int tok = rr < kHdrRows ? hdr_rows[rr] : act_row_of<2>(a, false, h.row0 + rr);
+      const int8_t *xp = act + (size_t)tok * a.act_stride;
+      const float *xsp = a.act_s + (size_t)tok * a.act_s_stride;
+#pragma unroll
+      for (int j = 0; j < kGuJLowBit; ++j) {
+        const uint32_t bl = lane + 32u * j, b = hk * nb2 + bl;
+        if (r < nr && bl < nb2) {
+          xr[r][j] = ld_cached32(xp + 32 * b);
+          xsr[r][j] = __ldg(xsp + b);
+        } else {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) xr[r][j].v[q] = 0u;
+          xsr[r][j] = 0.0f;
+        }
+        sx[r][j] = block_sum(xr[r][j]);
+      }
+    }
+    float v[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = 0.0f;
+    constexpr int kU = NV / 2;
+#pragma unroll
+    for (int f = 0; f < FP; ++f) {
+      const int fr = fp * FP + f;  // feature row within the item
+#pragma unroll
+      for (int j = 0; j < kGuJLowBit; ++j) {
+        const uint32_t bl = lane + 32u * j, b = hk * nb2 + bl;
+        if (bl < nb2) {
+#pragma unroll
+          for (int m = 0; m < 2; ++m) {  // gate, then up: one decoded block live
+            const uint16_t *scp = m == 0 ? gsc : usc;
+            const int8_t *cp = (m == 0 ? gcode : ucode) + (size_t)fr * rb + BB * b;
+            const float sw = half_bits_to_float(scp[(size_t)fr * nb + b]) * scale_mul<RFMT>();
+            WBlock<RFMT> wb;
+            if constexpr (RFMT == MOE_FMT_Q2S) wb.c = *(const uint2 *)cp;
+            else wb.c = *(const uint4 *)cp;
+            wb.prep();
+#pragma unroll
+            for (int r = 0; r < kStRows; ++r) {
+              if (r < nr) {  // warp-uniform
+                const int pd = wb.dot(xr[r][j], sx[r][j]);
+                const int iv = m * kU + f * kStRows + r;
+                v[iv] = __fmaf_rn((float)pd, sw * xsr[r][j], v[iv]);
+                if (TAPS && jt[f] >= 0)
+                  a.tap[(((size_t)(h.row0 + r0 + r) * 2 + m) * kNTap + (size_t)jt[f]) * a.tap_nb +
+                        b] = pd;
+              }
+            }
+          }
+        }
+      }
+    }
+    if (r0 + kStRows >= h.nrows) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    const float tot = transpose_sum<NV>(v, lane);
+    float *pp = part + (size_t)par * kStGroupWarps * NV;
+    if (lane < NV) pp[wi * NV + lane] = tot;
+    if (!group_sync(gbar, par, lane)) return false;
+    // warp wi finishes features (wi/2) FP + (wi%2) FP/2 .. + FP/2 - 1: lane l
+    // takes feature (wi%2) FP/2 + l/2 of the pair, row l%2
+    const int fl = hk * (FP / 2) + (lane >> 1), r = lane & 1;
+    if (lane < FP && r < nr) {
+      const int ig = fl * kStRows + r;
+      const float *p0 = pp + (2 * fp) * NV, *p1 = p0 + NV;
+      const float g = __fadd_rn(p0[ig], p1[ig]), u = __fadd_rn(p0[kU + ig], p1[kU + ig]);
+      const float hv = __fmul_rn(__fdiv_rn(g, __fadd_rn(1.0f, spec_exp(-g))), u);
+      a.out[(size_t)(h.row0 + r0 + r) * a.out_stride + h.n0 + fp * FP + fl] = hv;
+    }
+    par ^= 1u;
+  }
+  return true;
+}
+
 // down rows n0 + wi*RW .. + RW - 1 for every row (slot) of the item's expert,
 // in passes of 2 slots and segments of 32*kDnJ blocks (lane l: whole 32-blocks
 // l, l+32, ..), every h block of a segment loaded before any use.  Stage layout
@@ -440,8 +593,9 @@ __device__ __forceinline__ void down_stage(const StArgs &a, const StageHdr &h, c
   }
 }
 
-// MAT = 2: gate/up (RW = 1: four features a stage); MAT = 1: down (RW rows a warp)
-template <int MAT, int RW, bool TAPS>
+// MAT = 2: gate/up (RW = 1; routed weights of format RFMT); MAT = 1: down (RW
+// rows a warp; Q8_0)
+template <int MAT, int RW, bool TAPS, int RFMT>
 __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   constexpr int kRows = kStGroupWarps * RW;  // rows of each matrix per stage
   pdl_trigger();
@@ -471,8 +625,8 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   PlanView P(const_cast<int *>(a.plan), a.E);
   const SmemPlan S(plan_sm, P, a.E);  // ends in a CTA barrier: the mbarriers are ready
   const int U = P.hdr[0];
-  const int items = MAT == 2 ? P.hdr[1] / kRows : P.hdr[2] / kRows;
-  const Chunks ch = chunks_of<MAT, kRows>(a, S, U, items);
+  const ItemCount ic = item_count<MAT, kRows, RFMT>(a, S, U);
+  const Chunks ch = chunks_of(ic);
   if (warp == kStProdWarp) {
     if (lane != 0) return;
     // activation rows the header carries: gate/up tokens (down: the slots, which
@@ -498,7 +652,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
     Item cur;
     int arow[kAR + 1];
     if (have) {
-      cur = item_at<MAT, kRows>(a, S, U, g);
+      cur = item_at<MAT, kRows, RFMT>(a, S, U, ic, g);
 #pragma unroll
       for (int r = 0; r < kAR; ++r)
         arow[r] = r < cur.nrows ? act_row_of<MAT>(a, cur.sh, cur.row0 + r) : 0;
@@ -534,7 +688,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
 #pragma unroll
       for (int r = 0; r < kAR; ++r) arow_n[r] = 0;
       if (more) {
-        nxt = item_at<MAT, kRows>(a, S, U, g);
+        nxt = item_at<MAT, kRows, RFMT>(a, S, U, ic, g);
         const bool same = g == g_cur + 1 && nxt.row0 == cur.row0 && nxt.sh == cur.sh;
 #pragma unroll
         for (int r = 0; r < kAR; ++r)
@@ -549,7 +703,7 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
       hd->K = (int)cur.K;
 #pragma unroll
       for (int r = 0; r < kAR; ++r) hd->act_row[r] = arow[r];
-      const uint32_t qb = (uint32_t)kRows * cur.K, sb = (uint32_t)kRows * (cur.K / 16);
+      const uint32_t qb = (uint32_t)cur.nf * cur.rb, sb = (uint32_t)cur.nf * (cur.K / 16);
       uint8_t *w = st + kStHdrBytes;
       mbar_expect_tx(&full[s], MAT * (qb + sb));
 #pragma unroll
@@ -610,9 +764,18 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
     h.sh = hp->sh;
     h.K = hp->K;
     if (MAT == 2) {
-      if (!gateup_stage<TAPS>(a, h, hp->act_row, st + kStHdrBytes, wi, lane,
-                              part + (size_t)gi * 2 * kStGroupWarps * kGuVals, &gbar[gi], par,
-                              &empty[s])) {
+      float *gpart = part + (size_t)gi * kStPartPerGroup;
+      bool ok;
+      if constexpr (RFMT != MOE_FMT_Q8_0) {
+        ok = !h.sh ? gateup_stage_lb<RFMT, TAPS>(a, h, hp->act_row, st + kStHdrBytes, wi, lane,
+                                                 gpart, &gbar[gi], par, &empty[s])
+                   : gateup_stage<TAPS>(a, h, hp->act_row, st + kStHdrBytes, wi, lane, gpart,
+                                        &gbar[gi], par, &empty[s]);
+      } else {
+        ok = gateup_stage<TAPS>(a, h, hp->act_row, st + kStHdrBytes, wi, lane, gpart, &gbar[gi],
+                                par, &empty[s]);
+      }
+      if (!ok) {
         atomicOr(a.err, kErrTimeout);
         *abort_flag = 1;
         break;
@@ -634,10 +797,21 @@ size_t stream_smem(uint32_t stage_bytes, uint32_t E) {
   return (size_t)kStStages * stage_bytes + kStBarBytes + 4 * kStPartFloats + smem_plan_bytes(E);
 }
 
-// bytes of a stage: header, MAT matrices of `rows` weight rows of K codes and
-// K/32 fp16 scales
-uint64_t stage_bytes_for(int mat, uint32_t rows, uint32_t K) {
-  return kStHdrBytes + (uint64_t)mat * rows * (K + K / 16);
+// bytes of a stage: header, MAT matrices of `rows` weight rows of K weights in
+// format fmt and K/32 fp16 scales
+uint64_t stage_bytes_for(int mat, uint32_t rows, uint32_t K, int fmt = MOE_FMT_Q8_0) {
+  return kStHdrBytes + (uint64_t)mat * rows * (row_bytes(fmt, K) + K / 16);
+}
+
+// a gate/up stage holds a routed item or a shared-expert item (4 Q8_0 features)
+uint64_t gateup_stage_bytes(const moe_desc &D) {
+  const int fmt = D.routed_fmt;
+  const uint32_t fpi = fmt == MOE_FMT_Q2S    ? fpi_of<MOE_FMT_Q2S>()
+                       : fmt == MOE_FMT_E2M1 ? fpi_of<MOE_FMT_E2M1>()
+                                             : fpi_of<MOE_FMT_Q8_0>();
+  uint64_t b = stage_bytes_for(2, fpi, D.d, fmt);
+  if (D.f_shared) b = std::max<uint64_t>(b, stage_bytes_for(2, kStGroupWarps, D.d));
+  return b;
 }
 
 // down rows a warp takes per stage: the most of 6, 4, 2, 1 whose stage fits and
@@ -653,10 +827,10 @@ int down_rw(const moe_desc &D) {
   return 0;
 }
 
-template <int MAT, int RW, bool TAPS>
+template <int MAT, int RW, bool TAPS, int RFMT = MOE_FMT_Q8_0>
 cudaError_t run_stream(const Ctx &c, const StArgs &a) {
   static bool big_smem = false;
-  auto kern = k_stream<MAT, RW, TAPS>;
+  auto kern = k_stream<MAT, RW, TAPS, RFMT>;
   const size_t smem = stream_smem(a.stage_bytes, c.desc.n_expert);
   if (!big_smem) {
     const cudaError_t e =
@@ -671,14 +845,15 @@ cudaError_t run_stream(const Ctx &c, const StArgs &a) {
 
 }  // namespace
 
-// gate/up on the streamed GEMV: Q8_0 routed weights; d a multiple of 128 (a
+// gate/up on the streamed GEMV (any routed format): d a multiple of 128 (a
 // 4-feature scale slice is a whole number of 16-byte copies; K halves of whole
 // blocks) and at most 6144 (3 blocks a lane and row); 16-byte aligned scale
 // planes
 bool stream_gateup_ok(const Ctx &c) {
   const moe_desc &D = c.desc;
-  if (D.routed_fmt != MOE_FMT_Q8_0 || D.d % 128 || D.d > 64u * 32u * kGuJ) return false;
-  if (stage_bytes_for(2, kStGroupWarps, D.d) > kStStageMax) return false;
+  const uint32_t jmax = D.routed_fmt == MOE_FMT_Q8_0 ? kGuJ : kGuJLowBit;
+  if (D.d % 128 || D.d > 64u * 32u * jmax) return false;
+  if (gateup_stage_bytes(D) > kStStageMax) return false;
   if (!aligned16(c.wts.gate.scale) || !aligned16(c.wts.up.scale)) return false;
   if (D.f_shared && (!aligned16(c.wts.s_gate.scale) || !aligned16(c.wts.s_up.scale))) return false;
   return true;
@@ -718,6 +893,7 @@ cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm) {
   a.rows_per_slot = D.f;
   a.eslot = c.wts.expert_slot;
   a.act = (const int8_t *)(c.ws + c.L.xq);
+  a.act_t = c.L.xt ? (const int8_t *)(c.ws + c.L.xt) : nullptr;
   a.act_s = (const float *)(c.ws + c.L.xs);
   a.act_stride = D.d;
   a.act_s_stride = D.d / 32;
@@ -728,12 +904,20 @@ cudaError_t launch_gateup_stream(const Ctx &c, const int32_t *perm) {
   a.tap = taps ? (int32_t *)(c.ws + c.L.tap_gu) : nullptr;
   a.tap_nb = D.d / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
-  a.stage_bytes = (uint32_t)stage_bytes_for(2, kStGroupWarps, D.d);
+  a.stage_bytes = (uint32_t)gateup_stage_bytes(D);
   a.queue = (uint32_t *)(c.ws + c.L.sync) + kQueueStreamGateup;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase
                 : nullptr;
-  return taps ? run_stream<2, 1, true>(c, a) : run_stream<2, 1, false>(c, a);
+  switch (D.routed_fmt) {
+    case MOE_FMT_Q2S:
+      return taps ? run_stream<2, 1, true, MOE_FMT_Q2S>(c, a)
+                  : run_stream<2, 1, false, MOE_FMT_Q2S>(c, a);
+    case MOE_FMT_E2M1:
+      return taps ? run_stream<2, 1, true, MOE_FMT_E2M1>(c, a)
+                  : run_stream<2, 1, false, MOE_FMT_E2M1>(c, a);
+    default: return taps ? run_stream<2, 1, true>(c, a) : run_stream<2, 1, false>(c, a);
+  }
 }
 
 cudaError_t launch_down_stream(const Ctx &c) {
