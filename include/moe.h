@@ -295,7 +295,8 @@ moe_status moe_ffn_experts(const moe_desc *desc, const moe_weights *wts, const f
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);
 
 /* Row threshold of the tensor-core path of moe_layer for (desc, T) on the
- * current device: an expert (the shared expert included, with T rows, when
+ * current device (6 for Q8_0 and Q2S routed weights, 4 for E2M1, 0 with
+ * MOE_FLAG_FORCE_TC): an expert (the shared expert included, with T rows, when
  * f_shared == f) whose routed row count exceeds it runs its block dots on
  * tcgen05 tensor cores, the rest on the dp4a GEMV -- provided those experts'
  * gate/up tiles (128 features x 64 rows each) number at least the device's SM

@@ -2,7 +2,8 @@
 // into shared memory by the bulk-copy engine.
 //
 // The multi-kernel path's experts with few rows (every expert below 32 tokens a
-// call, the experts with at most 4 rows above) are bound by the weight stream:
+// call, above it the experts with at most 6 rows, 4 for e2m1) are bound by the
+// weight stream:
 // each selected expert's rows are read once per call and applied to all of its
 // rows (the union-of-experts read of NeutronStar README, "MTP speculative
 // decoding"; the indexed per-expert FFN).  Rather than every warp loading its

@@ -984,7 +984,7 @@ bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.d % 256 || D.f % 256 || (D.f_shared && D.f_shared % 256)) return false;
   // unforced, only from kTcMinTokens tokens: below that no expert brings enough
   // tiles to pay for the tensor kernels and their activation copies
-  return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T >= kTcMinTokens && T > kTcMinRows;
+  return (D.flags & MOE_FLAG_FORCE_TC) ? T > 0 : T >= kTcMinTokens && T > tc_min_rows_for(D.routed_fmt);
 }
 
 cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm) {

@@ -419,7 +419,7 @@ int32_t moe_tc_min_rows(const moe_desc *desc, uint32_t T) {
   if (!desc_ok(desc)) return -1;
   Ctx c = make_ctx(desc, nullptr, T, nullptr, nullptr);
   if (T == 0 || fused_eligible(c) || !tc_possible(*desc, T) || !tc_supported(*desc)) return -1;
-  return (desc->flags & MOE_FLAG_FORCE_TC) ? 0 : (int32_t)kTcMinRows;
+  return (desc->flags & MOE_FLAG_FORCE_TC) ? 0 : (int32_t)tc_min_rows_for(desc->routed_fmt);
 }
 
 const char *moe_layer_stage_name(const moe_desc *desc, uint32_t T, uint32_t i) {

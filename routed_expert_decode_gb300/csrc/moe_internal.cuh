@@ -90,8 +90,13 @@ constexpr uint32_t kQueueTcGateup = 2052, kQueueTcDown = 2054;
 static_assert(4 + 1024 + 1 <= kQueueStreamGateup && kQueueTcDown + 2 <= MOE_SYNC_BYTES / 4 - 2,
               "work queues overlap the fused kernel's counters");
 
-// rows per expert above which an expert runs on the tensor-core path
-constexpr uint32_t kTcMinRows = 4;
+// rows per expert above which an expert runs on the tensor-core path.  Timed on
+// the 256-expert layers: 6 for int8 and 2-bit weights (experts of 5-6 rows are
+// as fast or faster on the dp4a GEMV, whose weight stream they then join), 4
+// for e2m1 (whose GEMV spends more instructions a weight decoding codes)
+__host__ __device__ constexpr uint32_t tc_min_rows_for(int32_t routed_fmt) {
+  return routed_fmt == MOE_FMT_E2M1 ? 4u : 6u;
+}
 // calls with fewer tokens run every expert on the dp4a GEMV (no tensor kernel,
 // no activation copies launched): measured on the 256-expert layer, the GEMV
 // alone was as fast or faster up to 16 tokens a call, the tensor path faster

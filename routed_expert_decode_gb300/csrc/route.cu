@@ -505,14 +505,15 @@ cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32
 cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
                              const int32_t *perm, const int32_t *pos, uint32_t *err) {
   int *plan = (int *)(c.ws + c.L.plan);
-  // tensor path: 0 off, 1 for experts with more than kTcMinRows rows, 2 forced
+  // tensor path: 0 off, 1 for experts with more than tc_min_rows_for(fmt) rows,
+  // 2 forced
   const moe_desc &D = c.desc;
   int tc_mode = 0;
   // the same condition under which run_ffn launches the tensor kernels
   if (c.L.xperm && tc_supported(D)) tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
   const cudaError_t e = launch_k(k_plan, 1, kPlanThreads, 0, c.stream, c.chained, off, idx, perm,
                                  pos, c.T, D.n_expert, D.top_k, D.f, D.f_shared, D.d, tc_mode,
-                                 kTcMinRows, (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
+                                 tc_min_rows_for(D.routed_fmt), (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,
                                  c.e_lo, c.e_hi, c.shared_on ? 1 : 0, plan, err);
   c.chained = true;
   return e;

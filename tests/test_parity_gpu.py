@@ -260,11 +260,11 @@ def test_prefill_t512_full_size(gpu):
 
 def test_q2_t64_full_size(gpu):
     """The 2-bit layer at T=64 (auto dispatch: the shared expert and the 2-bit
-    experts with more than 4 rows on the tensor cores, when they fill the SMs)."""
+    experts with more than 6 rows on the tensor cores, when they fill the SMs)."""
     from routed_expert_decode_gb300 import moe
 
     layer = device_layer(synth.Q2_LAYER, gpu)
-    assert moe.tc_min_rows(layer.desc(), 64) == 4
+    assert moe.tc_min_rows(layer.desc(), 64) == 6
     print("q2_t64", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 33, 63]))
     print("q2_t64 gemv", run_case(synth.Q2_LAYER, 64, seed=0, device=gpu, sample=[0, 63],
                                   flags=moe.FLAG_FORCE_GEMV))
@@ -272,7 +272,8 @@ def test_q2_t64_full_size(gpu):
 
 def test_fp4_t64_full_size(gpu):
     """The e2m1 layer (the 2-bit layer's shape) at T=64, auto dispatch and
-    dp4a-only: the same exact block dots on both paths."""
+    dp4a-only: the same exact block dots on both paths (auto dispatch puts the
+    experts with more than 4 rows on the tensor cores)."""
     from routed_expert_decode_gb300 import moe
 
     layer = device_layer(synth.E2M1_LAYER, gpu)
