@@ -13,10 +13,14 @@ namespace {
 
 constexpr int kRouteWarps = 8;
 
-// One warp per token.  Lane l owns experts l, l+32, ...; each of the top_k
-// rounds takes every lane's best unpicked expert and reduces them with a
-// butterfly argmax whose order is (score descending, index ascending), so all
-// lanes agree on a unique winner and ties go to the lower index.
+// One warp per token.  Lane l owns experts l, l+32, ... (NPER of them: the
+// kernel is instantiated for E <= 256, 512 and 1024 so that its unrolled loops
+// are no longer than the layer needs -- this code runs once per call from a
+// cold instruction cache); each of the top_k rounds takes every lane's best
+// unpicked expert and reduces them with a butterfly argmax whose order is
+// (score descending, index ascending), so all lanes agree on a unique winner
+// and ties go to the lower index.
+template <int NPER>
 __global__ void __launch_bounds__(kRouteWarps * 32)
     k_route(const float *__restrict__ logits, const float *__restrict__ bias, uint32_t T,
             uint32_t E, uint32_t k, float s, uint32_t score, int32_t *__restrict__ idx,
@@ -28,9 +32,9 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   if (t >= T) return;
   const float *l = logits + (size_t)t * E;
   const int nper = (int)((E + 31) / 32);
-  float c[32], sg[32];
+  float c[NPER], sg[NPER];
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NPER; ++i) {
     const uint32_t e = (uint32_t)lane + 32u * i;
     c[i] = -INFINITY;
     sg[i] = 0.0f;
@@ -46,7 +50,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
     float bc = -INFINITY, bs = 0.0f;
     int be = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NPER; ++i) {
       if (i < nper && !((taken >> i) & 1u) && c[i] > bc) {
         bc = c[i];
         be = lane + 32 * i;
@@ -292,7 +296,10 @@ __global__ void __launch_bounds__(kPlanThreads)
     return tc_mode == 2 ? true : (uint32_t)rows > tc_min_rows;
   };
   const int ntile_n = (int)kTcTileN;
-  int ng = 0, ntc = 0, ntile_gu = 0, maxrows = 0, total;
+  __shared__ int rows_max;  // the most rows of any expert this call computes
+  if (tid == 0) rows_max = 0;
+  __syncthreads();
+  int ng = 0, ntc = 0, ntile_gu = 0, total;
   for (uint32_t base = 0; base < E; base += kPlanThreads) {
     const uint32_t e = base + tid;
     const int rows = e < E ? own_rows(e) : 0;
@@ -321,11 +328,12 @@ __global__ void __launch_bounds__(kPlanThreads)
     ng += gtotal;
     ntc += ttotal;
     ntile_gu += tiles_total;
-    if (tid == 0)
-      for (uint32_t q = base; q < base + kPlanThreads && q < E; ++q)
-        maxrows = max(maxrows, own_rows(q));
+    const int wmax = __reduce_max_sync(0xffffffffu, rows);
+    if ((tid & 31) == 0 && wmax > 0) atomicMax(&rows_max, wmax);
   }
+  __syncthreads();
   if (tid == 0) {
+    const int maxrows = rows_max;
     int U = ng;
     int items = U * (int)f;
     int V = ntc;
@@ -443,9 +451,10 @@ cudaError_t launch_route(const Ctx &c, const float *logits, const float *bias, i
                          float *w) {
   if (c.T == 0) return cudaSuccess;
   const unsigned grid = (c.T + kRouteWarps - 1) / kRouteWarps;
-  const cudaError_t e = launch_k(k_route, grid, kRouteWarps * 32, 0, c.stream, c.chained, logits,
-                                 bias, c.T, c.desc.n_expert, c.desc.top_k, c.desc.s,
-                                 c.desc.score, idx, w);
+  const uint32_t E = c.desc.n_expert;
+  auto kern = E <= 256 ? k_route<8> : E <= 512 ? k_route<16> : k_route<32>;
+  const cudaError_t e = launch_k(kern, grid, kRouteWarps * 32, 0, c.stream, c.chained, logits,
+                                 bias, c.T, E, c.desc.top_k, c.desc.s, c.desc.score, idx, w);
   c.chained = true;
   return e;
 }
