@@ -242,7 +242,51 @@ __device__ __forceinline__ int transposed_lane(int lane) {
   return (lane & 16) | ((lane & 3) << 2) | ((lane >> 2) & 3);
 }
 
-// requantise h per 32-block: one warp per (slot, block)
+// requantise h per 32-block.  A warp unit is 4 consecutive blocks of one slot
+// (lane l holds h[4l .. 4l+3] of the 128, so lanes 8j .. 8j+7 hold block j);
+// a fixed grid of warps walks the units two at a time, both units' loads
+// issued first.  Per block: amax over its 32 values (one 8-lane max over the
+// |h| bit patterns), scale amax / 127, codes as quant_one.
+__device__ __forceinline__ float4 requant_load(const float *h, uint64_t u, uint32_t groups,
+                                               uint32_t fmax, uint32_t R, uint32_t f, uint32_t fs,
+                                               uint64_t units, int lane) {
+  if (u >= units) return make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint32_t slot = (uint32_t)(u / groups), b = (uint32_t)(u % groups) * 4 + (lane >> 3);
+  const uint32_t width = slot < R ? f : fs;
+  if (32 * b >= width) return make_float4(0.f, 0.f, 0.f, 0.f);
+  return *reinterpret_cast<const float4 *>(h + (size_t)slot * fmax + 32 * b + 4 * (lane & 7));
+}
+
+__device__ __forceinline__ void requant_store(float4 v, uint64_t u, uint32_t groups,
+                                              uint32_t fmax, uint32_t R, uint32_t f, uint32_t fs,
+                                              uint64_t units, int lane, int8_t *__restrict__ hq,
+                                              float *__restrict__ hs, int8_t *__restrict__ ht) {
+  // every lane takes part in the shuffles; out-of-range lanes hold zeros
+  uint32_t m = max(max(__float_as_uint(fabsf(v.x)), __float_as_uint(fabsf(v.y))),
+                   max(__float_as_uint(fabsf(v.z)), __float_as_uint(fabsf(v.w))));
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) m = max(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (u >= units) return;
+  const uint32_t slot = (uint32_t)(u / groups), b = (uint32_t)(u % groups) * 4 + (lane >> 3);
+  const uint32_t width = slot < R ? f : fs;
+  if (32 * b >= width) return;
+  const float sc = __fdiv_rn(__uint_as_float(m), 127.0f);
+  const int q0 = quant_one(v.x, sc), q1 = quant_one(v.y, sc), q2 = quant_one(v.z, sc),
+            q3 = quant_one(v.w, sc);
+  const size_t i = (size_t)slot * fmax + 32 * b + 4 * (lane & 7);
+  *reinterpret_cast<char4 *>(hq + i) = make_char4((signed char)q0, (signed char)q1,
+                                                  (signed char)q2, (signed char)q3);
+  if (ht && slot < R) {
+    int8_t *tb = ht + (size_t)slot * fmax + 32 * b;
+    const int e0 = 4 * (lane & 7);
+    tb[transposed_lane(e0)] = (int8_t)q0;
+    tb[transposed_lane(e0 + 1)] = (int8_t)q1;
+    tb[transposed_lane(e0 + 2)] = (int8_t)q2;
+    tb[transposed_lane(e0 + 3)] = (int8_t)q3;
+  }
+  if ((lane & 7) == 0) hs[(size_t)slot * (fmax / 32) + b] = sc;
+}
+
 __global__ void __launch_bounds__(256)
     k_requant(const float *__restrict__ h, uint32_t slots, uint32_t R, uint32_t f, uint32_t fs,
               uint32_t fmax, int8_t *__restrict__ hq, float *__restrict__ hs,
@@ -250,21 +294,15 @@ __global__ void __launch_bounds__(256)
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const uint32_t nbmax = fmax / 32;
-  const uint64_t gw = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32;
-  if (gw >= (uint64_t)slots * nbmax) return;
-  const uint32_t slot = (uint32_t)(gw / nbmax), b = (uint32_t)(gw % nbmax);
-  const uint32_t width = slot < R ? f : fs;
-  if (b >= width / 32) return;
-  const size_t i = (size_t)slot * fmax + 32 * b + lane;
-  const float v = h[i];
-  // |h| of finite values orders as its bit pattern: one warp max reduction
-  const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v))));
-  const float sc = __fdiv_rn(amax, 127.0f);
-  const int8_t q = (int8_t)quant_one(v, sc);
-  hq[i] = q;
-  if (ht && slot < R) ht[(size_t)slot * fmax + 32 * b + transposed_lane(lane)] = q;
-  if (lane == 0) hs[(size_t)slot * nbmax + b] = sc;
+  const uint32_t groups = (fmax + 127) / 128;
+  const uint64_t units = (uint64_t)slots * groups;
+  const uint64_t nw = (uint64_t)gridDim.x * 8;
+  for (uint64_t u = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32; u < units; u += 2 * nw) {
+    const float4 v0 = requant_load(h, u, groups, fmax, R, f, fs, units, lane);
+    const float4 v1 = requant_load(h, u + nw, groups, fmax, R, f, fs, units, lane);
+    requant_store(v0, u, groups, fmax, R, f, fs, units, lane, hq, hs, ht);
+    requant_store(v1, u + nw, groups, fmax, R, f, fs, units, lane, hq, hs, ht);
+  }
 }
 
 // o[slot][m] for m in [m0, m0 + NF), rows of one expert: down rows (K = width)
@@ -484,10 +522,13 @@ cudaError_t launch_gateup(const Ctx &c, const int32_t *perm) {
 
 cudaError_t launch_requant_h(const Ctx &c) {
   const uint32_t slots = c.R + (c.desc.f_shared ? c.T : 0);
-  const uint64_t warps = (uint64_t)slots * (c.fmax / 32);
-  if (warps == 0) return cudaSuccess;
+  const uint64_t units = (uint64_t)slots * ((c.fmax + 127) / 128);
+  if (units == 0) return cudaSuccess;
+  // a fixed grid (6 CTAs of 8 warps an SM: all resident at the kernel's 40
+  // registers a thread) walking the units, two a warp at a time
+  const uint64_t ctas = std::min<uint64_t>((units + 15) / 16, (uint64_t)c.sm_count * 6);
   const cudaError_t e = launch_k(
-      k_requant, (unsigned)((warps + 7) / 8), 256, 0, c.stream, c.chained,
+      k_requant, (unsigned)ctas, 256, 0, c.stream, c.chained,
       (const float *)(c.ws + c.L.h), slots, c.R, c.desc.f, c.desc.f_shared, c.fmax,
       (int8_t *)(c.ws + c.L.hq), (float *)(c.ws + c.L.hs),
       c.L.ht ? (int8_t *)(c.ws + c.L.ht) : nullptr);
