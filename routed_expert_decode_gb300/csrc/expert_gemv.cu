@@ -379,7 +379,9 @@ __global__ void __launch_bounds__(kWarpsPerCta * 32, (min_ctas_dn<FMT, MAXR>()))
 
 // y[t][m] = o_shared[t][m] + sum_j w[t,j] * o[pos[t,j]][m], in that order
 // (only the slots of experts in [e_lo, e_hi), and the shared term if `shared`:
-// an expert-parallel rank's share of the sum)
+// an expert-parallel rank's share of the sum).  A thread takes 4 consecutive m
+// of one token (d is a multiple of 32) and issues the loads of 8 terms before
+// their multiply-adds.
 __global__ void __launch_bounds__(256)
     k_combine(const float *__restrict__ o, const float *__restrict__ w,
               const int32_t *__restrict__ pos, const int32_t *__restrict__ idx, uint32_t T,
@@ -387,23 +389,57 @@ __global__ void __launch_bounds__(256)
               bool all_experts, const int *__restrict__ plan, float *__restrict__ y) {
   pdl_trigger();
   pdl_wait();
+  const uint32_t d4 = d / 4;
   const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (uint64_t)T * d) return;
+  if (i >= (uint64_t)T * d4) return;
+  const uint32_t t = (uint32_t)(i / d4), m = 4 * (uint32_t)(i % d4);
+  float *yo = y + (size_t)t * d + m;
+  // y is the caller's: 16-byte stores only where it is 16-byte aligned
+  auto store = [&](float4 v) {
+    if (((uintptr_t)y & 15u) == 0) {
+      *reinterpret_cast<float4 *>(yo) = v;
+    } else {
+      yo[0] = v.x;
+      yo[1] = v.y;
+      yo[2] = v.z;
+      yo[3] = v.w;
+    }
+  };
   if (plan[4] != 1) {  // rejected routing arrays: no expert ran, pos[] is not trusted
-    y[i] = 0.0f;
+    store(make_float4(0.0f, 0.0f, 0.0f, 0.0f));
     return;
   }
-  const uint32_t t = (uint32_t)(i / d), m = (uint32_t)(i % d);
-  float acc = shared ? o[((size_t)R + t) * d + m] : 0.0f;
-  for (uint32_t j = 0; j < k; ++j) {
-    if (!all_experts) {
-      const uint32_t e = (uint32_t)idx[(size_t)t * k + j];
-      if (e < e_lo || e >= e_hi) continue;
+  float4 acc = shared ? *reinterpret_cast<const float4 *>(o + ((size_t)R + t) * d + m)
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  for (uint32_t j0 = 0; j0 < k; j0 += 8) {
+    float4 ov[8];
+    float wv[8];
+    bool use[8];
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      const uint32_t j = j0 + (uint32_t)jj;
+      use[jj] = j < k;
+      if (use[jj] && !all_experts) {
+        const uint32_t e = (uint32_t)idx[(size_t)t * k + j];
+        use[jj] = e >= e_lo && e < e_hi;
+      }
+      if (use[jj]) {
+        const int p = pos[(size_t)t * k + j];
+        wv[jj] = w[(size_t)t * k + j];
+        ov[jj] = *reinterpret_cast<const float4 *>(o + (size_t)p * d + m);
+      }
     }
-    const int p = pos[(size_t)t * k + j];
-    acc = __fmaf_rn(w[(size_t)t * k + j], o[(size_t)p * d + m], acc);
+#pragma unroll
+    for (int jj = 0; jj < 8; ++jj) {
+      if (use[jj]) {
+        acc.x = __fmaf_rn(wv[jj], ov[jj].x, acc.x);
+        acc.y = __fmaf_rn(wv[jj], ov[jj].y, acc.y);
+        acc.z = __fmaf_rn(wv[jj], ov[jj].z, acc.z);
+        acc.w = __fmaf_rn(wv[jj], ov[jj].w, acc.w);
+      }
+    }
   }
-  y[i] = acc;
+  store(acc);
 }
 
 // resident CTAs per SM of a persistent GEMV kernel with `smem` dynamic bytes
@@ -567,7 +603,7 @@ cudaError_t launch_down(const Ctx &c) {
 
 cudaError_t launch_combine(const Ctx &c, const float *w, const int32_t *pos,
                            const int32_t *idx, float *y) {
-  const uint64_t n = (uint64_t)c.T * c.desc.d;
+  const uint64_t n = (uint64_t)c.T * (c.desc.d / 4);  // threads: 4 outputs each
   if (n == 0) return cudaSuccess;
   const bool all = c.e_lo == 0 && c.e_hi >= c.desc.n_expert;
   const cudaError_t e = launch_k(

@@ -423,26 +423,62 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
 }
 
-// Activation quantiser: one warp per 32-block.
+// Activation quantiser.  A warp unit is 4 consecutive 32-blocks of x (lane l
+// holds values 4l .. 4l+3 of the 128, so lanes 8j .. 8j+7 hold block j); a
+// fixed grid of warps walks the units, two at a time with both units' loads
+// issued first.  Per block: amax over its 32 values, scale amax / 127, codes
+// as quant_one.
+__device__ __forceinline__ float4 quant_load(const float *x, uint64_t u, uint32_t nblocks,
+                                             int lane) {
+  const uint64_t b = 4 * u + (uint64_t)(lane >> 3);
+  if (b >= nblocks) return make_float4(0.f, 0.f, 0.f, 0.f);
+  const float *p = x + b * 32 + 4 * (lane & 7);
+  if (((uintptr_t)x & 15u) == 0) return *reinterpret_cast<const float4 *>(p);
+  return make_float4(p[0], p[1], p[2], p[3]);  // the caller's x, not 16-byte aligned
+}
+
+__device__ __forceinline__ void quant_store(float4 v, uint64_t u, uint32_t nblocks, int lane,
+                                            int8_t *__restrict__ xq, float *__restrict__ xs,
+                                            int8_t *__restrict__ xt) {
+  float a = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+#pragma unroll
+  for (int o = 4; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+  const uint64_t b = 4 * u + (uint64_t)(lane >> 3);
+  if (b >= nblocks) return;
+  const float sc = __fdiv_rn(a, 127.0f);
+  const int q0 = quant_one(v.x, sc), q1 = quant_one(v.y, sc), q2 = quant_one(v.z, sc),
+            q3 = quant_one(v.w, sc);
+  const int e0 = 4 * (lane & 7);
+  *reinterpret_cast<char4 *>(xq + b * 32 + e0) =
+      make_char4((signed char)q0, (signed char)q1, (signed char)q2, (signed char)q3);
+  // 2-bit routed weights also read the codes with each 16-code group 4x4
+  // transposed: code 16g + 4j + i at byte 16g + 4i + j
+  if (xt) {
+    int8_t *tb = xt + b * 32;
+    const int q[4] = {q0, q1, q2, q3};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int e = e0 + i;
+      tb[(e & 16) | ((e & 3) << 2) | ((e >> 2) & 3)] = (int8_t)q[i];
+    }
+  }
+  if ((lane & 7) == 0) xs[b] = sc;
+}
+
 __global__ void __launch_bounds__(256)
     k_quant(const float *__restrict__ x, uint32_t nblocks, int8_t *__restrict__ xq,
             float *__restrict__ xs, int8_t *__restrict__ xt) {
   pdl_trigger();
   pdl_wait();
   const int lane = threadIdx.x & 31;
-  const uint32_t b = blockIdx.x * 8 + threadIdx.x / 32;
-  if (b >= nblocks) return;
-  const float v = x[(size_t)b * 32 + lane];
-  float a = fabsf(v);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
-  const float sc = __fdiv_rn(a, 127.0f);
-  const int8_t q = (int8_t)quant_one(v, sc);
-  xq[(size_t)b * 32 + lane] = q;
-  // 2-bit routed weights also read the codes with each 16-code group 4x4
-  // transposed: code 16g + 4j + i at byte 16g + 4i + j
-  if (xt) xt[(size_t)b * 32 + ((lane & 16) | ((lane & 3) << 2) | ((lane >> 2) & 3))] = q;
-  if (lane == 0) xs[b] = sc;
+  const uint64_t units = ((uint64_t)nblocks + 3) / 4;
+  const uint64_t nw = (uint64_t)gridDim.x * 8;
+  for (uint64_t u = (uint64_t)blockIdx.x * 8 + threadIdx.x / 32; u < units; u += 2 * nw) {
+    const float4 v0 = quant_load(x, u, nblocks, lane);
+    const float4 v1 = quant_load(x, u + nw, nblocks, lane);
+    quant_store(v0, u, nblocks, lane, xq, xs, xt);
+    quant_store(v1, u + nw, nblocks, lane, xq, xs, xt);
+  }
 }
 
 }  // namespace
@@ -531,7 +567,11 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
 cudaError_t launch_quant_x(const Ctx &c, const float *x) {
   const uint32_t nblocks = c.T * (c.desc.d / 32);
   if (nblocks == 0) return cudaSuccess;
-  const cudaError_t e = launch_k(k_quant, (nblocks + 7) / 8, 256, 0, c.stream, c.chained, x,
+  // a fixed grid (at most 6 CTAs of 8 warps an SM) walking 4-block units, two a
+  // warp at a time
+  const uint32_t units = (nblocks + 3) / 4;
+  const uint32_t ctas = std::min<uint32_t>((units + 15) / 16, (uint32_t)c.sm_count * 6);
+  const cudaError_t e = launch_k(k_quant, ctas, 256, 0, c.stream, c.chained, x,
                                  nblocks, (int8_t *)(c.ws + c.L.xq), (float *)(c.ws + c.L.xs),
                                  c.L.xt ? (int8_t *)(c.ws + c.L.xt) : nullptr);
   c.chained = true;
