@@ -162,7 +162,7 @@ struct Item {
 // The call's items: the routed experts' first, then the shared expert's (the
 // last expert of the plan's list, when it is there).  Gate/up: routed items of
 // fpi_of<RFMT> features, shared items of 4 (Q8_0); down: NROWS output rows
-// throughout (Q8_0 weights only), out_per_e / NROWS per expert.
+// throughout, out_per_e / NROWS per expert.
 struct ItemCount {
   int routed, items;
 };
@@ -594,8 +594,98 @@ __device__ __forceinline__ void down_stage(const StArgs &a, const StageHdr &h, c
   }
 }
 
+// down rows n0 + wi*RW .. + RW - 1 of a routed item of 2-bit or e2m1 weights,
+// for every slot of its expert, in passes of 2 slots and segments of 32*kDnJ
+// blocks: lane l takes whole 32-blocks l, l+32, .., each row's block decoded
+// once from the stage (8 or 16 code bytes) and dotted with both slots' h blocks
+// (2-bit: h codes 16-code-group transposed) -- the register GEMV's exact block
+// dots.  Stage layout after the header: codes [4*RW][rb], scales [4*RW][K/32].
+// Arrives on the stage's empty barrier after its last read.
+template <int RFMT, int RW, bool TAPS>
+__device__ __forceinline__ void down_stage_lb(const StArgs &a, const StageHdr &h,
+                                              const uint8_t *w, int wi, int lane,
+                                              uint64_t *empty_bar) {
+  static_assert(RW * kStRows <= 16, "one transposed warp sum per pass");
+  constexpr int kRows = kStGroupWarps * RW;
+  constexpr int BB = RFMT == MOE_FMT_Q2S ? 8 : 16;  // code bytes a block
+  const uint32_t K = (uint32_t)h.K, nb = K / 32, rb = nb * BB;
+  const int8_t *wc = (const int8_t *)w + (size_t)wi * RW * rb;
+  const uint16_t *wsc = (const uint16_t *)(w + (size_t)kRows * rb) + (size_t)wi * RW * nb;
+  const int8_t *act = RFMT == MOE_FMT_Q2S ? a.act_t : a.act;
+  const int m0 = h.n0 + wi * RW;
+  int jt[RW];
+#pragma unroll
+  for (int q = 0; q < RW; ++q) jt[q] = TAPS ? tapped((uint32_t)(m0 + q), a.d) : -1;
+  for (int r0 = 0; r0 < h.nrows; r0 += kStRows) {
+    const int nr = min(kStRows, h.nrows - r0);
+    int slot[kStRows];
+    const int8_t *hp[kStRows];
+    const float *hsp[kStRows];
+#pragma unroll
+    for (int r = 0; r < kStRows; ++r) {
+      slot[r] = h.row0 + r0 + (r < nr ? r : 0);
+      hp[r] = act + (size_t)slot[r] * a.act_stride;
+      hsp[r] = a.act_s + (size_t)slot[r] * a.act_s_stride;
+    }
+    float v[16];  // [row q][slot r] at q * kStRows + r
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+#pragma unroll 1
+    for (uint32_t b0 = 0; b0 < nb; b0 += 32 * kDnJ) {
+      W8 hx[kStRows][kDnJ];
+      float hsc[kStRows][kDnJ];
+      int sx[kStRows][kDnJ];
+#pragma unroll
+      for (int r = 0; r < kStRows; ++r)
+#pragma unroll
+        for (int j = 0; j < kDnJ; ++j) {
+          const uint32_t b = b0 + lane + 32u * j;
+          if (r < nr && b < nb) {
+            hx[r][j] = ld_cached32(hp[r] + 32 * b);
+            hsc[r][j] = __ldg(hsp[r] + b);
+          } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) hx[r][j].v[q] = 0u;
+            hsc[r][j] = 0.0f;
+          }
+          sx[r][j] = block_sum(hx[r][j]);
+        }
+#pragma unroll
+      for (int q = 0; q < RW; ++q)
+#pragma unroll
+        for (int j = 0; j < kDnJ; ++j) {
+          const uint32_t b = b0 + lane + 32u * j;
+          if (b < nb) {
+            const float sw = half_bits_to_float(wsc[(size_t)q * nb + b]) * scale_mul<RFMT>();
+            WBlock<RFMT> wb;
+            const int8_t *cp = wc + (size_t)q * rb + BB * b;
+            if constexpr (RFMT == MOE_FMT_Q2S) wb.c = *(const uint2 *)cp;
+            else wb.c = *(const uint4 *)cp;
+            wb.prep();
+#pragma unroll
+            for (int r = 0; r < kStRows; ++r) {
+              if (r < nr) {
+                const int p = wb.dot(hx[r][j], sx[r][j]);
+                v[q * kStRows + r] = __fmaf_rn((float)p, sw * hsc[r][j], v[q * kStRows + r]);
+                if (TAPS && jt[q] >= 0)
+                  a.tap[((size_t)slot[r] * kNTap + (size_t)jt[q]) * a.tap_nb + b] = p;
+              }
+            }
+          }
+        }
+    }
+    if (r0 + kStRows >= h.nrows) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty_bar);
+    }
+    const float tot = transpose_sum<16>(v, lane);
+    const int q = lane / kStRows, r = lane % kStRows;
+    if (lane < 16 && q < RW && r < nr) a.out[(size_t)slot[r] * a.out_stride + m0 + q] = tot;
+  }
+}
+
 // MAT = 2: gate/up (RW = 1; routed weights of format RFMT); MAT = 1: down (RW
-// rows a warp; Q8_0)
+// rows a warp; routed weights of format RFMT, the shared expert's Q8_0)
 template <int MAT, int RW, bool TAPS, int RFMT>
 __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
   constexpr int kRows = kStGroupWarps * RW;  // rows of each matrix per stage
@@ -782,7 +872,12 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
         break;
       }
     } else {
-      down_stage<RW, TAPS>(a, h, st + kStHdrBytes, wi, lane, &empty[s]);
+      if constexpr (RFMT != MOE_FMT_Q8_0) {
+        if (!h.sh) down_stage_lb<RFMT, RW, TAPS>(a, h, st + kStHdrBytes, wi, lane, &empty[s]);
+        else down_stage<RW, TAPS>(a, h, st + kStHdrBytes, wi, lane, &empty[s]);
+      } else {
+        down_stage<RW, TAPS>(a, h, st + kStHdrBytes, wi, lane, &empty[s]);
+      }
     }
     c_work += clock64() - tg;
   }
@@ -815,14 +910,21 @@ uint64_t gateup_stage_bytes(const moe_desc &D) {
   return b;
 }
 
-// down rows a warp takes per stage: the most of 6, 4, 2, 1 whose stage fits and
-// whose items tile d
+// down rows a warp takes per stage: Q8_0 routed weights the most of 6, 4, 2, 1,
+// low-bit ones (whose rows are small) of 8, 4, whose stage fits (routed rows and
+// the shared expert's Q8_0 rows), whose items tile d and whose copies are whole
+// 16-byte units
 int down_rw(const moe_desc &D) {
-  const uint32_t kmax = D.f > D.f_shared ? D.f : D.f_shared;
-  for (int rw : {6, 4, 2, 1}) {
+  const bool low = D.routed_fmt != MOE_FMT_Q8_0;
+  if (row_bytes(D.routed_fmt, D.f) % 16) return 0;
+  for (int rw : {8, 6, 4, 2, 1}) {
+    if (low ? (rw != 8 && rw != 4) : rw == 8) continue;
     const uint32_t rows = (uint32_t)kStGroupWarps * rw;
-    if (D.d % rows || stage_bytes_for(1, rows, kmax) > kStStageMax) continue;
+    if (D.d % rows) continue;
+    if (stage_bytes_for(1, rows, D.f, D.routed_fmt) > kStStageMax) continue;
+    if (D.f_shared && stage_bytes_for(1, rows, D.f_shared) > kStStageMax) continue;
     if ((rw * D.f / 4) % 16 || (rw * D.f_shared / 4) % 16) continue;
+    if ((rows * row_bytes(D.routed_fmt, D.f)) % 16) continue;
     return rw;
   }
   return 0;
@@ -860,14 +962,17 @@ bool stream_gateup_ok(const Ctx &c) {
   return true;
 }
 
-// down: Q8_0 routed weights; an item shape that tiles d with 16-byte scale
-// copies (RW * K / 4 bytes a stage and a row offset); 16-byte aligned scale
-// planes
+// down (any routed format): an item shape that tiles d with 16-byte copies
+// (codes and RW * K / 4 bytes of scales a stage and a row offset); 16-byte
+// aligned scale planes
 bool stream_down_ok(const Ctx &c) {
   const moe_desc &D = c.desc;
-  if (D.routed_fmt != MOE_FMT_Q8_0 || down_rw(D) == 0) return false;
-  if (!aligned16(c.wts.down.scale)) return false;
-  if (D.f_shared && !aligned16(c.wts.s_down.scale)) return false;
+  if (down_rw(D) == 0) return false;
+  // 2-bit routed weights read the transposed h codes
+  if (D.routed_fmt == MOE_FMT_Q2S && !c.L.ht) return false;
+  if (!aligned16(c.wts.down.scale) || !aligned16(c.wts.down.q)) return false;
+  if (D.f_shared && (!aligned16(c.wts.s_down.scale) || !aligned16(c.wts.s_down.q)))
+    return false;
   return true;
 }
 
@@ -943,6 +1048,7 @@ cudaError_t launch_down_stream(const Ctx &c) {
   a.rows_per_slot = D.d;
   a.eslot = c.wts.expert_slot;
   a.act = (const int8_t *)(c.ws + c.L.hq);
+  a.act_t = c.L.ht ? (const int8_t *)(c.ws + c.L.ht) : nullptr;
   a.act_s = (const float *)(c.ws + c.L.hs);
   a.act_stride = c.fmax;
   a.act_s_stride = c.fmax / 32;
@@ -952,11 +1058,33 @@ cudaError_t launch_down_stream(const Ctx &c) {
   a.tap = taps ? (int32_t *)(c.ws + c.L.tap_dn) : nullptr;
   a.tap_nb = c.fmax / 32;
   a.err = (uint32_t *)(c.ws + c.L.err);
-  a.stage_bytes = (uint32_t)stage_bytes_for(1, (uint32_t)kStGroupWarps * rw, c.fmax);
+  const uint32_t rows = (uint32_t)kStGroupWarps * rw;
+  a.stage_bytes = (uint32_t)std::max<uint64_t>(stage_bytes_for(1, rows, D.f, D.routed_fmt),
+                                                D.f_shared ? stage_bytes_for(1, rows, D.f_shared)
+                                                           : 0);
   a.queue = (uint32_t *)(c.ws + c.L.sync) + kQueueStreamDown;
   a.trace = (D.flags & MOE_FLAG_TRACE) && c.L.trace
                 ? (unsigned long long *)(c.ws + c.L.trace) + kStTraceBase + kStTraceDown
                 : nullptr;
+  if (D.routed_fmt == MOE_FMT_Q2S || D.routed_fmt == MOE_FMT_E2M1) {
+    // low-bit routed rows: 8 rows a warp where the layer allows it (the
+    // 192-expert layers), else the Q8_0 kernel's choices
+    const bool q2 = D.routed_fmt == MOE_FMT_Q2S;
+    switch (rw) {
+      case 8:
+        return q2 ? (taps ? run_stream<1, 8, true, MOE_FMT_Q2S>(c, a)
+                          : run_stream<1, 8, false, MOE_FMT_Q2S>(c, a))
+                  : (taps ? run_stream<1, 8, true, MOE_FMT_E2M1>(c, a)
+                          : run_stream<1, 8, false, MOE_FMT_E2M1>(c, a));
+      case 4:
+        return q2 ? (taps ? run_stream<1, 4, true, MOE_FMT_Q2S>(c, a)
+                          : run_stream<1, 4, false, MOE_FMT_Q2S>(c, a))
+                  : (taps ? run_stream<1, 4, true, MOE_FMT_E2M1>(c, a)
+                          : run_stream<1, 4, false, MOE_FMT_E2M1>(c, a));
+      default:
+        return cudaErrorInvalidValue;  // down_rw gives low-bit layers 8 or 4 (or 0)
+    }
+  }
   switch (rw) {
     case 6: return taps ? run_stream<1, 6, true>(c, a) : run_stream<1, 6, false>(c, a);
     case 4: return taps ? run_stream<1, 4, true>(c, a) : run_stream<1, 4, false>(c, a);

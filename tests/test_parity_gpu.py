@@ -29,7 +29,8 @@ SMALL = [
     ("e1024_k32", _spec(E=1024, k=32, d=128, f=32, f_shared=0), 3),
     ("many_rows_per_expert", _spec(E=4, k=2, d=256, f=128, f_shared=64), 40),
     # d not a multiple of 128: gate/up on the register-streaming GEMV (down
-    # streamed for Q8_0, register GEMV for the low-bit formats)
+    # streamed where its rows copy in whole 16-byte units: Q8_0 and e2m1 here,
+    # the 2-bit layer's 24-byte rows on the register GEMV)
     ("d224_gemv_gateup", _spec(E=16, k=4, d=224, f=96, f_shared=64, s=2.5), 7),
     ("q2_d224_gemv_gateup", _spec(E=24, k=4, d=224, f=96, f_shared=64, fmt=1, s=1.0), 9),
     ("fp4_d160_gemv_gateup", _spec(E=24, k=4, d=160, f=128, f_shared=64, fmt=2, s=1.0), 9),
