@@ -748,10 +748,31 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
       for (int r = 0; r < kAR; ++r)
         arow[r] = r < cur.nrows ? act_row_of<MAT>(a, cur.sh, cur.row0 + r) : 0;
     }
+    int pf_row0 = -1, pf_sh = -1;
     for (int i = 0;; ++i) {
       if (*abort_flag) break;
       const int s = i % kStStages;
       const uint32_t use = (uint32_t)(i / kStStages);
+      // down: warm this SM's L1 with the h rows of the item's first pass, once
+      // per run of items with the same rows, before waiting for a stage (the
+      // consumers then find them there instead of in L2; measured slower for
+      // gate/up, whose x rows are 3x longer and come from the producer's queue
+      // one item ahead anyway)
+      if (MAT == 1 && have && (cur.row0 != pf_row0 || (int)cur.sh != pf_sh)) {
+        pf_row0 = cur.row0;
+        pf_sh = (int)cur.sh;
+        const int8_t *ab = RFMT == MOE_FMT_Q2S && !cur.sh ? a.act_t : a.act;
+        const int nr = min(cur.nrows, kStRows);
+        for (int r = 0; r < nr; ++r) {
+          const int row = MAT == 2 ? arow[r] : cur.row0 + r;
+          const char *p = (const char *)(ab + (size_t)row * a.act_stride);
+          for (uint32_t off = 0; off < cur.K; off += 128)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(p + off));
+          const char *ps = (const char *)(a.act_s + (size_t)row * a.act_s_stride);
+          for (uint32_t off = 0; off < cur.K / 8; off += 128)
+            asm volatile("prefetch.global.L1 [%0];" ::"l"(ps + off));
+        }
+      }
       const long long tw = clock64();
       if (use > 0 && !mbar_wait(&empty[s], (use - 1) & 1u, kStWaitCycles)) {
         atomicOr(a.err, kErrTimeout);
