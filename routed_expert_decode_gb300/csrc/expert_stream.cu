@@ -753,12 +753,13 @@ __global__ void __launch_bounds__(kStThreads, 1) k_stream(const StArgs a) {
       if (*abort_flag) break;
       const int s = i % kStStages;
       const uint32_t use = (uint32_t)(i / kStStages);
-      // down: warm this SM's L1 with the h rows of the item's first pass, once
-      // per run of items with the same rows, before waiting for a stage (the
-      // consumers then find them there instead of in L2; measured slower for
-      // gate/up, whose x rows are 3x longer and come from the producer's queue
-      // one item ahead anyway)
-      if (MAT == 1 && have && (cur.row0 != pf_row0 || (int)cur.sh != pf_sh)) {
+      // Q8_0 down: warm this SM's L1 with the h rows of the item's first pass,
+      // once per run of items with the same rows, before waiting for a stage
+      // (the consumers then find them there instead of in L2).  Measured slower
+      // for gate/up (x rows 3x longer) and no faster for the low-bit formats,
+      // whose consumers the weight decode binds.
+      if (MAT == 1 && RFMT == MOE_FMT_Q8_0 && have &&
+          (cur.row0 != pf_row0 || (int)cur.sh != pf_sh)) {
         pf_row0 = cur.row0;
         pf_sh = (int)cur.sh;
         const int8_t *ab = RFMT == MOE_FMT_Q2S && !cur.sh ? a.act_t : a.act;
