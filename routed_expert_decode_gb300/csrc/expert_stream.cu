@@ -46,9 +46,11 @@
 //    2 rows whose activation blocks they load at once; the halves' partial
 //    sums meet in shared memory, summed in half order, and h = silu(g)*u goes
 //    out in fp32; the requantisation kernel follows.
-//  * Down item: 4*RW consecutive output rows of one expert's down matrix; warp
-//    w takes RW of them against the h codes of every row (slot) of the expert,
-//    in passes of 2 slots whose h blocks it loads at once.
+//  * Down item: 4*RW consecutive output rows of one expert's down matrix (Q8_0,
+//    or 2-bit / e2m1 rows decoded a block at a time for both slots of a pass);
+//    warp w takes RW of them against the h codes of every row (slot) of the
+//    expert, in passes of 2 slots whose h blocks it loads at once.  For Q8_0
+//    the producer first prefetches each new run of items' h rows into L1.
 //  * Lane l holds whole 32-blocks l, l+32, ..: their exact int32 dots (the
 //    block-dot taps) scaled by w-scale * x-scale into fp32 sums that meet in
 //    the warp sum.  A block's two 16-byte halves are read from shared memory
