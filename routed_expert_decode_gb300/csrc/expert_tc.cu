@@ -879,11 +879,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 // activations for the tensor path in slot order (nothing when the plan sends no
 // expert to the tensor cores): an fp16 copy of the x codes, or for the routed
 // slots of an e2m1 layer (`digits`) the e4m3 digits of 2q, per 64-element
-// stage 64 bytes of 32-hi digits then 64 of 2-lo digits (the same 128 bytes)
+// stage 64 bytes of 32-hi digits then 64 of 2-lo digits (the same 128 bytes);
+// and the x block scales in slot order (the thread of a block's first chunk)
 __global__ void __launch_bounds__(256)
-    k_perm_x(const int8_t *__restrict__ xq, const int32_t *__restrict__ perm, uint32_t R,
-             uint32_t slots, uint32_t k, uint32_t d, const int *plan, uint32_t E,
-             __half *__restrict__ xperm, int digits) {
+    k_perm_x(const int8_t *__restrict__ xq, const float *__restrict__ xs,
+             const int32_t *__restrict__ perm, uint32_t R, uint32_t slots, uint32_t k,
+             uint32_t d, const int *plan, uint32_t E, __half *__restrict__ xperm,
+             float *__restrict__ xsperm, int digits) {
   pdl_trigger();
   pdl_wait();
   if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
@@ -892,6 +894,7 @@ __global__ void __launch_bounds__(256)
   if (i >= chunks) return;
   const uint32_t slot = (uint32_t)(i / (d / 8)), c = (uint32_t)(i % (d / 8));
   const uint32_t t = slot < R ? (uint32_t)perm[slot] / k : slot - R;
+  if ((c & 3u) == 0) xsperm[(size_t)slot * (d / 32) + c / 4] = xs[(size_t)t * (d / 32) + c / 4];
   const uint2 w = *(const uint2 *)(xq + (size_t)t * d + 8 * c);
   if (digits && slot < R) {
     uint32_t hi[2] = {0u, 0u}, lo[2] = {0u, 0u};
@@ -912,21 +915,6 @@ __global__ void __launch_bounds__(256)
   i8x4_to_h2x2(w.x, out.x, out.y);
   i8x4_to_h2x2(w.y, out.z, out.w);
   *(uint4 *)(xperm + (size_t)slot * d + 8 * c) = out;
-}
-
-// activation scales in slot order
-__global__ void __launch_bounds__(256)
-    k_perm_xs(const float *__restrict__ xs, const int32_t *__restrict__ perm, uint32_t R,
-              uint32_t slots, uint32_t k, uint32_t nb, const int *plan, uint32_t E,
-              float *__restrict__ xsperm) {
-  pdl_trigger();
-  pdl_wait();
-  if (PlanView(const_cast<int *>(plan), E).hdr[5] == 0) return;
-  const uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= (uint64_t)slots * nb) return;
-  const uint32_t slot = (uint32_t)(i / nb), b = (uint32_t)(i % nb);
-  const uint32_t t = slot < R ? (uint32_t)perm[slot] / k : slot - R;
-  xsperm[i] = xs[(size_t)t * nb + b];
 }
 
 // ---------------------------------------------------------------- host
@@ -1003,17 +991,13 @@ cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm) {
   const uint32_t slots = c.R + (c.desc.f_shared ? c.T : 0);
   const uint64_t n1 = (uint64_t)slots * (c.desc.d / 8);
   if (n1 == 0) return cudaSuccess;
-  cudaError_t e = launch_k(k_perm_x, (unsigned)((n1 + 255) / 256), 256, 0, c.stream, c.chained,
-                           (const int8_t *)(c.ws + c.L.xq), perm, c.R, slots, c.desc.top_k,
-                           c.desc.d, (const int *)(c.ws + c.L.plan), c.desc.n_expert,
-                           (__half *)(c.ws + c.L.xperm),
-                           c.desc.routed_fmt == MOE_FMT_E2M1 ? 1 : 0);
+  const cudaError_t e =
+      launch_k(k_perm_x, (unsigned)((n1 + 255) / 256), 256, 0, c.stream, c.chained,
+               (const int8_t *)(c.ws + c.L.xq), (const float *)(c.ws + c.L.xs), perm, c.R, slots,
+               c.desc.top_k, c.desc.d, (const int *)(c.ws + c.L.plan), c.desc.n_expert,
+               (__half *)(c.ws + c.L.xperm), (float *)(c.ws + c.L.xsperm),
+               c.desc.routed_fmt == MOE_FMT_E2M1 ? 1 : 0);
   c.chained = true;
-  if (e != cudaSuccess) return e;
-  const uint64_t n2 = (uint64_t)slots * (c.desc.d / 32);
-  e = launch_k(k_perm_xs, (unsigned)((n2 + 255) / 256), 256, 0, c.stream, true,
-               (const float *)(c.ws + c.L.xs), perm, c.R, slots, c.desc.top_k, c.desc.d / 32,
-               (const int *)(c.ws + c.L.plan), c.desc.n_expert, (float *)(c.ws + c.L.xsperm));
   return e;
 }
 
