@@ -291,7 +291,10 @@ moe_status moe_ffn_experts(const moe_desc *desc, const moe_weights *wts, const f
                            size_t ws_bytes, void *stream);
 
 /* Which implementation moe_layer uses for (desc, T) on the current device:
- * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel". */
+ * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel".  The fused
+ * kernel reads x in 16-byte vectors, so a call whose x is not 16-byte aligned
+ * takes the multi-kernel path whatever this returns (x and y need only the
+ * 4-byte alignment of their floats). */
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);
 
 /* Row threshold of the tensor-core path of moe_layer for (desc, T) on the

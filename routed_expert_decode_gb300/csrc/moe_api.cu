@@ -233,7 +233,9 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   uint32_t *err = (uint32_t *)(c.ws + c.L.err);
   cudaError_t e;
   float *logits_out = const_cast<float *>(w_router ? logits : nullptr);
-  if (T > 0 && fused_eligible(c)) {
+  // the fused kernel reads x in 16-byte vectors: an x that is not 16-byte
+  // aligned takes the multi-kernel path (whose quantiser reads it either way)
+  if (T > 0 && fused_eligible(c) && aligned(x, 16)) {
     if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
     if ((e = launch_decode_fused(c, x, logits, bias, y, w_router, logits_out)) != cudaSuccess)
       return from_cuda(e);

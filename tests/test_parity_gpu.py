@@ -125,6 +125,42 @@ def test_deterministic_across_runs(gpu):
     assert torch.equal(y1, y2)
 
 
+@pytest.mark.parametrize("T,fl", [(1, 0), (1, "gemv"), (7, 0), (40, "tc")])
+def test_x_and_y_only_float_aligned(gpu, T, fl):
+    """x and y at an odd float offset (4-byte, not 16-byte aligned): the fused
+    kernel, which reads x in 16-byte vectors, is not used and the multi-kernel
+    kernels read x and write y element by element there; the outputs equal the
+    aligned multi-kernel call's bit for bit."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=32, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    flags = {0: 0, "gemv": moe.FLAG_FORCE_GEMV, "tc": moe.FLAG_FORCE_TC}[fl]
+    logits, x = synth.token_inputs(spec, 31, T)
+    l_d = torch.from_numpy(logits).to(gpu)
+    b_d = torch.from_numpy(synth.bias(spec)).to(gpu)
+    n = T * spec.d
+    xbuf = torch.zeros(n + 4, dtype=torch.float32, device=gpu)
+    xbuf[1:1 + n] = torch.from_numpy(x).to(gpu).reshape(-1)
+    x_odd = xbuf[1:1 + n].view(T, spec.d)
+    x_al = torch.from_numpy(x).to(gpu)
+    ybuf = torch.full((n + 4,), float("nan"), dtype=torch.float32, device=gpu)
+    y_odd = ybuf[1:1 + n].view(T, spec.d)
+    y_al = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
+    # the aligned reference on the multi-kernel path (the unaligned call's path)
+    ref_desc = layer.desc(flags if flags else moe.FLAG_FORCE_GEMV)
+    desc = layer.desc(flags)
+    nws = max(moe.workspace_size(desc, T), moe.workspace_size(ref_desc, T))
+    ws = torch.zeros(nws, dtype=torch.uint8, device=gpu)
+    moe.layer(ref_desc, layer.weights, x_al, l_d, b_d, y_al, ws)
+    moe.layer(desc, layer.weights, x_odd, l_d, b_d, y_odd, ws)
+    torch.cuda.synchronize()
+    assert moe.check_device_error(ws) == 0
+    assert x_odd.data_ptr() % 16 != 0 and y_odd.data_ptr() % 16 != 0
+    assert torch.equal(y_odd, y_al)
+    assert torch.isnan(ybuf[0]) and torch.isnan(ybuf[1 + n])  # nothing written outside y
+
+
 @pytest.mark.parametrize("T", [16, 40])
 def test_streamed_gemv_repeatable_with_flushes(gpu, T):
     """The streamed GEMV's shared-memory ring (four stages read by three consumer
