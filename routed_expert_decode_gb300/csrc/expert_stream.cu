@@ -983,6 +983,9 @@ bool stream_gateup_ok(const Ctx &c) {
   if (gateup_stage_bytes(D) > kStStageMax) return false;
   if (!aligned16(c.wts.gate.scale) || !aligned16(c.wts.up.scale)) return false;
   if (D.f_shared && (!aligned16(c.wts.s_gate.scale) || !aligned16(c.wts.s_up.scale))) return false;
+  // bulk copies start on 16-byte boundaries (2-bit planes need only 8)
+  if (!aligned16(c.wts.gate.q) || !aligned16(c.wts.up.q)) return false;
+  if (D.f_shared && (!aligned16(c.wts.s_gate.q) || !aligned16(c.wts.s_up.q))) return false;
   return true;
 }
 

@@ -975,6 +975,17 @@ bool tc_supported(const moe_desc &D) {
   return encode_fn() != nullptr;
 }
 
+bool tc_weights_aligned(const Ctx &c) {
+  const moe_weights &w = c.wts;
+  auto a16 = [](const void *p) { return ((uintptr_t)p & 15u) == 0; };
+  bool ok = a16(w.gate.q) && a16(w.up.q) && a16(w.down.q) && a16(w.gate.scale) &&
+            a16(w.up.scale) && a16(w.down.scale);
+  if (c.desc.f_shared)
+    ok = ok && a16(w.s_gate.q) && a16(w.s_up.q) && a16(w.s_down.q) && a16(w.s_gate.scale) &&
+         a16(w.s_up.scale) && a16(w.s_down.scale);
+  return ok;
+}
+
 // can any expert of a T-token call land on the tensor path (workspace sizing)?
 bool tc_possible(const moe_desc &D, uint32_t T) {
   if (D.flags & MOE_FLAG_FORCE_GEMV) return false;

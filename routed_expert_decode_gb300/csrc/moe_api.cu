@@ -180,7 +180,7 @@ moe_status run_ffn(const Ctx &c, const float *x, const int32_t *idx, const float
   if ((e = launch_quant_x(c, x)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(4)) != cudaSuccess) return from_cuda(e);
   // tensor-core experts possible for this desc and T
-  const bool tc = c.L.xperm != 0 && tc_supported(c.desc);
+  const bool tc = c.L.xperm != 0 && tc_supported(c.desc) && tc_weights_aligned(c);
   if (tc && (e = launch_tc_prepare(c, perm)) != cudaSuccess) return from_cuda(e);
   if ((e = mk.mark(5)) != cudaSuccess) return from_cuda(e);
   if ((e = launch_gateup(c, perm)) != cudaSuccess) return from_cuda(e);

@@ -444,6 +444,9 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
                         const int32_t *perm, const int32_t *pos, uint32_t *err);
 // tensor-core path (expert_tc.cu)
 bool tc_supported(const moe_desc &D);
+// the weight planes the tensor maps read are 16-byte aligned (else no expert of
+// the call takes the tensor path)
+bool tc_weights_aligned(const Ctx &c);
 bool tc_possible(const moe_desc &D, uint32_t T);
 cudaError_t launch_tc_prepare(const Ctx &c, const int32_t *perm);
 cudaError_t launch_tc(const Ctx &c, int mat);

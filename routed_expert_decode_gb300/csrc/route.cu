@@ -555,7 +555,8 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
   const moe_desc &D = c.desc;
   int tc_mode = 0;
   // the same condition under which run_ffn launches the tensor kernels
-  if (c.L.xperm && tc_supported(D)) tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
+  if (c.L.xperm && tc_supported(D) && tc_weights_aligned(c))
+    tc_mode = (D.flags & MOE_FLAG_FORCE_TC) ? 2 : 1;
   const cudaError_t e = launch_k(k_plan, 1, kPlanThreads, 0, c.stream, c.chained, off, idx, perm,
                                  pos, c.T, D.n_expert, D.top_k, D.f, D.f_shared, D.d, tc_mode,
                                  tc_min_rows_for(D.routed_fmt), (uint32_t)c.sm_count, c.wts.expert_slot, c.wexp,

@@ -4,7 +4,7 @@ import pytest
 import torch
 
 import synth
-from parity import run_case, device_layer, poison_workspace
+from parity import Y_TOL, run_case, device_layer, poison_workspace
 
 pytestmark = pytest.mark.gpu
 
@@ -159,6 +159,55 @@ def test_x_and_y_only_float_aligned(gpu, T, fl):
     assert x_odd.data_ptr() % 16 != 0 and y_odd.data_ptr() % 16 != 0
     assert torch.equal(y_odd, y_al)
     assert torch.isnan(ybuf[0]) and torch.isnan(ybuf[1 + n])  # nothing written outside y
+
+
+@pytest.mark.parametrize("T,fl", [(7, 0), (40, "tc")])
+def test_two_bit_planes_only_8_byte_aligned(gpu, T, fl):
+    """2-bit routed code planes at an 8-byte (not 16-byte) offset, as moe_weights
+    allows them: the paths that need 16-byte aligned planes (the streamed GEMV's
+    bulk copies, the tensor maps) are not taken.  The block-dot taps equal the
+    aligned layer's bit for bit and y agrees within the layer tolerance."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=32, k=4, d=512, f=256, f_shared=256, fmt=1, s=1.0, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    keep = {}
+    w = moe.MoeWeights()
+    for name in ("gate", "up", "down"):
+        q = layer.tensors[name + "_q"].reshape(-1).view(torch.uint8)
+        buf = torch.zeros(q.numel() + 16, dtype=torch.uint8, device=gpu)
+        buf[8:8 + q.numel()] = q
+        keep[name] = buf
+        setattr(w, name, moe.MoeMat(buf.data_ptr() + 8, layer.tensors[name + "_s"].data_ptr()))
+    for name in ("s_gate", "s_up", "s_down"):
+        setattr(w, name, getattr(layer.weights, name))
+    w.expert_slot = layer.weights.expert_slot
+    w.n_slots = layer.weights.n_slots
+    assert w.gate.q % 16 == 8
+    flags = moe.FLAG_DEBUG_TAPS | (moe.FLAG_FORCE_TC if fl == "tc" else 0)
+    ref_flags = moe.FLAG_DEBUG_TAPS | moe.FLAG_FORCE_GEMV
+    logits, x = synth.token_inputs(spec, 17, T)
+    x_d, l_d = torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu)
+    b_d = torch.from_numpy(synth.bias(spec)).to(gpu)
+    out = {}
+    for key, fls, wts in (("ref", ref_flags, layer.weights), ("odd", flags, w)):
+        desc = layer.desc(fls)
+        ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
+        y = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
+        moe.layer(desc, wts, x_d, l_d, b_d, y, ws)
+        torch.cuda.synchronize()
+        assert moe.check_device_error(ws) == 0, key
+        L = moe.workspace_layout(desc, T)
+        slots = T * spec.k + T
+        n_gu = slots * 2 * L.n_tap * (spec.d // 32) * 4
+        n_dn = slots * L.n_tap * (max(spec.f, spec.f_shared) // 32) * 4
+        out[key] = (y.cpu().numpy(), ws[L.tap_gu:L.tap_gu + n_gu].cpu(),
+                    ws[L.tap_dn:L.tap_dn + n_dn].cpu())
+    assert torch.equal(out["ref"][1], out["odd"][1])
+    assert torch.equal(out["ref"][2], out["odd"][2])
+    g, f = out["odd"][0], out["ref"][0]
+    assert (np.abs(g - f).max(axis=1) / np.abs(f).max(axis=1)).max() <= Y_TOL
+    del keep
 
 
 @pytest.mark.parametrize("T", [16, 40])
