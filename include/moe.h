@@ -84,7 +84,12 @@ typedef enum {
 typedef enum { MOE_FMT_Q8_0 = 0, MOE_FMT_Q2S = 1, MOE_FMT_E2M1 = 2 } moe_fmt;
 
 /* One quantised matrix of all experts: q = code plane, scale = fp16 bits.
- * q must be 32-byte aligned, scale 16-byte aligned. */
+ * q must be aligned to 32 bytes (MOE_FMT_Q8_0), 8 (MOE_FMT_Q2S) or 16
+ * (MOE_FMT_E2M1), scale to 2 (else MOE_ERR_INVALID_ARG).  Every kernel path
+ * takes planes whose codes and scales are 16-byte aligned; with less aligned
+ * ones the kernels that copy them in 16-byte units (the fused decode kernel,
+ * the streamed GEMV for the matrices concerned, the tensor cores) are not
+ * used: the same integer block dots, outputs within the layer tolerance. */
 typedef struct {
   const void *q;
   const uint16_t *scale;
@@ -292,9 +297,9 @@ moe_status moe_ffn_experts(const moe_desc *desc, const moe_weights *wts, const f
 
 /* Which implementation moe_layer uses for (desc, T) on the current device:
  * "fused_decode" (one persistent kernel, T <= 2) or "multi_kernel".  The fused
- * kernel reads x in 16-byte vectors, so a call whose x is not 16-byte aligned
- * takes the multi-kernel path whatever this returns (x and y need only the
- * 4-byte alignment of their floats). */
+ * kernel reads x in 16-byte vectors, so a call whose x (or a weight plane, see
+ * moe_mat) is not 16-byte aligned takes the multi-kernel path whatever this
+ * returns (x and y need only the 4-byte alignment of their floats). */
 const char *moe_layer_path(const moe_desc *desc, uint32_t T);
 
 /* Row threshold of the tensor-core path of moe_layer for (desc, T) on the

@@ -37,6 +37,18 @@ bool mat_ok(const moe_mat &m, int fmt) {
   return true;
 }
 
+// The fused kernel streams weight rows and their scales with bulk copies, which
+// start on 16-byte boundaries: planes that are not 16-byte aligned (moe_mat
+// allows less) keep a call on the multi-kernel path.
+bool fused_weights_aligned(const moe_desc &d, const moe_weights &w) {
+  bool ok = aligned(w.gate.q, 16) && aligned(w.up.q, 16) && aligned(w.down.q, 16) &&
+            aligned(w.gate.scale, 16) && aligned(w.up.scale, 16) && aligned(w.down.scale, 16);
+  if (d.f_shared)
+    ok = ok && aligned(w.s_gate.q, 16) && aligned(w.s_up.q, 16) && aligned(w.s_down.q, 16) &&
+         aligned(w.s_gate.scale, 16) && aligned(w.s_up.scale, 16) && aligned(w.s_down.scale, 16);
+  return ok;
+}
+
 bool weights_ok(const moe_desc *d, const moe_weights *w) {
   if (!w) return false;
   const int f = d->routed_fmt;
@@ -233,9 +245,10 @@ moe_status run_layer(const moe_desc *desc, const moe_weights *wts, const float *
   uint32_t *err = (uint32_t *)(c.ws + c.L.err);
   cudaError_t e;
   float *logits_out = const_cast<float *>(w_router ? logits : nullptr);
-  // the fused kernel reads x in 16-byte vectors: an x that is not 16-byte
-  // aligned takes the multi-kernel path (whose quantiser reads it either way)
-  if (T > 0 && fused_eligible(c) && aligned(x, 16)) {
+  // the fused kernel reads x in 16-byte vectors and copies weight planes in
+  // 16-byte units: an x or planes not 16-byte aligned take the multi-kernel
+  // path (whose quantiser reads x either way)
+  if (T > 0 && fused_eligible(c) && aligned(x, 16) && fused_weights_aligned(*desc, *wts)) {
     if ((e = mk.mark(0)) != cudaSuccess) return from_cuda(e);
     if ((e = launch_decode_fused(c, x, logits, bias, y, w_router, logits_out)) != cudaSuccess)
       return from_cuda(e);

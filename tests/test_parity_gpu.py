@@ -210,6 +210,62 @@ def test_two_bit_planes_only_8_byte_aligned(gpu, T, fl):
     del keep
 
 
+@pytest.mark.parametrize("T,fl", [(1, 0), (7, 0), (40, "tc")])
+def test_q8_scale_planes_only_2_byte_aligned(gpu, T, fl):
+    """Q8_0 scale planes (routed and shared) at a 2-byte offset, as moe_weights
+    allows them: the fused decode kernel, the streamed GEMV and the tensor maps,
+    which copy scales in 16-byte units, are not used.  The block-dot taps equal
+    the aligned layer's bit for bit and y agrees within the layer tolerance."""
+    from routed_expert_decode_gb300 import moe
+
+    spec = _spec(E=32, k=4, d=512, f=256, f_shared=256, s=2.5, zipf_beta=0.4)
+    layer = device_layer(spec, gpu)
+    keep = {}
+    w = moe.MoeWeights()
+    for name, key in (("gate", "gate"), ("up", "up"), ("down", "down"),
+                      ("s_gate", "s_gate"), ("s_up", "s_up"), ("s_down", "s_down")):
+        m = getattr(layer.weights, name)
+        if name.startswith("s_"):
+            sc = layer.tensors[key + "_s"] if key + "_s" in layer.tensors else None
+        else:
+            sc = layer.tensors[key + "_s"]
+        if sc is None:
+            setattr(w, name, m)
+            continue
+        flat = sc.reshape(-1).view(torch.uint8)
+        buf = torch.zeros(flat.numel() + 32, dtype=torch.uint8, device=gpu)
+        buf[2:2 + flat.numel()] = flat
+        keep[name] = buf
+        setattr(w, name, moe.MoeMat(m.q, buf.data_ptr() + 2))
+    w.expert_slot = layer.weights.expert_slot
+    w.n_slots = layer.weights.n_slots
+    assert w.gate.scale % 16 == 2 and w.down.scale % 16 == 2
+    flags = moe.FLAG_DEBUG_TAPS | (moe.FLAG_FORCE_TC if fl == "tc" else 0)
+    ref_flags = moe.FLAG_DEBUG_TAPS | moe.FLAG_FORCE_GEMV
+    logits, x = synth.token_inputs(spec, 19, T)
+    x_d, l_d = torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu)
+    b_d = torch.from_numpy(synth.bias(spec)).to(gpu)
+    out = {}
+    for key, fls, wts in (("ref", ref_flags, layer.weights), ("odd", flags, w)):
+        desc = layer.desc(fls)
+        ws = torch.zeros(moe.workspace_size(desc, T), dtype=torch.uint8, device=gpu)
+        y = torch.empty((T, spec.d), dtype=torch.float32, device=gpu)
+        moe.layer(desc, wts, x_d, l_d, b_d, y, ws)
+        torch.cuda.synchronize()
+        assert moe.check_device_error(ws) == 0, key
+        L = moe.workspace_layout(desc, T)
+        slots = T * spec.k + T
+        n_gu = slots * 2 * L.n_tap * (spec.d // 32) * 4
+        n_dn = slots * L.n_tap * (max(spec.f, spec.f_shared) // 32) * 4
+        out[key] = (y.cpu().numpy(), ws[L.tap_gu:L.tap_gu + n_gu].cpu(),
+                    ws[L.tap_dn:L.tap_dn + n_dn].cpu())
+    assert torch.equal(out["ref"][1], out["odd"][1])
+    assert torch.equal(out["ref"][2], out["odd"][2])
+    g, f = out["odd"][0], out["ref"][0]
+    assert (np.abs(g - f).max(axis=1) / np.abs(f).max(axis=1)).max() <= Y_TOL
+    del keep
+
+
 @pytest.mark.parametrize("T", [16, 40])
 def test_streamed_gemv_repeatable_with_flushes(gpu, T):
     """The streamed GEMV's shared-memory ring (four stages read by three consumer
