@@ -60,7 +60,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,  /* bad shape, null or misaligned pointer */
-  MOE_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement */
+  MOE_ERR_UNSUPPORTED = 2,  /* valid request this library does not implement */
   MOE_ERR_WORKSPACE = 3,    /* ws_bytes < moe_workspace_size() */
   MOE_ERR_CUDA = 4,         /* a CUDA launch or runtime call failed */
   MOE_ERR_TIMEOUT = 5,      /* a bounded device wait gave up */
