@@ -37,8 +37,11 @@
  *             slots in order (no atomics: run-to-run deterministic).
  *
  * Memory: every pointer is caller-owned DEVICE memory except the desc/weights
- * structs (host).  The library allocates nothing.  Scratch comes from the
- * caller's workspace (moe_workspace_size).  Calls are asynchronous on `stream`
+ * structs (host).  The layer entry points allocate nothing; the one object
+ * that owns memory is an expert cache (moe_cache_create: host memory and CUDA
+ * events, including the pinned buffer moe_stream_layer reads the picks back
+ * into, freed by moe_cache_destroy).  Scratch comes from the caller's
+ * workspace (moe_workspace_size).  Calls are asynchronous on `stream`
  * (a cudaStream_t; NULL = legacy default stream), stateless and re-entrant as
  * long as concurrent calls use different workspaces.  Arguments are checked on
  * the host before anything is enqueued; nothing aborts or exits.  Device-side
@@ -407,7 +410,9 @@ moe_status moe_cache_get_stats(const moe_cache *cache, moe_cache_stats *out);
  * are used).  next_logits / next_bias (optional, device, [T][E] / [E]): the next
  * layer's router applied early to this layer's x -- their top-k picks are
  * read back with this layer's and prefetched for layer + 1 on prefetch_stream
- * while this layer runs.  Workspace as moe_layer. */
+ * while this layer runs.  Workspace as moe_layer.  A call with more routed rows
+ * than any before on this cache first grows the cache's pinned read-back
+ * buffer (MOE_ERR_CUDA if that allocation fails). */
 moe_status moe_stream_layer(moe_cache *cache, uint32_t layer, const moe_desc *desc,
                             const moe_weights *wts, const float *x, const float *logits,
                             const float *bias, uint32_t T, const float *next_logits,
