@@ -461,6 +461,44 @@ def test_fused_decode_full_size(gpu):
         print("fused t2", seed, run_case(synth.GLM_LAYER, 2, seed=seed, device=gpu))
 
 
+def test_decode_t1_every_bench_token(gpu):
+    """Every token the decode benchmark times (its workload's token seeds), through
+    the same untapped fused call: expert indices, routing weights, offsets,
+    permutation and int8 activations against the oracle for each of them, and
+    the whole bar (h codes within one step, y) on every tenth."""
+    import oracle
+    from parity import W_RTOL, compare_with_oracle
+    from routed_expert_decode_gb300 import moe
+
+    spec, T, seeds = synth.WORKLOADS["decode_t1"]
+    assert T == 1 and len(seeds) == 100
+    layer = device_layer(spec, gpu)
+    assert moe.layer_path(layer.desc(), T) == "fused_decode"
+    bias = synth.bias(spec)
+    bias_d = torch.from_numpy(bias).to(gpu)
+    worst = 0.0
+    for i, seed in enumerate(seeds):
+        logits, x = synth.token_inputs(spec, seed, T)
+        out = layer.forward(torch.from_numpy(x).to(gpu), torch.from_numpy(logits).to(gpu), bias_d)
+        torch.cuda.synchronize()
+        assert moe.check_device_error(layer.workspace(T, 0)) == 0
+        g = {k: (v.cpu().numpy() if isinstance(v, torch.Tensor) else v) for k, v in vars(out).items()}
+        r_idx, r_w = oracle.route(logits, bias, spec.k, spec.s, score=spec.score)
+        r_off, r_perm, r_pos = oracle.permute(r_idx, spec.E)
+        r_xq, r_xs = oracle.quantize(x)
+        assert np.array_equal(g["idx"].ravel(), r_idx.ravel()), f"seed {seed}: expert indices"
+        assert np.allclose(g["w"].ravel(), r_w.ravel(), rtol=W_RTOL, atol=0), f"seed {seed}: weights"
+        assert np.array_equal(g["off"].ravel(), r_off), f"seed {seed}: offsets"
+        assert np.array_equal(g["perm"].ravel(), r_perm), f"seed {seed}: permutation"
+        assert np.array_equal(g["pos"].ravel(), r_pos), f"seed {seed}: inverse permutation"
+        assert np.array_equal(g["xq"].ravel(), r_xq), f"seed {seed}: int8 activations"
+        assert np.array_equal(g["xs"].ravel(), r_xs), f"seed {seed}: activation scales"
+        if i % 10 == 0:
+            rep = compare_with_oracle(spec, T, x, logits, bias, g)
+            worst = max(worst, rep["max_y_err"])
+    print("decode_t1, 100 token seeds: worst sampled y error", worst)
+
+
 def test_fused_matches_multi_kernel_and_repeats(gpu):
     """The fused kernel and the multi-kernel path agree (same routing, same
     int8 codes, y within fp32 summation order), the fused kernel is
