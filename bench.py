@@ -538,12 +538,24 @@ def run_ours(args):
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(torch, dist, timed_ms(g_e2e[1].replay), dev)
         e2e_how = "the K steps captured as one CUDA graph"
+    # what a user reads back: the last two steps' y in pinned host memory equal
+    # an eager call on the same inputs (the same kernels, so bit for bit)
+    torch.cuda.synchronize()
+    for i in range(max(K - 2, 0), K):
+        s_ = step_seed[i]
+        y_ref = torch.empty_like(y_d[0])
+        moe.layer(desc, layer.weights, pin_in[s_][0].to(dev), pin_in[s_][1].to(dev), bias,
+                  y_ref, ws)
+        torch.cuda.synchronize()
+        if not torch.equal(y_h[i % 2], y_ref.cpu()):
+            raise RuntimeError(f"end-to-end step {i}: y read back differs from an eager call")
     e2e = {"value": round(job_throughput(T * K, world, e2e_ms), 2), "unit": "tokens/s",
            "h2d_bytes_per_step": T * spec.d * 4 + T * spec.E * 4,
            "d2h_bytes_per_step": T * spec.d * 4,
            "method": e2e_how + "; per step x and router logits in from pinned host memory, "
                      "moe_layer, y out to pinned host memory (copies in and copies out on "
                      "two more streams, double-buffered device buffers)",
+           "checked": "the last two steps' y as read back equal an eager call bit for bit",
            "eager_calls_value": round(job_throughput(T * K, world, eager_ms), 2)}
     assert moe.check_device_error(ws) == 0
 
