@@ -78,12 +78,43 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
   if ((uint32_t)lane < k) w[(size_t)t * k + lane] = __fmul_rn(s, __fdiv_rn(my_sigma, sum));
 }
 
+// Block-wide exclusive scan of one int per thread, for a block of 32 full warps
+// (1024 threads): each warp scans its 32 values by shuffles, warp 0 scans the
+// 32 warp totals, three barriers in all.  Returns the exclusive prefix; *total
+// gets the block sum.  wsum: 32 ints of shared memory, free again on return.
+__device__ int block_excl_scan(int v, int *wsum, int *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int t = wsum[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, t, o);
+      if (lane >= o) t += y;
+    }
+    wsum[lane] = t;  // inclusive prefix of the warp totals
+  }
+  __syncthreads();
+  const int before = warp > 0 ? wsum[warp - 1] : 0;
+  *total = wsum[31];
+  __syncthreads();
+  return before + x - v;
+}
+
 // Stable permutation without position atomics (1 CTA, 32 warps).
 // Rows r = t*k + j.  Warp w owns a contiguous range of tokens; (A) each warp
 // counts its rows per expert, (B) a per-expert scan over warps gives each warp's
 // starting rank, (C) a scan over experts gives off[], (D) each warp walks its
 // rows in order, ranking equal experts inside a 32-row group with match_any.
 constexpr int kPermThreads = 1024;
+static_assert(kPermThreads == 1024, "block_excl_scan takes 32 full warps");
 constexpr int kPermWarps = kPermThreads / 32;
 
 __global__ void __launch_bounds__(kPermThreads)
@@ -95,9 +126,8 @@ __global__ void __launch_bounds__(kPermThreads)
   extern __shared__ int smem[];
   int *hist = smem;                       // [kPermWarps][E]
   int *cnt = hist + (size_t)kPermWarps * E;  // [E]
-  int *scan = cnt + E;                    // [kPermThreads]
+  int *scan = cnt + E;                    // [32]: block_excl_scan's warp totals
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t R = T * k;
   for (uint32_t i = tid; i < (uint32_t)kPermWarps * E; i += kPermThreads) hist[i] = 0;
   __syncthreads();
   const uint32_t tok_per_warp = (T + kPermWarps - 1) / kPermWarps;
@@ -129,21 +159,13 @@ __global__ void __launch_bounds__(kPermThreads)
   for (uint32_t base = 0; base < E; base += kPermThreads) {
     const uint32_t e = base + tid;
     const int v = e < E ? cnt[e] : 0;
-    scan[tid] = v;
-    __syncthreads();
-    for (int o = 1; o < kPermThreads; o <<= 1) {
-      const int add = tid >= o ? scan[tid - o] : 0;
-      __syncthreads();
-      scan[tid] += add;
-      __syncthreads();
-    }
+    int chunk_total;
+    const int excl = carry + block_excl_scan(v, scan, &chunk_total);
     if (e < E) {
-      const int excl = carry + scan[tid] - v;
       off[e] = excl;
       cnt[e] = excl;  // cnt now holds off[e]
     }
-    carry += scan[kPermThreads - 1];
-    __syncthreads();
+    carry += chunk_total;
   }
   if (tid == 0) off[E] = carry;
   __syncthreads();
@@ -169,25 +191,8 @@ __global__ void __launch_bounds__(kPermThreads)
   }
 }
 
-// block-wide exclusive scan of one int per thread (kPlanThreads threads);
-// returns the exclusive prefix, *total gets the block sum
 constexpr int kPlanThreads = 1024;
-
-__device__ int block_excl_scan(int v, int *scan, int *total) {
-  const int tid = threadIdx.x;
-  scan[tid] = v;
-  __syncthreads();
-  for (int o = 1; o < kPlanThreads; o <<= 1) {
-    const int add = tid >= o ? scan[tid - o] : 0;
-    __syncthreads();
-    scan[tid] += add;
-    __syncthreads();
-  }
-  const int incl = scan[tid];
-  *total = scan[kPlanThreads - 1];
-  __syncthreads();
-  return incl - v;
-}
+static_assert(kPlanThreads == 1024, "block_excl_scan takes 32 full warps");
 
 // Work plan from off[] (1 CTA).  Validates off, perm, pos and idx against one
 // another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
@@ -207,7 +212,7 @@ __global__ void __launch_bounds__(kPlanThreads)
            uint32_t *err) {
   pdl_trigger();
   pdl_wait();
-  __shared__ int scan[kPlanThreads];
+  __shared__ int scan[32];  // block_excl_scan's warp totals
   __shared__ int bad;
   const int tid = threadIdx.x;
   const uint32_t R = T * k;
@@ -535,7 +540,7 @@ cudaError_t launch_router_logits(const moe_desc &d, const float *w_router, const
 cudaError_t launch_permute(const Ctx &c, const int32_t *idx, int32_t *off, int32_t *perm,
                            int32_t *pos, uint32_t *err) {
   const uint32_t E = c.desc.n_expert;
-  const size_t smem = sizeof(int) * ((size_t)kPermWarps * E + E + kPermThreads);
+  const size_t smem = sizeof(int) * ((size_t)kPermWarps * E + E + 32);
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
