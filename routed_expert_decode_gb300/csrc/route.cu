@@ -193,6 +193,7 @@ __global__ void __launch_bounds__(kPermThreads)
 
 constexpr int kPlanThreads = 1024;
 static_assert(kPlanThreads == 1024, "block_excl_scan takes 32 full warps");
+constexpr int kMaxExperts = 1024;  // moe_desc.n_expert, checked on the host
 
 // Work plan from off[] (1 CTA).  Validates off, perm, pos and idx against one
 // another; on any inconsistency it flags kErrBadOffsets / kErrBadIndex and plans
@@ -214,13 +215,17 @@ __global__ void __launch_bounds__(kPlanThreads)
   pdl_wait();
   __shared__ int scan[32];  // block_excl_scan's warp totals
   __shared__ int bad;
+  __shared__ int s_off[kMaxExperts + 1];  // off[], read from global memory once
+  __shared__ int s_ntc;                   // entries of the tensor-core list
   const int tid = threadIdx.x;
   const uint32_t R = T * k;
   PlanView P(plan, E);
-  if (tid == 0) bad = (off[0] != 0 || off[E] != (int)R) ? 1 : 0;
+  for (uint32_t e = tid; e <= E; e += kPlanThreads) s_off[e] = off[e];
+  if (tid == 0) bad = 0;
   __syncthreads();
+  if (tid == 0 && (s_off[0] != 0 || s_off[E] != (int)R)) bad = 1;
   for (uint32_t e = tid; e < E; e += kPlanThreads)
-    if (off[e + 1] < off[e]) bad = 1;
+    if (s_off[e + 1] < s_off[e]) bad = 1;
   __syncthreads();
   if (bad) {
     if (tid == 0) {
@@ -238,7 +243,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     int lo = 0, hi = (int)E;  // largest e with off[e] <= p
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
-      if (off[mid] <= (int)p) lo = mid; else hi = mid;
+      if (s_off[mid] <= (int)p) lo = mid; else hi = mid;
     }
     if (r < 0 || (uint32_t)r >= R || idx[r] != lo || pos[r] != (int)p) bad = 2;
   }
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   // rows of expert e this call computes: only the experts in [e_lo, e_hi) (the
   // share of one rank in an expert-parallel split; all of them by default)
   auto own_rows = [&](uint32_t e) -> int {
-    return e >= e_lo && e < e_hi ? off[e + 1] - off[e] : 0;
+    return e >= e_lo && e < e_hi ? s_off[e + 1] - s_off[e] : 0;
   };
   // with a slot table, every selected expert this call computes must have its
   // weights in a slot
@@ -319,13 +324,13 @@ __global__ void __launch_bounds__(kPlanThreads)
     const int tiles_total = total;
     if (gflag) {
       P.act_e[gu] = (int)e;
-      P.act_row0[gu] = off[e];
+      P.act_row0[gu] = s_off[e];
       P.act_rows[gu] = rows;
       P.item_gu[gu] = gu * (int)f;
     }
     if (tflag) {
       P.tc_e[tv] = (int)e;
-      P.tc_row0[tv] = off[e];
+      P.tc_row0[tv] = s_off[e];
       P.tc_rows[tv] = rows;
       P.tc_tile_gu[tv] = tile0;
       P.tc_tile_dn[tv] = (tile0 / (int)(f / kTcTileM)) * (int)(d / kTcTileM);
@@ -375,6 +380,7 @@ __global__ void __launch_bounds__(kPlanThreads)
     P.hdr[3] = maxrows;
     P.hdr[4] = 1;  // routing arrays validated: the combine may read pos[]
     P.hdr[5] = V;
+    s_ntc = V;
     P.hdr[6] = tiles_gu;
     P.hdr[7] = tiles_dn;
   }
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(kPlanThreads)
   // rows; the shared expert, with every token, leads).  The tensor kernels deal
   // tiles out in rounds of one per CTA, so the widest and costliest tiles go out
   // first and the narrow ones even out the CTAs' totals at the end.
-  const int V = P.hdr[5];
+  const int V = s_ntc;
   if (V > 1) {
     // (rows, expert) of every entry in shared memory while it fits
     __shared__ int key_rows[kPlanThreads], key_e[kPlanThreads];
@@ -408,8 +414,8 @@ __global__ void __launch_bounds__(kPlanThreads)
     for (int r = tid; r < V; r += kPlanThreads) {
       const int e = P.tc_tile_dn[r];
       P.tc_e[r] = e;
-      P.tc_row0[r] = e == (int)E ? (int)R : off[e];
-      P.tc_rows[r] = e == (int)E ? (int)T : off[e + 1] - off[e];
+      P.tc_row0[r] = e == (int)E ? (int)R : s_off[e];
+      P.tc_rows[r] = e == (int)E ? (int)T : s_off[e + 1] - s_off[e];
     }
     __syncthreads();
     // tile prefixes in the new order (the totals do not change)
