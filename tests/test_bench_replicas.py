@@ -35,7 +35,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_job_value_gloo():
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (threaded) process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0] == out[1]

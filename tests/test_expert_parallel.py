@@ -136,7 +136,7 @@ def _worker(rank, world, port, mode, out):
 @pytest.mark.parametrize("mode", ["decode", "prefill"])
 def test_two_ranks_match_single_rank_oracle_gloo(mode):
     world = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()  # no fork of this (threaded) process
     out = mgr.dict()
     mp.spawn(_worker, args=(world, _free_port(), mode, out), nprocs=world, join=True)
     for rank in range(world):
