@@ -564,6 +564,7 @@ cudaError_t launch_plan(const Ctx &c, const int32_t *off, const int32_t *idx,
   // tensor path: 0 off, 1 for experts with more than tc_min_rows_for(fmt) rows,
   // 2 forced
   const moe_desc &D = c.desc;
+  if (D.n_expert > (uint32_t)kMaxExperts) return cudaErrorInvalidValue;  // s_off's size
   int tc_mode = 0;
   // the same condition under which run_ffn launches the tensor kernels
   if (c.L.xperm && tc_supported(D) && tc_weights_aligned(c))
