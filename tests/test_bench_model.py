@@ -71,3 +71,16 @@ def test_macs_count_rows_times_weights():
     rows = 1 + 2 + 2  # two routed experts and the shared expert's two tokens
     assert m["gateup"] == 2 * spec.f * spec.d * rows
     assert m["down"] == spec.d * spec.f * rows
+
+
+def test_unit_fractions_at_the_peak_rates():
+    # a stage that issues exactly the dp4a peak (152 SMs x 64 a clock at
+    # 2070 MHz) for 1 ms, and a tensor stage at exactly 1000 TFLOP/s
+    dp4a_per_ms = 152 * bench.DP4A_PER_SM_CLK * 2070e6 * 1e-3
+    macs = {"gateup": 4 * dp4a_per_ms, "down": 2 * dp4a_per_ms,
+            "gateup_tc": 1000e12 * 1e-3 / 2, "down_tc": 0}
+    stage_ms = {"gateup": 1.0, "down": 1.0, "gateup_tc": 1.0, "down_tc": 1.0}
+    f = bench.unit_fractions(macs, stage_ms, 152, 2070.0, 2000.0)
+    assert f["gateup_dp4a_frac"] == 1.0 and f["down_dp4a_frac"] == 0.5
+    assert f["gateup_tc_tensor_frac"] == 0.5
+    assert "down_tc_tensor_frac" not in f  # no work on that stage
