@@ -153,6 +153,15 @@ def stage_bytes(spec, T: int, counts, tc_rows=None, sm_count=None):
 
 ROOFLINE_STAGES = ("gateup", "down", "gateup_tc", "down_tc", "decode_fused")
 
+FMT_NAMES = {0: "Q8_0", 1: "Q2S", 2: "E2M1"}
+
+
+def workload_desc(name: str, spec, T: int) -> str:
+    """The workload as both arms name it in config.workload."""
+    return (f"{name}: T={T}, E={spec.E}, top_k={spec.k}, d={spec.d}, f={spec.f}, "
+            f"f_shared={spec.f_shared}, fmt={FMT_NAMES[spec.fmt]}, s={spec.s}, "
+            f"zipf_beta={spec.zipf_beta}")
+
 # dp4a issue rate of one SM per clock: half the 128 fp32 lanes (a probe kernel
 # of independent dp4a chains measured 60.2 per SM per clock on this GB300)
 DP4A_PER_SM_CLK = 64
@@ -589,9 +598,7 @@ def run_ours(args):
         "dtype": "int8 x int8 -> int32 block dots, fp32 scales/accumulation",
         "data": "synthetic (seeded counter-based generator; random Q8_0 weights of the layer's shape)",
         "config": {
-            "workload": f"{args.workload}: T={T}, E={spec.E}, top_k={spec.k}, d={spec.d}, f={spec.f}, "
-                        f"f_shared={spec.f_shared}, fmt={'Q8_0' if spec.fmt == 0 else 'Q2S'}, "
-                        f"s={spec.s}, zipf_beta={spec.zipf_beta}",
+            "workload": workload_desc(args.workload, spec, T),
             "token_seeds": seeds_run(step_seed),
             "tokens_per_step": T,
             "l2": "flushed between steps (2x L2 write, then read back), outside the per-step "
@@ -1017,7 +1024,7 @@ def run_reference(args):
         "vs_baseline": None,
         "dtype": "int8 x int8 -> int32 block dots, fp64 sums (CPU oracle)",
         "data": "synthetic (seeded counter-based generator)",
-        "config": {"workload": args.workload, "tokens_per_step": 1,
+        "config": {"workload": workload_desc(args.workload, spec, T), "tokens_per_step": 1,
                    "host": f"{platform.machine()}, {os.cpu_count()} cores"},
         "cpu_baseline": {"value": round(value, 4), "unit": "tokens/s", "cores": 1,
                          "kind": "oracle", "sample": f"{K} steps x 1 token of {args.workload}"},

@@ -84,3 +84,15 @@ def test_unit_fractions_at_the_peak_rates():
     assert f["gateup_dp4a_frac"] == 1.0 and f["down_dp4a_frac"] == 0.5
     assert f["gateup_tc_tensor_frac"] == 0.5
     assert "down_tc_tensor_frac" not in f  # no work on that stage
+
+
+def test_both_arms_name_the_workload_alike():
+    spec, T, _ = synth.WORKLOADS["decode_t1"]
+    desc = bench.workload_desc("decode_t1", spec, T)
+    assert desc == ("decode_t1: T=1, E=256, top_k=8, d=6144, f=2048, f_shared=2048, fmt=Q8_0, "
+                    "s=2.5, zipf_beta=0.4")
+    line = bench.run_reference(bench.parse_args(["--impl", "reference", "--steps", "1",
+                                                 "--warmup", "0"]))
+    assert line["config"]["workload"] == desc
+    spec4, T4, _ = synth.WORKLOADS["fp4_t64"]
+    assert "fmt=E2M1" in bench.workload_desc("fp4_t64", spec4, T4)
